@@ -1,0 +1,305 @@
+"""Pins of the oracle's seeded sampler, Philox stream and frame loop against
+things other than itself: numpy's Philox4x64-10 raw words, the Gumbel
+distribution's mean and variance, numpy.argmax, kept sets enumerated by
+brute force on tiny vocabularies, hand-built boundary cases, and a
+chi-square test of Gumbel-max frequencies against the renormalised kept-set
+probabilities.
+
+Semantics: "Supported Models" (mstar docs), "Fish Audio S2-Pro notes"
+(temperature first, then top-k / top-p over the tempered probabilities; the
+top-p boundary keeps the token that carries the running total past top-p),
+"Chatterbox notes" (temperature under 1e-5 is greedy, top-k of the whole
+vocabulary or more is no filter), "Adding a Model" (vox-serve docs), "How a
+program runs" (per-request seeds) and "2. The program" (a different salt per
+sampling call; stop_tokens / audio_tokens); MOSS-TTS-Local on SGLang-Omni
+(mosi.cn blog), model section (12 codebooks, each fed back before the next).
+"""
+import math
+
+import numpy as np
+import pytest
+from scipy import stats
+
+import oracle
+
+
+# ---------------------------------------------------------------------------
+# Philox4x64-10 and the Gumbel noise
+# ---------------------------------------------------------------------------
+def _inc(ctr):
+    c = [int(x) for x in ctr]
+    for i in range(4):
+        c[i] = (c[i] + 1) % (1 << 64)
+        if c[i]:
+            break
+    return np.array(c, np.uint64)
+
+
+@pytest.mark.parametrize("key,ctr", [
+    ((0, 0), (0, 0, 0, 0)),
+    ((1, 2), (0, 0, 0, 0)),
+    ((12345, 7), (41, 3, 0, 0)),
+    ((2**64 - 1, 2**63 + 5), (2**64 - 1, 2**64 - 1, 9, 0)),
+    ((0xDEADBEEF, 0), (2**64 - 1, 0, 0, 0)),
+])
+def test_philox_matches_numpy_raw_words(key, ctr):
+    key = np.array(key, np.uint64)
+    ctr = np.array(ctr, np.uint64)
+    # numpy's Philox bumps its 256-bit counter before producing each block
+    want = np.random.Philox(counter=ctr, key=key).random_raw(4)
+    got = oracle.philox4x64_10(key, _inc(ctr))
+    np.testing.assert_array_equal(got, want)
+
+
+def _dec(ctr):
+    c = [int(x) for x in ctr]
+    for i in range(4):
+        borrow = c[i] == 0
+        c[i] = (c[i] - 1) % (1 << 64)
+        if not borrow:
+            break
+    return np.array(c, np.uint64)
+
+
+def test_uniform_uses_word0_and_is_strictly_inside_unit_interval():
+    for seed, salt, tok, step in [(0, 0, 0, 0), (9, 1, 151935, 77), (2**63, 12, 5, 2**40)]:
+        key = np.array([seed, salt], np.uint64)
+        ctr = np.array([tok, step, 0, 0], np.uint64)
+        words = np.random.Philox(counter=_dec(ctr), key=key).random_raw(4)
+        u = oracle.uniform(seed, salt, tok, step)
+        assert 0.0 < u < 1.0
+        assert u == (2 * (int(words[0]) >> 12) + 1) * 2.0 ** -53
+    # the extremes of the mapping are exact and strictly inside (0, 1)
+    assert (2 * 0 + 1) * 2.0 ** -53 > 0
+    assert (2 * (2**52 - 1) + 1) * 2.0 ** -53 < 1.0
+
+
+def test_gumbel_moments():
+    """Standard Gumbel: mean = Euler-Mascheroni gamma, variance = pi^2 / 6."""
+    g = np.array([oracle.gumbel(3, 1, t, 0) for t in range(200000)])
+    assert abs(g.mean() - np.euler_gamma) < 0.01
+    assert abs(g.var() - math.pi ** 2 / 6) < 0.02
+    # Kolmogorov-Smirnov against scipy's Gumbel
+    assert stats.kstest(g[:20000], "gumbel_r").pvalue > 1e-4
+
+
+# ---------------------------------------------------------------------------
+# Greedy conventions
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("temp", [0.0, 1e-6, 1e-5, -1.0])
+def test_greedy_is_numpy_argmax(temp):
+    rng = np.random.default_rng(0)
+    for _ in range(20):
+        x = rng.integers(-3, 3, size=37).astype(np.float32)  # many exact ties
+        tok, info = oracle.sample_row(x, seed=1, step=2, salt=0, temperature=temp, top_k=0, top_p=1.0)
+        assert tok == int(np.argmax(x)) and info["greedy"] == 1
+
+
+def test_top_k_one_and_tiny_top_p_are_argmax_for_any_seed():
+    rng = np.random.default_rng(1)
+    for i in range(50):
+        x = rng.normal(0, 2, size=300).astype(np.float32)
+        x[rng.integers(0, 300)] = x.max()  # a tie at the top: lowest id wins
+        a = int(np.argmax(x))
+        assert oracle.sample_row(x, i, i, 0, 0.7, 1, 1.0)[0] == a
+        assert oracle.sample_row(x, i, i, 3, 1.3, 0, 1e-9)[0] == a
+
+
+# ---------------------------------------------------------------------------
+# Kept sets by brute force
+# ---------------------------------------------------------------------------
+def _brute_kept(x32, temp, top_k, top_p):
+    """Kept set from pairwise comparisons (no sort): token i precedes j when
+    x_i > x_j, or x_i == x_j and i < j."""
+    V = len(x32)
+    x = [float(v) / float(np.float32(temp)) for v in x32]
+    before = lambda j, i: x[j] > x[i] or (x[j] == x[i] and j < i)
+    rank = [sum(before(j, i) for j in range(V)) for i in range(V)]
+    K = top_k if 0 < top_k < V else V
+    surv = [i for i in range(V) if rank[i] < K]
+    if top_p >= 1.0:
+        return set(surv), None
+    m = max(x)
+    e = {i: math.exp(x[i] - m) for i in surv}
+    Z = sum(e[i] for i in sorted(surv, key=lambda i: rank[i]))
+    kept = set()
+    for i in surv:
+        S = sum(e[j] for j in sorted(surv, key=lambda j: rank[j]) if rank[j] < rank[i])
+        if rank[i] == 0 or S < float(np.float32(top_p)) * Z:
+            kept.add(i)
+    probs = {i: e[i] for i in kept}
+    return kept, probs
+
+
+@pytest.mark.parametrize("V", [2, 3, 5, 8])
+def test_kept_set_count_matches_brute_force(V):
+    rng = np.random.default_rng(V)
+    for trial in range(300):
+        x = rng.normal(0, 1.5, size=V).astype(np.float32)
+        if trial % 5 == 0:
+            x[rng.integers(0, V)] = x[rng.integers(0, V)]  # exact tie
+        temp = float(rng.choice([0.5, 1.0, 2.0]))
+        k = int(rng.integers(0, V + 2))
+        p = float(rng.choice([0.3, 0.6, 0.9, 1.0]))
+        kept, _ = _brute_kept(x, temp, k, p)
+        tok, info = oracle.sample_row(x, trial, 0, 0, temp, k, p)
+        assert info["n_kept"] == len(kept)
+        assert tok in kept
+
+
+def test_top_p_boundary_prefix_exactly_p_drops_the_next_token():
+    # four equal logits: q = 1/4 each; p = 1/2.  The second token carries the
+    # running total from 1/4 to 1/2 and is kept; the third would start at
+    # exactly 1/2 = p and is dropped.  Ties go to the lower id.
+    x = np.zeros(4, np.float32)
+    seen = set()
+    for step in range(400):
+        tok, info = oracle.sample_row(x, 5, step, 0, 1.0, 0, 0.5)
+        assert info["n_kept"] == 2
+        seen.add(tok)
+    assert seen == {0, 1}
+
+
+def test_top_p_keeps_the_crossing_token():
+    # softmax probabilities about 0.5, 0.25, 0.125, 0.125; with p = 0.6 the
+    # second token takes the running total from 0.5 past 0.6 and is kept, the
+    # third starts above p and is dropped
+    x = np.array([3 * math.log(2), 2 * math.log(2), math.log(2), math.log(2)], np.float32)
+    kept, _ = _brute_kept(x, 1.0, 0, 0.6)
+    assert kept == {0, 1}  # 0.5 < 0.6 so the second token (crossing) is kept
+    for step in range(200):
+        tok, info = oracle.sample_row(x, 1, step, 0, 1.0, 0, 0.6)
+        assert info["n_kept"] == 2 and tok in kept
+
+
+def test_top_k_tie_at_the_cut_goes_to_lower_ids():
+    x = np.array([5, 3, 3, 3, 1], np.float32)
+    seen = set()
+    for step in range(300):
+        tok, info = oracle.sample_row(x, 2, step, 0, 4.0, 2, 1.0)
+        assert info["n_kept"] == 2
+        seen.add(tok)
+    assert seen == {0, 1}
+
+
+def test_top_k_of_whole_vocab_or_more_is_no_filter():
+    x = np.random.default_rng(3).normal(0, 1, 10).astype(np.float32)
+    for k in (0, 10, 11, 1000):
+        assert oracle.sample_row(x, 1, 0, 0, 1.0, k, 1.0)[1]["n_kept"] == 10
+
+
+@pytest.mark.parametrize("top_k,top_p,temp", [(0, 1.0, 1.0), (5, 1.0, 0.7), (0, 0.8, 1.3), (6, 0.7, 0.9)])
+def test_gumbel_max_frequencies_chi_square(top_k, top_p, temp):
+    """P(sample = i) equals the renormalised kept-set probability of i."""
+    x = np.random.default_rng(42).normal(0, 1.0, 16).astype(np.float32)
+    kept, probs = _brute_kept(x, temp, top_k, top_p)
+    if probs is None:
+        xs = np.array([float(v) / float(np.float32(temp)) for v in x])
+        e = np.exp(xs - xs.max())
+        probs = {i: e[i] for i in kept}
+    ids = sorted(kept)
+    p = np.array([probs[i] for i in ids])
+    p /= p.sum()
+    n = 40000
+    counts = np.zeros(16, np.int64)
+    for step in range(n):
+        counts[oracle.sample_row(x, 77, step, 9, temp, top_k, top_p)[0]] += 1
+    assert counts[[i for i in range(16) if i not in kept]].sum() == 0
+    chi = stats.chisquare(counts[ids], p * n)
+    assert chi.pvalue > 1e-4, chi
+
+
+def test_seed_salt_step_each_change_the_stream():
+    x = np.zeros(1000, np.float32)  # uniform over 1000 tokens
+    base = [oracle.sample_row(x, 1, s, 0, 1.0, 0, 1.0)[0] for s in range(30)]
+    assert base == [oracle.sample_row(x, 1, s, 0, 1.0, 0, 1.0)[0] for s in range(30)]
+    assert base != [oracle.sample_row(x, 2, s, 0, 1.0, 0, 1.0)[0] for s in range(30)]
+    assert base != [oracle.sample_row(x, 1, s, 1, 1.0, 0, 1.0)[0] for s in range(30)]
+    assert base != [oracle.sample_row(x, 1, s + 1, 0, 1.0, 0, 1.0)[0] for s in range(30)]
+
+
+def test_kinds_stop_takes_precedence():
+    stops = [7, 100]
+    assert oracle.token_kind(7, stops, 0, 50) == oracle.KIND_STOP
+    assert oracle.token_kind(100, stops, 0, 200) == oracle.KIND_STOP
+    assert oracle.token_kind(49, stops, 0, 50) == oracle.KIND_AUDIO
+    assert oracle.token_kind(50, stops, 0, 50) == oracle.KIND_OTHER
+    assert oracle.token_kind(3, [], 5, 9) == oracle.KIND_OTHER
+
+
+def test_batched_sampler_padding_and_advance():
+    rng = np.random.default_rng(4)
+    B, V = 6, 64
+    x = rng.normal(0, 2, (B, V)).astype(np.float32)
+    slots = np.array([1, 2, 0, 3, 4, 0], np.int32)
+    active = np.array([1, 1, 0, 1, 1, 0], np.int32)
+    seeds = np.arange(5, dtype=np.uint64) * 11
+    steps = np.array([100, 3, 4, 5, 6], np.int64)
+    T = np.full(5, 0.9, np.float32)
+    K = np.full(5, 10, np.int32)
+    P = np.full(5, 0.9, np.float32)
+    tok, kind, info, bad = oracle.seeded_sample(x, slots, active, seeds, steps, T, K, P, salt=0,
+                                                advance=True, stop_tokens=[5], audio_lo=10,
+                                                audio_hi=40)
+    assert bad == 0
+    assert list(steps) == [100, 4, 5, 6, 7]  # dummy slot 0 untouched
+    for b in range(B):
+        if not active[b]:
+            assert tok[b] == 0 and kind[b] == oracle.KIND_OTHER
+            continue
+        s = slots[b]
+        t1, _ = oracle.sample_row(x[b], seeds[s], steps[s] - 1, 0, T[s], K[s], P[s])
+        assert tok[b] == t1
+        assert kind[b] == oracle.token_kind(t1, [5], 10, 40)
+
+
+# ---------------------------------------------------------------------------
+# Frame loop
+# ---------------------------------------------------------------------------
+def _frame_inputs(seed=0, n_cb=12, B=3, V=64):
+    rng = np.random.default_rng(seed)
+    base = rng.normal(0, 3, (n_cb, B, V)).astype(np.float32)
+    fb = rng.normal(0, 1, (n_cb, V, V)).astype(np.float32)
+    slots = np.array([1, 0, 2][:B], np.int32)
+    active = np.array([1, 0, 1][:B], np.int32)
+    seeds = np.array([0, 21, 22], np.uint64)
+    T = np.full(3, 0.9, np.float32)
+    K = np.full(3, 8, np.int32)
+    P = np.full(3, 0.9, np.float32)
+    return base, fb, slots, active, seeds, T, K, P
+
+
+def test_frame_without_feedback_equals_independent_salted_samples():
+    base, fb, slots, active, seeds, T, K, P = _frame_inputs()
+    steps = np.array([0, 7, 9], np.int64)
+    codes, kind, _, bad = oracle.codebook_frame_sample(base, None, slots, active, seeds, steps, T, K, P)
+    assert bad == 0 and list(steps) == [0, 8, 10]
+    for b in range(3):
+        if not active[b]:
+            assert np.all(codes[b] == 0) and kind[b] == oracle.KIND_OTHER
+            continue
+        s = slots[b]
+        want = [oracle.sample_row(base[j, b], seeds[s], steps[s] - 1, 1 + j, T[s], K[s], P[s])[0]
+                for j in range(12)]
+        assert list(codes[b]) == want and kind[b] == oracle.KIND_AUDIO
+
+
+def test_frame_feedback_wiring():
+    """Codebook j > 0 samples base[j] + fb[j][code_{j-1}], added in fp32."""
+    base, fb, slots, active, seeds, T, K, P = _frame_inputs(seed=1)
+    steps = np.array([0, 3, 4], np.int64)
+    codes, _, _, _ = oracle.codebook_frame_sample(base, fb, slots, active, seeds, steps.copy(), T, K, P)
+    for b in (0, 2):
+        s = slots[b]
+        prev = None
+        for j in range(12):
+            row = base[j, b] if j == 0 else (base[j, b] + fb[j, prev]).astype(np.float32)
+            prev = oracle.sample_row(row, seeds[s], steps[s], 1 + j, T[s], K[s], P[s])[0]
+            assert codes[b, j] == prev
+    # the feedback matters: zero it and the codes change somewhere
+    codes0, _, _, _ = oracle.codebook_frame_sample(base, np.zeros_like(fb), slots, active, seeds,
+                                                   steps.copy(), T, K, P)
+    codes_none, _, _, _ = oracle.codebook_frame_sample(base, None, slots, active, seeds,
+                                                       steps.copy(), T, K, P)
+    np.testing.assert_array_equal(codes0, codes_none)
+    assert np.any(codes0 != codes)
