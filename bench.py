@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of one batched decode step over a paged KV cache on GB300.
+
+A step is the whole hot path over one batch of synthetic input: for every
+layer kv_append + paged_decode_attn, then seeded_sample over the logits
+(and, for the frame workload, one 12-codebook frame).  Inputs are resident
+in HBM when the timed region starts; the per-step KV footprint is far larger
+than L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``value`` is the step's algorithmic bytes
+(KV of every token inside each context + q + out + page-table reads +
+appended rows + logits [+ frame rows]) over the step time, in GB/s, summed
+over ranks (each rank runs its own replica: "replicas only", weak scaling).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn HBM GB/s (% of ~8 TB/s) and sampled rows/s at 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+def step_bytes(batch, cfg, vocab, frame_vocab=0):
+    """Algorithmic bytes of the pieces of one step (see the module doc)."""
+    act = batch.active.astype(bool)
+    n = batch.seq_lens[act].astype(float)
+    npg = (n + cfg.page_size - 1) // cfg.page_size
+    n_act = int(act.sum())
+    kv = float((n * 2 * cfg.num_kv_heads * cfg.head_dim * 2).sum())
+    qo = n_act * cfg.num_qo_heads * cfg.head_dim * 2 * 2
+    pt = float(npg.sum() * 4)
+    attn = kv + qo + pt
+    append = n_act * 2 * cfg.num_kv_heads * cfg.head_dim * 2 * 2
+    logits = n_act * vocab * 4
+    frame = 0
+    if cfg.n_codebooks:
+        frame = (2 * cfg.n_codebooks - 1) * n_act * frame_vocab * 4
+    return dict(attn_per_layer=attn, kv_per_layer=kv, append_per_layer=append, logits=logits,
+                frame=frame, step=cfg.num_layers * (attn + append) + logits + frame,
+                n_active=n_act)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attn_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    src = os.path.join(ROOT, "paged_kv_decode_pages_gb300", "csrc", "decode_attn.cu")
+    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        e = rec.get(workload)
+        if e and e.get("source_sha256_16") == h:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = str(device_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-i", sel, "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle, timed on host cores (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+class OracleRunner:
+    """Runs the fp64 oracle over whole layers of the workload (all rows), the
+    sampler and the frame, on inputs copied from the device."""
+
+    def __init__(self, batch, tensors):
+        import numpy as np
+        import oracle
+        from paged_kv_decode_pages_gb300 import workloads as W
+        self.np, self.oracle, self.W = np, oracle, W
+        self.batch, self.t = batch, tensors
+        act = batch.active.astype(bool)
+        self.rows = [b for b in range(batch.B) if act[b]]
+        # compact page table over the active rows: their pages renumbered 1..
+        pt = np.zeros_like(batch.page_table)
+        self.pages = []
+        o = 1
+        for b in self.rows:
+            k = batch.npages(b)
+            pt[b, :k] = np.arange(o, o + k)
+            self.pages.extend(batch.page_table[b, :k].tolist())
+            o += k
+        self.pt = pt
+        self.pages_t = None
+        self.logits = None if tensors.logits is None else tensors.logits.cpu().numpy()
+        self.base = None if tensors.base is None else tensors.base.cpu().numpy()
+        self.fb = None if tensors.fb is None else tensors.fb.cpu().numpy()
+
+    def layer_inputs(self, l):
+        import torch
+        W = self.W
+        c = self.t.cache
+        if self.pages_t is None:
+            self.pages_t = torch.as_tensor(self.pages, dtype=torch.int64, device=c.device)
+        body = c[l].index_select(0, self.pages_t).cpu()
+        compact = torch.zeros((1, body.shape[0] + 1) + tuple(body.shape[1:]), dtype=body.dtype)
+        compact[0, 1:] = body
+        return (W.bf16_bits(compact), W.bf16_bits(self.t.q[l]), W.bf16_bits(self.t.k[l]),
+                W.bf16_bits(self.t.v[l]))
+
+    def run_layer(self, inputs):
+        cb, q, k, v = inputs
+        b = self.batch
+        t0 = time.perf_counter()
+        self.oracle.kv_append(cb, 0, k, v, self.pt, b.seq_lens, b.active)
+        self.oracle.paged_decode_attn(cb, 0, q, self.pt, b.seq_lens, b.active)
+        return time.perf_counter() - t0
+
+    def run_sampler(self):
+        b = self.batch
+        t0 = time.perf_counter()
+        steps = b.steps.copy()
+        if self.logits is not None:
+            self.oracle.seeded_sample(self.logits, b.slots, b.active, b.seeds, steps,
+                                      b.temperature, b.top_k, b.top_p)
+        if self.base is not None:
+            self.oracle.codebook_frame_sample(self.base, self.fb, b.slots, b.active, b.seeds,
+                                              steps, b.temperature, b.top_k, b.top_p)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(batch, tensors, sizes, budget_s=12.0):
+    """The oracle on a bounded sample of the workload: whole layers (every
+    row) until about budget_s seconds of oracle compute, plus the sampler."""
+    import oracle
+    r = OracleRunner(batch, tensors)
+    L = batch.cfg.num_layers
+    t_total, nbytes, layers = 0.0, 0.0, 0
+    for l in range(L):
+        t_total += r.run_layer(r.layer_inputs(l))
+        nbytes += sizes["attn_per_layer"] + sizes["append_per_layer"]
+        layers += 1
+        if t_total >= budget_s:
+            break
+    t_total += r.run_sampler()
+    nbytes += sizes["logits"] + sizes["frame"]
+    return {"value": nbytes / t_total / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d layers (append + attention, all %d rows) + sampler%s, %.1f s"
+                      % (layers, L, batch.B, " + frame" if sizes["frame"] else "", t_total)}
+
+
+# ---------------------------------------------------------------------------
+def make_workload(name, device):
+    from paged_kv_decode_pages_gb300 import workloads as W
+    cfg = W.CONFIGS[name]
+    batch = W.make_batch(cfg)
+    tensors = W.Tensors(batch, device=device)
+    return cfg, batch, tensors
+
+
+def workload_config(cfg, batch, l2_note):
+    return {"workload": cfg.name, "layers": cfg.num_layers, "q_heads": cfg.num_qo_heads,
+            "kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim, "page_size": cfg.page_size,
+            "batch": batch.B, "active": int(batch.active.sum()),
+            "context_min": int(batch.seq_lens[batch.active == 1].min()),
+            "context_max": int(batch.seq_lens[batch.active == 1].max()),
+            "vocab": cfg.vocab, "temperature": cfg.temperature, "top_k": cfg.top_k,
+            "top_p": cfg.top_p, "n_codebooks": cfg.n_codebooks, "l2": l2_note}
+
+
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores: each step is one whole
+    layer of the workload (rotating) plus the sampler."""
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    cfg, batch, tensors = make_workload(args.workload, dev)
+    sizes = step_bytes(batch, cfg, cfg.vocab, cfg.frame_vocab)
+    r = OracleRunner(batch, tensors)
+    L = cfg.num_layers
+    tot, nbytes = 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        t = r.run_layer(r.layer_inputs(i % L)) + r.run_sampler()
+        if i >= args.warmup:
+            tot += t
+            nbytes += (sizes["attn_per_layer"] + sizes["append_per_layer"] + sizes["logits"]
+                       + sizes["frame"])
+    value = nbytes / tot / 1e9
+    sample = ("per step: 1 of %d layers (append + attention, all %d rows) + sampler%s"
+              % (L, batch.B, " + frame" if sizes["frame"] else ""))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(cfg, batch, "host memory"),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="long_context")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import paged_kv_decode_pages_gb300 as pkv
+    from paged_kv_decode_pages_gb300.step import DecodeStep
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    pkv.load()
+
+    cfg, batch, tensors = make_workload(args.workload, "cuda")
+    sizes = step_bytes(batch, cfg, cfg.vocab, cfg.frame_vocab)
+    step = DecodeStep(batch, tensors)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step.run(stream)
+    barrier()
+
+    # ---- device-resident timed region --------------------------------
+    clocks = Clocks(local)
+    attn_ev = []
+    samp_ev = []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.run(stream, attn_events=attn_ev)
+    e1.record(stream)
+    e1.synchronize()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(e0.elapsed_time(e1))
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    barrier()
+
+    # ---- sampler alone (rows/s), same stream, after the timed step loop
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    n_samp = 50
+    s0.record(stream)
+    for _ in range(n_samp):
+        step.sample(stream=stream)
+    s1.record(stream)
+    s1.synchronize()
+    sampler_us = s0.elapsed_time(s1) / n_samp * 1e3
+    barrier()
+
+    # ---- end to end: host (pinned) inputs in, tokens out, every step ----
+    host_in = [(tensors.q, tensors.q.cpu().pin_memory()), (tensors.k, tensors.k.cpu().pin_memory()),
+               (tensors.v, tensors.v.cpu().pin_memory()),
+               (step.page_table, step.page_table.cpu().pin_memory()),
+               (step.seq_lens, step.seq_lens.cpu().pin_memory()),
+               (step.active, step.active.cpu().pin_memory())]
+    if tensors.logits is not None:
+        host_in.append((tensors.logits, tensors.logits.cpu().pin_memory()))
+    if tensors.base is not None:
+        host_in.append((tensors.base, tensors.base.cpu().pin_memory()))
+    outs = [step.out_tok, step.out_kind] + ([step.out_codes] if tensors.base is not None else [])
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+    barrier()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        for d, h in host_in:
+            d.copy_(h, non_blocking=True)
+        step.run(stream)
+        for d, h in zip(outs, host_out):
+            h.copy_(d, non_blocking=True)
+    x1.record(stream)
+    x1.synchronize()
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1))
+    barrier()
+
+    ms_per_step = total_ms / args.steps
+    value = world * sizes["step"] * args.steps / (total_ms / 1e3) / 1e9
+    e2e_value = world * sizes["step"] * args.steps / (e2e_ms / 1e3) / 1e9
+    attn_avg_s = float(np.mean(attn_ms)) / 1e3
+    achieved = sizes["attn_per_layer"] / attn_avg_s / 1e9
+    peak, peak_src = peaks()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "compute": "bf16 in, fp32 accumulate (attention); fp64 sampler decisions",
+        "data": "synthetic",
+        "config": workload_config(cfg, batch, "inputs larger than L2: %.1f GB of KV per step"
+                                  % (sizes["kv_per_layer"] * cfg.num_layers / 1e9)),
+        "sampled_rows_per_s": world * sizes["n_active"] * args.steps / (total_ms / 1e3),
+        "sampler": {"us_per_call": sampler_us,
+                    "rows_per_s": sizes["n_active"] / (sampler_us / 1e6)},
+        "attn": {"us_per_layer": attn_avg_s * 1e6, "gbs": achieved,
+                 "bytes_per_layer": sizes["attn_per_layer"]},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": attn_traffic(cfg.name),
+                     "kernel": "pkv_paged_decode_attn (split + merge kernels), per layer",
+                     "peak_source": peak_src},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": args.steps * step.launches_per_step(),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(batch, tensors, sizes, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

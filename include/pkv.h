@@ -1,0 +1,244 @@
+/*
+ * pkv.h -- C ABI of the GB300 (sm_103a) paged-KV decode step.
+ *
+ * One batched decode step over a paged KV cache, as the vox-serve docs
+ * ("Adding a Model") state the problem: rows in; out_tok / out_kind out;
+ * padding entries (active == 0) point at a dummy slot and KV page 0, do
+ * real (ignored) work and never write another request's state; a request
+ * samples the same tokens whatever batch it lands in.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All array pointers are DEVICE pointers owned by the caller.  The
+ *    library allocates nothing, frees nothing, never synchronises and never
+ *    reads device memory from the host.
+ *  - `stream` is a cudaStream_t (NULL: the legacy default stream).  Work is
+ *    stream-ordered; launch shapes depend only on the scalar arguments, so a
+ *    call may be captured into a CUDA graph and replayed.
+ *  - Return value: PKV_OK, or an error status.  Host-side argument errors are
+ *    reported before anything is launched.  PKV_ERR_CUDA reports a launch
+ *    error (cudaGetLastError, which does not synchronise).
+ *  - Data errors found on the device (a page id outside [0, num_pages), a
+ *    seq_len outside [1, max_pages * page_size], a slot outside
+ *    [0, num_slots), a non-finite logit) are never trapped: the kernel
+ *    avoids the bad access (page 0 / slot 0 / no write instead), ORs a
+ *    PKV_DEV_ERR_* bit into *err_word when err_word is not NULL, and the
+ *    affected row's outputs are unspecified.  Other rows are unaffected.
+ *  - Page 0 and slot 0 are reserved for padding entries; no request may own
+ *    them.  Slots of the active rows of one call must be distinct.
+ *  - Tensors are C-contiguous unless a stride argument says otherwise.
+ *    Device pointers to bf16 / fp32 data must be 16-byte aligned.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG 1 /* null pointer, non-positive size, bad shape */
+#define PKV_ERR_UNSUPPORTED 2 /* valid, but outside what the kernels cover   */
+#define PKV_ERR_CUDA 3        /* a kernel launch failed                       */
+#define PKV_ERR_WORKSPACE 4   /* workspace missing or smaller than required   */
+
+/* ---- device-side error bits (ORed into *err_word) --------------------- */
+#define PKV_DEV_ERR_PAGE 0x1    /* page id outside [0, num_pages)             */
+#define PKV_DEV_ERR_SEQ_LEN 0x2 /* active row seq_len outside [1, max_pages*ps] */
+#define PKV_DEV_ERR_SLOT 0x4    /* active row slot outside [0, num_slots)     */
+#define PKV_DEV_ERR_TIMEOUT 0x8 /* a bounded wait on an async copy gave up    */
+#define PKV_DEV_ERR_LOGITS 0x10 /* NaN or +inf logit in an active row         */
+
+/* ---- out_kind codes ("Adding a Model", section "How a program runs":
+ *      out_kind is audio frame, stop, or other) ------------------------- */
+#define PKV_KIND_OTHER 0
+#define PKV_KIND_AUDIO 1
+#define PKV_KIND_STOP 2
+
+/* Geometry of the paged cache: one bf16 tensor
+ *   cache[num_layers][num_pages][2][page_size][num_kv_heads][head_dim]
+ * for all layers ("Adding a Model", section "1. The model code").  Index 0
+ * of dim 2 holds K, index 1 holds V. */
+typedef struct {
+  int32_t num_layers;
+  int32_t num_pages;
+  int32_t page_size;    /* tokens per page; 16 is the supported value       */
+  int32_t num_kv_heads;
+  int32_t head_dim;     /* 64 or 128                                         */
+} pkv_cache_t;
+
+/* Library version string, e.g. "pkv 0.1.0 sm_103a". */
+const char *pkv_version(void);
+
+/* Human-readable name of a status code. */
+const char *pkv_error_string(int status);
+
+/* Number of device-side error bits defined above (for binding checks). */
+int pkv_num_dev_error_bits(void);
+
+/* ------------------------------------------------------------------------
+ * pkv_kv_append -- set_kv_cache(kv_cache, k, v) of "Adding a Model",
+ * section "1. The model code": write each row's new key and value into the
+ * slot of layer `layer` that holds position seq_lens[b] - 1.
+ *
+ *   cache       bf16, the layout of pkv_cache_t; written in place.
+ *   k, v        bf16 [batch][num_kv_heads][head_dim], the new token's K, V.
+ *   page_table  int32 [batch][max_pages]; page_table[b][i] is the page that
+ *               holds positions [i*page_size, (i+1)*page_size) of row b.
+ *   seq_lens    int32 [batch]; the row's length INCLUDING this token.
+ *   active      int32 [batch]; 0 marks a padding entry.
+ *
+ * An active row writes cache[layer][page][0|1][(n-1) % page_size] with
+ * page = page_table[b][(n-1) / page_size], n = seq_lens[b].  A padding row
+ * writes its (ignored) k, v to page 0, slot 0, the dummy page, and nowhere
+ * else.  Nothing else in the cache changes.
+ * Errors: PKV_ERR_INVALID_ARG for a null pointer, batch <= 0, layer outside
+ * [0, num_layers), max_pages <= 0 or a bad geometry; PKV_ERR_UNSUPPORTED for
+ * num_kv_heads * head_dim not a multiple of 8.  Device: PKV_DEV_ERR_SEQ_LEN
+ * or PKV_DEV_ERR_PAGE, and that row writes nothing.
+ * ---------------------------------------------------------------------- */
+int pkv_kv_append(const pkv_cache_t *geom, void *cache, int layer,
+                  const void *k, const void *v, const int32_t *page_table,
+                  int max_pages, const int32_t *seq_lens,
+                  const int32_t *active, int batch, int32_t *err_word,
+                  void *stream);
+
+/* Workspace (bytes) pkv_paged_decode_attn needs for these sizes. */
+size_t pkv_decode_workspace_bytes(int batch, int num_qo_heads, int head_dim,
+                                  int max_pages, int page_size);
+
+/* ------------------------------------------------------------------------
+ * pkv_paged_decode_attn -- attn_wrapper.run(q, kv_cache) of "Adding a
+ * Model", section "1. The model code": grouped-query decode attention of one
+ * query token per row over that row's pages of layer `layer`.
+ *
+ * For row b, q head h, kv head g = h / (num_qo_heads / num_kv_heads) (section
+ * "2. The program" gives only the head counts; contiguous groups are the
+ * reading taken), n = seq_lens[b]:
+ *     s_t = sm_scale * <q[b][h], K_t>,   t = 0 .. n-1 (gathered via the
+ *                                         page table),
+ *     out[b][h] = sum_t softmax(s)_t * V_t,   lse[b][h] = log sum_t e^{s_t}.
+ *
+ *   q           bf16 [batch][num_qo_heads][head_dim].
+ *   sm_scale    softmax scale; pass 1/sqrt(head_dim) for the usual one.
+ *   out         [batch][num_qo_heads][head_dim], bf16 (rounded once, to
+ *               nearest even) or fp32 when out_fp32 != 0.
+ *   lse         fp32 [batch][num_qo_heads] natural-log log-sum-exp, or NULL.
+ *   workspace   device scratch of at least pkv_decode_workspace_bytes(...)
+ *               bytes (split partials); contents need not be initialised.
+ *               Calls that overlap on the device must not share it.
+ * Arithmetic: bf16 inputs, fp32 accumulation, long rows split into fixed
+ * 512-token pieces merged by log-sum-exp in split order, so the result of a
+ * row depends on its own inputs only (not on the batch it is in).
+ * Padding rows (active == 0) read nothing and write zeros (lse = -inf).
+ * Errors: PKV_ERR_INVALID_ARG (null pointer, bad sizes, num_qo_heads not a
+ * multiple of num_kv_heads), PKV_ERR_UNSUPPORTED (head_dim not 64 / 128,
+ * page_size != 16, more than 64 q heads per kv head), PKV_ERR_WORKSPACE.
+ * Device: PKV_DEV_ERR_SEQ_LEN (row written as zeros), PKV_DEV_ERR_PAGE (page 0
+ * read instead; row unspecified), PKV_DEV_ERR_TIMEOUT.
+ * ---------------------------------------------------------------------- */
+int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
+                          int layer, const void *q, int num_qo_heads,
+                          float sm_scale, const int32_t *page_table,
+                          int max_pages, const int32_t *seq_lens,
+                          const int32_t *active, int batch, void *out,
+                          int out_fp32, float *lse, void *workspace,
+                          size_t workspace_bytes, int32_t *err_word,
+                          void *stream);
+
+/* Workspace (bytes) pkv_seeded_sample needs for these sizes. */
+size_t pkv_sample_workspace_bytes(int batch, int vocab);
+
+/* ------------------------------------------------------------------------
+ * pkv_seeded_sample -- sample_into of "Adding a Model" (sections "How a
+ * program runs" and "2. The program") with the sampler semantics of
+ * "Supported Models" (mstar docs), "Fish Audio S2-Pro notes" and
+ * "Chatterbox notes".
+ *
+ * For each active row b with slot s = slots[b]:
+ *   - temperature[s] <= 1e-5: greedy, the lowest id among the largest logits;
+ *   - else x = logit / temperature[s] (fp64); order tokens by (x desc, id
+ *     asc); keep the first top_k[s] (0 or >= vocab: all); then, if
+ *     top_p[s] < 1, keep token r of that order iff r == 0 or
+ *     S_{r-1} < top_p * Z, where S is the running sum of exp(x - x_max) in
+ *     order and Z its total over the top-k survivors (the crossing token is
+ *     kept);
+ *   - the sample is the kept token with the largest x + g, g = -log(-log u),
+ *     u = (2 * (w >> 12) + 1) * 2^-53, w = word 0 of Philox4x64-10 with key
+ *     (seeds[s], salt) and counter (token id, steps[s], 0, 0); lowest id on
+ *     exact ties.  All of this is computed in fp64.
+ *   - out_kind: PKV_KIND_STOP if the token is in stop_tokens, else
+ *     PKV_KIND_AUDIO if audio_lo <= token < audio_hi, else PKV_KIND_OTHER.
+ *   - advance != 0: steps[s] += 1 after sampling.
+ * Padding rows: out_tok = 0, out_kind = OTHER, no state touched.
+ *
+ *   logits       fp32, row b at logits + b * row_stride (row_stride >= vocab,
+ *                a multiple of 4).
+ *   slots        int32 [batch]; active int32 [batch].
+ *   seeds        uint64 [num_slots]; steps int64 [num_slots] (read, and
+ *                written when advance); temperature fp32, top_k int32,
+ *                top_p fp32 [num_slots].
+ *   stop_tokens  int32 [n_stop] device array, or NULL when n_stop == 0.
+ *   out_tok, out_kind  int32 [batch].
+ *   workspace    at least pkv_sample_workspace_bytes(batch, vocab) bytes.
+ * The result of a row depends on its own logits and slot state only; it is
+ * bit-identical whatever batch size or batch position it is sampled at.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_WORKSPACE.  Device: PKV_DEV_ERR_SLOT
+ * (row gives token 0, OTHER, no state touched), PKV_DEV_ERR_LOGITS.
+ * ---------------------------------------------------------------------- */
+int pkv_seeded_sample(const float *logits, int64_t row_stride, int batch,
+                      int vocab, const int32_t *slots, const int32_t *active,
+                      int num_slots, const uint64_t *seeds, int64_t *steps,
+                      const float *temperature, const int32_t *top_k,
+                      const float *top_p, uint32_t salt, int advance,
+                      const int32_t *stop_tokens, int n_stop,
+                      int32_t audio_lo, int32_t audio_hi, int32_t *out_tok,
+                      int32_t *out_kind, void *workspace,
+                      size_t workspace_bytes, int32_t *err_word,
+                      void *stream);
+
+/* Workspace (bytes) pkv_codebook_frame_sample needs for these sizes. */
+size_t pkv_frame_workspace_bytes(int n_codebooks, int batch, int vocab);
+
+/* ------------------------------------------------------------------------
+ * pkv_codebook_frame_sample -- the frame-local codebook loop of
+ * MOSS-TTS-Local on SGLang-Omni (mosi.cn blog): per frame, the RVQ
+ * codebooks are sampled in order, each one fed back before the next, on a
+ * seeded GPU sampler ("AR Engine" section).
+ *
+ * For each active row b (slot s), for j = 0 .. n_codebooks-1 in order:
+ *     logits_j = base[j][b]                           (j == 0 or fb NULL)
+ *     logits_j = fl32(base[j][b] + fb[j][code_{j-1}])  (otherwise)
+ *     code_j   = the pkv_seeded_sample rule on logits_j with salt 1 + j and
+ *                the frame's step steps[s]
+ * then steps[s] += 1 (once per frame) and out_kind[b] = PKV_KIND_AUDIO.
+ * No trained local transformer exists here: the additive row gather is a
+ * synthetic stand-in that keeps the loop serial and data-dependent.
+ * Padding rows: codes 0, kind OTHER, no state touched.  One launch per
+ * frame; the 12-step loop runs inside the kernel.
+ *
+ *   base        fp32 [n_codebooks][batch][vocab].
+ *   fb          fp32 [n_codebooks][vocab][vocab] or NULL.
+ *   out_codes   int32 [batch][n_codebooks]; out_kind int32 [batch].
+ *   other arguments as for pkv_seeded_sample.
+ * Errors: as pkv_seeded_sample.
+ * ---------------------------------------------------------------------- */
+int pkv_codebook_frame_sample(const float *base, const float *fb,
+                              int n_codebooks, int batch, int vocab,
+                              const int32_t *slots, const int32_t *active,
+                              int num_slots, const uint64_t *seeds,
+                              int64_t *steps, const float *temperature,
+                              const int32_t *top_k, const float *top_p,
+                              int32_t *out_codes, int32_t *out_kind,
+                              void *workspace, size_t workspace_bytes,
+                              int32_t *err_word, void *stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,217 @@
+"""ctypes binding of libpkv (include/pkv.h).  Argument marshalling only: torch
+tensors become device pointers, the current torch CUDA stream becomes the
+``stream`` argument, and a non-zero status raises ``PkvError``.  There is no
+fallback of any kind: without the library (or a GPU) every call raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+KIND_OTHER, KIND_AUDIO, KIND_STOP = 0, 1, 2
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_U32 = ctypes.c_uint32
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+
+class pkv_cache_t(ctypes.Structure):
+    _fields_ = [("num_layers", _I32), ("num_pages", _I32), ("page_size", _I32),
+                ("num_kv_heads", _I32), ("head_dim", _I32)]
+
+
+# every symbol include/pkv.h declares, with its ctypes signature
+SIGNATURES = {
+    "pkv_version": (ctypes.c_char_p, []),
+    "pkv_error_string": (ctypes.c_char_p, [_I]),
+    "pkv_num_dev_error_bits": (_I, []),
+    "pkv_kv_append": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _P, _P, _I, _P, _P, _I, _P,
+                           _P]),
+    "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_paged_decode_attn": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _I, _F, _P, _I, _P,
+                                   _P, _I, _P, _I, _P, _P, _SZ, _P, _P]),
+    "pkv_sample_workspace_bytes": (_SZ, [_I, _I]),
+    "pkv_seeded_sample": (_I, [_P, _I64, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _U32, _I, _P,
+                               _I, _I32, _I32, _P, _P, _P, _SZ, _P, _P]),
+    "pkv_frame_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "pkv_codebook_frame_sample": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _SZ, _P, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (fn, error_string(status), status))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libpkv.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if build_if_missing and not _build.up_to_date():
+                _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError("libpkv.so is missing (%s); run paged_kv_decode_pages_gb300."
+                                   "build.build()" % path)
+            L = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def version() -> str:
+    return load().pkv_version().decode()
+
+
+def error_string(status: int) -> str:
+    return load().pkv_error_string(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != 0:
+        raise PkvError(fn, status)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _geom(cache):
+    L, P, two, ps, hkv, d = cache.shape
+    assert two == 2, "cache dim 2 must be 2 (K, V)"
+    return pkv_cache_t(L, P, ps, hkv, d)
+
+
+def _req(t, dtype, name, cuda=True):
+    import torch
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if cuda and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    return t
+
+
+# ---------------------------------------------------------------------------
+def kv_append(cache, layer, k, v, page_table, seq_lens, active, err_word=None, stream=None):
+    import torch
+    _req(cache, torch.bfloat16, "cache")
+    _req(k, torch.bfloat16, "k")
+    _req(v, torch.bfloat16, "v")
+    _req(page_table, torch.int32, "page_table")
+    _req(seq_lens, torch.int32, "seq_lens")
+    _req(active, torch.int32, "active")
+    g = _geom(cache)
+    st = load().pkv_kv_append(ctypes.byref(g), _ptr(cache), int(layer), _ptr(k), _ptr(v),
+                              _ptr(page_table), page_table.shape[1], _ptr(seq_lens),
+                              _ptr(active), seq_lens.shape[0], _ptr(err_word), _stream(stream))
+    _check("pkv_kv_append", st)
+
+
+def decode_workspace_bytes(batch, num_qo_heads, head_dim, max_pages, page_size=16) -> int:
+    return int(load().pkv_decode_workspace_bytes(batch, num_qo_heads, head_dim, max_pages,
+                                                 page_size))
+
+
+def paged_decode_attn(cache, layer, q, page_table, seq_lens, active, out, workspace,
+                      lse=None, sm_scale=None, err_word=None, stream=None):
+    import torch
+    _req(cache, torch.bfloat16, "cache")
+    _req(q, torch.bfloat16, "q")
+    _req(page_table, torch.int32, "page_table")
+    _req(seq_lens, torch.int32, "seq_lens")
+    _req(active, torch.int32, "active")
+    if out.dtype not in (torch.bfloat16, torch.float32) or not out.is_contiguous():
+        raise TypeError("out must be a contiguous bf16 or fp32 tensor")
+    g = _geom(cache)
+    B, Hq, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / (D ** 0.5)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().pkv_paged_decode_attn(
+        ctypes.byref(g), _ptr(cache), int(layer), _ptr(q), Hq, float(sm_scale), _ptr(page_table),
+        page_table.shape[1], _ptr(seq_lens), _ptr(active), B, _ptr(out),
+        int(out.dtype == torch.float32), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(err_word),
+        _stream(stream))
+    _check("pkv_paged_decode_attn", st)
+
+
+def sample_workspace_bytes(batch, vocab) -> int:
+    return int(load().pkv_sample_workspace_bytes(batch, vocab))
+
+
+def seeded_sample(logits, slots, active, seeds, steps, temperature, top_k, top_p, out_tok,
+                  out_kind, workspace, salt=0, advance=True, stop_tokens=None, audio_lo=0,
+                  audio_hi=0, err_word=None, stream=None):
+    import torch
+    if logits.dtype != torch.float32 or logits.stride(-1) != 1 or not logits.is_cuda:
+        raise TypeError("logits must be a CUDA fp32 tensor with unit last stride")
+    B, V = logits.shape
+    for t, dt, nm in ((slots, torch.int32, "slots"), (active, torch.int32, "active"),
+                      (seeds, torch.uint64, "seeds"), (steps, torch.int64, "steps"),
+                      (temperature, torch.float32, "temperature"), (top_k, torch.int32, "top_k"),
+                      (top_p, torch.float32, "top_p"), (out_tok, torch.int32, "out_tok"),
+                      (out_kind, torch.int32, "out_kind")):
+        _req(t, dt, nm)
+    n_stop = 0 if stop_tokens is None else stop_tokens.numel()
+    st = load().pkv_seeded_sample(
+        _ptr(logits), logits.stride(0), B, V, _ptr(slots), _ptr(active), seeds.numel(),
+        _ptr(seeds), _ptr(steps), _ptr(temperature), _ptr(top_k), _ptr(top_p), int(salt),
+        int(bool(advance)), _ptr(stop_tokens) if n_stop else None, n_stop, int(audio_lo),
+        int(audio_hi), _ptr(out_tok), _ptr(out_kind), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream))
+    _check("pkv_seeded_sample", st)
+
+
+def frame_workspace_bytes(n_codebooks, batch, vocab) -> int:
+    return int(load().pkv_frame_workspace_bytes(n_codebooks, batch, vocab))
+
+
+def codebook_frame_sample(base, fb, slots, active, seeds, steps, temperature, top_k, top_p,
+                          out_codes, out_kind, workspace, err_word=None, stream=None):
+    import torch
+    _req(base, torch.float32, "base")
+    if fb is not None:
+        _req(fb, torch.float32, "fb")
+    n_cb, B, V = base.shape
+    for t, dt, nm in ((slots, torch.int32, "slots"), (active, torch.int32, "active"),
+                      (seeds, torch.uint64, "seeds"), (steps, torch.int64, "steps"),
+                      (temperature, torch.float32, "temperature"), (top_k, torch.int32, "top_k"),
+                      (top_p, torch.float32, "top_p"), (out_codes, torch.int32, "out_codes"),
+                      (out_kind, torch.int32, "out_kind")):
+        _req(t, dt, nm)
+    st = load().pkv_codebook_frame_sample(
+        _ptr(base), _ptr(fb), n_cb, B, V, _ptr(slots), _ptr(active), seeds.numel(), _ptr(seeds),
+        _ptr(steps), _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(out_codes),
+        _ptr(out_kind), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(err_word), _stream(stream))
+    _check("pkv_codebook_frame_sample", st)

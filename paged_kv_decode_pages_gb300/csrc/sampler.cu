@@ -1,0 +1,892 @@
+// sampler.cu -- seeded temperature / top-k / top-p sampling (sample_into of
+// "Adding a Model", vox-serve docs) and the frame-local codebook loop
+// (MOSS-TTS-Local on SGLang-Omni, mosi.cn blog).
+//
+// Semantics ("Supported Models", mstar docs, "Fish Audio S2-Pro notes" and
+// "Chatterbox notes"): temperature first; top-k then top-p over the tempered
+// probabilities of the top-k survivors; the top-p boundary keeps the token
+// whose probability carries the running total past top-p; temperature
+// <= 1e-5 is greedy; a top-k of 0 or >= vocab is no filter.  Randomness:
+// Gumbel-max with Philox4x64-10 (Salmon et al., SC 2011) keyed by
+// (seed, salt) at counter (token, step, 0, 0), so a row's sample depends on
+// its own logits and slot state only.  Every decision (order, top-p cut,
+// Gumbel argmax) is taken in fp64 on values that are exact functions of
+// the fp32 logits.
+//
+// Structure:
+//  * order key: the fp32 logit mapped to a uint32 that sorts like the float
+//    (-0 folded onto +0); composite = key << 32 | ~token, so a larger
+//    composite comes first in (value desc, id asc) order, and composites
+//    are unique.
+//  * chunk pass (one CTA per 8192-token chunk of a row): chunk maximum;
+//    the chunk's 64 largest composites (radix select over 8-bit digits);
+//    for top-p over the whole vocabulary, the fp64 partial normaliser
+//    sum exp(x - x_chunkmax); for "keep everything", the chunk's Gumbel
+//    argmax.  The chunking depends on the vocabulary only.
+//  * finish (one CTA per row): merges the chunk records in chunk order,
+//    sorts the candidates, applies top-k / top-p with sequential fp64
+//    prefix sums in sorted order, and takes the Gumbel argmax.  Rows whose
+//    kept set is not decided by the top 64 tokens (top-k > 64, or top-p
+//    needing more than 64 tokens) take an exact general path that streams
+//    the row: radix select of the top-k threshold and progressive sorted
+//    extraction until the top-p crossing.
+//  * the frame kernel runs the same chunk pass and finish for each of the
+//    codebooks in turn inside one CTA per row.
+#include <math.h>
+
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+
+constexpr int SB = 256;                 // threads per sampler CTA
+constexpr int CHUNK = 8192;             // tokens per chunk
+constexpr int EPT = CHUNK / SB;         // tokens per thread in a chunk pass
+constexpr int NCAND = 64;               // candidates kept per chunk
+constexpr int MAX_CHUNKS = 64;          // vocab <= 64 * 8192
+constexpr int GEN_BLOCK = 1024;         // sorted block of the general path
+constexpr int SORT_CAP = MAX_CHUNKS * NCAND;  // 4096
+
+enum Mode : int { MODE_GREEDY = 0, MODE_TOPK_SMALL = 1, MODE_TOPP_FULL = 2, MODE_ALL = 3, MODE_GENERAL = 4 };
+
+struct ChunkRec {
+  uint64_t top1;       // largest composite of the chunk (0: chunk empty)
+  double mx;           // x of top1
+  double z;            // sum over the chunk of exp(x - mx)        (MODE_TOPP_FULL)
+  double gscore;       // best x + g of the chunk                  (MODE_ALL)
+  int32_t gid;         // its token
+  int32_t ncand;
+  uint64_t cand[NCAND];
+  uint64_t pad_[3];
+};
+static_assert(sizeof(ChunkRec) % 64 == 0, "ChunkRec");
+
+struct RowParams {
+  float temperature;
+  int32_t top_k;
+  float top_p;
+  uint32_t salt;
+  uint64_t seed;
+  int64_t step;
+  int K;       // top-k count after normalisation (V when off)
+  int mode;
+};
+
+// ---------------------------------------------------------------------------
+// Philox4x64-10 and Gumbel noise
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t philox_word0(uint64_t seed, uint32_t salt, uint64_t token,
+                                                 uint64_t step) {
+  const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+  const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+  uint64_t c0 = token, c1 = step, c2 = 0, c3 = 0;
+  uint64_t k0 = seed, k1 = salt;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+    const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+    const uint64_t n0 = hi1 ^ c1 ^ k0;
+    const uint64_t n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += W0;
+    k1 += W1;
+  }
+  return c0;
+}
+
+__device__ __forceinline__ double gumbel(const RowParams &P, int token) {
+  const uint64_t w = philox_word0(P.seed, P.salt, (uint64_t)(uint32_t)token, (uint64_t)P.step);
+  const double u = (double)(2ull * (w >> 12) + 1ull) * 0x1p-53;
+  return -log(-log(u));
+}
+
+// ---------------------------------------------------------------------------
+// order keys
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key(float f, bool &bad) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) {  // NaN: report, rank like -inf
+    bad = true;
+    u = 0xff800000u;
+  } else if (u == 0x7f800000u) {
+    bad = true;
+  }
+  if (u == 0x80000000u) u = 0u;  // -0 == +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  const uint32_t u = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, int token) {
+  return ((uint64_t)key << 32) | (uint32_t)(~(uint32_t)token);
+}
+__device__ __forceinline__ int comp_token(uint64_t c) { return (int)(~(uint32_t)c); }
+__device__ __forceinline__ double comp_x(uint64_t c, float temperature) {
+  return (double)key_value((uint32_t)(c >> 32)) / (double)temperature;
+}
+
+// ---------------------------------------------------------------------------
+// shared scratch
+// ---------------------------------------------------------------------------
+struct SampSmem {
+  uint32_t hist[256];
+  uint64_t red_u64[SB / 32];
+  double red_d[SB];
+  int32_t red_i[SB];
+  uint64_t sel_prefix;
+  uint32_t sel_want;
+  uint32_t sel_done;
+  uint32_t cnt;
+  int32_t flag;
+  int32_t token;
+  int32_t kept;
+  double zsum;
+  uint64_t sortbuf[SORT_CAP];
+  double xs[NCAND];
+  double es[GEN_BLOCK];
+};
+
+// ---------------------------------------------------------------------------
+// block primitives (all SB threads must call)
+// ---------------------------------------------------------------------------
+__device__ uint64_t block_max_u64(uint64_t v, SampSmem &sm) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const uint64_t o = __shfl_xor_sync(FULL_MASK, v, off);
+    v = o > v ? o : v;
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.red_u64[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint64_t r = sm.red_u64[0];
+#pragma unroll
+  for (int w = 1; w < SB / 32; ++w) r = sm.red_u64[w] > r ? sm.red_u64[w] : r;
+  __syncthreads();
+  return r;
+}
+
+// Sum in a fixed order: thread partials, then a fixed binary tree.
+__device__ double block_sum_d(double v, SampSmem &sm) {
+  __syncthreads();
+  sm.red_d[threadIdx.x] = v;
+  __syncthreads();
+  for (int s = SB / 2; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) sm.red_d[threadIdx.x] += sm.red_d[threadIdx.x + s];
+    __syncthreads();
+  }
+  const double r = sm.red_d[0];
+  __syncthreads();
+  return r;
+}
+
+// Argmax of (score desc, id asc); ids < 0 mark "none".
+__device__ __forceinline__ bool better(double s, int id, double bs, int bid) {
+  if (bid < 0) return id >= 0;
+  if (id < 0) return false;
+  return s > bs || (s == bs && id < bid);
+}
+
+__device__ int block_argmax(double s, int id, SampSmem &sm, double *best_score = nullptr) {
+  __syncthreads();
+  sm.red_d[threadIdx.x] = s;
+  sm.red_i[threadIdx.x] = id;
+  __syncthreads();
+  for (int st = SB / 2; st > 0; st >>= 1) {
+    if ((int)threadIdx.x < st) {
+      const double s2 = sm.red_d[threadIdx.x + st];
+      const int i2 = sm.red_i[threadIdx.x + st];
+      if (better(s2, i2, sm.red_d[threadIdx.x], sm.red_i[threadIdx.x])) {
+        sm.red_d[threadIdx.x] = s2;
+        sm.red_i[threadIdx.x] = i2;
+      }
+    }
+    __syncthreads();
+  }
+  const int r = sm.red_i[0];
+  if (best_score) *best_score = sm.red_d[0];
+  __syncthreads();
+  return r;
+}
+
+// Bitonic sort of n (power of two) u64 values in shared memory, descending.
+__device__ void block_sort_desc(uint64_t *v, int n) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += SB) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint64_t a = v[i], b = v[ixj];
+          const bool desc_block = (i & k) == 0;
+          if (desc_block ? (a < b) : (a > b)) {
+            v[i] = b;
+            v[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Warp 0 walks the 256-bin histogram from the top bin down and picks the
+// bin holding the `want`-th (1-based) largest element.  Results in sm.
+__device__ void select_bin(SampSmem &sm, int shift) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    // lane covers bins 255-8*lane .. 248-8*lane (descending)
+    uint32_t c[8];
+    uint32_t tot = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      c[e] = sm.hist[255 - 8 * lane - e];
+      tot += c[e];
+    }
+    uint32_t incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t o = __shfl_up_sync(FULL_MASK, incl, off);
+      if (lane >= off) incl += o;
+    }
+    const uint32_t excl = incl - tot;
+    const uint32_t want = sm.sel_want;
+    const bool mine = excl < want && want <= incl;
+    if (mine) {
+      uint32_t above = excl;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (above + c[e] >= want) {
+          const uint32_t bin = 255 - 8 * lane - e;
+          const uint32_t w2 = want - above;
+          sm.sel_prefix |= (uint64_t)bin << shift;
+          sm.sel_done = (w2 == c[e]) ? 1u : 0u;
+          sm.sel_want = w2;
+          break;
+        }
+        above += c[e];
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// chunk pass
+// ---------------------------------------------------------------------------
+__device__ void chunk_pass(const float *__restrict__ row, int V, int c, const RowParams &P,
+                           ChunkRec *rec, SampSmem &sm, int32_t *err) {
+  const int tid = threadIdx.x;
+  const int start = c * CHUNK;
+  const int cnt = min(CHUNK, V - start);
+  uint32_t key[EPT];
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) {
+    const int i = tid + j * SB;
+    key[j] = (i < cnt) ? order_key(row[start + i], bad) : 0u;  // may be written by this kernel: no __ldg
+  }
+  if (bad) report(err, PKV_DEV_ERR_LOGITS);
+  uint64_t mine = 0;
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) {
+    const int i = tid + j * SB;
+    if (i < cnt) {
+      const uint64_t cc = composite(key[j], start + i);
+      mine = cc > mine ? cc : mine;
+    }
+  }
+  const uint64_t top1 = block_max_u64(mine, sm);
+  if (tid == 0) rec->top1 = top1;
+  if (P.mode == MODE_GREEDY || P.mode == MODE_GENERAL) return;
+
+  if (P.mode == MODE_ALL) {
+    double bs = 0.0;
+    int bid = -1;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int i = tid + j * SB;
+      if (i < cnt) {
+        const int tok = start + i;
+        const double s = (double)key_value(key[j]) / (double)P.temperature + gumbel(P, tok);
+        if (better(s, tok, bs, bid)) {
+          bs = s;
+          bid = tok;
+        }
+      }
+    }
+    double best;
+    const int id = block_argmax(bs, bid, sm, &best);
+    if (tid == 0) {
+      rec->gscore = best;
+      rec->gid = id;
+    }
+    return;
+  }
+
+  // the chunk's NCAND largest composites
+  uint64_t thr = 0;  // keep composites >= thr
+  if (cnt > NCAND) {
+    if (tid == 0) {
+      sm.sel_prefix = 0;
+      sm.sel_want = NCAND;
+      sm.sel_done = 0;
+    }
+    __syncthreads();
+    uint64_t mask = 0;
+    for (int pass = 0; pass < 8; ++pass) {
+      const int shift = 56 - 8 * pass;
+      for (int i = tid; i < 256; i += SB) sm.hist[i] = 0;
+      __syncthreads();
+      const uint64_t prefix = sm.sel_prefix;
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) {
+        const int i = tid + j * SB;
+        if (i < cnt) {
+          const uint64_t cc = composite(key[j], start + i);
+          if ((cc & mask) == prefix) atomicAdd(&sm.hist[(cc >> shift) & 255u], 1u);
+        }
+      }
+      __syncthreads();
+      select_bin(sm, shift);
+      mask |= 255ull << shift;
+      if (sm.sel_done) break;
+    }
+    thr = sm.sel_prefix;
+    __syncthreads();
+  }
+  if (tid == 0) sm.cnt = 0;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) {
+    const int i = tid + j * SB;
+    if (i < cnt) {
+      const uint64_t cc = composite(key[j], start + i);
+      if (cc >= thr) {
+        const uint32_t pos = atomicAdd(&sm.cnt, 1u);
+        if (pos < NCAND) rec->cand[pos] = cc;
+      }
+    }
+  }
+  __syncthreads();
+  const int got = min((int)sm.cnt, NCAND);
+  for (int i = got + tid; i < NCAND; i += SB) rec->cand[i] = 0;
+  if (tid == 0) rec->ncand = got;
+
+  if (P.mode == MODE_TOPP_FULL) {
+    const double mx = comp_x(top1, P.temperature);
+    double z = 0.0;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int i = tid + j * SB;
+      if (i < cnt) z += exp((double)key_value(key[j]) / (double)P.temperature - mx);
+    }
+    z = block_sum_d(z, sm);
+    if (tid == 0) {
+      rec->mx = mx;
+      rec->z = z;
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// general path: exact, streams the row (used when the top 64 do not decide)
+// ---------------------------------------------------------------------------
+// Composite of rank `rank` (0-based, descending) among elements with
+// composite < upper.  Requires that many such elements to exist.
+__device__ uint64_t select_rank(const float *__restrict__ row, int V, uint64_t upper, int rank,
+                                SampSmem &sm) {
+  if (threadIdx.x == 0) {
+    sm.sel_prefix = 0;
+    sm.sel_want = (uint32_t)rank + 1u;
+    sm.sel_done = 0;
+  }
+  __syncthreads();
+  uint64_t mask = 0;
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    for (int i = threadIdx.x; i < 256; i += SB) sm.hist[i] = 0;
+    __syncthreads();
+    const uint64_t prefix = sm.sel_prefix;
+    bool dummy = false;
+    for (int i = threadIdx.x; i < V; i += SB) {
+      const uint64_t cc = composite(order_key(row[i], dummy), i);
+      if (cc < upper && (cc & mask) == prefix) atomicAdd(&sm.hist[(cc >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    select_bin(sm, shift);
+    mask |= 255ull << shift;
+    if (sm.sel_done) break;
+  }
+  const uint64_t r = sm.sel_prefix;
+  __syncthreads();
+  return r;
+}
+
+__device__ int general_sample(const float *__restrict__ row, int V, const RowParams &P,
+                              uint64_t top1, SampSmem &sm) {
+  const int tid = threadIdx.x;
+  const int K = P.K;
+  const uint64_t thrK = (K < V) ? select_rank(row, V, ~0ull, K - 1, sm) : 0ull;
+  uint64_t thr = thrK;
+  if (P.top_p < 1.0f) {
+    const double m = comp_x(top1, P.temperature);
+    double z = 0.0;
+    bool dummy = false;
+    for (int i = tid; i < V; i += SB) {
+      const uint32_t key = order_key(row[i], dummy);
+      if (composite(key, i) >= thrK) z += exp((double)key_value(key) / (double)P.temperature - m);
+    }
+    z = block_sum_d(z, sm);
+    const double pz = (double)P.top_p * z;
+    // progressive sorted extraction until the running sum reaches p * Z
+    uint64_t upper = ~0ull;
+    int taken = 0;
+    double S = 0.0;
+    uint64_t cutoff = top1;
+    bool done = false;
+    while (!done) {
+      const int M = min(GEN_BLOCK, K - taken);
+      const uint64_t lo = select_rank(row, V, upper, M - 1, sm);
+      if (tid == 0) sm.cnt = 0;
+      __syncthreads();
+      for (int i = tid; i < V; i += SB) {
+        const uint64_t cc = composite(order_key(row[i], dummy), i);
+        if (cc >= lo && cc < upper) {
+          const uint32_t pos = atomicAdd(&sm.cnt, 1u);
+          if (pos < GEN_BLOCK) sm.sortbuf[pos] = cc;
+        }
+      }
+      __syncthreads();
+      int n2 = 1;
+      while (n2 < M) n2 <<= 1;
+      for (int i = M + tid; i < n2; i += SB) sm.sortbuf[i] = 0;
+      __syncthreads();
+      block_sort_desc(sm.sortbuf, n2);
+      for (int r = tid; r < M; r += SB) sm.es[r] = exp(comp_x(sm.sortbuf[r], P.temperature) - m);
+      __syncthreads();
+      if (tid == 0) {
+        int r = 0;
+        for (; r < M; ++r) {
+          if (taken + r == 0 || S < pz) {
+            S += sm.es[r];
+            cutoff = sm.sortbuf[r];
+          } else {
+            break;
+          }
+        }
+        sm.flag = (r < M || taken + M >= K) ? 1 : 0;
+        sm.zsum = S;
+        sm.sel_prefix = cutoff;
+      }
+      __syncthreads();
+      done = sm.flag != 0;
+      S = sm.zsum;
+      cutoff = sm.sel_prefix;
+      taken += M;
+      upper = lo;
+      __syncthreads();
+    }
+    thr = cutoff;
+  }
+  // Gumbel argmax over the kept tokens (composite >= thr)
+  double bs = 0.0;
+  int bid = -1;
+  bool dummy = false;
+  for (int i = tid; i < V; i += SB) {
+    const uint32_t key = order_key(row[i], dummy);
+    if (composite(key, i) >= thr) {
+      const double s = (double)key_value(key) / (double)P.temperature + gumbel(P, i);
+      if (better(s, i, bs, bid)) {
+        bs = s;
+        bid = i;
+      }
+    }
+  }
+  return block_argmax(bs, bid, sm);
+}
+
+// ---------------------------------------------------------------------------
+// finish: one CTA per row
+// ---------------------------------------------------------------------------
+__device__ int finish_row(const float *__restrict__ row, int V, int nch, const RowParams &P,
+                          const ChunkRec *recs, SampSmem &sm) {
+  const int tid = threadIdx.x;
+  if (P.mode == MODE_GREEDY) {
+    uint64_t best = 0;
+    for (int c = 0; c < nch; ++c) best = recs[c].top1 > best ? recs[c].top1 : best;
+    return comp_token(best);
+  }
+  if (P.mode == MODE_ALL) {
+    double bs = 0.0;
+    int bid = -1;
+    for (int c = 0; c < nch; ++c)
+      if (better(recs[c].gscore, recs[c].gid, bs, bid)) {
+        bs = recs[c].gscore;
+        bid = recs[c].gid;
+      }
+    return bid;
+  }
+  uint64_t top1 = 0;
+  for (int c = 0; c < nch; ++c) top1 = recs[c].top1 > top1 ? recs[c].top1 : top1;
+  if (P.mode == MODE_GENERAL) return general_sample(row, V, P, top1, sm);
+
+  // gather and sort the candidates
+  const int ncand = nch * NCAND;
+  int n2 = 1;
+  while (n2 < ncand) n2 <<= 1;
+  for (int i = tid; i < n2; i += SB)
+    sm.sortbuf[i] = (i < ncand) ? recs[i / NCAND].cand[i % NCAND] : 0ull;
+  __syncthreads();
+  block_sort_desc(sm.sortbuf, n2);
+  const int nv = min(P.mode == MODE_TOPK_SMALL ? P.K : NCAND, V);
+  const double m = comp_x(sm.sortbuf[0], P.temperature);
+  for (int r = tid; r < nv; r += SB) {
+    sm.xs[r] = comp_x(sm.sortbuf[r], P.temperature);
+    sm.es[r] = exp(sm.xs[r] - m);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int kept = nv;
+    int fallback = 0;
+    if (P.top_p < 1.0f) {
+      double Z = 0.0;
+      if (P.mode == MODE_TOPK_SMALL) {
+        for (int r = 0; r < nv; ++r) Z += sm.es[r];
+      } else {
+        for (int c = 0; c < nch; ++c)
+          if (recs[c].top1 != 0ull) Z += recs[c].z * exp(recs[c].mx - m);
+      }
+      const double pz = (double)P.top_p * Z;
+      double S = 0.0;
+      kept = 0;
+      for (int r = 0; r < nv; ++r) {
+        if (r == 0 || S < pz) {
+          kept = r + 1;
+          S += sm.es[r];
+        } else {
+          break;
+        }
+      }
+      // top-p over the whole vocabulary still open after the top NCAND
+      if (P.mode == MODE_TOPP_FULL && kept == nv && nv < V && S < pz) fallback = 1;
+    }
+    sm.kept = kept;
+    sm.flag = fallback;
+  }
+  __syncthreads();
+  if (sm.flag) return general_sample(row, V, P, top1, sm);
+  const int kept = sm.kept;
+  double bs = 0.0;
+  int bid = -1;
+  for (int r = tid; r < kept; r += SB) {
+    const int tok = comp_token(sm.sortbuf[r]);
+    const double s = sm.xs[r] + gumbel(P, tok);
+    if (better(s, tok, bs, bid)) {
+      bs = s;
+      bid = tok;
+    }
+  }
+  return block_argmax(bs, bid, sm);
+}
+
+// ---------------------------------------------------------------------------
+// row parameters
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ RowParams row_params(int V, uint64_t seed, int64_t step, float temp,
+                                                int32_t top_k, float top_p, uint32_t salt) {
+  RowParams P;
+  P.temperature = temp;
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.salt = salt;
+  P.seed = seed;
+  P.step = step;
+  P.K = (top_k > 0 && top_k < V) ? top_k : V;
+  if (!(temp > 1e-5f))
+    P.mode = MODE_GREEDY;
+  else if (P.K <= NCAND)
+    P.mode = MODE_TOPK_SMALL;
+  else if (P.K == V)
+    P.mode = (top_p < 1.0f) ? MODE_TOPP_FULL : MODE_ALL;
+  else
+    P.mode = MODE_GENERAL;
+  return P;
+}
+
+__device__ __forceinline__ int32_t kind_of(int32_t tok, const int32_t *stop, int n_stop, int32_t lo,
+                                           int32_t hi) {
+  for (int i = 0; i < n_stop; ++i)
+    if (__ldg(stop + i) == tok) return PKV_KIND_STOP;
+  return (tok >= lo && tok < hi) ? PKV_KIND_AUDIO : PKV_KIND_OTHER;
+}
+
+struct SampleArgs {
+  const float *logits;
+  int64_t row_stride;
+  int batch;
+  int vocab;
+  int nch;
+  const int32_t *slots;
+  const int32_t *active;
+  int num_slots;
+  const uint64_t *seeds;
+  int64_t *steps;
+  const float *temperature;
+  const int32_t *top_k;
+  const float *top_p;
+  uint32_t salt;
+  int advance;
+  const int32_t *stop_tokens;
+  int n_stop;
+  int32_t audio_lo, audio_hi;
+  int32_t *out_tok;
+  int32_t *out_kind;
+  ChunkRec *recs;  // [B][nch]
+  int32_t *err;
+};
+
+__global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
+  __shared__ SampSmem sm;
+  const int b = blockIdx.y;
+  const int c = blockIdx.x;
+  if (!a.active[b]) return;
+  const int slot = a.slots[b];
+  if (slot < 0 || slot >= a.num_slots) return;
+  const RowParams P = row_params(a.vocab, a.seeds[slot], a.steps[slot], a.temperature[slot],
+                                 a.top_k[slot], a.top_p[slot], a.salt);
+  chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, c, P, a.recs + (int64_t)b * a.nch + c,
+             sm, a.err);
+}
+
+__global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
+  __shared__ SampSmem sm;
+  const int b = blockIdx.x;
+  if (!a.active[b]) {
+    if (threadIdx.x == 0) {
+      a.out_tok[b] = 0;
+      a.out_kind[b] = PKV_KIND_OTHER;
+    }
+    return;
+  }
+  const int slot = a.slots[b];
+  if (slot < 0 || slot >= a.num_slots) {
+    if (threadIdx.x == 0) {
+      a.out_tok[b] = 0;
+      a.out_kind[b] = PKV_KIND_OTHER;
+      report(a.err, PKV_DEV_ERR_SLOT);
+    }
+    return;
+  }
+  const RowParams P = row_params(a.vocab, a.seeds[slot], a.steps[slot], a.temperature[slot],
+                                 a.top_k[slot], a.top_p[slot], a.salt);
+  const int tok = finish_row(a.logits + (int64_t)b * a.row_stride, a.vocab, a.nch, P,
+                             a.recs + (int64_t)b * a.nch, sm);
+  if (threadIdx.x == 0) {
+    a.out_tok[b] = tok;
+    a.out_kind[b] = kind_of(tok, a.stop_tokens, a.n_stop, a.audio_lo, a.audio_hi);
+    if (a.advance) a.steps[slot] = P.step + 1;
+  }
+}
+
+struct FrameArgs {
+  const float *base;  // [n_cb][B][V]
+  const float *fb;    // [n_cb][V][V] or null
+  int n_cb;
+  int batch;
+  int vocab;
+  int nch;
+  const int32_t *slots;
+  const int32_t *active;
+  int num_slots;
+  const uint64_t *seeds;
+  int64_t *steps;
+  const float *temperature;
+  const int32_t *top_k;
+  const float *top_p;
+  int32_t *out_codes;
+  int32_t *out_kind;
+  ChunkRec *recs;   // [B][nch]
+  float *rows;      // [B][V]
+  int32_t *err;
+};
+
+__global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
+  __shared__ SampSmem sm;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int V = a.vocab;
+  if (!a.active[b]) {
+    for (int j = tid; j < a.n_cb; j += SB) a.out_codes[(int64_t)b * a.n_cb + j] = 0;
+    if (tid == 0) a.out_kind[b] = PKV_KIND_OTHER;
+    return;
+  }
+  const int slot = a.slots[b];
+  if (slot < 0 || slot >= a.num_slots) {
+    for (int j = tid; j < a.n_cb; j += SB) a.out_codes[(int64_t)b * a.n_cb + j] = 0;
+    if (tid == 0) {
+      a.out_kind[b] = PKV_KIND_OTHER;
+      report(a.err, PKV_DEV_ERR_SLOT);
+    }
+    return;
+  }
+  const int64_t step = a.steps[slot];
+  ChunkRec *recs = a.recs + (int64_t)b * a.nch;
+  float *rowbuf = a.rows + (int64_t)b * V;
+  int prev = 0;
+  for (int j = 0; j < a.n_cb; ++j) {
+    const float *row = a.base + ((int64_t)j * a.batch + b) * V;
+    if (j > 0 && a.fb != nullptr) {
+      const float *f = a.fb + ((int64_t)j * V + prev) * V;
+      for (int i = tid; i < V; i += SB) rowbuf[i] = __fadd_rn(row[i], f[i]);
+      __syncthreads();
+      row = rowbuf;
+    }
+    const RowParams P = row_params(V, a.seeds[slot], step, a.temperature[slot], a.top_k[slot],
+                                   a.top_p[slot], (uint32_t)(1 + j));
+    for (int c = 0; c < a.nch; ++c) {
+      chunk_pass(row, V, c, P, recs + c, sm, a.err);
+      __syncthreads();
+    }
+    const int tok = finish_row(row, V, a.nch, P, recs, sm);
+    if (tid == 0) {
+      a.out_codes[(int64_t)b * a.n_cb + j] = tok;
+      sm.token = tok;
+    }
+    __syncthreads();
+    prev = min(max(sm.token, 0), V - 1);
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.out_kind[b] = PKV_KIND_AUDIO;
+    a.steps[slot] = step + 1;
+  }
+}
+
+static int chunks_for(int V) { return (V + CHUNK - 1) / CHUNK; }
+
+}  // namespace pkv
+
+extern "C" size_t pkv_sample_workspace_bytes(int batch, int vocab) {
+  using namespace pkv;
+  if (batch <= 0 || vocab <= 0) return 0;
+  return align_up((size_t)batch * chunks_for(vocab) * sizeof(ChunkRec), 256);
+}
+
+extern "C" size_t pkv_frame_workspace_bytes(int n_codebooks, int batch, int vocab) {
+  using namespace pkv;
+  if (n_codebooks <= 0 || batch <= 0 || vocab <= 0) return 0;
+  return align_up((size_t)batch * chunks_for(vocab) * sizeof(ChunkRec), 256) +
+         align_up((size_t)batch * vocab * sizeof(float), 256);
+}
+
+static int check_sampler_common(int batch, int vocab, const int32_t *slots, const int32_t *active,
+                                int num_slots, const uint64_t *seeds, const int64_t *steps,
+                                const float *temperature, const int32_t *top_k,
+                                const float *top_p) {
+  if (batch <= 0 || vocab <= 0 || num_slots <= 0) return PKV_ERR_INVALID_ARG;
+  if (!slots || !active || !seeds || !steps || !temperature || !top_k || !top_p)
+    return PKV_ERR_INVALID_ARG;
+  if (vocab > pkv::MAX_CHUNKS * pkv::CHUNK) return PKV_ERR_UNSUPPORTED;
+  if (batch > 65535) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+extern "C" int pkv_seeded_sample(const float *logits, int64_t row_stride, int batch, int vocab,
+                                 const int32_t *slots, const int32_t *active, int num_slots,
+                                 const uint64_t *seeds, int64_t *steps, const float *temperature,
+                                 const int32_t *top_k, const float *top_p, uint32_t salt,
+                                 int advance, const int32_t *stop_tokens, int n_stop,
+                                 int32_t audio_lo, int32_t audio_hi, int32_t *out_tok,
+                                 int32_t *out_kind, void *workspace, size_t workspace_bytes,
+                                 int32_t *err_word, void *stream) {
+  using namespace pkv;
+  int st = check_sampler_common(batch, vocab, slots, active, num_slots, seeds, steps, temperature,
+                                top_k, top_p);
+  if (st != PKV_OK) return st;
+  if (!logits || !out_tok || !out_kind || row_stride < vocab || (row_stride & 3) != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (n_stop < 0 || (n_stop > 0 && !stop_tokens)) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(logits)) return PKV_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < pkv_sample_workspace_bytes(batch, vocab))
+    return PKV_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
+  SampleArgs a;
+  a.logits = logits;
+  a.row_stride = row_stride;
+  a.batch = batch;
+  a.vocab = vocab;
+  a.nch = chunks_for(vocab);
+  a.slots = slots;
+  a.active = active;
+  a.num_slots = num_slots;
+  a.seeds = seeds;
+  a.steps = steps;
+  a.temperature = temperature;
+  a.top_k = top_k;
+  a.top_p = top_p;
+  a.salt = salt;
+  a.advance = advance != 0;
+  a.stop_tokens = stop_tokens;
+  a.n_stop = n_stop;
+  a.audio_lo = audio_lo;
+  a.audio_hi = audio_hi;
+  a.out_tok = out_tok;
+  a.out_kind = out_kind;
+  a.recs = static_cast<ChunkRec *>(workspace);
+  a.err = err_word;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  sample_chunk_kernel<<<dim3((unsigned)a.nch, (unsigned)batch), SB, 0, s>>>(a);
+  int rc = launch_status();
+  if (rc != PKV_OK) return rc;
+  sample_finish_kernel<<<(unsigned)batch, SB, 0, s>>>(a);
+  return launch_status();
+}
+
+extern "C" int pkv_codebook_frame_sample(const float *base, const float *fb, int n_codebooks,
+                                         int batch, int vocab, const int32_t *slots,
+                                         const int32_t *active, int num_slots,
+                                         const uint64_t *seeds, int64_t *steps,
+                                         const float *temperature, const int32_t *top_k,
+                                         const float *top_p, int32_t *out_codes,
+                                         int32_t *out_kind, void *workspace,
+                                         size_t workspace_bytes, int32_t *err_word,
+                                         void *stream) {
+  using namespace pkv;
+  int st = check_sampler_common(batch, vocab, slots, active, num_slots, seeds, steps, temperature,
+                                top_k, top_p);
+  if (st != PKV_OK) return st;
+  if (!base || !out_codes || !out_kind || n_codebooks <= 0) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(base) || (fb && !aligned16(fb))) return PKV_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < pkv_frame_workspace_bytes(n_codebooks, batch, vocab))
+    return PKV_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
+  FrameArgs a;
+  a.base = base;
+  a.fb = fb;
+  a.n_cb = n_codebooks;
+  a.batch = batch;
+  a.vocab = vocab;
+  a.nch = chunks_for(vocab);
+  a.slots = slots;
+  a.active = active;
+  a.num_slots = num_slots;
+  a.seeds = seeds;
+  a.steps = steps;
+  a.temperature = temperature;
+  a.top_k = top_k;
+  a.top_p = top_p;
+  a.out_codes = out_codes;
+  a.out_kind = out_kind;
+  a.recs = static_cast<ChunkRec *>(workspace);
+  a.rows = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) +
+                                     align_up((size_t)batch * a.nch * sizeof(ChunkRec), 256));
+  a.err = err_word;
+  frame_kernel<<<(unsigned)batch, SB, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_status();
+}

@@ -1,0 +1,127 @@
+"""One decode step of a workload, driven through the C ABI.
+
+``DecodeStep`` owns the device-side inputs and outputs of one batch (page
+tables, lengths, per-slot sampler state, attention outputs, workspaces) and
+runs the hot path: for every layer kv_append then paged_decode_attn, then
+seeded_sample over the logits, then (frame workloads) one
+codebook_frame_sample.  It only orders calls and allocates buffers with
+torch; all arithmetic happens in libpkv's kernels.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+
+from . import _binding as B
+from .workloads import Batch, Tensors
+
+
+class DecodeStep:
+    def __init__(self, batch: Batch, tensors: Tensors, device="cuda", stop_tokens=None,
+                 audio_lo: int = 0, audio_hi: int = 0, out_fp32: bool = False,
+                 with_lse: bool = True):
+        import torch
+        cfg = batch.cfg
+        self.batch = batch
+        self.cfg = cfg
+        self.t = tensors
+        dev = torch.device(device)
+        self.device = dev
+        i32 = torch.int32
+        self.page_table = torch.as_tensor(batch.page_table, dtype=i32).to(dev)
+        self.seq_lens = torch.as_tensor(batch.seq_lens, dtype=i32).to(dev)
+        self.active = torch.as_tensor(batch.active, dtype=i32).to(dev)
+        self.slots = torch.as_tensor(batch.slots, dtype=i32).to(dev)
+        self.seeds = torch.as_tensor(batch.seeds.view(np.int64)).view(torch.uint64).to(dev)
+        self.steps = torch.as_tensor(batch.steps, dtype=torch.int64).to(dev)
+        self.temperature = torch.as_tensor(batch.temperature).to(dev)
+        self.top_k = torch.as_tensor(batch.top_k).to(dev)
+        self.top_p = torch.as_tensor(batch.top_p).to(dev)
+        self.stop_tokens = (None if not stop_tokens else
+                            torch.as_tensor(np.asarray(stop_tokens, np.int32)).to(dev))
+        self.audio_lo, self.audio_hi = int(audio_lo), int(audio_hi)
+        Bn = batch.B
+        L = tensors.layers
+        odt = torch.float32 if out_fp32 else torch.bfloat16
+        self.out = torch.empty((L, Bn, cfg.num_qo_heads, cfg.head_dim), dtype=odt, device=dev)
+        self.lse = (torch.empty((L, Bn, cfg.num_qo_heads), dtype=torch.float32, device=dev)
+                    if with_lse else None)
+        ws = B.decode_workspace_bytes(Bn, cfg.num_qo_heads, cfg.head_dim, batch.max_pages,
+                                      cfg.page_size)
+        self.attn_ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.out_tok = torch.empty(Bn, dtype=i32, device=dev)
+        self.out_kind = torch.empty(Bn, dtype=i32, device=dev)
+        self.samp_ws = None
+        if tensors.logits is not None:
+            self.samp_ws = torch.empty(B.sample_workspace_bytes(Bn, tensors.logits.shape[1]),
+                                       dtype=torch.uint8, device=dev)
+        self.frame_ws = None
+        if tensors.base is not None:
+            n_cb, _, Vf = tensors.base.shape
+            self.frame_ws = torch.empty(B.frame_workspace_bytes(n_cb, Bn, Vf), dtype=torch.uint8,
+                                        device=dev)
+            self.out_codes = torch.empty((Bn, n_cb), dtype=i32, device=dev)
+            self.frame_kind = torch.empty(Bn, dtype=i32, device=dev)
+        self.err = torch.zeros(1, dtype=i32, device=dev)
+
+    # -- the pieces of the step ------------------------------------------
+    def append(self, layer: int, stream=None):
+        t = self.t
+        B.kv_append(t.cache, layer, t.k[layer], t.v[layer], self.page_table, self.seq_lens,
+                    self.active, err_word=self.err, stream=stream)
+
+    def attend(self, layer: int, stream=None):
+        t = self.t
+        B.paged_decode_attn(t.cache, layer, t.q[layer], self.page_table, self.seq_lens,
+                            self.active, self.out[layer], self.attn_ws,
+                            lse=None if self.lse is None else self.lse[layer],
+                            err_word=self.err, stream=stream)
+
+    def sample(self, advance=True, salt=0, stream=None):
+        B.seeded_sample(self.t.logits, self.slots, self.active, self.seeds, self.steps,
+                        self.temperature, self.top_k, self.top_p, self.out_tok, self.out_kind,
+                        self.samp_ws, salt=salt, advance=advance, stop_tokens=self.stop_tokens,
+                        audio_lo=self.audio_lo, audio_hi=self.audio_hi, err_word=self.err,
+                        stream=stream)
+
+    def frame(self, stream=None):
+        t = self.t
+        B.codebook_frame_sample(t.base, t.fb, self.slots, self.active, self.seeds, self.steps,
+                                self.temperature, self.top_k, self.top_p, self.out_codes,
+                                self.frame_kind, self.frame_ws, err_word=self.err, stream=stream)
+
+    def run(self, stream=None, layers: Optional[range] = None, attn_events=None):
+        """The whole step.  ``attn_events``: optional list that receives one
+        (start, end) CUDA-event pair per paged_decode_attn call, recorded on
+        the launch stream."""
+        import torch
+        L = self.t.layers
+        st = stream if stream is not None else torch.cuda.current_stream()
+        for l in (layers if layers is not None else range(L)):
+            self.append(l, stream=st)
+            if attn_events is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                self.attend(l, stream=st)
+                e1.record(st)
+                attn_events.append((e0, e1))
+            else:
+                self.attend(l, stream=st)
+        if self.t.logits is not None:
+            self.sample(stream=st)
+        if self.t.base is not None:
+            self.frame(stream=st)
+
+    def launches_per_step(self) -> int:
+        """Kernel launches of one run(): append 1, attention 1 or 2 (merge when
+        any row can need more than one split), sampler 2, frame 1."""
+        L = self.t.layers
+        per_attn = 2 if self.batch.max_pages > 32 else 1
+        n = L * (1 + per_attn)
+        if self.t.logits is not None:
+            n += 2
+        if self.t.base is not None:
+            n += 1
+        return n

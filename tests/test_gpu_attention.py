@@ -1,0 +1,158 @@
+"""GPU parity of kv_append and paged_decode_attn against the fp64 oracle, on
+the same seeded inputs (drawn on the CPU, copied to both sides).
+
+Tolerances (bf16 inputs, fp32 accumulation): attention output within
+max-abs 1e-2 and mean-abs 1e-3 of the oracle; lse within 1e-3; the append
+bit-exact on every byte outside the dummy page 0 (which padding rows may
+all write)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_pages_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 1e-3
+
+
+def _cases():
+    C = W.CONFIGS
+    return {
+        "tiny": C["tiny"],
+        "qwen2_small": W.small_variant(C["qwen2_0p5b"], n_active=6, ctx_hi=700, layers=2),
+        "llama3_small": W.small_variant(C["llama3_3b"], n_active=5, ctx_hi=1100, layers=2),
+        "qwen3_frame_small": W.small_variant(C["qwen3_4b_frame"], n_active=4, ctx_hi=1500,
+                                             layers=2),
+        "long_small": W.small_variant(C["long_context"], n_active=3, n_pad=3, ctx_hi=2100,
+                                      layers=2).replace(ctx_lo=1500),
+        # split boundaries: 512 tokens per split, 16 per page
+        "edges_d128": W.Config(name="edges_d128", index=7, num_layers=1, num_qo_heads=8,
+                               num_kv_heads=2, head_dim=128, page_size=16, n_active=9, n_pad=2,
+                               ctx=(1, 15, 16, 17, 511, 512, 513, 528, 1025)),
+        "edges_d64_g7": W.Config(name="edges_d64_g7", index=8, num_layers=1, num_qo_heads=14,
+                                 num_kv_heads=2, head_dim=64, page_size=16, n_active=6, n_pad=1,
+                                 ctx=(1, 16, 33, 512, 513, 800), shuffle_pages=True),
+        "g1_mha": W.Config(name="g1_mha", index=9, num_layers=1, num_qo_heads=4, num_kv_heads=4,
+                           head_dim=128, page_size=16, n_active=3, n_pad=0, ctx=(5, 600, 40)),
+        "g12_two_qblocks": W.Config(name="g12", index=10, num_layers=1, num_qo_heads=24,
+                                    num_kv_heads=2, head_dim=128, page_size=16, n_active=3,
+                                    n_pad=1, ctx=(7, 700, 1200)),
+    }
+
+
+CASES = _cases()
+
+
+def _run(cfg, out_fp32):
+    from paged_kv_decode_pages_gb300.step import DecodeStep
+    batch = W.make_batch(cfg)
+    host = W.Tensors(batch, device="cpu", with_logits=False, with_frame=False)
+    cache_bits = W.bf16_bits(host.cache)
+    dev = W.Tensors.__new__(W.Tensors)
+    dev.cache = host.cache.cuda()
+    dev.q, dev.k, dev.v = host.q.cuda(), host.k.cuda(), host.v.cuda()
+    dev.logits = dev.base = dev.fb = None
+    dev.layers = host.layers
+    step = DecodeStep(batch, dev, out_fp32=out_fp32)
+    step.run()
+    torch.cuda.synchronize()
+    return batch, host, cache_bits, step
+
+
+@pytest.mark.parametrize("out_fp32", [True, False])
+@pytest.mark.parametrize("name", list(CASES))
+def test_append_and_attention_match_oracle(name, out_fp32):
+    cfg = CASES[name]
+    batch, host, cache_bits, step = _run(cfg, out_fp32)
+    assert int(step.err.item()) == 0
+    worst = 0.0
+    for l in range(host.layers):
+        bad = oracle.kv_append(cache_bits, l, W.bf16_bits(host.k[l]), W.bf16_bits(host.v[l]),
+                               batch.page_table, batch.seq_lens, batch.active)
+        assert bad == 0
+        want, want_lse, bad = oracle.paged_decode_attn(cache_bits, l, W.bf16_bits(host.q[l]),
+                                                       batch.page_table, batch.seq_lens,
+                                                       batch.active)
+        assert bad == 0
+        got = step.out[l].float().cpu().numpy().astype(np.float64)
+        err = np.abs(got - want)
+        assert err.max() <= MAX_ABS, (name, l, err.max())
+        assert err.mean() <= MEAN_ABS, (name, l, err.mean())
+        worst = max(worst, float(err.max()))
+        act = batch.active.astype(bool)
+        lse = step.lse[l].cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(lse[act] - want_lse[act]) <= LSE_ABS)
+        assert np.all(np.isneginf(lse[~act]))
+        assert np.all(got[~act] == 0.0)
+    # every byte of the cache outside page 0 equals the oracle's
+    got_cache = W.bf16_bits(step.t.cache)
+    np.testing.assert_array_equal(got_cache[:, 1:], cache_bits[:, 1:])
+    if out_fp32:
+        # fp32 output: far inside the contract (no bf16 rounding of the output)
+        assert worst < 1e-4, worst
+
+
+def test_single_token_and_identical_keys_closed_forms():
+    """n = 1 gives v itself; identical keys give the mean of V."""
+    from paged_kv_decode_pages_gb300.step import DecodeStep
+    cfg = W.Config(name="closed", index=11, num_layers=1, num_qo_heads=8, num_kv_heads=2,
+                   head_dim=128, page_size=16, n_active=2, n_pad=0, ctx=(1, 1000))
+    batch = W.make_batch(cfg)
+    host = W.Tensors(batch, device="cpu", with_logits=False, with_frame=False)
+    # row 1: every key equal to its new key
+    n = int(batch.seq_lens[1])
+    for t in range(n - 1):
+        p = batch.page_table[1, t // 16]
+        host.cache[0, p, 0, t % 16] = host.k[0, 1]
+    dev = W.Tensors.__new__(W.Tensors)
+    dev.cache, dev.q, dev.k, dev.v = host.cache.cuda(), host.q.cuda(), host.k.cuda(), host.v.cuda()
+    dev.logits = dev.base = dev.fb = None
+    dev.layers = 1
+    step = DecodeStep(batch, dev, out_fp32=True)
+    step.run()
+    out = step.out[0].cpu().double()
+    v_new = host.v[0].double()
+    for h in range(8):
+        assert torch.equal(out[0, h], v_new[0, h // 4])
+    # mean of V over row 1 (after the append)
+    vs = []
+    for t in range(n):
+        p = batch.page_table[1, t // 16]
+        vs.append(host.v[0, 1] if t == n - 1 else host.cache[0, p, 1, t % 16])
+    mean_v = torch.stack(vs).double().mean(0)
+    for h in range(8):
+        assert torch.allclose(out[1, h], mean_v[h // 4], atol=2e-5, rtol=0)
+
+
+def test_bad_inputs_set_error_bits_and_spare_other_rows():
+    from paged_kv_decode_pages_gb300.step import DecodeStep
+    cfg = W.Config(name="bad", index=12, num_layers=1, num_qo_heads=8, num_kv_heads=2,
+                   head_dim=64, page_size=16, n_active=4, n_pad=0, ctx=(40, 70, 90, 600))
+    batch = W.make_batch(cfg)
+    host = W.Tensors(batch, device="cpu", with_logits=False, with_frame=False)
+    cache_bits = W.bf16_bits(host.cache)
+    batch.page_table[0, 1] = batch.num_pages + 5        # page id out of range (read side)
+    batch.page_table[1, (70 - 1) // 16] = -7            # page id out of range (append side)
+    batch.seq_lens[2] = batch.max_pages * 16 + 3        # seq_len beyond the page table
+    dev = W.Tensors.__new__(W.Tensors)
+    dev.cache, dev.q, dev.k, dev.v = host.cache.cuda(), host.q.cuda(), host.k.cuda(), host.v.cuda()
+    dev.logits = dev.base = dev.fb = None
+    dev.layers = 1
+    step = DecodeStep(batch, dev, out_fp32=True)
+    step.run()
+    torch.cuda.synchronize()
+    err = int(step.err.item())
+    assert err & 0x1 and err & 0x2  # PKV_DEV_ERR_PAGE, PKV_DEV_ERR_SEQ_LEN
+    # row 3 is valid: exact parity; row 2 (bad length) is zeros
+    oracle.kv_append(cache_bits, 0, W.bf16_bits(host.k[0]), W.bf16_bits(host.v[0]),
+                     batch.page_table, batch.seq_lens, batch.active)
+    want, _, _ = oracle.paged_decode_attn(cache_bits, 0, W.bf16_bits(host.q[0]), batch.page_table,
+                                          batch.seq_lens, batch.active)
+    got = step.out[0].cpu().numpy()
+    assert np.abs(got[3] - want[3]).max() < 1e-4
+    assert np.all(got[2] == 0)
+    # the append wrote nothing for rows 1 (bad page) and 2 (bad length)
+    got_cache = W.bf16_bits(step.t.cache)
+    np.testing.assert_array_equal(got_cache[:, 1:], cache_bits[:, 1:])

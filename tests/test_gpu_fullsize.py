@@ -1,0 +1,102 @@
+"""Full-size parity: each configuration's whole step (every layer's append and
+attention, the sampler, the frame loop) runs at its full size in the launch
+configuration bench.py times; the oracle then recomputes sampled outputs
+one by one (two rows at the first and last layer) from the inputs drawn
+before the step ran, plus every row of the sampler."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_pages_gb300 import workloads as W
+from paged_kv_decode_pages_gb300.step import DecodeStep
+
+pytestmark = pytest.mark.gpu
+
+NEAR = 1e-6
+
+
+def _snapshot(dev, batch, layer, b):
+    """The pre-append pages of row b at `layer`, as a compact one-layer cache
+    whose page 0 is a dummy, with the row's page table remapped to 1..n."""
+    npg = batch.npages(b)
+    pages = torch.as_tensor(batch.page_table[b, :npg].astype(np.int64), device=dev.cache.device)
+    body = dev.cache[layer].index_select(0, pages)
+    compact = torch.zeros((1, npg + 1) + tuple(body.shape[1:]), dtype=body.dtype)
+    compact[0, 1:] = body.cpu()
+    pt = np.zeros((1, npg), np.int32)
+    pt[0] = np.arange(1, npg + 1)
+    return W.bf16_bits(compact), pt
+
+
+@pytest.mark.parametrize("name", ["qwen2_0p5b", "llama3_3b", "qwen3_4b_frame", "long_context"])
+def test_full_size_step_sampled_rows(name):
+    cfg = W.CONFIGS[name]
+    batch = W.make_batch(cfg)
+    dev = W.Tensors(batch, device="cuda")
+    L = cfg.num_layers
+    rows = [0, cfg.n_active - 1]
+    layers = [0, L - 1]
+    snaps = {(l, b): _snapshot(dev, batch, l, b) for l in layers for b in rows}
+    logits = dev.logits.cpu().numpy()
+    base = None if dev.base is None else dev.base.cpu().numpy()
+    fb = None if dev.fb is None else dev.fb.cpu().numpy()
+    qkv = {(l, b): (W.bf16_bits(dev.q[l, b:b + 1]), W.bf16_bits(dev.k[l, b:b + 1]),
+                    W.bf16_bits(dev.v[l, b:b + 1])) for l in layers for b in rows}
+    steps0 = batch.steps.copy()
+
+    step = DecodeStep(batch, dev)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.err.item()) == 0
+
+    worst = 0.0
+    for (l, b), (cbits, pt) in snaps.items():
+        q, k, v = qkv[(l, b)]
+        sl = batch.seq_lens[b:b + 1]
+        one = np.ones(1, np.int32)
+        assert oracle.kv_append(cbits, 0, k, v, pt, sl, one) == 0
+        want, want_lse, bad = oracle.paged_decode_attn(cbits, 0, q, pt, sl, one)
+        assert bad == 0
+        got = step.out[l, b].float().cpu().numpy().astype(np.float64)
+        err = np.abs(got - want[0])
+        assert err.max() <= 1e-2 and err.mean() <= 1e-3, (name, l, b, err.max(), err.mean())
+        worst = max(worst, float(err.max()))
+        lse = step.lse[l, b].cpu().numpy().astype(np.float64)
+        assert np.abs(lse - want_lse[0]).max() <= 1e-3
+        # the appended slot holds exactly the new k, v
+        n = int(batch.seq_lens[b])
+        page = int(batch.page_table[b, (n - 1) // 16])
+        slot_kv = W.bf16_bits(step.t.cache[l, page, :, (n - 1) % 16])
+        np.testing.assert_array_equal(slot_kv[0], k[0])
+        np.testing.assert_array_equal(slot_kv[1], v[0])
+    # padding rows: zeros
+    pad = batch.active == 0
+    if pad.any():
+        assert torch.all(step.out[:, torch.from_numpy(pad)] == 0)
+
+    # sampler: every row
+    s_steps = steps0.copy()
+    tok, kind, info, bad = oracle.seeded_sample(logits, batch.slots, batch.active, batch.seeds,
+                                                s_steps, batch.temperature, batch.top_k,
+                                                batch.top_p)
+    got_tok = step.out_tok.cpu().numpy()
+    near = (info["top2_gap_rel"] < NEAR) | (info["member_margin"] < NEAR)
+    assert not np.any((got_tok != tok) & ~near), np.nonzero(got_tok != tok)
+    print(name, "sampler near-ties:", int(near.sum()), "attn worst max-abs:", worst)
+
+    if base is not None:
+        f_steps = s_steps.copy()
+        codes, fkind, finfo, bad = oracle.codebook_frame_sample(
+            base, fb, batch.slots, batch.active, batch.seeds, f_steps, batch.temperature,
+            batch.top_k, batch.top_p)
+        got = step.out_codes.cpu().numpy()
+        for r in range(got.shape[0]):
+            for j in range(got.shape[1]):
+                if got[r, j] != codes[r, j]:
+                    assert (finfo[r, j]["top2_gap_rel"] < NEAR
+                            or finfo[r, j]["member_margin"] < NEAR), (r, j)
+                    break
+        np.testing.assert_array_equal(step.steps.cpu().numpy(), f_steps)
+    else:
+        np.testing.assert_array_equal(step.steps.cpu().numpy(), s_steps)
