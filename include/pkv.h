@@ -27,7 +27,7 @@
  *  - Page 0 and slot 0 are reserved for padding entries; no request may own
  *    them.  Slots of the active rows of one call must be distinct.
  *  - Tensors are C-contiguous unless a stride argument says otherwise.
- *    Device pointers to bf16 / fp32 data must be 16-byte aligned.
+ *    The cache, k, v and q must be 16-byte aligned; fp32 logits 4-byte.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -176,8 +176,8 @@ size_t pkv_sample_workspace_bytes(int batch, int vocab);
  *   - advance != 0: steps[s] += 1 after sampling.
  * Padding rows: out_tok = 0, out_kind = OTHER, no state touched.
  *
- *   logits       fp32, row b at logits + b * row_stride (row_stride >= vocab,
- *                a multiple of 4).
+ *   logits       fp32, row b at logits + b * row_stride (row_stride >= vocab;
+ *                4-byte aligned).
  *   slots        int32 [batch]; active int32 [batch].
  *   seeds        uint64 [num_slots]; steps int64 [num_slots] (read, and
  *                written when advance); temperature fp32, top_k int32,

@@ -88,38 +88,81 @@ _F = ctypes.c_float
 _D = ctypes.c_double
 
 
+class using_library:
+    """Context manager: route every oracle call through another build of
+    pkv_oracle.c (the mutation tests plant mistakes in a copy)."""
+
+    def __init__(self, path):
+        self.path = path
+        self.saved = None
+
+    def __enter__(self):
+        global _lib
+        with _lock:
+            self.saved = _lib
+            _lib = _load(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self.saved
+        return False
+
+
+def compile_variant(src_text: str, out_path: str) -> None:
+    """Compile a modified copy of the oracle source (used by the mutation
+    tests only)."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(src_text)
+    cc = os.environ.get("CC", "gcc")
+    r = subprocess.run([cc, "-O1", "-std=c11", "-shared", "-fPIC", src, "-o", out_path, "-lm"],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr)
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
-            path = build()
-            L = ctypes.CDLL(path)
-            L.pkvo_num_threads.restype = _I
-            L.pkvo_set_num_threads.argtypes = [_I]
-            L.pkvo_kv_append.restype = _I
-            L.pkvo_kv_append.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _I]
-            L.pkvo_paged_decode_attn.restype = _I
-            L.pkvo_paged_decode_attn.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _I, _D,
-                                                 _P, _I, _P, _P, _I, _P, _P]
-            L.pkvo_philox4x64_10.argtypes = [_P, _P, _P]
-            L.pkvo_uniform.restype = _D
-            L.pkvo_uniform.argtypes = [_U64, _U32, _I64, _I64]
-            L.pkvo_gumbel.restype = _D
-            L.pkvo_gumbel.argtypes = [_U64, _U32, _I64, _I64]
-            L.pkvo_sample_row.restype = ctypes.c_int32
-            L.pkvo_sample_row.argtypes = [_P, _I, _U64, _I64, _U32, _F, ctypes.c_int32, _F,
-                                          ctypes.POINTER(SampleInfo)]
-            L.pkvo_token_kind.restype = ctypes.c_int32
-            L.pkvo_token_kind.argtypes = [ctypes.c_int32, _P, _I, ctypes.c_int32, ctypes.c_int32]
-            L.pkvo_seeded_sample.restype = _I
-            L.pkvo_seeded_sample.argtypes = [_P, _I64, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P,
-                                             _U32, _I, _P, _I, ctypes.c_int32, ctypes.c_int32,
-                                             _P, _P, _P]
-            L.pkvo_codebook_frame_sample.restype = _I
-            L.pkvo_codebook_frame_sample.argtypes = [_P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
-                                                     _P, _P, _P, _P, _P, _P]
-            _lib = L
+            _lib = _load(build())
     return _lib
+
+
+def _load(path):
+    L = ctypes.CDLL(path)
+    L.pkvo_num_threads.restype = _I
+    L.pkvo_set_num_threads.argtypes = [_I]
+    L.pkvo_kv_append.restype = _I
+    L.pkvo_kv_append.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _I]
+    L.pkvo_paged_decode_attn.restype = _I
+    L.pkvo_paged_decode_attn.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _I, _D,
+                                         _P, _I, _P, _P, _I, _P, _P]
+    L.pkvo_philox4x64_10.argtypes = [_P, _P, _P]
+    L.pkvo_uniform.restype = _D
+    L.pkvo_uniform.argtypes = [_U64, _U32, _I64, _I64]
+    L.pkvo_gumbel.restype = _D
+    L.pkvo_gumbel.argtypes = [_U64, _U32, _I64, _I64]
+    L.pkvo_sample_row.restype = ctypes.c_int32
+    L.pkvo_sample_row.argtypes = [_P, _I, _U64, _I64, _U32, _F, ctypes.c_int32, _F,
+                                  ctypes.POINTER(SampleInfo)]
+    L.pkvo_token_kind.restype = ctypes.c_int32
+    L.pkvo_token_kind.argtypes = [ctypes.c_int32, _P, _I, ctypes.c_int32, ctypes.c_int32]
+    L.pkvo_seeded_sample.restype = _I
+    L.pkvo_seeded_sample.argtypes = [_P, _I64, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P,
+                                     _U32, _I, _P, _I, ctypes.c_int32, ctypes.c_int32,
+                                     _P, _P, _P]
+    L.pkvo_codebook_frame_sample.restype = _I
+    L.pkvo_codebook_frame_sample.argtypes = [_P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
+                                             _P, _P, _P, _P, _P, _P]
+    return L
 
 
 def _ptr(a):

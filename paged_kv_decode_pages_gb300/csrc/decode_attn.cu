@@ -4,26 +4,36 @@
 // [num_layers, num_pages, 2, page_size, num_kv_heads, head_dim].
 //
 // Design (HBM-bound; CUDA cores, no tensor cores):
-//  * split-KV: a row's pages are cut into fixed 32-page (512-token) splits;
-//    one CTA per (kv head, q-head block, split, row).  The split size does
+//  * work units: a row's pages are cut into fixed 32-page (512-token) splits;
+//    a unit is one (row, split, kv head, q-head block).  The split size does
 //    not depend on the batch, so a row's result depends on its inputs only.
-//  * each of the CTA's 4 warps streams its own pages (round-robin) through
-//    its own ring of NS shared-memory stages; a stage is one page of one kv
-//    head: 16 K rows + 16 V rows, each row head_dim bf16 contiguous in HBM,
-//    brought in by 32 bulk async copies (cp.async.bulk, the TMA engine) that
-//    complete on the stage's mbarrier.  Waits are bounded.
-//  * GQA sharing: the warp holds the q of all the group's heads in
-//    registers, so every K / V element is read from shared memory and
-//    converted once and used for every head of the group.
-//  * lanes: 8 lanes share one token, each lane owns head_dim/8 dims, read as
-//    16-byte vectors (conflict-free); q.k partial sums are summed over the
-//    8 lanes with 3 xor-shuffles; the online softmax runs in the log2
-//    domain with a lazy maximum (rescale only when a score exceeds the
-//    running maximum by more than 8).
-//  * the 4 groups x 4 warps of a CTA merge through shared memory; a row with
-//    one split writes its output directly, longer rows write (m, l, o)
-//    partials that a merge kernel folds in split order.
+//  * a one-CTA planner lists the splits of the active rows (prefix sums over
+//    the rows), zeroes the outputs of padding rows and resets the scheduling
+//    counter and the merge tickets, so the launch shapes stay static.
+//  * a persistent grid (SMs x resident CTAs) pulls units from an atomic
+//    counter.  Each of a CTA's 4 warps streams its pages of the unit
+//    (round-robin) through its own ring of NS shared-memory stages; a stage
+//    is one page of one kv head -- 16 K rows + 16 V rows, each head_dim bf16
+//    contiguous in HBM -- brought in by 32 bulk async copies (cp.async.bulk,
+//    the TMA engine) completing on the stage's mbarrier.  The ring runs on
+//    into the next unit, so its pages are in flight while the current unit
+//    is merged.  Waits are bounded.
+//  * GQA sharing: a warp holds the q of all the group's heads in registers,
+//    so every K / V element is read from shared memory and converted once
+//    and used for every head of the group.
+//  * lanes: 8 lanes share a token, each lane owns head_dim/8 dims read as
+//    16-byte vectors (conflict-free); q.k partial sums are summed over the 8
+//    lanes with 3 xor-shuffles; the online softmax runs in the log2 domain
+//    with a lazy maximum (rescale only when a score beats the running
+//    maximum by more than 8).
+//  * per unit, the 4 lane groups of a warp merge with shuffles, the 4 warps
+//    through shared memory; a one-split row writes its output directly,
+//    longer rows write (m, l, o) partials and the CTA that completes a row's
+//    last split (an atomic ticket) folds them in split order.
 #include <math.h>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "pkv_device.cuh"
 #include "pkv_host.h"
@@ -31,12 +41,21 @@
 namespace pkv {
 
 constexpr int ATTN_WARPS = 4;
+constexpr int ATTN_THREADS = ATTN_WARPS * 32;
 constexpr int ATTN_PAGES_PER_SPLIT = 32;
 constexpr int ATTN_PAGE = 16;
 constexpr float ATTN_TAU = 8.0f;       // lazy-rescale threshold (log2 units)
 constexpr float ATTN_NEG = -1.0e30f;   // "no score yet" (finite: keeps 2^(s-m) at 0)
 constexpr float LN2 = 0.69314718055994530942f;
 constexpr float LOG2E = 1.44269504088896340736f;
+constexpr int PLAN_THREADS = 1024;
+
+struct PlanHeader {
+  int32_t counter;      // next unit to hand out
+  int32_t total_units;
+  int32_t total_splits;
+  int32_t pad_;
+};
 
 struct AttnArgs {
   const unsigned char *cache;  // byte address of the cache
@@ -46,10 +65,13 @@ struct AttnArgs {
   int64_t tok_stride;          // bytes
   int num_pages;
   int num_kv_heads;
+  int head_dim;
+  int layer;
   const uint16_t *q;           // [B][Hq][D] bf16 bits
   int num_qo_heads;
   int group;                   // Hq / Hkv
   int qblocks;                 // q-head blocks per kv head
+  int gp;                      // q heads per block
   float qscale;                // sm_scale * log2(e)
   const int32_t *page_table;
   int max_pages;
@@ -61,11 +83,13 @@ struct AttnArgs {
   float *lse;
   float *ws_o;                 // [B][Hq][nsplit_max][D]
   float2 *ws_ml;               // [B][Hq][nsplit_max]
+  int32_t *row_start;          // [B + 1] first split of each row
+  int32_t *tickets;            // [B][Hkv * qblocks]
+  PlanHeader *plan;
   int nsplit_max;
   int32_t *err;
 };
 
-template <int D>
 __device__ __forceinline__ void store_out(const AttnArgs &a, int64_t idx, float v) {
   if (a.out_fp32)
     static_cast<float *>(a.out)[idx] = v;
@@ -73,6 +97,74 @@ __device__ __forceinline__ void store_out(const AttnArgs &a, int64_t idx, float 
     static_cast<uint16_t *>(a.out)[idx] = (uint16_t)f32_to_bf16_bits(v);
 }
 
+__device__ __forceinline__ int row_splits(const AttnArgs &a, int b, bool *bad) {
+  *bad = false;
+  if (!a.active[b]) return 0;
+  const int n = a.seq_lens[b];
+  if (n < 1 || (int64_t)n > (int64_t)a.max_pages * ATTN_PAGE) {
+    *bad = true;
+    return 0;
+  }
+  const int npages = (n + ATTN_PAGE - 1) / ATTN_PAGE;
+  return (npages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT;
+}
+
+// ---------------------------------------------------------------------------
+// planner: one CTA
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(PLAN_THREADS) attn_plan_kernel(const AttnArgs a) {
+  __shared__ int32_t scan[PLAN_THREADS];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x;
+  const int D = a.head_dim;
+  const int HB = a.num_kv_heads * a.qblocks;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < a.batch; base += PLAN_THREADS) {
+    const int b = base + tid;
+    int ns = 0;
+    if (b < a.batch) {
+      bool bad;
+      ns = row_splits(a, b, &bad);
+      if (bad) report(a.err, PKV_DEV_ERR_SEQ_LEN);
+      for (int i = 0; i < HB; ++i) a.tickets[(int64_t)b * HB + i] = 0;
+    }
+    // inclusive scan of ns over the block (Hillis-Steele)
+    scan[tid] = ns;
+    __syncthreads();
+    for (int off = 1; off < PLAN_THREADS; off <<= 1) {
+      const int v = tid >= off ? scan[tid - off] : 0;
+      __syncthreads();
+      scan[tid] += v;
+      __syncthreads();
+    }
+    if (b < a.batch) a.row_start[b] = carry + scan[tid] - ns;
+    __syncthreads();
+    if (tid == PLAN_THREADS - 1) carry += scan[tid];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.row_start[a.batch] = carry;
+    a.plan->counter = 0;
+    a.plan->total_splits = carry;
+    a.plan->total_units = carry * HB;
+  }
+  __syncthreads();
+  // padding or rejected rows (no split): zeros, lse = -inf; one warp per row
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int b = warp; b < a.batch; b += PLAN_THREADS / 32) {
+    if (a.row_start[b + 1] != a.row_start[b]) continue;
+    const int64_t base = (int64_t)b * a.num_qo_heads * D;
+    for (int i = lane; i < a.num_qo_heads * D; i += 32) store_out(a, base + i, 0.0f);
+    if (a.lse != nullptr)
+      for (int h = lane; h < a.num_qo_heads; h += 32)
+        a.lse[(int64_t)b * a.num_qo_heads + h] = -INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the persistent attention kernel
+// ---------------------------------------------------------------------------
 template <int D, int GP, int NS>
 struct AttnShape {
   static constexpr int T = 8 / GP;              // tokens per lane group per batch
@@ -83,321 +175,482 @@ struct AttnShape {
   static constexpr int ROW_BYTES = D * 2;
   static constexpr int STAGE_BYTES = 2 * ATTN_PAGE * ROW_BYTES;
   static constexpr int RING_BYTES = ATTN_WARPS * NS * STAGE_BYTES;
-  static constexpr int RED_BYTES = ATTN_WARPS * 4 * GP * (D * 4 + 8);
-  static constexpr int DATA_BYTES = RING_BYTES > RED_BYTES ? RING_BYTES : RED_BYTES;
-  static constexpr int SMEM_BYTES = DATA_BYTES + ATTN_WARPS * NS * 8;
+  static constexpr int RED_O_BYTES = ATTN_WARPS * GP * D * 4;
+  static constexpr int RED_ML_BYTES = ATTN_WARPS * GP * 8;
+  static constexpr int QBUF_BYTES = 2 * GP * D * 2;         // q of cur and next unit (bf16)
+  static constexpr int BAR_BYTES = ATTN_WARPS * NS * 8 + 2 * 8;
+  static constexpr int SMEM_BYTES =
+      RING_BYTES + RED_O_BYTES + RED_ML_BYTES + QBUF_BYTES + BAR_BYTES + 128;
   static_assert(GP == 2 || GP == 4 || GP == 8, "GP");
   static_assert(D == 64 || D == 128, "D");
 };
 
+struct Unit {
+  int valid;
+  int b, split, g, qb, h0, nh;
+  int n, p_begin, p_count, nsplit;
+};
+
+constexpr int ATTN_SMEM_ROWS = 512;  // rows whose split table lives in shared memory
+
+// rs: first split of each row [B + 1]; seq: lengths [B] (shared or global)
+__device__ __forceinline__ Unit decode_unit(const AttnArgs &a, int u, int gp, int total_units,
+                                            const int32_t *rs, const int32_t *seq) {
+  Unit U;
+  const int HB = a.num_kv_heads * a.qblocks;
+  U.valid = u < total_units;
+  U.b = U.split = U.g = U.qb = U.h0 = U.nh = U.n = U.p_begin = U.p_count = U.nsplit = 0;
+  if (!U.valid) return U;
+  const int su = u / HB, hb = u % HB;
+  // row of split `su`: the last b with rs[b] <= su
+  int lo = 0, hi = a.batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (rs[mid] <= su)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  U.b = lo;
+  U.split = su - rs[lo];
+  U.g = hb / a.qblocks;
+  U.qb = hb % a.qblocks;
+  U.h0 = U.g * a.group + U.qb * gp;
+  U.nh = min(gp, a.group - U.qb * gp);
+  U.n = seq[U.b];
+  const int npages = (U.n + ATTN_PAGE - 1) / ATTN_PAGE;
+  U.nsplit = (npages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT;
+  U.p_begin = U.split * ATTN_PAGES_PER_SPLIT;
+  U.p_count = min(npages - U.p_begin, ATTN_PAGES_PER_SPLIT);
+  return U;
+}
+
+__device__ __forceinline__ int warp_pages(const Unit &U, int warp) {
+  if (!U.valid || U.p_count <= warp) return 0;
+  return (U.p_count - warp + ATTN_WARPS - 1) / ATTN_WARPS;
+}
+
+// barrier 1 over the CTA's 128 threads (barrier 0 stays __syncthreads)
+__device__ __forceinline__ void named_barrier_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(ATTN_THREADS) : "memory");
+}
+
 template <int D, int GP, int NS>
-__global__ void __launch_bounds__(ATTN_WARPS * 32, 2) attn_split_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(ATTN_THREADS, 2)
+    attn_persistent_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap) {
   using S = AttnShape<D, GP, NS>;
   constexpr int T = S::T, DPL = S::DPL, NCH = S::NCH;
+  constexpr int NP = DPL / 2;  // fp32 pairs per lane per row
 
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::DATA_BYTES);
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // stage buffers start on a 128-byte boundary
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  float *red_o = reinterpret_cast<float *>(smem + S::RING_BYTES);                      // [4][GP][D]
+  float2 *red_ml = reinterpret_cast<float2 *>(smem + S::RING_BYTES + S::RED_O_BYTES);  // [4][GP]
+  uint16_t *qbuf = reinterpret_cast<uint16_t *>(smem + S::RING_BYTES + S::RED_O_BYTES +
+                                                S::RED_ML_BYTES);                    // [2][GP][D]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::RING_BYTES + S::RED_O_BYTES +
+                                                S::RED_ML_BYTES + S::QBUF_BYTES);
+  uint64_t *qbars = bars + ATTN_WARPS * NS;  // [2]
+  __shared__ int32_t s_unit[4];  // unit ids, circular: ordinal k at [k & 3]
+  __shared__ int32_t s_last;
+  __shared__ int32_t s_rs[ATTN_SMEM_ROWS + 1];
+  __shared__ int32_t s_seq[ATTN_SMEM_ROWS];
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
   const int grp = lane >> 3;
   const int li = lane & 7;
-
-  const int b = blockIdx.z;
-  const int split = blockIdx.y;
-  const int g = blockIdx.x / a.qblocks;
-  const int qb = blockIdx.x % a.qblocks;
-  const int h0 = g * a.group + qb * GP;
-  const int nh = min(GP, a.group - qb * GP);
+  const int gbase = lane & 24;  // first lane of the lane group
+  const int h_own = li / T;     // after the reduce-scatter, lane li holds value
+  const int tt_own = li % T;    // li = (head h_own, token tt_own) of its group
   const int Hq = a.num_qo_heads;
-
-  const bool act = a.active[b] != 0;
-  const int n = act ? a.seq_lens[b] : 0;
-  const bool bad_len = act && (n < 1 || (int64_t)n > (int64_t)a.max_pages * ATTN_PAGE);
-  if (!act || bad_len) {
-    // padding (or rejected) row: zeros, lse = -inf, written once by split 0
-    if (split == 0) {
-      for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
-        store_out<D>(a, ((int64_t)b * Hq + h0 + i / D) * D + i % D, 0.0f);
-      if (a.lse != nullptr && threadIdx.x < nh) a.lse[(int64_t)b * Hq + h0 + threadIdx.x] = -INFINITY;
-      if (bad_len && threadIdx.x == 0 && blockIdx.x == 0) report(a.err, PKV_DEV_ERR_SEQ_LEN);
-    }
-    return;
-  }
-  const int npages = (n + ATTN_PAGE - 1) / ATTN_PAGE;
-  const int nsplit = (npages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT;
-  if (split >= nsplit) return;
-  const int p_begin = split * ATTN_PAGES_PER_SPLIT;
-  const int p_count = min(npages - p_begin, ATTN_PAGES_PER_SPLIT);
-  const int my_count = p_count > warp ? (p_count - warp + ATTN_WARPS - 1) / ATTN_WARPS : 0;
 
   unsigned char *ring = smem + warp * NS * S::STAGE_BYTES;
   uint64_t *wbars = bars + warp * NS;
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&wbars[s], 1);
+    if (warp == 0) {
+      mbar_init(&qbars[0], 1);
+      mbar_init(&qbars[1], 1);
+    }
     fence_barrier_init();
   }
-  __syncwarp();
+  if (tid == 0) {
+    s_unit[0] = atomicAdd(&a.plan->counter, 1);
+    s_unit[1] = atomicAdd(&a.plan->counter, 1);
+  }
+  // the split table of the batch, in shared memory when it fits
+  const bool small_batch = a.batch <= ATTN_SMEM_ROWS;
+  if (small_batch) {
+    for (int b = tid; b <= a.batch; b += ATTN_THREADS) s_rs[b] = a.row_start[b];
+    for (int b = tid; b < a.batch; b += ATTN_THREADS) s_seq[b] = a.seq_lens[b];
+  }
+  const int total_units = a.plan->total_units;
+  __syncthreads();
+  const int32_t *rs = small_batch ? s_rs : a.row_start;
+  const int32_t *seq = small_batch ? s_seq : a.seq_lens;
+  const uint64_t policy = l2_evict_first_policy();
+  const int layer_page0 = a.layer * a.num_pages;
 
-  // q of the lane's dims for every head of the block, pre-scaled to log2 units
-  float qf[GP][DPL];
-#pragma unroll
-  for (int h = 0; h < GP; ++h) {
-    if (h < nh) {
-      const uint4 *qr = reinterpret_cast<const uint4 *>(a.q + ((int64_t)b * Hq + h0 + h) * D);
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float f[8];
-        unpack8(__ldg(qr + li + 8 * c), f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qf[h][8 * c + e] = f[e] * a.qscale;
+  int ordinal = 0;
+  Unit cur = decode_unit(a, s_unit[0], GP, total_units, rs, seq);
+  Unit nxt = decode_unit(a, s_unit[1], GP, total_units, rs, seq);
+  int cur_cnt = warp_pages(cur, warp);
+  int nxt_cnt = warp_pages(nxt, warp);
+
+  // page ids of the warp's pages of a unit: lane i holds the i-th
+  auto load_pids = [&](const Unit &U, int cnt) -> int {
+    int pid = 0;
+    if (lane < cnt) {
+      pid = __ldg(a.page_table + (int64_t)U.b * a.max_pages + U.p_begin + warp + lane * ATTN_WARPS);
+      if (pid < 0 || pid >= a.num_pages) {
+        report(a.err, PKV_DEV_ERR_PAGE);
+        pid = 0;
       }
-    } else {
-#pragma unroll
-      for (int d = 0; d < DPL; ++d) qf[h][d] = 0.0f;
     }
-  }
-
-  const unsigned char *head_base =
-      a.cache + a.layer_off + (int64_t)g * S::ROW_BYTES;
-  const int32_t *pt_row = a.page_table + (int64_t)b * a.max_pages;
-
-  // issue the 32 row copies of the warp's i-th page into ring slot `slot`
-  auto issue = [&](int i, int slot) {
-    const int pi = p_begin + warp + i * ATTN_WARPS;
-    int pid = __ldg(pt_row + pi);
-    if (pid < 0 || pid >= a.num_pages) {
-      if (lane == 0) report(a.err, PKV_DEV_ERR_PAGE);
-      pid = 0;
-    }
-    uint64_t *bar = &wbars[slot];
-    if (lane == 0) mbar_arrive_expect_tx(bar, S::STAGE_BYTES);
-    __syncwarp();
-    const int kv = lane >> 4;      // lanes 0-15: K rows, 16-31: V rows
-    const int t = lane & 15;
-    const unsigned char *src = head_base + (int64_t)pid * a.page_stride + kv * a.kv_stride +
-                               (int64_t)t * a.tok_stride;
-    unsigned char *dst = ring + slot * S::STAGE_BYTES + (kv * ATTN_PAGE + t) * S::ROW_BYTES;
-    bulk_copy_g2s(dst, src, S::ROW_BYTES, bar);
+    return pid;
   };
+  int pid_cur = load_pids(cur, cur_cnt);
+  int pid_nxt = load_pids(nxt, nxt_cnt);
 
-  float o[GP][DPL];
-  float m[GP], l[GP];
-#pragma unroll
-  for (int h = 0; h < GP; ++h) {
-    m[h] = ATTN_NEG;
-    l[h] = 0.0f;
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) o[h][d] = 0.0f;
-  }
+  // q rows of a unit's heads (contiguous in HBM) into q buffer `buf`
+  auto stage_q = [&](const Unit &U, int buf) {
+    if (tid == 0 && U.valid) {
+      fence_proxy_async_smem();
+      const uint32_t bytes = (uint32_t)(U.nh * D * 2);
+      mbar_arrive_expect_tx(&qbars[buf], bytes);
+      bulk_copy_g2s(qbuf + buf * GP * D, a.q + ((int64_t)U.b * Hq + U.h0) * D, bytes, &qbars[buf]);
+    }
+  };
+  stage_q(cur, 0);
+  stage_q(nxt, 1);
 
-  const int prologue = my_count < NS ? my_count : NS;
-  for (int i = 0; i < prologue; ++i) issue(i, i);
+  // issue pointer: which of (cur, nxt) and which of the warp's pages of it
+  int iss_u = 0, iss_i = 0;
+  int issued = 0, consumed = 0;
+  bool dead = false;  // a bounded wait gave up: stop streaming, keep the barriers
 
-  bool timed_out = false;
-  int consumed = 0;
-  for (int i = 0; i < my_count; ++i) {
-    const int slot = i % NS;
-    // the give-up decision must be warp-uniform: the shuffles below need all lanes
-    const bool landed = mbar_wait(&wbars[slot], (uint32_t)((i / NS) & 1));
-    if (!__all_sync(FULL_MASK, landed)) {
-      timed_out = true;
+  // one tensor TMA brings the page's 16 K rows and 16 V rows of kv head g
+  auto issue_one = [&](const Unit &U, int pids, int i) {
+    const int pid = __shfl_sync(FULL_MASK, pids, i);
+    if (lane == 0) {
+      const int slot = issued % NS;
+      uint64_t *bar = &wbars[slot];
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, S::STAGE_BYTES);
+      tma_load_5d(ring + slot * S::STAGE_BYTES, &tmap, 0, U.g, 0, 0, layer_page0 + pid, bar,
+                  policy);
+    }
+    ++issued;
+  };
+  auto top_up = [&]() {
+    if (dead) return;
+    while (issued - consumed < NS) {
+      if (iss_u == 0) {
+        if (iss_i < cur_cnt) {
+          issue_one(cur, pid_cur, iss_i++);
+          continue;
+        }
+        iss_u = 1;
+        iss_i = 0;
+      }
+      if (iss_i < nxt_cnt) {
+        issue_one(nxt, pid_nxt, iss_i++);
+        continue;
+      }
       break;
     }
-    consumed = i + 1;
-    const unsigned char *kst = ring + slot * S::STAGE_BYTES;
-    const unsigned char *vst = kst + ATTN_PAGE * S::ROW_BYTES;
-    const int tok0 = (p_begin + warp + i * ATTN_WARPS) * ATTN_PAGE;
-    const bool ragged = tok0 + ATTN_PAGE > n;
+  };
+
+  f32x2 q2[GP][NP];
+  f32x2 o2[GP][NP];
+  float m_all[GP];  // running maximum per head (log2 units), shared by the lane group
+  float m_own, l_own;
+
+  while (cur.valid) {
+    top_up();
+    // q of the lane's dims for every head of the block, pre-scaled to log2 units
+    const int qb_idx = ordinal & 1;
+    if (!mbar_wait(&qbars[qb_idx], (uint32_t)((ordinal >> 1) & 1)) && lane == 0)
+      report(a.err, PKV_DEV_ERR_TIMEOUT);
+    const uint16_t *qsrc = qbuf + qb_idx * GP * D;
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      m_all[h] = ATTN_NEG;
+#pragma unroll
+      for (int j = 0; j < NP; ++j) o2[h][j] = 0ull;
+      if (h < cur.nh) {
+        const uint4 *qr = reinterpret_cast<const uint4 *>(qsrc + h * D);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          float f[8];
+          unpack8(qr[li + 8 * c], f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            q2[h][4 * c + e] = pack2(f[2 * e] * a.qscale, f[2 * e + 1] * a.qscale);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NP; ++j) q2[h][j] = 0ull;
+      }
+    }
+    m_own = ATTN_NEG;
+    l_own = 0.0f;
+    const int n = cur.n;
+
+    for (int i = 0; i < cur_cnt && !dead; ++i) {
+      const int slot = consumed % NS;
+      const bool landed = mbar_wait(&wbars[slot], (uint32_t)((consumed / NS) & 1));
+      if (!__all_sync(FULL_MASK, landed)) {  // warp-uniform give-up
+        dead = true;
+        if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
+        break;
+      }
+      const unsigned char *kst = ring + slot * S::STAGE_BYTES;
+      const unsigned char *vst = kst + ATTN_PAGE * S::ROW_BYTES;
+      const int tok0 = (cur.p_begin + warp + i * ATTN_WARPS) * ATTN_PAGE;
+      const bool ragged = tok0 + ATTN_PAGE > n;
 
 #pragma unroll
-    for (int bt = 0; bt < S::BATCHES; ++bt) {
-      const int tb = bt * S::TOK_PER_BATCH + grp * T;  // first token of this lane group
-      float s[GP][T];
-#pragma unroll
-      for (int tt = 0; tt < T; ++tt) {
-        const uint4 *kr = reinterpret_cast<const uint4 *>(kst + (tb + tt) * S::ROW_BYTES);
-        float kf[DPL];
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) unpack8(kr[li + 8 * c], kf + 8 * c);
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-          float acc = 0.0f;
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) acc = fmaf(qf[h][d], kf[d], acc);
-          s[h][tt] = acc;
-        }
-      }
-      // sum the partial dot products over the 8 lanes of the group
-#pragma unroll
-      for (int off = 1; off < 8; off <<= 1) {
-#pragma unroll
-        for (int h = 0; h < GP; ++h)
-#pragma unroll
-          for (int tt = 0; tt < T; ++tt) s[h][tt] += __shfl_xor_sync(FULL_MASK, s[h][tt], off);
-      }
-      if (ragged) {
-#pragma unroll
-        for (int tt = 0; tt < T; ++tt)
-          if (tok0 + tb + tt >= n) {
-#pragma unroll
-            for (int h = 0; h < GP; ++h) s[h][tt] = -INFINITY;
-          }
-      }
-      // online softmax with a lazy maximum
-      bool need = false;
-#pragma unroll
-      for (int h = 0; h < GP; ++h)
-#pragma unroll
-        for (int tt = 0; tt < T; ++tt) need |= s[h][tt] > m[h] + ATTN_TAU;
-      if (__any_sync(FULL_MASK, need)) {
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-          float mx = s[h][0];
-#pragma unroll
-          for (int tt = 1; tt < T; ++tt) mx = fmaxf(mx, s[h][tt]);
-          const float mn = fmaxf(m[h], mx);
-          const float sc = fast_exp2(m[h] - mn);
-          l[h] *= sc;
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) o[h][d] *= sc;
-          m[h] = mn;
-        }
-      }
-      float p[GP][T];
-#pragma unroll
-      for (int h = 0; h < GP; ++h)
+      for (int bt = 0; bt < S::BATCHES; ++bt) {
+        const int tb = bt * S::TOK_PER_BATCH + grp * T;  // first token of this lane group
+        // partial q.k over the lane's dims: x[h * T + tt]
+        float x[8];
 #pragma unroll
         for (int tt = 0; tt < T; ++tt) {
-          p[h][tt] = fast_exp2(s[h][tt] - m[h]);
-          l[h] += p[h][tt];
+          const uint4 *kr = reinterpret_cast<const uint4 *>(kst + (tb + tt) * S::ROW_BYTES);
+          f32x2 k2[NP];
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            const uint4 w = kr[li + 8 * c];
+            k2[4 * c + 0] = bf16x2_to_f32x2(w.x);
+            k2[4 * c + 1] = bf16x2_to_f32x2(w.y);
+            k2[4 * c + 2] = bf16x2_to_f32x2(w.z);
+            k2[4 * c + 3] = bf16x2_to_f32x2(w.w);
+          }
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            f32x2 acc = fmul2(q2[h][0], k2[0]);
+#pragma unroll
+            for (int j = 1; j < NP; ++j) acc = ffma2(q2[h][j], k2[j], acc);
+            const float2 r = unpack2(acc);
+            x[h * T + tt] = r.x + r.y;
+          }
         }
+        // reduce-scatter over the 8 lanes of the group: lane li ends with the
+        // full dot product of value li
+        float y[4], z[2];
+        {
+          const bool up = li & 4;
 #pragma unroll
-      for (int tt = 0; tt < T; ++tt) {
-        const uint4 *vr = reinterpret_cast<const uint4 *>(vst + (tb + tt) * S::ROW_BYTES);
-        float vf[DPL];
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) unpack8(vr[li + 8 * c], vf + 8 * c);
-        if (ragged && tok0 + tb + tt >= n) {
-          // rows past the end of the sequence may hold any bits
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) vf[d] = 0.0f;
+          for (int k = 0; k < 4; ++k) {
+            const float send = up ? x[k] : x[k + 4];
+            const float keep = up ? x[k + 4] : x[k];
+            y[k] = keep + __shfl_xor_sync(FULL_MASK, send, 4);
+          }
         }
+        {
+          const bool up = li & 2;
 #pragma unroll
-        for (int h = 0; h < GP; ++h)
+          for (int k = 0; k < 2; ++k) {
+            const float send = up ? y[k] : y[k + 2];
+            const float keep = up ? y[k + 2] : y[k];
+            z[k] = keep + __shfl_xor_sync(FULL_MASK, send, 2);
+          }
+        }
+        float s;
+        {
+          const bool up = li & 1;
+          const float send = up ? z[0] : z[1];
+          const float keep = up ? z[1] : z[0];
+          s = keep + __shfl_xor_sync(FULL_MASK, send, 1);
+        }
+        if (ragged && tok0 + tb + tt_own >= n) s = -INFINITY;
+        // online softmax with a lazy maximum
+        if (__any_sync(FULL_MASK, s > m_own + ATTN_TAU)) {
+          float bm = s;  // maximum of this batch for head h_own
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(p[h][tt], vf[d], o[h][d]);
+          for (int off = 1; off < T; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, off));
+          float m_own_new = m_own;
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            const float mh = __shfl_sync(FULL_MASK, bm, gbase | (h * T));
+            const float mn = fmaxf(m_all[h], mh);
+            const float sc = fast_exp2(m_all[h] - mn);
+            const f32x2 sc2 = pack2(sc, sc);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) o2[h][j] = fmul2(o2[h][j], sc2);
+            m_all[h] = mn;
+            if (h == h_own) m_own_new = mn;
+          }
+          l_own *= fast_exp2(m_own - m_own_new);
+          m_own = m_own_new;
+        }
+        const float p = fast_exp2(s - m_own);
+        l_own += p;
+        // every lane of the group gets the group's 8 probabilities
+        float pv[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) pv[v] = __shfl_sync(FULL_MASK, p, gbase | v);
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) {
+          const uint4 *vr = reinterpret_cast<const uint4 *>(vst + (tb + tt) * S::ROW_BYTES);
+          f32x2 v2[NP];
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            const uint4 w = vr[li + 8 * c];
+            v2[4 * c + 0] = bf16x2_to_f32x2(w.x);
+            v2[4 * c + 1] = bf16x2_to_f32x2(w.y);
+            v2[4 * c + 2] = bf16x2_to_f32x2(w.z);
+            v2[4 * c + 3] = bf16x2_to_f32x2(w.w);
+          }
+          if (ragged && tok0 + tb + tt >= n) {
+            // rows past the end of the sequence may hold any bits
+#pragma unroll
+            for (int j = 0; j < NP; ++j) v2[j] = 0ull;
+          }
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            const f32x2 pp = pack2(pv[h * T + tt], pv[h * T + tt]);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) o2[h][j] = ffma2(pp, v2[j], o2[h][j]);
+          }
+        }
+      }
+      ++consumed;
+      __syncwarp();
+      top_up();
+    }
+
+    // ---- merge the 4 lane groups of the warp (shuffles) ----------------
+    // l per head: the sum over the T lanes of the head within the group
+    float lsum = l_own;
+#pragma unroll
+    for (int off = 1; off < T; off <<= 1) lsum += __shfl_xor_sync(FULL_MASK, lsum, off);
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      const float lh = __shfl_sync(FULL_MASK, lsum, gbase | (h * T));
+      float M = m_all[h];
+      M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, 8));
+      M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, 16));
+      const float w = fast_exp2(m_all[h] - M);
+      float L = lh * w;
+      L += __shfl_xor_sync(FULL_MASK, L, 8);
+      L += __shfl_xor_sync(FULL_MASK, L, 16);
+      const f32x2 w2 = pack2(w, w);
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        float2 v = unpack2(fmul2(o2[h][j], w2));
+        v.x += __shfl_xor_sync(FULL_MASK, v.x, 8);
+        v.y += __shfl_xor_sync(FULL_MASK, v.y, 8);
+        v.x += __shfl_xor_sync(FULL_MASK, v.x, 16);
+        v.y += __shfl_xor_sync(FULL_MASK, v.y, 16);
+        o2[h][j] = pack2(v.x, v.y);
+      }
+      m_all[h] = M;
+      if (grp == 0 && li == 0) red_ml[warp * GP + h] = make_float2(M, L);
+    }
+    if (grp == 0) {
+#pragma unroll
+      for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          float4 *dst = reinterpret_cast<float4 *>(red_o + (warp * GP + h) * D + (li + 8 * c) * 8);
+          const float2 a0 = unpack2(o2[h][4 * c + 0]), a1 = unpack2(o2[h][4 * c + 1]);
+          const float2 a2 = unpack2(o2[h][4 * c + 2]), a3 = unpack2(o2[h][4 * c + 3]);
+          dst[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
+          dst[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
+        }
+    }
+    // the unit after next: fetched now, read after the barrier
+    if (tid == 0) s_unit[(ordinal + 2) & 3] = atomicAdd(&a.plan->counter, 1);
+    named_barrier_sync();
+
+    // ---- merge the 4 warps; write the output or the split's partial -----
+    const int64_t bh0 = (int64_t)cur.b * Hq + cur.h0;
+    for (int idx = tid; idx < cur.nh * D; idx += ATTN_THREADS) {
+      const int h = idx / D, d = idx % D;
+      float M = ATTN_NEG;
+#pragma unroll
+      for (int w = 0; w < ATTN_WARPS; ++w) M = fmaxf(M, red_ml[w * GP + h].x);
+      float L = 0.0f, O = 0.0f;
+#pragma unroll
+      for (int w = 0; w < ATTN_WARPS; ++w) {
+        const float2 ml = red_ml[w * GP + h];
+        const float wt = fast_exp2(ml.x - M);
+        L = fmaf(ml.y, wt, L);
+        O = fmaf(red_o[(w * GP + h) * D + d], wt, O);
+      }
+      const int64_t bh = bh0 + h;
+      if (cur.nsplit == 1) {
+        store_out(a, bh * D + d, O / L);
+        if (d == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(L)) * LN2;
+      } else {
+        const int64_t ps = bh * a.nsplit_max + cur.split;
+        a.ws_o[ps * D + d] = O;
+        if (d == 0) a.ws_ml[ps] = make_float2(M, L);
       }
     }
-    __syncwarp();
-    if (i + NS < my_count) {
-      fence_proxy_async_smem();
-      issue(i + NS, slot);
+    if (cur.nsplit > 1) {
+      // the CTA that completes the last split of (row, head block) folds
+      // the partials in split order
+      __threadfence();
+      named_barrier_sync();
+      if (tid == 0) {
+        const int HB = a.num_kv_heads * a.qblocks;
+        int32_t *ticket = a.tickets + (int64_t)cur.b * HB + cur.g * a.qblocks + cur.qb;
+        const int done = atomicAdd(ticket, 1);
+        s_last = (done == cur.nsplit - 1);
+        if (s_last) *ticket = 0;
+      }
+      named_barrier_sync();
+      if (s_last) {
+        __threadfence();
+        for (int idx = tid; idx < cur.nh * D; idx += ATTN_THREADS) {
+          const int h = idx / D, d = idx % D;
+          const int64_t bh = bh0 + h;
+          const float2 *ml = a.ws_ml + bh * a.nsplit_max;
+          const float *po = a.ws_o + bh * a.nsplit_max * D + d;
+          float M = ATTN_NEG;
+#pragma unroll 8
+          for (int s = 0; s < cur.nsplit; ++s) M = fmaxf(M, __ldcg(ml + s).x);
+          float L = 0.0f, O = 0.0f;
+#pragma unroll 8
+          for (int s = 0; s < cur.nsplit; ++s) {
+            const float2 v = __ldcg(ml + s);
+            const float wt = fast_exp2(v.x - M);
+            L = fmaf(v.y, wt, L);
+            O = fmaf(__ldcg(po + (int64_t)s * D), wt, O);
+          }
+          store_out(a, bh * D + d, O / L);
+          if (d == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(L)) * LN2;
+        }
+      }
     }
-  }
-  if (timed_out) {
-    if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
-    // let the copies still in flight land before the shared memory is reused
-    const int issued = my_count < consumed + NS ? my_count : consumed + NS;
-    for (int i = consumed; i < issued; ++i)
-      (void)mbar_wait(&wbars[i % NS], (uint32_t)((i / NS) & 1), 100000000ull);
-  }
-
-  // ---- merge the 16 lane groups of the CTA through shared memory --------
-  __syncthreads();
-  float *red_o = reinterpret_cast<float *>(smem);                              // [16][GP][D]
-  float2 *red_ml = reinterpret_cast<float2 *>(smem + ATTN_WARPS * 4 * GP * D * 4);  // [16][GP]
-  const int gi = warp * 4 + grp;
-  if (li == 0) {
-#pragma unroll
-    for (int h = 0; h < GP; ++h) red_ml[gi * GP + h] = make_float2(m[h], l[h]);
-  }
-#pragma unroll
-  for (int h = 0; h < GP; ++h)
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      float4 *dst = reinterpret_cast<float4 *>(red_o + (gi * GP + h) * D + (li + 8 * c) * 8);
-      dst[0] = make_float4(o[h][8 * c + 0], o[h][8 * c + 1], o[h][8 * c + 2], o[h][8 * c + 3]);
-      dst[1] = make_float4(o[h][8 * c + 4], o[h][8 * c + 5], o[h][8 * c + 6], o[h][8 * c + 7]);
-    }
-  __syncthreads();
-
-  for (int idx = threadIdx.x; idx < nh * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx % D;
-    float M = ATTN_NEG;
-#pragma unroll
-    for (int q = 0; q < ATTN_WARPS * 4; ++q) M = fmaxf(M, red_ml[q * GP + h].x);
-    float L = 0.0f, O = 0.0f;
-#pragma unroll
-    for (int q = 0; q < ATTN_WARPS * 4; ++q) {
-      const float2 ml = red_ml[q * GP + h];
-      const float w = fast_exp2(ml.x - M);
-      L = fmaf(ml.y, w, L);
-      O = fmaf(red_o[(q * GP + h) * D + d], w, O);
-    }
-    const int64_t bh = (int64_t)b * Hq + h0 + h;
-    if (nsplit == 1) {
-      store_out<D>(a, bh * D + d, O / L);
-      if (d == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(L)) * LN2;
+    // rotate units; the barrier also protects red_o / red_ml for the next merge
+    named_barrier_sync();
+    ++ordinal;
+    cur = nxt;
+    cur_cnt = nxt_cnt;
+    pid_cur = pid_nxt;
+    nxt = decode_unit(a, s_unit[(ordinal + 1) & 3], GP, total_units, rs, seq);
+    nxt_cnt = warp_pages(nxt, warp);
+    pid_nxt = load_pids(nxt, nxt_cnt);
+    stage_q(nxt, (ordinal + 1) & 1);
+    if (iss_u == 1) {
+      iss_u = 0;  // pages already issued of the old "next" unit belong to "cur" now
     } else {
-      const int64_t ps = bh * a.nsplit_max + split;
-      a.ws_o[ps * D + d] = O;
-      if (d == 0) a.ws_ml[ps] = make_float2(M, L);
+      iss_i = 0;  // the warp had issued nothing of the old "next" unit
     }
   }
-}
-
-// Fold the split partials of rows with more than one split, in split order.
-template <int D>
-__global__ void __launch_bounds__(D) attn_merge_kernel(const AttnArgs a) {
-  const int h = blockIdx.x;
-  const int b = blockIdx.y;
-  const int d = threadIdx.x;
-  if (!a.active[b]) return;
-  const int n = a.seq_lens[b];
-  if (n < 1 || (int64_t)n > (int64_t)a.max_pages * ATTN_PAGE) return;
-  const int npages = (n + ATTN_PAGE - 1) / ATTN_PAGE;
-  const int nsplit = (npages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT;
-  if (nsplit <= 1) return;
-  const int64_t bh = (int64_t)b * a.num_qo_heads + h;
-  const float2 *ml = a.ws_ml + bh * a.nsplit_max;
-  const float *po = a.ws_o + bh * a.nsplit_max * D + d;
-  float M = ATTN_NEG;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[s].x);
-  float L = 0.0f, O = 0.0f;
-  for (int s = 0; s < nsplit; ++s) {
-    const float2 v = ml[s];
-    const float w = fast_exp2(v.x - M);
-    L = fmaf(v.y, w, L);
-    O = fmaf(po[(int64_t)s * D], w, O);
+  if (dead) {
+    // let the copies still in flight land before the CTA's shared memory goes
+    for (int k = consumed; k < issued; ++k)
+      (void)mbar_wait(&wbars[k % NS], (uint32_t)((k / NS) & 1), 100000000ull);
   }
-  store_out<D>(a, bh * D + d, O / L);
-  if (d == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(L)) * LN2;
-}
-
-template <int D, int GP, int NS>
-static int launch_attn(const AttnArgs &a, int hkv, cudaStream_t st) {
-  using S = AttnShape<D, GP, NS>;
-  auto kern = attn_split_kernel<D, GP, NS>;
-  static unsigned long long configured = 0;  // one bit per device; a race only repeats the call
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(configured & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) !=
-        cudaSuccess)
-      return PKV_ERR_CUDA;
-    configured |= bit;
-  }
-  dim3 grid((unsigned)(hkv * a.qblocks), (unsigned)a.nsplit_max, (unsigned)a.batch);
-  kern<<<grid, ATTN_WARPS * 32, S::SMEM_BYTES, st>>>(a);
-  int rc = launch_status();
-  if (rc != PKV_OK) return rc;
-  if (a.nsplit_max > 1) {
-    attn_merge_kernel<D><<<dim3((unsigned)a.num_qo_heads, (unsigned)a.batch), D, 0, st>>>(a);
-    rc = launch_status();
-  }
-  return rc;
 }
 
 // q heads per CTA: the group rounded up to 2 / 4 / 8, at most 4 for
@@ -409,20 +662,97 @@ static int heads_per_cta(int D, int group) {
   return gp < cap ? gp : cap;
 }
 
+template <int D, int GP, int NS>
+static int launch_attn(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t st) {
+  using S = AttnShape<D, GP, NS>;
+  auto kern = attn_persistent_kernel<D, GP, NS>;
+  static int grid_for_device[64] = {0};  // persistent grid per device (0: not known yet)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  int &grid = grid_for_device[dev & 63];
+  if (grid == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) !=
+        cudaSuccess)
+      return PKV_ERR_CUDA;
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, ATTN_THREADS,
+                                                      S::SMEM_BYTES) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (per_sm < 1) return PKV_ERR_UNSUPPORTED;
+    grid = sms * per_sm;
+  }
+  attn_plan_kernel<<<1, PLAN_THREADS, 0, st>>>(a);
+  int rc = launch_status();
+  if (rc != PKV_OK) return rc;
+  kern<<<grid, ATTN_THREADS, S::SMEM_BYTES, st>>>(a, tmap);
+  return launch_status();
+}
+
 template <int D>
-static int dispatch_gp(const AttnArgs &a, int hkv, int gp, cudaStream_t st) {
+static int dispatch_gp(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t st) {
   constexpr int NS = D == 128 ? 3 : 6;
-  switch (gp) {
-    case 2: return launch_attn<D, 2, NS>(a, hkv, st);
-    case 4: return launch_attn<D, 4, NS>(a, hkv, st);
+  switch (a.gp) {
+    case 2: return launch_attn<D, 2, NS>(a, tmap, st);
+    case 4: return launch_attn<D, 4, NS>(a, tmap, st);
     default:
-      if constexpr (D == 64) return launch_attn<D, 8, NS>(a, hkv, st);
+      if constexpr (D == 64) return launch_attn<D, 8, NS>(a, tmap, st);
       return PKV_ERR_UNSUPPORTED;
   }
 }
 
+// The driver's tensor-map encoder, fetched once through the runtime (no
+// link-time dependency on libcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 5-D view of the whole cache for the TMA engine, innermost first:
+// (head_dim, kv head, slot, K/V, layer * num_pages + page).  One box is one
+// page of one kv head: head_dim x 1 x page_size x 2 x 1.
+static int encode_cache_map(CUtensorMap *map, const void *cache, const pkv_cache_t *g) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t D = (cuuint64_t)g->head_dim, H = (cuuint64_t)g->num_kv_heads;
+  const cuuint64_t PS = (cuuint64_t)g->page_size;
+  const cuuint64_t dims[5] = {D, H, PS, 2, (cuuint64_t)g->num_layers * (cuuint64_t)g->num_pages};
+  const cuuint64_t strides[4] = {D * 2, H * D * 2, PS * H * D * 2, 2 * PS * H * D * 2};
+  const cuuint32_t box[5] = {(cuuint32_t)D, 1, (cuuint32_t)PS, 2, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
+}
+
 static size_t nsplit_for(int max_pages) {
   return (size_t)((max_pages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT);
+}
+
+struct WsLayout {
+  size_t o, ml, row_start, tickets, plan, total;
+};
+
+static WsLayout ws_layout(int batch, int num_qo_heads, int head_dim, int max_pages) {
+  WsLayout w;
+  const size_t units = (size_t)batch * num_qo_heads * nsplit_for(max_pages);
+  w.o = 0;
+  w.ml = align_up(units * head_dim * sizeof(float), 256);
+  w.row_start = w.ml + align_up(units * sizeof(float2), 256);
+  w.tickets = w.row_start + align_up((size_t)(batch + 1) * sizeof(int32_t), 256);
+  w.plan = w.tickets + align_up((size_t)batch * num_qo_heads * sizeof(int32_t), 256);
+  w.total = w.plan + 256;
+  return w;
 }
 
 }  // namespace pkv
@@ -432,9 +762,7 @@ extern "C" size_t pkv_decode_workspace_bytes(int batch, int num_qo_heads, int he
   using namespace pkv;
   if (batch <= 0 || num_qo_heads <= 0 || head_dim <= 0 || max_pages <= 0 || page_size <= 0)
     return 0;
-  const size_t ns = nsplit_for(max_pages);
-  const size_t units = (size_t)batch * num_qo_heads * ns;
-  return align_up(units * head_dim * sizeof(float), 256) + align_up(units * sizeof(float2), 256);
+  return ws_layout(batch, num_qo_heads, head_dim, max_pages).total;
 }
 
 extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache, int layer,
@@ -455,12 +783,12 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
   const int group = num_qo_heads / geom->num_kv_heads;
   if ((D != 64 && D != 128) || geom->page_size != ATTN_PAGE || group > 64)
     return PKV_ERR_UNSUPPORTED;
-  if (batch > 65535 || nsplit_for(max_pages) > 65535) return PKV_ERR_UNSUPPORTED;
+  if ((int64_t)batch * num_qo_heads * (int64_t)nsplit_for(max_pages) > (1ll << 30))
+    return PKV_ERR_UNSUPPORTED;
   if (!aligned16(cache) || !aligned16(q)) return PKV_ERR_INVALID_ARG;
-  const size_t need = pkv_decode_workspace_bytes(batch, num_qo_heads, D, max_pages, ATTN_PAGE);
-  const int nsplit_max = (int)nsplit_for(max_pages);
-  if (nsplit_max > 1 && (workspace == nullptr || workspace_bytes < need)) return PKV_ERR_WORKSPACE;
-  if (workspace != nullptr && ((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(batch, num_qo_heads, D, max_pages);
+  if (workspace == nullptr || workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
 
   AttnArgs a;
   const int64_t row_bytes = (int64_t)D * 2;
@@ -471,11 +799,12 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
   a.layer_off = a.page_stride * (int64_t)geom->num_pages * layer;
   a.num_pages = geom->num_pages;
   a.num_kv_heads = geom->num_kv_heads;
+  a.head_dim = D;
   a.q = static_cast<const uint16_t *>(q);
   a.num_qo_heads = num_qo_heads;
   a.group = group;
-  const int gp = heads_per_cta(D, group);
-  a.qblocks = (group + gp - 1) / gp;
+  a.gp = heads_per_cta(D, group);
+  a.qblocks = (group + a.gp - 1) / a.gp;
   a.qscale = sm_scale * LOG2E;
   a.page_table = page_table;
   a.max_pages = max_pages;
@@ -485,14 +814,19 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
   a.out = out;
   a.out_fp32 = out_fp32 != 0;
   a.lse = lse;
-  a.nsplit_max = nsplit_max;
-  const size_t units = (size_t)batch * num_qo_heads * nsplit_max;
-  a.ws_o = static_cast<float *>(workspace);
-  a.ws_ml = workspace ? reinterpret_cast<float2 *>(static_cast<unsigned char *>(workspace) +
-                                                   align_up(units * D * sizeof(float), 256))
-                      : nullptr;
+  a.nsplit_max = (int)nsplit_for(max_pages);
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  a.ws_o = reinterpret_cast<float *>(ws + wl.o);
+  a.ws_ml = reinterpret_cast<float2 *>(ws + wl.ml);
+  a.row_start = reinterpret_cast<int32_t *>(ws + wl.row_start);
+  a.tickets = reinterpret_cast<int32_t *>(ws + wl.tickets);
+  a.plan = reinterpret_cast<PlanHeader *>(ws + wl.plan);
   a.err = err_word;
+  a.layer = layer;
+  if ((int64_t)geom->num_layers * geom->num_pages > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  alignas(64) CUtensorMap tmap;
+  st = encode_cache_map(&tmap, cache, geom);
+  if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return D == 128 ? dispatch_gp<128>(a, geom->num_kv_heads, gp, s)
-                  : dispatch_gp<64>(a, geom->num_kv_heads, gp, s);
+  return D == 128 ? dispatch_gp<128>(a, tmap, s) : dispatch_gp<64>(a, tmap, s);
 }

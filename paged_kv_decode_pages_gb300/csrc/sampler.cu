@@ -19,15 +19,16 @@
 //    composite comes first in (value desc, id asc) order, and composites
 //    are unique.
 //  * chunk pass (one CTA per 8192-token chunk of a row): chunk maximum;
-//    the chunk's 64 largest composites (radix select over 8-bit digits);
+//    the chunk's largest composites (its top-k, or 512 for top-p over the
+//    whole vocabulary; radix select over 8-bit digits);
 //    for top-p over the whole vocabulary, the fp64 partial normaliser
 //    sum exp(x - x_chunkmax); for "keep everything", the chunk's Gumbel
 //    argmax.  The chunking depends on the vocabulary only.
 //  * finish (one CTA per row): merges the chunk records in chunk order,
 //    sorts the candidates, applies top-k / top-p with sequential fp64
 //    prefix sums in sorted order, and takes the Gumbel argmax.  Rows whose
-//    kept set is not decided by the top 64 tokens (top-k > 64, or top-p
-//    needing more than 64 tokens) take an exact general path that streams
+//    kept set is not decided by those candidates (top-k > 512, or top-p
+//    needing more than 512 tokens) take an exact general path that streams
 //    the row: radix select of the top-k threshold and progressive sorted
 //    extraction until the top-p crossing.
 //  * the frame kernel runs the same chunk pass and finish for each of the
@@ -42,10 +43,9 @@ namespace pkv {
 constexpr int SB = 256;                 // threads per sampler CTA
 constexpr int CHUNK = 8192;             // tokens per chunk
 constexpr int EPT = CHUNK / SB;         // tokens per thread in a chunk pass
-constexpr int NCAND = 64;               // candidates kept per chunk
+constexpr int NCAND = 512;              // most candidates kept per chunk
 constexpr int MAX_CHUNKS = 64;          // vocab <= 64 * 8192
-constexpr int GEN_BLOCK = 1024;         // sorted block of the general path
-constexpr int SORT_CAP = MAX_CHUNKS * NCAND;  // 4096
+constexpr int GEN_BLOCK = 1024;         // sorted block (finish and general path)
 
 enum Mode : int { MODE_GREEDY = 0, MODE_TOPK_SMALL = 1, MODE_TOPP_FULL = 2, MODE_ALL = 3, MODE_GENERAL = 4 };
 
@@ -59,6 +59,7 @@ struct ChunkRec {
   uint64_t cand[NCAND];
   uint64_t pad_[3];
 };
+// candidates per chunk: top-k rows keep their k, top-p rows NCAND
 static_assert(sizeof(ChunkRec) % 64 == 0, "ChunkRec");
 
 struct RowParams {
@@ -70,6 +71,7 @@ struct RowParams {
   int64_t step;
   int K;       // top-k count after normalisation (V when off)
   int mode;
+  int nc;      // candidates per chunk
 };
 
 // ---------------------------------------------------------------------------
@@ -147,7 +149,7 @@ struct SampSmem {
   int32_t token;
   int32_t kept;
   double zsum;
-  uint64_t sortbuf[SORT_CAP];
+  uint64_t sortbuf[GEN_BLOCK];
   double xs[NCAND];
   double es[GEN_BLOCK];
 };
@@ -328,12 +330,13 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
     return;
   }
 
-  // the chunk's NCAND largest composites
+  // the chunk's nc largest composites
+  const int nc = P.nc;
   uint64_t thr = 0;  // keep composites >= thr
-  if (cnt > NCAND) {
+  if (cnt > nc) {
     if (tid == 0) {
       sm.sel_prefix = 0;
-      sm.sel_want = NCAND;
+      sm.sel_want = (uint32_t)nc;
       sm.sel_done = 0;
     }
     __syncthreads();
@@ -368,13 +371,13 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
       const uint64_t cc = composite(key[j], start + i);
       if (cc >= thr) {
         const uint32_t pos = atomicAdd(&sm.cnt, 1u);
-        if (pos < NCAND) rec->cand[pos] = cc;
+        if (pos < (uint32_t)nc) rec->cand[pos] = cc;
       }
     }
   }
   __syncthreads();
-  const int got = min((int)sm.cnt, NCAND);
-  for (int i = got + tid; i < NCAND; i += SB) rec->cand[i] = 0;
+  const int got = min((int)sm.cnt, nc);
+  for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0;
   if (tid == 0) rec->ncand = got;
 
   if (P.mode == MODE_TOPP_FULL) {
@@ -395,8 +398,40 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
 }
 
 // ---------------------------------------------------------------------------
-// general path: exact, streams the row (used when the top 64 do not decide)
+// general path: exact, streams the row (used when the candidates do not decide)
 // ---------------------------------------------------------------------------
+// Composite of rank `rank` (0-based, descending) among the values get(i),
+// i < n, that are below `upper` (0 marks "no value").  Requires that many
+// such values to exist.
+template <class Get>
+__device__ uint64_t select_rank_of(int n, Get get, uint64_t upper, int rank, SampSmem &sm) {
+  if (threadIdx.x == 0) {
+    sm.sel_prefix = 0;
+    sm.sel_want = (uint32_t)rank + 1u;
+    sm.sel_done = 0;
+  }
+  __syncthreads();
+  uint64_t mask = 0;
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    for (int i = threadIdx.x; i < 256; i += SB) sm.hist[i] = 0;
+    __syncthreads();
+    const uint64_t prefix = sm.sel_prefix;
+    for (int i = threadIdx.x; i < n; i += SB) {
+      const uint64_t cc = get(i);
+      if (cc != 0ull && cc < upper && (cc & mask) == prefix)
+        atomicAdd(&sm.hist[(cc >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    select_bin(sm, shift);
+    mask |= 255ull << shift;
+    if (sm.sel_done) break;
+  }
+  const uint64_t r = sm.sel_prefix;
+  __syncthreads();
+  return r;
+}
+
 // Composite of rank `rank` (0-based, descending) among elements with
 // composite < upper.  Requires that many such elements to exist.
 __device__ uint64_t select_rank(const float *__restrict__ row, int V, uint64_t upper, int rank,
@@ -428,21 +463,26 @@ __device__ uint64_t select_rank(const float *__restrict__ row, int V, uint64_t u
   return r;
 }
 
+// z_known >= 0: the normaliser over the top-k survivors, already computed
+// relative to the row maximum (top-p over the whole vocabulary).
 __device__ int general_sample(const float *__restrict__ row, int V, const RowParams &P,
-                              uint64_t top1, SampSmem &sm) {
+                              uint64_t top1, double z_known, SampSmem &sm) {
   const int tid = threadIdx.x;
   const int K = P.K;
   const uint64_t thrK = (K < V) ? select_rank(row, V, ~0ull, K - 1, sm) : 0ull;
   uint64_t thr = thrK;
   if (P.top_p < 1.0f) {
     const double m = comp_x(top1, P.temperature);
-    double z = 0.0;
     bool dummy = false;
-    for (int i = tid; i < V; i += SB) {
-      const uint32_t key = order_key(row[i], dummy);
-      if (composite(key, i) >= thrK) z += exp((double)key_value(key) / (double)P.temperature - m);
+    double z = z_known;
+    if (z < 0.0) {
+      z = 0.0;
+      for (int i = tid; i < V; i += SB) {
+        const uint32_t key = order_key(row[i], dummy);
+        if (composite(key, i) >= thrK) z += exp((double)key_value(key) / (double)P.temperature - m);
+      }
+      z = block_sum_d(z, sm);
     }
-    z = block_sum_d(z, sm);
     const double pz = (double)P.top_p * z;
     // progressive sorted extraction until the running sum reaches p * Z
     uint64_t upper = ~0ull;
@@ -534,17 +574,35 @@ __device__ int finish_row(const float *__restrict__ row, int V, int nch, const R
   }
   uint64_t top1 = 0;
   for (int c = 0; c < nch; ++c) top1 = recs[c].top1 > top1 ? recs[c].top1 : top1;
-  if (P.mode == MODE_GENERAL) return general_sample(row, V, P, top1, sm);
+  if (P.mode == MODE_GENERAL) return general_sample(row, V, P, top1, -1.0, sm);
 
-  // gather and sort the candidates
-  const int ncand = nch * NCAND;
+  // the nc largest of the union of the chunks' candidates, sorted
+  const int nc = P.nc;
+  const int nu = nch * nc;
+  auto cand_at = [&](int i) -> uint64_t { return recs[i / nc].cand[i % nc]; };
+  int nsort;
+  if (nu <= GEN_BLOCK) {
+    nsort = nu;
+    for (int i = tid; i < nu; i += SB) sm.sortbuf[i] = cand_at(i);
+  } else {
+    const uint64_t thr = select_rank_of(nu, cand_at, ~0ull, nc - 1, sm);
+    if (tid == 0) sm.cnt = 0;
+    __syncthreads();
+    for (int i = tid; i < nu; i += SB) {
+      const uint64_t cc = cand_at(i);
+      if (cc >= thr) {
+        const uint32_t pos = atomicAdd(&sm.cnt, 1u);
+        if (pos < (uint32_t)nc) sm.sortbuf[pos] = cc;
+      }
+    }
+    nsort = nc;
+  }
   int n2 = 1;
-  while (n2 < ncand) n2 <<= 1;
-  for (int i = tid; i < n2; i += SB)
-    sm.sortbuf[i] = (i < ncand) ? recs[i / NCAND].cand[i % NCAND] : 0ull;
+  while (n2 < nsort) n2 <<= 1;
+  for (int i = nsort + tid; i < n2; i += SB) sm.sortbuf[i] = 0ull;
   __syncthreads();
   block_sort_desc(sm.sortbuf, n2);
-  const int nv = min(P.mode == MODE_TOPK_SMALL ? P.K : NCAND, V);
+  const int nv = min(nc, V);
   const double m = comp_x(sm.sortbuf[0], P.temperature);
   for (int r = tid; r < nv; r += SB) {
     sm.xs[r] = comp_x(sm.sortbuf[r], P.temperature);
@@ -573,14 +631,15 @@ __device__ int finish_row(const float *__restrict__ row, int V, int nch, const R
           break;
         }
       }
-      // top-p over the whole vocabulary still open after the top NCAND
+      // top-p over the whole vocabulary still open after the top nc
       if (P.mode == MODE_TOPP_FULL && kept == nv && nv < V && S < pz) fallback = 1;
+      sm.zsum = Z;
     }
     sm.kept = kept;
     sm.flag = fallback;
   }
   __syncthreads();
-  if (sm.flag) return general_sample(row, V, P, top1, sm);
+  if (sm.flag) return general_sample(row, V, P, top1, sm.zsum, sm);
   const int kept = sm.kept;
   double bs = 0.0;
   int bid = -1;
@@ -616,6 +675,7 @@ __device__ __forceinline__ RowParams row_params(int V, uint64_t seed, int64_t st
     P.mode = (top_p < 1.0f) ? MODE_TOPP_FULL : MODE_ALL;
   else
     P.mode = MODE_GENERAL;
+  P.nc = P.mode == MODE_TOPK_SMALL ? P.K : NCAND;
   return P;
 }
 
@@ -809,10 +869,9 @@ extern "C" int pkv_seeded_sample(const float *logits, int64_t row_stride, int ba
   int st = check_sampler_common(batch, vocab, slots, active, num_slots, seeds, steps, temperature,
                                 top_k, top_p);
   if (st != PKV_OK) return st;
-  if (!logits || !out_tok || !out_kind || row_stride < vocab || (row_stride & 3) != 0)
-    return PKV_ERR_INVALID_ARG;
+  if (!logits || !out_tok || !out_kind || row_stride < vocab) return PKV_ERR_INVALID_ARG;
   if (n_stop < 0 || (n_stop > 0 && !stop_tokens)) return PKV_ERR_INVALID_ARG;
-  if (!aligned16(logits)) return PKV_ERR_INVALID_ARG;
+  if (((uintptr_t)logits & 3u) != 0) return PKV_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < pkv_sample_workspace_bytes(batch, vocab))
     return PKV_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
@@ -862,7 +921,7 @@ extern "C" int pkv_codebook_frame_sample(const float *base, const float *fb, int
                                 top_k, top_p);
   if (st != PKV_OK) return st;
   if (!base || !out_codes || !out_kind || n_codebooks <= 0) return PKV_ERR_INVALID_ARG;
-  if (!aligned16(base) || (fb && !aligned16(fb))) return PKV_ERR_INVALID_ARG;
+  if (((uintptr_t)base & 3u) != 0 || ((uintptr_t)fb & 3u) != 0) return PKV_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < pkv_frame_workspace_bytes(n_codebooks, batch, vocab))
     return PKV_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;

@@ -115,11 +115,10 @@ class DecodeStep:
             self.frame(stream=st)
 
     def launches_per_step(self) -> int:
-        """Kernel launches of one run(): append 1, attention 1 or 2 (merge when
-        any row can need more than one split), sampler 2, frame 1."""
+        """Kernel launches of one run(): per layer append 1 + attention 2
+        (planner + persistent kernel); sampler 2; frame 1."""
         L = self.t.layers
-        per_attn = 2 if self.batch.max_pages > 32 else 1
-        n = L * (1 + per_attn)
+        n = L * 3
         if self.t.logits is not None:
             n += 2
         if self.t.base is not None:

@@ -116,8 +116,11 @@ def test_config_samplers_match_oracle(name, B):
     dict(V=1024, T=1e-6, k=5, p=0.5, std=2.0, dist="ties"),  # greedy with ties
     dict(V=3000, T=0.7, k=1, p=0.9, std=2.0, dist="ties"),   # top-k 1 with ties
     dict(V=5, T=1.0, k=0, p=0.9, std=1.0),             # vocab below the candidate count
-    dict(V=20000, T=1.0, k=64, p=1.0, std=1.0),        # top-k at the candidate count
-    dict(V=20000, T=1.0, k=65, p=1.0, std=1.0),        # general path: top-k > 64
+    dict(V=20000, T=1.0, k=64, p=1.0, std=1.0),        # top-k from the chunk candidates
+    dict(V=20000, T=1.0, k=65, p=0.97, std=1.0),
+    dict(V=40000, T=1.0, k=256, p=0.99, std=1.0),
+    dict(V=40000, T=1.0, k=512, p=0.99, std=1.0),      # top-k at the candidate count
+    dict(V=40000, T=1.0, k=513, p=1.0, std=1.0),       # general path: top-k > 512
     dict(V=20000, T=2.0, k=1000, p=0.9, std=1.0),      # general path with top-p
     dict(V=20000, T=1.0, k=0, p=1.0, std=1.0),         # keep everything
     dict(V=20000, T=5.0, k=0, p=0.95, std=1.0),        # top-p needs thousands of tokens

@@ -1,0 +1,95 @@
+"""The pins are strong enough: each plausible mistake below, planted in a copy
+of the oracle's C source and compiled on the CPU, makes at least one pin of
+tests/test_oracle_attention.py or tests/test_oracle_sampler.py fail.  (The
+real oracle is untouched; the mutant is loaded only inside this test.)"""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+import test_oracle_attention as TA
+import test_oracle_sampler as TS
+
+# (name, original text, planted mistake)
+MUTANTS = [
+    ("gqa head mapping by modulo", "const int g = h / group;",
+     "const int g = h % num_kv_heads;"),
+    ("softmax scale dropped", "s[t] = sm_scale * dot;", "s[t] = dot;"),
+    ("keys read from the V half", "pg, 0, t % page_size, g);", "pg, 1, t % page_size, g);"),
+    ("values read from the K half", "pg, 1, t % page_size, g);", "pg, 0, t % page_size, g);"),
+    ("softmax not normalised", "double p = s[t] / z;", "double p = s[t];"),
+    ("lse without the max", "lse[bh] = m + log(z);", "lse[bh] = log(z);"),
+    ("append slot off by one", "slot = pos % page_size;", "slot = (pos + 1) % page_size;"),
+    ("philox xors the wrong high half", "uint64_t y0 = hi1 ^ x1 ^ k0;",
+     "uint64_t y0 = hi0 ^ x1 ^ k0;"),
+    ("philox bumps k1 by the wrong constant", "k1 += PHILOX_W1;", "k1 += PHILOX_W0;"),
+    ("uniform from word 1", "uint64_t j = w[0] >> 12;", "uint64_t j = w[1] >> 12;"),
+    ("gumbel sign flipped", "return -log(-log(u));", "return log(-log(u));"),
+    ("top-p boundary inclusive", "if (r == 0 || S < pz) {", "if (r == 0 || S <= pz) {"),
+    ("top-p drops the crossing token", "if (r == 0 || S < pz) {",
+     "if (r == 0 || S + e[r] < pz) {"),
+    ("ties to the higher id", "return (p->id > q->id) - (p->id < q->id);",
+     "return (p->id < q->id) - (p->id > q->id);"),
+    ("top-k keeps one too many", "int K = (top_k > 0 && top_k < V) ? top_k : V;",
+     "int K = (top_k > 0 && top_k < V) ? top_k + 1 : V;"),
+    ("greedy only at zero temperature", "if (!(temperature > 1e-5f)) {",
+     "if (!(temperature > 0.0f)) {"),
+    ("frame salt starts at 0", "step, (uint32_t)(1 + j),", "step, (uint32_t)(j),"),
+    ("frame feedback from the previous codebook's table",
+     "const float *fj = fb + ((int64_t)j * V + prev) * V;",
+     "const float *fj = fb + ((int64_t)(j - 1) * V + prev) * V;"),
+]
+
+
+def _pins():
+    """(name, callable) of the pin checks, cheapest first."""
+    return [
+        ("philox", lambda: [TS.test_philox_matches_numpy_raw_words(k, c) for k, c in [
+            ((12345, 7), (41, 3, 0, 0)), ((2**64 - 1, 2**63 + 5), (2**64 - 1, 2**64 - 1, 9, 0))]]),
+        ("uniform", TS.test_uniform_uses_word0_and_is_strictly_inside_unit_interval),
+        ("append", TA.test_append_writes_exactly_the_slot_and_nothing_else),
+        ("sdpa", lambda: [TA.test_attention_matches_torch_sdpa_fp64(*a)
+                          for a in [(4, 64, True), (3, 128, True)]]),
+        ("single token", TA.test_single_token_returns_its_value),
+        ("identical keys", TA.test_identical_keys_give_mean_of_values),
+        ("halves", TA.test_two_halves_merge_by_lse_to_the_whole),
+        ("greedy", lambda: [TS.test_greedy_is_numpy_argmax(t) for t in (0.0, 1e-6)]),
+        ("top-k/top-p argmax", TS.test_top_k_one_and_tiny_top_p_are_argmax_for_any_seed),
+        ("boundary p", TS.test_top_p_boundary_prefix_exactly_p_drops_the_next_token),
+        ("crossing", TS.test_top_p_keeps_the_crossing_token),
+        ("top-k ties", TS.test_top_k_tie_at_the_cut_goes_to_lower_ids),
+        ("kept sets", lambda: [TS.test_kept_set_count_matches_brute_force(v) for v in (5, 8)]),
+        ("frame salts", TS.test_frame_without_feedback_equals_independent_salted_samples),
+        ("frame feedback", TS.test_frame_feedback_wiring),
+        ("gumbel moments", TS.test_gumbel_moments),
+        ("chi-square", lambda: TS.test_gumbel_max_frequencies_chi_square(0, 1.0, 1.0)),
+    ]
+
+
+def test_every_mutant_source_edit_applies_once():
+    src = oracle.source_text()
+    for name, old, _ in MUTANTS:
+        assert src.count(old) == 1, name
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(name, old, new, workdir):
+    src = oracle.source_text().replace(old, new)
+    path = os.path.join(workdir, "mutant_%d.so" % abs(hash(name)))
+    oracle.compile_variant(src, path)
+    caught = None
+    with oracle.using_library(path):
+        for pin, fn in _pins():
+            try:
+                fn()
+            except AssertionError:
+                caught = pin
+                break
+    assert caught is not None, "no pin catches: %s" % name
