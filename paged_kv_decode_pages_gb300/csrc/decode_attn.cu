@@ -9,13 +9,13 @@
 //    not depend on the batch, so a row's result depends on its inputs only.
 //  * a one-CTA planner lists the splits of the active rows (prefix sums over
 //    the rows), zeroes the outputs of padding rows and resets the scheduling
-//    counter and the merge tickets, so the launch shapes stay static.
+//    counter, so the launch shapes stay static.
 //  * a persistent grid (SMs x resident CTAs) pulls units from an atomic
 //    counter.  Each of a CTA's 4 warps streams its pages of the unit
 //    (round-robin) through its own ring of NS shared-memory stages; a stage
 //    is one page of one kv head -- 16 K rows + 16 V rows, each head_dim bf16
-//    contiguous in HBM -- brought in by 32 bulk async copies (cp.async.bulk,
-//    the TMA engine) completing on the stage's mbarrier.  The ring runs on
+//    contiguous in HBM -- brought in by one tiled tensor TMA
+//    (cp.async.bulk.tensor) completing on the stage's mbarrier.  The ring runs on
 //    into the next unit, so its pages are in flight while the current unit
 //    is merged.  Waits are bounded.
 //  * GQA sharing: a warp holds the q of all the group's heads in registers,
@@ -26,10 +26,13 @@
 //    lanes with 3 xor-shuffles; the online softmax runs in the log2 domain
 //    with a lazy maximum (rescale only when a score beats the running
 //    maximum by more than 8).
-//  * per unit, the 4 lane groups of a warp merge with shuffles, the 4 warps
-//    through shared memory; a one-split row writes its output directly,
-//    longer rows write (m, l, o) partials and the CTA that completes a row's
-//    last split (an atomic ticket) folds them in split order.
+//  * a page's two 8-token batches are processed together (more independent
+//    work per warp between the shuffle steps).
+//  * per unit, the 4 lane groups of a warp merge with shuffles and the 4
+//    warps through shared memory into one (m, l, o) partial; a merge kernel
+//    then folds each row's partials in split order.  No fences, tickets or
+//    blocking atomics sit in the streaming loop: the next unit's id is
+//    fetched one unit ahead.
 #include <math.h>
 
 #include <cuda.h>
@@ -84,7 +87,6 @@ struct AttnArgs {
   float *ws_o;                 // [B][Hq][nsplit_max][D]
   float2 *ws_ml;               // [B][Hq][nsplit_max]
   int32_t *row_start;          // [B + 1] first split of each row
-  int32_t *tickets;            // [B][Hkv * qblocks]
   PlanHeader *plan;
   int nsplit_max;
   int32_t *err;
@@ -127,7 +129,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) attn_plan_kernel(const AttnArgs 
       bool bad;
       ns = row_splits(a, b, &bad);
       if (bad) report(a.err, PKV_DEV_ERR_SEQ_LEN);
-      for (int i = 0; i < HB; ++i) a.tickets[(int64_t)b * HB + i] = 0;
     }
     // inclusive scan of ns over the block (Hillis-Steele)
     scan[tid] = ns;
@@ -169,26 +170,27 @@ template <int D, int GP, int NS>
 struct AttnShape {
   static constexpr int T = 8 / GP;              // tokens per lane group per batch
   static constexpr int TOK_PER_BATCH = 4 * T;   // tokens per warp per batch
-  static constexpr int BATCHES = ATTN_PAGE / TOK_PER_BATCH;
+  static constexpr int NB = ATTN_PAGE / TOK_PER_BATCH;  // batches per page
   static constexpr int DPL = D / 8;             // dims per lane
   static constexpr int NCH = DPL / 8;           // 16-byte chunks per lane per row
+  static constexpr int NP = DPL / 2;            // fp32 pairs per lane per row
   static constexpr int ROW_BYTES = D * 2;
   static constexpr int STAGE_BYTES = 2 * ATTN_PAGE * ROW_BYTES;
   static constexpr int RING_BYTES = ATTN_WARPS * NS * STAGE_BYTES;
+  static constexpr int QBUF_BYTES = 2 * GP * D * 2;         // staged q of cur / next (bf16)
   static constexpr int RED_O_BYTES = ATTN_WARPS * GP * D * 4;
   static constexpr int RED_ML_BYTES = ATTN_WARPS * GP * 8;
-  static constexpr int QBUF_BYTES = 2 * GP * D * 2;         // q of cur and next unit (bf16)
   static constexpr int BAR_BYTES = ATTN_WARPS * NS * 8 + 2 * 8;
   static constexpr int SMEM_BYTES =
-      RING_BYTES + RED_O_BYTES + RED_ML_BYTES + QBUF_BYTES + BAR_BYTES + 128;
+      RING_BYTES + QBUF_BYTES + RED_O_BYTES + RED_ML_BYTES + BAR_BYTES + 128;
   static_assert(GP == 2 || GP == 4 || GP == 8, "GP");
   static_assert(D == 64 || D == 128, "D");
 };
 
 struct Unit {
   int valid;
-  int b, split, g, qb, h0, nh;
-  int n, p_begin, p_count, nsplit;
+  int b, split, g, h0, nh;
+  int n, p_begin, p_count;
 };
 
 constexpr int ATTN_SMEM_ROWS = 512;  // rows whose split table lives in shared memory
@@ -199,7 +201,7 @@ __device__ __forceinline__ Unit decode_unit(const AttnArgs &a, int u, int gp, in
   Unit U;
   const int HB = a.num_kv_heads * a.qblocks;
   U.valid = u < total_units;
-  U.b = U.split = U.g = U.qb = U.h0 = U.nh = U.n = U.p_begin = U.p_count = U.nsplit = 0;
+  U.b = U.split = U.g = U.h0 = U.nh = U.n = U.p_begin = U.p_count = 0;
   if (!U.valid) return U;
   const int su = u / HB, hb = u % HB;
   // row of split `su`: the last b with rs[b] <= su
@@ -214,12 +216,11 @@ __device__ __forceinline__ Unit decode_unit(const AttnArgs &a, int u, int gp, in
   U.b = lo;
   U.split = su - rs[lo];
   U.g = hb / a.qblocks;
-  U.qb = hb % a.qblocks;
-  U.h0 = U.g * a.group + U.qb * gp;
-  U.nh = min(gp, a.group - U.qb * gp);
+  const int qb = hb % a.qblocks;
+  U.h0 = U.g * a.group + qb * gp;
+  U.nh = min(gp, a.group - qb * gp);
   U.n = seq[U.b];
   const int npages = (U.n + ATTN_PAGE - 1) / ATTN_PAGE;
-  U.nsplit = (npages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT;
   U.p_begin = U.split * ATTN_PAGES_PER_SPLIT;
   U.p_count = min(npages - U.p_begin, ATTN_PAGES_PER_SPLIT);
   return U;
@@ -239,22 +240,22 @@ template <int D, int GP, int NS>
 __global__ void __launch_bounds__(ATTN_THREADS, 2)
     attn_persistent_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap) {
   using S = AttnShape<D, GP, NS>;
-  constexpr int T = S::T, DPL = S::DPL, NCH = S::NCH;
-  constexpr int NP = DPL / 2;  // fp32 pairs per lane per row
+  constexpr int T = S::T, NCH = S::NCH, NP = S::NP, NB = S::NB;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // stage buffers start on a 128-byte boundary
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  float *red_o = reinterpret_cast<float *>(smem + S::RING_BYTES);                      // [4][GP][D]
-  float2 *red_ml = reinterpret_cast<float2 *>(smem + S::RING_BYTES + S::RED_O_BYTES);  // [4][GP]
-  uint16_t *qbuf = reinterpret_cast<uint16_t *>(smem + S::RING_BYTES + S::RED_O_BYTES +
-                                                S::RED_ML_BYTES);                    // [2][GP][D]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::RING_BYTES + S::RED_O_BYTES +
-                                                S::RED_ML_BYTES + S::QBUF_BYTES);
+  unsigned char *p = smem + S::RING_BYTES;
+  uint16_t *qbuf = reinterpret_cast<uint16_t *>(p);  // [2][GP][D]
+  p += S::QBUF_BYTES;
+  float *red_o = reinterpret_cast<float *>(p);  // [4][GP][D]
+  p += S::RED_O_BYTES;
+  float2 *red_ml = reinterpret_cast<float2 *>(p);  // [4][GP]
+  p += S::RED_ML_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(p);
   uint64_t *qbars = bars + ATTN_WARPS * NS;  // [2]
   __shared__ int32_t s_unit[4];  // unit ids, circular: ordinal k at [k & 3]
-  __shared__ int32_t s_last;
   __shared__ int32_t s_rs[ATTN_SMEM_ROWS + 1];
   __shared__ int32_t s_seq[ATTN_SMEM_ROWS];
 
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   Unit nxt = decode_unit(a, s_unit[1], GP, total_units, rs, seq);
   int cur_cnt = warp_pages(cur, warp);
   int nxt_cnt = warp_pages(nxt, warp);
+  int next_id = 0;  // id of the unit after next, fetched a unit ahead (thread 0)
 
   // page ids of the warp's pages of a unit: lane i holds the i-th
   auto load_pids = [&](const Unit &U, int cnt) -> int {
@@ -328,37 +330,40 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   stage_q(cur, 0);
   stage_q(nxt, 1);
 
+  // ring positions
+  int iss_slot = 0, con_slot = 0;
+  uint32_t con_phase = 0;
+  int inflight = 0;
   // issue pointer: which of (cur, nxt) and which of the warp's pages of it
   int iss_u = 0, iss_i = 0;
-  int issued = 0, consumed = 0;
   bool dead = false;  // a bounded wait gave up: stop streaming, keep the barriers
 
   // one tensor TMA brings the page's 16 K rows and 16 V rows of kv head g
-  auto issue_one = [&](const Unit &U, int pids, int i) {
+  auto issue_one = [&](int g, int pids, int i) {
     const int pid = __shfl_sync(FULL_MASK, pids, i);
     if (lane == 0) {
-      const int slot = issued % NS;
-      uint64_t *bar = &wbars[slot];
+      uint64_t *bar = &wbars[iss_slot];
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, S::STAGE_BYTES);
-      tma_load_5d(ring + slot * S::STAGE_BYTES, &tmap, 0, U.g, 0, 0, layer_page0 + pid, bar,
+      tma_load_5d(ring + iss_slot * S::STAGE_BYTES, &tmap, 0, g, 0, 0, layer_page0 + pid, bar,
                   policy);
     }
-    ++issued;
+    iss_slot = iss_slot + 1 == NS ? 0 : iss_slot + 1;
+    ++inflight;
   };
   auto top_up = [&]() {
     if (dead) return;
-    while (issued - consumed < NS) {
+    while (inflight < NS) {
       if (iss_u == 0) {
         if (iss_i < cur_cnt) {
-          issue_one(cur, pid_cur, iss_i++);
+          issue_one(cur.g, pid_cur, iss_i++);
           continue;
         }
         iss_u = 1;
         iss_i = 0;
       }
       if (iss_i < nxt_cnt) {
-        issue_one(nxt, pid_nxt, iss_i++);
+        issue_one(nxt.g, pid_nxt, iss_i++);
         continue;
       }
       break;
@@ -371,6 +376,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   float m_own, l_own;
 
   while (cur.valid) {
+    if (tid == 0) next_id = atomicAdd(&a.plan->counter, 1);  // used at the epilogue
     top_up();
     // q of the lane's dims for every head of the block, pre-scaled to log2 units
     const int qb_idx = ordinal & 1;
@@ -400,28 +406,28 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
     m_own = ATTN_NEG;
     l_own = 0.0f;
     const int n = cur.n;
+    const int tok_base = cur.p_begin * ATTN_PAGE;
 
     for (int i = 0; i < cur_cnt && !dead; ++i) {
-      const int slot = consumed % NS;
-      const bool landed = mbar_wait(&wbars[slot], (uint32_t)((consumed / NS) & 1));
+      const bool landed = mbar_wait(&wbars[con_slot], con_phase);
       if (!__all_sync(FULL_MASK, landed)) {  // warp-uniform give-up
         dead = true;
         if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
         break;
       }
-      const unsigned char *kst = ring + slot * S::STAGE_BYTES;
+      const unsigned char *kst = ring + con_slot * S::STAGE_BYTES;
       const unsigned char *vst = kst + ATTN_PAGE * S::ROW_BYTES;
-      const int tok0 = (cur.p_begin + warp + i * ATTN_WARPS) * ATTN_PAGE;
+      const int tok0 = tok_base + (warp + i * ATTN_WARPS) * ATTN_PAGE;
       const bool ragged = tok0 + ATTN_PAGE > n;
 
+      // ---- q.k for every batch of the page: x[b][h * T + tt] ----------
+      float x[NB][8];
 #pragma unroll
-      for (int bt = 0; bt < S::BATCHES; ++bt) {
-        const int tb = bt * S::TOK_PER_BATCH + grp * T;  // first token of this lane group
-        // partial q.k over the lane's dims: x[h * T + tt]
-        float x[8];
+      for (int b = 0; b < NB; ++b) {
 #pragma unroll
         for (int tt = 0; tt < T; ++tt) {
-          const uint4 *kr = reinterpret_cast<const uint4 *>(kst + (tb + tt) * S::ROW_BYTES);
+          const int tok = b * S::TOK_PER_BATCH + grp * T + tt;
+          const uint4 *kr = reinterpret_cast<const uint4 *>(kst + tok * S::ROW_BYTES);
           f32x2 k2[NP];
 #pragma unroll
           for (int c = 0; c < NCH; ++c) {
@@ -437,67 +443,75 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
 #pragma unroll
             for (int j = 1; j < NP; ++j) acc = ffma2(q2[h][j], k2[j], acc);
             const float2 r = unpack2(acc);
-            x[h * T + tt] = r.x + r.y;
+            x[b][h * T + tt] = r.x + r.y;
           }
         }
-        // reduce-scatter over the 8 lanes of the group: lane li ends with the
-        // full dot product of value li
+      }
+      // ---- reduce-scatter over the 8 lanes of a group: lane li ends with
+      //      the full dot product of value li, for each batch ------------
+      float s[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
         float y[4], z[2];
-        {
-          const bool up = li & 4;
+        const bool u4 = li & 4, u2 = li & 2, u1 = li & 1;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float send = up ? x[k] : x[k + 4];
-            const float keep = up ? x[k + 4] : x[k];
-            y[k] = keep + __shfl_xor_sync(FULL_MASK, send, 4);
-          }
+        for (int k = 0; k < 4; ++k) {
+          const float send = u4 ? x[b][k] : x[b][k + 4];
+          const float keep = u4 ? x[b][k + 4] : x[b][k];
+          y[k] = keep + __shfl_xor_sync(FULL_MASK, send, 4);
         }
-        {
-          const bool up = li & 2;
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const float send = up ? y[k] : y[k + 2];
-            const float keep = up ? y[k + 2] : y[k];
-            z[k] = keep + __shfl_xor_sync(FULL_MASK, send, 2);
-          }
+        for (int k = 0; k < 2; ++k) {
+          const float send = u2 ? y[k] : y[k + 2];
+          const float keep = u2 ? y[k + 2] : y[k];
+          z[k] = keep + __shfl_xor_sync(FULL_MASK, send, 2);
         }
-        float s;
-        {
-          const bool up = li & 1;
-          const float send = up ? z[0] : z[1];
-          const float keep = up ? z[1] : z[0];
-          s = keep + __shfl_xor_sync(FULL_MASK, send, 1);
+        const float send = u1 ? z[0] : z[1];
+        const float keep = u1 ? z[1] : z[0];
+        s[b] = keep + __shfl_xor_sync(FULL_MASK, send, 1);
+        if (ragged && tok0 + b * S::TOK_PER_BATCH + grp * T + tt_own >= n) s[b] = -INFINITY;
+      }
+      // ---- online softmax with a lazy maximum -------------------------
+      bool need = false;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) need |= s[b] > m_own + ATTN_TAU;
+      if (__any_sync(FULL_MASK, need)) {
+        float bm = s[0];  // maximum of the page for head h_own
+#pragma unroll
+        for (int b = 1; b < NB; ++b) bm = fmaxf(bm, s[b]);
+#pragma unroll
+        for (int off = 1; off < T; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, off));
+        float m_own_new = m_own;
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+          const float mh = __shfl_sync(FULL_MASK, bm, gbase | (h * T));
+          const float mn = fmaxf(m_all[h], mh);
+          const float sc = fast_exp2(m_all[h] - mn);
+          const f32x2 sc2 = pack2(sc, sc);
+#pragma unroll
+          for (int j = 0; j < NP; ++j) o2[h][j] = fmul2(o2[h][j], sc2);
+          m_all[h] = mn;
+          if (h == h_own) m_own_new = mn;
         }
-        if (ragged && tok0 + tb + tt_own >= n) s = -INFINITY;
-        // online softmax with a lazy maximum
-        if (__any_sync(FULL_MASK, s > m_own + ATTN_TAU)) {
-          float bm = s;  // maximum of this batch for head h_own
+        l_own *= fast_exp2(m_own - m_own_new);
+        m_own = m_own_new;
+      }
+      // ---- probabilities, gathered to every lane of the group ----------
+      float pv[NB][8];
 #pragma unroll
-          for (int off = 1; off < T; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, off));
-          float m_own_new = m_own;
+      for (int b = 0; b < NB; ++b) {
+        const float pr = fast_exp2(s[b] - m_own);
+        l_own += pr;
 #pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            const float mh = __shfl_sync(FULL_MASK, bm, gbase | (h * T));
-            const float mn = fmaxf(m_all[h], mh);
-            const float sc = fast_exp2(m_all[h] - mn);
-            const f32x2 sc2 = pack2(sc, sc);
+        for (int v = 0; v < 8; ++v) pv[b][v] = __shfl_sync(FULL_MASK, pr, gbase | v);
+      }
+      // ---- p.v -------------------------------------------------------
 #pragma unroll
-            for (int j = 0; j < NP; ++j) o2[h][j] = fmul2(o2[h][j], sc2);
-            m_all[h] = mn;
-            if (h == h_own) m_own_new = mn;
-          }
-          l_own *= fast_exp2(m_own - m_own_new);
-          m_own = m_own_new;
-        }
-        const float p = fast_exp2(s - m_own);
-        l_own += p;
-        // every lane of the group gets the group's 8 probabilities
-        float pv[8];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) pv[v] = __shfl_sync(FULL_MASK, p, gbase | v);
+      for (int b = 0; b < NB; ++b) {
 #pragma unroll
         for (int tt = 0; tt < T; ++tt) {
-          const uint4 *vr = reinterpret_cast<const uint4 *>(vst + (tb + tt) * S::ROW_BYTES);
+          const int tok = b * S::TOK_PER_BATCH + grp * T + tt;
+          const uint4 *vr = reinterpret_cast<const uint4 *>(vst + tok * S::ROW_BYTES);
           f32x2 v2[NP];
 #pragma unroll
           for (int c = 0; c < NCH; ++c) {
@@ -507,20 +521,22 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
             v2[4 * c + 2] = bf16x2_to_f32x2(w.z);
             v2[4 * c + 3] = bf16x2_to_f32x2(w.w);
           }
-          if (ragged && tok0 + tb + tt >= n) {
+          if (ragged && tok0 + tok >= n) {
             // rows past the end of the sequence may hold any bits
 #pragma unroll
             for (int j = 0; j < NP; ++j) v2[j] = 0ull;
           }
 #pragma unroll
           for (int h = 0; h < GP; ++h) {
-            const f32x2 pp = pack2(pv[h * T + tt], pv[h * T + tt]);
+            const f32x2 pp = pack2(pv[b][h * T + tt], pv[b][h * T + tt]);
 #pragma unroll
             for (int j = 0; j < NP; ++j) o2[h][j] = ffma2(pp, v2[j], o2[h][j]);
           }
         }
       }
-      ++consumed;
+      con_slot = con_slot + 1 == NS ? 0 : con_slot + 1;
+      con_phase ^= (con_slot == 0);
+      --inflight;
       __syncwarp();
       top_up();
     }
@@ -550,7 +566,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
         v.y += __shfl_xor_sync(FULL_MASK, v.y, 16);
         o2[h][j] = pack2(v.x, v.y);
       }
-      m_all[h] = M;
       if (grp == 0 && li == 0) red_ml[warp * GP + h] = make_float2(M, L);
     }
     if (grp == 0) {
@@ -565,11 +580,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
           dst[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
         }
     }
-    // the unit after next: fetched now, read after the barrier
-    if (tid == 0) s_unit[(ordinal + 2) & 3] = atomicAdd(&a.plan->counter, 1);
+    if (tid == 0) s_unit[(ordinal + 2) & 3] = next_id;
     named_barrier_sync();
 
-    // ---- merge the 4 warps; write the output or the split's partial -----
+    // ---- merge the 4 warps into the split's partial (m, l, o) ----------
     const int64_t bh0 = (int64_t)cur.b * Hq + cur.h0;
     for (int idx = tid; idx < cur.nh * D; idx += ATTN_THREADS) {
       const int h = idx / D, d = idx % D;
@@ -584,53 +598,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
         L = fmaf(ml.y, wt, L);
         O = fmaf(red_o[(w * GP + h) * D + d], wt, O);
       }
-      const int64_t bh = bh0 + h;
-      if (cur.nsplit == 1) {
-        store_out(a, bh * D + d, O / L);
-        if (d == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(L)) * LN2;
-      } else {
-        const int64_t ps = bh * a.nsplit_max + cur.split;
-        a.ws_o[ps * D + d] = O;
-        if (d == 0) a.ws_ml[ps] = make_float2(M, L);
-      }
+      const int64_t ps = (bh0 + h) * a.nsplit_max + cur.split;
+      a.ws_o[ps * D + d] = O;
+      if (d == 0) a.ws_ml[ps] = make_float2(M, L);
     }
-    if (cur.nsplit > 1) {
-      // the CTA that completes the last split of (row, head block) folds
-      // the partials in split order
-      __threadfence();
-      named_barrier_sync();
-      if (tid == 0) {
-        const int HB = a.num_kv_heads * a.qblocks;
-        int32_t *ticket = a.tickets + (int64_t)cur.b * HB + cur.g * a.qblocks + cur.qb;
-        const int done = atomicAdd(ticket, 1);
-        s_last = (done == cur.nsplit - 1);
-        if (s_last) *ticket = 0;
-      }
-      named_barrier_sync();
-      if (s_last) {
-        __threadfence();
-        for (int idx = tid; idx < cur.nh * D; idx += ATTN_THREADS) {
-          const int h = idx / D, d = idx % D;
-          const int64_t bh = bh0 + h;
-          const float2 *ml = a.ws_ml + bh * a.nsplit_max;
-          const float *po = a.ws_o + bh * a.nsplit_max * D + d;
-          float M = ATTN_NEG;
-#pragma unroll 8
-          for (int s = 0; s < cur.nsplit; ++s) M = fmaxf(M, __ldcg(ml + s).x);
-          float L = 0.0f, O = 0.0f;
-#pragma unroll 8
-          for (int s = 0; s < cur.nsplit; ++s) {
-            const float2 v = __ldcg(ml + s);
-            const float wt = fast_exp2(v.x - M);
-            L = fmaf(v.y, wt, L);
-            O = fmaf(__ldcg(po + (int64_t)s * D), wt, O);
-          }
-          store_out(a, bh * D + d, O / L);
-          if (d == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(L)) * LN2;
-        }
-      }
-    }
-    // rotate units; the barrier also protects red_o / red_ml for the next merge
+    // rotate units; the barrier also protects red_o / red_ml
     named_barrier_sync();
     ++ordinal;
     cur = nxt;
@@ -648,9 +620,42 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   }
   if (dead) {
     // let the copies still in flight land before the CTA's shared memory goes
-    for (int k = consumed; k < issued; ++k)
-      (void)mbar_wait(&wbars[k % NS], (uint32_t)((k / NS) & 1), 100000000ull);
+    for (int k = 0; k < inflight; ++k) {
+      (void)mbar_wait(&wbars[con_slot], con_phase, 100000000ull);
+      con_slot = con_slot + 1 == NS ? 0 : con_slot + 1;
+      con_phase ^= (con_slot == 0);
+    }
   }
+}
+
+// Fold each active row's split partials in split order: out = sum_s w_s o_s
+// / sum_s w_s l_s with w_s = 2^(m_s - max m).  One CTA per (row, q head).
+template <int D>
+__global__ void __launch_bounds__(D) attn_merge_kernel(const AttnArgs a) {
+  const int h = blockIdx.x;
+  const int b = blockIdx.y;
+  const int d = threadIdx.x;
+  if (!a.active[b]) return;
+  const int n = a.seq_lens[b];
+  if (n < 1 || (int64_t)n > (int64_t)a.max_pages * ATTN_PAGE) return;
+  const int npages = (n + ATTN_PAGE - 1) / ATTN_PAGE;
+  const int nsplit = (npages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT;
+  const int64_t bh = (int64_t)b * a.num_qo_heads + h;
+  const float2 *ml = a.ws_ml + bh * a.nsplit_max;
+  const float *po = a.ws_o + bh * a.nsplit_max * D + d;
+  float M = ATTN_NEG;
+#pragma unroll 8
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[s].x);
+  float L = 0.0f, O = 0.0f;
+#pragma unroll 8
+  for (int s = 0; s < nsplit; ++s) {
+    const float2 v = ml[s];
+    const float w = fast_exp2(v.x - M);
+    L = fmaf(v.y, w, L);
+    O = fmaf(po[(int64_t)s * D], w, O);
+  }
+  store_out(a, bh * D + d, O / L);
+  if (d == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(L)) * LN2;
 }
 
 // q heads per CTA: the group rounded up to 2 / 4 / 8, at most 4 for
@@ -687,6 +692,9 @@ static int launch_attn(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t 
   int rc = launch_status();
   if (rc != PKV_OK) return rc;
   kern<<<grid, ATTN_THREADS, S::SMEM_BYTES, st>>>(a, tmap);
+  rc = launch_status();
+  if (rc != PKV_OK) return rc;
+  attn_merge_kernel<D><<<dim3((unsigned)a.num_qo_heads, (unsigned)a.batch), D, 0, st>>>(a);
   return launch_status();
 }
 
@@ -740,7 +748,7 @@ static size_t nsplit_for(int max_pages) {
 }
 
 struct WsLayout {
-  size_t o, ml, row_start, tickets, plan, total;
+  size_t o, ml, row_start, plan, total;
 };
 
 static WsLayout ws_layout(int batch, int num_qo_heads, int head_dim, int max_pages) {
@@ -749,8 +757,7 @@ static WsLayout ws_layout(int batch, int num_qo_heads, int head_dim, int max_pag
   w.o = 0;
   w.ml = align_up(units * head_dim * sizeof(float), 256);
   w.row_start = w.ml + align_up(units * sizeof(float2), 256);
-  w.tickets = w.row_start + align_up((size_t)(batch + 1) * sizeof(int32_t), 256);
-  w.plan = w.tickets + align_up((size_t)batch * num_qo_heads * sizeof(int32_t), 256);
+  w.plan = w.row_start + align_up((size_t)(batch + 1) * sizeof(int32_t), 256);
   w.total = w.plan + 256;
   return w;
 }
@@ -819,7 +826,6 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
   a.ws_o = reinterpret_cast<float *>(ws + wl.o);
   a.ws_ml = reinterpret_cast<float2 *>(ws + wl.ml);
   a.row_start = reinterpret_cast<int32_t *>(ws + wl.row_start);
-  a.tickets = reinterpret_cast<int32_t *>(ws + wl.tickets);
   a.plan = reinterpret_cast<PlanHeader *>(ws + wl.plan);
   a.err = err_word;
   a.layer = layer;

@@ -115,10 +115,10 @@ class DecodeStep:
             self.frame(stream=st)
 
     def launches_per_step(self) -> int:
-        """Kernel launches of one run(): per layer append 1 + attention 2
-        (planner + persistent kernel); sampler 2; frame 1."""
+        """Kernel launches of one run(): per layer append 1 + attention 3
+        (planner, persistent kernel, split merge); sampler 2; frame 1."""
         L = self.t.layers
-        n = L * 3
+        n = L * 4
         if self.t.logits is not None:
             n += 2
         if self.t.base is not None:
