@@ -150,6 +150,42 @@ int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
                           size_t workspace_bytes, int32_t *err_word,
                           void *stream);
 
+/* ------------------------------------------------------------------------
+ * pkv_paged_decode_attn_static -- pkv_paged_decode_attn for callers that
+ * cannot hand the library any device scratch.  (The source pages have no
+ * counterpart: this is an addition of this library.)
+ *
+ * Some hosts can pass device pointers for their own tensors but have no
+ * device allocator to offer -- a plugin inside another framework, a foreign
+ * language runtime, or a serving engine that reserves all device memory at
+ * start-up and allows no allocation afterwards.  This entry point takes the
+ * same arguments as pkv_paged_decode_attn minus the workspace and uses a
+ * scratch array of PKV_ATTN_STATIC_SCRATCH_BYTES that the library keeps in
+ * device memory (a file-scope __device__ array: every GPU that loads the
+ * library holds it until the process exits).  It allocates and frees
+ * nothing.
+ *
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current) and remembers it;
+ *     make that first call before any stream capture begins.
+ *   - Problems whose pkv_decode_workspace_bytes(...) exceeds
+ *     PKV_ATTN_STATIC_SCRATCH_BYTES are rejected with PKV_ERR_WORKSPACE
+ *     before anything is launched.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero): calls that can overlap on the
+ *     GPU (other streams, other host threads) race on it; serialise them.
+ * Results are those of pkv_paged_decode_attn on the same inputs.
+ * ---------------------------------------------------------------------- */
+#define PKV_ATTN_STATIC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+
+int pkv_paged_decode_attn_static(const pkv_cache_t *geom, const void *cache,
+                                 int layer, const void *q, int num_qo_heads,
+                                 float sm_scale, const int32_t *page_table,
+                                 int max_pages, const int32_t *seq_lens,
+                                 const int32_t *active, int batch, void *out,
+                                 int out_fp32, float *lse, int32_t *err_word,
+                                 void *stream);
+
 /* Workspace (bytes) pkv_seeded_sample needs for these sizes. */
 size_t pkv_sample_workspace_bytes(int batch, int vocab);
 

@@ -12,7 +12,7 @@ does, and raises if it is missing.
 
 _BINDING = (
     "load", "library_path", "version", "error_string", "PkvError",
-    "kv_append", "paged_decode_attn", "decode_workspace_bytes",
+    "kv_append", "paged_decode_attn", "decode_workspace_bytes", "paged_decode_attn_static",
     "seeded_sample", "sample_workspace_bytes",
     "codebook_frame_sample", "frame_workspace_bytes",
     "KIND_OTHER", "KIND_AUDIO", "KIND_STOP",

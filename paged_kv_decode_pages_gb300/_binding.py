@@ -36,6 +36,8 @@ SIGNATURES = {
     "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_paged_decode_attn": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _I, _F, _P, _I, _P,
                                    _P, _I, _P, _I, _P, _P, _SZ, _P, _P]),
+    "pkv_paged_decode_attn_static": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _I, _F, _P,
+                                          _I, _P, _P, _I, _P, _I, _P, _P, _P]),
     "pkv_sample_workspace_bytes": (_SZ, [_I, _I]),
     "pkv_seeded_sample": (_I, [_P, _I64, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _U32, _I, _P,
                                _I, _I32, _I32, _P, _P, _P, _SZ, _P, _P]),
@@ -163,6 +165,32 @@ def paged_decode_attn(cache, layer, q, page_table, seq_lens, active, out, worksp
         int(out.dtype == torch.float32), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(err_word),
         _stream(stream))
     _check("pkv_paged_decode_attn", st)
+
+
+STATIC_SCRATCH_BYTES = 32 << 20  # PKV_ATTN_STATIC_SCRATCH_BYTES
+
+
+def paged_decode_attn_static(cache, layer, q, page_table, seq_lens, active, out, lse=None,
+                             sm_scale=None, err_word=None, stream=None):
+    """pkv_paged_decode_attn_static: the same attention with the library's
+    own device scratch, for callers that have no device memory to lend."""
+    import torch
+    _req(cache, torch.bfloat16, "cache")
+    _req(q, torch.bfloat16, "q")
+    _req(page_table, torch.int32, "page_table")
+    _req(seq_lens, torch.int32, "seq_lens")
+    _req(active, torch.int32, "active")
+    if out.dtype not in (torch.bfloat16, torch.float32) or not out.is_contiguous():
+        raise TypeError("out must be a contiguous bf16 or fp32 tensor")
+    g = _geom(cache)
+    B, Hq, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / (D ** 0.5)
+    st = load().pkv_paged_decode_attn_static(
+        ctypes.byref(g), _ptr(cache), int(layer), _ptr(q), Hq, float(sm_scale), _ptr(page_table),
+        page_table.shape[1], _ptr(seq_lens), _ptr(active), B, _ptr(out),
+        int(out.dtype == torch.float32), _ptr(lse), _ptr(err_word), _stream(stream))
+    _check("pkv_paged_decode_attn_static", st)
 
 
 def sample_workspace_bytes(batch, vocab) -> int:

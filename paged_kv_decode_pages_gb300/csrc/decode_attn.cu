@@ -836,3 +836,56 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return D == 128 ? dispatch_gp<128>(a, tmap, s) : dispatch_gp<64>(a, tmap, s);
 }
+
+// ---------------------------------------------------------------------------
+// Static-scratch variant: the same kernels, with their scratch in a
+// file-scope device array instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+namespace pkv {
+
+// Every device that loads the library holds this array until the process
+// exits.  The kernels need nothing in it to start at zero: the planner
+// rewrites the split table and the unit counter on every call and each
+// partial is written before it is read.
+static __device__ __align__(256) unsigned char g_attn_scratch[PKV_ATTN_STATIC_SCRATCH_BYTES];
+
+constexpr int MAX_DEVICES = 64;
+static void *g_scratch_addr[MAX_DEVICES];  // device address of g_attn_scratch, per device
+
+// Device address of the array on the current device, looked up once per
+// device (the host-side name is only a stand-in for it).
+static int static_scratch_address(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 0 || dev >= MAX_DEVICES) return PKV_ERR_UNSUPPORTED;
+  if (g_scratch_addr[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || ptr == nullptr)
+      return PKV_ERR_CUDA;
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return PKV_OK;
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_paged_decode_attn_static(const pkv_cache_t *geom, const void *cache, int layer,
+                                            const void *q, int num_qo_heads, float sm_scale,
+                                            const int32_t *page_table, int max_pages,
+                                            const int32_t *seq_lens, const int32_t *active,
+                                            int batch, void *out, int out_fp32, float *lse,
+                                            int32_t *err_word, void *stream) {
+  using namespace pkv;
+  if (geom == nullptr) return PKV_ERR_INVALID_ARG;
+  const size_t need =
+      pkv_decode_workspace_bytes(batch, num_qo_heads, geom->head_dim, max_pages, geom->page_size);
+  if (need == 0) return PKV_ERR_INVALID_ARG;
+  if (need > (size_t)PKV_ATTN_STATIC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  const int st = static_scratch_address(&scratch);
+  if (st != PKV_OK) return st;
+  return pkv_paged_decode_attn(geom, cache, layer, q, num_qo_heads, sm_scale, page_table,
+                               max_pages, seq_lens, active, batch, out, out_fp32, lse, scratch,
+                               (size_t)PKV_ATTN_STATIC_SCRATCH_BYTES, err_word, stream);
+}
