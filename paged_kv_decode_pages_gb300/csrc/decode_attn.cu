@@ -117,6 +117,7 @@ __device__ __forceinline__ int row_splits(const AttnArgs &a, int b, bool *bad) {
 __global__ void __launch_bounds__(PLAN_THREADS) attn_plan_kernel(const AttnArgs a) {
   __shared__ int32_t scan[PLAN_THREADS];
   __shared__ int32_t carry;
+  pdl_wait();
   const int tid = threadIdx.x;
   const int D = a.head_dim;
   const int HB = a.num_kv_heads * a.qblocks;
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) attn_plan_kernel(const AttnArgs 
       for (int h = lane; h < a.num_qo_heads; h += 32)
         a.lse[(int64_t)b * a.num_qo_heads + h] = -INFINITY;
   }
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -279,6 +281,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
     }
     fence_barrier_init();
   }
+  pdl_wait();     // the planner's table and counter
+  pdl_trigger();  // the merge kernel may queue behind this grid now
   if (tid == 0) {
     s_unit[0] = atomicAdd(&a.plan->counter, 1);
     s_unit[1] = atomicAdd(&a.plan->counter, 1);
@@ -628,13 +632,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   }
 }
 
-// Fold each active row's split partials in split order: out = sum_s w_s o_s
-// / sum_s w_s l_s with w_s = 2^(m_s - max m).  One CTA per (row, q head).
+// Fold each active row's split partials: out = sum_s w_s o_s / sum_s w_s l_s
+// with w_s = 2^(m_s - max m).  One CTA per (row, q head); its 4 warps take
+// every 4th split (a fixed assignment, so the result is deterministic), each
+// lane a float vector of dims, folding with a running maximum; the 4 warps
+// then combine through shared memory.
 template <int D>
-__global__ void __launch_bounds__(D) attn_merge_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(ATTN_THREADS) attn_merge_kernel(const AttnArgs a) {
+  constexpr int VEC = D / 32;  // dims per lane
+  __shared__ float s_m[ATTN_WARPS], s_l[ATTN_WARPS];
+  __shared__ __align__(16) float s_o[ATTN_WARPS][D];
   const int h = blockIdx.x;
   const int b = blockIdx.y;
-  const int d = threadIdx.x;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();  // the partials of the persistent kernel
   if (!a.active[b]) return;
   const int n = a.seq_lens[b];
   if (n < 1 || (int64_t)n > (int64_t)a.max_pages * ATTN_PAGE) return;
@@ -642,20 +653,49 @@ __global__ void __launch_bounds__(D) attn_merge_kernel(const AttnArgs a) {
   const int nsplit = (npages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT;
   const int64_t bh = (int64_t)b * a.num_qo_heads + h;
   const float2 *ml = a.ws_ml + bh * a.nsplit_max;
-  const float *po = a.ws_o + bh * a.nsplit_max * D + d;
-  float M = ATTN_NEG;
-#pragma unroll 8
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[s].x);
-  float L = 0.0f, O = 0.0f;
-#pragma unroll 8
-  for (int s = 0; s < nsplit; ++s) {
+  const float *po = a.ws_o + bh * a.nsplit_max * D + lane * VEC;
+  float M = ATTN_NEG, L = 0.0f, O[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) O[e] = 0.0f;
+#pragma unroll 4
+  for (int s = w; s < nsplit; s += ATTN_WARPS) {
     const float2 v = ml[s];
-    const float w = fast_exp2(v.x - M);
-    L = fmaf(v.y, w, L);
-    O = fmaf(po[(int64_t)s * D], w, O);
+    float o[VEC];
+    if constexpr (VEC == 4) {
+      const float4 t = *reinterpret_cast<const float4 *>(po + (int64_t)s * D);
+      o[0] = t.x, o[1] = t.y, o[2] = t.z, o[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2 *>(po + (int64_t)s * D);
+      o[0] = t.x, o[1] = t.y;
+    }
+    const float mn = fmaxf(M, v.x);
+    const float sc = fast_exp2(M - mn), wt = fast_exp2(v.x - mn);
+    L = fmaf(L, sc, v.y * wt);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) O[e] = fmaf(O[e], sc, o[e] * wt);
+    M = mn;
   }
-  store_out(a, bh * D + d, O / L);
-  if (d == 0 && a.lse != nullptr) a.lse[bh] = (M + log2f(L)) * LN2;
+  if (lane == 0) {
+    s_m[w] = M;
+    s_l[w] = L;
+  }
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) s_o[w][lane * VEC + e] = O[e];
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += ATTN_THREADS) {
+    float Mx = ATTN_NEG;
+#pragma unroll
+    for (int k = 0; k < ATTN_WARPS; ++k) Mx = fmaxf(Mx, s_m[k]);
+    float Lt = 0.0f, Ot = 0.0f;
+#pragma unroll
+    for (int k = 0; k < ATTN_WARPS; ++k) {
+      const float wt = fast_exp2(s_m[k] - Mx);
+      Lt = fmaf(s_l[k], wt, Lt);
+      Ot = fmaf(s_o[k][d], wt, Ot);
+    }
+    store_out(a, bh * D + d, Ot / Lt);
+    if (d == 0 && a.lse != nullptr) a.lse[bh] = (Mx + log2f(Lt)) * LN2;
+  }
 }
 
 // q heads per CTA: the group rounded up to 2 / 4 / 8, at most 4 for
@@ -688,13 +728,13 @@ static int launch_attn(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t 
     if (per_sm < 1) return PKV_ERR_UNSUPPORTED;
     grid = sms * per_sm;
   }
-  attn_plan_kernel<<<1, PLAN_THREADS, 0, st>>>(a);
-  int rc = launch_status();
-  if (rc != PKV_OK) return rc;
-  kern<<<grid, ATTN_THREADS, S::SMEM_BYTES, st>>>(a, tmap);
-  rc = launch_status();
-  if (rc != PKV_OK) return rc;
-  attn_merge_kernel<D><<<dim3((unsigned)a.num_qo_heads, (unsigned)a.batch), D, 0, st>>>(a);
+  if (launch_pdl(attn_plan_kernel, dim3(1), dim3(PLAN_THREADS), 0, st, a) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (launch_pdl(kern, dim3(grid), dim3(ATTN_THREADS), S::SMEM_BYTES, st, a, tmap) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (launch_pdl(attn_merge_kernel<D>, dim3((unsigned)a.num_qo_heads, (unsigned)a.batch),
+                 dim3(ATTN_THREADS), 0, st, a) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return launch_status();
 }
 

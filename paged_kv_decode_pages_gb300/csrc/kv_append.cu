@@ -31,6 +31,7 @@ struct AppendArgs {
 };
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
+  pdl_wait();
   const int64_t total = (int64_t)a.batch * 2 * a.row_chunks;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -98,6 +99,8 @@ extern "C" int pkv_kv_append(const pkv_cache_t *geom, void *cache, int layer, co
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 4096) blocks = 4096;
-  kv_append_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (launch_pdl(kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                 static_cast<cudaStream_t>(stream), a) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return launch_status();
 }

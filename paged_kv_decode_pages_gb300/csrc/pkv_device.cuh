@@ -24,6 +24,18 @@ __device__ __forceinline__ void report(int32_t *err, int bits) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor on the stream has finished;
+// pdl_wait() blocks until the predecessor's grid has completed and its
+// memory is visible (a no-op for a normal launch), pdl_trigger() lets the
+// next kernel on the stream start launching.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // shared-memory addresses, mbarriers, bulk async copies
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
