@@ -242,6 +242,9 @@ __device__ void select_bin(SampSmem &sm, int shift) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     // lane covers bins 255-8*lane .. 248-8*lane (descending)
+    // every lane reads the wanted rank before the scan below (a warp-wide
+    // sync point), as one lane overwrites it afterwards
+    const uint32_t want = sm.sel_want;
     uint32_t c[8];
     uint32_t tot = 0;
 #pragma unroll
@@ -256,7 +259,6 @@ __device__ void select_bin(SampSmem &sm, int shift) {
       if (lane >= off) incl += o;
     }
     const uint32_t excl = incl - tot;
-    const uint32_t want = sm.sel_want;
     const bool mine = excl < want && want <= incl;
     if (mine) {
       uint32_t above = excl;
