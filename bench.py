@@ -406,7 +406,8 @@ def main(argv=None):
                  "bytes_per_layer": sizes["attn_per_layer"]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": attn_traffic(cfg.name),
-                     "kernel": "pkv_paged_decode_attn (split + merge kernels), per layer",
+                     "kernel": "pkv_paged_decode_attn (planner, persistent split kernel, merge "
+                               "kernel), per layer",
                      "peak_source": peak_src},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
