@@ -8,8 +8,10 @@
 //    a unit is one (row, split, kv head, q-head block).  The split size does
 //    not depend on the batch, so a row's result depends on its inputs only.
 //  * a one-CTA planner lists the splits of the active rows (prefix sums over
-//    the rows), zeroes the outputs of padding rows and resets the scheduling
-//    counter, so the launch shapes stay static.
+//    the rows) and resets the scheduling counter, so the launch shapes stay
+//    static.  It reads only lengths and flags, which no kernel of this
+//    library writes, so it does its work while its predecessor (the KV
+//    append) still runs and waits for that predecessor only at its end.
 //  * a persistent grid (SMs x resident CTAs) pulls units from an atomic
 //    counter.  Each of a CTA's 4 warps streams its pages of the unit
 //    (round-robin) through its own ring of NS shared-memory stages; a stage
@@ -30,7 +32,8 @@
 //    work per warp between the shuffle steps).
 //  * per unit, the 4 lane groups of a warp merge with shuffles and the 4
 //    warps through shared memory into one (m, l, o) partial; a merge kernel
-//    then folds each row's partials in split order.  No fences, tickets or
+//    then folds each row's partials in split order and writes the zeros of
+//    padding rows.  No fences, tickets or
 //    blocking atomics sit in the streaming loop: the next unit's id is
 //    fetched one unit ahead.
 #include <math.h>
@@ -117,9 +120,10 @@ __device__ __forceinline__ int row_splits(const AttnArgs &a, int b, bool *bad) {
 __global__ void __launch_bounds__(PLAN_THREADS) attn_plan_kernel(const AttnArgs a) {
   __shared__ int32_t scan[PLAN_THREADS];
   __shared__ int32_t carry;
-  pdl_wait();
+  // the persistent kernel may launch and set up now; it waits for this grid
+  // to complete before it reads the table
+  pdl_trigger();
   const int tid = threadIdx.x;
-  const int D = a.head_dim;
   const int HB = a.num_kv_heads * a.qblocks;
   if (tid == 0) carry = 0;
   __syncthreads();
@@ -151,18 +155,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) attn_plan_kernel(const AttnArgs 
     a.plan->total_splits = carry;
     a.plan->total_units = carry * HB;
   }
-  __syncthreads();
-  // padding or rejected rows (no split): zeros, lse = -inf; one warp per row
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int b = warp; b < a.batch; b += PLAN_THREADS / 32) {
-    if (a.row_start[b + 1] != a.row_start[b]) continue;
-    const int64_t base = (int64_t)b * a.num_qo_heads * D;
-    for (int i = lane; i < a.num_qo_heads * D; i += 32) store_out(a, base + i, 0.0f);
-    if (a.lse != nullptr)
-      for (int h = lane; h < a.num_qo_heads; h += 32)
-        a.lse[(int64_t)b * a.num_qo_heads + h] = -INFINITY;
-  }
-  pdl_trigger();
+  // completes only after the predecessor has: the persistent kernel, which
+  // waits for this grid, then sees the predecessor's cache writes too
+  pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -635,45 +630,70 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
 // Fold each active row's split partials: out = sum_s w_s o_s / sum_s w_s l_s
 // with w_s = 2^(m_s - max m).  One CTA per (row, q head); its 4 warps take
 // every 4th split (a fixed assignment, so the result is deterministic), each
-// lane a float vector of dims, folding with a running maximum; the 4 warps
-// then combine through shared memory.
+// lane a float vector of dims.  A warp issues the loads of up to 16 of its
+// splits at once and folds them with one rescale; the 4 warps then combine
+// through shared memory.  Padding and rejected rows get zeros and
+// lse = -inf.
 template <int D>
 __global__ void __launch_bounds__(ATTN_THREADS) attn_merge_kernel(const AttnArgs a) {
   constexpr int VEC = D / 32;  // dims per lane
+  constexpr int BLK = 16;      // splits in flight per warp
   __shared__ float s_m[ATTN_WARPS], s_l[ATTN_WARPS];
   __shared__ __align__(16) float s_o[ATTN_WARPS][D];
   const int h = blockIdx.x;
   const int b = blockIdx.y;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();  // the partials of the persistent kernel
-  if (!a.active[b]) return;
+  pdl_trigger();
+  const int64_t bh = (int64_t)b * a.num_qo_heads + h;
   const int n = a.seq_lens[b];
-  if (n < 1 || (int64_t)n > (int64_t)a.max_pages * ATTN_PAGE) return;
+  if (!a.active[b] || n < 1 || (int64_t)n > (int64_t)a.max_pages * ATTN_PAGE) {
+    for (int d = threadIdx.x; d < D; d += ATTN_THREADS) store_out(a, bh * D + d, 0.0f);
+    if (threadIdx.x == 0 && a.lse != nullptr) a.lse[bh] = -INFINITY;
+    return;
+  }
   const int npages = (n + ATTN_PAGE - 1) / ATTN_PAGE;
   const int nsplit = (npages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT;
-  const int64_t bh = (int64_t)b * a.num_qo_heads + h;
   const float2 *ml = a.ws_ml + bh * a.nsplit_max;
   const float *po = a.ws_o + bh * a.nsplit_max * D + lane * VEC;
   float M = ATTN_NEG, L = 0.0f, O[VEC];
 #pragma unroll
   for (int e = 0; e < VEC; ++e) O[e] = 0.0f;
-#pragma unroll 4
-  for (int s = w; s < nsplit; s += ATTN_WARPS) {
-    const float2 v = ml[s];
-    float o[VEC];
-    if constexpr (VEC == 4) {
-      const float4 t = *reinterpret_cast<const float4 *>(po + (int64_t)s * D);
-      o[0] = t.x, o[1] = t.y, o[2] = t.z, o[3] = t.w;
-    } else {
-      const float2 t = *reinterpret_cast<const float2 *>(po + (int64_t)s * D);
-      o[0] = t.x, o[1] = t.y;
-    }
-    const float mn = fmaxf(M, v.x);
-    const float sc = fast_exp2(M - mn), wt = fast_exp2(v.x - mn);
-    L = fmaf(L, sc, v.y * wt);
+  for (int s0 = w; s0 < nsplit; s0 += ATTN_WARPS * BLK) {
+    float2 v[BLK];
+    float o[BLK][VEC];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) O[e] = fmaf(O[e], sc, o[e] * wt);
-    M = mn;
+    for (int k = 0; k < BLK; ++k) {
+      const int s = s0 + k * ATTN_WARPS;
+      v[k] = make_float2(ATTN_NEG, 0.0f);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) o[k][e] = 0.0f;
+      if (s < nsplit) {
+        v[k] = ml[s];
+        if constexpr (VEC == 4) {
+          const float4 t = *reinterpret_cast<const float4 *>(po + (int64_t)s * D);
+          o[k][0] = t.x, o[k][1] = t.y, o[k][2] = t.z, o[k][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2 *>(po + (int64_t)s * D);
+          o[k][0] = t.x, o[k][1] = t.y;
+        }
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int k = 0; k < BLK; ++k) mb = fmaxf(mb, v[k].x);
+    const float sc = fast_exp2(M - mb);
+    L *= sc;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) O[e] *= sc;
+#pragma unroll
+    for (int k = 0; k < BLK; ++k) {
+      const float wt = fast_exp2(v[k].x - mb);
+      L = fmaf(v[k].y, wt, L);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) O[e] = fmaf(o[k][e], wt, O[e]);
+    }
+    M = mb;
   }
   if (lane == 0) {
     s_m[w] = M;

@@ -32,6 +32,7 @@ struct AppendArgs {
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
   pdl_wait();
+  pdl_trigger();  // the next kernel waits for this grid before reading the cache
   const int64_t total = (int64_t)a.batch * 2 * a.row_chunks;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
