@@ -395,7 +395,8 @@ def main(argv=None):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "compute": "bf16 in, fp32 accumulate (attention); fp64 sampler decisions",
+        "compute": "bf16 in, fp32 accumulate (attention); sampler decisions in fp64, "
+                   "chunk normalisers in double-float fp32 pairs",
         "data": "synthetic",
         "config": workload_config(cfg, batch, "inputs larger than L2: %.1f GB of KV per step"
                                   % (sizes["kv_per_layer"] * cfg.num_layers / 1e9)),

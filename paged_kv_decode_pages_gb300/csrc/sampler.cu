@@ -21,9 +21,15 @@
 //  * chunk pass (one CTA per 8192-token chunk of a row): chunk maximum;
 //    the chunk's largest composites (its top-k, or 512 for top-p over the
 //    whole vocabulary; radix select over 8-bit digits);
-//    for top-p over the whole vocabulary, the fp64 partial normaliser
-//    sum exp(x - x_chunkmax); for "keep everything", the chunk's Gumbel
-//    argmax.  The chunking depends on the vocabulary only.
+//    for top-p over the whole vocabulary, the partial normaliser
+//    sum exp(x - x_chunkmax) = sum 2^(logit * log2(e) / T - t_chunkmax) in
+//    double-float arithmetic (fp32 pairs): Tang's table-driven exp2 (ACM
+//    TOMS 15(2), 1989) with a double-float table of 2^(j/32) and a degree-4
+//    polynomial, each term within 3e-9 of itself, summed with exact
+//    two-sum corrections -- on this GPU one fp64 warp instruction costs as
+//    much issue time as several dozen fp32 ones, and this is the only
+//    per-logit transcendental of the path; for "keep everything", the
+//    chunk's Gumbel argmax.  The chunking depends on the vocabulary only.
 //  * finish (one CTA per row): merges the chunk records in chunk order,
 //    sorts the candidates, applies top-k / top-p with sequential fp64
 //    prefix sums in sorted order, and takes the Gumbel argmax.  Rows whose
@@ -72,7 +78,128 @@ struct RowParams {
   int K;       // top-k count after normalisation (V when off)
   int mode;
   int nc;      // candidates per chunk
+  float c2h, c2l;  // log2(e) / T as a double-float
 };
+
+// ---------------------------------------------------------------------------
+// double-float arithmetic (Dekker 1971; Knuth TAOCP vol. 2, 4.2.2)
+// ---------------------------------------------------------------------------
+struct DF {
+  float h, l;
+};
+
+// s + e == a + b exactly
+__device__ __forceinline__ DF df_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+// the same for |a| >= |b|
+__device__ __forceinline__ DF df_fast_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = df_two_sum(a.h, b.h);
+  return df_fast_two_sum(s.h, __fadd_rn(s.l, __fadd_rn(a.l, b.l)));
+}
+__device__ __forceinline__ DF df_mul(DF a, DF b) {
+  const float p = __fmul_rn(a.h, b.h);
+  float e = fmaf(a.h, b.h, -p);
+  e = fmaf(a.h, b.l, fmaf(a.l, b.h, e));
+  return df_fast_two_sum(p, e);
+}
+__device__ __forceinline__ DF df_mul_f(DF a, float b) {
+  const float p = __fmul_rn(a.h, b);
+  return df_fast_two_sum(p, fmaf(a.l, b, fmaf(a.h, b, -p)));
+}
+__device__ __forceinline__ DF df_div_f(DF a, float b) {
+  const float q1 = __fdiv_rn(a.h, b);
+  const float r = __fadd_rn(fmaf(-q1, b, a.h), a.l);
+  return df_fast_two_sum(q1, __fdiv_rn(r, b));
+}
+// a < b for normalised double-floats
+__device__ __forceinline__ bool df_lt(DF a, DF b) { return a.h < b.h || (a.h == b.h && a.l < b.l); }
+__device__ __forceinline__ DF df_shfl_xor(DF v, int m) {
+  return {__shfl_xor_sync(FULL_MASK, v.h, m), __shfl_xor_sync(FULL_MASK, v.l, m)};
+}
+__device__ __forceinline__ DF df_shfl_up(DF v, int d) {
+  return {__shfl_up_sync(FULL_MASK, v.h, d), __shfl_up_sync(FULL_MASK, v.l, d)};
+}
+__device__ __forceinline__ DF df_shfl(DF v, int src) {
+  return {__shfl_sync(FULL_MASK, v.h, src), __shfl_sync(FULL_MASK, v.l, src)};
+}
+
+// log2(e) and ln(2) as double-floats
+constexpr float LOG2E_H = 0x1.715476p+0f, LOG2E_L = 0x1.4ae0c0p-26f;
+constexpr float LN2_H = 0x1.62e430p-1f, LN2_L = -0x1.05c610p-29f;
+
+// 2^(j/32), j = 0..31, split into an fp32 value and an fp32 correction
+// (each pair is within 4e-15 of 2^(j/32))
+__constant__ float c_exp2_tab_h[32] = {
+    0x1.000000p+0f, 0x1.059b0ep+0f, 0x1.0b5586p+0f, 0x1.11301ep+0f, 0x1.172b84p+0f,
+    0x1.1d4874p+0f, 0x1.2387a6p+0f, 0x1.29e9e0p+0f, 0x1.306fe0p+0f, 0x1.371a74p+0f,
+    0x1.3dea64p+0f, 0x1.44e086p+0f, 0x1.4bfdaep+0f, 0x1.5342b6p+0f, 0x1.5ab07ep+0f,
+    0x1.6247ecp+0f, 0x1.6a09e6p+0f, 0x1.71f75ep+0f, 0x1.7a1148p+0f, 0x1.82589ap+0f,
+    0x1.8ace54p+0f, 0x1.93737cp+0f, 0x1.9c4918p+0f, 0x1.a5503cp+0f, 0x1.ae89fap+0f,
+    0x1.b7f770p+0f, 0x1.c199bep+0f, 0x1.cb720ep+0f, 0x1.d5818ep+0f, 0x1.dfc974p+0f,
+    0x1.ea4afap+0f, 0x1.f50766p+0f};
+__constant__ float c_exp2_tab_l[32] = {
+    0.0f,             -0x1.9d4f52p-25f, 0x1.9f3122p-25f,  -0x1.fdb496p-25f, -0x1.c15742p-27f,
+    -0x1.d2e8cap-25f, 0x1.ceac48p-25f,  -0x1.5c0424p-25f, 0x1.4636e2p-25f,  -0x1.18aac6p-25f,
+    0x1.824684p-25f,  0x1.8624b4p-30f,  -0x1.593abcp-25f, -0x1.2c5610p-25f, -0x1.5bd5ecp-27f,
+    -0x1.f8b550p-25f, 0x1.9fcef4p-26f,  0x1.1d8beep-25f,  -0x1.829fd0p-25f, -0x1.accc7cp-26f,
+    0x1.15506ep-27f,  -0x1.e64744p-25f, 0x1.51f848p-27f,  -0x1.b83b54p-25f, -0x1.a94b14p-26f,
+    -0x1.a09438p-25f, -0x1.3d56b2p-27f, -0x1.8837ccp-27f, -0x1.822dbcp-27f, -0x1.908c94p-25f,
+    0x1.52486cp-27f,  -0x1.246eb0p-26f};
+
+// t = v * c2 - tm <= ~0 with c2, tm double-floats
+struct Exp2Ctx {
+  float c2h, c2l, th, tl;
+};
+
+__device__ __forceinline__ Exp2Ctx exp2_ctx(const RowParams &P, float vmax) {
+  const DF tm = df_mul_f(DF{P.c2h, P.c2l}, vmax);
+  return {P.c2h, P.c2l, tm.h, tm.l};
+}
+
+// 2^(v * c2 - tm) as a normalised double-float; 0 below 2^-125 and for a
+// -inf v (whose products give NaN and fail the range test).
+__device__ __forceinline__ DF df_exp2_rel(float v, const Exp2Ctx &c, const float *tab_h,
+                                          const float *tab_l) {
+  // v * c2 = ph + pl
+  const float ph = __fmul_rn(v, c.c2h);
+  const float pl = fmaf(v, c.c2l, fmaf(v, c.c2h, -ph));
+  // t = s.h + tlow
+  const DF s = df_two_sum(ph, -c.th);
+  const float tlow = __fsub_rn(__fadd_rn(s.l, pl), c.tl);
+  if (!(s.h > -125.0f)) return {0.0f, 0.0f};
+  // n = rint(32 s.h) = 32 k + j; s.h - n / 32 is exact
+  const float y = fmaf(s.h, 32.0f, 12582912.0f);
+  const int n = __float_as_int(y) - 0x4B400000;
+  const float g = fmaf(__fsub_rn(y, 12582912.0f), -0.03125f, s.h);
+  const float r = __fadd_rn(g, tlow);
+  // 2^r - 1 = u + u^2/2 + u^3/6 + u^4/24, u = r ln 2, |u| < 0.011
+  const float u = fmaf(r, LN2_H, __fmul_rn(r, LN2_L));
+  float q = fmaf(u, 1.0f / 24.0f, 1.0f / 6.0f);
+  q = fmaf(q, u, 0.5f);
+  q = fmaf(q, u, 1.0f);
+  q = __fmul_rn(q, u);
+  const int j = n & 31, k = n >> 5;
+  const float t0 = tab_h[j];
+  const DF e = df_fast_two_sum(t0, fmaf(t0, q, tab_l[j]));
+  const float sc = __int_as_float((k + 127) << 23);  // 2^k, k in [-125, 0]
+  return {__fmul_rn(e.h, sc), __fmul_rn(e.l, sc)};
+}
+
+// acc += e, keeping the exact rounding error of the high parts
+__device__ __forceinline__ void df_accumulate(DF &acc, DF e) {
+  const DF s = df_two_sum(acc.h, e.h);
+  acc.h = s.h;
+  acc.l = __fadd_rn(acc.l, __fadd_rn(s.l, e.l));
+}
+
 
 // ---------------------------------------------------------------------------
 // Philox4x64-10 and Gumbel noise
@@ -137,6 +264,8 @@ __device__ __forceinline__ double comp_x(uint64_t c, float temperature) {
 // shared scratch
 // ---------------------------------------------------------------------------
 struct SampSmem {
+  float e2h[32], e2l[32];  // the 2^(j/32) table
+  float wh[SB / 32], wl[SB / 32];
   uint32_t hist[256];
   uint64_t red_u64[SB / 32];
   double red_d[SB];
@@ -185,6 +314,31 @@ __device__ double block_sum_d(double v, SampSmem &sm) {
   const double r = sm.red_d[0];
   __syncthreads();
   return r;
+}
+
+// Double-float sum in a fixed order (xor tree in each warp, then the warps
+// in order); every thread gets the result.
+__device__ DF block_sum_df(DF v, SampSmem &sm) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v = df_add(v, df_shfl_xor(v, off));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    sm.wh[threadIdx.x >> 5] = v.h;
+    sm.wl[threadIdx.x >> 5] = v.l;
+  }
+  __syncthreads();
+  DF r = {sm.wh[0], sm.wl[0]};
+#pragma unroll
+  for (int w = 1; w < SB / 32; ++w) r = df_add(r, DF{sm.wh[w], sm.wl[w]});
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ void load_exp2_table(SampSmem &sm) {
+  if (threadIdx.x < 32) {
+    sm.e2h[threadIdx.x] = c_exp2_tab_h[threadIdx.x];
+    sm.e2l[threadIdx.x] = c_exp2_tab_l[threadIdx.x];
+  }
 }
 
 // Argmax of (score desc, id asc); ids < 0 mark "none".
@@ -383,17 +537,16 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
   if (tid == 0) rec->ncand = got;
 
   if (P.mode == MODE_TOPP_FULL) {
-    const double mx = comp_x(top1, P.temperature);
-    double z = 0.0;
+    // sum over the chunk of exp(x - mx) = 2^(t - t_max), t = logit * log2(e) / T
+    const Exp2Ctx ctx = exp2_ctx(P, key_value((uint32_t)(top1 >> 32)));
+    DF acc = {0.0f, 0.0f};
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int i = tid + j * SB;
-      if (i < cnt) z += exp((double)key_value(key[j]) / (double)P.temperature - mx);
-    }
-    z = block_sum_d(z, sm);
+    for (int j = 0; j < EPT; ++j)
+      if (tid + j * SB < cnt) df_accumulate(acc, df_exp2_rel(key_value(key[j]), ctx, sm.e2h, sm.e2l));
+    const DF z = block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
     if (tid == 0) {
-      rec->mx = mx;
-      rec->z = z;
+      rec->mx = comp_x(top1, P.temperature);
+      rec->z = (double)z.h + (double)z.l;
     }
   }
   __syncthreads();
@@ -678,6 +831,9 @@ __device__ __forceinline__ RowParams row_params(int V, uint64_t seed, int64_t st
   else
     P.mode = MODE_GENERAL;
   P.nc = P.mode == MODE_TOPK_SMALL ? P.K : NCAND;
+  const DF c2 = P.mode == MODE_GREEDY ? DF{0.0f, 0.0f} : df_div_f(DF{LOG2E_H, LOG2E_L}, temp);
+  P.c2h = c2.h;
+  P.c2l = c2.l;
   return P;
 }
 
@@ -720,6 +876,7 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   if (!a.active[b]) return;
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) return;
+  load_exp2_table(sm);  // read after the first barrier of the chunk pass
   const RowParams P = row_params(a.vocab, a.seeds[slot], a.steps[slot], a.temperature[slot],
                                  a.top_k[slot], a.top_p[slot], a.salt);
   chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, c, P, a.recs + (int64_t)b * a.nch + c,
@@ -797,6 +954,7 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     }
     return;
   }
+  load_exp2_table(sm);  // read after the first barrier of the chunk pass
   const int64_t step = a.steps[slot];
   ChunkRec *recs = a.recs + (int64_t)b * a.nch;
   float *rowbuf = a.rows + (int64_t)b * V;
