@@ -50,6 +50,7 @@ constexpr int SB = 256;                 // threads per sampler CTA
 constexpr int CHUNK = 8192;             // tokens per chunk
 constexpr int EPT = CHUNK / SB;         // tokens per thread in a chunk pass
 constexpr int NCAND = 512;              // most candidates kept per chunk
+constexpr int NC_MIN = 64;              // least candidates kept per chunk
 constexpr int MAX_CHUNKS = 64;          // vocab <= 64 * 8192
 constexpr int GEN_BLOCK = 1024;         // sorted block (finish and general path)
 
@@ -61,11 +62,11 @@ struct ChunkRec {
   double z;            // sum over the chunk of exp(x - mx)        (MODE_TOPP_FULL)
   double gscore;       // best x + g of the chunk                  (MODE_ALL)
   int32_t gid;         // its token
-  int32_t ncand;
+  int32_t ncand;       // candidates kept
+  uint64_t thr;        // the smallest of them when the chunk holds more tokens (else 0)
   uint64_t cand[NCAND];
-  uint64_t pad_[3];
+  uint64_t pad_[2];
 };
-// candidates per chunk: top-k rows keep their k, top-p rows NCAND
 static_assert(sizeof(ChunkRec) % 64 == 0, "ChunkRec");
 
 struct RowParams {
@@ -277,9 +278,9 @@ struct SampSmem {
   int32_t flag;
   int32_t token;
   int32_t kept;
+  int32_t done;
   double zsum;
   uint64_t sortbuf[GEN_BLOCK];
-  double xs[NCAND];
   double es[GEN_BLOCK];
 };
 
@@ -374,15 +375,14 @@ __device__ int block_argmax(double s, int id, SampSmem &sm, double *best_score =
 __device__ void block_sort_desc(uint64_t *v, int n) {
   for (int k = 2; k <= n; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += SB) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint64_t a = v[i], b = v[ixj];
-          const bool desc_block = (i & k) == 0;
-          if (desc_block ? (a < b) : (a > b)) {
-            v[i] = b;
-            v[ixj] = a;
-          }
+      // one compare-exchange pair (i, i + j) per thread, bit j of i clear
+      for (int p = threadIdx.x; p < n / 2; p += SB) {
+        const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
+        const uint64_t a = v[i], b = v[i + j];
+        const bool desc_block = (i & k) == 0;
+        if (desc_block ? (a < b) : (a > b)) {
+          v[i] = b;
+          v[i + j] = a;
         }
       }
       __syncthreads();
@@ -534,7 +534,10 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
   __syncthreads();
   const int got = min((int)sm.cnt, nc);
   for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0;
-  if (tid == 0) rec->ncand = got;
+  if (tid == 0) {
+    rec->ncand = got;
+    rec->thr = cnt > nc ? thr : 0ull;
+  }
 
   if (P.mode == MODE_TOPP_FULL) {
     // sum over the chunk of exp(x - mx) = 2^(t - t_max), t = logit * log2(e) / T
@@ -707,6 +710,38 @@ __device__ int general_sample(const float *__restrict__ row, int V, const RowPar
 }
 
 // ---------------------------------------------------------------------------
+// top-p scan (one warp): rank r is kept iff r == 0 or the sum of the kept
+// probabilities before it is below p * Z.  Scans es[0, n) of ranks r0 + i
+// with the running sum `carry` (prefix sums over 32 ranks at a time by
+// shuffles); returns true when the cut falls inside, with *kept = the
+// number kept from this block.
+// ---------------------------------------------------------------------------
+__device__ bool topp_scan_warp(const double *es, int n, int r0, double &carry, double pz,
+                               int *kept) {
+  const int lane = threadIdx.x & 31;
+  for (int base = 0; base < n; base += 32) {
+    const int r = base + lane;
+    double inc = r < n ? es[r] : 0.0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const double o = __shfl_up_sync(FULL_MASK, inc, off);
+      if (lane >= off) inc += o;
+    }
+    double ex = __shfl_up_sync(FULL_MASK, inc, 1);
+    if (lane == 0) ex = 0.0;
+    const bool stop = r < n && r0 + r > 0 && !(carry + ex < pz);
+    const unsigned bm = __ballot_sync(FULL_MASK, stop);
+    if (bm) {
+      *kept = base + __ffs(bm) - 1;
+      return true;
+    }
+    carry += __shfl_sync(FULL_MASK, inc, 31);
+  }
+  *kept = n;
+  return false;
+}
+
+// ---------------------------------------------------------------------------
 // finish: one CTA per row
 // ---------------------------------------------------------------------------
 __device__ int finish_row(const float *__restrict__ row, int V, int nch, const RowParams &P,
@@ -731,76 +766,117 @@ __device__ int finish_row(const float *__restrict__ row, int V, int nch, const R
   for (int c = 0; c < nch; ++c) top1 = recs[c].top1 > top1 ? recs[c].top1 : top1;
   if (P.mode == MODE_GENERAL) return general_sample(row, V, P, top1, -1.0, sm);
 
-  // the nc largest of the union of the chunks' candidates, sorted
+  // the largest of the union of the chunks' candidates, sorted: the top-k,
+  // or (top-p over the whole vocabulary) up to NCAND tokens
   const int nc = P.nc;
   const int nu = nch * nc;
+  const bool full = P.mode == MODE_TOPP_FULL;
   auto cand_at = [&](int i) -> uint64_t { return recs[i / nc].cand[i % nc]; };
+  if (tid == 0) sm.cnt = 0;
+  __syncthreads();
+  if (tid < nch) atomicAdd(&sm.cnt, (uint32_t)recs[tid].ncand);
+  __syncthreads();
+  const int nreal = (int)sm.cnt;
+  const int nv = min(full ? NCAND : P.K, nreal);
+  __syncthreads();
   int nsort;
   if (nu <= GEN_BLOCK) {
     nsort = nu;
     for (int i = tid; i < nu; i += SB) sm.sortbuf[i] = cand_at(i);
   } else {
-    const uint64_t thr = select_rank_of(nu, cand_at, ~0ull, nc - 1, sm);
+    const uint64_t thr = select_rank_of(nu, cand_at, ~0ull, nv - 1, sm);
     if (tid == 0) sm.cnt = 0;
     __syncthreads();
     for (int i = tid; i < nu; i += SB) {
       const uint64_t cc = cand_at(i);
-      if (cc >= thr) {
+      if (cc != 0ull && cc >= thr) {
         const uint32_t pos = atomicAdd(&sm.cnt, 1u);
-        if (pos < (uint32_t)nc) sm.sortbuf[pos] = cc;
+        if (pos < (uint32_t)nv) sm.sortbuf[pos] = cc;
       }
     }
-    nsort = nc;
+    nsort = nv;
   }
   int n2 = 1;
   while (n2 < nsort) n2 <<= 1;
   for (int i = nsort + tid; i < n2; i += SB) sm.sortbuf[i] = 0ull;
   __syncthreads();
   block_sort_desc(sm.sortbuf, n2);
-  const int nv = min(nc, V);
   const double m = comp_x(sm.sortbuf[0], P.temperature);
-  for (int r = tid; r < nv; r += SB) {
-    sm.xs[r] = comp_x(sm.sortbuf[r], P.temperature);
-    sm.es[r] = exp(sm.xs[r] - m);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int kept = nv;
-    int fallback = 0;
-    if (P.top_p < 1.0f) {
-      double Z = 0.0;
-      if (P.mode == MODE_TOPK_SMALL) {
-        for (int r = 0; r < nv; ++r) Z += sm.es[r];
-      } else {
-        for (int c = 0; c < nch; ++c)
-          if (recs[c].top1 != 0ull) Z += recs[c].z * exp(recs[c].mx - m);
-      }
-      const double pz = (double)P.top_p * Z;
-      double S = 0.0;
-      kept = 0;
-      for (int r = 0; r < nv; ++r) {
-        if (r == 0 || S < pz) {
-          kept = r + 1;
-          S += sm.es[r];
-        } else {
-          break;
-        }
-      }
-      // top-p over the whole vocabulary still open after the top nc
-      if (P.mode == MODE_TOPP_FULL && kept == nv && nv < V && S < pz) fallback = 1;
-      sm.zsum = Z;
+  const bool topp = P.top_p < 1.0f;
+  double Z = 0.0;
+  if (topp && full) {
+    // the chunks' partial normalisers, rescaled to the row maximum in
+    // parallel and added in chunk order
+    if (tid < nch) sm.red_d[tid] = recs[tid].top1 != 0ull ? recs[tid].z * exp(recs[tid].mx - m) : 0.0;
+    __syncthreads();
+    if (tid == 0) {
+      double z = 0.0;
+      for (int c = 0; c < nch; ++c) z += sm.red_d[c];
+      sm.zsum = z;
     }
-    sm.kept = kept;
-    sm.flag = fallback;
+    __syncthreads();
+    Z = sm.zsum;
   }
-  __syncthreads();
-  if (sm.flag) return general_sample(row, V, P, top1, sm.zsum, sm);
+  // e^(x - m) of the sorted candidates, in blocks of 64, 128, ... only as far
+  // as the top-p scan reaches (all of them for top-k)
+  double carry = 0.0;  // warp 0: the running sum before the block
+  int lo = 0, hi = topp && full ? min(64, nv) : nv;
+  for (;;) {
+    for (int r = lo + tid; r < hi; r += SB) sm.es[r] = exp(comp_x(sm.sortbuf[r], P.temperature) - m);
+    __syncthreads();
+    if (!topp) {
+      if (tid == 0) {
+        sm.kept = nv;
+        sm.flag = 0;
+      }
+      __syncthreads();
+      break;
+    }
+    if (!full) {
+      // Z over the top-k survivors (one block)
+      double part = 0.0;
+      for (int r = tid; r < nv; r += SB) part += sm.es[r];
+      Z = block_sum_d(part, sm);
+      if (tid == 0) sm.zsum = Z;
+    }
+    if (tid < 32) {
+      int k;
+      const bool cut = topp_scan_warp(sm.es + lo, hi - lo, lo, carry, (double)P.top_p * Z, &k);
+      if (tid == 0) {
+        sm.done = (cut || hi == nv) ? 1 : 0;
+        sm.kept = lo + k;
+        // top-p over the whole vocabulary still open after the top nc
+        sm.flag = (!cut && hi == nv && full && nv < V) ? 1 : 0;
+      }
+    }
+    __syncthreads();
+    const bool done = sm.done != 0;
+    __syncthreads();
+    if (done) break;
+    lo = hi;
+    hi = min(2 * hi + 64, nv);
+  }
+  // The extracted prefix is the exact global order over the prefix the
+  // decision read (the kept set; for top-k the K survivors) unless a chunk
+  // that holds more tokens than it gave has its last candidate strictly
+  // inside that prefix.  The top-k also needs K candidates in the union.
+  if (!sm.flag) {
+    const int decided = (topp && full) ? sm.kept : nv;
+    const uint64_t last = sm.sortbuf[decided - 1];
+    __syncthreads();
+    if (tid == 0 && !full && P.K > nreal) sm.flag = 1;
+    if (tid < nch && recs[tid].thr > last) sm.flag = 1;
+    __syncthreads();
+  }
+  // (the chunks' normaliser is exact whatever the candidates; the top-k one
+  // is not when the union missed some of the top-k)
+  if (sm.flag) return general_sample(row, V, P, top1, full ? sm.zsum : -1.0, sm);
   const int kept = sm.kept;
   double bs = 0.0;
   int bid = -1;
   for (int r = tid; r < kept; r += SB) {
     const int tok = comp_token(sm.sortbuf[r]);
-    const double s = sm.xs[r] + gumbel(P, tok);
+    const double s = comp_x(sm.sortbuf[r], P.temperature) + gumbel(P, tok);
     if (better(s, tok, bs, bid)) {
       bs = s;
       bid = tok;
@@ -830,7 +906,11 @@ __device__ __forceinline__ RowParams row_params(int V, uint64_t seed, int64_t st
     P.mode = (top_p < 1.0f) ? MODE_TOPP_FULL : MODE_ALL;
   else
     P.mode = MODE_GENERAL;
-  P.nc = P.mode == MODE_TOPK_SMALL ? P.K : NCAND;
+  // candidates per chunk: enough that the union can hold the top-k (or the
+  // 512 tokens top-p over the whole vocabulary may read), and at least 64
+  const int kcap = P.mode == MODE_TOPK_SMALL ? P.K : NCAND;
+  const int nch = (V + CHUNK - 1) / CHUNK;
+  P.nc = min(kcap, max(NC_MIN, (kcap + nch - 1) / nch));
   const DF c2 = P.mode == MODE_GREEDY ? DF{0.0f, 0.0f} : df_div_f(DF{LOG2E_H, LOG2E_L}, temp);
   P.c2h = c2.h;
   P.c2l = c2.l;

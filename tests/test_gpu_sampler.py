@@ -82,6 +82,10 @@ def _logits(B, V, std, seed, dist="normal"):
         return rng.normal(0, std, (B, V)).astype(np.float32)
     if dist == "ties":
         return rng.integers(-4, 4, (B, V)).astype(np.float32)
+    if dist == "conc":  # the largest logits all in the first 8192-token chunk
+        x = rng.normal(0, std, (B, V)).astype(np.float32)
+        x[:, :8192] += np.float32(6.0)
+        return x
     raise ValueError(dist)
 
 
@@ -128,6 +132,9 @@ def test_config_samplers_match_oracle(name, B):
     dict(V=8193, T=0.9, k=30, p=0.8, std=3.0),         # ragged second chunk of one token
     dict(V=16384, T=1.0, k=50, p=0.9, std=1.0, dist="ties"),  # many exact ties
     dict(V=70000, T=3.0, k=0, p=0.999, std=1.0),       # general path, many blocks
+    dict(V=40000, T=1.0, k=200, p=0.99, std=1.0),      # top-k above the per-chunk candidates
+    dict(V=40000, T=1.0, k=300, p=0.99, std=1.0, dist="conc"),  # one chunk holds the top-k
+    dict(V=151936, T=0.5, k=0, p=0.95, std=1.0, dist="conc"),   # one chunk holds the top-p set
 ])
 def test_sampler_modes_and_edges(case):
     B = 7
