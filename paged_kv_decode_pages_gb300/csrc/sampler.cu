@@ -10,8 +10,9 @@
 // Gumbel-max with Philox4x64-10 (Salmon et al., SC 2011) keyed by
 // (seed, salt) at counter (token, step, 0, 0), so a row's sample depends on
 // its own logits and slot state only.  Every decision (order, top-p cut,
-// Gumbel argmax) is taken in fp64 on values that are exact functions of
-// the fp32 logits.
+// Gumbel argmax) is taken in fp64; the values compared are exact functions
+// of the fp32 logits except the top-p normaliser's chunk partials, which
+// are within 3e-9 of themselves (see the chunk pass).
 //
 // Structure:
 //  * order key: the fp32 logit mapped to a uint32 that sorts like the float
@@ -19,8 +20,9 @@
 //    composite comes first in (value desc, id asc) order, and composites
 //    are unique.
 //  * chunk pass (one CTA per 8192-token chunk of a row): chunk maximum;
-//    the chunk's largest composites (its top-k, or 512 for top-p over the
-//    whole vocabulary; radix select over 8-bit digits);
+//    the chunk's nc largest composites by a radix select over 8-bit digits,
+//    nc = min(kcap, max(64, ceil(kcap / chunks))) with kcap = the top-k, or
+//    512 for top-p over the whole vocabulary, and the smallest of them;
 //    for top-p over the whole vocabulary, the partial normaliser
 //    sum exp(x - x_chunkmax) = sum 2^(logit * log2(e) / T - t_chunkmax) in
 //    double-float arithmetic (fp32 pairs): Tang's table-driven exp2 (ACM
@@ -30,11 +32,15 @@
 //    much issue time as several dozen fp32 ones, and this is the only
 //    per-logit transcendental of the path; for "keep everything", the
 //    chunk's Gumbel argmax.  The chunking depends on the vocabulary only.
-//  * finish (one CTA per row): merges the chunk records in chunk order,
-//    sorts the candidates, applies top-k / top-p with sequential fp64
-//    prefix sums in sorted order, and takes the Gumbel argmax.  Rows whose
-//    kept set is not decided by those candidates (top-k > 512, or top-p
-//    needing more than 512 tokens) take an exact general path that streams
+//  * finish (one CTA per row): the kcap largest of the chunks' candidates
+//    (radix select over the union), sorted; top-k / top-p with fp64 prefix
+//    sums in sorted order (a warp prefix scan, exponentials computed in
+//    blocks only as far as the scan reaches); the Gumbel argmax.  The
+//    sorted candidates are the exact global order over the prefix the
+//    decision read unless a chunk holding more tokens than it gave has its
+//    smallest candidate strictly inside that prefix; such rows, and rows
+//    whose kept set is not decided by kcap tokens (top-k > 512, or top-p
+//    needing more than 512 tokens), take an exact general path that streams
 //    the row: radix select of the top-k threshold and progressive sorted
 //    extraction until the top-p crossing.
 //  * the frame kernel runs the same chunk pass and finish for each of the

@@ -1,0 +1,83 @@
+// Runs pkv_seeded_sample's two kernels (sample_chunk_kernel, then
+// sample_finish_kernel) on the CPU emulation of CUDA.  The kernels' source is
+// the library's sampler.cu up to the end of its namespace, included below as
+// "sampler_dev.inc" (written by the test).  Input and output are raw files:
+//   in:  int32 B, V, num_slots; fp32 logits[B*V]; int32 slots[B], active[B];
+//        uint64 seeds[S]; int64 steps[S]; fp32 temperature[S]; int32 top_k[S];
+//        fp32 top_p[S]
+//   out: int32 out_tok[B], out_kind[B], err
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "sampler_dev.inc"
+
+template <class T>
+static void rd(FILE *f, std::vector<T> &v, size_t n) {
+  v.resize(n);
+  if (fread(v.data(), sizeof(T), n, f) != n) {
+    fprintf(stderr, "short input\n");
+    exit(2);
+  }
+}
+
+int main(int argc, char **argv) {
+  if (argc != 3) return 2;
+  FILE *f = fopen(argv[1], "rb");
+  if (!f) return 2;
+  int32_t hdr[3];
+  if (fread(hdr, sizeof(int32_t), 3, f) != 3) return 2;
+  const int B = hdr[0], V = hdr[1], S = hdr[2];
+  std::vector<float> logits, temp, top_p;
+  std::vector<int32_t> slots, active, top_k;
+  std::vector<uint64_t> seeds;
+  std::vector<int64_t> steps;
+  rd(f, logits, (size_t)B * V);
+  rd(f, slots, B);
+  rd(f, active, B);
+  rd(f, seeds, S);
+  rd(f, steps, S);
+  rd(f, temp, S);
+  rd(f, top_k, S);
+  rd(f, top_p, S);
+  fclose(f);
+
+  using namespace pkv;
+  std::vector<int32_t> out_tok(B, -1), out_kind(B, -1);
+  int32_t err = 0;
+  SampleArgs a{};
+  a.logits = logits.data();
+  a.row_stride = V;
+  a.batch = B;
+  a.vocab = V;
+  a.nch = chunks_for(V);
+  a.slots = slots.data();
+  a.active = active.data();
+  a.num_slots = S;
+  a.seeds = seeds.data();
+  a.steps = steps.data();
+  a.temperature = temp.data();
+  a.top_k = top_k.data();
+  a.top_p = top_p.data();
+  a.salt = 0;
+  a.advance = 0;
+  a.out_tok = out_tok.data();
+  a.out_kind = out_kind.data();
+  const size_t bytes = align_up((size_t)B * a.nch * sizeof(ChunkRec), 256);
+  void *ws = aligned_alloc(256, bytes);
+  memset(ws, 0xAB, bytes);  // not zeroed: the kernels must not read what they did not write
+  a.recs = static_cast<ChunkRec *>(ws);
+  a.err = &err;
+  emu_launch(sample_chunk_kernel, dim3(a.nch, B), SB, a);
+  emu_launch(sample_finish_kernel, dim3(B), SB, a);
+  free(ws);
+
+  FILE *o = fopen(argv[2], "wb");
+  if (!o) return 2;
+  fwrite(out_tok.data(), sizeof(int32_t), B, o);
+  fwrite(out_kind.data(), sizeof(int32_t), B, o);
+  fwrite(&err, sizeof(int32_t), 1, o);
+  fclose(o);
+  return 0;
+}
