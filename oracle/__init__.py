@@ -162,6 +162,9 @@ def _load(path):
     L.pkvo_codebook_frame_sample.restype = _I
     L.pkvo_codebook_frame_sample.argtypes = [_P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
                                              _P, _P, _P, _P, _P, _P]
+    L.pkvo_frame_sample.restype = _I
+    L.pkvo_frame_sample.argtypes = [_P, _I, ctypes.c_int32, _P, _P, _I, _I, _I, _P, _P, _I,
+                                    _P, _P, _P, _P, _P, _P, _P, _P]
     return L
 
 
@@ -310,6 +313,43 @@ def codebook_frame_sample(base, fb, slots, active, seeds, steps, temperature, to
                                            sd.shape[0], _ptr(sd), _ptr(steps), _ptr(tp), _ptr(tk),
                                            _ptr(pp), _ptr(codes), _ptr(kind), _ptr(info))
     return codes, kind, info, bad
+
+
+CODE_PAD = -1  # codebook channels of a frame that stopped
+
+
+def frame_sample(ctrl, stop_ctrl, base, fb, slots, active, seeds, steps, temperature, top_k,
+                 top_p):
+    """A full frame row per active row: ctrl fp32 [B, Vc] is sampled on
+    channel 0 (salt 0); a sampled ``stop_ctrl`` fills the codebook channels
+    with CODE_PAD and gives kind STOP, else channels 1..n_cb are the
+    codebook_frame_sample codes and the kind is AUDIO.  base fp32
+    [n_cb, B, V]; fb fp32 [n_cb, V, V] or None.  ``steps`` is advanced in
+    place once per frame for active rows.  Returns (out_rows [B, 1 + n_cb],
+    out_kind [B], info [B, 1 + n_cb], n_bad)."""
+    ct = _c(ctrl, np.float32)
+    bs = _c(base, np.float32)
+    n_cb, B, V = bs.shape
+    assert ct.shape[0] == B
+    Vc = ct.shape[1]
+    f = None if fb is None else _c(fb, np.float32)
+    if f is not None:
+        assert f.shape == (n_cb, V, V)
+    sl = _c(slots, np.int32)
+    ac = _c(active, np.int32)
+    sd = _c(seeds, np.uint64)
+    assert steps.dtype == np.int64 and steps.flags.c_contiguous
+    tp = _c(temperature, np.float32)
+    tk = _c(top_k, np.int32)
+    pp = _c(top_p, np.float32)
+    rows = np.zeros((B, 1 + n_cb), np.int32)
+    kind = np.zeros(B, np.int32)
+    info = np.zeros((B, 1 + n_cb), _INFO_DTYPE)
+    bad = lib().pkvo_frame_sample(_ptr(ct), Vc, int(stop_ctrl), _ptr(bs), _ptr(f), n_cb, B, V,
+                                  _ptr(sl), _ptr(ac), sd.shape[0], _ptr(sd), _ptr(steps),
+                                  _ptr(tp), _ptr(tk), _ptr(pp), _ptr(rows), _ptr(kind),
+                                  _ptr(info))
+    return rows, kind, info, bad
 
 
 def have_compiler() -> bool:

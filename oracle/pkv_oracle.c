@@ -35,10 +35,14 @@
  *                     program", decode_tokens); stop_tokens() / audio_tokens()
  *                     classify the sampled token into out_kind.
  *   frame loop     -- MOSS-TTS-Local on SGLang-Omni (mosi.cn blog), section
- *                     on the model: per frame, 12 RVQ codebooks sampled in
- *                     order, each fed back before the next; section
- *                     "AR Engine": the whole frame runs on a seeded GPU
- *                     sampler with per-request seeds and counters.
+ *                     on the model: per frame, one local-transformer layer
+ *                     first gives a stop/continue decision, then 12 RVQ
+ *                     codebooks are sampled in order, each fed back before
+ *                     the next; a frame row holds 13 channels, channel 0
+ *                     the control token and 1..12 the codes; section
+ *                     "AR Engine": the 13 samplings of a frame run on a
+ *                     seeded GPU sampler with per-request seeds and
+ *                     counters.
  *
  * Readings where the pages are silent (each one is listed in the design
  * notes of the repository):
@@ -64,7 +68,14 @@
  *   - frame loop feedback (no trained weights exist): the logits of
  *     codebook j > 0 are base[j] + fb[j][code_{j-1}], the add rounded once
  *     to fp32 like any fp32 logits tensor; salt = 1 + j; the per-slot step
- *     is read once per frame and advanced once per frame.
+ *     is read once per frame and advanced once per frame;
+ *   - the stop/continue sample (no trained weights exist): channel 0
+ *     samples caller-given control logits [B][Vc] with salt 0 and the
+ *     slot's temperature / top-k / top-p; when it returns the caller's stop
+ *     token, the frame's codebook channels hold the pad code -1, nothing
+ *     else is sampled and the row's kind is STOP; otherwise the codebooks
+ *     follow as above and the kind is AUDIO.  The control token does not
+ *     feed the codebooks.
  *
  * Every floating-point decision here is taken in fp64 (bf16 and fp32 inputs
  * convert to double exactly).
@@ -81,6 +92,7 @@
 #define PKVO_KIND_OTHER 0
 #define PKVO_KIND_AUDIO 1
 #define PKVO_KIND_STOP 2
+#define PKVO_CODE_PAD (-1) /* codebook channels of a frame that stopped */
 
 /* ------------------------------------------------------------------ */
 /* Number of threads OpenMP would use (1 without OpenMP).              */
@@ -502,6 +514,38 @@ int pkvo_seeded_sample(const float *logits, int64_t row_stride, int B, int V,
 /* active rows whose slot is out of range.  info may be NULL, else it  */
 /* receives [B][n_cb] records.                                          */
 /* ------------------------------------------------------------------ */
+/* The codebooks of row b in order at the given step: codebook j samples
+ * base[j][b] (+ fb[j][code_{j-1}] for j > 0) with salt 1 + j.  Writes
+ * codes[j] and, when info is not NULL, info[j].  row: scratch of V floats. */
+static void frame_codes_row(const float *base, const float *fb, int n_cb, int B,
+                            int V, int b, uint64_t seed, int64_t step,
+                            float temperature, int32_t top_k, float top_p,
+                            float *row, int32_t *codes,
+                            pkvo_sample_info *info) {
+  int32_t prev = 0;
+  for (int j = 0; j < n_cb; ++j) {
+    const float *bj = base + ((int64_t)j * B + b) * V;
+    if (j > 0 && fb) {
+      const float *fj = fb + ((int64_t)j * V + prev) * V;
+      /* The fp32 sum, rounded once: the exact sum of two binary32 values
+       * rounded to binary64 and then to binary32 equals the binary32
+       * rounding of the exact sum, since 53 >= 2 * 24 + 2. */
+      for (int i = 0; i < V; ++i) row[i] = (float)((double)bj[i] + (double)fj[i]);
+    } else {
+      for (int i = 0; i < V; ++i) row[i] = bj[i];
+    }
+    prev = pkvo_sample_row(row, V, seed, step, (uint32_t)(1 + j), temperature,
+                           top_k, top_p, info ? &info[j] : NULL);
+    codes[j] = prev;
+  }
+}
+
+static void clear_info(pkvo_sample_info *r) {
+  memset(r, 0, sizeof *r);
+  r->top2_gap_rel = INFINITY;
+  r->member_margin = INFINITY;
+}
+
 int pkvo_codebook_frame_sample(const float *base, const float *fb, int n_cb,
                                int B, int V, const int32_t *slots,
                                const int32_t *active, int num_slots,
@@ -514,12 +558,7 @@ int pkvo_codebook_frame_sample(const float *base, const float *fb, int n_cb,
   for (int b = 0; b < B; ++b) {
     for (int j = 0; j < n_cb; ++j) {
       out_codes[(int64_t)b * n_cb + j] = 0;
-      if (info) {
-        pkvo_sample_info *r = &info[(int64_t)b * n_cb + j];
-        memset(r, 0, sizeof *r);
-        r->top2_gap_rel = INFINITY;
-        r->member_margin = INFINITY;
-      }
+      if (info) clear_info(&info[(int64_t)b * n_cb + j]);
     }
     out_kind[b] = PKVO_KIND_OTHER;
     if (!active[b]) continue;
@@ -528,24 +567,69 @@ int pkvo_codebook_frame_sample(const float *base, const float *fb, int n_cb,
       ++bad;
       continue;
     }
-    const int64_t step = steps[s];
-    int32_t prev = 0;
-    for (int j = 0; j < n_cb; ++j) {
-      const float *bj = base + ((int64_t)j * B + b) * V;
-      if (j > 0 && fb) {
-        const float *fj = fb + ((int64_t)j * V + prev) * V;
-        /* The fp32 sum, rounded once: the exact sum of two binary32 values
-         * rounded to binary64 and then to binary32 equals the binary32
-         * rounding of the exact sum, since 53 >= 2 * 24 + 2. */
-        for (int i = 0; i < V; ++i) row[i] = (float)((double)bj[i] + (double)fj[i]);
-      } else {
-        for (int i = 0; i < V; ++i) row[i] = bj[i];
-      }
-      prev = pkvo_sample_row(row, V, seeds[s], step, (uint32_t)(1 + j),
-                             temperature[s], top_k[s], top_p[s],
-                             info ? &info[(int64_t)b * n_cb + j] : NULL);
-      out_codes[(int64_t)b * n_cb + j] = prev;
+    frame_codes_row(base, fb, n_cb, B, V, b, seeds[s], steps[s], temperature[s],
+                    top_k[s], top_p[s], row, out_codes + (int64_t)b * n_cb,
+                    info ? &info[(int64_t)b * n_cb] : NULL);
+    out_kind[b] = PKVO_KIND_AUDIO;
+  }
+  for (int b = 0; b < B; ++b) {
+    if (!active[b]) continue;
+    int32_t s = slots[b];
+    if (s < 0 || s >= num_slots) continue;
+    steps[s] += 1;
+  }
+  free(row);
+  return bad;
+}
+
+/* ------------------------------------------------------------------ */
+/* A full frame row: the stop/continue sample on channel 0, then the   */
+/* codebooks (MOSS-TTS-Local blog, section on the model: 13 channels,  */
+/* a stop/continue decision first, then the 12 codebooks in order).    */
+/*   ctrl fp32 [B][Vc]; base, fb as above;                             */
+/*   out_rows int32 [B][1 + n_cb]; out_kind int32 [B].                  */
+/* Channel 0 samples ctrl[b] with salt 0 at the frame's step; when it   */
+/* returns stop_ctrl, channels 1..n_cb hold PKVO_CODE_PAD and the kind  */
+/* is STOP, else they hold the codes and the kind is AUDIO.  The step   */
+/* is advanced once per frame for each active row.  Padding rows (and  */
+/* rows whose slot is out of range) get zeros and OTHER.  info may be   */
+/* NULL, else it receives [B][1 + n_cb] records (channel order).        */
+/* Returns the number of active rows whose slot is out of range.        */
+/* ------------------------------------------------------------------ */
+int pkvo_frame_sample(const float *ctrl, int Vc, int32_t stop_ctrl,
+                      const float *base, const float *fb, int n_cb, int B, int V,
+                      const int32_t *slots, const int32_t *active, int num_slots,
+                      const uint64_t *seeds, int64_t *steps,
+                      const float *temperature, const int32_t *top_k,
+                      const float *top_p, int32_t *out_rows, int32_t *out_kind,
+                      pkvo_sample_info *info) {
+  const int W = 1 + n_cb;
+  int bad = 0;
+  float *row = (float *)malloc(sizeof(float) * (size_t)(V > 0 ? V : 1));
+  for (int b = 0; b < B; ++b) {
+    int32_t *r = out_rows + (int64_t)b * W;
+    for (int j = 0; j < W; ++j) {
+      r[j] = 0;
+      if (info) clear_info(&info[(int64_t)b * W + j]);
     }
+    out_kind[b] = PKVO_KIND_OTHER;
+    if (!active[b]) continue;
+    int32_t s = slots[b];
+    if (s < 0 || s >= num_slots) {
+      ++bad;
+      continue;
+    }
+    r[0] = pkvo_sample_row(ctrl + (int64_t)b * Vc, Vc, seeds[s], steps[s], 0u,
+                           temperature[s], top_k[s], top_p[s],
+                           info ? &info[(int64_t)b * W] : NULL);
+    if (r[0] == stop_ctrl) {
+      for (int j = 1; j < W; ++j) r[j] = PKVO_CODE_PAD;
+      out_kind[b] = PKVO_KIND_STOP;
+      continue;
+    }
+    frame_codes_row(base, fb, n_cb, B, V, b, seeds[s], steps[s], temperature[s],
+                    top_k[s], top_p[s], row, r + 1,
+                    info ? &info[(int64_t)b * W + 1] : NULL);
     out_kind[b] = PKVO_KIND_AUDIO;
   }
   for (int b = 0; b < B; ++b) {

@@ -39,6 +39,13 @@ MUTANTS = [
     ("frame feedback from the previous codebook's table",
      "const float *fj = fb + ((int64_t)j * V + prev) * V;",
      "const float *fj = fb + ((int64_t)(j - 1) * V + prev) * V;"),
+    ("control sample with a codebook's salt",
+     "r[0] = pkvo_sample_row(ctrl + (int64_t)b * Vc, Vc, seeds[s], steps[s], 0u,",
+     "r[0] = pkvo_sample_row(ctrl + (int64_t)b * Vc, Vc, seeds[s], steps[s], 1u,"),
+    ("a stop leaves the codes unpadded", "for (int j = 1; j < W; ++j) r[j] = PKVO_CODE_PAD;",
+     "for (int j = 1; j < W; ++j) r[j] = 0;"),
+    ("a stop still samples the codes", "      out_kind[b] = PKVO_KIND_STOP;\n      continue;",
+     "      out_kind[b] = PKVO_KIND_STOP;"),
 ]
 
 
@@ -62,6 +69,9 @@ def _pins():
         ("kept sets", lambda: [TS.test_kept_set_count_matches_brute_force(v) for v in (5, 8)]),
         ("frame salts", TS.test_frame_without_feedback_equals_independent_salted_samples),
         ("frame feedback", TS.test_frame_feedback_wiring),
+        ("full frame gating", TS.test_full_frame_channel0_is_the_salt0_sample_and_gates_the_codes),
+        ("full frame never stops", TS.test_full_frame_that_never_stops_is_the_codebook_frame),
+        ("full frame always stops", TS.test_full_frame_that_always_stops_is_a_pad_row),
         ("gumbel moments", TS.test_gumbel_moments),
         ("chi-square", lambda: TS.test_gumbel_max_frequencies_chi_square(0, 1.0, 1.0)),
     ]

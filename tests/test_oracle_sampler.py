@@ -303,3 +303,61 @@ def test_frame_feedback_wiring():
                                                        steps.copy(), T, K, P)
     np.testing.assert_array_equal(codes0, codes_none)
     assert np.any(codes0 != codes)
+
+
+# ---------------------------------------------------------------------------
+# Full frame: the stop/continue sample on channel 0, then the codebooks
+# ---------------------------------------------------------------------------
+STOP = 2  # the stop token of a 4-token control vocabulary in these tests
+
+
+def _ctrl(bias_stop):
+    """Control logits [3, 4]; bias_stop[b] is added to the stop token's."""
+    rng = np.random.default_rng(17)
+    c = rng.normal(0, 1.0, (3, 4)).astype(np.float32)
+    c[:, STOP] += np.asarray(bias_stop, np.float32)
+    return c
+
+
+def test_full_frame_channel0_is_the_salt0_sample_and_gates_the_codes():
+    base, fb, slots, active, seeds, T, K, P = _frame_inputs(seed=2)
+    ctrl = _ctrl([30.0, 0.0, -np.inf])  # row 0 must stop, row 2 cannot
+    steps = np.array([0, 3, 4], np.int64)
+    rows, kind, _, bad = oracle.frame_sample(ctrl, STOP, base, fb, slots, active, seeds,
+                                             steps, T, K, P)
+    assert bad == 0 and list(steps) == [0, 4, 5]  # once per frame, stopped or not
+    codes, _, _, _ = oracle.codebook_frame_sample(base, fb, slots, active, seeds,
+                                                  np.array([0, 3, 4], np.int64), T, K, P)
+    assert np.all(rows[1] == 0) and kind[1] == oracle.KIND_OTHER  # padding row
+    for b in (0, 2):
+        s = slots[b]
+        c0 = oracle.sample_row(ctrl[b], seeds[s], steps[s] - 1, 0, T[s], K[s], P[s])[0]
+        assert rows[b, 0] == c0
+    assert rows[0, 0] == STOP and kind[0] == oracle.KIND_STOP
+    assert np.all(rows[0, 1:] == oracle.CODE_PAD)
+    assert rows[2, 0] != STOP and kind[2] == oracle.KIND_AUDIO
+    np.testing.assert_array_equal(rows[2, 1:], codes[2])
+
+
+def test_full_frame_that_never_stops_is_the_codebook_frame():
+    base, fb, slots, active, seeds, T, K, P = _frame_inputs(seed=3)
+    ctrl = _ctrl([-np.inf] * 3)
+    s1, s2 = np.array([0, 5, 6], np.int64), np.array([0, 5, 6], np.int64)
+    rows, kind, _, _ = oracle.frame_sample(ctrl, STOP, base, fb, slots, active, seeds, s1, T, K, P)
+    codes, ckind, _, _ = oracle.codebook_frame_sample(base, fb, slots, active, seeds, s2, T, K, P)
+    np.testing.assert_array_equal(rows[:, 1:], codes)
+    np.testing.assert_array_equal(kind, ckind)
+    np.testing.assert_array_equal(s1, s2)
+    assert np.all(rows[[0, 2], 0] != STOP)
+
+
+def test_full_frame_that_always_stops_is_a_pad_row():
+    base, fb, slots, active, seeds, T, K, P = _frame_inputs(seed=4)
+    ctrl = np.full((3, 4), -np.inf, np.float32)
+    ctrl[:, STOP] = 0.0  # the only finite control logit
+    steps = np.array([0, 1, 2], np.int64)
+    rows, kind, _, _ = oracle.frame_sample(ctrl, STOP, base, fb, slots, active, seeds, steps,
+                                           T, K, P)
+    for b in (0, 2):
+        assert list(rows[b]) == [STOP] + [oracle.CODE_PAD] * 12 and kind[b] == oracle.KIND_STOP
+    assert list(steps) == [0, 2, 3]
