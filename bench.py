@@ -3,7 +3,8 @@
 
 A step is the whole hot path over one batch of synthetic input: for every
 layer kv_append + paged_decode_attn, then seeded_sample over the logits
-(and, for the frame workload, one 12-codebook frame).  Inputs are resident
+(and, for the frame workload, one frame: a stop/continue sample on channel
+0 that gates 12 sequentially sampled codebooks).  Inputs are resident
 in HBM when the timed region starts; the per-step KV footprint is far larger
 than L2, so no flush is needed between steps.
 
@@ -51,7 +52,9 @@ def step_bytes(batch, cfg, vocab, frame_vocab=0):
     logits = n_act * vocab * 4
     frame = 0
     if cfg.n_codebooks:
-        frame = (2 * cfg.n_codebooks - 1) * n_act * frame_vocab * 4
+        # codebook logits + feedback rows (a frame that stops reads fewer:
+        # counted as if none stopped) + the control logits
+        frame = (2 * cfg.n_codebooks - 1) * n_act * frame_vocab * 4 + n_act * cfg.ctrl_vocab * 4
     return dict(attn_per_layer=attn, kv_per_layer=kv, append_per_layer=append, logits=logits,
                 frame=frame, step=cfg.num_layers * (attn + append) + logits + frame,
                 n_active=n_act)
@@ -167,6 +170,7 @@ class OracleRunner:
         self.logits = None if tensors.logits is None else tensors.logits.cpu().numpy()
         self.base = None if tensors.base is None else tensors.base.cpu().numpy()
         self.fb = None if tensors.fb is None else tensors.fb.cpu().numpy()
+        self.ctrl = None if tensors.ctrl is None else tensors.ctrl.cpu().numpy()
 
     def layer_inputs(self, l):
         import torch
@@ -195,7 +199,10 @@ class OracleRunner:
         if self.logits is not None:
             self.oracle.seeded_sample(self.logits, b.slots, b.active, b.seeds, steps,
                                       b.temperature, b.top_k, b.top_p)
-        if self.base is not None:
+        if self.base is not None and self.ctrl is not None:
+            self.oracle.frame_sample(self.ctrl, b.cfg.ctrl_stop, self.base, self.fb, b.slots,
+                                     b.active, b.seeds, steps, b.temperature, b.top_k, b.top_p)
+        elif self.base is not None:
             self.oracle.codebook_frame_sample(self.base, self.fb, b.slots, b.active, b.seeds,
                                               steps, b.temperature, b.top_k, b.top_p)
         return time.perf_counter() - t0
@@ -356,6 +363,25 @@ def main(argv=None):
     sampler_us = s0.elapsed_time(s1) / n_samp * 1e3
     barrier()
 
+    # ---- the frame alone (frame workloads), same stream ----------------
+    frame_line = None
+    if tensors.base is not None:
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        n_frames = 50
+        f0.record(stream)
+        for _ in range(n_frames):
+            step.frame(stream=stream)
+        f1.record(stream)
+        f1.synchronize()
+        frame_us = f0.elapsed_time(f1) / n_frames * 1e3
+        n_cb = tensors.base.shape[0]
+        frame_line = {"us_per_frame": frame_us,
+                      "frames_per_s": sizes["n_active"] / (frame_us / 1e6),
+                      "samplings_per_frame": n_cb + (1 if tensors.ctrl is not None else 0),
+                      "codes_per_s": sizes["n_active"] * n_cb / (frame_us / 1e6)}
+        barrier()
+
     # ---- end to end: host (pinned) inputs in, tokens out, every step ----
     host_in = [(tensors.q, tensors.q.cpu().pin_memory()), (tensors.k, tensors.k.cpu().pin_memory()),
                (tensors.v, tensors.v.cpu().pin_memory()),
@@ -403,6 +429,7 @@ def main(argv=None):
         "sampled_rows_per_s": world * sizes["n_active"] * args.steps / (total_ms / 1e3),
         "sampler": {"us_per_call": sampler_us,
                     "rows_per_s": sizes["n_active"] / (sampler_us / 1e6)},
+        **({"frame": frame_line} if frame_line else {}),
         "attn": {"us_per_layer": attn_avg_s * 1e6, "gbs": achieved,
                  "bytes_per_layer": sizes["attn_per_layer"]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -59,6 +59,9 @@ extern "C" {
 #define PKV_KIND_AUDIO 1
 #define PKV_KIND_STOP 2
 
+/* Codebook channels of a frame whose stop/continue sample said stop. */
+#define PKV_CODE_PAD (-1)
+
 /* Geometry of the paged cache: one bf16 tensor
  *   cache[num_layers][num_pages][2][page_size][num_kv_heads][head_dim]
  * for all layers ("Adding a Model", section "1. The model code").  Index 0
@@ -272,6 +275,48 @@ int pkv_codebook_frame_sample(const float *base, const float *fb,
                               int32_t *out_codes, int32_t *out_kind,
                               void *workspace, size_t workspace_bytes,
                               int32_t *err_word, void *stream);
+
+/* Workspace (bytes) pkv_frame_sample needs for these sizes. */
+size_t pkv_frame_sample_workspace_bytes(int n_codebooks, int batch, int vocab,
+                                        int ctrl_vocab);
+
+/* ------------------------------------------------------------------------
+ * pkv_frame_sample -- a full frame row of MOSS-TTS-Local on SGLang-Omni
+ * (mosi.cn blog, section on the model): per frame, the local transformer
+ * first gives a stop/continue decision, then the codebooks are sampled in
+ * order; a frame row has 1 + n_codebooks channels, channel 0 the control
+ * token and the rest the codes (the "[T, 13]" rows); the 13 samplings of a
+ * frame run on a seeded GPU sampler ("AR Engine" section).
+ *
+ * For each active row b (slot s), at the frame's step steps[s]:
+ *     out_rows[b][0] = the pkv_seeded_sample rule on ctrl_logits[b] with
+ *                      salt 0 and the slot's temperature / top-k / top-p;
+ *     if it is stop_ctrl: out_rows[b][1..] = PKV_CODE_PAD, nothing else is
+ *                      sampled, out_kind[b] = PKV_KIND_STOP;
+ *     else:            out_rows[b][1 + j] = code_j of
+ *                      pkv_codebook_frame_sample (salts 1 .. n_codebooks),
+ *                      out_kind[b] = PKV_KIND_AUDIO;
+ * then steps[s] += 1 (once per frame, stopped or not).  No trained local
+ * transformer exists here: the control logits are the caller's, and the
+ * control token does not feed the codebooks.  Padding rows: zeros, kind
+ * OTHER, no state touched.  One launch per frame.
+ *
+ *   ctrl_logits fp32 [batch][ctrl_vocab], 4-byte aligned.
+ *   stop_ctrl   the control token that means stop, in [0, ctrl_vocab).
+ *   out_rows    int32 [batch][1 + n_codebooks].
+ *   other arguments as for pkv_codebook_frame_sample.
+ * Errors: as pkv_codebook_frame_sample; PKV_ERR_INVALID_ARG also for a
+ * NULL ctrl_logits or a stop_ctrl outside [0, ctrl_vocab).
+ * ---------------------------------------------------------------------- */
+int pkv_frame_sample(const float *ctrl_logits, int ctrl_vocab, int32_t stop_ctrl,
+                     const float *base, const float *fb, int n_codebooks,
+                     int batch, int vocab, const int32_t *slots,
+                     const int32_t *active, int num_slots,
+                     const uint64_t *seeds, int64_t *steps,
+                     const float *temperature, const int32_t *top_k,
+                     const float *top_p, int32_t *out_rows, int32_t *out_kind,
+                     void *workspace, size_t workspace_bytes,
+                     int32_t *err_word, void *stream);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -15,7 +15,8 @@ _BINDING = (
     "kv_append", "paged_decode_attn", "decode_workspace_bytes", "paged_decode_attn_static",
     "seeded_sample", "sample_workspace_bytes",
     "codebook_frame_sample", "frame_workspace_bytes",
-    "KIND_OTHER", "KIND_AUDIO", "KIND_STOP",
+    "frame_sample", "frame_sample_workspace_bytes",
+    "KIND_OTHER", "KIND_AUDIO", "KIND_STOP", "CODE_PAD",
 )
 
 __all__ = list(_BINDING)

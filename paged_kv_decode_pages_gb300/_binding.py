@@ -11,6 +11,7 @@ import threading
 from . import build as _build
 
 KIND_OTHER, KIND_AUDIO, KIND_STOP = 0, 1, 2
+CODE_PAD = -1  # PKV_CODE_PAD
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -44,6 +45,9 @@ SIGNATURES = {
     "pkv_frame_workspace_bytes": (_SZ, [_I, _I, _I]),
     "pkv_codebook_frame_sample": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _SZ, _P, _P]),
+    "pkv_frame_sample_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "pkv_frame_sample": (_I, [_P, _I, _I32, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P,
+                              _P, _P, _P, _SZ, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -243,3 +247,31 @@ def codebook_frame_sample(base, fb, slots, active, seeds, steps, temperature, to
         _ptr(out_kind), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(err_word), _stream(stream))
     _check("pkv_codebook_frame_sample", st)
+
+
+def frame_sample_workspace_bytes(n_codebooks, batch, vocab, ctrl_vocab) -> int:
+    return int(load().pkv_frame_sample_workspace_bytes(n_codebooks, batch, vocab, ctrl_vocab))
+
+
+def frame_sample(ctrl, stop_ctrl, base, fb, slots, active, seeds, steps, temperature, top_k,
+                 top_p, out_rows, out_kind, workspace, err_word=None, stream=None):
+    """pkv_frame_sample: channel 0 (stop/continue, from ``ctrl`` [B, Vc])
+    then the codebooks; out_rows int32 [B, 1 + n_codebooks]."""
+    import torch
+    _req(ctrl, torch.float32, "ctrl")
+    _req(base, torch.float32, "base")
+    if fb is not None:
+        _req(fb, torch.float32, "fb")
+    n_cb, B, V = base.shape
+    for t, dt, nm in ((slots, torch.int32, "slots"), (active, torch.int32, "active"),
+                      (seeds, torch.uint64, "seeds"), (steps, torch.int64, "steps"),
+                      (temperature, torch.float32, "temperature"), (top_k, torch.int32, "top_k"),
+                      (top_p, torch.float32, "top_p"), (out_rows, torch.int32, "out_rows"),
+                      (out_kind, torch.int32, "out_kind")):
+        _req(t, dt, nm)
+    st = load().pkv_frame_sample(
+        _ptr(ctrl), ctrl.shape[1], int(stop_ctrl), _ptr(base), _ptr(fb), n_cb, B, V, _ptr(slots),
+        _ptr(active), seeds.numel(), _ptr(seeds), _ptr(steps), _ptr(temperature), _ptr(top_k),
+        _ptr(top_p), _ptr(out_rows), _ptr(out_kind), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream))
+    _check("pkv_frame_sample", st)

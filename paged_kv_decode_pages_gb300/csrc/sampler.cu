@@ -1000,6 +1000,11 @@ __global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
 }
 
 struct FrameArgs {
+  const float *ctrl;  // [B][ctrl_vocab] control logits, or null (no channel 0)
+  int ctrl_vocab;
+  int ctrl_nch;
+  int32_t stop_ctrl;
+  int row_w;          // ints per output row: n_cb, or 1 + n_cb with a control channel
   const float *base;  // [n_cb][B][V]
   const float *fb;    // [n_cb][V][V] or null
   int n_cb;
@@ -1026,14 +1031,15 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int V = a.vocab;
+  int32_t *out = a.out_codes + (int64_t)b * a.row_w;
   if (!a.active[b]) {
-    for (int j = tid; j < a.n_cb; j += SB) a.out_codes[(int64_t)b * a.n_cb + j] = 0;
+    for (int j = tid; j < a.row_w; j += SB) out[j] = 0;
     if (tid == 0) a.out_kind[b] = PKV_KIND_OTHER;
     return;
   }
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) {
-    for (int j = tid; j < a.n_cb; j += SB) a.out_codes[(int64_t)b * a.n_cb + j] = 0;
+    for (int j = tid; j < a.row_w; j += SB) out[j] = 0;
     if (tid == 0) {
       a.out_kind[b] = PKV_KIND_OTHER;
       report(a.err, PKV_DEV_ERR_SLOT);
@@ -1042,7 +1048,34 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
   }
   load_exp2_table(sm);  // read after the first barrier of the chunk pass
   const int64_t step = a.steps[slot];
-  ChunkRec *recs = a.recs + (int64_t)b * a.nch;
+  ChunkRec *recs = a.recs + (int64_t)b * (a.nch > a.ctrl_nch ? a.nch : a.ctrl_nch);
+  if (a.ctrl != nullptr) {
+    // channel 0: the stop/continue sample (salt 0); a stop ends the frame
+    const float *crow = a.ctrl + (int64_t)b * a.ctrl_vocab;
+    const RowParams P = row_params(a.ctrl_vocab, a.seeds[slot], step, a.temperature[slot],
+                                   a.top_k[slot], a.top_p[slot], 0u);
+    for (int c = 0; c < a.ctrl_nch; ++c) {
+      chunk_pass(crow, a.ctrl_vocab, c, P, recs + c, sm, a.err);
+      __syncthreads();
+    }
+    const int tok = finish_row(crow, a.ctrl_vocab, a.ctrl_nch, P, recs, sm);
+    if (tid == 0) {
+      out[0] = tok;
+      sm.token = tok;
+    }
+    __syncthreads();
+    const bool stop = sm.token == a.stop_ctrl;
+    __syncthreads();
+    if (stop) {
+      for (int j = 1 + tid; j < a.row_w; j += SB) out[j] = PKV_CODE_PAD;
+      if (tid == 0) {
+        a.out_kind[b] = PKV_KIND_STOP;
+        a.steps[slot] = step + 1;
+      }
+      return;
+    }
+  }
+  int32_t *codes = out + (a.row_w - a.n_cb);
   float *rowbuf = a.rows + (int64_t)b * V;
   int prev = 0;
   for (int j = 0; j < a.n_cb; ++j) {
@@ -1061,7 +1094,7 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     }
     const int tok = finish_row(row, V, a.nch, P, recs, sm);
     if (tid == 0) {
-      a.out_codes[(int64_t)b * a.n_cb + j] = tok;
+      codes[j] = tok;
       sm.token = tok;
     }
     __syncthreads();
@@ -1084,11 +1117,22 @@ extern "C" size_t pkv_sample_workspace_bytes(int batch, int vocab) {
   return align_up((size_t)batch * chunks_for(vocab) * sizeof(ChunkRec), 256);
 }
 
-extern "C" size_t pkv_frame_workspace_bytes(int n_codebooks, int batch, int vocab) {
+static size_t frame_ws_bytes(int batch, int vocab, int ctrl_vocab) {
   using namespace pkv;
-  if (n_codebooks <= 0 || batch <= 0 || vocab <= 0) return 0;
-  return align_up((size_t)batch * chunks_for(vocab) * sizeof(ChunkRec), 256) +
+  const int nch = chunks_for(vocab > ctrl_vocab ? vocab : ctrl_vocab);
+  return align_up((size_t)batch * nch * sizeof(ChunkRec), 256) +
          align_up((size_t)batch * vocab * sizeof(float), 256);
+}
+
+extern "C" size_t pkv_frame_workspace_bytes(int n_codebooks, int batch, int vocab) {
+  if (n_codebooks <= 0 || batch <= 0 || vocab <= 0) return 0;
+  return frame_ws_bytes(batch, vocab, 0);
+}
+
+extern "C" size_t pkv_frame_sample_workspace_bytes(int n_codebooks, int batch, int vocab,
+                                                   int ctrl_vocab) {
+  if (n_codebooks <= 0 || batch <= 0 || vocab <= 0 || ctrl_vocab <= 0) return 0;
+  return frame_ws_bytes(batch, vocab, ctrl_vocab);
 }
 
 static int check_sampler_common(int batch, int vocab, const int32_t *slots, const int32_t *active,
@@ -1153,25 +1197,29 @@ extern "C" int pkv_seeded_sample(const float *logits, int64_t row_stride, int ba
   return launch_status();
 }
 
-extern "C" int pkv_codebook_frame_sample(const float *base, const float *fb, int n_codebooks,
-                                         int batch, int vocab, const int32_t *slots,
-                                         const int32_t *active, int num_slots,
-                                         const uint64_t *seeds, int64_t *steps,
-                                         const float *temperature, const int32_t *top_k,
-                                         const float *top_p, int32_t *out_codes,
-                                         int32_t *out_kind, void *workspace,
-                                         size_t workspace_bytes, int32_t *err_word,
-                                         void *stream) {
+static int launch_frame(const float *ctrl, int ctrl_vocab, int32_t stop_ctrl, const float *base,
+                        const float *fb, int n_codebooks, int batch, int vocab,
+                        const int32_t *slots, const int32_t *active, int num_slots,
+                        const uint64_t *seeds, int64_t *steps, const float *temperature,
+                        const int32_t *top_k, const float *top_p, int32_t *out, int32_t *out_kind,
+                        void *workspace, size_t workspace_bytes, int32_t *err_word, void *stream) {
   using namespace pkv;
   int st = check_sampler_common(batch, vocab, slots, active, num_slots, seeds, steps, temperature,
                                 top_k, top_p);
   if (st != PKV_OK) return st;
-  if (!base || !out_codes || !out_kind || n_codebooks <= 0) return PKV_ERR_INVALID_ARG;
-  if (((uintptr_t)base & 3u) != 0 || ((uintptr_t)fb & 3u) != 0) return PKV_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < pkv_frame_workspace_bytes(n_codebooks, batch, vocab))
+  if (!base || !out || !out_kind || n_codebooks <= 0) return PKV_ERR_INVALID_ARG;
+  if (((uintptr_t)base & 3u) != 0 || ((uintptr_t)fb & 3u) != 0 || ((uintptr_t)ctrl & 3u) != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (ctrl_vocab > MAX_CHUNKS * CHUNK) return PKV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < frame_ws_bytes(batch, vocab, ctrl ? ctrl_vocab : 0))
     return PKV_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
   FrameArgs a;
+  a.ctrl = ctrl;
+  a.ctrl_vocab = ctrl ? ctrl_vocab : 0;
+  a.ctrl_nch = ctrl ? chunks_for(ctrl_vocab) : 0;
+  a.stop_ctrl = stop_ctrl;
+  a.row_w = (ctrl ? 1 : 0) + n_codebooks;
   a.base = base;
   a.fb = fb;
   a.n_cb = n_codebooks;
@@ -1186,12 +1234,42 @@ extern "C" int pkv_codebook_frame_sample(const float *base, const float *fb, int
   a.temperature = temperature;
   a.top_k = top_k;
   a.top_p = top_p;
-  a.out_codes = out_codes;
+  a.out_codes = out;
   a.out_kind = out_kind;
   a.recs = static_cast<ChunkRec *>(workspace);
+  const int rec_nch = a.nch > a.ctrl_nch ? a.nch : a.ctrl_nch;
   a.rows = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) +
-                                     align_up((size_t)batch * a.nch * sizeof(ChunkRec), 256));
+                                     align_up((size_t)batch * rec_nch * sizeof(ChunkRec), 256));
   a.err = err_word;
   frame_kernel<<<(unsigned)batch, SB, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return launch_status();
+}
+
+extern "C" int pkv_codebook_frame_sample(const float *base, const float *fb, int n_codebooks,
+                                         int batch, int vocab, const int32_t *slots,
+                                         const int32_t *active, int num_slots,
+                                         const uint64_t *seeds, int64_t *steps,
+                                         const float *temperature, const int32_t *top_k,
+                                         const float *top_p, int32_t *out_codes,
+                                         int32_t *out_kind, void *workspace,
+                                         size_t workspace_bytes, int32_t *err_word,
+                                         void *stream) {
+  return launch_frame(nullptr, 0, 0, base, fb, n_codebooks, batch, vocab, slots, active, num_slots,
+                      seeds, steps, temperature, top_k, top_p, out_codes, out_kind, workspace,
+                      workspace_bytes, err_word, stream);
+}
+
+extern "C" int pkv_frame_sample(const float *ctrl_logits, int ctrl_vocab, int32_t stop_ctrl,
+                                const float *base, const float *fb, int n_codebooks, int batch,
+                                int vocab, const int32_t *slots, const int32_t *active,
+                                int num_slots, const uint64_t *seeds, int64_t *steps,
+                                const float *temperature, const int32_t *top_k,
+                                const float *top_p, int32_t *out_rows, int32_t *out_kind,
+                                void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                void *stream) {
+  if (!ctrl_logits || ctrl_vocab <= 0 || stop_ctrl < 0 || stop_ctrl >= ctrl_vocab)
+    return PKV_ERR_INVALID_ARG;
+  return launch_frame(ctrl_logits, ctrl_vocab, stop_ctrl, base, fb, n_codebooks, batch, vocab,
+                      slots, active, num_slots, seeds, steps, temperature, top_k, top_p, out_rows,
+                      out_kind, workspace, workspace_bytes, err_word, stream);
 }

@@ -3,9 +3,11 @@
 ``DecodeStep`` owns the device-side inputs and outputs of one batch (page
 tables, lengths, per-slot sampler state, attention outputs, workspaces) and
 runs the hot path: for every layer kv_append then paged_decode_attn, then
-seeded_sample over the logits, then (frame workloads) one
-codebook_frame_sample.  It only orders calls and allocates buffers with
-torch; all arithmetic happens in libpkv's kernels.
+seeded_sample over the logits, then (frame workloads) one frame: a
+frame_sample (stop/continue on channel 0, then the codebooks) when the
+workload has control logits, else a codebook_frame_sample.  It only orders
+calls and allocates buffers with torch; all arithmetic happens in libpkv's
+kernels.
 """
 from __future__ import annotations
 
@@ -59,9 +61,14 @@ class DecodeStep:
         self.frame_ws = None
         if tensors.base is not None:
             n_cb, _, Vf = tensors.base.shape
-            self.frame_ws = torch.empty(B.frame_workspace_bytes(n_cb, Bn, Vf), dtype=torch.uint8,
-                                        device=dev)
-            self.out_codes = torch.empty((Bn, n_cb), dtype=i32, device=dev)
+            if tensors.ctrl is not None:
+                # frame rows: channel 0 the control token, then the codes
+                nbytes = B.frame_sample_workspace_bytes(n_cb, Bn, Vf, tensors.ctrl.shape[1])
+                self.out_codes = torch.empty((Bn, 1 + n_cb), dtype=i32, device=dev)
+            else:
+                nbytes = B.frame_workspace_bytes(n_cb, Bn, Vf)
+                self.out_codes = torch.empty((Bn, n_cb), dtype=i32, device=dev)
+            self.frame_ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
             self.frame_kind = torch.empty(Bn, dtype=i32, device=dev)
         self.err = torch.zeros(1, dtype=i32, device=dev)
 
@@ -87,6 +94,12 @@ class DecodeStep:
 
     def frame(self, stream=None):
         t = self.t
+        if t.ctrl is not None:
+            B.frame_sample(t.ctrl, self.cfg.ctrl_stop, t.base, t.fb, self.slots, self.active,
+                           self.seeds, self.steps, self.temperature, self.top_k, self.top_p,
+                           self.out_codes, self.frame_kind, self.frame_ws, err_word=self.err,
+                           stream=stream)
+            return
         B.codebook_frame_sample(t.base, t.fb, self.slots, self.active, self.seeds, self.steps,
                                 self.temperature, self.top_k, self.top_p, self.out_codes,
                                 self.frame_kind, self.frame_ws, err_word=self.err, stream=stream)

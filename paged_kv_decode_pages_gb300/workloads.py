@@ -16,8 +16,10 @@ Recipe:
   * contexts (seq_len after the append) and page permutations:
     ``numpy.random.default_rng(2000 + config index)``;
   * cache, q, k, v ~ N(0, 1) bf16, logits ~ N(0, sigma^2) fp32, frame
-    base ~ N(0, sigma^2), frame feedback ~ N(0, 1): ``torch.Generator`` seeded
-    1000 + config index (Tiny: 0), drawn in a fixed order;
+    base ~ N(0, sigma^2), frame feedback ~ N(0, 1), frame control logits
+    ~ N(0, sigma_c^2) with ``ctrl_stop_bias`` added to the stop token's:
+    ``torch.Generator`` seeded 1000 + config index (Tiny: 0), drawn in a
+    fixed order;
   * request r of config c samples with seed 10000 * c + r (Tiny: r), at step 0;
   * pages are handed out from page 1 in row order, contiguously, or as a
     random permutation of 1..P-1 for the Llama-3.2-3B shape;
@@ -57,6 +59,10 @@ class Config:
     n_codebooks: int = 0                  # > 0: the step ends with a codebook frame
     frame_vocab: int = 0
     frame_logit_std: float = 0.0
+    ctrl_vocab: int = 0                   # > 0: the frame opens with a stop/continue sample
+    ctrl_stop: int = 1                    # the control token that means stop
+    ctrl_logit_std: float = 1.0
+    ctrl_stop_bias: float = 0.0
 
     @property
     def batch(self) -> int:
@@ -88,7 +94,8 @@ CONFIGS = {
         name="qwen3_4b_frame", index=3, num_layers=36, num_qo_heads=32, num_kv_heads=8,
         head_dim=128, page_size=16, n_active=32, n_pad=0, ctx_lo=256, ctx_hi=8192,
         vocab=1024, logit_std=3.0, temperature=0.9, top_k=40, top_p=0.9, n_codebooks=12,
-        frame_vocab=1024, frame_logit_std=3.0),
+        frame_vocab=1024, frame_logit_std=3.0, ctrl_vocab=2, ctrl_stop=1, ctrl_logit_std=1.0,
+        ctrl_stop_bias=-2.0),
     "long_context": Config(
         name="long_context", index=4, num_layers=36, num_qo_heads=32, num_kv_heads=8,
         head_dim=128, page_size=16, n_active=8, n_pad=8, ctx_lo=16384, ctx_hi=32768,
@@ -205,13 +212,17 @@ class Tensors:
             self.logits.normal_(0.0, cfg.logit_std, generator=g)
         if with_frame is None:
             with_frame = cfg.n_codebooks > 0
-        self.base = self.fb = None
+        self.base = self.fb = self.ctrl = None
         if with_frame and cfg.n_codebooks > 0:
             Vf = cfg.frame_vocab
             self.base = torch.empty((cfg.n_codebooks, B, Vf), dtype=torch.float32, device=device)
             self.base.normal_(0.0, cfg.frame_logit_std, generator=g)
             self.fb = torch.empty((cfg.n_codebooks, Vf, Vf), dtype=torch.float32, device=device)
             self.fb.normal_(0.0, 1.0, generator=g)
+            if cfg.ctrl_vocab > 0:
+                self.ctrl = torch.empty((B, cfg.ctrl_vocab), dtype=torch.float32, device=device)
+                self.ctrl.normal_(0.0, cfg.ctrl_logit_std, generator=g)
+                self.ctrl[:, cfg.ctrl_stop] += cfg.ctrl_stop_bias
         self.layers = L
 
 

@@ -41,6 +41,7 @@ def test_full_size_step_sampled_rows(name):
     logits = dev.logits.cpu().numpy()
     base = None if dev.base is None else dev.base.cpu().numpy()
     fb = None if dev.fb is None else dev.fb.cpu().numpy()
+    ctrl = None if dev.ctrl is None else dev.ctrl.cpu().numpy()
     qkv = {(l, b): (W.bf16_bits(dev.q[l, b:b + 1]), W.bf16_bits(dev.k[l, b:b + 1]),
                     W.bf16_bits(dev.v[l, b:b + 1])) for l in layers for b in rows}
     steps0 = batch.steps.copy()
@@ -87,9 +88,14 @@ def test_full_size_step_sampled_rows(name):
 
     if base is not None:
         f_steps = s_steps.copy()
-        codes, fkind, finfo, bad = oracle.codebook_frame_sample(
-            base, fb, batch.slots, batch.active, batch.seeds, f_steps, batch.temperature,
-            batch.top_k, batch.top_p)
+        if ctrl is not None:  # channel 0 (stop/continue), then the codes
+            codes, fkind, finfo, bad = oracle.frame_sample(
+                ctrl, cfg.ctrl_stop, base, fb, batch.slots, batch.active, batch.seeds, f_steps,
+                batch.temperature, batch.top_k, batch.top_p)
+        else:
+            codes, fkind, finfo, bad = oracle.codebook_frame_sample(
+                base, fb, batch.slots, batch.active, batch.seeds, f_steps, batch.temperature,
+                batch.top_k, batch.top_p)
         got = step.out_codes.cpu().numpy()
         for r in range(got.shape[0]):
             for j in range(got.shape[1]):

@@ -255,3 +255,90 @@ def test_frame_without_feedback_equals_salted_samples():
     for j in range(cfg.n_codebooks):
         tok, _, _, _ = gpu_sample(host.base[j].numpy(), rows, salt=1 + j, advance=False)
         np.testing.assert_array_equal(codes[:, j][batch.active == 1], tok[batch.active == 1])
+
+
+# ---------------------------------------------------------------------------
+# Full frame: stop/continue on channel 0 gating the codebooks
+# ---------------------------------------------------------------------------
+def _gpu_full_frame(batch, host, ctrl, stop):
+    d = {}
+    d["slots"] = torch.from_numpy(batch.slots).cuda()
+    d["active"] = torch.from_numpy(batch.active).cuda()
+    d["seeds"] = torch.from_numpy(batch.seeds.view(np.int64)).view(torch.uint64).cuda()
+    d["steps"] = torch.from_numpy(batch.steps.copy()).cuda()
+    d["temperature"] = torch.from_numpy(batch.temperature).cuda()
+    d["top_k"] = torch.from_numpy(batch.top_k).cuda()
+    d["top_p"] = torch.from_numpy(batch.top_p).cuda()
+    n_cb, B, V = host.base.shape
+    rows = torch.full((B, 1 + n_cb), -7, dtype=torch.int32, device="cuda")
+    kind = torch.empty(B, dtype=torch.int32, device="cuda")
+    ws = torch.empty(pkv.frame_sample_workspace_bytes(n_cb, B, V, ctrl.shape[1]),
+                     dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.frame_sample(torch.from_numpy(ctrl).cuda(), stop, host.base.cuda(),
+                     None if host.fb is None else host.fb.cuda(), d["slots"], d["active"],
+                     d["seeds"], d["steps"], d["temperature"], d["top_k"], d["top_p"], rows, kind,
+                     ws, err_word=err)
+    torch.cuda.synchronize()
+    return rows.cpu().numpy(), kind.cpu().numpy(), d["steps"].cpu().numpy(), int(err.item())
+
+
+def _compare_frame_rows(got, want, info):
+    """Identical up to the first near-tie of a row, after which the feedback
+    may legitimately diverge."""
+    for b in range(got.shape[0]):
+        for j in range(got.shape[1]):
+            if got[b, j] != want[b, j]:
+                nt = info[b, j]
+                assert nt["top2_gap_rel"] < NEAR or nt["member_margin"] < NEAR, (b, j)
+                break
+
+
+@pytest.mark.parametrize("ctrl_vocab,stop,bias", [
+    (2, 1, -1.0),      # the configuration's channel 0: continue / stop
+    (2, 1, 0.0),       # about half the rows stop
+    (300, 17, 2.0),    # a larger control vocabulary (a single chunk)
+    (9000, 8191, 4.0), # control vocabulary over two chunks, stop in the first
+])
+def test_full_frame_matches_oracle(ctrl_vocab, stop, bias):
+    cfg = W.CONFIGS["qwen3_4b_frame"]
+    batch, host = _frame(cfg, 33, True)  # the 32 rows of the configuration + 1 padding row
+    rng = np.random.default_rng(ctrl_vocab + stop)
+    ctrl = rng.normal(0, 1.0, (batch.B, ctrl_vocab)).astype(np.float32)
+    ctrl[:, stop] += np.float32(bias)
+    rows, kind, steps, err = _gpu_full_frame(batch, host, ctrl, stop)
+    assert err == 0
+    wsteps = batch.steps.copy()
+    wrows, wkind, info, bad = oracle.frame_sample(ctrl, stop, host.base.numpy(), host.fb.numpy(),
+                                                  batch.slots, batch.active, batch.seeds, wsteps,
+                                                  batch.temperature, batch.top_k, batch.top_p)
+    assert bad == 0
+    np.testing.assert_array_equal(steps, wsteps)
+    _compare_frame_rows(rows, wrows, info)
+    agree = rows[:, 0] == wrows[:, 0]
+    np.testing.assert_array_equal(kind[agree], wkind[agree])
+    stopped = (rows[:, 0] == stop) & (batch.active == 1)
+    assert np.all(rows[stopped, 1:] == pkv.CODE_PAD)
+    assert np.all(kind[stopped] == pkv.KIND_STOP)
+    assert np.all(kind[(rows[:, 0] != stop) & (batch.active == 1)] == pkv.KIND_AUDIO)
+    assert np.all(rows[batch.active == 0] == 0)
+
+
+def test_full_frame_stop_and_continue_both_occur_in_the_configuration():
+    cfg = W.CONFIGS["qwen3_4b_frame"]
+    batch = W.make_batch(cfg)
+    host = W.Tensors(batch, device="cpu", layers=1, with_logits=False, with_frame=True)
+    rows, kind, _, err = _gpu_full_frame(batch, host, host.ctrl.numpy(), cfg.ctrl_stop)
+    assert err == 0
+    act = batch.active == 1
+    n_stop = int((kind[act] == pkv.KIND_STOP).sum())
+    assert 0 < n_stop < int(act.sum()), n_stop
+
+
+def test_full_frame_rejects_a_stop_token_outside_the_control_vocabulary():
+    cfg = W.CONFIGS["qwen3_4b_frame"]
+    batch, host = _frame(cfg, 5, True)
+    ctrl = np.zeros((batch.B, 2), np.float32)
+    with pytest.raises(pkv.PkvError) as e:
+        _gpu_full_frame(batch, host, ctrl, 2)
+    assert e.value.status == 1  # PKV_ERR_INVALID_ARG
