@@ -71,12 +71,15 @@ class SampleInfo(ctypes.Structure):
         ("pad_", ctypes.c_int32),
         ("top2_gap_rel", ctypes.c_double),
         ("member_margin", ctypes.c_double),
+        ("logprob_raw", ctypes.c_double),
+        ("logprob_proc", ctypes.c_double),
     ]
 
 
 _INFO_DTYPE = np.dtype([
     ("token", np.int32), ("n_kept", np.int32), ("greedy", np.int32),
     ("pad_", np.int32), ("top2_gap_rel", np.float64), ("member_margin", np.float64),
+    ("logprob_raw", np.float64), ("logprob_proc", np.float64),
 ])
 
 _P = ctypes.c_void_p
@@ -162,6 +165,12 @@ def _load(path):
     L.pkvo_codebook_frame_sample.restype = _I
     L.pkvo_codebook_frame_sample.argtypes = [_P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
                                              _P, _P, _P, _P, _P, _P]
+    L.pkvo_sample_row_ext.restype = ctypes.c_int32
+    L.pkvo_sample_row_ext.argtypes = [_P, _I, _U64, _I64, _U32, _F, ctypes.c_int32, _F, _F, _F,
+                                      _P, _I, ctypes.POINTER(SampleInfo)]
+    L.pkvo_seeded_sample_ext.restype = _I
+    L.pkvo_seeded_sample_ext.argtypes = [_P, _I64, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P,
+                                         _P, _P, _P, _P, _I, _U32, _I, _P, _P, _P, _P]
     L.pkvo_frame_sample.restype = _I
     L.pkvo_frame_sample.argtypes = [_P, _I, ctypes.c_int32, _P, _P, _I, _I, _I, _P, _P, _I,
                                     _P, _P, _P, _P, _P, _P, _P, _P]
@@ -257,6 +266,56 @@ def sample_row(logits, seed, step, salt, temperature, top_k, top_p):
     tok = lib().pkvo_sample_row(_ptr(x), x.shape[0], int(seed), int(step), int(salt),
                                 float(temperature), int(top_k), float(top_p), ctypes.byref(info))
     return int(tok), {f: getattr(info, f) for f, _ in SampleInfo._fields_ if f != "pad_"}
+
+
+def sample_row_ext(logits, seed, step, salt, temperature, top_k, top_p, min_p=0.0,
+                   rep_penalty=1.0, pen_tokens=()):
+    """One row with the further controls (repetition penalty over
+    ``pen_tokens``, min_p) and log-probs; returns (token, info dict)."""
+    x = _c(logits, np.float32)
+    pt = np.ascontiguousarray(pen_tokens, np.int32)
+    info = SampleInfo()
+    tok = lib().pkvo_sample_row_ext(_ptr(x), x.shape[0], int(seed), int(step), int(salt),
+                                    float(temperature), int(top_k), float(top_p), float(min_p),
+                                    float(rep_penalty), _ptr(pt) if pt.size else None, pt.size,
+                                    ctypes.byref(info))
+    return int(tok), {f: getattr(info, f) for f, _ in SampleInfo._fields_ if f != "pad_"}
+
+
+def seeded_sample_ext(logits, slots, active, seeds, steps, temperature, top_k, top_p,
+                      min_p=None, rep_penalty=None, rep_window=None, history=None,
+                      hist_len=None, salt=0, advance=True):
+    """seeded_sample with min_p / repetition penalty (per slot, each None =
+    off), the per-slot history ring ``history`` int32 [num_slots, cap] and
+    ``hist_len`` int32 [num_slots] (updated in place when advance, like
+    ``steps``).  Returns (out_tok, logprob_raw, logprob_proc, info, n_bad)."""
+    x = _c(logits, np.float32)
+    B, V = x.shape
+    sl = _c(slots, np.int32)
+    ac = _c(active, np.int32)
+    sd = _c(seeds, np.uint64)
+    assert steps.dtype == np.int64 and steps.flags.c_contiguous
+    tp = _c(temperature, np.float32)
+    tk = _c(top_k, np.int32)
+    pp = _c(top_p, np.float32)
+    mp = None if min_p is None else _c(min_p, np.float32)
+    rp = None if rep_penalty is None else _c(rep_penalty, np.float32)
+    rw = None if rep_window is None else _c(rep_window, np.int32)
+    cap = 0
+    if history is not None:
+        assert history.dtype == np.int32 and history.flags.c_contiguous
+        assert hist_len.dtype == np.int32 and hist_len.flags.c_contiguous
+        cap = history.shape[1]
+    out_tok = np.zeros(B, np.int32)
+    lraw = np.zeros(B, np.float32)
+    lproc = np.zeros(B, np.float32)
+    info = np.zeros(B, _INFO_DTYPE)
+    bad = lib().pkvo_seeded_sample_ext(_ptr(x), V, B, V, _ptr(sl), _ptr(ac), sd.shape[0],
+                                       _ptr(sd), _ptr(steps), _ptr(tp), _ptr(tk), _ptr(pp),
+                                       _ptr(mp), _ptr(rp), _ptr(rw), _ptr(history), _ptr(hist_len),
+                                       cap, int(salt), int(bool(advance)), _ptr(out_tok),
+                                       _ptr(lraw), _ptr(lproc), _ptr(info))
+    return out_tok, lraw, lproc, info, bad
 
 
 def token_kind(tok, stop_tokens=(), audio_lo=0, audio_hi=0):

@@ -335,8 +335,12 @@ typedef struct {
   int32_t greedy;       /* 1 when temperature <= 1e-5 */
   int32_t pad_;
   double top2_gap_rel;  /* (best - second) / max(1, |best|) over kept, +inf if 1 kept */
-  double member_margin; /* min distance of a top-p prefix sum from p*Z, relative to Z
-                           (+inf when top-p is off or no boundary exists) */
+  double member_margin; /* min distance of a top-p prefix sum from p*Z, relative to Z,
+                           and of exp(x - x_max) from min_p at the min_p cut
+                           (+inf when both are off or no boundary exists) */
+  double logprob_raw;   /* log-softmax of the unprocessed logits at the token */
+  double logprob_proc;  /* log-probability of the token in the distribution it
+                           was drawn from (0 for greedy) */
 } pkvo_sample_info;
 
 typedef struct {
@@ -352,31 +356,70 @@ static int cmp_xid(const void *a, const void *b) {
   return (p->id > q->id) - (p->id < q->id);
 }
 
-/* logits: fp32 [V].  Returns the sampled token. */
-int32_t pkvo_sample_row(const float *logits, int V, uint64_t seed, int64_t step,
-                        uint32_t salt, float temperature, int32_t top_k,
-                        float top_p, pkvo_sample_info *info) {
+/* logits: fp32 [V].  Returns the sampled token.  The order of the
+ * transforms is the pages' (Chatterbox notes: repetition penalty ->
+ * temperature -> min_p -> top_p), with top-k after the temperature:
+ *   1. repetition penalty: each distinct id of pen_tokens[0..n_pen) in
+ *      [0, V) gets logit / rep_penalty if the logit is positive, else
+ *      logit * rep_penalty, in fp32 like the logits (rep_penalty 1: off);
+ *   2. temperature: x = logit / T (<= 1e-5: greedy argmax, lowest id);
+ *   3. top-k (0 or >= V: off);
+ *   4. min_p (<= 0: off): rank r of the order is kept iff r == 0 or
+ *      exp(x_r - x_max) >= min_p;
+ *   5. top-p over the renormalised survivors (R7 rule);
+ *   6. Gumbel-max over the kept tokens.
+ * info (may be NULL) also gets the log-softmax of the raw logits at the
+ * token and its log-probability under the renormalised kept set. */
+int32_t pkvo_sample_row_ext(const float *logits, int V, uint64_t seed, int64_t step,
+                            uint32_t salt, float temperature, int32_t top_k,
+                            float top_p, float min_p, float rep_penalty,
+                            const int32_t *pen_tokens, int n_pen,
+                            pkvo_sample_info *info) {
   pkvo_sample_info local;
   if (!info) info = &local;
   memset(info, 0, sizeof *info);
   info->top2_gap_rel = INFINITY;
   info->member_margin = INFINITY;
 
+  /* raw log-softmax normaliser */
+  double mraw = -INFINITY, zraw = 0.0;
+  for (int i = 0; i < V; ++i)
+    if ((double)logits[i] > mraw) mraw = (double)logits[i];
+  for (int i = 0; i < V; ++i) zraw += exp((double)logits[i] - mraw);
+  const double lse_raw = mraw + log(zraw);
+
+  /* 1. repetition penalty on a copy */
+  float *pl = (float *)malloc(sizeof(float) * (size_t)(V > 0 ? V : 1));
+  memcpy(pl, logits, sizeof(float) * (size_t)V);
+  if (rep_penalty != 1.0f && n_pen > 0) {
+    unsigned char *done = (unsigned char *)calloc((size_t)V, 1);
+    for (int i = 0; i < n_pen; ++i) {
+      const int32_t t = pen_tokens[i];
+      if (t < 0 || t >= V || done[t]) continue;
+      done[t] = 1;
+      pl[t] = pl[t] > 0.0f ? pl[t] / rep_penalty : pl[t] * rep_penalty;
+    }
+    free(done);
+  }
+
   if (!(temperature > 1e-5f)) {
     /* greedy: the first maximum, i.e. the lowest id among equal logits */
     int32_t best = 0;
     for (int i = 1; i < V; ++i)
-      if (logits[i] > logits[best]) best = i;
+      if (pl[i] > pl[best]) best = i;
     info->token = best;
     info->n_kept = 1;
     info->greedy = 1;
+    info->logprob_raw = (double)logits[best] - lse_raw;
+    info->logprob_proc = 0.0;
+    free(pl);
     return best;
   }
 
   xid_t *ord = (xid_t *)malloc(sizeof(xid_t) * (size_t)V);
   const double T = (double)temperature;
   for (int i = 0; i < V; ++i) {
-    ord[i].x = (double)logits[i] / T;
+    ord[i].x = (double)pl[i] / T;
     ord[i].id = i;
   }
   qsort(ord, (size_t)V, sizeof(xid_t), cmp_xid);
@@ -384,20 +427,30 @@ int32_t pkvo_sample_row(const float *logits, int V, uint64_t seed, int64_t step,
   /* top-k: 0 or >= V means no filter */
   int K = (top_k > 0 && top_k < V) ? top_k : V;
 
-  /* top-p over the renormalised top-k survivors */
-  int kept = K;
+  const double m = ord[0].x;
+  double *e = (double *)malloc(sizeof(double) * (size_t)K);
+  for (int r = 0; r < K; ++r) e[r] = exp(ord[r].x - m);
+
+  /* min_p over the top-k survivors */
+  int Kp = K;
+  if (min_p > 0.0f) {
+    Kp = 1;
+    while (Kp < K && e[Kp] >= (double)min_p) ++Kp;
+    double d = fabs(e[Kp - 1] - (double)min_p);
+    if (Kp < K && fabs(e[Kp] - (double)min_p) < d) d = fabs(e[Kp] - (double)min_p);
+    if (Kp > 1 || Kp < K) info->member_margin = d;
+  }
+
+  /* top-p over the renormalised survivors */
+  int kept = Kp;
+  double S = 0.0; /* mass of the kept tokens */
+  for (int r = 0; r < Kp; ++r) S += e[r];
   if (top_p < 1.0f) {
-    const double m = ord[0].x;
-    double *e = (double *)malloc(sizeof(double) * (size_t)K);
-    double Z = 0.0;
-    for (int r = 0; r < K; ++r) {
-      e[r] = exp(ord[r].x - m);
-      Z += e[r];
-    }
+    const double Z = S;
     const double pz = (double)top_p * Z;
-    double S = 0.0; /* S_{r-1}: mass of the tokens before r */
+    S = 0.0; /* S_{r-1}: mass of the tokens before r */
     kept = 0;
-    for (int r = 0; r < K; ++r) {
+    for (int r = 0; r < Kp; ++r) {
       if (r == 0 || S < pz) {
         kept = r + 1;
         S += e[r];
@@ -412,18 +465,18 @@ int32_t pkvo_sample_row(const float *logits, int V, uint64_t seed, int64_t step,
       for (int r = 0; r + 1 < kept; ++r) Sprev += e[r];
       double margin = INFINITY;
       if (kept >= 2) margin = fabs(pz - Sprev) / Z;
-      if (kept < K) {
+      if (kept < Kp) {
         double d2 = fabs(S - pz) / Z;
         if (d2 < margin) margin = d2;
       }
-      info->member_margin = margin;
+      if (margin < info->member_margin) info->member_margin = margin;
     }
-    free(e);
   }
 
   /* Gumbel-max over the kept tokens */
   double best = -INFINITY, second = -INFINITY;
   int32_t best_id = ord[0].id;
+  double best_x = ord[0].x;
   for (int r = 0; r < kept; ++r) {
     int32_t id = ord[r].id;
     double sc = ord[r].x + pkvo_gumbel(seed, salt, id, step);
@@ -431,6 +484,7 @@ int32_t pkvo_sample_row(const float *logits, int V, uint64_t seed, int64_t step,
       second = best;
       best = sc;
       best_id = id;
+      best_x = ord[r].x;
     } else if (sc > second) {
       second = sc;
     }
@@ -441,8 +495,19 @@ int32_t pkvo_sample_row(const float *logits, int V, uint64_t seed, int64_t step,
   }
   info->token = best_id;
   info->n_kept = kept;
+  info->logprob_raw = (double)logits[best_id] - lse_raw;
+  info->logprob_proc = (best_x - m) - log(S);
+  free(e);
   free(ord);
+  free(pl);
   return best_id;
+}
+
+int32_t pkvo_sample_row(const float *logits, int V, uint64_t seed, int64_t step,
+                        uint32_t salt, float temperature, int32_t top_k,
+                        float top_p, pkvo_sample_info *info) {
+  return pkvo_sample_row_ext(logits, V, seed, step, salt, temperature, top_k, top_p, 0.0f,
+                             1.0f, NULL, 0, info);
 }
 
 /* stop_tokens() / audio_tokens() of "Adding a Model", section "2. The
@@ -499,6 +564,81 @@ int pkvo_seeded_sample(const float *logits, int64_t row_stride, int B, int V,
       int32_t s = slots[b];
       if (s < 0 || s >= num_slots) continue;
       steps[s] += 1;
+    }
+  }
+  return bad;
+}
+
+/* ------------------------------------------------------------------ */
+/* pkvo_seeded_sample with the further sampling controls of the        */
+/* program's sampler settings ("Adding a Model", section "2. The       */
+/* program": min_p, repetition_penalty, repetition_window) in the      */
+/* order of pkvo_sample_row_ext, and the raw / processed log-probs     */
+/* ("Adding a Model": enable_logprobs, "logprobs_mode": "processed").   */
+/*   min_p, rep_penalty float [num_slots], rep_window int32 [num_slots] */
+/*   (each may be NULL: off / off / whole history);                    */
+/*   history int32 [num_slots][hist_cap], hist_len int32 [num_slots]:  */
+/*   the slot's sampled tokens as a ring (token n at n % hist_cap);     */
+/*   the penalised ids are the last w = min(window, hist_len, hist_cap) */
+/*   (window < 0: min(hist_len, hist_cap); 0: none) of them.  With      */
+/*   advance, the sampled token is appended (history may be NULL: no   */
+/*   penalty and nothing appended).  logprob_raw / logprob_proc float  */
+/*   [B] (each may be NULL); padding rows get 0.                       */
+/* ------------------------------------------------------------------ */
+int pkvo_seeded_sample_ext(const float *logits, int64_t row_stride, int B, int V,
+                           const int32_t *slots, const int32_t *active,
+                           int num_slots, const uint64_t *seeds, int64_t *steps,
+                           const float *temperature, const int32_t *top_k,
+                           const float *top_p, const float *min_p,
+                           const float *rep_penalty, const int32_t *rep_window,
+                           int32_t *history, int32_t *hist_len, int hist_cap,
+                           uint32_t salt, int advance, int32_t *out_tok,
+                           float *logprob_raw, float *logprob_proc,
+                           pkvo_sample_info *info) {
+  int bad = 0;
+  int32_t *pen = (int32_t *)malloc(sizeof(int32_t) * (size_t)(hist_cap > 0 ? hist_cap : 1));
+  for (int b = 0; b < B; ++b) {
+    pkvo_sample_info local;
+    pkvo_sample_info *in = info ? &info[b] : &local;
+    memset(in, 0, sizeof *in);
+    in->top2_gap_rel = INFINITY;
+    in->member_margin = INFINITY;
+    out_tok[b] = 0;
+    if (logprob_raw) logprob_raw[b] = 0.0f;
+    if (logprob_proc) logprob_proc[b] = 0.0f;
+    if (!active[b]) continue;
+    int32_t s = slots[b];
+    if (s < 0 || s >= num_slots) {
+      ++bad;
+      continue;
+    }
+    int n_pen = 0;
+    if (history && hist_cap > 0) {
+      const int64_t len = hist_len[s];
+      const int32_t w = rep_window ? rep_window[s] : -1;
+      int64_t n = len < hist_cap ? len : hist_cap;
+      if (w >= 0 && w < n) n = w;
+      for (int64_t i = 0; i < n; ++i) pen[n_pen++] = history[(int64_t)s * hist_cap + (len - 1 - i) % hist_cap];
+    }
+    int32_t tok = pkvo_sample_row_ext(logits + (int64_t)b * row_stride, V, seeds[s], steps[s],
+                                      salt, temperature[s], top_k[s], top_p[s],
+                                      min_p ? min_p[s] : 0.0f,
+                                      rep_penalty ? rep_penalty[s] : 1.0f, pen, n_pen, in);
+    out_tok[b] = tok;
+    if (logprob_raw) logprob_raw[b] = (float)in->logprob_raw;
+    if (logprob_proc) logprob_proc[b] = (float)in->logprob_proc;
+  }
+  free(pen);
+  if (advance) {
+    for (int b = 0; b < B; ++b) {
+      if (!active[b]) continue;
+      int32_t s = slots[b];
+      if (s < 0 || s >= num_slots) continue;
+      steps[s] += 1;
+      if (history && hist_cap > 0) {
+        history[(int64_t)s * hist_cap + hist_len[s] % hist_cap] = out_tok[b];
+        hist_len[s] += 1;
+      }
     }
   }
   return bad;

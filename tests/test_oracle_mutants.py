@@ -46,6 +46,19 @@ MUTANTS = [
      "for (int j = 1; j < W; ++j) r[j] = 0;"),
     ("a stop still samples the codes", "      out_kind[b] = PKVO_KIND_STOP;\n      continue;",
      "      out_kind[b] = PKVO_KIND_STOP;"),
+    ("penalty multiplies positive logits", "pl[t] = pl[t] > 0.0f ? pl[t] / rep_penalty : pl[t] * rep_penalty;",
+     "pl[t] = pl[t] * rep_penalty;"),
+    ("penalty compounds repeats", "if (t < 0 || t >= V || done[t]) continue;",
+     "if (t < 0 || t >= V) continue;"),
+    ("min_p keeps strictly above", "while (Kp < K && e[Kp] >= (double)min_p) ++Kp;",
+     "while (Kp < K && e[Kp] > (double)min_p) ++Kp;"),
+    ("top-p ignores min_p", "  for (int r = 0; r < Kp; ++r) S += e[r];\n  if (top_p < 1.0f) {",
+     "  for (int r = 0; r < K; ++r) S += e[r];\n  if (top_p < 1.0f) {"),
+    ("raw log-prob from the penalised logits", "  for (int i = 0; i < V; ++i) zraw += exp((double)logits[i] - mraw);",
+     "  for (int i = 0; i < V; ++i) zraw += exp((double)logits[i] - mraw + 0.25 * (i == 0));"),
+    ("penalty window from the oldest token",
+     "pen[n_pen++] = history[(int64_t)s * hist_cap + (len - 1 - i) % hist_cap];",
+     "pen[n_pen++] = history[(int64_t)s * hist_cap + i % hist_cap];"),
 ]
 
 
@@ -72,6 +85,14 @@ def _pins():
         ("full frame gating", TS.test_full_frame_channel0_is_the_salt0_sample_and_gates_the_codes),
         ("full frame never stops", TS.test_full_frame_that_never_stops_is_the_codebook_frame),
         ("full frame always stops", TS.test_full_frame_that_always_stops_is_a_pad_row),
+        ("ext off", TS.test_ext_with_the_controls_off_is_the_base_sampler),
+        ("raw logprob", TS.test_raw_logprob_is_scipy_log_softmax_of_the_unprocessed_logits),
+        ("processed logprob forms", TS.test_processed_logprob_closed_forms),
+        ("penalty rule", TS.test_repetition_penalty_rule_closed_form),
+        ("min_p ties", TS.test_min_p_keeps_exactly_the_ties_with_the_maximum_at_one),
+        ("history ring", TS.test_seeded_sample_ext_history_ring_and_window),
+        ("processed logprob freq", lambda: TS.test_processed_logprob_is_the_sampling_distribution(
+            0.8, 6, 0.9, 0.05, 1.8)),
         ("gumbel moments", TS.test_gumbel_moments),
         ("chi-square", lambda: TS.test_gumbel_max_frequencies_chi_square(0, 1.0, 1.0)),
     ]

@@ -361,3 +361,144 @@ def test_full_frame_that_always_stops_is_a_pad_row():
     for b in (0, 2):
         assert list(rows[b]) == [STOP] + [oracle.CODE_PAD] * 12 and kind[b] == oracle.KIND_STOP
     assert list(steps) == [0, 2, 3]
+
+
+# ---------------------------------------------------------------------------
+# Further controls: repetition penalty, min_p; raw / processed log-probs
+# ---------------------------------------------------------------------------
+def test_ext_with_the_controls_off_is_the_base_sampler():
+    rng = np.random.default_rng(31)
+    for trial in range(40):
+        x = rng.normal(0, 2, 300).astype(np.float32)
+        k, p, T = [(0, 1.0, 1.0), (20, 0.9, 0.7), (0, 0.5, 1.3), (5, 1.0, 0.8)][trial % 4]
+        a = oracle.sample_row(x, 7, trial, 3, T, k, p)[0]
+        b = oracle.sample_row_ext(x, 7, trial, 3, T, k, p, min_p=0.0, rep_penalty=1.0,
+                                  pen_tokens=[1, 2, 3])[0]
+        assert a == b
+
+
+def test_raw_logprob_is_scipy_log_softmax_of_the_unprocessed_logits():
+    scipy_special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(32)
+    for trial in range(20):
+        x = rng.normal(0, 3, 500).astype(np.float32)
+        tok, info = oracle.sample_row_ext(x, 9, trial, 0, 0.8, 40, 0.9, min_p=0.05,
+                                          rep_penalty=1.7, pen_tokens=list(range(0, 500, 7)))
+        want = scipy_special.log_softmax(x.astype(np.float64))[tok]
+        assert abs(info["logprob_raw"] - want) < 1e-12
+
+
+def test_processed_logprob_closed_forms():
+    rng = np.random.default_rng(33)
+    x = rng.normal(0, 2, 64).astype(np.float32)
+    # no processing at T = 1: the raw log-prob
+    _, info = oracle.sample_row_ext(x, 1, 2, 0, 1.0, 0, 1.0)
+    assert abs(info["logprob_proc"] - info["logprob_raw"]) < 1e-12
+    # a point mass: greedy, top-k 1, min_p 1 without ties
+    for kw in (dict(temperature=0.0, top_k=0), dict(temperature=1.0, top_k=1),
+               dict(temperature=1.0, top_k=0, min_p=1.0)):
+        T, k = kw.pop("temperature"), kw.pop("top_k")
+        _, info = oracle.sample_row_ext(x, 1, 2, 0, T, k, 1.0, **kw)
+        assert info["logprob_proc"] == 0.0 and info["n_kept"] == 1
+
+
+@pytest.mark.parametrize("T,k,p,min_p,pen", [(1.0, 0, 1.0, 0.1, 1.0), (0.8, 6, 0.9, 0.05, 1.8),
+                                             (1.5, 0, 0.7, 0.2, 0.6)])
+def test_processed_logprob_is_the_sampling_distribution(T, k, p, min_p, pen):
+    """Gumbel-max frequencies over many steps against exp(logprob_proc)
+    reported for each drawn token (a chi-square over the kept tokens)."""
+    scipy_stats = pytest.importorskip("scipy.stats")
+    rng = np.random.default_rng(34)
+    x = rng.normal(0, 0.5, 12).astype(np.float32)
+    pen_tokens = [0, 3, 3, 7]
+    n = 20000
+    counts = {}
+    prob = {}
+    for step in range(n):
+        tok, info = oracle.sample_row_ext(x, 5, step, 0, T, k, p, min_p=min_p, rep_penalty=pen,
+                                          pen_tokens=pen_tokens)
+        counts[tok] = counts.get(tok, 0) + 1
+        lp = info["logprob_proc"]
+        if tok in prob:
+            assert abs(prob[tok] - lp) < 1e-12  # the same distribution every step
+        prob[tok] = lp
+    toks = sorted(counts)
+    assert len(toks) >= 3, toks  # the filters leave a distribution to test
+    p_obs = np.array([counts[t] for t in toks], float)
+    p_exp = np.exp(np.array([prob[t] for t in toks]))
+    assert abs(p_exp.sum() - 1.0) < 1e-3  # every kept token was drawn
+    chi2, pv = scipy_stats.chisquare(p_obs, p_exp / p_exp.sum() * n)
+    assert pv > 1e-4, (pv, toks)
+
+
+def test_repetition_penalty_rule_closed_form():
+    """Greedy picks expose the penalised logits: positive / pen, negative
+    * pen, zero unchanged, once per distinct id, ids outside [0, V) ignored."""
+    x = np.array([3.0, 2.5, -1.0, -1.2, 0.0, -4.0], np.float32)
+    g = lambda pen, toks: oracle.sample_row_ext(x, 0, 0, 0, 0.0, 0, 1.0, rep_penalty=pen,
+                                                pen_tokens=toks)[0]
+    assert g(1.5, [0]) == 1                  # 3 / 1.5 = 2 < 2.5
+    assert g(1.1, [0]) == 0                  # 3 / 1.1 > 2.5
+    assert g(1.1, [0, 0, 0, 0]) == 0         # not compounded by repeats
+    y = np.array([-1.0, -1.2, -5.0], np.float32)
+    gy = lambda pen, toks: oracle.sample_row_ext(y, 0, 0, 0, 0.0, 0, 1.0, rep_penalty=pen,
+                                                 pen_tokens=toks)[0]
+    assert gy(1.3, [0]) == 1                 # -1.3 < -1.2
+    assert gy(1.3, [0, -1, 7]) == 1          # out-of-range ids are ignored
+    z = np.array([0.0, -0.5], np.float32)
+    assert oracle.sample_row_ext(z, 0, 0, 0, 0.0, 0, 1.0, rep_penalty=50.0,
+                                 pen_tokens=[0])[0] == 0  # 0 stays 0
+
+
+def test_min_p_keeps_exactly_the_ties_with_the_maximum_at_one():
+    x = np.array([1.0, 2.0, 2.0, 1.999, 2.0], np.float32)
+    seen = set()
+    for step in range(300):
+        tok, info = oracle.sample_row_ext(x, 3, step, 0, 1.0, 0, 1.0, min_p=1.0)
+        assert info["n_kept"] == 3
+        seen.add(tok)
+    assert seen == {1, 2, 4}
+
+
+def test_seeded_sample_ext_history_ring_and_window():
+    V = 16
+    x = np.zeros((2, V), np.float32)
+    x[:, 5] = 2.0
+    x[:, 9] = 1.9
+    slots = np.array([1, 2], np.int32)
+    active = np.array([1, 1], np.int32)
+    seeds = np.array([0, 11, 12], np.uint64)
+    T = np.zeros(3, np.float32)  # greedy: the penalty decides
+    K = np.zeros(3, np.int32)
+    P = np.ones(3, np.float32)
+    pen = np.full(3, 2.0, np.float32)
+    win = np.array([-1, 1, 1], np.int32)
+    cap = 4
+    hist = np.zeros((3, cap), np.int32)
+    hlen = np.zeros(3, np.int32)
+    # slot 1: history ring [5, 3, 3, 3, 3] (len 5 wraps): window 1 sees only the last 3
+    for t in (5, 3, 3, 3, 3):
+        hist[1, hlen[1] % cap] = t
+        hlen[1] += 1
+    # slot 2: history [5, 1, 2]: window 1 sees only the newest, 2 (not 5)
+    for t in (5, 1, 2):
+        hist[2, hlen[2] % cap] = t
+        hlen[2] += 1
+    steps = np.zeros(3, np.int64)
+    tok, lraw, lproc, info, bad = oracle.seeded_sample_ext(x, slots, active, seeds, steps, T, K, P,
+                                                           rep_penalty=pen, rep_window=win,
+                                                           history=hist, hist_len=hlen)
+    assert bad == 0 and list(tok) == [5, 5]
+    assert list(hlen) == [0, 6, 4] and hist[1, 5 % cap] == 5 and hist[2, 3] == 5
+    # with the whole history in the window slot 2 avoids 5
+    hist2, hlen2 = np.zeros((3, cap), np.int32), np.zeros(3, np.int32)
+    for t in (5, 1, 2):
+        hist2[2, hlen2[2] % cap] = t
+        hlen2[2] += 1
+    tok2, _, _, _, _ = oracle.seeded_sample_ext(x, slots, active, seeds, np.zeros(3, np.int64),
+                                                T, K, P, rep_penalty=pen,
+                                                rep_window=np.array([-1, 1, -1], np.int32),
+                                                history=hist2, hist_len=hlen2)
+    assert tok2[1] == 9
+    assert list(steps) == [0, 1, 1]
+    assert np.all(lproc == 0.0)  # greedy
