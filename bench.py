@@ -363,6 +363,23 @@ def main(argv=None):
     sampler_us = s0.elapsed_time(s1) / n_samp * 1e3
     barrier()
 
+    # ---- the sampler with min_p, repetition penalty and log-probs ------
+    ext_line = None
+    if tensors.logits is not None:
+        ext_set = dict(min_p=0.05, rep_penalty=1.2, rep_window=-1, hist_cap=256)
+        step.enable_ext(**ext_set)
+        for _ in range(3):
+            step.sample_ext(stream=stream)
+        s0.record(stream)
+        for _ in range(n_samp):
+            step.sample_ext(stream=stream)
+        s1.record(stream)
+        s1.synchronize()
+        ext_us = s0.elapsed_time(s1) / n_samp * 1e3
+        ext_line = {"us_per_call": ext_us, "rows_per_s": sizes["n_active"] / (ext_us / 1e6),
+                    "settings": dict(ext_set, logprobs="raw and processed")}
+        barrier()
+
     # ---- the frame alone (frame workloads), same stream ----------------
     frame_line = None
     if tensors.base is not None:
@@ -429,6 +446,7 @@ def main(argv=None):
         "sampled_rows_per_s": world * sizes["n_active"] * args.steps / (total_ms / 1e3),
         "sampler": {"us_per_call": sampler_us,
                     "rows_per_s": sizes["n_active"] / (sampler_us / 1e6)},
+        **({"sampler_ext": ext_line} if ext_line else {}),
         **({"frame": frame_line} if frame_line else {}),
         "attn": {"us_per_layer": attn_avg_s * 1e6, "gbs": achieved,
                  "bytes_per_layer": sizes["attn_per_layer"]},

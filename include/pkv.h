@@ -52,6 +52,7 @@ extern "C" {
 #define PKV_DEV_ERR_SLOT 0x4    /* active row slot outside [0, num_slots)     */
 #define PKV_DEV_ERR_TIMEOUT 0x8 /* a bounded wait on an async copy gave up    */
 #define PKV_DEV_ERR_LOGITS 0x10 /* NaN or +inf logit in an active row         */
+#define PKV_DEV_ERR_HISTORY 0x20 /* negative token-history length             */
 
 /* ---- out_kind codes ("Adding a Model", section "How a program runs":
  *      out_kind is audio frame, stop, or other) ------------------------- */
@@ -239,6 +240,83 @@ int pkv_seeded_sample(const float *logits, int64_t row_stride, int batch,
                       int32_t *out_kind, void *workspace,
                       size_t workspace_bytes, int32_t *err_word,
                       void *stream);
+
+/* ------------------------------------------------------------------------
+ * The further sampler settings of a program ("Adding a Model", section
+ * "2. The program": min_p, repetition_penalty, repetition_window) and the
+ * log-probs it may ask for ("Supported Models", "Qwen3.5 / Qwen3.8":
+ * enable_logprobs, and "logprobs_mode": "processed"), applied in the order
+ * of that page's Chatterbox notes with top-k before min_p.  Every pointer
+ * may be NULL, which turns that control off.  All arrays are device
+ * memory.
+ *
+ *   min_p        fp32 [num_slots]: after top-k, keep rank r >= 1 only while
+ *                exp(x_r - x_max) >= min_p[s] (the ranks that pass form a
+ *                prefix of the order; <= 0 is off).
+ *   rep_penalty  fp32 [num_slots]: before temperature, each distinct token
+ *                of the slot's penalty window has its logit divided by the
+ *                penalty when positive and multiplied by it otherwise (fp32,
+ *                correctly rounded); 1 is off.
+ *   rep_window   int32 [num_slots]: the window is the last
+ *                min(rep_window[s], hist_len[s], hist_cap) sampled tokens
+ *                (a negative window, or NULL: min(hist_len[s], hist_cap)).
+ *   history      int32 [num_slots][hist_cap]: the slot's sampled tokens as
+ *                a ring, token n of the slot at n % hist_cap; with advance,
+ *                the new token is stored at hist_len[s] % hist_cap and
+ *                hist_len[s] incremented.  NULL: no penalty, nothing stored.
+ *   hist_len     int32 [num_slots] (required with history; a negative
+ *                entry raises PKV_DEV_ERR_HISTORY and that slot's row is
+ *                sampled without penalty and stores nothing).
+ *   hist_cap     ring capacity (> 0 with history).
+ *   logprob_raw  fp32 [batch]: log-softmax of the unprocessed logits at the
+ *                sampled token.
+ *   logprob_proc fp32 [batch]: log of the sampled token's probability in
+ *                the distribution it was drawn from (after penalty,
+ *                temperature, top-k, min_p and top-p, renormalised over the
+ *                kept tokens); 0 for greedy rows.
+ * Both log-probs are computed in fp64 and rounded to fp32 (the raw
+ * normaliser's terms within 3e-9 of themselves); padding rows get 0.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_sample_ext {
+  const float *min_p;
+  const float *rep_penalty;
+  const int32_t *rep_window;
+  int32_t *history;
+  int32_t *hist_len;
+  int32_t hist_cap;
+  float *logprob_raw;
+  float *logprob_proc;
+} pkv_sample_ext_t;
+
+/* Workspace (bytes) pkv_seeded_sample_ext needs for these sizes (enough for
+ * any settings; pkv_sample_workspace_bytes suffices when no row can be
+ * penalised, i.e. history or rep_penalty is NULL). */
+size_t pkv_sample_ext_workspace_bytes(int batch, int vocab);
+
+/* ------------------------------------------------------------------------
+ * pkv_seeded_sample_ext -- pkv_seeded_sample with the settings of
+ * pkv_sample_ext_t, applied in the order repetition penalty, temperature,
+ * top-k, min_p, top-p (top-p renormalised over the tokens that pass top-k
+ * and min_p), then the same Gumbel-max draw.  ext == NULL, or all its
+ * pointers NULL, is exactly pkv_seeded_sample.  Arguments and results
+ * otherwise as for pkv_seeded_sample; the struct itself is read on the host
+ * during the call.  Two active rows must not share a slot.
+ * Errors: as pkv_seeded_sample; PKV_ERR_INVALID_ARG also for history
+ * without hist_len or with hist_cap <= 0, and for misaligned arrays.
+ * Device: as pkv_seeded_sample, and PKV_DEV_ERR_HISTORY.
+ * ---------------------------------------------------------------------- */
+int pkv_seeded_sample_ext(const float *logits, int64_t row_stride, int batch,
+                          int vocab, const int32_t *slots,
+                          const int32_t *active, int num_slots,
+                          const uint64_t *seeds, int64_t *steps,
+                          const float *temperature, const int32_t *top_k,
+                          const float *top_p, uint32_t salt, int advance,
+                          const int32_t *stop_tokens, int n_stop,
+                          int32_t audio_lo, int32_t audio_hi,
+                          int32_t *out_tok, int32_t *out_kind,
+                          const pkv_sample_ext_t *ext, void *workspace,
+                          size_t workspace_bytes, int32_t *err_word,
+                          void *stream);
 
 /* Workspace (bytes) pkv_codebook_frame_sample needs for these sizes. */
 size_t pkv_frame_workspace_bytes(int n_codebooks, int batch, int vocab);

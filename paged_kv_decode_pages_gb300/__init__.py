@@ -13,7 +13,7 @@ does, and raises if it is missing.
 _BINDING = (
     "load", "library_path", "version", "error_string", "PkvError",
     "kv_append", "paged_decode_attn", "decode_workspace_bytes", "paged_decode_attn_static",
-    "seeded_sample", "sample_workspace_bytes",
+    "seeded_sample", "sample_workspace_bytes", "seeded_sample_ext", "sample_ext_workspace_bytes",
     "codebook_frame_sample", "frame_workspace_bytes",
     "frame_sample", "frame_sample_workspace_bytes",
     "KIND_OTHER", "KIND_AUDIO", "KIND_STOP", "CODE_PAD",

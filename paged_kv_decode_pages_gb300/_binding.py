@@ -27,6 +27,12 @@ class pkv_cache_t(ctypes.Structure):
                 ("num_kv_heads", _I32), ("head_dim", _I32)]
 
 
+class pkv_sample_ext_t(ctypes.Structure):
+    _fields_ = [("min_p", _P), ("rep_penalty", _P), ("rep_window", _P), ("history", _P),
+                ("hist_len", _P), ("hist_cap", _I32), ("logprob_raw", _P),
+                ("logprob_proc", _P)]
+
+
 # every symbol include/pkv.h declares, with its ctypes signature
 SIGNATURES = {
     "pkv_version": (ctypes.c_char_p, []),
@@ -42,6 +48,10 @@ SIGNATURES = {
     "pkv_sample_workspace_bytes": (_SZ, [_I, _I]),
     "pkv_seeded_sample": (_I, [_P, _I64, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _U32, _I, _P,
                                _I, _I32, _I32, _P, _P, _P, _SZ, _P, _P]),
+    "pkv_sample_ext_workspace_bytes": (_SZ, [_I, _I]),
+    "pkv_seeded_sample_ext": (_I, [_P, _I64, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _U32, _I,
+                                   _P, _I, _I32, _I32, _P, _P, ctypes.POINTER(pkv_sample_ext_t),
+                                   _P, _SZ, _P, _P]),
     "pkv_frame_workspace_bytes": (_SZ, [_I, _I, _I]),
     "pkv_codebook_frame_sample": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _SZ, _P, _P]),
@@ -222,6 +232,53 @@ def seeded_sample(logits, slots, active, seeds, steps, temperature, top_k, top_p
         int(audio_hi), _ptr(out_tok), _ptr(out_kind), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream))
     _check("pkv_seeded_sample", st)
+
+
+def sample_ext_workspace_bytes(batch, vocab) -> int:
+    return int(load().pkv_sample_ext_workspace_bytes(batch, vocab))
+
+
+def seeded_sample_ext(logits, slots, active, seeds, steps, temperature, top_k, top_p, out_tok,
+                      out_kind, workspace, min_p=None, rep_penalty=None, rep_window=None,
+                      history=None, hist_len=None, logprob_raw=None, logprob_proc=None, salt=0,
+                      advance=True, stop_tokens=None, audio_lo=0, audio_hi=0, err_word=None,
+                      stream=None):
+    """seeded_sample with the further settings (each None = off): min_p,
+    rep_penalty fp32 [num_slots], rep_window int32 [num_slots], the token
+    ring history int32 [num_slots, cap] with hist_len int32 [num_slots]
+    (appended to when advance), and the fp32 [B] log-prob outputs."""
+    import torch
+    if logits.dtype != torch.float32 or logits.stride(-1) != 1 or not logits.is_cuda:
+        raise TypeError("logits must be a CUDA fp32 tensor with unit last stride")
+    B, V = logits.shape
+    for t, dt, nm in ((slots, torch.int32, "slots"), (active, torch.int32, "active"),
+                      (seeds, torch.uint64, "seeds"), (steps, torch.int64, "steps"),
+                      (temperature, torch.float32, "temperature"), (top_k, torch.int32, "top_k"),
+                      (top_p, torch.float32, "top_p"), (out_tok, torch.int32, "out_tok"),
+                      (out_kind, torch.int32, "out_kind")):
+        _req(t, dt, nm)
+    for t, dt, nm in ((min_p, torch.float32, "min_p"), (rep_penalty, torch.float32, "rep_penalty"),
+                      (rep_window, torch.int32, "rep_window"), (history, torch.int32, "history"),
+                      (hist_len, torch.int32, "hist_len"),
+                      (logprob_raw, torch.float32, "logprob_raw"),
+                      (logprob_proc, torch.float32, "logprob_proc")):
+        if t is not None:
+            _req(t, dt, nm)
+    cap = 0
+    if history is not None:
+        if history.dim() != 2 or history.shape[1] < 1 or hist_len is None:
+            raise ValueError("history must be [num_slots, cap >= 1] and comes with hist_len")
+        cap = history.shape[1]
+    ext = pkv_sample_ext_t(_ptr(min_p), _ptr(rep_penalty), _ptr(rep_window), _ptr(history),
+                           _ptr(hist_len), cap, _ptr(logprob_raw), _ptr(logprob_proc))
+    n_stop = 0 if stop_tokens is None else stop_tokens.numel()
+    st = load().pkv_seeded_sample_ext(
+        _ptr(logits), logits.stride(0), B, V, _ptr(slots), _ptr(active), seeds.numel(),
+        _ptr(seeds), _ptr(steps), _ptr(temperature), _ptr(top_k), _ptr(top_p), int(salt),
+        int(bool(advance)), _ptr(stop_tokens) if n_stop else None, n_stop, int(audio_lo),
+        int(audio_hi), _ptr(out_tok), _ptr(out_kind), ctypes.byref(ext), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream))
+    _check("pkv_seeded_sample_ext", st)
 
 
 def frame_workspace_bytes(n_codebooks, batch, vocab) -> int:

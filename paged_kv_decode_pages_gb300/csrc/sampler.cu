@@ -43,6 +43,15 @@
 //    needing more than 512 tokens), take an exact general path that streams
 //    the row: radix select of the top-k threshold and progressive sorted
 //    extraction until the top-p crossing.
+//  * further settings (pkv_seeded_sample_ext; "Adding a Model", "2. The
+//    program", in the order of the Chatterbox notes of "Supported Models"
+//    with top-k before min_p): the repetition penalty is applied to the
+//    order keys of the window's tokens as the chunk pass loads them (a
+//    shared bitmap per chunk, copied to the workspace for the general
+//    path); min_p cuts the sorted candidates at the first rank >= 1 with
+//    exp(x - x_max) < min_p and top-p renormalises over the ranks before
+//    it; the raw log-prob uses per-chunk log-sum-exp partials of the
+//    unprocessed logits, the processed one the kept ranks' mass.
 //  * the frame kernel runs the same chunk pass and finish for each of the
 //    codebooks in turn inside one CTA per row.
 #include <math.h>
@@ -71,7 +80,9 @@ struct ChunkRec {
   int32_t ncand;       // candidates kept
   uint64_t thr;        // the smallest of them when the chunk holds more tokens (else 0)
   uint64_t cand[NCAND];
-  uint64_t pad_[2];
+  float rmax;          // largest unprocessed logit of the chunk      (raw log-probs)
+  float rzh, rzl;      // sum over the chunk of exp(logit - rmax)      (raw log-probs)
+  uint32_t gkey;       // order key of gid                            (MODE_ALL)
 };
 static_assert(sizeof(ChunkRec) % 64 == 0, "ChunkRec");
 
@@ -86,7 +97,21 @@ struct RowParams {
   int mode;
   int nc;      // candidates per chunk
   float c2h, c2l;  // log2(e) / T as a double-float
+  // further controls (pkv_seeded_sample_ext; all off otherwise)
+  float min_p;           // <= 0: off
+  float pen;             // repetition penalty
+  int n_pen;             // window length (0: no penalty)
+  const int32_t *hist;   // the slot's ring of sampled tokens
+  int64_t hist_len;
+  int hist_cap;
+  int lp_raw, lp_proc;   // log-probs requested
+  int need_z;            // chunk pass computes the normaliser over the whole row
 };
+
+// i-th newest token of the penalty window
+__device__ __forceinline__ int32_t pen_token(const RowParams &P, int i) {
+  return P.hist[(P.hist_len - 1 - i) % P.hist_cap];
+}
 
 // ---------------------------------------------------------------------------
 // double-float arithmetic (Dekker 1971; Knuth TAOCP vol. 2, 4.2.2)
@@ -166,9 +191,9 @@ struct Exp2Ctx {
   float c2h, c2l, th, tl;
 };
 
-__device__ __forceinline__ Exp2Ctx exp2_ctx(const RowParams &P, float vmax) {
-  const DF tm = df_mul_f(DF{P.c2h, P.c2l}, vmax);
-  return {P.c2h, P.c2l, tm.h, tm.l};
+__device__ __forceinline__ Exp2Ctx exp2_ctx(float c2h, float c2l, float vmax) {
+  const DF tm = df_mul_f(DF{c2h, c2l}, vmax);
+  return {c2h, c2l, tm.h, tm.l};
 }
 
 // 2^(v * c2 - tm) as a normalised double-float; 0 below 2^-125 and for a
@@ -267,6 +292,25 @@ __device__ __forceinline__ double comp_x(uint64_t c, float temperature) {
   return (double)key_value((uint32_t)(c >> 32)) / (double)temperature;
 }
 
+// repetition penalty of one logit: a positive logit is divided by the
+// penalty, any other multiplied by it (fp32, correctly rounded)
+__device__ __forceinline__ float penalise(float v, float pen) {
+  return v > 0.0f ? __fdiv_rn(v, pen) : __fmul_rn(v, pen);
+}
+
+// A logits row as the sampler sees it: the fp32 values with the penalty
+// applied to the tokens marked in pbits (one bit per token; null: none).
+struct RowView {
+  const float *x;
+  const uint32_t *pbits;
+  float pen;
+  __device__ __forceinline__ uint32_t key(int i, bool &bad) const {
+    float v = x[i];
+    if (pbits != nullptr && ((pbits[i >> 5] >> (i & 31)) & 1u)) v = penalise(v, pen);
+    return order_key(v, bad);
+  }
+};
+
 // ---------------------------------------------------------------------------
 // shared scratch
 // ---------------------------------------------------------------------------
@@ -285,7 +329,12 @@ struct SampSmem {
   int32_t token;
   int32_t kept;
   int32_t done;
+  int32_t kp;
   double zsum;
+  double s_kept;     // mass (relative to the row maximum) of the kept tokens
+  double m_row;      // x of the row maximum
+  double xbest;      // x of the sampled token
+  uint32_t penbits[CHUNK / 32];  // penalised tokens of the chunk
   uint64_t sortbuf[GEN_BLOCK];
   double es[GEN_BLOCK];
 };
@@ -442,8 +491,22 @@ __device__ void select_bin(SampSmem &sm, int shift) {
 // ---------------------------------------------------------------------------
 // chunk pass
 // ---------------------------------------------------------------------------
+// sum over the chunk of 2^(v * c2 - t_max), in double-float; all threads
+// get it
+__device__ __forceinline__ DF chunk_exp_sum(const uint32_t (&key)[EPT], int cnt,
+                                            const Exp2Ctx &ctx, SampSmem &sm) {
+  DF acc = {0.0f, 0.0f};
+#pragma unroll
+  for (int j = 0; j < EPT; ++j)
+    if ((int)threadIdx.x + j * SB < cnt)
+      df_accumulate(acc, df_exp2_rel(key_value(key[j]), ctx, sm.e2h, sm.e2l));
+  return block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
+}
+
+// pbits: the row's penalty bitmap in global memory, written for this chunk
+// when the row is penalised (may be null otherwise)
 __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const RowParams &P,
-                           ChunkRec *rec, SampSmem &sm, int32_t *err) {
+                           ChunkRec *rec, uint32_t *pbits, SampSmem &sm, int32_t *err) {
   const int tid = threadIdx.x;
   const int start = c * CHUNK;
   const int cnt = min(CHUNK, V - start);
@@ -455,6 +518,43 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
     key[j] = (i < cnt) ? order_key(row[start + i], bad) : 0u;  // may be written by this kernel: no __ldg
   }
   if (bad) report(err, PKV_DEV_ERR_LOGITS);
+  if (P.lp_raw) {
+    // raw log-softmax partials: chunk maximum of the unprocessed logits and
+    // sum exp(logit - max) = sum 2^((logit - max) log2(e))
+    uint32_t km = 0;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j)
+      if (tid + j * SB < cnt) km = key[j] > km ? key[j] : km;
+    const float rmax = key_value((uint32_t)block_max_u64(km, sm));
+    const DF z = chunk_exp_sum(key, cnt, exp2_ctx(LOG2E_H, LOG2E_L, rmax), sm);
+    if (tid == 0) {
+      rec->rmax = rmax;
+      rec->rzh = z.h;
+      rec->rzl = z.l;
+    }
+  }
+  if (P.n_pen > 0) {
+    // the penalty window's tokens that fall in this chunk, as a bitmap
+    // (a token repeated in the window is penalised once)
+    for (int w = tid; w < CHUNK / 32; w += SB) sm.penbits[w] = 0u;
+    __syncthreads();
+    for (int i = tid; i < P.n_pen; i += SB) {
+      const int32_t t = pen_token(P, i);
+      if (t >= start && t < start + cnt)
+        atomicOr(&sm.penbits[(t - start) >> 5], 1u << ((t - start) & 31));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int i = tid + j * SB;
+      if (i < cnt && ((sm.penbits[i >> 5] >> (i & 31)) & 1u)) {
+        bool b2 = false;
+        key[j] = order_key(penalise(key_value(key[j]), P.pen), b2);
+      }
+    }
+    if (pbits != nullptr)
+      for (int w = tid; w < (cnt + 31) / 32; w += SB) pbits[c * (CHUNK / 32) + w] = sm.penbits[w];
+  }
   uint64_t mine = 0;
 #pragma unroll
   for (int j = 0; j < EPT; ++j) {
@@ -471,6 +571,7 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
   if (P.mode == MODE_ALL) {
     double bs = 0.0;
     int bid = -1;
+    uint32_t bkey = 0;
 #pragma unroll
     for (int j = 0; j < EPT; ++j) {
       const int i = tid + j * SB;
@@ -480,6 +581,7 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
         if (better(s, tok, bs, bid)) {
           bs = s;
           bid = tok;
+          bkey = key[j];
         }
       }
     }
@@ -489,70 +591,66 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
       rec->gscore = best;
       rec->gid = id;
     }
-    return;
-  }
-
-  // the chunk's nc largest composites
-  const int nc = P.nc;
-  uint64_t thr = 0;  // keep composites >= thr
-  if (cnt > nc) {
-    if (tid == 0) {
-      sm.sel_prefix = 0;
-      sm.sel_want = (uint32_t)nc;
-      sm.sel_done = 0;
-    }
-    __syncthreads();
-    uint64_t mask = 0;
-    for (int pass = 0; pass < 8; ++pass) {
-      const int shift = 56 - 8 * pass;
-      for (int i = tid; i < 256; i += SB) sm.hist[i] = 0;
+    if (bid == id && id >= 0) rec->gkey = bkey;
+  } else {
+    // the chunk's nc largest composites
+    const int nc = P.nc;
+    uint64_t thr = 0;  // keep composites >= thr
+    if (cnt > nc) {
+      if (tid == 0) {
+        sm.sel_prefix = 0;
+        sm.sel_want = (uint32_t)nc;
+        sm.sel_done = 0;
+      }
       __syncthreads();
-      const uint64_t prefix = sm.sel_prefix;
+      uint64_t mask = 0;
+      for (int pass = 0; pass < 8; ++pass) {
+        const int shift = 56 - 8 * pass;
+        for (int i = tid; i < 256; i += SB) sm.hist[i] = 0;
+        __syncthreads();
+        const uint64_t prefix = sm.sel_prefix;
 #pragma unroll
-      for (int j = 0; j < EPT; ++j) {
-        const int i = tid + j * SB;
-        if (i < cnt) {
-          const uint64_t cc = composite(key[j], start + i);
-          if ((cc & mask) == prefix) atomicAdd(&sm.hist[(cc >> shift) & 255u], 1u);
+        for (int j = 0; j < EPT; ++j) {
+          const int i = tid + j * SB;
+          if (i < cnt) {
+            const uint64_t cc = composite(key[j], start + i);
+            if ((cc & mask) == prefix) atomicAdd(&sm.hist[(cc >> shift) & 255u], 1u);
+          }
+        }
+        __syncthreads();
+        select_bin(sm, shift);
+        mask |= 255ull << shift;
+        if (sm.sel_done) break;
+      }
+      thr = sm.sel_prefix;
+      __syncthreads();
+    }
+    if (tid == 0) sm.cnt = 0;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int i = tid + j * SB;
+      if (i < cnt) {
+        const uint64_t cc = composite(key[j], start + i);
+        if (cc >= thr) {
+          const uint32_t pos = atomicAdd(&sm.cnt, 1u);
+          if (pos < (uint32_t)nc) rec->cand[pos] = cc;
         }
       }
-      __syncthreads();
-      select_bin(sm, shift);
-      mask |= 255ull << shift;
-      if (sm.sel_done) break;
     }
-    thr = sm.sel_prefix;
     __syncthreads();
-  }
-  if (tid == 0) sm.cnt = 0;
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < EPT; ++j) {
-    const int i = tid + j * SB;
-    if (i < cnt) {
-      const uint64_t cc = composite(key[j], start + i);
-      if (cc >= thr) {
-        const uint32_t pos = atomicAdd(&sm.cnt, 1u);
-        if (pos < (uint32_t)nc) rec->cand[pos] = cc;
-      }
+    const int got = min((int)sm.cnt, nc);
+    for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0;
+    if (tid == 0) {
+      rec->ncand = got;
+      rec->thr = cnt > nc ? thr : 0ull;
     }
-  }
-  __syncthreads();
-  const int got = min((int)sm.cnt, nc);
-  for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0;
-  if (tid == 0) {
-    rec->ncand = got;
-    rec->thr = cnt > nc ? thr : 0ull;
   }
 
-  if (P.mode == MODE_TOPP_FULL) {
+  if (P.need_z) {
     // sum over the chunk of exp(x - mx) = 2^(t - t_max), t = logit * log2(e) / T
-    const Exp2Ctx ctx = exp2_ctx(P, key_value((uint32_t)(top1 >> 32)));
-    DF acc = {0.0f, 0.0f};
-#pragma unroll
-    for (int j = 0; j < EPT; ++j)
-      if (tid + j * SB < cnt) df_accumulate(acc, df_exp2_rel(key_value(key[j]), ctx, sm.e2h, sm.e2l));
-    const DF z = block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
+    const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
+    const DF z = chunk_exp_sum(key, cnt, ctx, sm);
     if (tid == 0) {
       rec->mx = comp_x(top1, P.temperature);
       rec->z = (double)z.h + (double)z.l;
@@ -598,7 +696,7 @@ __device__ uint64_t select_rank_of(int n, Get get, uint64_t upper, int rank, Sam
 
 // Composite of rank `rank` (0-based, descending) among elements with
 // composite < upper.  Requires that many such elements to exist.
-__device__ uint64_t select_rank(const float *__restrict__ row, int V, uint64_t upper, int rank,
+__device__ uint64_t select_rank(const RowView &rv, int V, uint64_t upper, int rank,
                                 SampSmem &sm) {
   if (threadIdx.x == 0) {
     sm.sel_prefix = 0;
@@ -614,7 +712,7 @@ __device__ uint64_t select_rank(const float *__restrict__ row, int V, uint64_t u
     const uint64_t prefix = sm.sel_prefix;
     bool dummy = false;
     for (int i = threadIdx.x; i < V; i += SB) {
-      const uint64_t cc = composite(order_key(row[i], dummy), i);
+      const uint64_t cc = composite(rv.key(i, dummy), i);
       if (cc < upper && (cc & mask) == prefix) atomicAdd(&sm.hist[(cc >> shift) & 255u], 1u);
     }
     __syncthreads();
@@ -628,39 +726,49 @@ __device__ uint64_t select_rank(const float *__restrict__ row, int V, uint64_t u
 }
 
 // z_known >= 0: the normaliser over the top-k survivors, already computed
-// relative to the row maximum (top-p over the whole vocabulary).
-__device__ int general_sample(const float *__restrict__ row, int V, const RowParams &P,
-                              uint64_t top1, double z_known, SampSmem &sm) {
+// relative to the row maximum (top-p over the whole vocabulary, min_p off).
+// With log-probs requested, leaves the kept mass, the row maximum's x and
+// the sampled token's x in sm.s_kept, sm.m_row and sm.xbest.
+__device__ int general_sample(const RowView &rv, int V, const RowParams &P, uint64_t top1,
+                              double z_known, SampSmem &sm) {
   const int tid = threadIdx.x;
   const int K = P.K;
-  const uint64_t thrK = (K < V) ? select_rank(row, V, ~0ull, K - 1, sm) : 0ull;
+  const uint64_t thrK = (K < V) ? select_rank(rv, V, ~0ull, K - 1, sm) : 0ull;
+  const double m = comp_x(top1, P.temperature);
+  const bool minp = P.min_p > 0.0f;
+  const bool topp = P.top_p < 1.0f;
+  bool dummy = false;
   uint64_t thr = thrK;
-  if (P.top_p < 1.0f) {
-    const double m = comp_x(top1, P.temperature);
-    bool dummy = false;
+  double S = 0.0;  // top-p: the kept mass
+  if (topp) {
     double z = z_known;
     if (z < 0.0) {
+      // the normaliser over the top-k survivors that pass min_p
       z = 0.0;
       for (int i = tid; i < V; i += SB) {
-        const uint32_t key = order_key(row[i], dummy);
-        if (composite(key, i) >= thrK) z += exp((double)key_value(key) / (double)P.temperature - m);
+        const uint32_t key = rv.key(i, dummy);
+        const uint64_t cc = composite(key, i);
+        if (cc >= thrK) {
+          const double e = exp((double)key_value(key) / (double)P.temperature - m);
+          if (!minp || cc == top1 || e >= (double)P.min_p) z += e;
+        }
       }
       z = block_sum_d(z, sm);
     }
     const double pz = (double)P.top_p * z;
-    // progressive sorted extraction until the running sum reaches p * Z
+    // progressive sorted extraction until the running sum reaches p * Z or
+    // a token falls below min_p
     uint64_t upper = ~0ull;
     int taken = 0;
-    double S = 0.0;
     uint64_t cutoff = top1;
     bool done = false;
     while (!done) {
       const int M = min(GEN_BLOCK, K - taken);
-      const uint64_t lo = select_rank(row, V, upper, M - 1, sm);
+      const uint64_t lo = select_rank(rv, V, upper, M - 1, sm);
       if (tid == 0) sm.cnt = 0;
       __syncthreads();
       for (int i = tid; i < V; i += SB) {
-        const uint64_t cc = composite(order_key(row[i], dummy), i);
+        const uint64_t cc = composite(rv.key(i, dummy), i);
         if (cc >= lo && cc < upper) {
           const uint32_t pos = atomicAdd(&sm.cnt, 1u);
           if (pos < GEN_BLOCK) sm.sortbuf[pos] = cc;
@@ -677,7 +785,7 @@ __device__ int general_sample(const float *__restrict__ row, int V, const RowPar
       if (tid == 0) {
         int r = 0;
         for (; r < M; ++r) {
-          if (taken + r == 0 || S < pz) {
+          if (taken + r == 0 || (S < pz && (!minp || sm.es[r] >= (double)P.min_p))) {
             S += sm.es[r];
             cutoff = sm.sortbuf[r];
           } else {
@@ -698,21 +806,41 @@ __device__ int general_sample(const float *__restrict__ row, int V, const RowPar
     }
     thr = cutoff;
   }
-  // Gumbel argmax over the kept tokens (composite >= thr)
-  double bs = 0.0;
+  // Gumbel argmax over the kept tokens (composite >= thr; without top-p,
+  // also passing min_p)
+  const bool filt = minp && !topp;
+  const bool mass = P.lp_proc && !topp;
+  double bs = 0.0, bx = 0.0, sk = 0.0;
   int bid = -1;
-  bool dummy = false;
   for (int i = tid; i < V; i += SB) {
-    const uint32_t key = order_key(row[i], dummy);
-    if (composite(key, i) >= thr) {
-      const double s = (double)key_value(key) / (double)P.temperature + gumbel(P, i);
+    const uint32_t key = rv.key(i, dummy);
+    const uint64_t cc = composite(key, i);
+    if (cc >= thr) {
+      const double x = (double)key_value(key) / (double)P.temperature;
+      if (filt || mass) {
+        const double e = exp(x - m);
+        if (filt && !(cc == top1 || e >= (double)P.min_p)) continue;
+        sk += e;
+      }
+      const double s = x + gumbel(P, i);
       if (better(s, i, bs, bid)) {
         bs = s;
         bid = i;
+        bx = x;
       }
     }
   }
-  return block_argmax(bs, bid, sm);
+  const int id = block_argmax(bs, bid, sm);
+  if (P.lp_proc) {
+    const double kept_mass = topp ? S : block_sum_d(sk, sm);
+    if (bid == id) sm.xbest = bx;
+    if (tid == 0) {
+      sm.s_kept = kept_mass;
+      sm.m_row = m;
+    }
+    __syncthreads();
+  }
+  return id;
 }
 
 // ---------------------------------------------------------------------------
@@ -750,7 +878,10 @@ __device__ bool topp_scan_warp(const double *es, int n, int r0, double &carry, d
 // ---------------------------------------------------------------------------
 // finish: one CTA per row
 // ---------------------------------------------------------------------------
-__device__ int finish_row(const float *__restrict__ row, int V, int nch, const RowParams &P,
+// With log-probs requested (and not greedy), leaves the kept mass relative
+// to the row maximum, that maximum's x and the sampled token's x in
+// sm.s_kept, sm.m_row and sm.xbest.
+__device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
                           const ChunkRec *recs, SampSmem &sm) {
   const int tid = threadIdx.x;
   if (P.mode == MODE_GREEDY) {
@@ -758,22 +889,40 @@ __device__ int finish_row(const float *__restrict__ row, int V, int nch, const R
     for (int c = 0; c < nch; ++c) best = recs[c].top1 > best ? recs[c].top1 : best;
     return comp_token(best);
   }
+  uint64_t top1 = 0;
+  for (int c = 0; c < nch; ++c) top1 = recs[c].top1 > top1 ? recs[c].top1 : top1;
   if (P.mode == MODE_ALL) {
     double bs = 0.0;
     int bid = -1;
+    uint32_t bkey = 0;
     for (int c = 0; c < nch; ++c)
       if (better(recs[c].gscore, recs[c].gid, bs, bid)) {
         bs = recs[c].gscore;
         bid = recs[c].gid;
+        bkey = recs[c].gkey;
       }
+    if (P.lp_proc) {
+      // the kept mass is the whole row's: the chunks' normalisers
+      const double m = comp_x(top1, P.temperature);
+      __syncthreads();
+      if (tid < nch)
+        sm.red_d[tid] = recs[tid].top1 != 0ull ? recs[tid].z * exp(recs[tid].mx - m) : 0.0;
+      __syncthreads();
+      if (tid == 0) {
+        double z = 0.0;
+        for (int c = 0; c < nch; ++c) z += sm.red_d[c];
+        sm.s_kept = z;
+        sm.m_row = m;
+        sm.xbest = (double)key_value(bkey) / (double)P.temperature;
+      }
+      __syncthreads();
+    }
     return bid;
   }
-  uint64_t top1 = 0;
-  for (int c = 0; c < nch; ++c) top1 = recs[c].top1 > top1 ? recs[c].top1 : top1;
-  if (P.mode == MODE_GENERAL) return general_sample(row, V, P, top1, -1.0, sm);
+  if (P.mode == MODE_GENERAL) return general_sample(rv, V, P, top1, -1.0, sm);
 
   // the largest of the union of the chunks' candidates, sorted: the top-k,
-  // or (top-p over the whole vocabulary) up to NCAND tokens
+  // or (K == V with top-p or min_p) up to NCAND tokens
   const int nc = P.nc;
   const int nu = nch * nc;
   const bool full = P.mode == MODE_TOPP_FULL;
@@ -809,10 +958,14 @@ __device__ int finish_row(const float *__restrict__ row, int V, int nch, const R
   block_sort_desc(sm.sortbuf, n2);
   const double m = comp_x(sm.sortbuf[0], P.temperature);
   const bool topp = P.top_p < 1.0f;
+  const bool minp = P.min_p > 0.0f;
+  // Z: the normaliser the top-p cut is taken against.  Top-p over the whole
+  // vocabulary without min_p: the chunks' partial normalisers, rescaled to
+  // the row maximum in parallel and added in chunk order; otherwise the sum
+  // over the ranks that pass top-k and min_p, once those are known.
   double Z = 0.0;
-  if (topp && full) {
-    // the chunks' partial normalisers, rescaled to the row maximum in
-    // parallel and added in chunk order
+  bool zready = false;
+  if (full && !minp) {
     if (tid < nch) sm.red_d[tid] = recs[tid].top1 != 0ull ? recs[tid].z * exp(recs[tid].mx - m) : 0.0;
     __syncthreads();
     if (tid == 0) {
@@ -822,52 +975,82 @@ __device__ int finish_row(const float *__restrict__ row, int V, int nch, const R
     }
     __syncthreads();
     Z = sm.zsum;
+    zready = true;
   }
   // e^(x - m) of the sorted candidates, in blocks of 64, 128, ... only as far
-  // as the top-p scan reaches (all of them for top-k)
-  double carry = 0.0;  // warp 0: the running sum before the block
-  int lo = 0, hi = topp && full ? min(64, nv) : nv;
+  // as the min_p boundary and the top-p scan reach (all of them for top-k)
+  double carry = 0.0;  // warp 0: the running sum before the scanned block
+  int lo = 0, hi = full ? min(64, nv) : nv;
+  int kp = minp ? -1 : nv;  // ranks [0, kp) pass min_p (-1: not found yet)
+  int scan_lo = 0;
+  if (tid == 0) sm.flag = 0;
   for (;;) {
     for (int r = lo + tid; r < hi; r += SB) sm.es[r] = exp(comp_x(sm.sortbuf[r], P.temperature) - m);
     __syncthreads();
-    if (!topp) {
-      if (tid == 0) {
-        sm.kept = nv;
-        sm.flag = 0;
+    if (kp < 0) {
+      // the first rank >= 1 below min_p (relative to the maximum)
+      if (tid < 32) {
+        int found = -1;
+        for (int base = max(lo, 1); base < hi && found < 0; base += 32) {
+          const int r = base + tid;
+          const unsigned bm = __ballot_sync(FULL_MASK, r < hi && sm.es[r] < (double)P.min_p);
+          if (bm) found = base + __ffs(bm) - 1;
+        }
+        if (tid == 0) sm.kp = found >= 0 ? found : (hi == nv ? nv : -1);
       }
+      __syncthreads();
+      kp = sm.kp;
+      __syncthreads();
+      if (kp < 0) {
+        lo = hi;
+        hi = min(2 * hi + 64, nv);
+        continue;
+      }
+      if (full && kp == nv && nv < V) {
+        // every candidate passes min_p: the boundary lies beyond them
+        if (tid == 0) sm.flag = 1;
+        __syncthreads();
+        break;
+      }
+    }
+    if (!topp) {
+      if (tid == 0) sm.kept = kp;
       __syncthreads();
       break;
     }
-    if (!full) {
-      // Z over the top-k survivors (one block)
+    if (!zready) {
       double part = 0.0;
-      for (int r = tid; r < nv; r += SB) part += sm.es[r];
+      for (int r = tid; r < kp; r += SB) part += sm.es[r];
       Z = block_sum_d(part, sm);
-      if (tid == 0) sm.zsum = Z;
+      zready = true;
     }
+    const int end = min(hi, kp);
     if (tid < 32) {
       int k;
-      const bool cut = topp_scan_warp(sm.es + lo, hi - lo, lo, carry, (double)P.top_p * Z, &k);
+      const bool cut =
+          topp_scan_warp(sm.es + scan_lo, end - scan_lo, scan_lo, carry, (double)P.top_p * Z, &k);
       if (tid == 0) {
-        sm.done = (cut || hi == nv) ? 1 : 0;
-        sm.kept = lo + k;
-        // top-p over the whole vocabulary still open after the top nc
-        sm.flag = (!cut && hi == nv && full && nv < V) ? 1 : 0;
+        sm.done = (cut || end == kp) ? 1 : 0;
+        sm.kept = scan_lo + k;
+        // top-p over the whole vocabulary still open after the candidates
+        sm.flag = (!cut && end == kp && kp == nv && full && nv < V) ? 1 : 0;
       }
     }
     __syncthreads();
     const bool done = sm.done != 0;
     __syncthreads();
     if (done) break;
+    scan_lo = end;
     lo = hi;
     hi = min(2 * hi + 64, nv);
   }
   // The extracted prefix is the exact global order over the prefix the
-  // decision read (the kept set; for top-k the K survivors) unless a chunk
-  // that holds more tokens than it gave has its last candidate strictly
-  // inside that prefix.  The top-k also needs K candidates in the union.
+  // decision read (the kept set; the ranks through the min_p boundary; for
+  // top-k the K survivors) unless a chunk that holds more tokens than it
+  // gave has its last candidate strictly inside that prefix.  The top-k
+  // also needs K candidates in the union.
   if (!sm.flag) {
-    const int decided = (topp && full) ? sm.kept : nv;
+    const int decided = !full ? nv : (minp ? min(kp + 1, nv) : sm.kept);
     const uint64_t last = sm.sortbuf[decided - 1];
     __syncthreads();
     if (tid == 0 && !full && P.K > nreal) sm.flag = 1;
@@ -876,26 +1059,43 @@ __device__ int finish_row(const float *__restrict__ row, int V, int nch, const R
   }
   // (the chunks' normaliser is exact whatever the candidates; the top-k one
   // is not when the union missed some of the top-k)
-  if (sm.flag) return general_sample(row, V, P, top1, full ? sm.zsum : -1.0, sm);
+  if (sm.flag) return general_sample(rv, V, P, top1, (full && !minp) ? Z : -1.0, sm);
   const int kept = sm.kept;
-  double bs = 0.0;
+  double bs = 0.0, bx = 0.0;
   int bid = -1;
   for (int r = tid; r < kept; r += SB) {
     const int tok = comp_token(sm.sortbuf[r]);
-    const double s = comp_x(sm.sortbuf[r], P.temperature) + gumbel(P, tok);
+    const double x = comp_x(sm.sortbuf[r], P.temperature);
+    const double s = x + gumbel(P, tok);
     if (better(s, tok, bs, bid)) {
       bs = s;
       bid = tok;
+      bx = x;
     }
   }
-  return block_argmax(bs, bid, sm);
+  const int id = block_argmax(bs, bid, sm);
+  if (P.lp_proc) {
+    double part = 0.0;
+    for (int r = tid; r < kept; r += SB) part += sm.es[r];
+    const double sk = block_sum_d(part, sm);
+    if (bid == id) sm.xbest = bx;
+    if (tid == 0) {
+      sm.s_kept = sk;
+      sm.m_row = m;
+    }
+    __syncthreads();
+  }
+  return id;
 }
 
 // ---------------------------------------------------------------------------
 // row parameters
 // ---------------------------------------------------------------------------
+// min_p > 0 turns on the min_p filter; lp_proc asks for the processed
+// log-prob (the penalty window and the raw log-prob are set by the caller)
 __device__ __forceinline__ RowParams row_params(int V, uint64_t seed, int64_t step, float temp,
-                                                int32_t top_k, float top_p, uint32_t salt) {
+                                                int32_t top_k, float top_p, uint32_t salt,
+                                                float min_p = 0.0f, int lp_proc = 0) {
   RowParams P;
   P.temperature = temp;
   P.top_k = top_k;
@@ -909,9 +1109,20 @@ __device__ __forceinline__ RowParams row_params(int V, uint64_t seed, int64_t st
   else if (P.K <= NCAND)
     P.mode = MODE_TOPK_SMALL;
   else if (P.K == V)
-    P.mode = (top_p < 1.0f) ? MODE_TOPP_FULL : MODE_ALL;
+    P.mode = (top_p < 1.0f || min_p > 0.0f) ? MODE_TOPP_FULL : MODE_ALL;
   else
     P.mode = MODE_GENERAL;
+  P.min_p = min_p;
+  P.pen = 1.0f;
+  P.n_pen = 0;
+  P.hist = nullptr;
+  P.hist_len = 0;
+  P.hist_cap = 1;
+  P.lp_raw = 0;
+  P.lp_proc = P.mode == MODE_GREEDY ? 0 : lp_proc;
+  // the whole row's normaliser: top-p over it, or the kept mass of "keep
+  // everything"; min_p takes its normaliser from the candidates instead
+  P.need_z = (P.mode == MODE_TOPP_FULL && !(min_p > 0.0f)) || (P.mode == MODE_ALL && P.lp_proc);
   // candidates per chunk: enough that the union can hold the top-k (or the
   // 512 tokens top-p over the whole vocabulary may read), and at least 64
   const int kcap = P.mode == MODE_TOPK_SMALL ? P.K : NCAND;
@@ -953,7 +1164,44 @@ struct SampleArgs {
   int32_t *out_kind;
   ChunkRec *recs;  // [B][nch]
   int32_t *err;
+  // further controls (null: off)
+  const float *min_p;          // [num_slots]
+  const float *rep_penalty;    // [num_slots]
+  const int32_t *rep_window;   // [num_slots] (null: the whole history)
+  int32_t *history;            // [num_slots][hist_cap] ring of sampled tokens
+  int32_t *hist_len;           // [num_slots]
+  int hist_cap;
+  float *lp_raw;               // [B]
+  float *lp_proc;              // [B]
+  uint32_t *pbits;             // [B][nch * CHUNK / 32] penalty bitmaps
 };
+
+__device__ __forceinline__ RowParams sample_row_params(const SampleArgs &a, int slot) {
+  RowParams P = row_params(a.vocab, a.seeds[slot], a.steps[slot], a.temperature[slot],
+                           a.top_k[slot], a.top_p[slot], a.salt,
+                           a.min_p != nullptr ? a.min_p[slot] : 0.0f, a.lp_proc != nullptr);
+  P.lp_raw = a.lp_raw != nullptr;
+  const float pen = a.rep_penalty != nullptr ? a.rep_penalty[slot] : 1.0f;
+  if (a.history != nullptr && pen != 1.0f) {
+    // the window: the last min(window, length, capacity) tokens
+    const int64_t len = a.hist_len[slot];
+    const int32_t w = a.rep_window != nullptr ? a.rep_window[slot] : -1;
+    int64_t n = len < a.hist_cap ? len : (int64_t)a.hist_cap;
+    if (w >= 0 && w < n) n = w;
+    if (n > 0) {
+      P.n_pen = (int)n;
+      P.pen = pen;
+      P.hist = a.history + (int64_t)slot * a.hist_cap;
+      P.hist_len = len;
+      P.hist_cap = a.hist_cap;
+    }
+  }
+  return P;
+}
+
+__device__ __forceinline__ uint32_t *row_pbits(const SampleArgs &a, int b) {
+  return a.pbits != nullptr ? a.pbits + (int64_t)b * a.nch * (CHUNK / 32) : nullptr;
+}
 
 __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   __shared__ SampSmem sm;
@@ -963,39 +1211,74 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) return;
   load_exp2_table(sm);  // read after the first barrier of the chunk pass
-  const RowParams P = row_params(a.vocab, a.seeds[slot], a.steps[slot], a.temperature[slot],
-                                 a.top_k[slot], a.top_p[slot], a.salt);
+  const RowParams P = sample_row_params(a, slot);
   chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, c, P, a.recs + (int64_t)b * a.nch + c,
-             sm, a.err);
+             row_pbits(a, b), sm, a.err);
+}
+
+__device__ __forceinline__ void sample_skip_row(const SampleArgs &a, int b) {
+  a.out_tok[b] = 0;
+  a.out_kind[b] = PKV_KIND_OTHER;
+  if (a.lp_raw != nullptr) a.lp_raw[b] = 0.0f;
+  if (a.lp_proc != nullptr) a.lp_proc[b] = 0.0f;
 }
 
 __global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
   __shared__ SampSmem sm;
   const int b = blockIdx.x;
+  const int tid = threadIdx.x;
   if (!a.active[b]) {
-    if (threadIdx.x == 0) {
-      a.out_tok[b] = 0;
-      a.out_kind[b] = PKV_KIND_OTHER;
-    }
+    if (tid == 0) sample_skip_row(a, b);
     return;
   }
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) {
-    if (threadIdx.x == 0) {
-      a.out_tok[b] = 0;
-      a.out_kind[b] = PKV_KIND_OTHER;
+    if (tid == 0) {
+      sample_skip_row(a, b);
       report(a.err, PKV_DEV_ERR_SLOT);
     }
     return;
   }
-  const RowParams P = row_params(a.vocab, a.seeds[slot], a.steps[slot], a.temperature[slot],
-                                 a.top_k[slot], a.top_p[slot], a.salt);
-  const int tok = finish_row(a.logits + (int64_t)b * a.row_stride, a.vocab, a.nch, P,
-                             a.recs + (int64_t)b * a.nch, sm);
-  if (threadIdx.x == 0) {
+  const RowParams P = sample_row_params(a, slot);
+  const float *row = a.logits + (int64_t)b * a.row_stride;
+  const ChunkRec *recs = a.recs + (int64_t)b * a.nch;
+  const RowView rv = {row, P.n_pen > 0 ? row_pbits(a, b) : nullptr, P.pen};
+  const int tok = finish_row(rv, a.vocab, a.nch, P, recs, sm);
+  double lse_raw = 0.0;
+  if (P.lp_raw) {
+    // log-sum-exp of the unprocessed row: the chunks' partials rescaled to
+    // the row maximum in parallel, added in chunk order
+    float rm = recs[0].rmax;
+    for (int c = 1; c < a.nch; ++c) rm = fmaxf(rm, recs[c].rmax);
+    __syncthreads();
+    if (tid < a.nch)
+      sm.red_d[tid] = ((double)recs[tid].rzh + (double)recs[tid].rzl) *
+                      exp((double)recs[tid].rmax - (double)rm);
+    __syncthreads();
+    if (tid == 0) {
+      double z = 0.0;
+      for (int c = 0; c < a.nch; ++c) z += sm.red_d[c];
+      lse_raw = (double)rm + log(z);
+    }
+  }
+  if (tid == 0) {
     a.out_tok[b] = tok;
     a.out_kind[b] = kind_of(tok, a.stop_tokens, a.n_stop, a.audio_lo, a.audio_hi);
-    if (a.advance) a.steps[slot] = P.step + 1;
+    if (a.lp_raw != nullptr) a.lp_raw[b] = (float)((double)row[tok] - lse_raw);
+    if (a.lp_proc != nullptr)
+      a.lp_proc[b] = P.mode == MODE_GREEDY ? 0.0f : (float)((sm.xbest - sm.m_row) - log(sm.s_kept));
+    if (a.advance) {
+      a.steps[slot] = P.step + 1;
+      if (a.history != nullptr) {
+        const int32_t len = a.hist_len[slot];
+        if (len < 0) {
+          report(a.err, PKV_DEV_ERR_HISTORY);
+        } else {
+          a.history[(int64_t)slot * a.hist_cap + len % a.hist_cap] = tok;
+          a.hist_len[slot] = len + 1;
+        }
+      }
+    }
   }
 }
 
@@ -1055,10 +1338,10 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     const RowParams P = row_params(a.ctrl_vocab, a.seeds[slot], step, a.temperature[slot],
                                    a.top_k[slot], a.top_p[slot], 0u);
     for (int c = 0; c < a.ctrl_nch; ++c) {
-      chunk_pass(crow, a.ctrl_vocab, c, P, recs + c, sm, a.err);
+      chunk_pass(crow, a.ctrl_vocab, c, P, recs + c, nullptr, sm, a.err);
       __syncthreads();
     }
-    const int tok = finish_row(crow, a.ctrl_vocab, a.ctrl_nch, P, recs, sm);
+    const int tok = finish_row(RowView{crow, nullptr, 1.0f}, a.ctrl_vocab, a.ctrl_nch, P, recs, sm);
     if (tid == 0) {
       out[0] = tok;
       sm.token = tok;
@@ -1089,10 +1372,10 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     const RowParams P = row_params(V, a.seeds[slot], step, a.temperature[slot], a.top_k[slot],
                                    a.top_p[slot], (uint32_t)(1 + j));
     for (int c = 0; c < a.nch; ++c) {
-      chunk_pass(row, V, c, P, recs + c, sm, a.err);
+      chunk_pass(row, V, c, P, recs + c, nullptr, sm, a.err);
       __syncthreads();
     }
-    const int tok = finish_row(row, V, a.nch, P, recs, sm);
+    const int tok = finish_row(RowView{row, nullptr, 1.0f}, V, a.nch, P, recs, sm);
     if (tid == 0) {
       codes[j] = tok;
       sm.token = tok;
@@ -1115,6 +1398,14 @@ extern "C" size_t pkv_sample_workspace_bytes(int batch, int vocab) {
   using namespace pkv;
   if (batch <= 0 || vocab <= 0) return 0;
   return align_up((size_t)batch * chunks_for(vocab) * sizeof(ChunkRec), 256);
+}
+
+// the chunk records, then one penalty bitmap of nch * CHUNK bits per row
+extern "C" size_t pkv_sample_ext_workspace_bytes(int batch, int vocab) {
+  using namespace pkv;
+  if (batch <= 0 || vocab <= 0) return 0;
+  return pkv_sample_workspace_bytes(batch, vocab) +
+         align_up((size_t)batch * chunks_for(vocab) * (CHUNK / 8), 256);
 }
 
 static size_t frame_ws_bytes(int batch, int vocab, int ctrl_vocab) {
@@ -1147,25 +1438,37 @@ static int check_sampler_common(int batch, int vocab, const int32_t *slots, cons
   return PKV_OK;
 }
 
-extern "C" int pkv_seeded_sample(const float *logits, int64_t row_stride, int batch, int vocab,
-                                 const int32_t *slots, const int32_t *active, int num_slots,
-                                 const uint64_t *seeds, int64_t *steps, const float *temperature,
-                                 const int32_t *top_k, const float *top_p, uint32_t salt,
-                                 int advance, const int32_t *stop_tokens, int n_stop,
-                                 int32_t audio_lo, int32_t audio_hi, int32_t *out_tok,
-                                 int32_t *out_kind, void *workspace, size_t workspace_bytes,
-                                 int32_t *err_word, void *stream) {
+static bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
+
+static int launch_sample(const float *logits, int64_t row_stride, int batch, int vocab,
+                         const int32_t *slots, const int32_t *active, int num_slots,
+                         const uint64_t *seeds, int64_t *steps, const float *temperature,
+                         const int32_t *top_k, const float *top_p, uint32_t salt, int advance,
+                         const int32_t *stop_tokens, int n_stop, int32_t audio_lo,
+                         int32_t audio_hi, int32_t *out_tok, int32_t *out_kind,
+                         const pkv_sample_ext_t *ext, void *workspace, size_t workspace_bytes,
+                         int32_t *err_word, void *stream) {
   using namespace pkv;
   int st = check_sampler_common(batch, vocab, slots, active, num_slots, seeds, steps, temperature,
                                 top_k, top_p);
   if (st != PKV_OK) return st;
   if (!logits || !out_tok || !out_kind || row_stride < vocab) return PKV_ERR_INVALID_ARG;
   if (n_stop < 0 || (n_stop > 0 && !stop_tokens)) return PKV_ERR_INVALID_ARG;
-  if (((uintptr_t)logits & 3u) != 0) return PKV_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < pkv_sample_workspace_bytes(batch, vocab))
-    return PKV_ERR_WORKSPACE;
+  if (!aligned4(logits)) return PKV_ERR_INVALID_ARG;
+  pkv_sample_ext_t e = {};
+  if (ext != nullptr) e = *ext;
+  if (e.history != nullptr && (e.hist_len == nullptr || e.hist_cap <= 0))
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned4(e.min_p) || !aligned4(e.rep_penalty) || !aligned4(e.rep_window) ||
+      !aligned4(e.history) || !aligned4(e.hist_len) || !aligned4(e.logprob_raw) ||
+      !aligned4(e.logprob_proc))
+    return PKV_ERR_INVALID_ARG;
+  const bool penal = e.history != nullptr && e.rep_penalty != nullptr;
+  const size_t need = penal ? pkv_sample_ext_workspace_bytes(batch, vocab)
+                            : pkv_sample_workspace_bytes(batch, vocab);
+  if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
-  SampleArgs a;
+  SampleArgs a{};
   a.logits = logits;
   a.row_stride = row_stride;
   a.batch = batch;
@@ -1189,12 +1492,52 @@ extern "C" int pkv_seeded_sample(const float *logits, int64_t row_stride, int ba
   a.out_kind = out_kind;
   a.recs = static_cast<ChunkRec *>(workspace);
   a.err = err_word;
+  a.min_p = e.min_p;
+  a.rep_penalty = penal ? e.rep_penalty : nullptr;
+  a.rep_window = e.rep_window;
+  a.history = e.history;
+  a.hist_len = e.history != nullptr ? e.hist_len : nullptr;
+  a.hist_cap = e.history != nullptr ? e.hist_cap : 1;
+  a.lp_raw = e.logprob_raw;
+  a.lp_proc = e.logprob_proc;
+  a.pbits = penal ? reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(workspace) +
+                                                 pkv_sample_workspace_bytes(batch, vocab))
+                  : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   sample_chunk_kernel<<<dim3((unsigned)a.nch, (unsigned)batch), SB, 0, s>>>(a);
   int rc = launch_status();
   if (rc != PKV_OK) return rc;
   sample_finish_kernel<<<(unsigned)batch, SB, 0, s>>>(a);
   return launch_status();
+}
+
+extern "C" int pkv_seeded_sample(const float *logits, int64_t row_stride, int batch, int vocab,
+                                 const int32_t *slots, const int32_t *active, int num_slots,
+                                 const uint64_t *seeds, int64_t *steps, const float *temperature,
+                                 const int32_t *top_k, const float *top_p, uint32_t salt,
+                                 int advance, const int32_t *stop_tokens, int n_stop,
+                                 int32_t audio_lo, int32_t audio_hi, int32_t *out_tok,
+                                 int32_t *out_kind, void *workspace, size_t workspace_bytes,
+                                 int32_t *err_word, void *stream) {
+  return launch_sample(logits, row_stride, batch, vocab, slots, active, num_slots, seeds, steps,
+                       temperature, top_k, top_p, salt, advance, stop_tokens, n_stop, audio_lo,
+                       audio_hi, out_tok, out_kind, nullptr, workspace, workspace_bytes, err_word,
+                       stream);
+}
+
+extern "C" int pkv_seeded_sample_ext(const float *logits, int64_t row_stride, int batch,
+                                     int vocab, const int32_t *slots, const int32_t *active,
+                                     int num_slots, const uint64_t *seeds, int64_t *steps,
+                                     const float *temperature, const int32_t *top_k,
+                                     const float *top_p, uint32_t salt, int advance,
+                                     const int32_t *stop_tokens, int n_stop, int32_t audio_lo,
+                                     int32_t audio_hi, int32_t *out_tok, int32_t *out_kind,
+                                     const pkv_sample_ext_t *ext, void *workspace,
+                                     size_t workspace_bytes, int32_t *err_word, void *stream) {
+  return launch_sample(logits, row_stride, batch, vocab, slots, active, num_slots, seeds, steps,
+                       temperature, top_k, top_p, salt, advance, stop_tokens, n_stop, audio_lo,
+                       audio_hi, out_tok, out_kind, ext, workspace, workspace_bytes, err_word,
+                       stream);
 }
 
 static int launch_frame(const float *ctrl, int ctrl_vocab, int32_t stop_ctrl, const float *base,

@@ -92,6 +92,39 @@ class DecodeStep:
                         audio_lo=self.audio_lo, audio_hi=self.audio_hi, err_word=self.err,
                         stream=stream)
 
+    def enable_ext(self, min_p=0.05, rep_penalty=1.2, rep_window=-1, hist_cap=256, seed=0):
+        """Per-slot settings for sample_ext: the same min_p, penalty and
+        window on every slot, and a full history ring of ``hist_cap`` seeded
+        random tokens per slot (as after hist_cap generated tokens)."""
+        import torch
+        dev = self.device
+        S = self.seeds.numel()
+        V = self.t.logits.shape[1]
+        rng = np.random.default_rng(seed)
+        self.ext_min_p = torch.full((S,), float(min_p), dtype=torch.float32, device=dev)
+        self.ext_pen = torch.full((S,), float(rep_penalty), dtype=torch.float32, device=dev)
+        self.ext_window = torch.full((S,), int(rep_window), dtype=torch.int32, device=dev)
+        self.ext_history = torch.as_tensor(
+            rng.integers(0, V, (S, hist_cap)).astype(np.int32)).to(dev)
+        self.ext_hist_len = torch.full((S,), hist_cap, dtype=torch.int32, device=dev)
+        Bn = self.batch.B
+        self.lp_raw = torch.zeros(Bn, dtype=torch.float32, device=dev)
+        self.lp_proc = torch.zeros(Bn, dtype=torch.float32, device=dev)
+        self.ext_ws = torch.empty(B.sample_ext_workspace_bytes(Bn, V), dtype=torch.uint8,
+                                  device=dev)
+
+    def sample_ext(self, advance=True, salt=0, stream=None):
+        """seeded_sample_ext with the settings of enable_ext and both log-probs."""
+        B.seeded_sample_ext(self.t.logits, self.slots, self.active, self.seeds, self.steps,
+                            self.temperature, self.top_k, self.top_p, self.out_tok,
+                            self.out_kind, self.ext_ws, min_p=self.ext_min_p,
+                            rep_penalty=self.ext_pen, rep_window=self.ext_window,
+                            history=self.ext_history, hist_len=self.ext_hist_len,
+                            logprob_raw=self.lp_raw, logprob_proc=self.lp_proc, salt=salt,
+                            advance=advance, stop_tokens=self.stop_tokens,
+                            audio_lo=self.audio_lo, audio_hi=self.audio_hi, err_word=self.err,
+                            stream=stream)
+
     def frame(self, stream=None):
         t = self.t
         if t.ctrl is not None:

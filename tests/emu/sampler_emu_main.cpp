@@ -2,10 +2,15 @@
 // sample_finish_kernel) on the CPU emulation of CUDA.  The kernels' source is
 // the library's sampler.cu up to the end of its namespace, included below as
 // "sampler_dev.inc" (written by the test).  Input and output are raw files:
-//   in:  int32 B, V, num_slots; fp32 logits[B*V]; int32 slots[B], active[B];
-//        uint64 seeds[S]; int64 steps[S]; fp32 temperature[S]; int32 top_k[S];
-//        fp32 top_p[S]
-//   out: int32 out_tok[B], out_kind[B], err
+//   in:  int32 B, V, num_slots, ext; fp32 logits[B*V]; int32 slots[B],
+//        active[B]; uint64 seeds[S]; int64 steps[S]; fp32 temperature[S];
+//        int32 top_k[S]; fp32 top_p[S]; then, when ext != 0 (the further
+//        settings of pkv_seeded_sample_ext): fp32 min_p[S], rep_penalty[S];
+//        int32 rep_window[S], hist_cap, history[S*hist_cap], hist_len[S],
+//        advance
+//   out: int32 out_tok[B], out_kind[B], err; when ext != 0 also fp32
+//        logprob_raw[B], logprob_proc[B]; int32 hist_len[S],
+//        history[S*hist_cap]; int64 steps[S]
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -26,9 +31,9 @@ int main(int argc, char **argv) {
   if (argc != 3) return 2;
   FILE *f = fopen(argv[1], "rb");
   if (!f) return 2;
-  int32_t hdr[3];
-  if (fread(hdr, sizeof(int32_t), 3, f) != 3) return 2;
-  const int B = hdr[0], V = hdr[1], S = hdr[2];
+  int32_t hdr[4];
+  if (fread(hdr, sizeof(int32_t), 4, f) != 4) return 2;
+  const int B = hdr[0], V = hdr[1], S = hdr[2], ext = hdr[3];
   std::vector<float> logits, temp, top_p;
   std::vector<int32_t> slots, active, top_k;
   std::vector<uint64_t> seeds;
@@ -41,6 +46,20 @@ int main(int argc, char **argv) {
   rd(f, temp, S);
   rd(f, top_k, S);
   rd(f, top_p, S);
+  std::vector<float> min_p, pen, lp_raw(B, 7.0f), lp_proc(B, 7.0f);
+  std::vector<int32_t> window, history, hist_len, misc;
+  int cap = 1, advance = 0;
+  if (ext) {
+    rd(f, min_p, S);
+    rd(f, pen, S);
+    rd(f, window, S);
+    rd(f, misc, 1);
+    cap = misc[0];
+    rd(f, history, (size_t)S * cap);
+    rd(f, hist_len, S);
+    rd(f, misc, 1);
+    advance = misc[0];
+  }
   fclose(f);
 
   using namespace pkv;
@@ -61,13 +80,25 @@ int main(int argc, char **argv) {
   a.top_k = top_k.data();
   a.top_p = top_p.data();
   a.salt = 0;
-  a.advance = 0;
+  a.advance = advance;
   a.out_tok = out_tok.data();
   a.out_kind = out_kind.data();
-  const size_t bytes = align_up((size_t)B * a.nch * sizeof(ChunkRec), 256);
+  const size_t rec_bytes = align_up((size_t)B * a.nch * sizeof(ChunkRec), 256);
+  const size_t bytes = rec_bytes + align_up((size_t)B * a.nch * (CHUNK / 8), 256);
   void *ws = aligned_alloc(256, bytes);
   memset(ws, 0xAB, bytes);  // not zeroed: the kernels must not read what they did not write
   a.recs = static_cast<ChunkRec *>(ws);
+  if (ext) {
+    a.min_p = min_p.data();
+    a.rep_penalty = pen.data();
+    a.rep_window = window.data();
+    a.history = history.data();
+    a.hist_len = hist_len.data();
+    a.hist_cap = cap;
+    a.lp_raw = lp_raw.data();
+    a.lp_proc = lp_proc.data();
+    a.pbits = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(ws) + rec_bytes);
+  }
   a.err = &err;
   emu_launch(sample_chunk_kernel, dim3(a.nch, B), SB, a);
   emu_launch(sample_finish_kernel, dim3(B), SB, a);
@@ -78,6 +109,13 @@ int main(int argc, char **argv) {
   fwrite(out_tok.data(), sizeof(int32_t), B, o);
   fwrite(out_kind.data(), sizeof(int32_t), B, o);
   fwrite(&err, sizeof(int32_t), 1, o);
+  if (ext) {
+    fwrite(lp_raw.data(), sizeof(float), B, o);
+    fwrite(lp_proc.data(), sizeof(float), B, o);
+    fwrite(hist_len.data(), sizeof(int32_t), S, o);
+    fwrite(history.data(), sizeof(int32_t), (size_t)S * cap, o);
+    fwrite(steps.data(), sizeof(int64_t), S, o);
+  }
   fclose(o);
   return 0;
 }

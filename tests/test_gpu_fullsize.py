@@ -106,3 +106,48 @@ def test_full_size_step_sampled_rows(name):
         np.testing.assert_array_equal(step.steps.cpu().numpy(), f_steps)
     else:
         np.testing.assert_array_equal(step.steps.cpu().numpy(), s_steps)
+
+
+EXT_SETTINGS = dict(min_p=0.05, rep_penalty=1.2, rep_window=-1, hist_cap=256)  # as bench.py
+
+
+@pytest.mark.parametrize("name", ["qwen2_0p5b", "llama3_3b", "long_context"])
+def test_full_size_sampler_ext_every_row(name):
+    """seeded_sample_ext at the configuration's full batch and vocabulary, with
+    the settings bench.py times (min_p, penalty over a full 256-token ring,
+    both log-probs): every row against the oracle."""
+    cfg = W.CONFIGS[name]
+    batch = W.make_batch(cfg)
+    dev = W.Tensors(batch, device="cuda")
+    step = DecodeStep(batch, dev)
+    step.enable_ext(**EXT_SETTINGS)
+    logits = dev.logits.cpu().numpy()
+    hist = step.ext_history.cpu().numpy()
+    hlen = step.ext_hist_len.cpu().numpy()
+    steps0 = batch.steps.copy()
+    step.sample_ext()
+    torch.cuda.synchronize()
+    assert int(step.err.item()) == 0
+    S = batch.seeds.shape[0]
+    s_steps = steps0.copy()
+    tok, lraw, lproc, info, bad = oracle.seeded_sample_ext(
+        logits, batch.slots, batch.active, batch.seeds, s_steps, batch.temperature, batch.top_k,
+        batch.top_p, min_p=np.full(S, EXT_SETTINGS["min_p"], np.float32),
+        rep_penalty=np.full(S, EXT_SETTINGS["rep_penalty"], np.float32),
+        rep_window=np.full(S, EXT_SETTINGS["rep_window"], np.int32), history=hist,
+        hist_len=hlen)
+    assert bad == 0
+    got = step.out_tok.cpu().numpy()
+    near = (info["top2_gap_rel"] < NEAR) | (info["member_margin"] < NEAR)
+    mism = got != tok
+    assert not np.any(mism & ~near), np.nonzero(mism & ~near)
+    same = ~mism
+    for mine, want in ((step.lp_raw, lraw), (step.lp_proc, lproc)):
+        g = mine.cpu().numpy().astype(np.float64)[same]
+        w = want[same].astype(np.float32)
+        assert np.all(np.abs(g - w) <= 1e-7 + 2 * np.spacing(np.abs(w)).astype(np.float64))
+    np.testing.assert_array_equal(step.steps.cpu().numpy(), s_steps)
+    np.testing.assert_array_equal(step.ext_hist_len.cpu().numpy(), hlen)
+    if not np.any(mism):
+        np.testing.assert_array_equal(step.ext_history.cpu().numpy(), hist)
+    print(name, "ext sampler near-ties:", int(near.sum()))

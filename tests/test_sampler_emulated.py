@@ -42,22 +42,46 @@ def emu_binary(tmp_path_factory):
     return exe
 
 
-def _run(exe, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p):
+def _run(exe, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p, ext=None):
+    """ext: dict of min_p, rep_penalty, rep_window, history [S, cap],
+    hist_len, advance (the pkv_seeded_sample_ext settings).  Returns
+    (out_tok, out_kind, err) and, with ext, also (logprob_raw, logprob_proc,
+    hist_len, history, steps) after the call."""
     B, V = x.shape
     S = seeds.shape[0]
     inp, out = tmp_path / "in.bin", tmp_path / "out.bin"
     with open(inp, "wb") as f:
-        np.array([B, V, S], np.int32).tofile(f)
-        for arr, dt in ((x, np.float32), (slots, np.int32), (active, np.int32), (seeds, np.uint64),
-                        (steps, np.int64), (temp, np.float32), (top_k, np.int32),
-                        (top_p, np.float32)):
+        np.array([B, V, S, 0 if ext is None else 1], np.int32).tofile(f)
+        arrs = [(x, np.float32), (slots, np.int32), (active, np.int32), (seeds, np.uint64),
+                (steps, np.int64), (temp, np.float32), (top_k, np.int32), (top_p, np.float32)]
+        if ext is not None:
+            cap = ext["history"].shape[1]
+            arrs += [(ext["min_p"], np.float32), (ext["rep_penalty"], np.float32),
+                     (ext["rep_window"], np.int32), (np.array([cap]), np.int32),
+                     (ext["history"], np.int32), (ext["hist_len"], np.int32),
+                     (np.array([int(ext["advance"])]), np.int32)]
+        for arr, dt in arrs:
             np.ascontiguousarray(arr, dtype=dt).tofile(f)
     env = dict(os.environ, ASAN_OPTIONS="detect_leaks=0")
     r = subprocess.run([str(exe), str(inp), str(out)], capture_output=True, text=True, env=env,
                        timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
-    res = np.fromfile(out, np.int32)
-    return res[:B], res[B:2 * B], int(res[2 * B])
+    raw = open(out, "rb").read()
+    res = np.frombuffer(raw, np.int32, 2 * B + 1)
+    base = (res[:B].copy(), res[B:2 * B].copy(), int(res[2 * B]))
+    if ext is None:
+        return base
+    off = 4 * (2 * B + 1)
+    lraw = np.frombuffer(raw, np.float32, B, off)
+    lproc = np.frombuffer(raw, np.float32, B, off + 4 * B)
+    off += 8 * B
+    hl = np.frombuffer(raw, np.int32, S, off)
+    off += 4 * S
+    cap = ext["history"].shape[1]
+    hist = np.frombuffer(raw, np.int32, S * cap, off).reshape(S, cap)
+    off += 4 * S * cap
+    st = np.frombuffer(raw, np.int64, S, off)
+    return base + (lraw.copy(), lproc.copy(), hl.copy(), hist.copy(), st.copy())
 
 
 CASES = [
@@ -101,3 +125,81 @@ def test_emulated_sampler_matches_oracle(emu_binary, tmp_path, B, V, std, T, k, 
     mism = got != want
     assert not np.any(mism & ~near), (np.nonzero(mism & ~near), got, want)
     assert got[-1] == 0 and kind[-1] == 0
+
+
+def _lp_close(got, want):
+    """fp32 log-probs: both sides round an fp64 value; the device's raw
+    normaliser terms are within 3e-9 of themselves."""
+    want = np.asarray(want, np.float32)
+    return (np.abs(got.astype(np.float64) - want.astype(np.float64))
+            <= 1e-7 + 2 * np.spacing(np.abs(want)).astype(np.float64))
+
+
+EXT_CASES = [
+    # B, V, std, T, k, p, min_p, penalty, window, dist
+    (3, 20000, 1.0, 1.0, 0, 1.0, 0.05, 1.0, -1, "normal"),    # min_p keeps > 512: general path
+    (3, 20000, 3.0, 1.0, 0, 1.0, 0.1, 1.0, -1, "normal"),     # min_p cut among the candidates
+    (3, 6561, 3.0, 1.0, 200, 1.0, 0.3, 1.4, 4, "normal"),     # top-k + min_p, short window
+    (3, 20000, 1.0, 1.0, 0, 0.9, 1e-4, 1.0, -1, "normal"),    # min_p boundary past the candidates
+    (3, 20000, 2.0, 0.8, 50, 0.9, 0.02, 1.3, 16, "normal"),   # penalty + top-k + min_p + top-p
+    (3, 6561, 2.0, 0.0, 0, 1.0, 0.0, 2.0, -1, "normal"),      # greedy with penalty
+    (3, 20000, 1.0, 1.0, 0, 1.0, 0.0, 1.2, -1, "normal"),     # keep everything + penalty
+    (3, 40000, 1.0, 1.0, 600, 0.95, 0.001, 1.5, 8, "normal"), # general path: top-k > 512
+    (2, 151936, 3.0, 0.7, 0, 0.95, 0.01, 1.1, -1, "conc"),    # long-context sampler
+]
+
+
+@pytest.mark.parametrize("B,V,std,T,k,p,mp,pen,win,dist", EXT_CASES)
+def test_emulated_sampler_ext_matches_oracle(emu_binary, tmp_path, B, V, std, T, k, p, mp, pen,
+                                             win, dist):
+    rng = np.random.default_rng(V + k + 7)
+    x = rng.normal(0, std, (B, V)).astype(np.float32)
+    if dist == "conc":
+        x[:, :8192] += np.float32(6.0)
+    x[0, 3 % V] = -np.inf
+    B1 = B + 1
+    x = np.concatenate([x, np.zeros((1, V), np.float32)])
+    slots = np.arange(1, B1 + 1, dtype=np.int32)
+    slots[-1] = 0
+    active = np.ones(B1, np.int32)
+    active[-1] = 0
+    S = B1 + 1
+    seeds = (np.arange(S, dtype=np.uint64) + np.uint64(31))
+    steps = np.full(S, 5, np.int64)
+    temp = np.full(S, T, np.float32)
+    top_k = np.full(S, k, np.int32)
+    top_p = np.full(S, p, np.float32)
+    # histories: each row's recent tokens include its own leaders (so the
+    # penalty changes the order) and a repeat; the ring has wrapped
+    cap = 24
+    history = rng.integers(0, V, (S, cap)).astype(np.int32)
+    hist_len = np.full(S, 30, np.int32)
+    for b in range(B):
+        lead = np.argsort(-x[b], kind="stable")[:6].astype(np.int32)
+        s = slots[b]
+        for i, t in enumerate(list(lead) + [lead[0]]):
+            history[s, (hist_len[s] - 1 - 2 * i) % cap] = t
+    ext = dict(min_p=np.full(S, mp, np.float32), rep_penalty=np.full(S, pen, np.float32),
+               rep_window=np.full(S, win, np.int32), history=history.copy(),
+               hist_len=hist_len.copy(), advance=True)
+    got, kind, err, lraw, lproc, hl, hist, st = _run(emu_binary, tmp_path, x, slots, active, seeds,
+                                                     steps, temp, top_k, top_p, ext)
+    w_steps = steps.copy()
+    w_hist = history.copy()
+    w_len = hist_len.copy()
+    want, wraw, wproc, info, _ = oracle.seeded_sample_ext(
+        x, slots, active, seeds, w_steps, temp, top_k, top_p, min_p=ext["min_p"],
+        rep_penalty=ext["rep_penalty"], rep_window=ext["rep_window"], history=w_hist,
+        hist_len=w_len, advance=True)
+    assert err & ~0x10 == 0
+    near = (info["top2_gap_rel"] < NEAR) | (info["member_margin"] < NEAR)
+    mism = got != want
+    assert not np.any(mism & ~near), (np.nonzero(mism & ~near), got, want)
+    same = ~mism
+    assert np.all(_lp_close(lraw[same], wraw[same])), (lraw, wraw)
+    assert np.all(_lp_close(lproc[same], wproc[same])), (lproc, wproc)
+    assert got[-1] == 0 and lraw[-1] == 0 and lproc[-1] == 0
+    np.testing.assert_array_equal(st, w_steps)
+    np.testing.assert_array_equal(hl, w_len)
+    if not np.any(mism):
+        np.testing.assert_array_equal(hist, w_hist)
