@@ -399,6 +399,23 @@ def main(argv=None):
                       "codes_per_s": sizes["n_active"] * n_cb / (frame_us / 1e6)}
         barrier()
 
+    # ---- the same step replayed as one captured CUDA graph -------------
+    step.capture()
+    for _ in range(3):
+        step.replay()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        step.replay()
+    g1.record(stream)
+    g1.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1)) / args.steps
+    graph_line = {"ms_per_step": graph_ms,
+                  "value": world * sizes["step"] / (graph_ms / 1e3) / 1e9, "unit": "GB/s",
+                  "kernels_per_replay": step.launches_per_step()}
+    barrier()
+
     # ---- end to end: host (pinned) inputs in, tokens out, every step ----
     host_in = [(tensors.q, tensors.q.cpu().pin_memory()), (tensors.k, tensors.k.cpu().pin_memory()),
                (tensors.v, tensors.v.cpu().pin_memory()),
@@ -446,6 +463,7 @@ def main(argv=None):
         "sampled_rows_per_s": world * sizes["n_active"] * args.steps / (total_ms / 1e3),
         "sampler": {"us_per_call": sampler_us,
                     "rows_per_s": sizes["n_active"] / (sampler_us / 1e6)},
+        "graph": graph_line,
         **({"sampler_ext": ext_line} if ext_line else {}),
         **({"frame": frame_line} if frame_line else {}),
         "attn": {"us_per_layer": attn_avg_s * 1e6, "gbs": achieved,

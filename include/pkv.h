@@ -70,7 +70,8 @@ extern "C" {
 typedef struct {
   int32_t num_layers;
   int32_t num_pages;
-  int32_t page_size;    /* tokens per page; 16 is the supported value       */
+  int32_t page_size;    /* tokens per page: a multiple of 16, at most 1024
+                           (16 as in vox-serve, 128 as in mstar's pools)    */
   int32_t num_kv_heads;
   int32_t head_dim;     /* 64 or 128                                         */
 } pkv_cache_t;
@@ -141,7 +142,8 @@ size_t pkv_decode_workspace_bytes(int batch, int num_qo_heads, int head_dim,
  * Padding rows (active == 0) read nothing and write zeros (lse = -inf).
  * Errors: PKV_ERR_INVALID_ARG (null pointer, bad sizes, num_qo_heads not a
  * multiple of num_kv_heads), PKV_ERR_UNSUPPORTED (head_dim not 64 / 128,
- * page_size != 16, more than 64 q heads per kv head), PKV_ERR_WORKSPACE.
+ * page_size not a multiple of 16 or above 1024, more than 64 q heads per kv
+ * head), PKV_ERR_WORKSPACE.
  * Device: PKV_DEV_ERR_SEQ_LEN (row written as zeros), PKV_DEV_ERR_PAGE (page 0
  * read instead; row unspecified), PKV_DEV_ERR_TIMEOUT.
  * ---------------------------------------------------------------------- */

@@ -4,8 +4,10 @@
 // [num_layers, num_pages, 2, page_size, num_kv_heads, head_dim].
 //
 // Design (HBM-bound; CUDA cores, no tensor cores):
-//  * work units: a row's pages are cut into fixed 32-page (512-token) splits;
-//    a unit is one (row, split, kv head, q-head block).  The split size does
+//  * blocks: the kernel streams a row's context in 16-token blocks; a page
+//    of page_size tokens (any multiple of 16) is page_size / 16 blocks.
+//  * work units: a row's blocks are cut into fixed 32-block (512-token)
+//    splits; a unit is one (row, split, kv head, q-head block).  The split size does
 //    not depend on the batch, so a row's result depends on its inputs only.
 //  * a one-CTA planner lists the splits of the active rows (prefix sums over
 //    the rows) and resets the scheduling counter, so the launch shapes stay
@@ -13,9 +15,9 @@
 //    library writes, so it does its work while its predecessor (the KV
 //    append) still runs and waits for that predecessor only at its end.
 //  * a persistent grid (SMs x resident CTAs) pulls units from an atomic
-//    counter.  Each of a CTA's 4 warps streams its pages of the unit
+//    counter.  Each of a CTA's 4 warps streams its blocks of the unit
 //    (round-robin) through its own ring of NS shared-memory stages; a stage
-//    is one page of one kv head -- 16 K rows + 16 V rows, each head_dim bf16
+//    is one block of one kv head -- 16 K rows + 16 V rows, each head_dim bf16
 //    contiguous in HBM -- brought in by one tiled tensor TMA
 //    (cp.async.bulk.tensor) completing on the stage's mbarrier.  The ring runs on
 //    into the next unit, so its pages are in flight while the current unit
@@ -48,8 +50,9 @@ namespace pkv {
 
 constexpr int ATTN_WARPS = 4;
 constexpr int ATTN_THREADS = ATTN_WARPS * 32;
-constexpr int ATTN_PAGES_PER_SPLIT = 32;
-constexpr int ATTN_PAGE = 16;
+constexpr int ATTN_PAGES_PER_SPLIT = 32;  // 16-token blocks per split
+constexpr int ATTN_PAGE = 16;             // tokens per block (a page is page_size / 16 blocks)
+constexpr int ATTN_MAX_PAGE_SIZE = 1024;
 constexpr float ATTN_TAU = 8.0f;       // lazy-rescale threshold (log2 units)
 constexpr float ATTN_NEG = -1.0e30f;   // "no score yet" (finite: keeps 2^(s-m) at 0)
 constexpr float LN2 = 0.69314718055994530942f;
@@ -81,6 +84,8 @@ struct AttnArgs {
   float qscale;                // sm_scale * log2(e)
   const int32_t *page_table;
   int max_pages;
+  int bpp;                     // 16-token blocks per page
+  int64_t max_tokens;          // max_pages * page_size
   const int32_t *seq_lens;
   const int32_t *active;
   int batch;
@@ -106,7 +111,7 @@ __device__ __forceinline__ int row_splits(const AttnArgs &a, int b, bool *bad) {
   *bad = false;
   if (!a.active[b]) return 0;
   const int n = a.seq_lens[b];
-  if (n < 1 || (int64_t)n > (int64_t)a.max_pages * ATTN_PAGE) {
+  if (n < 1 || (int64_t)n > a.max_tokens) {
     *bad = true;
     return 0;
   }
@@ -302,15 +307,19 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   int nxt_cnt = warp_pages(nxt, warp);
   int next_id = 0;  // id of the unit after next, fetched a unit ahead (thread 0)
 
-  // page ids of the warp's pages of a unit: lane i holds the i-th
+  // the warp's blocks of a unit: lane i holds the i-th as page * bpp + the
+  // block's index inside its page
   auto load_pids = [&](const Unit &U, int cnt) -> int {
     int pid = 0;
     if (lane < cnt) {
-      pid = __ldg(a.page_table + (int64_t)U.b * a.max_pages + U.p_begin + warp + lane * ATTN_WARPS);
+      const int blk = U.p_begin + warp + lane * ATTN_WARPS;
+      const int pg = a.bpp == 1 ? blk : blk / a.bpp;
+      pid = __ldg(a.page_table + (int64_t)U.b * a.max_pages + pg);
       if (pid < 0 || pid >= a.num_pages) {
         report(a.err, PKV_DEV_ERR_PAGE);
         pid = 0;
       }
+      pid = pid * a.bpp + (blk - pg * a.bpp);
     }
     return pid;
   };
@@ -337,15 +346,17 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   int iss_u = 0, iss_i = 0;
   bool dead = false;  // a bounded wait gave up: stop streaming, keep the barriers
 
-  // one tensor TMA brings the page's 16 K rows and 16 V rows of kv head g
+  // one tensor TMA brings the block's 16 K rows and 16 V rows of kv head g
   auto issue_one = [&](int g, int pids, int i) {
-    const int pid = __shfl_sync(FULL_MASK, pids, i);
+    const int c = __shfl_sync(FULL_MASK, pids, i);
     if (lane == 0) {
+      const int pid = a.bpp == 1 ? c : c / a.bpp;
+      const int sub = c - pid * a.bpp;
       uint64_t *bar = &wbars[iss_slot];
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, S::STAGE_BYTES);
-      tma_load_5d(ring + iss_slot * S::STAGE_BYTES, &tmap, 0, g, 0, 0, layer_page0 + pid, bar,
-                  policy);
+      tma_load_5d(ring + iss_slot * S::STAGE_BYTES, &tmap, 0, g, sub * ATTN_PAGE, 0,
+                  layer_page0 + pid, bar, policy);
     }
     iss_slot = iss_slot + 1 == NS ? 0 : iss_slot + 1;
     ++inflight;
@@ -647,7 +658,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_merge_kernel(const AttnArgs
   pdl_trigger();
   const int64_t bh = (int64_t)b * a.num_qo_heads + h;
   const int n = a.seq_lens[b];
-  if (!a.active[b] || n < 1 || (int64_t)n > (int64_t)a.max_pages * ATTN_PAGE) {
+  if (!a.active[b] || n < 1 || (int64_t)n > a.max_tokens) {
     for (int d = threadIdx.x; d < D; d += ATTN_THREADS) store_out(a, bh * D + d, 0.0f);
     if (threadIdx.x == 0 && a.lse != nullptr) a.lse[bh] = -INFINITY;
     return;
@@ -787,7 +798,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 5-D view of the whole cache for the TMA engine, innermost first:
 // (head_dim, kv head, slot, K/V, layer * num_pages + page).  One box is one
-// page of one kv head: head_dim x 1 x page_size x 2 x 1.
+// 16-token block of one page and kv head: head_dim x 1 x 16 x 2 x 1.
 static int encode_cache_map(CUtensorMap *map, const void *cache, const pkv_cache_t *g) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return PKV_ERR_CUDA;
@@ -795,7 +806,7 @@ static int encode_cache_map(CUtensorMap *map, const void *cache, const pkv_cache
   const cuuint64_t PS = (cuuint64_t)g->page_size;
   const cuuint64_t dims[5] = {D, H, PS, 2, (cuuint64_t)g->num_layers * (cuuint64_t)g->num_pages};
   const cuuint64_t strides[4] = {D * 2, H * D * 2, PS * H * D * 2, 2 * PS * H * D * 2};
-  const cuuint32_t box[5] = {(cuuint32_t)D, 1, (cuuint32_t)PS, 2, 1};
+  const cuuint32_t box[5] = {(cuuint32_t)D, 1, (cuuint32_t)ATTN_PAGE, 2, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -803,17 +814,19 @@ static int encode_cache_map(CUtensorMap *map, const void *cache, const pkv_cache
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
 }
 
-static size_t nsplit_for(int max_pages) {
-  return (size_t)((max_pages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT);
+// splits of the longest possible row (max_tokens = max_pages * page_size)
+static size_t nsplit_for(int64_t max_tokens) {
+  const int64_t blocks = (max_tokens + ATTN_PAGE - 1) / ATTN_PAGE;
+  return (size_t)((blocks + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT);
 }
 
 struct WsLayout {
   size_t o, ml, row_start, plan, total;
 };
 
-static WsLayout ws_layout(int batch, int num_qo_heads, int head_dim, int max_pages) {
+static WsLayout ws_layout(int batch, int num_qo_heads, int head_dim, int64_t max_tokens) {
   WsLayout w;
-  const size_t units = (size_t)batch * num_qo_heads * nsplit_for(max_pages);
+  const size_t units = (size_t)batch * num_qo_heads * nsplit_for(max_tokens);
   w.o = 0;
   w.ml = align_up(units * head_dim * sizeof(float), 256);
   w.row_start = w.ml + align_up(units * sizeof(float2), 256);
@@ -829,7 +842,7 @@ extern "C" size_t pkv_decode_workspace_bytes(int batch, int num_qo_heads, int he
   using namespace pkv;
   if (batch <= 0 || num_qo_heads <= 0 || head_dim <= 0 || max_pages <= 0 || page_size <= 0)
     return 0;
-  return ws_layout(batch, num_qo_heads, head_dim, max_pages).total;
+  return ws_layout(batch, num_qo_heads, head_dim, (int64_t)max_pages * page_size).total;
 }
 
 extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache, int layer,
@@ -848,12 +861,16 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
   if (!(sm_scale == sm_scale)) return PKV_ERR_INVALID_ARG;  // NaN
   const int D = geom->head_dim;
   const int group = num_qo_heads / geom->num_kv_heads;
-  if ((D != 64 && D != 128) || geom->page_size != ATTN_PAGE || group > 64)
+  if ((D != 64 && D != 128) || geom->page_size % ATTN_PAGE != 0 ||
+      geom->page_size > ATTN_MAX_PAGE_SIZE || group > 64)
     return PKV_ERR_UNSUPPORTED;
-  if ((int64_t)batch * num_qo_heads * (int64_t)nsplit_for(max_pages) > (1ll << 30))
+  const int64_t max_tokens = (int64_t)max_pages * geom->page_size;
+  if (max_tokens > INT32_MAX ||
+      (int64_t)batch * num_qo_heads * (int64_t)nsplit_for(max_tokens) > (1ll << 30) ||
+      (int64_t)geom->num_pages * (geom->page_size / ATTN_PAGE) > INT32_MAX)
     return PKV_ERR_UNSUPPORTED;
   if (!aligned16(cache) || !aligned16(q)) return PKV_ERR_INVALID_ARG;
-  const WsLayout wl = ws_layout(batch, num_qo_heads, D, max_pages);
+  const WsLayout wl = ws_layout(batch, num_qo_heads, D, max_tokens);
   if (workspace == nullptr || workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
 
@@ -875,13 +892,15 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
   a.qscale = sm_scale * LOG2E;
   a.page_table = page_table;
   a.max_pages = max_pages;
+  a.bpp = geom->page_size / ATTN_PAGE;
+  a.max_tokens = max_tokens;
   a.seq_lens = seq_lens;
   a.active = active;
   a.batch = batch;
   a.out = out;
   a.out_fp32 = out_fp32 != 0;
   a.lse = lse;
-  a.nsplit_max = (int)nsplit_for(max_pages);
+  a.nsplit_max = (int)nsplit_for(max_tokens);
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   a.ws_o = reinterpret_cast<float *>(ws + wl.o);
   a.ws_ml = reinterpret_cast<float2 *>(ws + wl.ml);

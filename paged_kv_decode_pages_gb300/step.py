@@ -71,6 +71,8 @@ class DecodeStep:
             self.frame_ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
             self.frame_kind = torch.empty(Bn, dtype=i32, device=dev)
         self.err = torch.zeros(1, dtype=i32, device=dev)
+        self.graph = None
+        self._warm = False
 
     # -- the pieces of the step ------------------------------------------
     def append(self, layer: int, stream=None):
@@ -144,6 +146,7 @@ class DecodeStep:
         import torch
         L = self.t.layers
         st = stream if stream is not None else torch.cuda.current_stream()
+        self._warm = True
         for l in (layers if layers is not None else range(L)):
             self.append(l, stream=st)
             if attn_events is not None:
@@ -159,6 +162,31 @@ class DecodeStep:
             self.sample(stream=st)
         if self.t.base is not None:
             self.frame(stream=st)
+
+    def capture(self):
+        """Capture one whole run() -- every layer's append and attention, the
+        sampler and the frame -- as one CUDA graph; replay() then launches
+        the step with one call.  The graph reads the buffers this object
+        owns, so new inputs are written into them before a replay.  A step
+        is run once on a side stream first (outside the capture) unless one
+        already ran, so that the library's per-device set-up (kernel
+        attributes, the persistent grid size) never happens during capture."""
+        import torch
+        if not self._warm:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                self.run(stream=side)
+            torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        self.graph = g
+
+    def replay(self):
+        """One step through the captured graph (on the current stream)."""
+        self.graph.replay()
 
     def launches_per_step(self) -> int:
         """Kernel launches of one run(): per layer append 1 + attention 3

@@ -100,6 +100,13 @@ CONFIGS = {
         name="long_context", index=4, num_layers=36, num_qo_heads=32, num_kv_heads=8,
         head_dim=128, page_size=16, n_active=8, n_pad=8, ctx_lo=16384, ctx_hi=32768,
         vocab=151936, logit_std=4.0, temperature=0.7, top_k=0, top_p=0.95),
+    # the long-context step on a pool of 128-token pages handed out in a
+    # random order (the page size of mstar's KV pools)
+    "long_context_p128": Config(
+        name="long_context_p128", index=5, num_layers=36, num_qo_heads=32, num_kv_heads=8,
+        head_dim=128, page_size=128, n_active=8, n_pad=8, ctx_lo=16384, ctx_hi=32768,
+        shuffle_pages=True, vocab=151936, logit_std=4.0, temperature=0.7, top_k=0,
+        top_p=0.95),
 }
 
 

@@ -39,6 +39,20 @@ def _cases():
         "g12_two_qblocks": W.Config(name="g12", index=10, num_layers=1, num_qo_heads=24,
                                     num_kv_heads=2, head_dim=128, page_size=16, n_active=3,
                                     n_pad=1, ctx=(7, 700, 1200)),
+        # pages of 32, 64 and 128 tokens (the kernels stream 16-token blocks):
+        # page and split boundaries, shuffled pools
+        "page32_shuffled": W.Config(name="page32", index=12, num_layers=1, num_qo_heads=8,
+                                    num_kv_heads=2, head_dim=128, page_size=32, n_active=7,
+                                    n_pad=1, ctx=(1, 31, 32, 33, 513, 1100, 48),
+                                    shuffle_pages=True),
+        "page64_d64_g7": W.Config(name="page64", index=13, num_layers=1, num_qo_heads=14,
+                                  num_kv_heads=2, head_dim=64, page_size=64, n_active=5,
+                                  n_pad=1, ctx=(63, 64, 65, 512, 700), shuffle_pages=True),
+        "page128": W.Config(name="page128", index=14, num_layers=2, num_qo_heads=32,
+                            num_kv_heads=8, head_dim=128, page_size=128, n_active=7, n_pad=2,
+                            ctx=(1, 127, 128, 129, 513, 2100, 4000), shuffle_pages=True),
+        "long_p128_small": W.small_variant(W.CONFIGS["long_context_p128"], n_active=3, n_pad=2,
+                                           ctx_hi=2600, layers=2).replace(ctx_lo=1500),
     }
 
 

@@ -29,7 +29,8 @@ def _snapshot(dev, batch, layer, b):
     return W.bf16_bits(compact), pt
 
 
-@pytest.mark.parametrize("name", ["qwen2_0p5b", "llama3_3b", "qwen3_4b_frame", "long_context"])
+@pytest.mark.parametrize("name", ["qwen2_0p5b", "llama3_3b", "qwen3_4b_frame", "long_context",
+                                  "long_context_p128"])
 def test_full_size_step_sampled_rows(name):
     cfg = W.CONFIGS[name]
     batch = W.make_batch(cfg)
@@ -67,8 +68,8 @@ def test_full_size_step_sampled_rows(name):
         assert np.abs(lse - want_lse[0]).max() <= 1e-3
         # the appended slot holds exactly the new k, v
         n = int(batch.seq_lens[b])
-        page = int(batch.page_table[b, (n - 1) // 16])
-        slot_kv = W.bf16_bits(step.t.cache[l, page, :, (n - 1) % 16])
+        page = int(batch.page_table[b, (n - 1) // cfg.page_size])
+        slot_kv = W.bf16_bits(step.t.cache[l, page, :, (n - 1) % cfg.page_size])
         np.testing.assert_array_equal(slot_kv[0], k[0])
         np.testing.assert_array_equal(slot_kv[1], v[0])
     # padding rows: zeros
