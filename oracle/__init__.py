@@ -145,6 +145,12 @@ def _load(path):
     L.pkvo_set_num_threads.argtypes = [_I]
     L.pkvo_kv_append.restype = _I
     L.pkvo_kv_append.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _I]
+    L.pkvo_kv_append_tokens.restype = _I
+    L.pkvo_kv_append_tokens.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P,
+                                        _I]
+    L.pkvo_prefill_attn.restype = _I
+    L.pkvo_prefill_attn.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _I, _D, _P, _P, _I, _P, _P,
+                                    _I, _P, _P]
     L.pkvo_paged_decode_attn.restype = _I
     L.pkvo_paged_decode_attn.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _I, _D,
                                          _P, _I, _P, _P, _I, _P, _P]
@@ -234,6 +240,53 @@ def paged_decode_attn(cache_bits, layer, q_bits, page_table, seq_lens, active, s
     bad = lib().pkvo_paged_decode_attn(_ptr(cache_bits), L, P, ps, Hkv, D, int(layer), _ptr(q), Hq,
                                        float(sm_scale), _ptr(pt), pt.shape[1], _ptr(sl), _ptr(ac),
                                        B, _ptr(out), _ptr(lse))
+    return out, lse, bad
+
+
+# --------------------------------------------------------------------------
+# Prefill / mixed steps: ragged new tokens per request
+# --------------------------------------------------------------------------
+def kv_append_tokens(cache_bits, layer, k_bits, v_bits, qo_indptr, page_table, seq_lens, active):
+    """In place on ``cache_bits``.  k_bits / v_bits: uint16 [T, Hkv, D] with
+    request b's new tokens at rows [qo_indptr[b], qo_indptr[b+1]), ending at
+    position seq_lens[b] - 1.  Returns the count of rejected active requests."""
+    assert cache_bits.dtype == np.uint16 and cache_bits.flags.c_contiguous
+    L, P, two, ps, Hkv, D = cache_bits.shape
+    k = _c(k_bits, np.uint16)
+    v = _c(v_bits, np.uint16)
+    ind = _c(qo_indptr, np.int32)
+    pt = _c(page_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    ac = _c(active, np.int32)
+    B = sl.shape[0]
+    assert ind.shape[0] == B + 1 and k.shape[0] >= ind[-1]
+    return lib().pkvo_kv_append_tokens(_ptr(cache_bits), L, P, ps, Hkv, D, int(layer), _ptr(k),
+                                       _ptr(v), _ptr(ind), _ptr(pt), pt.shape[1], _ptr(sl),
+                                       _ptr(ac), B)
+
+
+def prefill_attn(cache_bits, layer, q_bits, qo_indptr, page_table, seq_lens, active,
+                 sm_scale=None):
+    """Causal attention of the new tokens (q_bits uint16 [T, Hq, D]) over the
+    paged cache.  Returns (out fp64 [T, Hq, D], lse fp64 [T, Hq], n_bad)."""
+    assert cache_bits.dtype == np.uint16 and cache_bits.flags.c_contiguous
+    L, P, two, ps, Hkv, D = cache_bits.shape
+    q = _c(q_bits, np.uint16)
+    T, Hq, Dq = q.shape
+    assert Dq == D and Hq % Hkv == 0
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    ind = _c(qo_indptr, np.int32)
+    pt = _c(page_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    ac = _c(active, np.int32)
+    B = sl.shape[0]
+    assert ind.shape[0] == B + 1 and int(ind[-1]) <= T
+    out = np.zeros((T, Hq, D), np.float64)
+    lse = np.full((T, Hq), -np.inf, np.float64)
+    bad = lib().pkvo_prefill_attn(_ptr(cache_bits), L, P, ps, Hkv, D, int(layer), _ptr(q), Hq,
+                                  float(sm_scale), _ptr(ind), _ptr(pt), pt.shape[1], _ptr(sl),
+                                  _ptr(ac), B, _ptr(out), _ptr(lse))
     return out, lse, bad
 
 

@@ -22,6 +22,13 @@
  *                     (section "2. The program").  Written as gather, then a
  *                     plain softmax, then a weighted sum: no online softmax,
  *                     no splitting, no reordering.
+ *   prefill        -- "Adding a Model", "How a program runs": lm_prefill
+ *                     runs prompt rows (row buckets); "Supported Models",
+ *                     Qwen3.5 / Qwen3.8 notes: text prefill and mixed
+ *                     steps.  Each request's new tokens are appended at
+ *                     consecutive positions ending at seq_len - 1 and each
+ *                     attends causally to its request's positions up to
+ *                     its own (a decode row is one new token).
  *   seeded sample  -- "Supported Models" (mstar docs), "Fish Audio S2-Pro
  *                     notes": temperature first, then top-k and top-p over the
  *                     tempered probabilities, and the top-p boundary keeps the
@@ -267,6 +274,160 @@ int pkvo_paged_decode_attn(const uint16_t *cache, int num_layers,
     free(qd);
   }
   free(ok);
+  return bad;
+}
+
+/* ------------------------------------------------------------------ */
+/* Prefill / mixed steps ("Adding a Model", section "How a program     */
+/* runs": lm_prefill feeds prompt rows, one graph per row bucket;       */
+/* "Supported Models", Qwen3.5 / Qwen3.8 notes: text prefill and mixed  */
+/* steps, a mixed step carrying decode rows beside prompt rows).        */
+/* Request b brings q_b = qo_indptr[b+1] - qo_indptr[b] new tokens,     */
+/* packed at rows [qo_indptr[b], qo_indptr[b+1]) of k, v and q; with    */
+/* n_b = seq_lens[b] (counting them), token i sits at position          */
+/* n_b - q_b + i.  A decode row is q_b = 1.  Padding requests           */
+/* (active == 0) write every token to page 0, slot 0 and read nothing. */
+/* ------------------------------------------------------------------ */
+
+/* Request b's new tokens and their first position; 0 when the request
+ * is malformed (q < 0, n < q, n < 1 with q > 0, n beyond the table, or
+ * a page id out of range for one of its positions). */
+static int prefill_request_ok(const int32_t *qo_indptr, const int32_t *page_table,
+                              int max_pages, int page_size, int num_pages,
+                              const int32_t *seq_lens, int b, int *q_out,
+                              int *pos0_out) {
+  const int q = qo_indptr[b + 1] - qo_indptr[b];
+  const int n = seq_lens[b];
+  *q_out = q;
+  *pos0_out = n - q;
+  if (q < 0 || n < q || (int64_t)n > (int64_t)max_pages * page_size) return 0;
+  if (q > 0 && n < 1) return 0;
+  const int npages = (n + page_size - 1) / page_size;
+  for (int i = 0; i < npages; ++i) {
+    const int32_t pg = page_table[(int64_t)b * max_pages + i];
+    if (pg < 0 || pg >= num_pages) return 0;
+  }
+  return 1;
+}
+
+/* Multi-token append: token i of request b into the slot of position
+ * n_b - q_b + i.  k, v bf16 [T][Hkv][D] with T = qo_indptr[B].  Returns
+ * the number of malformed active requests (they write nothing). */
+int pkvo_kv_append_tokens(uint16_t *cache, int num_layers, int num_pages,
+                          int page_size, int num_kv_heads, int head_dim,
+                          int layer, const uint16_t *k, const uint16_t *v,
+                          const int32_t *qo_indptr, const int32_t *page_table,
+                          int max_pages, const int32_t *seq_lens,
+                          const int32_t *active, int B) {
+  (void)num_layers;
+  int bad = 0;
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  for (int b = 0; b < B; ++b) {
+    int q, pos0;
+    const int ok = prefill_request_ok(qo_indptr, page_table, max_pages, page_size,
+                                      num_pages, seq_lens, b, &q, &pos0);
+    if (active[b] && !ok) {
+      ++bad;
+      continue;
+    }
+    if (!active[b] && q < 0) continue;
+    for (int i = 0; i < q; ++i) {
+      int64_t page = 0, slot = 0; /* padding: the dummy page 0, slot 0 */
+      if (active[b]) {
+        const int64_t pos = (int64_t)pos0 + i;
+        page = page_table[(int64_t)b * max_pages + pos / page_size];
+        slot = pos % page_size;
+      }
+      const int64_t t = (int64_t)qo_indptr[b] + i;
+      for (int kv = 0; kv < 2; ++kv) {
+        const uint16_t *src = (kv == 0 ? k : v) + t * row;
+        const int64_t dst = cache_offset(num_pages, page_size, num_kv_heads, head_dim,
+                                         layer, page, kv, slot, 0);
+        memcpy(cache + dst, src, (size_t)row * sizeof(uint16_t));
+      }
+    }
+  }
+  return bad;
+}
+
+/* Causal attention of the new tokens over the paged cache: the token at
+ * position p attends to positions [0, p] of its own request (what was
+ * cached before the step and the step's tokens up to itself), with the
+ * same gather / plain softmax / weighted sum as the decode oracle.
+ *   q    bf16 [T][Hq][D];  out fp64 [T][Hq][D];  lse fp64 [T][Hq] or NULL.
+ * Rows of padding or malformed requests get zeros and lse = -inf.
+ * Returns the number of malformed active requests. */
+int pkvo_prefill_attn(const uint16_t *cache, int num_layers, int num_pages,
+                      int page_size, int num_kv_heads, int head_dim, int layer,
+                      const uint16_t *q, int num_qo_heads, double sm_scale,
+                      const int32_t *qo_indptr, const int32_t *page_table,
+                      int max_pages, const int32_t *seq_lens,
+                      const int32_t *active, int B, double *out, double *lse) {
+  (void)num_layers;
+  const int D = head_dim;
+  const int Hq = num_qo_heads;
+  const int group = num_qo_heads / num_kv_heads;
+  const int64_t T = qo_indptr[B];
+  int bad = 0;
+  /* owner request, position and validity of every token row */
+  int32_t *req = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+  int32_t *pos = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+  for (int64_t t = 0; t < T; ++t) req[t] = -1;
+  for (int b = 0; b < B; ++b) {
+    int qn, pos0;
+    const int ok = prefill_request_ok(qo_indptr, page_table, max_pages, page_size,
+                                      num_pages, seq_lens, b, &qn, &pos0);
+    if (active[b] && !ok) ++bad;
+    if (!active[b] || !ok) continue;
+    for (int i = 0; i < qn; ++i) {
+      req[qo_indptr[b] + i] = b;
+      pos[qo_indptr[b] + i] = pos0 + i;
+    }
+  }
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t th = 0; th < T * Hq; ++th) {
+    const int64_t t = th / Hq;
+    const int h = (int)(th % Hq);
+    double *o = out + th * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (lse) lse[th] = -INFINITY;
+    const int b = req[t];
+    if (b < 0) continue;
+    const int n = pos[t] + 1; /* keys [0, pos] */
+    const int g = h / group;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    for (int d = 0; d < D; ++d) qd[d] = bf16_bits_to_double(q[th * D + d]);
+    for (int j = 0; j < n; ++j) {
+      const int32_t pg = page_table[(int64_t)b * max_pages + j / page_size];
+      const int64_t off = cache_offset(num_pages, page_size, num_kv_heads, D, layer,
+                                       pg, 0, j % page_size, g);
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qd[d] * bf16_bits_to_double(cache[off + d]);
+      s[j] = sm_scale * dot;
+    }
+    double m = s[0];
+    for (int j = 1; j < n; ++j)
+      if (s[j] > m) m = s[j];
+    double z = 0.0;
+    for (int j = 0; j < n; ++j) {
+      s[j] = exp(s[j] - m);
+      z += s[j];
+    }
+    for (int j = 0; j < n; ++j) {
+      const int32_t pg = page_table[(int64_t)b * max_pages + j / page_size];
+      const int64_t off = cache_offset(num_pages, page_size, num_kv_heads, D, layer,
+                                       pg, 1, j % page_size, g);
+      const double p = s[j] / z;
+      for (int d = 0; d < D; ++d) o[d] += p * bf16_bits_to_double(cache[off + d]);
+    }
+    if (lse) lse[th] = m + log(z);
+    free(s);
+    free(qd);
+  }
+  free(pos);
+  free(req);
   return bad;
 }
 

@@ -29,7 +29,7 @@ Recipe:
 from __future__ import annotations
 
 import dataclasses
-from typing import Optional, Sequence
+from typing import Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -230,6 +230,174 @@ class Tensors:
                 self.ctrl = torch.empty((B, cfg.ctrl_vocab), dtype=torch.float32, device=device)
                 self.ctrl.normal_(0.0, cfg.ctrl_logit_std, generator=g)
                 self.ctrl[:, cfg.ctrl_stop] += cfg.ctrl_stop_bias
+        self.layers = L
+
+
+# --------------------------------------------------------------------------
+# Prefill / mixed steps ("Adding a Model", "How a program runs": prompt rows
+# in row buckets; "Supported Models", Qwen3.5 / Qwen3.8 notes: text prefill
+# and mixed steps replayed by total tokens on a ladder of buckets)
+# --------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class PrefillConfig:
+    """Request b brings new_b tokens after prefix_b cached ones (a decode row
+    is new_b = 1).  Either ``reqs`` lists (prefix, new) pairs, or n_prefill
+    prompt requests draw prefix ~ U{prefix_lo..prefix_hi} and new ~
+    U{new_lo..new_hi} and n_decode decode rows draw a context ~
+    U{ctx_lo..ctx_hi} (prefix = context - 1).  The packed token count is
+    padded up to the next bucket of LADDER by one padding request (active 0)
+    at the end."""
+    name: str
+    index: int
+    num_layers: int
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    reqs: Optional[Sequence[Tuple[int, int]]] = None
+    n_prefill: int = 0
+    prefix_lo: int = 0
+    prefix_hi: int = 0
+    new_lo: int = 1
+    new_hi: int = 1
+    n_decode: int = 0
+    ctx_lo: int = 1
+    ctx_hi: int = 1
+    bucket: bool = True
+    shuffle_pages: bool = False
+
+    @property
+    def group(self) -> int:
+        return self.num_qo_heads // self.num_kv_heads
+
+    def replace(self, **kw) -> "PrefillConfig":
+        return dataclasses.replace(self, **kw)
+
+
+PREFILL_CONFIGS = {
+    # small enough for the oracle: empty and long prefixes, 1-token decode
+    # rows, tiles cut by the ragged tails
+    "prefill_tiny": PrefillConfig(
+        name="prefill_tiny", index=20, num_layers=1, num_qo_heads=8, num_kv_heads=2,
+        head_dim=64, page_size=16,
+        reqs=((0, 1), (0, 17), (5, 40), (30, 1), (100, 130), (0, 57), (257, 4))),
+    # a mixed step of the Qwen3-4B shape: 4 prompts (up to 4k cached tokens,
+    # 0.5-2k new ones) beside 28 decode rows
+    "mixed_qwen3_4b": PrefillConfig(
+        name="mixed_qwen3_4b", index=21, num_layers=36, num_qo_heads=32, num_kv_heads=8,
+        head_dim=128, page_size=16, n_prefill=4, prefix_lo=0, prefix_hi=4096, new_lo=512,
+        new_hi=2048, n_decode=28, ctx_lo=256, ctx_hi=8192),
+    # a text prefill of 8 whole 2k prompts, 128-token pages (mstar's pools)
+    "prefill_qwen3_4b_p128": PrefillConfig(
+        name="prefill_qwen3_4b_p128", index=22, num_layers=36, num_qo_heads=32,
+        num_kv_heads=8, head_dim=128, page_size=128, n_prefill=8, prefix_lo=0, prefix_hi=0,
+        new_lo=2048, new_hi=2048, shuffle_pages=True),
+}
+
+
+@dataclasses.dataclass
+class PrefillBatch:
+    cfg: PrefillConfig
+    qo_indptr: np.ndarray     # int32 [B + 1]
+    seq_lens: np.ndarray      # int32 [B]  (after the append)
+    active: np.ndarray        # int32 [B]
+    page_table: np.ndarray    # int32 [B, max_pages]
+    num_pages: int
+
+    @property
+    def B(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def T(self) -> int:
+        return int(self.qo_indptr[-1])
+
+    @property
+    def max_pages(self) -> int:
+        return int(self.page_table.shape[1])
+
+    def new_tokens(self, b: int) -> int:
+        return int(self.qo_indptr[b + 1] - self.qo_indptr[b])
+
+
+# token buckets of captured prefill / mixed steps: powers of two from 32 to
+# 8192 plus 2176, 4352 and 8704 (a step past the last one runs unpadded)
+LADDER = tuple(sorted([32 << i for i in range(9)] + [2176, 4352, 8704]))
+
+
+def ladder_bucket(n: int) -> int:
+    """The smallest bucket of the ladder >= n (n itself past the ladder)."""
+    for b in LADDER:
+        if b >= n:
+            return b
+    return n
+
+
+def make_prefill_batch(cfg: PrefillConfig) -> PrefillBatch:
+    ps = cfg.page_size
+    rng = np.random.default_rng(2000 + cfg.index)
+    if cfg.reqs is not None:
+        reqs = [(int(a), int(b)) for a, b in cfg.reqs]
+    else:
+        reqs = []
+        for _ in range(cfg.n_prefill):
+            reqs.append((int(rng.integers(cfg.prefix_lo, cfg.prefix_hi + 1)),
+                         int(rng.integers(cfg.new_lo, cfg.new_hi + 1))))
+        for _ in range(cfg.n_decode):
+            reqs.append((int(rng.integers(cfg.ctx_lo, cfg.ctx_hi + 1)) - 1, 1))
+    T_real = sum(q for _, q in reqs)
+    T = ladder_bucket(T_real) if cfg.bucket else T_real
+    pad = T - T_real
+    B = len(reqs) + (1 if pad > 0 else 0)
+    qo = np.zeros(B + 1, np.int32)
+    seq = np.ones(B, np.int32)
+    act = np.zeros(B, np.int32)
+    for b, (pre, q) in enumerate(reqs):
+        qo[b + 1] = qo[b] + q
+        seq[b] = pre + q
+        act[b] = 1
+    if pad > 0:
+        qo[B] = qo[B - 1] + pad
+        seq[B - 1] = pad
+    npg = [(int(seq[b]) + ps - 1) // ps for b in range(len(reqs))]
+    max_pages = max(npg + [1])
+    num_pages = int(sum(npg)) + 1
+    ids = np.arange(1, num_pages, dtype=np.int64)
+    if cfg.shuffle_pages:
+        ids = rng.permutation(ids)
+    pt = np.zeros((B, max_pages), np.int32)
+    o = 0
+    for b, n in enumerate(npg):
+        pt[b, :n] = ids[o:o + n]
+        o += n
+    return PrefillBatch(cfg, qo, seq, act, pt, num_pages)
+
+
+class PrefillTensors:
+    """cache [L, P, 2, ps, Hkv, D] and per layer q [T, Hq, D], k, v
+    [T, Hkv, D], all ~ N(0, 1) bf16, drawn on ``device`` from
+    ``torch.Generator(1000 + index)`` in that order (cache layer by layer,
+    then q, k, v per layer)."""
+
+    def __init__(self, batch: PrefillBatch, device="cpu", layers: Optional[int] = None):
+        import torch
+        cfg = batch.cfg
+        L = cfg.num_layers if layers is None else layers
+        g = torch.Generator(device=device)
+        g.manual_seed(1000 + cfg.index)
+        bf = torch.bfloat16
+        shape = (L, batch.num_pages, 2, cfg.page_size, cfg.num_kv_heads, cfg.head_dim)
+        self.cache = torch.empty(shape, dtype=bf, device=device)
+        for l in range(L):
+            self.cache[l].normal_(0.0, 1.0, generator=g)
+        T = batch.T
+        self.q = torch.empty((L, T, cfg.num_qo_heads, cfg.head_dim), dtype=bf, device=device)
+        self.k = torch.empty((L, T, cfg.num_kv_heads, cfg.head_dim), dtype=bf, device=device)
+        self.v = torch.empty((L, T, cfg.num_kv_heads, cfg.head_dim), dtype=bf, device=device)
+        for l in range(L):
+            self.q[l].normal_(0.0, 1.0, generator=g)
+            self.k[l].normal_(0.0, 1.0, generator=g)
+            self.v[l].normal_(0.0, 1.0, generator=g)
         self.layers = L
 
 

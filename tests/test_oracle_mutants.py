@@ -1,6 +1,7 @@
 """The pins are strong enough: each plausible mistake below, planted in a copy
 of the oracle's C source and compiled on the CPU, makes at least one pin of
-tests/test_oracle_attention.py or tests/test_oracle_sampler.py fail.  (The
+tests/test_oracle_attention.py, tests/test_oracle_prefill.py or
+tests/test_oracle_sampler.py fail.  (The
 real oracle is untouched; the mutant is loaded only inside this test.)"""
 import os
 import tempfile
@@ -9,18 +10,23 @@ import pytest
 
 import oracle
 import test_oracle_attention as TA
+import test_oracle_prefill as TP
 import test_oracle_sampler as TS
 
 # (name, original text, planted mistake)
 MUTANTS = [
-    ("gqa head mapping by modulo", "const int g = h / group;",
-     "const int g = h % num_kv_heads;"),
+    ("gqa head mapping by modulo", "const int n = seq_lens[b];\n    const int g = h / group;",
+     "const int n = seq_lens[b];\n    const int g = h % num_kv_heads;"),
+    ("prefill gqa head mapping by modulo",
+     "const int n = pos[t] + 1; /* keys [0, pos] */\n    const int g = h / group;",
+     "const int n = pos[t] + 1; /* keys [0, pos] */\n    const int g = h % num_kv_heads;"),
     ("softmax scale dropped", "s[t] = sm_scale * dot;", "s[t] = dot;"),
     ("keys read from the V half", "pg, 0, t % page_size, g);", "pg, 1, t % page_size, g);"),
     ("values read from the K half", "pg, 1, t % page_size, g);", "pg, 0, t % page_size, g);"),
     ("softmax not normalised", "double p = s[t] / z;", "double p = s[t];"),
     ("lse without the max", "lse[bh] = m + log(z);", "lse[bh] = log(z);"),
-    ("append slot off by one", "slot = pos % page_size;", "slot = (pos + 1) % page_size;"),
+    ("append slot off by one", "slot = pos % page_size;\n      if (page < 0",
+     "slot = (pos + 1) % page_size;\n      if (page < 0"),
     ("philox xors the wrong high half", "uint64_t y0 = hi1 ^ x1 ^ k0;",
      "uint64_t y0 = hi0 ^ x1 ^ k0;"),
     ("philox bumps k1 by the wrong constant", "k1 += PHILOX_W1;", "k1 += PHILOX_W0;"),
@@ -56,6 +62,16 @@ MUTANTS = [
      "  for (int r = 0; r < K; ++r) S += e[r];\n  if (top_p < 1.0f) {"),
     ("raw log-prob from the penalised logits", "  for (int i = 0; i < V; ++i) zraw += exp((double)logits[i] - mraw);",
      "  for (int i = 0; i < V; ++i) zraw += exp((double)logits[i] - mraw + 0.25 * (i == 0));"),
+    ("prefill attends one key too far", "const int n = pos[t] + 1; /* keys [0, pos] */",
+     "const int n = pos[t] + 2; /* keys [0, pos] */"),
+    ("prefill excludes the token itself", "const int n = pos[t] + 1; /* keys [0, pos] */",
+     "const int n = pos[t] > 0 ? pos[t] : 1; /* keys [0, pos] */"),
+    ("prefill positions counted from the prefix start", "      pos[qo_indptr[b] + i] = pos0 + i;",
+     "      pos[qo_indptr[b] + i] = i;"),
+    ("prefill tokens appended one slot late", "        const int64_t pos = (int64_t)pos0 + i;",
+     "        const int64_t pos = (int64_t)pos0 + i + 1;"),
+    ("prefill keys of another request", "      const int32_t pg = page_table[(int64_t)b * max_pages + j / page_size];\n      const int64_t off = cache_offset(num_pages, page_size, num_kv_heads, D, layer,\n                                       pg, 0, j % page_size, g);",
+     "      const int32_t pg = page_table[(int64_t)(b > 0 ? b - 1 : b) * max_pages + j / page_size];\n      const int64_t off = cache_offset(num_pages, page_size, num_kv_heads, D, layer,\n                                       pg, 0, j % page_size, g);"),
     ("penalty window from the oldest token",
      "pen[n_pen++] = history[(int64_t)s * hist_cap + (len - 1 - i) % hist_cap];",
      "pen[n_pen++] = history[(int64_t)s * hist_cap + i % hist_cap];"),
@@ -74,6 +90,13 @@ def _pins():
         ("single token", TA.test_single_token_returns_its_value),
         ("identical keys", TA.test_identical_keys_give_mean_of_values),
         ("halves", TA.test_two_halves_merge_by_lse_to_the_whole),
+        ("prefill append", TP.test_append_tokens_bytes),
+        ("prefill first token", TP.test_first_token_of_an_empty_prefix_attends_only_to_itself),
+        ("prefill running mean", TP.test_identical_keys_give_the_running_mean_of_the_values),
+        ("prefill decode", TP.test_one_new_token_per_request_is_the_decode_oracle),
+        ("prefill chunked", TP.test_chunked_prefill_equals_one_step),
+        ("prefill sdpa", lambda: [TP.test_prefill_oracle_matches_torch_sdpa_with_a_causal_mask(n)
+                                  for n in TP.CASES]),
         ("greedy", lambda: [TS.test_greedy_is_numpy_argmax(t) for t in (0.0, 1e-6)]),
         ("top-k/top-p argmax", TS.test_top_k_one_and_tiny_top_p_are_argmax_for_any_seed),
         ("boundary p", TS.test_top_p_boundary_prefix_exactly_p_drops_the_next_token),
