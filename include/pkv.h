@@ -53,6 +53,8 @@ extern "C" {
 #define PKV_DEV_ERR_TIMEOUT 0x8 /* a bounded wait on an async copy gave up    */
 #define PKV_DEV_ERR_LOGITS 0x10 /* NaN or +inf logit in an active row         */
 #define PKV_DEV_ERR_HISTORY 0x20 /* negative token-history length             */
+#define PKV_DEV_ERR_INDPTR 0x40  /* qo_indptr not 0-based, not non-decreasing,
+                                    or past the packed token count            */
 
 /* ---- out_kind codes ("Adding a Model", section "How a program runs":
  *      out_kind is audio frame, stop, or other) ------------------------- */
@@ -191,6 +193,58 @@ int pkv_paged_decode_attn_static(const pkv_cache_t *geom, const void *cache,
                                  const int32_t *active, int batch, void *out,
                                  int out_fp32, float *lse, int32_t *err_word,
                                  void *stream);
+
+/* ------------------------------------------------------------------------
+ * Prefill and mixed steps ("Adding a Model", "How a program runs": lm_prefill
+ * runs prompt rows, one graph per row bucket; "Supported Models", Qwen3.5 /
+ * Qwen3.8 notes: text prefill and mixed steps, replayed by total tokens).
+ * A step's new tokens are packed: request b owns rows
+ * [qo_indptr[b], qo_indptr[b+1]) of k, v, q and out (q_b of them), and with
+ * n_b = seq_lens[b] (counting them) its token i sits at position
+ * n_b - q_b + i.  A decode row is q_b = 1.  qo_indptr int32 [batch + 1],
+ * qo_indptr[0] = 0, non-decreasing, qo_indptr[batch] <= total_tokens (rows
+ * past it are not touched).  Padding requests (active == 0) write their
+ * tokens to page 0, slot 0 and get zero outputs.
+ * ---------------------------------------------------------------------- */
+
+/* pkv_kv_append_tokens -- every new token's k, v (bf16 [total_tokens][Hkv]
+ * [head_dim]) into the slot of its position in layer `layer`.  Errors as
+ * pkv_kv_append; device: PKV_DEV_ERR_SEQ_LEN (request with seq_len < q_b,
+ * seq_len < 1 or past max_pages * page_size: it writes nothing),
+ * PKV_DEV_ERR_PAGE, PKV_DEV_ERR_INDPTR (a token row that no request owns
+ * writes nothing). */
+int pkv_kv_append_tokens(const pkv_cache_t *geom, void *cache, int layer,
+                         const void *k, const void *v, int total_tokens,
+                         const int32_t *qo_indptr, const int32_t *page_table,
+                         int max_pages, const int32_t *seq_lens,
+                         const int32_t *active, int batch, int32_t *err_word,
+                         void *stream);
+
+/* Workspace (bytes) pkv_prefill_attn needs for `batch` requests. */
+size_t pkv_prefill_workspace_bytes(int batch);
+
+/* pkv_prefill_attn -- causal grouped-query attention of the new tokens over
+ * the paged cache of layer `layer` (after pkv_kv_append_tokens): the token
+ * at position p of request b, q head h, attends to positions [0, p] of b
+ * with kv head h / (num_qo_heads / num_kv_heads):
+ *     out[t][h] = sum_j softmax_j(sm_scale * q[t][h] . K_j) V_j
+ *   q    bf16 [total_tokens][num_qo_heads][head_dim] (16-byte aligned)
+ *   out  bf16 [total_tokens][num_qo_heads][head_dim] (rounded to nearest
+ *        even once, from fp32 accumulation)
+ *   lse  fp32 [total_tokens][num_qo_heads] natural-log log-sum-exp, or NULL
+ * Tensor cores (tcgen05, bf16 operands, fp32 accumulation in tensor
+ * memory); a row's result depends on its own request only.  head_dim 64 or
+ * 128, page_size a multiple of 16 up to 1024, up to 128 q heads per kv head.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE.
+ * Device: PKV_DEV_ERR_SEQ_LEN (rows written as zeros), PKV_DEV_ERR_PAGE
+ * (page 0 read instead), PKV_DEV_ERR_INDPTR, PKV_DEV_ERR_TIMEOUT. */
+int pkv_prefill_attn(const pkv_cache_t *geom, const void *cache, int layer,
+                     const void *q, int num_qo_heads, float sm_scale,
+                     int total_tokens, const int32_t *qo_indptr,
+                     const int32_t *page_table, int max_pages,
+                     const int32_t *seq_lens, const int32_t *active, int batch,
+                     void *out, float *lse, void *workspace,
+                     size_t workspace_bytes, int32_t *err_word, void *stream);
 
 /* Workspace (bytes) pkv_seeded_sample needs for these sizes. */
 size_t pkv_sample_workspace_bytes(int batch, int vocab);

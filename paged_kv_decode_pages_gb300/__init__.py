@@ -1,6 +1,8 @@
 """GB300-native paged-KV decode step: KV append, grouped-query paged decode
-attention, seeded temperature / top-k / top-p sampling and the frame-local
-codebook loop, as hand-written CUDA for sm_103a behind a small C ABI
+attention, seeded temperature / top-k / top-p sampling (with min_p,
+repetition penalty and log-probs), the frame-local codebook loop, and the
+prefill / mixed step (multi-token append, causal paged attention on the
+tensor cores), as hand-written CUDA for sm_103a behind a small C ABI
 (``include/pkv.h``, ``libpkv.so``).
 
 The Python names below are a thin ctypes binding with the C names minus the
@@ -13,6 +15,7 @@ does, and raises if it is missing.
 _BINDING = (
     "load", "library_path", "version", "error_string", "PkvError",
     "kv_append", "paged_decode_attn", "decode_workspace_bytes", "paged_decode_attn_static",
+    "kv_append_tokens", "prefill_attn", "prefill_workspace_bytes",
     "seeded_sample", "sample_workspace_bytes", "seeded_sample_ext", "sample_ext_workspace_bytes",
     "codebook_frame_sample", "frame_workspace_bytes",
     "frame_sample", "frame_sample_workspace_bytes",

@@ -45,6 +45,11 @@ SIGNATURES = {
                                    _P, _I, _P, _I, _P, _P, _SZ, _P, _P]),
     "pkv_paged_decode_attn_static": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _I, _F, _P,
                                           _I, _P, _P, _I, _P, _I, _P, _P, _P]),
+    "pkv_kv_append_tokens": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _P, _I, _P, _P, _I,
+                                  _P, _P, _I, _P, _P]),
+    "pkv_prefill_workspace_bytes": (_SZ, [_I]),
+    "pkv_prefill_attn": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _I, _F, _I, _P, _P, _I, _P,
+                              _P, _I, _P, _P, _P, _SZ, _P, _P]),
     "pkv_sample_workspace_bytes": (_SZ, [_I, _I]),
     "pkv_seeded_sample": (_I, [_P, _I64, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _U32, _I, _P,
                                _I, _I32, _I32, _P, _P, _P, _SZ, _P, _P]),
@@ -205,6 +210,56 @@ def paged_decode_attn_static(cache, layer, q, page_table, seq_lens, active, out,
         page_table.shape[1], _ptr(seq_lens), _ptr(active), B, _ptr(out),
         int(out.dtype == torch.float32), _ptr(lse), _ptr(err_word), _stream(stream))
     _check("pkv_paged_decode_attn_static", st)
+
+
+def kv_append_tokens(cache, layer, k, v, qo_indptr, page_table, seq_lens, active, err_word=None,
+                     stream=None):
+    """The packed new tokens k, v (bf16 [T, Hkv, D]) of a prefill / mixed step
+    into their positions (request b: rows qo_indptr[b] .. qo_indptr[b+1],
+    ending at position seq_lens[b] - 1)."""
+    import torch
+    _req(cache, torch.bfloat16, "cache")
+    for t, nm in ((k, "k"), (v, "v")):
+        _req(t, torch.bfloat16, nm)
+    for t, nm in ((qo_indptr, "qo_indptr"), (page_table, "page_table"), (seq_lens, "seq_lens"),
+                  (active, "active")):
+        _req(t, torch.int32, nm)
+    g = _geom(cache)
+    st = load().pkv_kv_append_tokens(ctypes.byref(g), _ptr(cache), int(layer), _ptr(k), _ptr(v),
+                                     k.shape[0], _ptr(qo_indptr), _ptr(page_table),
+                                     page_table.shape[1], _ptr(seq_lens), _ptr(active),
+                                     seq_lens.shape[0], _ptr(err_word), _stream(stream))
+    _check("pkv_kv_append_tokens", st)
+
+
+def prefill_workspace_bytes(batch) -> int:
+    return int(load().pkv_prefill_workspace_bytes(batch))
+
+
+def prefill_attn(cache, layer, q, qo_indptr, page_table, seq_lens, active, out, workspace,
+                 lse=None, sm_scale=None, err_word=None, stream=None):
+    """Causal attention of the packed new tokens q (bf16 [T, Hq, D]) over the
+    paged cache into out (bf16 [T, Hq, D]); lse fp32 [T, Hq] optional."""
+    import torch
+    _req(cache, torch.bfloat16, "cache")
+    _req(q, torch.bfloat16, "q")
+    _req(out, torch.bfloat16, "out")
+    for t, nm in ((qo_indptr, "qo_indptr"), (page_table, "page_table"), (seq_lens, "seq_lens"),
+                  (active, "active")):
+        _req(t, torch.int32, nm)
+    if lse is not None:
+        _req(lse, torch.float32, "lse")
+    g = _geom(cache)
+    T, Hq, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / (D ** 0.5)
+    st = load().pkv_prefill_attn(ctypes.byref(g), _ptr(cache), int(layer), _ptr(q), Hq,
+                                 float(sm_scale), T, _ptr(qo_indptr), _ptr(page_table),
+                                 page_table.shape[1], _ptr(seq_lens), _ptr(active),
+                                 seq_lens.shape[0], _ptr(out), _ptr(lse), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(err_word),
+                                 _stream(stream))
+    _check("pkv_prefill_attn", st)
 
 
 def sample_workspace_bytes(batch, vocab) -> int:

@@ -14,4 +14,4 @@ extern "C" const char *pkv_error_string(int status) {
   }
 }
 
-extern "C" int pkv_num_dev_error_bits(void) { return 5; }
+extern "C" int pkv_num_dev_error_bits(void) { return 7; }

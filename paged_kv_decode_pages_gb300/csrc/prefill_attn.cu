@@ -1,0 +1,733 @@
+// prefill_attn.cu -- causal attention of a step's new tokens over the paged
+// cache: prompt rows of a prefill ("Adding a Model", vox-serve docs, "How a
+// program runs": lm_prefill over row buckets) and mixed steps that carry
+// decode rows beside prompt rows ("Supported Models", mstar docs, Qwen3.5 /
+// Qwen3.8 notes).  Request b's q_b new tokens (packed rows qo_indptr[b] ..
+// qo_indptr[b+1]) sit at positions seq_len - q_b .. seq_len - 1, already
+// appended to the cache; the token at position p attends to positions
+// [0, p] of its request.
+//
+// This is a dense contraction, so it runs on the 5th-generation tensor
+// cores:
+//  * a tile is 128 MMA rows: tq = 128 / G tokens x the G q heads of one kv
+//    head (GQA packing: every K / V tile read serves the whole group);
+//  * one CTA per (request, q tile, kv head); a one-CTA planner lists the
+//    tiles (prefix sums), heaviest tile of each request first;
+//  * warp 4 is the producer and MMA issuer: tiled tensor TMA brings Q (once)
+//    and 128-key K and V tiles (16-token blocks of the pages, 128-byte
+//    swizzle, two stages each) into shared memory; tcgen05.mma computes
+//    S = Q K^T into tensor memory and O += P V into tensor memory
+//    (bf16 operands, fp32 accumulation), each completion signalled by
+//    tcgen05.commit on an mbarrier;
+//  * warps 0-3 own one row each: they read the row of S from tensor memory,
+//    apply the causal mask, run the online softmax in log2 units with a
+//    lazy maximum (O is rescaled in tensor memory only when the running
+//    maximum grows by more than 8), write P as bf16 into shared memory in
+//    the MMA's swizzled layout, and at the end read O, divide by the row
+//    sum and store it;
+//  * stale cache slots past a request's last position are zeroed in shared
+//    memory before they meet P (whose entries there are 0), so whatever an
+//    unwritten slot holds cannot reach the output;
+//  * every wait is bounded; a give-up is reported and the CTA drains its
+//    tensor-core work before it frees its tensor memory.
+#include <math.h>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+
+constexpr int PF_M = 128;          // MMA rows of a tile
+constexpr int PF_N = 128;          // keys of a KV tile
+constexpr int PF_BLK = 16;         // tokens of one cache block (one TMA box)
+constexpr int PF_THREADS = 160;    // 4 softmax warps + the producer warp
+constexpr int PF_CHUNK = 16384;    // 128 rows x 128 bytes (64 bf16): one swizzle column
+constexpr int PF_TMEM_COLS = 256;  // S (128 columns) + O (up to 128)
+constexpr int PF_PLAN_THREADS = 1024;
+constexpr float PF_TAU = 8.0f;     // lazy-rescale threshold (log2 units)
+
+struct PfHeader {
+  int32_t total_tiles;
+  int32_t total_units;
+  int32_t pad_[2];
+};
+
+struct PfArgs {
+  int layer;
+  int num_pages;
+  int bpp;  // 16-token blocks per page
+  int num_kv_heads;
+  int num_qo_heads;
+  int group;
+  int tq;   // tokens per tile
+  int T;
+  float qscale;  // sm_scale * log2(e)
+  const int32_t *qo_indptr;
+  const int32_t *page_table;
+  int max_pages;
+  int64_t max_tokens;
+  const int32_t *seq_lens;
+  const int32_t *active;
+  int batch;
+  uint16_t *out;  // bf16 [T][Hq][D]
+  float *lse;     // [T][Hq] or null
+  int32_t *tile_start;  // [B + 1]
+  PfHeader *hdr;
+  int32_t *err;
+};
+
+// ---------------------------------------------------------------------------
+// tcgen05 / tensor-memory wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle.  K-major operands: rows
+// of 128 bytes, 8-row groups 1024 bytes apart (sbo); the leading offset is
+// not used.  MN-major operands: lbo = distance between 64-element atoms
+// along MN, sbo = distance between 8-row groups along K.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version of the 5th-generation tensor cores
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, A
+// K-major, B K-major or MN-major, M x N.
+__host__ __device__ constexpr uint32_t bf16_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+// 32 consecutive 32-bit columns of the warp's 32 lanes
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0, int c1, int c2,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// planner: one CTA lists the q tiles of every request (prefix sums)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int request_tiles(const PfArgs &a, int b) {
+  const int q = a.qo_indptr[b + 1] - a.qo_indptr[b];
+  return q > 0 ? (q + a.tq - 1) / a.tq : 0;
+}
+
+__global__ void __launch_bounds__(PF_PLAN_THREADS) prefill_plan_kernel(const PfArgs a) {
+  __shared__ int32_t scan[PF_PLAN_THREADS];
+  __shared__ int32_t carry;
+  pdl_trigger();
+  const int tid = threadIdx.x;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < a.batch; base += PF_PLAN_THREADS) {
+    const int b = base + tid;
+    int nt = 0;
+    if (b < a.batch) {
+      if (a.qo_indptr[b + 1] < a.qo_indptr[b] || (b == 0 && a.qo_indptr[0] != 0))
+        report(a.err, PKV_DEV_ERR_INDPTR);
+      else
+        nt = request_tiles(a, b);
+    }
+    scan[tid] = nt;
+    __syncthreads();
+    for (int off = 1; off < PF_PLAN_THREADS; off <<= 1) {
+      const int v = tid >= off ? scan[tid - off] : 0;
+      __syncthreads();
+      scan[tid] += v;
+      __syncthreads();
+    }
+    if (b < a.batch) a.tile_start[b] = carry + scan[tid] - nt;
+    __syncthreads();
+    if (tid == PF_PLAN_THREADS - 1) carry += scan[tid];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.tile_start[a.batch] = carry;
+    a.hdr->total_tiles = carry;
+    a.hdr->total_units = carry * a.num_kv_heads;
+    if (a.qo_indptr[a.batch] > a.T) report(a.err, PKV_DEV_ERR_INDPTR);
+  }
+  pdl_wait();  // completes after the append that wrote the step's tokens
+}
+
+// ---------------------------------------------------------------------------
+// the attention kernel
+// ---------------------------------------------------------------------------
+template <int D>
+struct PfShape {
+  static constexpr int NCH = D / 64;                  // 64-dim swizzle columns
+  static constexpr int Q_BYTES = NCH * PF_CHUNK;
+  static constexpr int KV_BYTES = NCH * PF_CHUNK;     // one K or V stage
+  static constexpr int P_BYTES = 2 * PF_CHUNK;        // 128 rows x 128 keys
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int NBAR = 10;
+  static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
+};
+
+template <int D>
+__global__ void __launch_bounds__(PF_THREADS, 1)
+    prefill_attn_kernel(const PfArgs a, const __grid_constant__ CUtensorMap kv_map,
+                        const __grid_constant__ CUtensorMap q_map) {
+  using S = PfShape<D>;
+  constexpr int NCH = S::NCH;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char *qs = sm + S::OFF_Q;
+  unsigned char *ks = sm + S::OFF_K;  // [2][NCH][128 rows][128 B]
+  unsigned char *vs = sm + S::OFF_V;
+  unsigned char *ps = sm + S::OFF_P;  // [2 key columns][128 rows][128 B]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::OFF_BAR);
+  uint64_t *bar_q = bars + 0;
+  uint64_t *bar_k = bars + 1;  // [2]
+  uint64_t *bar_v = bars + 3;  // [2]
+  uint64_t *bar_s = bars + 5;
+  uint64_t *bar_o = bars + 6;
+  uint64_t *bar_p = bars + 7;
+  uint64_t *bar_fin = bars + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::NBAR);
+  int32_t *dead = reinterpret_cast<int32_t *>(tmem_slot + 1);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int Hkv = a.num_kv_heads;
+  const int G = a.group;
+  const int Hq = a.num_qo_heads;
+
+  pdl_wait();  // the planner's table, the append's cache writes
+  pdl_trigger();
+  const int u = blockIdx.x;
+  if (u >= a.hdr->total_units) return;
+  const int su = u / Hkv, g = u % Hkv;
+  // request of tile su: the last b with tile_start[b] <= su
+  int lo = 0, hi = a.batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.tile_start[mid] <= su)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int b = lo;
+  const int q = a.qo_indptr[b + 1] - a.qo_indptr[b];
+  const int ntiles_b = a.tile_start[b + 1] - a.tile_start[b];
+  const int ti = ntiles_b - 1 - (su - a.tile_start[b]);  // heaviest tile first
+  const int n = a.seq_lens[b];
+  const int t0 = a.qo_indptr[b] + ti * a.tq;
+  const int ntok = min(a.tq, q - ti * a.tq);
+  const int pos0 = n - q + ti * a.tq;  // position of the tile's first token
+  const bool ok = a.active[b] && q <= n && n >= 1 && (int64_t)n <= a.max_tokens;
+
+  if (!ok) {
+    // padding or malformed request: zeros, lse = -inf
+    if (a.active[b] && ti == ntiles_b - 1 && g == 0 && tid == 0) report(a.err, PKV_DEV_ERR_SEQ_LEN);
+    const int rows = ntok * G;
+    for (int r = warp; r < rows; r += PF_THREADS / 32) {
+      const int t = t0 + r / G, h = g * G + r % G;
+      if (t >= a.T) break;
+      uint16_t *o = a.out + ((int64_t)t * Hq + h) * D;
+      for (int d = lane * 2; d < D; d += 64) *reinterpret_cast<uint32_t *>(o + d) = 0u;
+      if (a.lse != nullptr && lane == 0) a.lse[(int64_t)t * Hq + h] = -INFINITY;
+    }
+    return;
+  }
+  const int p_max = pos0 + ntok - 1;
+  const int nkv = p_max / PF_N + 1;        // KV tiles
+  const int last_blk = (n - 1) / PF_BLK;   // block of the request's last position
+  const int kt_stale = (n - 1) / PF_N;     // the KV tile that holds slots past n - 1
+
+  if (tid == 0) {
+    for (int i = 0; i < S::NBAR; ++i) mbar_init(&bars[i], i == 7 ? 128u : 1u);
+    *dead = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(PF_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_s = tmem;        // S: columns [0, 128)
+  const uint32_t tm_o = tmem + 128;  // O: columns [128, 128 + D)
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    const uint64_t policy = l2_evict_first_policy();
+    const int page0 = a.layer * a.num_pages;
+    auto load_kv = [&](int kt, int kv, unsigned char *dst, uint64_t *bar) {
+      mbar_arrive_expect_tx(bar, (uint32_t)(NCH * 8 * PF_BLK * 128));
+      for (int i = 0; i < 8; ++i) {
+        int blk = kt * 8 + i;
+        if (blk > last_blk) blk = last_blk;  // past the request: any valid block (zeroed below)
+        const int pg = blk / a.bpp;
+        const int sub = blk - pg * a.bpp;
+        int pid = __ldg(a.page_table + (int64_t)b * a.max_pages + pg);
+        if (pid < 0 || pid >= a.num_pages) {
+          report(a.err, PKV_DEV_ERR_PAGE);
+          pid = 0;
+        }
+        for (int c = 0; c < NCH; ++c)
+          tma_load_5d(dst + c * PF_CHUNK + i * PF_BLK * 128, &kv_map, c * 64, g, sub * PF_BLK,
+                      kv, page0 + pid, bar, policy);
+      }
+    };
+    constexpr uint32_t IDESC_S = bf16_idesc(PF_M, PF_N, false);
+    constexpr uint32_t IDESC_O = bf16_idesc(PF_M, D, true);
+    const uint32_t qa = smem_addr(qs), ka = smem_addr(ks), va = smem_addr(vs), pa = smem_addr(ps);
+    auto issue_s = [&](int stage) {
+      const uint32_t kb = ka + stage * S::KV_BYTES;
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * PF_CHUNK + (k & 3) * 32;
+        tc_mma(tm_s, sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024), IDESC_S,
+               k > 0);
+      }
+      tc_commit(bar_s);
+    };
+    auto issue_o = [&](int stage, bool acc) {
+      const uint32_t vb = va + stage * S::KV_BYTES;
+#pragma unroll
+      for (int k = 0; k < PF_N / 16; ++k) {
+        const uint32_t poff = (k >> 2) * PF_CHUNK + (k & 3) * 32;
+        tc_mma(tm_o, sw128_desc(pa + poff, 16, 1024), sw128_desc(vb + k * 16 * 128, PF_CHUNK, 1024),
+               IDESC_O, (acc || k > 0) ? 1u : 0u);
+      }
+      tc_commit(bar_o);
+    };
+    bool alive = true;
+    auto wait = [&](uint64_t *bar, uint32_t parity) {  // warp-uniform give-up
+      if (!alive) return;
+      if (!__all_sync(FULL_MASK, mbar_wait(bar, parity))) {
+        alive = false;
+        if (lane == 0) {
+          report(a.err, PKV_DEV_ERR_TIMEOUT);
+          atomicExch(dead, 1);
+        }
+      }
+    };
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_q, (uint32_t)(NCH * a.tq * G * 128));
+      for (int c = 0; c < NCH; ++c) tma_load_3d(qs + c * PF_CHUNK, &q_map, c * 64, g * G, t0, bar_q);
+      load_kv(0, 0, ks, &bar_k[0]);
+      load_kv(0, 1, vs, &bar_v[0]);
+      if (nkv > 1) {
+        load_kv(1, 0, ks + S::KV_BYTES, &bar_k[1]);
+        load_kv(1, 1, vs + S::KV_BYTES, &bar_v[1]);
+      }
+    }
+    wait(bar_q, 0);
+    wait(&bar_k[0], 0);
+    if (alive && lane == 0) {
+      tc_fence_after();
+      issue_s(0);
+    }
+    for (int kt = 0; kt < nkv && alive; ++kt) {
+      const int st = kt & 1;
+      const uint32_t ph = (uint32_t)((kt >> 1) & 1);
+      wait(bar_p, (uint32_t)(kt & 1));  // S[kt] read, P[kt] written, O rescaled
+      if (!alive) break;
+      tc_fence_after();
+      if (lane == 0 && kt + 2 < nkv) load_kv(kt + 2, 0, ks + st * S::KV_BYTES, &bar_k[st]);
+      wait(&bar_v[st], ph);
+      if (!alive) break;
+      if (kt == kt_stale) {
+        // slots past the request's last position: zero the V rows
+        const int r0 = n - kt * PF_N;
+        unsigned char *vt = vs + st * S::KV_BYTES;
+        for (int r = r0 + lane; r < PF_N; r += 32)
+          for (int c = 0; c < NCH; ++c) {
+            uint4 *row = reinterpret_cast<uint4 *>(vt + c * PF_CHUNK + r * 128);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) row[j] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        tc_fence_after();
+        issue_o(st, kt > 0);
+      }
+      if (kt + 1 < nkv) {
+        wait(&bar_k[st ^ 1], (uint32_t)(((kt + 1) >> 1) & 1));
+        if (!alive) break;
+        if (lane == 0) {
+          tc_fence_after();
+          issue_s(st ^ 1);
+        }
+      }
+      if (kt + 2 < nkv) {
+        wait(bar_o, (uint32_t)(kt & 1));  // PV[kt] done: its V stage is free
+        if (!alive) break;
+        if (lane == 0) load_kv(kt + 2, 1, vs + st * S::KV_BYTES, &bar_v[st]);
+      }
+    }
+    // drain: every MMA this thread issued has completed
+    if (lane == 0) {
+      tc_commit(bar_fin);
+      if (!mbar_wait(bar_fin, 0)) report(a.err, PKV_DEV_ERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------ softmax warps
+    const int r = tid;  // row of the tile (TMEM lane)
+    const int tok = r / G;
+    const int hj = r % G;
+    const bool valid = tok < ntok && r < a.tq * G && t0 + tok < a.T;
+    const int p = pos0 + tok;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // l_run: sum of the fp32 weights (for lse); w_run: sum of the weights as
+    // rounded to bf16 for P.V (normalises O, so the output is a weighted
+    // mean of the values with the weights the tensor cores actually used)
+    float m_run = -INFINITY, l_run = 0.0f, w_run = 0.0f;
+    bool alive = true;
+    for (int kt = 0; kt < nkv; ++kt) {
+      if (!__all_sync(FULL_MASK, mbar_wait(bar_s, (uint32_t)(kt & 1)))) {  // warp-uniform
+        alive = false;
+        if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + lane_off + c * 32, sr[c]);
+      tmem_wait_ld();
+      const int lim = valid ? p - kt * PF_N : -1;  // keys <= lim are allowed
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x = (c * 32 + j <= lim) ? __uint_as_float(sr[c][j]) * a.qscale : -INFINITY;
+          sr[c][j] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      float m_ref = m_run, alpha = 1.0f;
+      if (mx > m_run + PF_TAU) {
+        m_ref = mx;
+        alpha = fast_exp2(m_run - mx);  // 0 when m_run = -inf
+      }
+      const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
+      float sum = 0.0f, wsum = 0.0f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = fast_exp2(__uint_as_float(sr[c][j]) - m_use);
+          const float p1 = fast_exp2(__uint_as_float(sr[c][j + 1]) - m_use);
+          sum += p0 + p1;
+          const uint32_t w = pack_bf16x2(p0, p1);
+          wsum += bf16lo(w) + bf16hi(w);
+          pk[(c * 32 + j) >> 1] = w;
+        }
+      l_run = l_run * alpha + sum;
+      w_run = w_run * alpha + wsum;
+      const bool resc = kt > 0 && alpha != 1.0f;
+      m_run = m_ref;
+      if (kt > 0) {
+        // PV[kt-1] done: O is stable and the P buffer free
+        if (!__all_sync(FULL_MASK, mbar_wait(bar_o, (uint32_t)((kt - 1) & 1)))) {
+          alive = false;
+          if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(FULL_MASK, resc)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tm_o + lane_off + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st32(tm_o + lane_off + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P row r, keys 0..127, as two 64-key swizzle columns
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4 *dst = reinterpret_cast<uint4 *>(ps + c * PF_CHUNK + r * 128 + ((j ^ (r & 7)) << 4));
+          *dst = make_uint4(pk[c * 32 + 4 * j], pk[c * 32 + 4 * j + 1], pk[c * 32 + 4 * j + 2],
+                            pk[c * 32 + 4 * j + 3]);
+        }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+    if (alive && __all_sync(FULL_MASK, mbar_wait(bar_o, (uint32_t)((nkv - 1) & 1)))) {
+      tc_fence_after();
+      const float inv = w_run > 0.0f ? 1.0f / w_run : 0.0f;
+      const int t = t0 + tok;
+      uint16_t *orow = a.out + ((int64_t)t * Hq + g * G + hj) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tm_o + lane_off + c * 32, o);
+        tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
+            *reinterpret_cast<uint4 *>(orow + c * 32 + j) = w;
+          }
+        }
+      }
+      if (valid && a.lse != nullptr)
+        a.lse[(int64_t)t * Hq + g * G + hj] =
+            l_run > 0.0f ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+    } else if (lane == 0) {
+      report(a.err, PKV_DEV_ERR_TIMEOUT);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(PF_TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 pf_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// (head_dim, kv head, slot, K/V, layer * num_pages + page); one box = 64
+// dims x 16 slots of one kv head, K or V, 128-byte swizzled
+static int encode_kv_map(CUtensorMap *map, const void *cache, const pkv_cache_t *g) {
+  auto enc = pf_encoder();
+  if (enc == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t D = (cuuint64_t)g->head_dim, H = (cuuint64_t)g->num_kv_heads;
+  const cuuint64_t PS = (cuuint64_t)g->page_size;
+  const cuuint64_t dims[5] = {D, H, PS, 2, (cuuint64_t)g->num_layers * (cuuint64_t)g->num_pages};
+  const cuuint64_t strides[4] = {D * 2, H * D * 2, PS * H * D * 2, 2 * PS * H * D * 2};
+  const cuuint32_t box[5] = {64, 1, (cuuint32_t)PF_BLK, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
+}
+
+// q [T][Hq][D]: one box = 64 dims x G heads x tq tokens, 128-byte swizzled
+static int encode_q_map(CUtensorMap *map, const void *q, int T, int Hq, int D, int G, int tq) {
+  auto enc = pf_encoder();
+  if (enc == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)tq};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
+}
+
+struct PfWs {
+  size_t tile_start, hdr, total;
+};
+static PfWs pf_ws(int batch) {
+  PfWs w;
+  w.tile_start = 0;
+  w.hdr = align_up((size_t)(batch + 1) * sizeof(int32_t), 256);
+  w.total = w.hdr + 256;
+  return w;
+}
+
+template <int D>
+static int launch_prefill(const PfArgs &a, const CUtensorMap &kvm, const CUtensorMap &qm,
+                          int max_units, cudaStream_t st) {
+  using S = PfShape<D>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(prefill_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             S::SMEM_BYTES) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  if (launch_pdl(prefill_plan_kernel, dim3(1), dim3(PF_PLAN_THREADS), 0, st, a) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (launch_pdl(prefill_attn_kernel<D>, dim3((unsigned)max_units), dim3(PF_THREADS),
+                 (size_t)S::SMEM_BYTES, st, a, kvm, qm) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return launch_status();
+}
+
+}  // namespace pkv
+
+extern "C" size_t pkv_prefill_workspace_bytes(int batch) {
+  if (batch <= 0) return 0;
+  return pkv::pf_ws(batch).total;
+}
+
+extern "C" int pkv_prefill_attn(const pkv_cache_t *geom, const void *cache, int layer,
+                                const void *q, int num_qo_heads, float sm_scale, int total_tokens,
+                                const int32_t *qo_indptr, const int32_t *page_table,
+                                int max_pages, const int32_t *seq_lens, const int32_t *active,
+                                int batch, void *out, float *lse, void *workspace,
+                                size_t workspace_bytes, int32_t *err_word, void *stream) {
+  using namespace pkv;
+  int st = check_geometry(geom);
+  if (st != PKV_OK) return st;
+  if (!cache || !q || !qo_indptr || !page_table || !seq_lens || !active || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (batch <= 0 || total_tokens <= 0 || max_pages <= 0 || layer < 0 ||
+      layer >= geom->num_layers || num_qo_heads <= 0 || num_qo_heads % geom->num_kv_heads != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return PKV_ERR_INVALID_ARG;
+  const int D = geom->head_dim;
+  const int G = num_qo_heads / geom->num_kv_heads;
+  if ((D != 64 && D != 128) || geom->page_size % PF_BLK != 0 || geom->page_size > 1024 ||
+      G > PF_M)
+    return PKV_ERR_UNSUPPORTED;
+  const int64_t max_tokens = (int64_t)max_pages * geom->page_size;
+  if (max_tokens > INT32_MAX || (int64_t)geom->num_layers * geom->num_pages > INT32_MAX)
+    return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(cache) || !aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  const PfWs wl = pf_ws(batch);
+  if (workspace == nullptr || workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
+
+  PfArgs a;
+  a.layer = layer;
+  a.num_pages = geom->num_pages;
+  a.bpp = geom->page_size / PF_BLK;
+  a.num_kv_heads = geom->num_kv_heads;
+  a.num_qo_heads = num_qo_heads;
+  a.group = G;
+  a.tq = PF_M / G;
+  a.T = total_tokens;
+  a.qscale = sm_scale * 1.44269504088896340736f;
+  a.qo_indptr = qo_indptr;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.max_tokens = max_tokens;
+  a.seq_lens = seq_lens;
+  a.active = active;
+  a.batch = batch;
+  a.out = static_cast<uint16_t *>(out);
+  a.lse = lse;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  a.tile_start = reinterpret_cast<int32_t *>(ws + wl.tile_start);
+  a.hdr = reinterpret_cast<PfHeader *>(ws + wl.hdr);
+  a.err = err_word;
+  // tiles: sum over requests of ceil(q_b / tq) <= T / tq + B
+  const int64_t max_units = ((int64_t)(total_tokens + a.tq - 1) / a.tq + batch) * geom->num_kv_heads;
+  if (max_units > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  alignas(64) CUtensorMap kvm, qm;
+  st = encode_kv_map(&kvm, cache, geom);
+  if (st != PKV_OK) return st;
+  st = encode_q_map(&qm, q, total_tokens, num_qo_heads, D, G, a.tq);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return D == 128 ? launch_prefill<128>(a, kvm, qm, (int)max_units, s)
+                  : launch_prefill<64>(a, kvm, qm, (int)max_units, s);
+}

@@ -198,3 +198,62 @@ class DecodeStep:
         if self.t.base is not None:
             n += 1
         return n
+
+
+class PrefillStep:
+    """One prefill / mixed step of a PrefillBatch: for every layer the
+    multi-token append, then causal paged attention of the new tokens.  Owns
+    the device copies of the batch description, the outputs and the
+    workspace; computes nothing itself."""
+
+    def __init__(self, batch, tensors, device="cuda", with_lse=True):
+        import torch
+        cfg = batch.cfg
+        dev = torch.device(device)
+        self.batch, self.cfg, self.t, self.device = batch, cfg, tensors, dev
+        i32 = torch.int32
+        self.qo_indptr = torch.as_tensor(batch.qo_indptr, dtype=i32).to(dev)
+        self.page_table = torch.as_tensor(batch.page_table, dtype=i32).to(dev)
+        self.seq_lens = torch.as_tensor(batch.seq_lens, dtype=i32).to(dev)
+        self.active = torch.as_tensor(batch.active, dtype=i32).to(dev)
+        L = tensors.layers
+        T = batch.T
+        self.out = torch.empty((L, T, cfg.num_qo_heads, cfg.head_dim), dtype=torch.bfloat16,
+                               device=dev)
+        self.lse = (torch.empty((L, T, cfg.num_qo_heads), dtype=torch.float32, device=dev)
+                    if with_lse else None)
+        self.ws = torch.empty(max(B.prefill_workspace_bytes(batch.B), 256), dtype=torch.uint8,
+                              device=dev)
+        self.err = torch.zeros(1, dtype=i32, device=dev)
+
+    def append(self, layer, stream=None):
+        t = self.t
+        B.kv_append_tokens(t.cache, layer, t.k[layer], t.v[layer], self.qo_indptr,
+                           self.page_table, self.seq_lens, self.active, err_word=self.err,
+                           stream=stream)
+
+    def attend(self, layer, stream=None):
+        t = self.t
+        B.prefill_attn(t.cache, layer, t.q[layer], self.qo_indptr, self.page_table,
+                       self.seq_lens, self.active, self.out[layer], self.ws,
+                       lse=None if self.lse is None else self.lse[layer], err_word=self.err,
+                       stream=stream)
+
+    def run(self, stream=None, attn_events=None):
+        import torch
+        st = stream if stream is not None else torch.cuda.current_stream()
+        for l in range(self.t.layers):
+            self.append(l, stream=st)
+            if attn_events is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                self.attend(l, stream=st)
+                e1.record(st)
+                attn_events.append((e0, e1))
+            else:
+                self.attend(l, stream=st)
+
+    def launches_per_step(self) -> int:
+        """Per layer: the append, the planner and the attention kernel."""
+        return 3 * self.t.layers

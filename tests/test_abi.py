@@ -43,7 +43,7 @@ def test_version_and_error_strings(lib):
     assert "sm_103a" in pkv.version()
     assert pkv.error_string(0) == "ok"
     assert "workspace" in pkv.error_string(4)
-    assert lib.pkv_num_dev_error_bits() == 5
+    assert lib.pkv_num_dev_error_bits() == 7
 
 
 def test_workspace_sizes_are_host_only(lib):
