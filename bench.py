@@ -15,6 +15,12 @@ over ranks (each rank runs its own replica: "replicas only", weak scaling).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+A prefill / mixed-step workload (``--workload mixed_qwen3_4b`` or
+``prefill_qwen3_4b_p128``) times instead, per layer, the multi-token append
+and the tensor-core causal attention of the step's new tokens, and reports
+new tokens/s with the attention kernel's TFLOP/s against the measured bf16
+tensor peak.
 """
 from __future__ import annotations
 
@@ -230,6 +236,192 @@ def cpu_baseline(batch, tensors, sizes, budget_s=12.0):
 
 
 # ---------------------------------------------------------------------------
+# prefill / mixed steps
+# ---------------------------------------------------------------------------
+PREFILL_METRIC = "prefill / mixed step: new tokens/s and causal-attention TFLOP/s at 1 GB300"
+
+
+def prefill_flops(batch):
+    """Algorithmic FLOPs of one layer's attention: every new token of an
+    active request, every q head, 2*D for q.k and 2*D for p.v per key of its
+    causal range [0, pos]."""
+    cfg = batch.cfg
+    keys = 0
+    for b in range(batch.B):
+        if not batch.active[b]:
+            continue
+        q, n = batch.new_tokens(b), int(batch.seq_lens[b])
+        keys += q * (n - q) + q * (q + 1) // 2
+    return 4.0 * cfg.head_dim * cfg.num_qo_heads * keys
+
+
+def tensor_peak(sustained=True):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops_sustained" if sustained else "bf16_tflops"]), "measured"
+    except Exception:
+        return (1700.0 if sustained else 1900.0), "fallback"
+
+
+def prefill_cpu_baseline(batch, tensors, budget_s=12.0):
+    """The oracle's append + attention on a bounded sample of layer 0: the
+    last 32 new tokens of every active request (the rest of the cache as
+    drawn), repeated until about budget_s seconds."""
+    import numpy as np
+    import torch
+    import oracle
+    from paged_kv_decode_pages_gb300 import workloads as W
+    cfg = batch.cfg
+    rows = [b for b in range(batch.B) if batch.active[b]]
+    pages, o = [], 1
+    pt = np.zeros((len(rows), batch.max_pages), np.int32)
+    for i, b in enumerate(rows):
+        k = (int(batch.seq_lens[b]) + cfg.page_size - 1) // cfg.page_size
+        pt[i, :k] = np.arange(o, o + k)
+        pages.extend(batch.page_table[b, :k].tolist())
+        o += k
+    c = tensors.cache[0].index_select(0, torch.as_tensor(pages, device=tensors.cache.device))
+    compact = torch.zeros((1, c.shape[0] + 1) + tuple(c.shape[1:]), dtype=c.dtype)
+    compact[0, 1:] = c.cpu()
+    cb = W.bf16_bits(compact)
+    take = [min(32, batch.new_tokens(b)) for b in rows]
+    ind = np.concatenate([[0], np.cumsum(take)]).astype(np.int32)
+    sel = np.concatenate([np.arange(int(batch.qo_indptr[b + 1]) - k, int(batch.qo_indptr[b + 1]))
+                          for b, k in zip(rows, take)])
+    selt = torch.as_tensor(sel, device=tensors.q.device)
+    q = W.bf16_bits(tensors.q[0].index_select(0, selt))
+    k_ = W.bf16_bits(tensors.k[0].index_select(0, selt))
+    v_ = W.bf16_bits(tensors.v[0].index_select(0, selt))
+    sl = batch.seq_lens[rows].astype(np.int32)
+    act = np.ones(len(rows), np.int32)
+    flops = 4.0 * cfg.head_dim * cfg.num_qo_heads * sum(
+        t * (int(n) - t) + t * (t + 1) // 2 for t, n in zip(take, sl))
+    t_total, reps = 0.0, 0
+    while t_total < budget_s and reps < 50:
+        t0 = time.perf_counter()
+        oracle.kv_append_tokens(cb, 0, k_, v_, ind, pt, sl, act)
+        oracle.prefill_attn(cb, 0, q, ind, pt, sl, act)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": flops * reps / t_total / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "layer 0, the last 32 new tokens of each of %d requests (append + causal "
+                      "attention), %d repetitions, %.1f s" % (len(rows), reps, t_total)}
+
+
+def run_prefill(args, rank, world):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import paged_kv_decode_pages_gb300 as pkv
+    from paged_kv_decode_pages_gb300 import workloads as W
+    from paged_kv_decode_pages_gb300.step import PrefillStep
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    pkv.load()
+    cfg = W.PREFILL_CONFIGS[args.workload]
+    batch = W.make_prefill_batch(cfg)
+    tensors = W.PrefillTensors(batch, device="cuda")
+    step = PrefillStep(batch, tensors)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step.run(stream)
+    barrier()
+    clocks = Clocks(local)
+    attn_ev = []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.run(stream, attn_events=attn_ev)
+    e1.record(stream)
+    e1.synchronize()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(e0.elapsed_time(e1))
+    attn_s = float(np.mean([a.elapsed_time(b) for a, b in attn_ev])) / 1e3
+    assert int(step.err.item()) == 0, "device error word %#x" % int(step.err.item())
+    barrier()
+
+    # end to end: every layer's q, k, v from pinned host memory, the last
+    # layer's output back
+    host_in = [(tensors.q, tensors.q.cpu().pin_memory()), (tensors.k, tensors.k.cpu().pin_memory()),
+               (tensors.v, tensors.v.cpu().pin_memory())]
+    out_last = step.out[-1]
+    host_out = torch.empty(out_last.shape, dtype=out_last.dtype, pin_memory=True)
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    barrier()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        for d, h in host_in:
+            d.copy_(h, non_blocking=True)
+        step.run(stream)
+        host_out.copy_(out_last, non_blocking=True)
+    x1.record(stream)
+    x1.synchronize()
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1))
+    barrier()
+
+    real = int(sum(batch.new_tokens(b) for b in range(batch.B) if batch.active[b]))
+    flops = prefill_flops(batch)
+    achieved = flops / attn_s / 1e12
+    peak, src = tensor_peak(sustained=True)
+    line = {
+        "metric": PREFILL_METRIC, "value": world * real * args.steps / (total_ms / 1e3),
+        "unit": "new tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "compute": "bf16 operands, fp32 accumulation in tensor memory (tcgen05)",
+        "config": {"workload": cfg.name, "layers": cfg.num_layers, "q_heads": cfg.num_qo_heads,
+                   "kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
+                   "page_size": cfg.page_size, "requests": int(batch.active.sum()),
+                   "new_tokens": real, "bucket": batch.T,
+                   "prompt_requests": int(sum(1 for b in range(batch.B)
+                                              if batch.active[b] and batch.new_tokens(b) > 1)),
+                   "l2": "inputs larger than L2: %.1f GB of KV across the layers"
+                         % (tensors.cache.numel() * 2 / 1e9)},
+        "attn": {"us_per_layer": attn_s * 1e6, "tflops": achieved, "flops_per_layer": flops},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "pkv_prefill_attn (planner + tcgen05 attention kernel), per layer",
+                     "peak_source": src + " (bf16, sustained)"},
+        "e2e": {"value": world * real * args.steps / (e2e_ms / 1e3), "unit": "new tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(batch, tensors, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+# ---------------------------------------------------------------------------
 def make_workload(name, device):
     from paged_kv_decode_pages_gb300 import workloads as W
     cfg = W.CONFIGS[name]
@@ -298,6 +490,11 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    from paged_kv_decode_pages_gb300 import workloads as W
+    if args.workload in W.PREFILL_CONFIGS:
+        if args.impl == "reference":
+            raise SystemExit("the reference arm times the decode step workloads")
+        return run_prefill(args, rank, world)
     if args.impl == "reference":
         return run_reference(args, rank, world)
 

@@ -235,7 +235,8 @@ size_t pkv_prefill_workspace_bytes(int batch);
  * Tensor cores (tcgen05, bf16 operands, fp32 accumulation in tensor
  * memory); a row's result depends on its own request only.  head_dim 64 or
  * 128, page_size a multiple of 16 up to 1024, up to 128 q heads per kv head.
- * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE.
+ * Errors: PKV_ERR_INVALID_ARG (also for sm_scale <= 0 or NaN),
+ * PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE.
  * Device: PKV_DEV_ERR_SEQ_LEN (rows written as zeros), PKV_DEV_ERR_PAGE
  * (page 0 read instead), PKV_DEV_ERR_INDPTR, PKV_DEV_ERR_TIMEOUT. */
 int pkv_prefill_attn(const pkv_cache_t *geom, const void *cache, int layer,

@@ -44,7 +44,7 @@ namespace pkv {
 constexpr int PF_M = 128;          // MMA rows of a tile
 constexpr int PF_N = 128;          // keys of a KV tile
 constexpr int PF_BLK = 16;         // tokens of one cache block (one TMA box)
-constexpr int PF_THREADS = 160;    // 4 softmax warps + the producer warp
+constexpr int PF_THREADS = 192;    // 4 softmax warps, the load warp, the MMA warp
 constexpr int PF_CHUNK = 16384;    // 128 rows x 128 bytes (64 bf16): one swizzle column
 constexpr int PF_TMEM_COLS = 256;  // S (128 columns) + O (up to 128)
 constexpr int PF_PLAN_THREADS = 1024;
@@ -239,7 +239,7 @@ struct PfShape {
   static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
   static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int NBAR = 10;
+  static constexpr int NBAR = 14;
   static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
 };
 
@@ -264,6 +264,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   uint64_t *bar_o = bars + 6;
   uint64_t *bar_p = bars + 7;
   uint64_t *bar_fin = bars + 8;
+  uint64_t *bar_sfree = bars + 9;   // S read out of tensor memory by all 128 rows
+  uint64_t *bar_kfree = bars + 10;  // [2] S of the K stage's tile has completed
+  uint64_t *bar_vfree = bars + 12;  // [2] P.V of the V stage's tile has completed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::NBAR);
   int32_t *dead = reinterpret_cast<int32_t *>(tmem_slot + 1);
 
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int kt_stale = (n - 1) / PF_N;     // the KV tile that holds slots past n - 1
 
   if (tid == 0) {
-    for (int i = 0; i < S::NBAR; ++i) mbar_init(&bars[i], i == 7 ? 128u : 1u);
+    for (int i = 0; i < S::NBAR; ++i) mbar_init(&bars[i], (i == 7 || i == 9) ? 128u : 1u);
     *dead = 0;
     fence_barrier_init();
   }
@@ -335,31 +338,76 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const uint32_t tm_s = tmem;        // S: columns [0, 128)
   const uint32_t tm_o = tmem + 128;  // O: columns [128, 128 + D)
 
+  bool alive = true;
+  auto wait = [&](uint64_t *bar, uint32_t parity) {  // warp-uniform give-up
+    if (!alive) return;
+    if (!__all_sync(FULL_MASK, mbar_wait(bar, parity))) {
+      alive = false;
+      if (lane == 0) {
+        report(a.err, PKV_DEV_ERR_TIMEOUT);
+        atomicExch(dead, 1);
+      }
+    }
+  };
   if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    const uint64_t policy = l2_evict_first_policy();
+    // ----------------------------------------------------------- load warp
+    // K and V of tile kt into stage kt & 1 as soon as the MMAs of tile
+    // kt - 2 have released it; the next tile's page ids are looked up
+    // (lanes 0-7, one block each) while the warp waits
+    const uint64_t policy = l2_evict_last_policy();  // every q tile re-reads the tiles
     const int page0 = a.layer * a.num_pages;
-    auto load_kv = [&](int kt, int kv, unsigned char *dst, uint64_t *bar) {
-      mbar_arrive_expect_tx(bar, (uint32_t)(NCH * 8 * PF_BLK * 128));
-      for (int i = 0; i < 8; ++i) {
-        int blk = kt * 8 + i;
-        if (blk > last_blk) blk = last_blk;  // past the request: any valid block (zeroed below)
-        const int pg = blk / a.bpp;
-        const int sub = blk - pg * a.bpp;
-        int pid = __ldg(a.page_table + (int64_t)b * a.max_pages + pg);
-        if (pid < 0 || pid >= a.num_pages) {
-          report(a.err, PKV_DEV_ERR_PAGE);
-          pid = 0;
+    auto page_of = [&](int kt) -> int {  // raw page id of block lane of tile kt
+      int blk = kt * 8 + (lane & 7);
+      if (blk > last_blk) blk = last_blk;  // past the request: any valid block (zeroed later)
+      return lane < 8 ? __ldg(a.page_table + (int64_t)b * a.max_pages + blk / a.bpp) : 0;
+    };
+    auto load_kv = [&](int kt, int raw, int kv, unsigned char *dst, uint64_t *bar) {
+      int blk = kt * 8 + (lane & 7);
+      if (blk > last_blk) blk = last_blk;
+      int pid = raw;
+      if (lane < 8 && (pid < 0 || pid >= a.num_pages)) {
+        if (kv == 0) report(a.err, PKV_DEV_ERR_PAGE);
+        pid = 0;
+      }
+      const int c = pid * a.bpp + blk % a.bpp;
+      int c8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c8[i] = __shfl_sync(FULL_MASK, c, i);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, (uint32_t)(NCH * 8 * PF_BLK * 128));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int pg = c8[i] / a.bpp, sub = c8[i] - pg * a.bpp;
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch)
+            tma_load_5d(dst + ch * PF_CHUNK + i * PF_BLK * 128, &kv_map, ch * 64, g, sub * PF_BLK,
+                        kv, page0 + pg, bar, policy);
         }
-        for (int c = 0; c < NCH; ++c)
-          tma_load_5d(dst + c * PF_CHUNK + i * PF_BLK * 128, &kv_map, c * 64, g, sub * PF_BLK,
-                      kv, page0 + pid, bar, policy);
       }
     };
+    int raw = page_of(0);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_q, (uint32_t)(NCH * a.tq * G * 128));
+      for (int ch = 0; ch < NCH; ++ch)
+        tma_load_3d(qs + ch * PF_CHUNK, &q_map, ch * 64, g * G, t0, bar_q);
+    }
+    for (int kt = 0; kt < nkv && alive; ++kt) {
+      const int st = kt & 1;
+      const int raw_next = kt + 1 < nkv ? page_of(kt + 1) : 0;
+      if (kt >= 2) wait(&bar_kfree[st], (uint32_t)(((kt >> 1) + 1) & 1));
+      if (!alive) break;
+      load_kv(kt, raw, 0, ks + st * S::KV_BYTES, &bar_k[st]);
+      if (kt >= 2) wait(&bar_vfree[st], (uint32_t)(((kt >> 1) + 1) & 1));
+      if (!alive) break;
+      load_kv(kt, raw, 1, vs + st * S::KV_BYTES, &bar_v[st]);
+      raw = raw_next;
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA warp
     constexpr uint32_t IDESC_S = bf16_idesc(PF_M, PF_N, false);
     constexpr uint32_t IDESC_O = bf16_idesc(PF_M, D, true);
     const uint32_t qa = smem_addr(qs), ka = smem_addr(ks), va = smem_addr(vs), pa = smem_addr(ps);
-    auto issue_s = [&](int stage) {
+    auto issue_s = [&](int stage) {  // S = Q K^T, then release the K stage
       const uint32_t kb = ka + stage * S::KV_BYTES;
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
@@ -368,8 +416,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                k > 0);
       }
       tc_commit(bar_s);
+      tc_commit(&bar_kfree[stage]);
     };
-    auto issue_o = [&](int stage, bool acc) {
+    auto issue_o = [&](int stage, bool acc) {  // O += P V, then release the V stage
       const uint32_t vb = va + stage * S::KV_BYTES;
 #pragma unroll
       for (int k = 0; k < PF_N / 16; ++k) {
@@ -378,28 +427,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                IDESC_O, (acc || k > 0) ? 1u : 0u);
       }
       tc_commit(bar_o);
+      tc_commit(&bar_vfree[stage]);
     };
-    bool alive = true;
-    auto wait = [&](uint64_t *bar, uint32_t parity) {  // warp-uniform give-up
-      if (!alive) return;
-      if (!__all_sync(FULL_MASK, mbar_wait(bar, parity))) {
-        alive = false;
-        if (lane == 0) {
-          report(a.err, PKV_DEV_ERR_TIMEOUT);
-          atomicExch(dead, 1);
-        }
-      }
-    };
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, (uint32_t)(NCH * a.tq * G * 128));
-      for (int c = 0; c < NCH; ++c) tma_load_3d(qs + c * PF_CHUNK, &q_map, c * 64, g * G, t0, bar_q);
-      load_kv(0, 0, ks, &bar_k[0]);
-      load_kv(0, 1, vs, &bar_v[0]);
-      if (nkv > 1) {
-        load_kv(1, 0, ks + S::KV_BYTES, &bar_k[1]);
-        load_kv(1, 1, vs + S::KV_BYTES, &bar_v[1]);
-      }
-    }
     wait(bar_q, 0);
     wait(&bar_k[0], 0);
     if (alive && lane == 0) {
@@ -408,13 +437,22 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
     for (int kt = 0; kt < nkv && alive; ++kt) {
       const int st = kt & 1;
-      const uint32_t ph = (uint32_t)((kt >> 1) & 1);
-      wait(bar_p, (uint32_t)(kt & 1));  // S[kt] read, P[kt] written, O rescaled
+      const uint32_t par = (uint32_t)(kt & 1);
+      // S[kt+1] as soon as S[kt] has been read: it runs on the tensor cores
+      // while the softmax of tile kt is computed
+      wait(bar_sfree, par);
+      if (kt + 1 < nkv) {
+        wait(&bar_k[st ^ 1], (uint32_t)(((kt + 1) >> 1) & 1));
+        if (!alive) break;
+        if (lane == 0) {
+          tc_fence_after();
+          issue_s(st ^ 1);
+        }
+      }
+      wait(bar_p, par);  // P[kt] written, O rescaled
+      wait(&bar_v[st], (uint32_t)((kt >> 1) & 1));
       if (!alive) break;
       tc_fence_after();
-      if (lane == 0 && kt + 2 < nkv) load_kv(kt + 2, 0, ks + st * S::KV_BYTES, &bar_k[st]);
-      wait(&bar_v[st], ph);
-      if (!alive) break;
       if (kt == kt_stale) {
         // slots past the request's last position: zero the V rows
         const int r0 = n - kt * PF_N;
@@ -428,23 +466,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (lane == 0) {
-        tc_fence_after();
-        issue_o(st, kt > 0);
-      }
-      if (kt + 1 < nkv) {
-        wait(&bar_k[st ^ 1], (uint32_t)(((kt + 1) >> 1) & 1));
-        if (!alive) break;
-        if (lane == 0) {
-          tc_fence_after();
-          issue_s(st ^ 1);
-        }
-      }
-      if (kt + 2 < nkv) {
-        wait(bar_o, (uint32_t)(kt & 1));  // PV[kt] done: its V stage is free
-        if (!alive) break;
-        if (lane == 0) load_kv(kt + 2, 1, vs + st * S::KV_BYTES, &bar_v[st]);
-      }
+      if (lane == 0) issue_o(st, kt > 0);
     }
     // drain: every MMA this thread issued has completed
     if (lane == 0) {
@@ -476,37 +498,54 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + lane_off + c * 32, sr[c]);
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_sfree);  // the tensor cores may overwrite S now
+      // causal mask (raw scores; only tiles that reach past some row's
+      // position need it)
       const int lim = valid ? p - kt * PF_N : -1;  // keys <= lim are allowed
       float mx = -INFINITY;
+      if (__any_sync(FULL_MASK, lim < PF_N - 1)) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x = (c * 32 + j <= lim) ? __uint_as_float(sr[c][j]) * a.qscale : -INFINITY;
-          sr[c][j] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
+          for (int j = 0; j < 32; ++j) {
+            const float x = (c * 32 + j <= lim) ? __uint_as_float(sr[c][j]) : -INFINITY;
+            sr[c][j] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(sr[c][j]));
+      }
+      mx *= a.qscale;  // log2 units (qscale > 0)
       float m_ref = m_run, alpha = 1.0f;
       if (mx > m_run + PF_TAU) {
         m_ref = mx;
         alpha = fast_exp2(m_run - mx);  // 0 when m_run = -inf
       }
       const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
-      float sum = 0.0f, wsum = 0.0f;
+      // p = 2^(s * qscale - m), two at a time
+      const f32x2 sc2 = pack2(a.qscale, a.qscale), nm2 = pack2(-m_use, -m_use);
+      f32x2 acc = pack2(0.0f, 0.0f), wacc = pack2(0.0f, 0.0f);
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          const float p0 = fast_exp2(__uint_as_float(sr[c][j]) - m_use);
-          const float p1 = fast_exp2(__uint_as_float(sr[c][j + 1]) - m_use);
-          sum += p0 + p1;
+          const float2 t = unpack2(
+              ffma2(pack2(__uint_as_float(sr[c][j]), __uint_as_float(sr[c][j + 1])), sc2, nm2));
+          const float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
+          const f32x2 pp = pack2(p0, p1);
+          acc = fadd2(acc, pp);
           const uint32_t w = pack_bf16x2(p0, p1);
-          wsum += bf16lo(w) + bf16hi(w);
+          wacc = fadd2(wacc, pack2(bf16lo(w), bf16hi(w)));
           pk[(c * 32 + j) >> 1] = w;
         }
-      l_run = l_run * alpha + sum;
-      w_run = w_run * alpha + wsum;
+      const float2 accf = unpack2(acc), waccf = unpack2(wacc);
+      l_run = l_run * alpha + (accf.x + accf.y);
+      w_run = w_run * alpha + (waccf.x + waccf.y);
       const bool resc = kt > 0 && alpha != 1.0f;
       m_run = m_ref;
       if (kt > 0) {
@@ -682,7 +721,7 @@ extern "C" int pkv_prefill_attn(const pkv_cache_t *geom, const void *cache, int 
   if (batch <= 0 || total_tokens <= 0 || max_pages <= 0 || layer < 0 ||
       layer >= geom->num_layers || num_qo_heads <= 0 || num_qo_heads % geom->num_kv_heads != 0)
     return PKV_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale)) return PKV_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.0f)) return PKV_ERR_INVALID_ARG;  // the row maximum is taken on raw scores
   const int D = geom->head_dim;
   const int G = num_qo_heads / geom->num_kv_heads;
   if ((D != 64 && D != 128) || geom->page_size % PF_BLK != 0 || geom->page_size > 1024 ||
