@@ -107,6 +107,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   }
 }
 
+// The same, polling without a suspend hint: for hand-offs on a critical
+// path, where waking a suspended thread costs more than the wait itself.
+// Still bounded: the global timer is checked every 256 polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity,
+                                               uint64_t limit_ns = 4000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // One bulk (non-tensor) TMA copy global -> shared, completing on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,

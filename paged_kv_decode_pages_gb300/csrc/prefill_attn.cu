@@ -246,6 +246,7 @@ struct PfShape {
 template <int D>
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_attn_kernel(const PfArgs a, const __grid_constant__ CUtensorMap kv_map,
+                        const __grid_constant__ CUtensorMap kv_map128,
                         const __grid_constant__ CUtensorMap q_map) {
   using S = PfShape<D>;
   constexpr int NCH = S::NCH;
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   bool alive = true;
   auto wait = [&](uint64_t *bar, uint32_t parity) {  // warp-uniform give-up
     if (!alive) return;
-    if (!__all_sync(FULL_MASK, mbar_wait(bar, parity))) {
+    if (!__all_sync(FULL_MASK, mbar_wait_spin(bar, parity))) {
       alive = false;
       if (lane == 0) {
         report(a.err, PKV_DEV_ERR_TIMEOUT);
@@ -361,6 +362,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       if (blk > last_blk) blk = last_blk;  // past the request: any valid block (zeroed later)
       return lane < 8 ? __ldg(a.page_table + (int64_t)b * a.max_pages + blk / a.bpp) : 0;
     };
+    // pages of 128 tokens or more (a multiple of 128): a tile lies in one
+    // page and comes in as NCH boxes of 128 rows
+    const bool whole = (a.bpp & 7) == 0;
     auto load_kv = [&](int kt, int raw, int kv, unsigned char *dst, uint64_t *bar) {
       int blk = kt * 8 + (lane & 7);
       if (blk > last_blk) blk = last_blk;
@@ -375,13 +379,23 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       for (int i = 0; i < 8; ++i) c8[i] = __shfl_sync(FULL_MASK, c, i);
       if (lane == 0) {
         mbar_arrive_expect_tx(bar, (uint32_t)(NCH * 8 * PF_BLK * 128));
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int pg = c8[i] / a.bpp, sub = c8[i] - pg * a.bpp;
+        if (whole) {
+          // block 0 of the tile sits at an in-page offset that is a multiple
+          // of 8 blocks; the whole 128-row box stays inside the page
+          const int pg = c8[0] / a.bpp, sub = c8[0] - pg * a.bpp;
 #pragma unroll
           for (int ch = 0; ch < NCH; ++ch)
-            tma_load_5d(dst + ch * PF_CHUNK + i * PF_BLK * 128, &kv_map, ch * 64, g, sub * PF_BLK,
-                        kv, page0 + pg, bar, policy);
+            tma_load_5d(dst + ch * PF_CHUNK, &kv_map128, ch * 64, g, sub * PF_BLK, kv, page0 + pg,
+                        bar, policy);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int pg = c8[i] / a.bpp, sub = c8[i] - pg * a.bpp;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
+              tma_load_5d(dst + ch * PF_CHUNK + i * PF_BLK * 128, &kv_map, ch * 64, g,
+                          sub * PF_BLK, kv, page0 + pg, bar, policy);
+          }
         }
       }
     };
@@ -471,7 +485,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // drain: every MMA this thread issued has completed
     if (lane == 0) {
       tc_commit(bar_fin);
-      if (!mbar_wait(bar_fin, 0)) report(a.err, PKV_DEV_ERR_TIMEOUT);
+      if (!mbar_wait_spin(bar_fin, 0)) report(a.err, PKV_DEV_ERR_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -488,7 +502,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     float m_run = -INFINITY, l_run = 0.0f, w_run = 0.0f;
     bool alive = true;
     for (int kt = 0; kt < nkv; ++kt) {
-      if (!__all_sync(FULL_MASK, mbar_wait(bar_s, (uint32_t)(kt & 1)))) {  // warp-uniform
+      if (!__all_sync(FULL_MASK, mbar_wait_spin(bar_s, (uint32_t)(kt & 1)))) {  // warp-uniform
         alive = false;
         if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
         break;
@@ -550,7 +564,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       m_run = m_ref;
       if (kt > 0) {
         // PV[kt-1] done: O is stable and the P buffer free
-        if (!__all_sync(FULL_MASK, mbar_wait(bar_o, (uint32_t)((kt - 1) & 1)))) {
+        if (!__all_sync(FULL_MASK, mbar_wait_spin(bar_o, (uint32_t)((kt - 1) & 1)))) {
           alive = false;
           if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
           break;
@@ -582,7 +596,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar_p);
     }
-    if (alive && __all_sync(FULL_MASK, mbar_wait(bar_o, (uint32_t)((nkv - 1) & 1)))) {
+    if (alive && __all_sync(FULL_MASK, mbar_wait_spin(bar_o, (uint32_t)((nkv - 1) & 1)))) {
       tc_fence_after();
       const float inv = w_run > 0.0f ? 1.0f / w_run : 0.0f;
       const int t = t0 + tok;
@@ -639,14 +653,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 pf_encoder() {
 
 // (head_dim, kv head, slot, K/V, layer * num_pages + page); one box = 64
 // dims x 16 slots of one kv head, K or V, 128-byte swizzled
-static int encode_kv_map(CUtensorMap *map, const void *cache, const pkv_cache_t *g) {
+static int encode_kv_map(CUtensorMap *map, const void *cache, const pkv_cache_t *g,
+                         int box_rows) {
   auto enc = pf_encoder();
   if (enc == nullptr) return PKV_ERR_CUDA;
   const cuuint64_t D = (cuuint64_t)g->head_dim, H = (cuuint64_t)g->num_kv_heads;
   const cuuint64_t PS = (cuuint64_t)g->page_size;
   const cuuint64_t dims[5] = {D, H, PS, 2, (cuuint64_t)g->num_layers * (cuuint64_t)g->num_pages};
   const cuuint64_t strides[4] = {D * 2, H * D * 2, PS * H * D * 2, 2 * PS * H * D * 2};
-  const cuuint32_t box[5] = {64, 1, (cuuint32_t)PF_BLK, 1, 1};
+  const cuuint32_t box[5] = {64, 1, (cuuint32_t)box_rows, 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -680,8 +695,8 @@ static PfWs pf_ws(int batch) {
 }
 
 template <int D>
-static int launch_prefill(const PfArgs &a, const CUtensorMap &kvm, const CUtensorMap &qm,
-                          int max_units, cudaStream_t st) {
+static int launch_prefill(const PfArgs &a, const CUtensorMap &kvm, const CUtensorMap &kvm128,
+                          const CUtensorMap &qm, int max_units, cudaStream_t st) {
   using S = PfShape<D>;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -695,7 +710,7 @@ static int launch_prefill(const PfArgs &a, const CUtensorMap &kvm, const CUtenso
   if (launch_pdl(prefill_plan_kernel, dim3(1), dim3(PF_PLAN_THREADS), 0, st, a) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (launch_pdl(prefill_attn_kernel<D>, dim3((unsigned)max_units), dim3(PF_THREADS),
-                 (size_t)S::SMEM_BYTES, st, a, kvm, qm) != cudaSuccess)
+                 (size_t)S::SMEM_BYTES, st, a, kvm, kvm128, qm) != cudaSuccess)
     return PKV_ERR_CUDA;
   return launch_status();
 }
@@ -761,12 +776,15 @@ extern "C" int pkv_prefill_attn(const pkv_cache_t *geom, const void *cache, int 
   // tiles: sum over requests of ceil(q_b / tq) <= T / tq + B
   const int64_t max_units = ((int64_t)(total_tokens + a.tq - 1) / a.tq + batch) * geom->num_kv_heads;
   if (max_units > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  alignas(64) CUtensorMap kvm, qm;
-  st = encode_kv_map(&kvm, cache, geom);
+  alignas(64) CUtensorMap kvm, kvm128, qm;
+  st = encode_kv_map(&kvm, cache, geom, PF_BLK);
+  if (st != PKV_OK) return st;
+  // 128-row boxes (used only when a page holds a multiple of 128 tokens)
+  st = encode_kv_map(&kvm128, cache, geom, geom->page_size % PF_N == 0 ? PF_N : PF_BLK);
   if (st != PKV_OK) return st;
   st = encode_q_map(&qm, q, total_tokens, num_qo_heads, D, G, a.tq);
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return D == 128 ? launch_prefill<128>(a, kvm, qm, (int)max_units, s)
-                  : launch_prefill<64>(a, kvm, qm, (int)max_units, s);
+  return D == 128 ? launch_prefill<128>(a, kvm, kvm128, qm, (int)max_units, s)
+                  : launch_prefill<64>(a, kvm, kvm128, qm, (int)max_units, s);
 }
