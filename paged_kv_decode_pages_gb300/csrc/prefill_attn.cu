@@ -75,7 +75,8 @@ struct PfArgs {
   int batch;
   uint16_t *out;  // bf16 [T][Hq][D]
   float *lse;     // [T][Hq] or null
-  int32_t *tile_start;  // [B + 1]
+  int32_t *tile_start;  // [B + 1] first tile of each position of the schedule
+  int32_t *order;       // [B] request at each position (longest context first)
   PfHeader *hdr;
   int32_t *err;
 };
@@ -187,21 +188,41 @@ __device__ __forceinline__ int request_tiles(const PfArgs &a, int b) {
   return q > 0 ? (q + a.tq - 1) / a.tq : 0;
 }
 
+// schedule key of a request: its context length (the KV its heaviest tile
+// streams), -1 when it has no tiles
+__device__ __forceinline__ int request_key(const PfArgs &a, int b) {
+  const int q = a.qo_indptr[b + 1] - a.qo_indptr[b];
+  if (q <= 0) return -1;
+  const int n = a.seq_lens[b];
+  return n > 0 ? n : 0;
+}
+
 __global__ void __launch_bounds__(PF_PLAN_THREADS) prefill_plan_kernel(const PfArgs a) {
   __shared__ int32_t scan[PF_PLAN_THREADS];
   __shared__ int32_t carry;
   pdl_trigger();
   const int tid = threadIdx.x;
   if (tid == 0) carry = 0;
+  // the schedule: requests by descending context length (ties by index), so
+  // that the longest units start first and the short ones fill the tail
+  for (int b = tid; b < a.batch; b += PF_PLAN_THREADS) {
+    if (a.qo_indptr[b + 1] < a.qo_indptr[b] || (b == 0 && a.qo_indptr[0] != 0))
+      report(a.err, PKV_DEV_ERR_INDPTR);
+    const int kb = request_key(a, b);
+    int rank = 0;
+    for (int o = 0; o < a.batch; ++o) {
+      const int ko = request_key(a, o);
+      rank += (ko > kb || (ko == kb && o < b)) ? 1 : 0;
+    }
+    a.order[rank] = b;
+  }
   __syncthreads();
   for (int base = 0; base < a.batch; base += PF_PLAN_THREADS) {
-    const int b = base + tid;
+    const int i = base + tid;
     int nt = 0;
-    if (b < a.batch) {
-      if (a.qo_indptr[b + 1] < a.qo_indptr[b] || (b == 0 && a.qo_indptr[0] != 0))
-        report(a.err, PKV_DEV_ERR_INDPTR);
-      else
-        nt = request_tiles(a, b);
+    if (i < a.batch) {
+      const int b = a.order[i];
+      if (a.qo_indptr[b + 1] >= a.qo_indptr[b]) nt = request_tiles(a, b);
     }
     scan[tid] = nt;
     __syncthreads();
@@ -211,7 +232,7 @@ __global__ void __launch_bounds__(PF_PLAN_THREADS) prefill_plan_kernel(const PfA
       scan[tid] += v;
       __syncthreads();
     }
-    if (b < a.batch) a.tile_start[b] = carry + scan[tid] - nt;
+    if (i < a.batch) a.tile_start[i] = carry + scan[tid] - nt;
     __syncthreads();
     if (tid == PF_PLAN_THREADS - 1) carry += scan[tid];
     __syncthreads();
@@ -283,7 +304,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int u = blockIdx.x;
   if (u >= a.hdr->total_units) return;
   const int su = u / Hkv, g = u % Hkv;
-  // request of tile su: the last b with tile_start[b] <= su
+  // schedule position of tile su: the last i with tile_start[i] <= su
   int lo = 0, hi = a.batch - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -292,10 +313,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     else
       hi = mid - 1;
   }
-  const int b = lo;
+  const int b = a.order[lo];
   const int q = a.qo_indptr[b + 1] - a.qo_indptr[b];
-  const int ntiles_b = a.tile_start[b + 1] - a.tile_start[b];
-  const int ti = ntiles_b - 1 - (su - a.tile_start[b]);  // heaviest tile first
+  const int ntiles_b = a.tile_start[lo + 1] - a.tile_start[lo];
+  const int ti = ntiles_b - 1 - (su - a.tile_start[lo]);  // heaviest tile first
   const int n = a.seq_lens[b];
   const int t0 = a.qo_indptr[b] + ti * a.tq;
   const int ntok = min(a.tq, q - ti * a.tq);
@@ -684,12 +705,13 @@ static int encode_q_map(CUtensorMap *map, const void *q, int T, int Hq, int D, i
 }
 
 struct PfWs {
-  size_t tile_start, hdr, total;
+  size_t tile_start, order, hdr, total;
 };
 static PfWs pf_ws(int batch) {
   PfWs w;
   w.tile_start = 0;
-  w.hdr = align_up((size_t)(batch + 1) * sizeof(int32_t), 256);
+  w.order = align_up((size_t)(batch + 1) * sizeof(int32_t), 256);
+  w.hdr = w.order + align_up((size_t)batch * sizeof(int32_t), 256);
   w.total = w.hdr + 256;
   return w;
 }
@@ -771,6 +793,7 @@ extern "C" int pkv_prefill_attn(const pkv_cache_t *geom, const void *cache, int 
   a.lse = lse;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   a.tile_start = reinterpret_cast<int32_t *>(ws + wl.tile_start);
+  a.order = reinterpret_cast<int32_t *>(ws + wl.order);
   a.hdr = reinterpret_cast<PfHeader *>(ws + wl.hdr);
   a.err = err_word;
   // tiles: sum over requests of ceil(q_b / tq) <= T / tq + B
