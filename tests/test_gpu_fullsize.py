@@ -152,3 +152,61 @@ def test_full_size_sampler_ext_every_row(name):
     if not np.any(mism):
         np.testing.assert_array_equal(step.ext_history.cpu().numpy(), hist)
     print(name, "ext sampler near-ties:", int(near.sum()))
+
+
+@pytest.mark.parametrize("name", ["mixed_qwen3_4b", "prefill_qwen3_4b_p128"])
+def test_full_size_prefill_step_sampled_windows(name):
+    """A prefill / mixed step at its full size (every layer, the launch
+    configuration bench.py times); the oracle then recomputes windows of
+    new tokens of sampled requests at the first and last layer from the
+    cache the step left (causality: a window's outputs need only the keys
+    up to its last position, all in that cache)."""
+    from paged_kv_decode_pages_gb300.step import PrefillStep
+    cfg = W.PREFILL_CONFIGS[name]
+    batch = W.make_prefill_batch(cfg)
+    dev = W.PrefillTensors(batch, device="cuda")
+    q_in = {l: W.bf16_bits(dev.q[l]) for l in (0, cfg.num_layers - 1)}
+    kv_in = {l: (W.bf16_bits(dev.k[l]), W.bf16_bits(dev.v[l])) for l in (0, cfg.num_layers - 1)}
+    step = PrefillStep(batch, dev)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.err.item()) == 0
+    act = [b for b in range(batch.B) if batch.active[b]]
+    prompts = [b for b in act if batch.new_tokens(b) > 1]
+    decodes = [b for b in act if batch.new_tokens(b) == 1]
+    picks = prompts[:2] + decodes[:2]
+    ps = cfg.page_size
+    worst = 0.0
+    for l in (0, cfg.num_layers - 1):
+        for b in picks:
+            n, qn = int(batch.seq_lens[b]), batch.new_tokens(b)
+            lo0 = int(batch.qo_indptr[b])
+            # windows: the first and the last 8 new tokens (or the only one)
+            wins = [(0, min(8, qn)), (max(0, qn - 8), qn)]
+            npg = (n + ps - 1) // ps
+            pages = torch.as_tensor(batch.page_table[b, :npg].astype(np.int64), device="cuda")
+            body = step.t.cache[l].index_select(0, pages).cpu()
+            compact = torch.zeros((1, npg + 1) + tuple(body.shape[1:]), dtype=body.dtype)
+            compact[0, 1:] = body
+            cb = W.bf16_bits(compact)
+            pt = np.arange(1, npg + 1, dtype=np.int32)[None, :]
+            # the appended tokens are exactly the inputs
+            kk, vv = kv_in[l]
+            for i in (0, qn - 1):
+                pos = n - qn + i
+                got_k = W.bf16_bits(step.t.cache[l, int(batch.page_table[b, pos // ps]), 0,
+                                                 pos % ps])
+                np.testing.assert_array_equal(got_k, kk[lo0 + i])
+            for a0, a1 in wins:
+                ind = np.array([0, a1 - a0], np.int32)
+                sl = np.array([n - qn + a1], np.int32)
+                want, want_lse, bad = oracle.prefill_attn(cb, 0, q_in[l][lo0 + a0:lo0 + a1], ind,
+                                                          pt, sl, np.ones(1, np.int32))
+                assert bad == 0
+                got = step.out[l, lo0 + a0:lo0 + a1].float().cpu().numpy().astype(np.float64)
+                err = np.abs(got - want)
+                assert err.max() <= 1e-2 and err.mean() <= 1e-3, (name, l, b, a0, err.max())
+                worst = max(worst, float(err.max()))
+                lse = step.lse[l, lo0 + a0:lo0 + a1].cpu().numpy().astype(np.float64)
+                assert np.abs(lse - want_lse).max() <= 1e-3
+    print(name, "prefill windows worst max-abs", worst)
