@@ -44,7 +44,7 @@ namespace pkv {
 constexpr int PF_M = 128;          // MMA rows of a tile
 constexpr int PF_N = 128;          // keys of a KV tile
 constexpr int PF_BLK = 16;         // tokens of one cache block (one TMA box)
-constexpr int PF_THREADS = 192;    // 4 softmax warps, the load warp, the MMA warp
+constexpr int PF_THREADS = 224;    // 4 softmax warps, K load warp, MMA warp, V load warp
 constexpr int PF_CHUNK = 16384;    // 128 rows x 128 bytes (64 bf16): one swizzle column
 constexpr int PF_TMEM_COLS = 256;  // S (128 columns) + O (up to 128)
 constexpr int PF_PLAN_THREADS = 1024;
@@ -371,8 +371,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       }
     }
   };
-  if (warp == 4) {
-    // ----------------------------------------------------------- load warp
+  if (warp == 4 || warp == 6) {
+    // ---------------------------------------------------------- load warps
+    // warp 4 brings Q and the K tiles, warp 6 the V tiles (on small pages a
+    // tile is 8 boxes per 64-dim column, and two warps issue them in parallel)
     // K and V of tile kt into stage kt & 1 as soon as the MMAs of tile
     // kt - 2 have released it; the next tile's page ids are looked up
     // (lanes 0-7, one block each) while the warp waits
@@ -420,8 +422,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
       }
     };
+    const int kv = warp == 4 ? 0 : 1;
+    uint64_t *full = kv == 0 ? bar_k : bar_v;
+    uint64_t *freed = kv == 0 ? bar_kfree : bar_vfree;
+    unsigned char *buf = kv == 0 ? ks : vs;
     int raw = page_of(0);
-    if (lane == 0) {
+    if (kv == 0 && lane == 0) {
       mbar_arrive_expect_tx(bar_q, (uint32_t)(NCH * a.tq * G * 128));
       for (int ch = 0; ch < NCH; ++ch)
         tma_load_3d(qs + ch * PF_CHUNK, &q_map, ch * 64, g * G, t0, bar_q);
@@ -429,12 +435,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     for (int kt = 0; kt < nkv && alive; ++kt) {
       const int st = kt & 1;
       const int raw_next = kt + 1 < nkv ? page_of(kt + 1) : 0;
-      if (kt >= 2) wait(&bar_kfree[st], (uint32_t)(((kt >> 1) + 1) & 1));
+      if (kt >= 2) wait(&freed[st], (uint32_t)(((kt >> 1) + 1) & 1));
       if (!alive) break;
-      load_kv(kt, raw, 0, ks + st * S::KV_BYTES, &bar_k[st]);
-      if (kt >= 2) wait(&bar_vfree[st], (uint32_t)(((kt >> 1) + 1) & 1));
-      if (!alive) break;
-      load_kv(kt, raw, 1, vs + st * S::KV_BYTES, &bar_v[st]);
+      load_kv(kt, raw, kv, buf + st * S::KV_BYTES, &full[st]);
       raw = raw_next;
     }
   } else if (warp == 5) {
