@@ -397,29 +397,25 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         pid = 0;
       }
       const int c = pid * a.bpp + blk % a.bpp;
-      int c8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c8[i] = __shfl_sync(FULL_MASK, c, i);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar, (uint32_t)(NCH * 8 * PF_BLK * 128));
-        if (whole) {
-          // block 0 of the tile sits at an in-page offset that is a multiple
-          // of 8 blocks; the whole 128-row box stays inside the page
-          const int pg = c8[0] / a.bpp, sub = c8[0] - pg * a.bpp;
-#pragma unroll
-          for (int ch = 0; ch < NCH; ++ch)
-            tma_load_5d(dst + ch * PF_CHUNK, &kv_map128, ch * 64, g, sub * PF_BLK, kv, page0 + pg,
-                        bar, policy);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int pg = c8[i] / a.bpp, sub = c8[i] - pg * a.bpp;
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch)
-              tma_load_5d(dst + ch * PF_CHUNK + i * PF_BLK * 128, &kv_map, ch * 64, g,
-                          sub * PF_BLK, kv, page0 + pg, bar, policy);
-          }
+      const int c0 = __shfl_sync(FULL_MASK, c, 0);
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(NCH * 8 * PF_BLK * 128));
+      __syncwarp();
+      if (whole) {
+        // block 0 of the tile sits at an in-page offset that is a multiple
+        // of 8 blocks; one 128-row box per 64-dim column (lane ch) stays
+        // inside the page
+        if (lane < NCH) {
+          const int pg0 = c0 / a.bpp, sub0 = c0 - pg0 * a.bpp;
+          tma_load_5d(dst + lane * PF_CHUNK, &kv_map128, lane * 64, g, sub0 * PF_BLK, kv,
+                      page0 + pg0, bar, policy);
         }
+      } else if (lane < 8) {
+        // lane i issues the boxes of block i (the issue cost is per thread)
+        const int pg = c / a.bpp, sub = c - pg * a.bpp;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch)
+          tma_load_5d(dst + ch * PF_CHUNK + lane * PF_BLK * 128, &kv_map, ch * 64, g,
+                      sub * PF_BLK, kv, page0 + pg, bar, policy);
       }
     };
     const int kv = warp == 4 ? 0 : 1;
