@@ -17,14 +17,15 @@
 //    and 128-key K and V tiles (16-token blocks of the pages, 128-byte
 //    swizzle, two stages each) into shared memory; tcgen05.mma computes
 //    S = Q K^T into tensor memory and O += P V into tensor memory
-//    (bf16 operands, fp32 accumulation), each completion signalled by
-//    tcgen05.commit on an mbarrier;
+//    (bf16 operands, fp32 accumulation; P is the A operand straight from
+//    tensor memory, so P.V reads only V from shared memory), each
+//    completion signalled by tcgen05.commit on an mbarrier;
 //  * warps 0-3 own one row each: they read the row of S from tensor memory,
 //    apply the causal mask, run the online softmax in log2 units with a
 //    lazy maximum (O is rescaled in tensor memory only when the running
-//    maximum grows by more than 8), write P as bf16 into shared memory in
-//    the MMA's swizzled layout, and at the end read O, divide by the row
-//    sum and store it;
+//    maximum grows by more than 8), write P as bf16 pairs into tensor memory
+//    (tcgen05.st), and at the end read O, divide by the row sum and store
+//    it;
 //  * stale cache slots past a request's last position are zeroed in shared
 //    memory before they meet P (whose entries there are 0), so whatever an
 //    unwritten slot holds cannot reach the output;
@@ -46,7 +47,7 @@ constexpr int PF_N = 128;          // keys of a KV tile
 constexpr int PF_BLK = 16;         // tokens of one cache block (one TMA box)
 constexpr int PF_THREADS = 224;    // 4 softmax warps, K load warp, MMA warp, V load warp
 constexpr int PF_CHUNK = 16384;    // 128 rows x 128 bytes (64 bf16): one swizzle column
-constexpr int PF_TMEM_COLS = 256;  // S (128 columns) + O (up to 128)
+constexpr int PF_TMEM_COLS = 512;  // S (128 columns), O (up to 128), P (64: bf16 pairs)
 constexpr int PF_PLAN_THREADS = 1024;
 constexpr float PF_TAU = 8.0f;     // lazy-rescale threshold (log2 units)
 
@@ -119,6 +120,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same with A (M x K, bf16 pairs along K in each 32-bit column) read from
+// tensor memory: no shared-memory traffic for A.
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -254,14 +267,15 @@ struct PfShape {
   static constexpr int NCH = D / 64;                  // 64-dim swizzle columns
   static constexpr int Q_BYTES = NCH * PF_CHUNK;
   static constexpr int KV_BYTES = NCH * PF_CHUNK;     // one K or V stage
-  static constexpr int P_BYTES = 2 * PF_CHUNK;        // 128 rows x 128 keys
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr int NBAR = 14;
-  static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
+  // + alignment slack; at least 120 KB, so that one CTA (which holds all
+  // 512 tensor-memory columns) is resident per SM
+  static constexpr int SMEM_BYTES =
+      OFF_BAR + NBAR * 8 + 16 + 1024 > 120 * 1024 ? OFF_BAR + NBAR * 8 + 16 + 1024 : 120 * 1024;
 };
 
 template <int D>
@@ -277,7 +291,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   unsigned char *qs = sm + S::OFF_Q;
   unsigned char *ks = sm + S::OFF_K;  // [2][NCH][128 rows][128 B]
   unsigned char *vs = sm + S::OFF_V;
-  unsigned char *ps = sm + S::OFF_P;  // [2 key columns][128 rows][128 B]
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::OFF_BAR);
   uint64_t *bar_q = bars + 0;
   uint64_t *bar_k = bars + 1;  // [2]
@@ -359,6 +372,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_s = tmem;        // S: columns [0, 128)
   const uint32_t tm_o = tmem + 128;  // O: columns [128, 128 + D)
+  const uint32_t tm_p = tmem + 256;  // P: columns [256, 320), keys 2c, 2c + 1 in column c
 
   bool alive = true;
   auto wait = [&](uint64_t *bar, uint32_t parity) {  // warp-uniform give-up
@@ -440,26 +454,29 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // ------------------------------------------------------------ MMA warp
     constexpr uint32_t IDESC_S = bf16_idesc(PF_M, PF_N, false);
     constexpr uint32_t IDESC_O = bf16_idesc(PF_M, D, true);
-    const uint32_t qa = smem_addr(qs), ka = smem_addr(ks), va = smem_addr(vs), pa = smem_addr(ps);
+    // descriptors of the operand bases, built once; a K step only moves the
+    // start address (bits 0-13, in 16-byte units; every address here is
+    // below 256 KB, so the sum never carries out of the field)
+    const uint64_t dq = sw128_desc(smem_addr(qs), 16, 1024);
+    const uint64_t dk = sw128_desc(smem_addr(ks), 16, 1024);
+    const uint64_t dv = sw128_desc(smem_addr(vs), PF_CHUNK, 1024);
+    constexpr uint32_t STAGE16 = S::KV_BYTES >> 4;
     auto issue_s = [&](int stage) {  // S = Q K^T, then release the K stage
-      const uint32_t kb = ka + stage * S::KV_BYTES;
+      const uint64_t kb = dk + stage * STAGE16;
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k >> 2) * PF_CHUNK + (k & 3) * 32;
-        tc_mma(tm_s, sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024), IDESC_S,
-               k > 0);
+        const uint32_t off = ((k >> 2) * PF_CHUNK + (k & 3) * 32) >> 4;
+        tc_mma(tm_s, dq + off, kb + off, IDESC_S, k > 0);
       }
       tc_commit(bar_s);
       tc_commit(&bar_kfree[stage]);
     };
     auto issue_o = [&](int stage, bool acc) {  // O += P V, then release the V stage
-      const uint32_t vb = va + stage * S::KV_BYTES;
+      const uint64_t vb = dv + stage * STAGE16;
 #pragma unroll
-      for (int k = 0; k < PF_N / 16; ++k) {
-        const uint32_t poff = (k >> 2) * PF_CHUNK + (k & 3) * 32;
-        tc_mma(tm_o, sw128_desc(pa + poff, 16, 1024), sw128_desc(vb + k * 16 * 128, PF_CHUNK, 1024),
-               IDESC_O, (acc || k > 0) ? 1u : 0u);
-      }
+      for (int k = 0; k < PF_N / 16; ++k)  // 16 keys = 8 columns of P
+        tc_mma_ta(tm_o, tm_p + k * 8, vb + ((k * 16 * 128) >> 4), IDESC_O,
+                  (acc || k > 0) ? 1u : 0u);
       tc_commit(bar_o);
       tc_commit(&bar_vfree[stage]);
     };
@@ -603,16 +620,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           tmem_wait_st();
         }
       }
-      // P row r, keys 0..127, as two 64-key swizzle columns
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4 *dst = reinterpret_cast<uint4 *>(ps + c * PF_CHUNK + r * 128 + ((j ^ (r & 7)) << 4));
-          *dst = make_uint4(pk[c * 32 + 4 * j], pk[c * 32 + 4 * j + 1], pk[c * 32 + 4 * j + 2],
-                            pk[c * 32 + 4 * j + 3]);
-        }
-      fence_proxy_async_smem();
+      // P row r into tensor memory: column c holds keys 2c (low half), 2c + 1
+      tmem_st32(tm_p + lane_off, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+      tmem_st32(tm_p + lane_off + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_p);
     }
