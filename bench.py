@@ -12,6 +12,10 @@ Prints ONE JSON line (rank 0).  ``value`` is the step's algorithmic bytes
 (KV of every token inside each context + q + out + page-table reads +
 appended rows + logits [+ frame rows]) over the step time, in GB/s, summed
 over ranks (each rank runs its own replica: "replicas only", weak scaling).
+The step is timed as one captured CUDA graph replayed per step (the
+production launch; bit-identical to launching the kernels one by one);
+``roofline`` times each attention call with CUDA events in a second pass
+that launches the kernels one by one (reported under ``eager``).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
@@ -532,20 +536,39 @@ def main(argv=None):
         step.run(stream)
     barrier()
 
-    # ---- device-resident timed region --------------------------------
+    # ---- device-resident timed region: the step replayed as one captured
+    # CUDA graph (how the pages run a decode step) ------------------------
+    step.capture()
+    for _ in range(3):
+        step.replay()
+    barrier()
     clocks = Clocks(local)
-    attn_ev = []
-    samp_ev = []
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.replay()
+    e1.record(stream)
+    e1.synchronize()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(e0.elapsed_time(e1))
+    barrier()
+
+    # ---- the same step launched kernel by kernel, with CUDA events around
+    # every attention call (the roofline of the attention kernel) ----------
+    attn_ev = []
     e0.record(stream)
     for _ in range(args.steps):
         step.run(stream, attn_events=attn_ev)
     e1.record(stream)
     e1.synchronize()
-    clk = clocks.stop()
-    total_ms = max_over_ranks(e0.elapsed_time(e1))
+    eager_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    eager_line = {"ms_per_step": eager_ms,
+                  "value": world * sizes["step"] / (eager_ms / 1e3) / 1e9, "unit": "GB/s",
+                  "note": "kernel-by-kernel launches with an event pair around each "
+                          "attention call (these events keep the planner from overlapping "
+                          "the KV append)"}
     barrier()
 
     # ---- sampler alone (rows/s), same stream, after the timed step loop
@@ -596,22 +619,6 @@ def main(argv=None):
                       "codes_per_s": sizes["n_active"] * n_cb / (frame_us / 1e6)}
         barrier()
 
-    # ---- the same step replayed as one captured CUDA graph -------------
-    step.capture()
-    for _ in range(3):
-        step.replay()
-    g0 = torch.cuda.Event(enable_timing=True)
-    g1 = torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    for _ in range(args.steps):
-        step.replay()
-    g1.record(stream)
-    g1.synchronize()
-    graph_ms = max_over_ranks(g0.elapsed_time(g1)) / args.steps
-    graph_line = {"ms_per_step": graph_ms,
-                  "value": world * sizes["step"] / (graph_ms / 1e3) / 1e9, "unit": "GB/s",
-                  "kernels_per_replay": step.launches_per_step()}
-    barrier()
 
     # ---- end to end: host (pinned) inputs in, tokens out, every step ----
     host_in = [(tensors.q, tensors.q.cpu().pin_memory()), (tensors.k, tensors.k.cpu().pin_memory()),
@@ -634,7 +641,7 @@ def main(argv=None):
     for _ in range(args.steps):
         for d, h in host_in:
             d.copy_(h, non_blocking=True)
-        step.run(stream)
+        step.replay()
         for d, h in zip(outs, host_out):
             h.copy_(d, non_blocking=True)
     x1.record(stream)
@@ -660,7 +667,8 @@ def main(argv=None):
         "sampled_rows_per_s": world * sizes["n_active"] * args.steps / (total_ms / 1e3),
         "sampler": {"us_per_call": sampler_us,
                     "rows_per_s": sizes["n_active"] / (sampler_us / 1e6)},
-        "graph": graph_line,
+        "launch": "one captured CUDA graph per step (%d kernels)" % step.launches_per_step(),
+        "eager": eager_line,
         **({"sampler_ext": ext_line} if ext_line else {}),
         **({"frame": frame_line} if frame_line else {}),
         "attn": {"us_per_layer": attn_avg_s * 1e6, "gbs": achieved,
