@@ -80,10 +80,10 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def attn_traffic(workload):
-    """DRAM bytes per attention launch from the committed ncu summary, if it
-    was taken on the current kernel source; else None."""
-    src = os.path.join(ROOT, "paged_kv_decode_pages_gb300", "csrc", "decode_attn.cu")
+def attn_traffic(workload, source="decode_attn.cu"):
+    """DRAM bytes per attention launch (one layer) from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    src = os.path.join(ROOT, "paged_kv_decode_pages_gb300", "csrc", source)
     path = os.path.join(ROOT, "profiles", "attn_traffic.json")
     try:
         with open(path) as f:
@@ -407,7 +407,8 @@ def run_prefill(args, rank, world):
                          % (tensors.cache.numel() * 2 / 1e9)},
         "attn": {"us_per_layer": attn_s * 1e6, "tflops": achieved, "flops_per_layer": flops},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": attn_traffic(cfg.name, "prefill_attn.cu"),
                      "kernel": "pkv_prefill_attn (planner + tcgen05 attention kernel), per layer",
                      "peak_source": src + " (bf16, sustained)"},
         "e2e": {"value": world * real * args.steps / (e2e_ms / 1e3), "unit": "new tokens/s",

@@ -303,7 +303,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   uint64_t *bar_kfree = bars + 10;  // [2] S of the K stage's tile has completed
   uint64_t *bar_vfree = bars + 12;  // [2] P.V of the V stage's tile has completed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::NBAR);
-  int32_t *dead = reinterpret_cast<int32_t *>(tmem_slot + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -356,7 +355,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
   if (tid == 0) {
     for (int i = 0; i < S::NBAR; ++i) mbar_init(&bars[i], (i == 7 || i == 9) ? 128u : 1u);
-    *dead = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -379,10 +377,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     if (!alive) return;
     if (!__all_sync(FULL_MASK, mbar_wait_spin(bar, parity))) {
       alive = false;
-      if (lane == 0) {
-        report(a.err, PKV_DEV_ERR_TIMEOUT);
-        atomicExch(dead, 1);
-      }
+      if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
     }
   };
   if (warp == 4 || warp == 6) {
@@ -537,7 +532,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // rounded to bf16 for P.V (normalises O, so the output is a weighted
     // mean of the values with the weights the tensor cores actually used)
     float m_run = -INFINITY, l_run = 0.0f, w_run = 0.0f;
-    bool alive = true;
     for (int kt = 0; kt < nkv; ++kt) {
       if (!__all_sync(FULL_MASK, mbar_wait_spin(bar_s, (uint32_t)(kt & 1)))) {  // warp-uniform
         alive = false;
