@@ -14,8 +14,9 @@ appended rows + logits [+ frame rows]) over the step time, in GB/s, summed
 over ranks (each rank runs its own replica: "replicas only", weak scaling).
 The step is timed as one captured CUDA graph replayed per step (the
 production launch; bit-identical to launching the kernels one by one);
-``roofline`` times each attention call with CUDA events in a second pass
-that launches the kernels one by one (reported under ``eager``).
+``roofline`` times the attention calls of every layer captured alone as a
+second graph (CUDA events around its replays), and a third pass launches
+the step's kernels one by one (reported under ``eager``).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
@@ -555,8 +556,23 @@ def main(argv=None):
     total_ms = max_over_ranks(e0.elapsed_time(e1))
     barrier()
 
+    # ---- the attention kernels alone: every layer's planner + persistent
+    # kernel + merge captured as one graph, events around K replays (the
+    # roofline of the attention kernel) ------------------------------------
+    step.capture_attention()
+    for _ in range(3):
+        step.replay_attention()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.replay_attention()
+    e1.record(stream)
+    e1.synchronize()
+    attn_avg_s = max_over_ranks(e0.elapsed_time(e1)) / 1e3 / (args.steps * cfg.num_layers)
+    barrier()
+
     # ---- the same step launched kernel by kernel, with CUDA events around
-    # every attention call (the roofline of the attention kernel) ----------
+    # every attention call -------------------------------------------------
     attn_ev = []
     e0.record(stream)
     for _ in range(args.steps):
@@ -567,9 +583,10 @@ def main(argv=None):
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
     eager_line = {"ms_per_step": eager_ms,
                   "value": world * sizes["step"] / (eager_ms / 1e3) / 1e9, "unit": "GB/s",
+                  "attn_us_per_call": float(np.mean(attn_ms)) * 1e3,
                   "note": "kernel-by-kernel launches with an event pair around each "
                           "attention call (these events keep the planner from overlapping "
-                          "the KV append)"}
+                          "the KV append; on small layers the host's launch time shows)"}
     barrier()
 
     # ---- sampler alone (rows/s), same stream, after the timed step loop
@@ -653,7 +670,6 @@ def main(argv=None):
     ms_per_step = total_ms / args.steps
     value = world * sizes["step"] * args.steps / (total_ms / 1e3) / 1e9
     e2e_value = world * sizes["step"] * args.steps / (e2e_ms / 1e3) / 1e9
-    attn_avg_s = float(np.mean(attn_ms)) / 1e3
     achieved = sizes["attn_per_layer"] / attn_avg_s / 1e9
     peak, peak_src = peaks()
     line = {
@@ -673,7 +689,8 @@ def main(argv=None):
         **({"sampler_ext": ext_line} if ext_line else {}),
         **({"frame": frame_line} if frame_line else {}),
         "attn": {"us_per_layer": attn_avg_s * 1e6, "gbs": achieved,
-                 "bytes_per_layer": sizes["attn_per_layer"]},
+                 "bytes_per_layer": sizes["attn_per_layer"],
+                 "timing": "graph of every layer's attention calls, %d replays" % args.steps},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": attn_traffic(cfg.name),
                      "kernel": "pkv_paged_decode_attn (planner, persistent split kernel, merge "

@@ -9,13 +9,17 @@
 //  * work units: a row's blocks are cut into fixed 32-block (512-token)
 //    splits; a unit is one (row, split, kv head, q-head block).  The split size does
 //    not depend on the batch, so a row's result depends on its inputs only.
-//  * a one-CTA planner lists the splits of the active rows (prefix sums over
-//    the rows) and resets the scheduling counter, so the launch shapes stay
-//    static.  It reads only lengths and flags, which no kernel of this
-//    library writes, so it does its work while its predecessor (the KV
-//    append) still runs and waits for that predecessor only at its end.
-//  * a persistent grid (SMs x resident CTAs) pulls units from an atomic
-//    counter.  Each of a CTA's 4 warps streams its blocks of the unit
+//  * a one-CTA planner lists the splits of the active rows and resets the
+//    scheduling counter, so the launch shapes stay static.  Units are handed
+//    out largest first: every full 32-block split (prefix sums over the
+//    rows), then each row's shorter last split in descending size (a
+//    counting sort).  The order only decides which CTA takes a unit, never
+//    how a row's result is formed.  The planner reads only lengths and
+//    flags, which no kernel of this library writes, so it does its work
+//    while its predecessor (the KV append) still runs and waits for that
+//    predecessor only at its end.
+//  * a persistent grid (SMs x resident CTAs): CTA i starts on unit i and
+//    pulls the rest from an atomic counter.  Each of a CTA's 4 warps streams its blocks of the unit
 //    (round-robin) through its own ring of NS shared-memory stages; a stage
 //    is one block of one kv head -- 16 K rows + 16 V rows, each head_dim bf16
 //    contiguous in HBM -- brought in by one tiled tensor TMA
@@ -63,7 +67,7 @@ struct PlanHeader {
   int32_t counter;      // next unit to hand out
   int32_t total_units;
   int32_t total_splits;
-  int32_t pad_;
+  int32_t full_splits;  // splits of 32 whole blocks; they come first
 };
 
 struct AttnArgs {
@@ -94,7 +98,9 @@ struct AttnArgs {
   float *lse;
   float *ws_o;                 // [B][Hq][nsplit_max][D]
   float2 *ws_ml;               // [B][Hq][nsplit_max]
-  int32_t *row_start;          // [B + 1] first split of each row
+  int32_t *row_start;          // [B + 1] first full split of each row, then
+                               // [B] rows of the short last splits, longest first
+  int32_t *part_rows;          // row_start + B + 1
   PlanHeader *plan;
   int nsplit_max;
   int32_t *err;
@@ -107,7 +113,8 @@ __device__ __forceinline__ void store_out(const AttnArgs &a, int64_t idx, float 
     static_cast<uint16_t *>(a.out)[idx] = (uint16_t)f32_to_bf16_bits(v);
 }
 
-__device__ __forceinline__ int row_splits(const AttnArgs &a, int b, bool *bad) {
+// 16-token blocks of row b (0 for padding and rejected rows)
+__device__ __forceinline__ int row_blocks(const AttnArgs &a, int b, bool *bad) {
   *bad = false;
   if (!a.active[b]) return 0;
   const int n = a.seq_lens[b];
@@ -115,33 +122,37 @@ __device__ __forceinline__ int row_splits(const AttnArgs &a, int b, bool *bad) {
     *bad = true;
     return 0;
   }
-  const int npages = (n + ATTN_PAGE - 1) / ATTN_PAGE;
-  return (npages + ATTN_PAGES_PER_SPLIT - 1) / ATTN_PAGES_PER_SPLIT;
+  return (n + ATTN_PAGE - 1) / ATTN_PAGE;
 }
 
 // ---------------------------------------------------------------------------
 // planner: one CTA
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(PLAN_THREADS) attn_plan_kernel(const AttnArgs a) {
+  constexpr int SPL = ATTN_PAGES_PER_SPLIT;
   __shared__ int32_t scan[PLAN_THREADS];
   __shared__ int32_t carry;
+  __shared__ int32_t bin[SPL];  // short last splits per size, then the next slot of each size
   // the persistent kernel may launch and set up now; it waits for this grid
   // to complete before it reads the table
   pdl_trigger();
   const int tid = threadIdx.x;
   const int HB = a.num_kv_heads * a.qblocks;
   if (tid == 0) carry = 0;
+  if (tid < SPL) bin[tid] = 0;
   __syncthreads();
   for (int base = 0; base < a.batch; base += PLAN_THREADS) {
     const int b = base + tid;
-    int ns = 0;
+    int nf = 0;
     if (b < a.batch) {
       bool bad;
-      ns = row_splits(a, b, &bad);
+      const int nb = row_blocks(a, b, &bad);
       if (bad) report(a.err, PKV_DEV_ERR_SEQ_LEN);
+      nf = nb / SPL;
+      if (nb % SPL) atomicAdd(&bin[nb % SPL], 1);
     }
-    // inclusive scan of ns over the block (Hillis-Steele)
-    scan[tid] = ns;
+    // inclusive scan of the full splits over the block (Hillis-Steele)
+    scan[tid] = nf;
     __syncthreads();
     for (int off = 1; off < PLAN_THREADS; off <<= 1) {
       const int v = tid >= off ? scan[tid - off] : 0;
@@ -149,16 +160,33 @@ __global__ void __launch_bounds__(PLAN_THREADS) attn_plan_kernel(const AttnArgs 
       scan[tid] += v;
       __syncthreads();
     }
-    if (b < a.batch) a.row_start[b] = carry + scan[tid] - ns;
+    if (b < a.batch) a.row_start[b] = carry + scan[tid] - nf;
     __syncthreads();
     if (tid == PLAN_THREADS - 1) carry += scan[tid];
     __syncthreads();
   }
+  // first slot of each size, longest first: bin[r] = rows with a longer
+  // short split
   if (tid == 0) {
+    int acc = 0;
+    for (int r = SPL - 1; r >= 1; --r) {
+      const int c = bin[r];
+      bin[r] = acc;
+      acc += c;
+    }
     a.row_start[a.batch] = carry;
     a.plan->counter = 0;
-    a.plan->total_splits = carry;
-    a.plan->total_units = carry * HB;
+    a.plan->full_splits = carry;
+    a.plan->total_splits = carry + acc;
+    a.plan->total_units = (carry + acc) * HB;
+  }
+  __syncthreads();
+  // the rows of the short splits in their slots (the order within a size
+  // does not matter: each unit writes its own partial)
+  for (int b = tid; b < a.batch; b += PLAN_THREADS) {
+    bool bad;
+    const int r = row_blocks(a, b, &bad) % SPL;
+    if (r) a.part_rows[atomicAdd(&bin[r], 1)] = b;
   }
   // completes only after the predecessor has: the persistent kernel, which
   // waits for this grid, then sees the predecessor's cache writes too
@@ -196,33 +224,46 @@ struct Unit {
 };
 
 constexpr int ATTN_SMEM_ROWS = 512;  // rows whose split table lives in shared memory
+// static shared memory of the persistent kernel (unit ring + split table)
+constexpr int ATTN_STATIC_SMEM = 4 * (4 + 1 + (2 * ATTN_SMEM_ROWS + 1) + ATTN_SMEM_ROWS) + 128;
+constexpr int SM_SMEM_BYTES = 228 * 1024;  // shared memory of one SM (1 KB reserved per CTA)
 
-// rs: first split of each row [B + 1]; seq: lengths [B] (shared or global)
+// rs: first full split of each row [B + 1], followed by the rows of the
+// short splits; seq: lengths [B] (each in shared or global memory).  Units
+// [0, full * HB) are full splits, the rest the short last splits in the
+// planner's order.
 __device__ __forceinline__ Unit decode_unit(const AttnArgs &a, int u, int gp, int total_units,
-                                            const int32_t *rs, const int32_t *seq) {
+                                            int full, const int32_t *rs, const int32_t *seq) {
   Unit U;
   const int HB = a.num_kv_heads * a.qblocks;
   U.valid = u < total_units;
   U.b = U.split = U.g = U.h0 = U.nh = U.n = U.p_begin = U.p_count = 0;
   if (!U.valid) return U;
   const int su = u / HB, hb = u % HB;
-  // row of split `su`: the last b with rs[b] <= su
-  int lo = 0, hi = a.batch - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (rs[mid] <= su)
-      lo = mid;
-    else
-      hi = mid - 1;
+  if (su < full) {
+    // row of full split `su`: the last b with rs[b] <= su (a row without
+    // full splits shares its rs with the next row, so it is never chosen)
+    int lo = 0, hi = a.batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (rs[mid] <= su)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    U.b = lo;
+    U.split = su - rs[lo];
+  } else {
+    U.b = rs[a.batch + 1 + su - full];
+    U.split = -1;  // the row's last split, set below
   }
-  U.b = lo;
-  U.split = su - rs[lo];
   U.g = hb / a.qblocks;
   const int qb = hb % a.qblocks;
   U.h0 = U.g * a.group + qb * gp;
   U.nh = min(gp, a.group - qb * gp);
   U.n = seq[U.b];
   const int npages = (U.n + ATTN_PAGE - 1) / ATTN_PAGE;
+  if (U.split < 0) U.split = npages / ATTN_PAGES_PER_SPLIT;
   U.p_begin = U.split * ATTN_PAGES_PER_SPLIT;
   U.p_count = min(npages - U.p_begin, ATTN_PAGES_PER_SPLIT);
   return U;
@@ -243,6 +284,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
     attn_persistent_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap) {
   using S = AttnShape<D, GP, NS>;
   constexpr int T = S::T, NCH = S::NCH, NP = S::NP, NB = S::NB;
+  static_assert(2 * (S::SMEM_BYTES + ATTN_STATIC_SMEM + 1024) <= SM_SMEM_BYTES,
+                "two CTAs per SM");
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // stage buffers start on a 128-byte boundary
@@ -258,7 +301,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   uint64_t *bars = reinterpret_cast<uint64_t *>(p);
   uint64_t *qbars = bars + ATTN_WARPS * NS;  // [2]
   __shared__ int32_t s_unit[4];  // unit ids, circular: ordinal k at [k & 3]
-  __shared__ int32_t s_rs[ATTN_SMEM_ROWS + 1];
+  __shared__ int32_t s_rs[2 * ATTN_SMEM_ROWS + 1];
   __shared__ int32_t s_seq[ATTN_SMEM_ROWS];
 
   const int tid = threadIdx.x;
@@ -283,17 +326,23 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   }
   pdl_wait();     // the planner's table and counter
   pdl_trigger();  // the merge kernel may queue behind this grid now
+  // every CTA starts on unit blockIdx.x; later units come from the counter
+  // (offset by the grid), so a batch with fewer units than CTAs gives each
+  // CTA at most one instead of two to the first half of the grid
   if (tid == 0) {
-    s_unit[0] = atomicAdd(&a.plan->counter, 1);
-    s_unit[1] = atomicAdd(&a.plan->counter, 1);
+    s_unit[0] = (int)blockIdx.x;
+    s_unit[1] = (int)gridDim.x + atomicAdd(&a.plan->counter, 1);
   }
   // the split table of the batch, in shared memory when it fits
   const bool small_batch = a.batch <= ATTN_SMEM_ROWS;
+  __shared__ int32_t s_full;  // full splits (read once per unit, not held in registers)
+  const int total_units = a.plan->total_units;
+  const int nshort = a.plan->total_splits - a.plan->full_splits;
+  if (tid == 0) s_full = a.plan->full_splits;
   if (small_batch) {
-    for (int b = tid; b <= a.batch; b += ATTN_THREADS) s_rs[b] = a.row_start[b];
+    for (int i = tid; i <= a.batch + nshort; i += ATTN_THREADS) s_rs[i] = a.row_start[i];
     for (int b = tid; b < a.batch; b += ATTN_THREADS) s_seq[b] = a.seq_lens[b];
   }
-  const int total_units = a.plan->total_units;
   __syncthreads();
   const int32_t *rs = small_batch ? s_rs : a.row_start;
   const int32_t *seq = small_batch ? s_seq : a.seq_lens;
@@ -301,8 +350,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   const int layer_page0 = a.layer * a.num_pages;
 
   int ordinal = 0;
-  Unit cur = decode_unit(a, s_unit[0], GP, total_units, rs, seq);
-  Unit nxt = decode_unit(a, s_unit[1], GP, total_units, rs, seq);
+  Unit cur = decode_unit(a, s_unit[0], GP, total_units, s_full, rs, seq);
+  Unit nxt = decode_unit(a, s_unit[1], GP, total_units, s_full, rs, seq);
   int cur_cnt = warp_pages(cur, warp);
   int nxt_cnt = warp_pages(nxt, warp);
   int next_id = 0;  // id of the unit after next, fetched a unit ahead (thread 0)
@@ -386,7 +435,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   float m_own, l_own;
 
   while (cur.valid) {
-    if (tid == 0) next_id = atomicAdd(&a.plan->counter, 1);  // used at the epilogue
+    if (tid == 0) next_id = (int)gridDim.x + atomicAdd(&a.plan->counter, 1);  // used at the epilogue
     top_up();
     // q of the lane's dims for every head of the block, pre-scaled to log2 units
     const int qb_idx = ordinal & 1;
@@ -618,7 +667,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
     cur = nxt;
     cur_cnt = nxt_cnt;
     pid_cur = pid_nxt;
-    nxt = decode_unit(a, s_unit[(ordinal + 1) & 3], GP, total_units, rs, seq);
+    nxt = decode_unit(a, s_unit[(ordinal + 1) & 3], GP, total_units, s_full, rs, seq);
     nxt_cnt = warp_pages(nxt, warp);
     pid_nxt = load_pids(nxt, nxt_cnt);
     stage_q(nxt, (ordinal + 1) & 1);
@@ -830,7 +879,7 @@ static WsLayout ws_layout(int batch, int num_qo_heads, int head_dim, int64_t max
   w.o = 0;
   w.ml = align_up(units * head_dim * sizeof(float), 256);
   w.row_start = w.ml + align_up(units * sizeof(float2), 256);
-  w.plan = w.row_start + align_up((size_t)(batch + 1) * sizeof(int32_t), 256);
+  w.plan = w.row_start + align_up((size_t)(2 * batch + 1) * sizeof(int32_t), 256);
   w.total = w.plan + 256;
   return w;
 }
@@ -905,6 +954,7 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
   a.ws_o = reinterpret_cast<float *>(ws + wl.o);
   a.ws_ml = reinterpret_cast<float2 *>(ws + wl.ml);
   a.row_start = reinterpret_cast<int32_t *>(ws + wl.row_start);
+  a.part_rows = a.row_start + batch + 1;
   a.plan = reinterpret_cast<PlanHeader *>(ws + wl.plan);
   a.err = err_word;
   a.layer = layer;

@@ -188,6 +188,25 @@ class DecodeStep:
         """One step through the captured graph (on the current stream)."""
         self.graph.replay()
 
+    def capture_attention(self):
+        """Capture the attention calls of every layer alone (planner,
+        persistent kernel and merge per layer, back to back) as a second
+        graph, to time the attention kernels without host launch gaps.
+        Needs a run() (or capture()) first."""
+        import torch
+        if not self._warm:
+            raise RuntimeError("run the step once before capture_attention()")
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for l in range(self.t.layers):
+                self.attend(l)
+        self.attn_graph = g
+
+    def replay_attention(self):
+        """Every layer's attention through the graph of capture_attention()."""
+        self.attn_graph.replay()
+
     def launches_per_step(self) -> int:
         """Kernel launches of one run(): per layer append 1 + attention 3
         (planner, persistent kernel, split merge); sampler 2; frame 1."""

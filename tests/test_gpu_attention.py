@@ -53,6 +53,11 @@ def _cases():
                             ctx=(1, 127, 128, 129, 513, 2100, 4000), shuffle_pages=True),
         "long_p128_small": W.small_variant(W.CONFIGS["long_context_p128"], n_active=3, n_pad=2,
                                            ctx_hi=2600, layers=2).replace(ctx_lo=1500),
+        # more rows than the kernel's shared-memory split table holds (512):
+        # the unit table is read from global memory
+        "wide_batch_600": W.Config(name="wide600", index=15, num_layers=1, num_qo_heads=4,
+                                   num_kv_heads=2, head_dim=64, page_size=16, n_active=600,
+                                   n_pad=24, ctx_lo=1, ctx_hi=1100, shuffle_pages=True),
     }
 
 

@@ -75,3 +75,23 @@ def test_graph_replay_equals_eager(cfg):
             _same(want, _outputs(step))
     assert not torch.equal(want["out"], eager["out"])
     assert int(want["err"].item()) == 0
+
+
+def test_attention_only_graph_equals_eager():
+    """The attention-only graph (the bench's attention timing) computes the
+    same outputs as the eager attention calls."""
+    cfg = W.small_variant(W.CONFIGS["qwen2_0p5b"], n_active=9, ctx_hi=1500, layers=3)
+    batch = W.make_batch(cfg)
+    dev = W.Tensors(batch, device="cuda")
+    step = DecodeStep(batch, dev)
+    step.run()
+    torch.cuda.synchronize()
+    want_out, want_lse = step.out.clone(), step.lse.clone()
+    step.capture_attention()
+    step.out.zero_()
+    step.lse.zero_()
+    step.replay_attention()
+    torch.cuda.synchronize()
+    assert torch.equal(step.out, want_out)
+    assert torch.equal(step.lse, want_lse)
+    assert int(step.err.item()) == 0
