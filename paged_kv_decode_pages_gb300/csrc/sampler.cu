@@ -319,6 +319,7 @@ struct SampSmem {
   float wh[SB / 32], wl[SB / 32];
   uint32_t hist[256];
   uint64_t red_u64[SB / 32];
+  uint64_t red_u64b[SB / 32];
   double red_d[SB];
   int32_t red_i[SB];
   uint64_t sel_prefix;
@@ -503,9 +504,124 @@ __device__ __forceinline__ DF chunk_exp_sum(const uint32_t (&key)[EPT], int cnt,
   return block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
 }
 
-// pbits: the row's penalty bitmap in global memory, written for this chunk
-// when the row is penalised (may be null otherwise)
-__device__ void chunk_pass(const float *__restrict__ row, int V, int c, const RowParams &P,
+// The largest of a thread's N values get(j), as four independent partial
+// maxima (short dependency chains)
+template <int N, class Get>
+__device__ __forceinline__ uint64_t thread_max(Get get) {
+  uint64_t m[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const uint64_t x = get(j);
+    m[j & 3] = x > m[j & 3] ? x : m[j & 3];
+  }
+  const uint64_t a = m[0] > m[1] ? m[0] : m[1], b = m[2] > m[3] ? m[2] : m[3];
+  return a > b ? a : b;
+}
+
+// The n largest of the block's values without a radix select or a full
+// sort.  Each thread holds N values, get(j) for j < N; 0 means "no value" and
+// the other values are distinct.  Needs n <= SB and at least n nonzero
+// values.  A lower bound L with at least n values >= L comes from the
+// threads' largest values: each warp sorts its 32 (a bitonic network over
+// the lanes) and offers its q-th largest, q = ceil(n / 8); L is the
+// smallest offer, so every warp holds q values >= L (or L is 0 and every
+// nonzero value passes).  The nonzero values >= L -- typically a few dozen
+// more than n -- are gathered into gbuf (SB entries, shared memory) and
+// each one's rank among them is counted: ranks 0 .. n-1 are the n largest,
+// written to out[rank] (descending order), and rank n-1 also to *thr when
+// thr is not null.  top1 receives the largest value in any case.  Returns
+// false, having written nothing to out, when more than SB values pass the
+// bound.
+template <int N, class Get>
+__device__ bool block_top_n(Get get, int n, uint64_t *out, uint64_t *thr, uint64_t *gbuf,
+                            SampSmem &sm, uint64_t &top1) {
+  constexpr int NW = SB / 32;
+  static_assert(N <= 32, "N");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = (n + NW - 1) / NW;
+  uint64_t v = thread_max<N>(get);
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t o = __shfl_xor_sync(FULL_MASK, v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  const uint64_t offer = __shfl_sync(FULL_MASK, v, q - 1);
+  __syncthreads();  // earlier readers of red_u64, red_u64b, cnt and gbuf are done
+  if (lane == 0) {
+    sm.red_u64[warp] = offer;
+    sm.red_u64b[warp] = v;  // the warp's largest
+  }
+  if (tid == 0) sm.cnt = 0;
+  __syncthreads();
+  uint64_t L = sm.red_u64[0], top = sm.red_u64b[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) {
+    L = sm.red_u64[w] < L ? sm.red_u64[w] : L;
+    top = sm.red_u64b[w] > top ? sm.red_u64b[w] : top;
+  }
+  top1 = top;
+  // gather: a slot range per warp (one atomic), lanes in order inside it;
+  // bit j of pm marks the thread's value j (independent tests, no chain)
+  uint32_t pm = 0;
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const uint64_t x = get(j);
+    if (x != 0ull && x >= L) pm |= 1u << j;
+  }
+  const int cnt = __popc(pm);
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int t = __shfl_up_sync(FULL_MASK, incl, off);
+    if (lane >= off) incl += t;
+  }
+  int base = 0;
+  if (lane == 31) base = (int)atomicAdd(&sm.cnt, (uint32_t)incl);
+  base = __shfl_sync(FULL_MASK, base, 31);
+  const int pos = base + incl - cnt;
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+    if ((pm >> j) & 1u) {
+      const int at = pos + __popc(pm & ((1u << j) - 1u));
+      if (at < SB) gbuf[at] = get(j);
+    }
+  __syncthreads();
+  const int C = (int)sm.cnt;
+  if (C > SB) return false;  // the same answer in every thread
+  if (tid < C) {
+    const uint64_t me = gbuf[tid];
+    int r = 0;
+    for (int k = 0; k < C; ++k) r += gbuf[k] > me ? 1 : 0;
+    if (r < n) out[r] = me;
+    if (r == n - 1 && thr != nullptr) *thr = me;
+  }
+  __syncthreads();
+  return true;
+}
+
+// The thread's logits of chunk c (element tid + j * SB in raw[j]), every
+// load issued before any is used so that all of them are in flight at once.
+// The frame kernel writes the rows it samples: plain loads, no __ldg.
+__device__ __forceinline__ void load_chunk(const float *row, int V, int c, float (&raw)[EPT]) {
+  const int tid = threadIdx.x;
+  const int start = c * CHUNK;
+  const int cnt = min(CHUNK, V - start);
+  if (cnt == CHUNK) {
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) raw[j] = row[start + tid + j * SB];
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) raw[j] = tid + j * SB < cnt ? row[start + tid + j * SB] : 0.0f;
+  }
+}
+
+// raw: the thread's logits of chunk c (load_chunk).  pbits: the row's
+// penalty bitmap in global memory, written for this chunk when the row is
+// penalised (may be null otherwise)
+__device__ void chunk_pass(const float (&raw)[EPT], int V, int c, const RowParams &P,
                            ChunkRec *rec, uint32_t *pbits, SampSmem &sm, int32_t *err) {
   const int tid = threadIdx.x;
   const int start = c * CHUNK;
@@ -515,7 +631,7 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
 #pragma unroll
   for (int j = 0; j < EPT; ++j) {
     const int i = tid + j * SB;
-    key[j] = (i < cnt) ? order_key(row[start + i], bad) : 0u;  // may be written by this kernel: no __ldg
+    key[j] = (i < cnt) ? order_key(raw[j], bad) : 0u;
   }
   if (bad) report(err, PKV_DEV_ERR_LOGITS);
   if (P.lp_raw) {
@@ -555,16 +671,21 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
     if (pbits != nullptr)
       for (int w = tid; w < (cnt + 31) / 32; w += SB) pbits[c * (CHUNK / 32) + w] = sm.penbits[w];
   }
-  uint64_t mine = 0;
-#pragma unroll
-  for (int j = 0; j < EPT; ++j) {
+  auto comp_at = [&](int j) -> uint64_t {
     const int i = tid + j * SB;
-    if (i < cnt) {
-      const uint64_t cc = composite(key[j], start + i);
-      mine = cc > mine ? cc : mine;
-    }
+    return i < cnt ? composite(key[j], start + i) : 0ull;
+  };
+  // the chunk's nc largest composites (candidate modes), and its largest
+  const int nc = P.nc;
+  const bool sel = P.mode == MODE_TOPK_SMALL || P.mode == MODE_TOPP_FULL;
+  uint64_t top1 = 0;
+  bool fast = false;
+  if (sel && cnt > nc && nc <= SB) {
+    fast = block_top_n<EPT>(comp_at, nc, rec->cand, &rec->thr, sm.sortbuf, sm, top1);
+    if (fast && tid == 0) rec->ncand = nc;
+  } else {
+    top1 = block_max_u64(thread_max<EPT>(comp_at), sm);
   }
-  const uint64_t top1 = block_max_u64(mine, sm);
   if (tid == 0) rec->top1 = top1;
   if (P.mode == MODE_GREEDY || P.mode == MODE_GENERAL) return;
 
@@ -593,10 +714,9 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
     }
     if (bid == id && id >= 0) rec->gkey = bkey;
   } else {
-    // the chunk's nc largest composites
-    const int nc = P.nc;
+    // the chunk's nc largest composites, unless the fast selection wrote them
     uint64_t thr = 0;  // keep composites >= thr
-    if (cnt > nc) {
+    if (!fast && cnt > nc) {
       if (tid == 0) {
         sm.sel_prefix = 0;
         sm.sel_want = (uint32_t)nc;
@@ -625,25 +745,27 @@ __device__ void chunk_pass(const float *__restrict__ row, int V, int c, const Ro
       thr = sm.sel_prefix;
       __syncthreads();
     }
-    if (tid == 0) sm.cnt = 0;
-    __syncthreads();
+    if (!fast) {
+      if (tid == 0) sm.cnt = 0;
+      __syncthreads();
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int i = tid + j * SB;
-      if (i < cnt) {
-        const uint64_t cc = composite(key[j], start + i);
-        if (cc >= thr) {
-          const uint32_t pos = atomicAdd(&sm.cnt, 1u);
-          if (pos < (uint32_t)nc) rec->cand[pos] = cc;
+      for (int j = 0; j < EPT; ++j) {
+        const int i = tid + j * SB;
+        if (i < cnt) {
+          const uint64_t cc = composite(key[j], start + i);
+          if (cc >= thr) {
+            const uint32_t pos = atomicAdd(&sm.cnt, 1u);
+            if (pos < (uint32_t)nc) rec->cand[pos] = cc;
+          }
         }
       }
-    }
-    __syncthreads();
-    const int got = min((int)sm.cnt, nc);
-    for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0;
-    if (tid == 0) {
-      rec->ncand = got;
-      rec->thr = cnt > nc ? thr : 0ull;
+      __syncthreads();
+      const int got = min((int)sm.cnt, nc);
+      for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0;
+      if (tid == 0) {
+        rec->ncand = got;
+        rec->thr = cnt > nc ? thr : 0ull;
+      }
     }
   }
 
@@ -935,7 +1057,20 @@ __device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
   const int nv = min(full ? NCAND : P.K, nreal);
   __syncthreads();
   int nsort;
-  if (nu <= GEN_BLOCK) {
+  bool sorted = false;
+  if (nu <= GEN_BLOCK && nv <= SB) {
+    // the nv largest of the union, in order (the decision reads no further)
+    auto get = [&](int k) -> uint64_t {
+      const int i = tid + k * SB;
+      return i < nu ? cand_at(i) : 0ull;
+    };
+    uint64_t t1;
+    sorted = block_top_n<GEN_BLOCK / SB>(get, nv, sm.sortbuf, nullptr,
+                                         reinterpret_cast<uint64_t *>(sm.es), sm, t1);
+  }
+  if (sorted) {
+    nsort = nv;
+  } else if (nu <= GEN_BLOCK) {
     nsort = nu;
     for (int i = tid; i < nu; i += SB) sm.sortbuf[i] = cand_at(i);
   } else {
@@ -951,11 +1086,13 @@ __device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
     }
     nsort = nv;
   }
-  int n2 = 1;
-  while (n2 < nsort) n2 <<= 1;
-  for (int i = nsort + tid; i < n2; i += SB) sm.sortbuf[i] = 0ull;
-  __syncthreads();
-  block_sort_desc(sm.sortbuf, n2);
+  if (!sorted) {
+    int n2 = 1;
+    while (n2 < nsort) n2 <<= 1;
+    for (int i = nsort + tid; i < n2; i += SB) sm.sortbuf[i] = 0ull;
+    __syncthreads();
+    block_sort_desc(sm.sortbuf, n2);
+  }
   const double m = comp_x(sm.sortbuf[0], P.temperature);
   const bool topp = P.top_p < 1.0f;
   const bool minp = P.min_p > 0.0f;
@@ -1207,13 +1344,16 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   __shared__ SampSmem sm;
   const int b = blockIdx.y;
   const int c = blockIdx.x;
+  // the logits first (every row of the batch is readable), so that their
+  // loads overlap the row's flags and settings
+  float raw[EPT];
+  load_chunk(a.logits + (int64_t)b * a.row_stride, a.vocab, c, raw);
   if (!a.active[b]) return;
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) return;
   load_exp2_table(sm);  // read after the first barrier of the chunk pass
   const RowParams P = sample_row_params(a, slot);
-  chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, c, P, a.recs + (int64_t)b * a.nch + c,
-             row_pbits(a, b), sm, a.err);
+  chunk_pass(raw, a.vocab, c, P, a.recs + (int64_t)b * a.nch + c, row_pbits(a, b), sm, a.err);
 }
 
 __device__ __forceinline__ void sample_skip_row(const SampleArgs &a, int b) {
@@ -1338,7 +1478,9 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     const RowParams P = row_params(a.ctrl_vocab, a.seeds[slot], step, a.temperature[slot],
                                    a.top_k[slot], a.top_p[slot], 0u);
     for (int c = 0; c < a.ctrl_nch; ++c) {
-      chunk_pass(crow, a.ctrl_vocab, c, P, recs + c, nullptr, sm, a.err);
+      float raw[EPT];
+      load_chunk(crow, a.ctrl_vocab, c, raw);
+      chunk_pass(raw, a.ctrl_vocab, c, P, recs + c, nullptr, sm, a.err);
       __syncthreads();
     }
     const int tok = finish_row(RowView{crow, nullptr, 1.0f}, a.ctrl_vocab, a.ctrl_nch, P, recs, sm);
@@ -1372,7 +1514,9 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     const RowParams P = row_params(V, a.seeds[slot], step, a.temperature[slot], a.top_k[slot],
                                    a.top_p[slot], (uint32_t)(1 + j));
     for (int c = 0; c < a.nch; ++c) {
-      chunk_pass(row, V, c, P, recs + c, nullptr, sm, a.err);
+      float raw[EPT];
+      load_chunk(row, V, c, raw);
+      chunk_pass(raw, V, c, P, recs + c, nullptr, sm, a.err);
       __syncthreads();
     }
     const int tok = finish_row(RowView{row, nullptr, 1.0f}, V, a.nch, P, recs, sm);

@@ -95,6 +95,14 @@ CASES = [
     (3, 40000, 1.0, 1.0, 513, 1.0, "normal"),     # general path: top-k > 512
     (2, 151936, 4.0, 0.7, 0, 0.95, "normal"),     # long-context sampler
     (2, 151936, 1.0, 0.5, 0, 0.95, "conc"),       # one chunk holds the top-p set
+    # the chunk pass's candidate selection: the lower bound from the thread
+    # maxima passes more than 256 composites (radix select instead) ...
+    (3, 40000, 1.0, 1.0, 50, 0.9, "stripe"),
+    # ... one thread's elements are each chunk's 32 largest ...
+    (3, 40000, 1.0, 1.0, 50, 0.95, "thread"),
+    # ... a short last chunk (808 tokens) and a chunk with idle warps
+    (3, 9000, 1.0, 1.0, 100, 1.0, "normal"),
+    (3, 200, 1.0, 1.0, 20, 0.9, "normal"),
 ]
 
 
@@ -104,6 +112,10 @@ def test_emulated_sampler_matches_oracle(emu_binary, tmp_path, B, V, std, T, k, 
     x = rng.normal(0, std, (B, V)).astype(np.float32)
     if dist == "conc":
         x[:, :8192] += np.float32(6.0)
+    elif dist == "stripe":  # a chunk thread's elements (stride 256) share one level
+        x = (-(np.arange(V) % 256) * 0.05 + rng.normal(0, 1e-3, (B, V))).astype(np.float32)
+    elif dist == "thread":
+        x[:, np.arange(V) % 256 == 5] += np.float32(6.0)
     x[0, 3 % V] = -np.inf  # a masked token
     B1 = B + 1  # plus one padding row
     x = np.concatenate([x, np.zeros((1, V), np.float32)])
