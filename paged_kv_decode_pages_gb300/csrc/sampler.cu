@@ -19,10 +19,15 @@
 //    (-0 folded onto +0); composite = key << 32 | ~token, so a larger
 //    composite comes first in (value desc, id asc) order, and composites
 //    are unique.
-//  * chunk pass (one CTA per 8192-token chunk of a row): chunk maximum;
-//    the chunk's nc largest composites by a radix select over 8-bit digits,
-//    nc = min(kcap, max(64, ceil(kcap / chunks))) with kcap = the top-k, or
-//    512 for top-p over the whole vocabulary, and the smallest of them;
+//  * chunk pass (one CTA per 8192-token chunk of a row; its logits are
+//    loaded before the row's settings): chunk maximum; the chunk's nc
+//    largest composites, nc = min(kcap, max(64, ceil(kcap / chunks))) with
+//    kcap = the top-k, or 512 for top-p over the whole vocabulary, and the
+//    smallest of them.  For nc <= 256 they come from a lower bound taken
+//    from the warps' sorted thread maxima and exact rank counting over the
+//    few composites above it (block_top_n), in descending order; otherwise,
+//    or when more than 256 composites pass the bound, from a radix select
+//    over 8-bit digits;
 //    for top-p over the whole vocabulary, the partial normaliser
 //    sum exp(x - x_chunkmax) = sum 2^(logit * log2(e) / T - t_chunkmax) in
 //    double-float arithmetic (fp32 pairs): Tang's table-driven exp2 (ACM
@@ -32,8 +37,9 @@
 //    much issue time as several dozen fp32 ones, and this is the only
 //    per-logit transcendental of the path; for "keep everything", the
 //    chunk's Gumbel argmax.  The chunking depends on the vocabulary only.
-//  * finish (one CTA per row): the kcap largest of the chunks' candidates
-//    (radix select over the union), sorted; top-k / top-p with fp64 prefix
+//  * finish (one CTA per row): the kcap largest of the chunks' candidates,
+//    in order (block_top_n over the union when kcap <= 256, else a radix
+//    select over the union and a bitonic sort); top-k / top-p with fp64 prefix
 //    sums in sorted order (a warp prefix scan, exponentials computed in
 //    blocks only as far as the scan reaches); the Gumbel argmax.  The
 //    sorted candidates are the exact global order over the prefix the
