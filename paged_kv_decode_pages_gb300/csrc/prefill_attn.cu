@@ -9,22 +9,27 @@
 //
 // This is a dense contraction, so it runs on the 5th-generation tensor
 // cores:
-//  * a tile is 128 MMA rows: tq = 128 / G tokens x the G q heads of one kv
-//    head (GQA packing: every K / V tile read serves the whole group);
-//  * one CTA per (request, q tile, kv head); a one-CTA planner lists the
-//    tiles (prefix sums), heaviest tile of each request first;
-//  * warp 4 is the producer and MMA issuer: tiled tensor TMA brings Q (once)
-//    and 128-key K and V tiles (16-token blocks of the pages, 128-byte
-//    swizzle, two stages each) into shared memory; tcgen05.mma computes
-//    S = Q K^T into tensor memory and O += P V into tensor memory
-//    (bf16 operands, fp32 accumulation; P is the A operand straight from
-//    tensor memory, so P.V reads only V from shared memory), each
-//    completion signalled by tcgen05.commit on an mbarrier;
-//  * warps 0-3 own one row each: they read the row of S from tensor memory,
-//    apply the causal mask, run the online softmax in log2 units with a
-//    lazy maximum (O is rescaled in tensor memory only when the running
-//    maximum grows by more than 8), write P as bf16 pairs into tensor memory
-//    (tcgen05.st), and at the end read O, divide by the row sum and store
+//  * a q tile is 128 MMA rows: tq = 128 / G tokens x the G q heads of one
+//    kv head (GQA packing: every K / V tile read serves the whole group);
+//  * one CTA per (request, pair of consecutive q tiles, kv head): the two
+//    tiles share every K / V tile, and while one tile's softmax runs on the
+//    CUDA cores the tensor cores work on the other's products; a one-CTA
+//    planner lists the pairs (prefix sums), requests with the longest
+//    context first and the heaviest pair of each request first;
+//  * a K load warp (both tiles' Q once, then the K tiles) and a V load warp
+//    bring 128-key tiles (16-token blocks of the pages, or 128-row boxes on
+//    128-token pages; 128-byte swizzle) into shared memory by tiled tensor
+//    TMA; an MMA warp issues, per KV tile, S = Q K^T of both tiles into
+//    tensor memory and then O += P V of both (bf16 operands, fp32
+//    accumulation in tensor memory), each completion signalled by
+//    tcgen05.commit on an mbarrier.  Tensor memory holds S and O of both
+//    tiles (all 512 columns), so P goes through shared memory;
+//  * two softmax warpgroups, one per tile, own one row per thread: they
+//    read the row of S from tensor memory, apply the causal mask, run the
+//    online softmax in log2 units with a lazy maximum (O is rescaled in
+//    tensor memory only when the running maximum grows by more than 8),
+//    write P as bf16 into shared memory in the swizzled K-major layout of
+//    the A operand, and at the end read O, divide by the row sum and store
 //    it;
 //  * stale cache slots past a request's last position are zeroed in shared
 //    memory before they meet P (whose entries there are 0), so whatever an
@@ -45,14 +50,15 @@ namespace pkv {
 constexpr int PF_M = 128;          // MMA rows of a tile
 constexpr int PF_N = 128;          // keys of a KV tile
 constexpr int PF_BLK = 16;         // tokens of one cache block (one TMA box)
-constexpr int PF_THREADS = 224;    // 4 softmax warps, K load warp, MMA warp, V load warp
+constexpr int PF_SM_WARPS = 8;     // two softmax warpgroups, one per q tile of the unit
+constexpr int PF_THREADS = 352;    // + K load warp, MMA warp, V load warp
 constexpr int PF_CHUNK = 16384;    // 128 rows x 128 bytes (64 bf16): one swizzle column
-constexpr int PF_TMEM_COLS = 512;  // S (128 columns), O (up to 128), P (64: bf16 pairs)
+constexpr int PF_TMEM_COLS = 512;  // S of both tiles (128 columns each), O of both (128 each)
 constexpr int PF_PLAN_THREADS = 1024;
 constexpr float PF_TAU = 8.0f;     // lazy-rescale threshold (log2 units)
 
 struct PfHeader {
-  int32_t total_tiles;
+  int32_t total_pairs;
   int32_t total_units;
   int32_t pad_[2];
 };
@@ -76,7 +82,7 @@ struct PfArgs {
   int batch;
   uint16_t *out;  // bf16 [T][Hq][D]
   float *lse;     // [T][Hq] or null
-  int32_t *tile_start;  // [B + 1] first tile of each position of the schedule
+  int32_t *tile_start;  // [B + 1] first unit (pair of q tiles) of each position of the schedule
   int32_t *order;       // [B] request at each position (longest context first)
   PfHeader *hdr;
   int32_t *err;
@@ -194,11 +200,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------------------
-// planner: one CTA lists the q tiles of every request (prefix sums)
+// planner: one CTA lists the units (pairs of q tiles) of every request
+// (prefix sums)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int request_tiles(const PfArgs &a, int b) {
+// units of a request: pairs of its q tiles (the last unit of an odd count
+// holds one tile)
+__device__ __forceinline__ int request_units(const PfArgs &a, int b) {
   const int q = a.qo_indptr[b + 1] - a.qo_indptr[b];
-  return q > 0 ? (q + a.tq - 1) / a.tq : 0;
+  return q > 0 ? ((q + a.tq - 1) / a.tq + 1) / 2 : 0;
 }
 
 // schedule key of a request: its context length (the KV its heaviest tile
@@ -235,7 +244,7 @@ __global__ void __launch_bounds__(PF_PLAN_THREADS) prefill_plan_kernel(const PfA
     int nt = 0;
     if (i < a.batch) {
       const int b = a.order[i];
-      if (a.qo_indptr[b + 1] >= a.qo_indptr[b]) nt = request_tiles(a, b);
+      if (a.qo_indptr[b + 1] >= a.qo_indptr[b]) nt = request_units(a, b);
     }
     scan[tid] = nt;
     __syncthreads();
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(PF_PLAN_THREADS) prefill_plan_kernel(const PfA
   }
   if (tid == 0) {
     a.tile_start[a.batch] = carry;
-    a.hdr->total_tiles = carry;
+    a.hdr->total_pairs = carry;
     a.hdr->total_units = carry * a.num_kv_heads;
     if (a.qo_indptr[a.batch] > a.T) report(a.err, PKV_DEV_ERR_INDPTR);
   }
@@ -265,17 +274,30 @@ __global__ void __launch_bounds__(PF_PLAN_THREADS) prefill_plan_kernel(const PfA
 template <int D>
 struct PfShape {
   static constexpr int NCH = D / 64;                  // 64-dim swizzle columns
-  static constexpr int Q_BYTES = NCH * PF_CHUNK;
-  static constexpr int KV_BYTES = NCH * PF_CHUNK;     // one K or V stage
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
-  static constexpr int NBAR = 14;
+  static constexpr int TILE_BYTES = NCH * PF_CHUNK;   // a Q tile, or one K / V stage
+  static constexpr int P_BYTES = 2 * PF_CHUNK;        // P: 128 rows x 128 keys
+  static constexpr int NK = 2;                        // K stages
+  static constexpr int NV = D == 64 ? 2 : 1;          // V stages (head_dim 128: the space
+                                                      // is taken by the two tiles' Q and P)
+  static constexpr int OFF_Q = 0;                     // [2 tiles]
+  static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
+  static constexpr int OFF_P = OFF_V + NV * TILE_BYTES;  // [2 tiles]
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int NBAR = 18;
   // + alignment slack; at least 120 KB, so that one CTA (which holds all
   // 512 tensor-memory columns) is resident per SM
-  static constexpr int SMEM_BYTES =
-      OFF_BAR + NBAR * 8 + 16 + 1024 > 120 * 1024 ? OFF_BAR + NBAR * 8 + 16 + 1024 : 120 * 1024;
+  static constexpr int RAW = OFF_BAR + NBAR * 8 + 16 + 1024;
+  static constexpr int SMEM_BYTES = RAW > 120 * 1024 ? RAW : 120 * 1024;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+// One tile of a unit: its tokens, their positions and the KV tiles they read.
+struct PfTile {
+  int t0;    // first packed row
+  int ntok;  // tokens (0: no tile)
+  int pos0;  // position of the first token
+  int nkv;   // 128-key tiles read (0: no tile)
 };
 
 template <int D>
@@ -284,24 +306,25 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         const __grid_constant__ CUtensorMap kv_map128,
                         const __grid_constant__ CUtensorMap q_map) {
   using S = PfShape<D>;
-  constexpr int NCH = S::NCH;
+  constexpr int NCH = S::NCH, NV = S::NV;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char *qs = sm + S::OFF_Q;
-  unsigned char *ks = sm + S::OFF_K;  // [2][NCH][128 rows][128 B]
-  unsigned char *vs = sm + S::OFF_V;
+  unsigned char *qs = sm + S::OFF_Q;  // [2 tiles][NCH][128 rows][128 B]
+  unsigned char *ks = sm + S::OFF_K;  // [NK][NCH][128 rows][128 B]
+  unsigned char *vs = sm + S::OFF_V;  // [NV][NCH][128 rows][128 B]
+  unsigned char *ps = sm + S::OFF_P;  // [2 tiles][2 key columns][128 rows][128 B]
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::OFF_BAR);
-  uint64_t *bar_q = bars + 0;
-  uint64_t *bar_k = bars + 1;  // [2]
-  uint64_t *bar_v = bars + 3;  // [2]
-  uint64_t *bar_s = bars + 5;
-  uint64_t *bar_o = bars + 6;
-  uint64_t *bar_p = bars + 7;
-  uint64_t *bar_fin = bars + 8;
-  uint64_t *bar_sfree = bars + 9;   // S read out of tensor memory by all 128 rows
-  uint64_t *bar_kfree = bars + 10;  // [2] S of the K stage's tile has completed
-  uint64_t *bar_vfree = bars + 12;  // [2] P.V of the V stage's tile has completed
+  uint64_t *bar_q = bars + 0;       // both tiles' Q
+  uint64_t *bar_k = bars + 1;       // [2] K stage loaded
+  uint64_t *bar_v = bars + 3;       // [2] V stage loaded
+  uint64_t *bar_s = bars + 5;       // [tile] S computed
+  uint64_t *bar_sfree = bars + 7;   // [tile] S read out of tensor memory by all 128 rows
+  uint64_t *bar_p = bars + 9;       // [tile] P written, O rescaled (128 rows)
+  uint64_t *bar_o = bars + 11;      // [tile] P.V computed
+  uint64_t *bar_kfree = bars + 13;  // [2] the S products of the K stage's tile have completed
+  uint64_t *bar_vfree = bars + 15;  // [2] the P.V products of the V stage's tile have completed
+  uint64_t *bar_fin = bars + 17;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::NBAR);
 
   const int tid = threadIdx.x;
@@ -316,7 +339,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int u = blockIdx.x;
   if (u >= a.hdr->total_units) return;
   const int su = u / Hkv, g = u % Hkv;
-  // schedule position of tile su: the last i with tile_start[i] <= su
+  // schedule position of unit su: the last i with tile_start[i] <= su
   int lo = 0, hi = a.batch - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -327,34 +350,48 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   }
   const int b = a.order[lo];
   const int q = a.qo_indptr[b + 1] - a.qo_indptr[b];
-  const int ntiles_b = a.tile_start[lo + 1] - a.tile_start[lo];
-  const int ti = ntiles_b - 1 - (su - a.tile_start[lo]);  // heaviest tile first
+  const int nt = (q + a.tq - 1) / a.tq;  // q tiles of the request
+  const int pi = su - a.tile_start[lo];  // pair index, heaviest first
   const int n = a.seq_lens[b];
-  const int t0 = a.qo_indptr[b] + ti * a.tq;
-  const int ntok = min(a.tq, q - ti * a.tq);
-  const int pos0 = n - q + ti * a.tq;  // position of the tile's first token
   const bool ok = a.active[b] && q <= n && n >= 1 && (int64_t)n <= a.max_tokens;
+  // tile A: the later (longer) q tile of the pair; tile B the one before it
+  PfTile tl[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int ti = nt - 1 - 2 * pi - x;
+    if (ti < 0) {
+      tl[x] = PfTile{0, 0, 0, 0};
+      continue;
+    }
+    tl[x].t0 = a.qo_indptr[b] + ti * a.tq;
+    tl[x].ntok = min(a.tq, q - ti * a.tq);
+    tl[x].pos0 = n - q + ti * a.tq;
+    tl[x].nkv = ok ? (tl[x].pos0 + tl[x].ntok - 1) / PF_N + 1 : 0;
+  }
 
   if (!ok) {
     // padding or malformed request: zeros, lse = -inf
-    if (a.active[b] && ti == ntiles_b - 1 && g == 0 && tid == 0) report(a.err, PKV_DEV_ERR_SEQ_LEN);
-    const int rows = ntok * G;
-    for (int r = warp; r < rows; r += PF_THREADS / 32) {
-      const int t = t0 + r / G, h = g * G + r % G;
-      if (t >= a.T) break;
-      uint16_t *o = a.out + ((int64_t)t * Hq + h) * D;
-      for (int d = lane * 2; d < D; d += 64) *reinterpret_cast<uint32_t *>(o + d) = 0u;
-      if (a.lse != nullptr && lane == 0) a.lse[(int64_t)t * Hq + h] = -INFINITY;
+    if (a.active[b] && pi == 0 && g == 0 && tid == 0) report(a.err, PKV_DEV_ERR_SEQ_LEN);
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int rows = tl[x].ntok * G;
+      for (int r = warp; r < rows; r += PF_THREADS / 32) {
+        const int t = tl[x].t0 + r / G, h = g * G + r % G;
+        if (t >= a.T) break;
+        uint16_t *o = a.out + ((int64_t)t * Hq + h) * D;
+        for (int d = lane * 2; d < D; d += 64) *reinterpret_cast<uint32_t *>(o + d) = 0u;
+        if (a.lse != nullptr && lane == 0) a.lse[(int64_t)t * Hq + h] = -INFINITY;
+      }
     }
     return;
   }
-  const int p_max = pos0 + ntok - 1;
-  const int nkv = p_max / PF_N + 1;        // KV tiles
+  const int nkv = tl[0].nkv;               // KV tiles read by the unit (tile A reads the most)
   const int last_blk = (n - 1) / PF_BLK;   // block of the request's last position
   const int kt_stale = (n - 1) / PF_N;     // the KV tile that holds slots past n - 1
 
   if (tid == 0) {
-    for (int i = 0; i < S::NBAR; ++i) mbar_init(&bars[i], (i == 7 || i == 9) ? 128u : 1u);
+    for (int i = 0; i < S::NBAR; ++i)
+      mbar_init(&bars[i], (i >= 7 && i <= 10) ? 128u : 1u);  // sfree, p: one arrival per row
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -367,10 +404,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_s = tmem;        // S: columns [0, 128)
-  const uint32_t tm_o = tmem + 128;  // O: columns [128, 128 + D)
-  const uint32_t tm_p = tmem + 256;  // P: columns [256, 320), keys 2c, 2c + 1 in column c
+  const uint32_t tmem = *tmem_slot;  // S of tile x: columns [128x, 128x + 128); O: 256 + 128x
 
   bool alive = true;
   auto wait = [&](uint64_t *bar, uint32_t parity) {  // warp-uniform give-up
@@ -380,13 +414,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
     }
   };
-  if (warp == 4 || warp == 6) {
+  if (warp == PF_SM_WARPS || warp == PF_SM_WARPS + 2) {
     // ---------------------------------------------------------- load warps
-    // warp 4 brings Q and the K tiles, warp 6 the V tiles (on small pages a
-    // tile is 8 boxes per 64-dim column, and two warps issue them in parallel)
-    // K and V of tile kt into stage kt & 1 as soon as the MMAs of tile
-    // kt - 2 have released it; the next tile's page ids are looked up
-    // (lanes 0-7, one block each) while the warp waits
+    // the first brings both tiles' Q and the K tiles, the second the V
+    // tiles (on small pages a KV tile is 8 boxes per 64-dim column, and two
+    // warps issue them in parallel).  A stage is refilled as soon as the
+    // MMAs that read it have completed; the next tile's page ids are looked
+    // up (lanes 0-7, one block each) while the warp waits.
     const uint64_t policy = l2_evict_last_policy();  // every q tile re-reads the tiles
     const int page0 = a.layer * a.num_pages;
     auto page_of = [&](int kt) -> int {  // raw page id of block lane of tile kt
@@ -427,26 +461,33 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                       sub * PF_BLK, kv, page0 + pg, bar, policy);
       }
     };
-    const int kv = warp == 4 ? 0 : 1;
+    const int kv = warp == PF_SM_WARPS ? 0 : 1;
+    const int nst = kv == 0 ? S::NK : NV;
     uint64_t *full = kv == 0 ? bar_k : bar_v;
     uint64_t *freed = kv == 0 ? bar_kfree : bar_vfree;
     unsigned char *buf = kv == 0 ? ks : vs;
     int raw = page_of(0);
     if (kv == 0 && lane == 0) {
-      mbar_arrive_expect_tx(bar_q, (uint32_t)(NCH * a.tq * G * 128));
-      for (int ch = 0; ch < NCH; ++ch)
-        tma_load_3d(qs + ch * PF_CHUNK, &q_map, ch * 64, g * G, t0, bar_q);
+      const int ntiles = tl[1].ntok > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(bar_q, (uint32_t)(ntiles * NCH * a.tq * G * 128));
+      for (int x = 0; x < ntiles; ++x)
+        for (int ch = 0; ch < NCH; ++ch)
+          tma_load_3d(qs + x * S::TILE_BYTES + ch * PF_CHUNK, &q_map, ch * 64, g * G, tl[x].t0,
+                      bar_q);
     }
     for (int kt = 0; kt < nkv && alive; ++kt) {
-      const int st = kt & 1;
+      const int st = kt % nst, use = kt / nst;
       const int raw_next = kt + 1 < nkv ? page_of(kt + 1) : 0;
-      if (kt >= 2) wait(&freed[st], (uint32_t)(((kt >> 1) + 1) & 1));
+      if (use >= 1) wait(&freed[st], (uint32_t)((use - 1) & 1));
       if (!alive) break;
-      load_kv(kt, raw, kv, buf + st * S::KV_BYTES, &full[st]);
+      load_kv(kt, raw, kv, buf + st * S::TILE_BYTES, &full[st]);
       raw = raw_next;
     }
-  } else if (warp == 5) {
+  } else if (warp == PF_SM_WARPS + 1) {
     // ------------------------------------------------------------ MMA warp
+    // per KV tile kt: S of both tiles for kt + 1 as soon as each softmax has
+    // read its S of kt (they run on the tensor cores during the softmax),
+    // then P.V of both tiles for kt
     constexpr uint32_t IDESC_S = bf16_idesc(PF_M, PF_N, false);
     constexpr uint32_t IDESC_O = bf16_idesc(PF_M, D, true);
     // descriptors of the operand bases, built once; a K step only moves the
@@ -455,54 +496,57 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const uint64_t dq = sw128_desc(smem_addr(qs), 16, 1024);
     const uint64_t dk = sw128_desc(smem_addr(ks), 16, 1024);
     const uint64_t dv = sw128_desc(smem_addr(vs), PF_CHUNK, 1024);
-    constexpr uint32_t STAGE16 = S::KV_BYTES >> 4;
-    auto issue_s = [&](int stage) {  // S = Q K^T, then release the K stage
-      const uint64_t kb = dk + stage * STAGE16;
+    const uint64_t dp = sw128_desc(smem_addr(ps), 16, 1024);
+    constexpr uint32_t TILE16 = S::TILE_BYTES >> 4;
+    constexpr uint32_t P16 = S::P_BYTES >> 4;
+    auto issue_s = [&](int x, int stage) {  // S_x = Q_x K^T
+      const uint64_t qb = dq + x * TILE16, kb = dk + stage * TILE16;
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = ((k >> 2) * PF_CHUNK + (k & 3) * 32) >> 4;
-        tc_mma(tm_s, dq + off, kb + off, IDESC_S, k > 0);
+        tc_mma(tmem + 128 * x, qb + off, kb + off, IDESC_S, k > 0);
       }
-      tc_commit(bar_s);
-      tc_commit(&bar_kfree[stage]);
+      tc_commit(&bar_s[x]);
     };
-    auto issue_o = [&](int stage, bool acc) {  // O += P V, then release the V stage
-      const uint64_t vb = dv + stage * STAGE16;
+    auto issue_o = [&](int x, int stage, bool acc) {  // O_x += P_x V
+      const uint64_t pb = dp + x * P16, vb = dv + stage * TILE16;
 #pragma unroll
-      for (int k = 0; k < PF_N / 16; ++k)  // 16 keys = 8 columns of P
-        tc_mma_ta(tm_o, tm_p + k * 8, vb + ((k * 16 * 128) >> 4), IDESC_O,
-                  (acc || k > 0) ? 1u : 0u);
-      tc_commit(bar_o);
-      tc_commit(&bar_vfree[stage]);
+      for (int k = 0; k < PF_N / 16; ++k) {
+        const uint32_t poff = ((k >> 2) * PF_CHUNK + (k & 3) * 32) >> 4;
+        tc_mma(tmem + 256 + 128 * x, pb + poff, vb + ((k * 16 * 128) >> 4), IDESC_O,
+               (acc || k > 0) ? 1u : 0u);
+      }
+      tc_commit(&bar_o[x]);
     };
     wait(bar_q, 0);
     wait(&bar_k[0], 0);
     if (alive && lane == 0) {
       tc_fence_after();
-      issue_s(0);
+      issue_s(0, 0);
+      if (tl[1].nkv > 0) issue_s(1, 0);
+      tc_commit(&bar_kfree[0]);
     }
     for (int kt = 0; kt < nkv && alive; ++kt) {
-      const int st = kt & 1;
+      const int nx = kt + 1;
       const uint32_t par = (uint32_t)(kt & 1);
-      // S[kt+1] as soon as S[kt] has been read: it runs on the tensor cores
-      // while the softmax of tile kt is computed
-      wait(bar_sfree, par);
-      if (kt + 1 < nkv) {
-        wait(&bar_k[st ^ 1], (uint32_t)(((kt + 1) >> 1) & 1));
-        if (!alive) break;
-        if (lane == 0) {
+      if (nx < nkv) wait(&bar_k[nx & 1], (uint32_t)((nx >> 1) & 1));
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (kt < tl[x].nkv) wait(&bar_sfree[x], par);
+        if (alive && nx < tl[x].nkv && lane == 0) {
           tc_fence_after();
-          issue_s(st ^ 1);
+          issue_s(x, nx & 1);
         }
       }
-      wait(bar_p, par);  // P[kt] written, O rescaled
-      wait(&bar_v[st], (uint32_t)((kt >> 1) & 1));
+      if (alive && nx < nkv && lane == 0) tc_commit(&bar_kfree[nx & 1]);
+      const int vst = kt % NV;
+      wait(&bar_v[vst], (uint32_t)((kt / NV) & 1));
       if (!alive) break;
       tc_fence_after();
       if (kt == kt_stale) {
         // slots past the request's last position: zero the V rows
         const int r0 = n - kt * PF_N;
-        unsigned char *vt = vs + st * S::KV_BYTES;
+        unsigned char *vt = vs + vst * S::TILE_BYTES;
         for (int r = r0 + lane; r < PF_N; r += 32)
           for (int c = 0; c < NCH; ++c) {
             uint4 *row = reinterpret_cast<uint4 *>(vt + c * PF_CHUNK + r * 128);
@@ -512,7 +556,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (lane == 0) issue_o(st, kt > 0);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (kt >= tl[x].nkv) continue;
+        wait(&bar_p[x], par);  // P_x[kt] written, O_x rescaled
+        if (alive && lane == 0) {
+          tc_fence_after();
+          issue_o(x, vst, kt > 0);
+        }
+      }
+      if (alive && lane == 0) tc_commit(&bar_vfree[vst]);
     }
     // drain: every MMA this thread issued has completed
     if (lane == 0) {
@@ -520,20 +573,25 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       if (!mbar_wait_spin(bar_fin, 0)) report(a.err, PKV_DEV_ERR_TIMEOUT);
     }
     __syncwarp();
-  } else {
+  } else if (warp < PF_SM_WARPS) {
     // ------------------------------------------------------ softmax warps
-    const int r = tid;  // row of the tile (TMEM lane)
+    // warpgroup x owns tile x; thread r of the group owns row r (TMEM lane)
+    const int x = warp >> 2;
+    const PfTile T = x ? tl[1] : tl[0];
+    const int r = tid & 127;
     const int tok = r / G;
     const int hj = r % G;
-    const bool valid = tok < ntok && r < a.tq * G && t0 + tok < a.T;
-    const int p = pos0 + tok;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const bool valid = tok < T.ntok && r < a.tq * G && T.t0 + tok < a.T;
+    const int p = T.pos0 + tok;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tm_s = tmem + 128 * x, tm_o = tmem + 256 + 128 * x;
+    unsigned char *pbuf = ps + x * S::P_BYTES;
     // l_run: sum of the fp32 weights (for lse); w_run: sum of the weights as
     // rounded to bf16 for P.V (normalises O, so the output is a weighted
     // mean of the values with the weights the tensor cores actually used)
     float m_run = -INFINITY, l_run = 0.0f, w_run = 0.0f;
-    for (int kt = 0; kt < nkv; ++kt) {
-      if (!__all_sync(FULL_MASK, mbar_wait_spin(bar_s, (uint32_t)(kt & 1)))) {  // warp-uniform
+    for (int kt = 0; kt < T.nkv; ++kt) {
+      if (!__all_sync(FULL_MASK, mbar_wait_spin(&bar_s[x], (uint32_t)(kt & 1)))) {  // warp-uniform
         alive = false;
         if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
         break;
@@ -544,7 +602,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + lane_off + c * 32, sr[c]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar_sfree);  // the tensor cores may overwrite S now
+      mbar_arrive(&bar_sfree[x]);  // the tensor cores may overwrite S now
       // causal mask (raw scores; only tiles that reach past some row's
       // position need it)
       const int lim = valid ? p - kt * PF_N : -1;  // keys <= lim are allowed
@@ -554,9 +612,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float x = (c * 32 + j <= lim) ? __uint_as_float(sr[c][j]) : -INFINITY;
-            sr[c][j] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
+            const float v = (c * 32 + j <= lim) ? __uint_as_float(sr[c][j]) : -INFINITY;
+            sr[c][j] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
           }
       } else {
 #pragma unroll
@@ -594,8 +652,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       const bool resc = kt > 0 && alpha != 1.0f;
       m_run = m_ref;
       if (kt > 0) {
-        // PV[kt-1] done: O is stable and the P buffer free
-        if (!__all_sync(FULL_MASK, mbar_wait_spin(bar_o, (uint32_t)((kt - 1) & 1)))) {
+        // P.V[kt-1] done: O is stable and the P buffer free
+        if (!__all_sync(FULL_MASK, mbar_wait_spin(&bar_o[x], (uint32_t)((kt - 1) & 1)))) {
           alive = false;
           if (lane == 0) report(a.err, PKV_DEV_ERR_TIMEOUT);
           break;
@@ -614,40 +672,50 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           tmem_wait_st();
         }
       }
-      // P row r into tensor memory: column c holds keys 2c (low half), 2c + 1
-      tmem_st32(tm_p + lane_off, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-      tmem_st32(tm_p + lane_off + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
-      tmem_wait_st();
+      // P row r, keys 0..127, as two 64-key swizzle columns (the A operand
+      // of P.V, K-major)
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4 *dst =
+              reinterpret_cast<uint4 *>(pbuf + c * PF_CHUNK + r * 128 + ((j ^ (r & 7)) << 4));
+          *dst = make_uint4(pk[c * 32 + 4 * j], pk[c * 32 + 4 * j + 1], pk[c * 32 + 4 * j + 2],
+                            pk[c * 32 + 4 * j + 3]);
+        }
+      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(&bar_p[x]);
     }
-    if (alive && __all_sync(FULL_MASK, mbar_wait_spin(bar_o, (uint32_t)((nkv - 1) & 1)))) {
-      tc_fence_after();
-      const float inv = w_run > 0.0f ? 1.0f / w_run : 0.0f;
-      const int t = t0 + tok;
-      uint16_t *orow = a.out + ((int64_t)t * Hq + g * G + hj) * D;
+    if (T.nkv > 0) {
+      if (alive && __all_sync(FULL_MASK, mbar_wait_spin(&bar_o[x], (uint32_t)((T.nkv - 1) & 1)))) {
+        tc_fence_after();
+        const float inv = w_run > 0.0f ? 1.0f / w_run : 0.0f;
+        const int t = T.t0 + tok;
+        uint16_t *orow = a.out + ((int64_t)t * Hq + g * G + hj) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tm_o + lane_off + c * 32, o);
-        tmem_wait_ld();
-        if (valid) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tm_o + lane_off + c * 32, o);
+          tmem_wait_ld();
+          if (valid) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
-            *reinterpret_cast<uint4 *>(orow + c * 32 + j) = w;
+            for (int j = 0; j < 32; j += 8) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
+              *reinterpret_cast<uint4 *>(orow + c * 32 + j) = w;
+            }
           }
         }
+        if (valid && a.lse != nullptr)
+          a.lse[(int64_t)t * Hq + g * G + hj] =
+              l_run > 0.0f ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+      } else if (lane == 0) {
+        report(a.err, PKV_DEV_ERR_TIMEOUT);
       }
-      if (valid && a.lse != nullptr)
-        a.lse[(int64_t)t * Hq + g * G + hj] =
-            l_run > 0.0f ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
-    } else if (lane == 0) {
-      report(a.err, PKV_DEV_ERR_TIMEOUT);
     }
   }
   tc_fence_before();
