@@ -340,13 +340,25 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   if (u >= a.hdr->total_units) return;
   const int su = u / Hkv, g = u % Hkv;
   // schedule position of unit su: the last i with tile_start[i] <= su
-  int lo = 0, hi = a.batch - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.tile_start[mid] <= su)
-      lo = mid;
-    else
-      hi = mid - 1;
+  // (tile_start is non-decreasing).  Up to 64 requests: the warp's lanes
+  // test 32 positions per load; else a binary search.
+  int lo = 0;
+  if (a.batch <= 64) {
+    for (int base = 0; base < a.batch; base += 32) {
+      const int i = base + lane;
+      const unsigned m = __ballot_sync(FULL_MASK, i < a.batch && a.tile_start[i] <= su);
+      if (m) lo = base + 31 - __clz(m);
+      if (m != FULL_MASK) break;
+    }
+  } else {
+    int hi = a.batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.tile_start[mid] <= su)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
   }
   const int b = a.order[lo];
   const int q = a.qo_indptr[b + 1] - a.qo_indptr[b];
@@ -868,8 +880,12 @@ extern "C" int pkv_prefill_attn(const pkv_cache_t *geom, const void *cache, int 
   a.order = reinterpret_cast<int32_t *>(ws + wl.order);
   a.hdr = reinterpret_cast<PfHeader *>(ws + wl.hdr);
   a.err = err_word;
-  // tiles: sum over requests of ceil(q_b / tq) <= T / tq + B
-  const int64_t max_units = ((int64_t)(total_tokens + a.tq - 1) / a.tq + batch) * geom->num_kv_heads;
+  // units: sum over requests of ceil(nt_b / 2), nt_b = ceil(q_b / tq), with
+  // sum nt_b <= ceil(T / tq) + B, so at most (ceil(T / tq) + 2B + 1) / 2
+  // (a CTA past the planner's count exits at once, but holds an SM while
+  // it does)
+  const int64_t tiles_bound = (int64_t)(total_tokens + a.tq - 1) / a.tq + batch;
+  const int64_t max_units = ((tiles_bound + batch + 1) / 2) * geom->num_kv_heads;
   if (max_units > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   alignas(64) CUtensorMap kvm, kvm128, qm;
   st = encode_kv_map(&kvm, cache, geom, PF_BLK);

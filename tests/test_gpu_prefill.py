@@ -33,6 +33,11 @@ CASES = {
         name="p128_small", index=41, num_layers=1, num_qo_heads=32, num_kv_heads=8,
         head_dim=128, page_size=128, reqs=((0, 300), (129, 257), (1000, 1), (0, 1)),
         shuffle_pages=True),
+    # more than 64 requests: the kernel finds a unit's request by binary search
+    "many_requests_70": W.PrefillConfig(
+        name="many70", index=43, num_layers=1, num_qo_heads=8, num_kv_heads=2, head_dim=64,
+        page_size=16, reqs=tuple(((7 * i) % 90, 1 + (13 * i) % 40) for i in range(70)),
+        bucket=False),
     "g8_d128_long_prefix": W.PrefillConfig(
         name="long_prefix", index=42, num_layers=1, num_qo_heads=16, num_kv_heads=2,
         head_dim=128, page_size=16, reqs=((3000, 40), (2047, 129), (0, 16)), bucket=False),
