@@ -74,6 +74,7 @@ constexpr int NCAND = 512;              // most candidates kept per chunk
 constexpr int NC_MIN = 64;              // least candidates kept per chunk
 constexpr int MAX_CHUNKS = 64;          // vocab <= 64 * 8192
 constexpr int GEN_BLOCK = 1024;         // sorted block (finish and general path)
+constexpr int GUMBEL_PRE = 128;         // top-k up to this: noise computed beside the exponentials
 
 enum Mode : int { MODE_GREEDY = 0, MODE_TOPK_SMALL = 1, MODE_TOPP_FULL = 2, MODE_ALL = 3, MODE_GENERAL = 4 };
 
@@ -91,6 +92,7 @@ struct ChunkRec {
   uint32_t gkey;       // order key of gid                            (MODE_ALL)
 };
 static_assert(sizeof(ChunkRec) % 64 == 0, "ChunkRec");
+static_assert(((GUMBEL_PRE + 31) & ~31) + GUMBEL_PRE <= SB, "noise warps fit the CTA");
 
 struct RowParams {
   float temperature;
@@ -344,6 +346,7 @@ struct SampSmem {
   uint32_t penbits[CHUNK / 32];  // penalised tokens of the chunk
   uint64_t sortbuf[GEN_BLOCK];
   double es[GEN_BLOCK];
+  double gs[GUMBEL_PRE];  // Gumbel noise of the first ranks (top-k of at most GUMBEL_PRE)
 };
 
 // ---------------------------------------------------------------------------
@@ -1127,6 +1130,15 @@ __device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
   int kp = minp ? -1 : nv;  // ranks [0, kp) pass min_p (-1: not found yet)
   int scan_lo = 0;
   if (tid == 0) sm.flag = 0;
+  // A top-k of at most GUMBEL_PRE: the Gumbel noise of every candidate is
+  // computed now, by the warps the first block of exponentials (ranks
+  // [0, nv), threads [0, nv)) leaves idle, instead of after the top-p cut;
+  // the values are the same, the fp64 work overlaps.
+  const bool pre_g = !full && nv <= GUMBEL_PRE;
+  if (pre_g) {
+    const int g0 = (nv + 31) & ~31;  // first thread of the noise warps
+    if (tid >= g0 && tid < g0 + nv) sm.gs[tid - g0] = gumbel(P, comp_token(sm.sortbuf[tid - g0]));
+  }
   for (;;) {
     for (int r = lo + tid; r < hi; r += SB) sm.es[r] = exp(comp_x(sm.sortbuf[r], P.temperature) - m);
     __syncthreads();
@@ -1209,7 +1221,7 @@ __device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
   for (int r = tid; r < kept; r += SB) {
     const int tok = comp_token(sm.sortbuf[r]);
     const double x = comp_x(sm.sortbuf[r], P.temperature);
-    const double s = x + gumbel(P, tok);
+    const double s = x + (pre_g ? sm.gs[r] : gumbel(P, tok));
     if (better(s, tok, bs, bid)) {
       bs = s;
       bid = tok;
