@@ -53,6 +53,10 @@ def _cases():
                             ctx=(1, 127, 128, 129, 513, 2100, 4000), shuffle_pages=True),
         "long_p128_small": W.small_variant(W.CONFIGS["long_context_p128"], n_active=3, n_pad=2,
                                            ctx_hi=2600, layers=2).replace(ctx_lo=1500),
+        # every row a whole number of 512-token splits: no short last split
+        "whole_splits": W.Config(name="whole", index=16, num_layers=1, num_qo_heads=8,
+                                 num_kv_heads=2, head_dim=128, page_size=16, n_active=3,
+                                 n_pad=1, ctx=(512, 1024, 2048)),
         # more rows than the kernel's shared-memory split table holds (512):
         # the unit table is read from global memory
         "wide_batch_600": W.Config(name="wide600", index=15, num_layers=1, num_qo_heads=4,
