@@ -6,8 +6,10 @@
 // at positions seq_len - q .. seq_len - 1 of their requests.
 //
 // Bytes moved: per row 2 * num_kv_heads * head_dim * 2 read + the same
-// written.  The kernel is a gather-free scatter of 16-byte chunks: one
-// thread per 16-byte chunk, grid-stride, every store a full 16-byte vector.
+// written.  The kernels are gather-free scatters of 16-byte chunks: one warp
+// per (row, K or V) -- the row's destination (owner request, page, slot) is
+// found once per warp, and each lane moves every 32nd chunk of the row, all
+// of its loads in flight at once; every store a full 16-byte vector.
 #include "pkv_device.cuh"
 #include "pkv_host.h"
 
@@ -32,35 +34,48 @@ struct AppendArgs {
   int32_t *err;
 };
 
-__global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
+constexpr int APPEND_THREADS = 256;
+
+// one warp copies a row of row_chunks 16-byte chunks from src to dst
+__device__ __forceinline__ void copy_row(uint4 *dst, const uint4 *src, int row_chunks, int lane) {
+  int c = lane;
+  for (; c + 96 < row_chunks; c += 128) {  // four chunks per lane in flight
+    const uint4 x0 = __ldg(src + c), x1 = __ldg(src + c + 32);
+    const uint4 x2 = __ldg(src + c + 64), x3 = __ldg(src + c + 96);
+    dst[c] = x0;
+    dst[c + 32] = x1;
+    dst[c + 64] = x2;
+    dst[c + 96] = x3;
+  }
+  for (; c < row_chunks; c += 32) dst[c] = __ldg(src + c);
+}
+
+__global__ void __launch_bounds__(APPEND_THREADS) kv_append_kernel(const AppendArgs a) {
   pdl_wait();
   pdl_trigger();  // the next kernel waits for this grid before reading the cache
-  const int64_t total = (int64_t)a.batch * 2 * a.row_chunks;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i % a.row_chunks);
-    const int64_t bk = i / a.row_chunks;
-    const int kv = (int)(bk & 1);
-    const int b = (int)(bk >> 1);
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)a.batch * 2;
+  const int64_t wstep = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < rows; w += wstep) {
+    const int kv = (int)(w & 1);
+    const int b = (int)(w >> 1);
     int64_t page = 0, slot = 0;
     if (a.active[b]) {
       const int n = a.seq_lens[b];
       if (n < 1 || (int64_t)n > (int64_t)a.max_pages * a.page_size) {
-        if (c == 0 && kv == 0) report(a.err, PKV_DEV_ERR_SEQ_LEN);
+        if (lane == 0 && kv == 0) report(a.err, PKV_DEV_ERR_SEQ_LEN);
         continue;
       }
       const int pos = n - 1;
       page = a.page_table[(int64_t)b * a.max_pages + pos / a.page_size];
       slot = pos % a.page_size;
       if (page < 0 || page >= a.num_pages) {
-        if (c == 0 && kv == 0) report(a.err, PKV_DEV_ERR_PAGE);
+        if (lane == 0 && kv == 0) report(a.err, PKV_DEV_ERR_PAGE);
         continue;
       }
     }
-    const uint4 *src = (kv == 0 ? a.k : a.v) + (int64_t)b * a.row_chunks + c;
-    uint4 *dst = a.cache + a.layer_off + page * a.page_stride + kv * a.kv_stride +
-                 slot * a.slot_stride + c;
-    *dst = __ldg(src);
+    copy_row(a.cache + a.layer_off + page * a.page_stride + kv * a.kv_stride + slot * a.slot_stride,
+             (kv == 0 ? a.k : a.v) + (int64_t)b * a.row_chunks, a.row_chunks, lane);
   }
 }
 
@@ -79,13 +94,12 @@ __global__ void __launch_bounds__(256) kv_append_tokens_kernel(const AppendTokAr
   const AppendArgs &a = t.base;
   pdl_wait();
   pdl_trigger();
-  const int64_t total = (int64_t)t.total_tokens * 2 * a.row_chunks;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i % a.row_chunks);
-    const int64_t tk = i / a.row_chunks;
-    const int kv = (int)(tk & 1);
-    const int tok = (int)(tk >> 1);
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)t.total_tokens * 2;
+  const int64_t wstep = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < rows; w += wstep) {
+    const int kv = (int)(w & 1);
+    const int tok = (int)(w >> 1);
     // owner request: the last b with qo_indptr[b] <= tok
     int lo = 0, hi = a.batch - 1;
     while (lo < hi) {
@@ -98,7 +112,7 @@ __global__ void __launch_bounds__(256) kv_append_tokens_kernel(const AppendTokAr
     const int b = lo;
     const int first = __ldg(t.qo_indptr + b), end = __ldg(t.qo_indptr + b + 1);
     if (tok < first || tok >= end) {
-      if (c == 0 && kv == 0) report(a.err, PKV_DEV_ERR_INDPTR);
+      if (lane == 0 && kv == 0) report(a.err, PKV_DEV_ERR_INDPTR);
       continue;
     }
     int64_t page = 0, slot = 0;
@@ -106,21 +120,19 @@ __global__ void __launch_bounds__(256) kv_append_tokens_kernel(const AppendTokAr
       const int q = end - first;
       const int n = a.seq_lens[b];
       if (n < q || n < 1 || (int64_t)n > (int64_t)a.max_pages * a.page_size) {
-        if (c == 0 && kv == 0 && tok == first) report(a.err, PKV_DEV_ERR_SEQ_LEN);
+        if (lane == 0 && kv == 0 && tok == first) report(a.err, PKV_DEV_ERR_SEQ_LEN);
         continue;
       }
       const int pos = n - q + (tok - first);
       page = a.page_table[(int64_t)b * a.max_pages + pos / a.page_size];
       slot = pos % a.page_size;
       if (page < 0 || page >= a.num_pages) {
-        if (c == 0 && kv == 0) report(a.err, PKV_DEV_ERR_PAGE);
+        if (lane == 0 && kv == 0) report(a.err, PKV_DEV_ERR_PAGE);
         continue;
       }
     }
-    const uint4 *src = (kv == 0 ? a.k : a.v) + (int64_t)tok * a.row_chunks + c;
-    uint4 *dst = a.cache + a.layer_off + page * a.page_stride + kv * a.kv_stride +
-                 slot * a.slot_stride + c;
-    *dst = __ldg(src);
+    copy_row(a.cache + a.layer_off + page * a.page_stride + kv * a.kv_stride + slot * a.slot_stride,
+             (kv == 0 ? a.k : a.v) + (int64_t)tok * a.row_chunks, a.row_chunks, lane);
   }
 }
 
@@ -158,11 +170,10 @@ extern "C" int pkv_kv_append(const pkv_cache_t *geom, void *cache, int layer, co
   a.batch = batch;
   a.err = err_word;
 
-  const int64_t total = (int64_t)batch * 2 * a.row_chunks;
-  const int threads = 256;
-  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t warps = (int64_t)batch * 2;  // one per (row, K or V)
+  int64_t blocks = (warps + APPEND_THREADS / 32 - 1) / (APPEND_THREADS / 32);
   if (blocks > 4096) blocks = 4096;
-  if (launch_pdl(kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+  if (launch_pdl(kv_append_kernel, dim3((unsigned)blocks), dim3(APPEND_THREADS), 0,
                  static_cast<cudaStream_t>(stream), a) != cudaSuccess)
     return PKV_ERR_CUDA;
   return launch_status();
@@ -206,11 +217,10 @@ extern "C" int pkv_kv_append_tokens(const pkv_cache_t *geom, void *cache, int la
   t.qo_indptr = qo_indptr;
   t.total_tokens = total_tokens;
 
-  const int64_t total = (int64_t)total_tokens * 2 * a.row_chunks;
-  const int threads = 256;
-  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t warps = (int64_t)total_tokens * 2;  // one per (token, K or V)
+  int64_t blocks = (warps + APPEND_THREADS / 32 - 1) / (APPEND_THREADS / 32);
   if (blocks > 8192) blocks = 8192;
-  if (launch_pdl(kv_append_tokens_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+  if (launch_pdl(kv_append_tokens_kernel, dim3((unsigned)blocks), dim3(APPEND_THREADS), 0,
                  static_cast<cudaStream_t>(stream), t) != cudaSuccess)
     return PKV_ERR_CUDA;
   return launch_status();
