@@ -92,9 +92,17 @@ struct AppendTokArgs {
 
 __global__ void __launch_bounds__(256) kv_append_tokens_kernel(const AppendTokArgs t) {
   const AppendArgs &a = t.base;
+  constexpr int SMEM_REQS = 1024;  // request tables up to this size are searched in shared memory
+  __shared__ int32_t s_ind[SMEM_REQS + 1];
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
+  const bool in_smem = a.batch <= SMEM_REQS;
+  if (in_smem) {
+    for (int i = threadIdx.x; i <= a.batch; i += blockDim.x) s_ind[i] = __ldg(t.qo_indptr + i);
+    __syncthreads();
+  }
+  const int32_t *ind = in_smem ? s_ind : t.qo_indptr;
   const int64_t rows = (int64_t)t.total_tokens * 2;
   const int64_t wstep = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < rows; w += wstep) {
@@ -104,13 +112,13 @@ __global__ void __launch_bounds__(256) kv_append_tokens_kernel(const AppendTokAr
     int lo = 0, hi = a.batch - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(t.qo_indptr + mid) <= tok)
+      if (ind[mid] <= tok)
         lo = mid;
       else
         hi = mid - 1;
     }
     const int b = lo;
-    const int first = __ldg(t.qo_indptr + b), end = __ldg(t.qo_indptr + b + 1);
+    const int first = ind[b], end = ind[b + 1];
     if (tok < first || tok >= end) {
       if (lane == 0 && kv == 0) report(a.err, PKV_DEV_ERR_INDPTR);
       continue;
