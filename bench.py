@@ -246,6 +246,34 @@ def cpu_baseline(batch, tensors, sizes, budget_s=12.0):
 PREFILL_METRIC = "prefill / mixed step: new tokens/s and causal-attention TFLOP/s at 1 GB300"
 
 
+def rank_barrier(world, device):
+    """Every rank's device work done, then (N > 1) a barrier over the ranks."""
+    import torch
+    import torch.distributed as dist
+    if device == "cuda":
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+
+def rank_max(x, world, device):
+    """The maximum of a per-rank time over the ranks (N > 1: one all-reduce
+    on a tensor of the process group's device)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replicas_throughput(units_per_rank, world, max_ms):
+    """Whole-job throughput of N replicas: all ranks' units over the slowest
+    rank's time (units per second)."""
+    return world * units_per_rank / (max_ms / 1e3)
+
+
 def prefill_flops(batch):
     """Algorithmic FLOPs of one layer's attention: every new token of an
     active request, every q head, 2*D for q.k and 2*D for p.v per key of its
@@ -337,16 +365,10 @@ def run_prefill(args, rank, world):
     stream = torch.cuda.current_stream()
 
     def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        rank_barrier(world, "cuda")
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(x, world, "cuda")
 
     for _ in range(args.warmup):
         step.run(stream)
@@ -420,7 +442,7 @@ def run_prefill(args, rank, world):
     achieved = flops / attn_s / 1e12
     peak, src = tensor_peak(sustained=True)
     line = {
-        "metric": PREFILL_METRIC, "value": world * real * args.steps / (total_ms / 1e3),
+        "metric": PREFILL_METRIC, "value": replicas_throughput(real * args.steps, world, total_ms),
         "unit": "new tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -439,7 +461,7 @@ def run_prefill(args, rank, world):
                      "traffic": attn_traffic(cfg.name, "prefill_attn.cu"),
                      "kernel": "pkv_prefill_attn (planner + tcgen05 attention kernel), per layer",
                      "peak_source": src + " (bf16, sustained)"},
-        "e2e": {"value": world * real * args.steps / (e2e_ms / 1e3), "unit": "new tokens/s",
+        "e2e": {"value": replicas_throughput(real * args.steps, world, e2e_ms), "unit": "new tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": step.launches_per_step() * args.steps,
@@ -550,16 +572,10 @@ def main(argv=None):
     stream = torch.cuda.current_stream()
 
     def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        rank_barrier(world, "cuda")
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(x, world, "cuda")
 
     for _ in range(args.warmup):
         step.run(stream)
@@ -731,8 +747,8 @@ def main(argv=None):
     barrier()
 
     ms_per_step = total_ms / args.steps
-    value = world * sizes["step"] * args.steps / (total_ms / 1e3) / 1e9
-    e2e_value = world * sizes["step"] * args.steps / (e2e_ms / 1e3) / 1e9
+    value = replicas_throughput(sizes["step"] * args.steps, world, total_ms) / 1e9
+    e2e_value = replicas_throughput(sizes["step"] * args.steps, world, e2e_ms) / 1e9
     achieved = sizes["attn_per_layer"] / attn_avg_s / 1e9
     peak, peak_src = peaks()
     line = {
