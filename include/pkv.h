@@ -87,6 +87,20 @@ const char *pkv_error_string(int status);
 /* Number of device-side error bits defined above (for binding checks). */
 int pkv_num_dev_error_bits(void);
 
+/* pkv_selftest_wait_timeout -- a diagnostic, not part of the decode step.
+ * Every wait of the library's kernels (an mbarrier that a bulk copy or
+ * another warp completes) is bounded: when it runs out, the kernel sets
+ * PKV_DEV_ERR_TIMEOUT in the error word, stops waiting and returns, and the
+ * CUDA context stays usable.  This call runs that same bounded wait in one
+ * thread block on an mbarrier that nothing completes, so that the give-up
+ * path can be exercised without any fault: after it, *err_word has
+ * PKV_DEV_ERR_TIMEOUT set.
+ *   limit_ns   the wait's limit, 1 .. 1e9 nanoseconds (else
+ *              PKV_ERR_INVALID_ARG).
+ *   err_word   device int32, OR-ed into; not NULL. */
+int pkv_selftest_wait_timeout(unsigned long long limit_ns, int32_t *err_word,
+                              void *stream);
+
 /* ------------------------------------------------------------------------
  * pkv_kv_append -- set_kv_cache(kv_cache, k, v) of "Adding a Model",
  * section "1. The model code": write each row's new key and value into the

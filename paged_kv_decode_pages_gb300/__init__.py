@@ -19,7 +19,7 @@ _BINDING = (
     "seeded_sample", "sample_workspace_bytes", "seeded_sample_ext", "sample_ext_workspace_bytes",
     "codebook_frame_sample", "frame_workspace_bytes",
     "frame_sample", "frame_sample_workspace_bytes",
-    "KIND_OTHER", "KIND_AUDIO", "KIND_STOP", "CODE_PAD",
+    "KIND_OTHER", "KIND_AUDIO", "KIND_STOP", "CODE_PAD", "selftest_wait_timeout",
 )
 
 __all__ = list(_BINDING)

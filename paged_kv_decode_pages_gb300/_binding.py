@@ -41,6 +41,7 @@ SIGNATURES = {
     "pkv_kv_append": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _P, _P, _I, _P, _P, _I, _P,
                            _P]),
     "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P, _P]),
     "pkv_paged_decode_attn": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _I, _F, _P, _I, _P,
                                    _P, _I, _P, _I, _P, _P, _SZ, _P, _P]),
     "pkv_paged_decode_attn_static": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _I, _F, _P,
@@ -184,6 +185,15 @@ def paged_decode_attn(cache, layer, q, page_table, seq_lens, active, out, worksp
         int(out.dtype == torch.float32), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(err_word),
         _stream(stream))
     _check("pkv_paged_decode_attn", st)
+
+
+def selftest_wait_timeout(limit_ns, err_word, stream=None):
+    """pkv_selftest_wait_timeout: the kernels' bounded wait run on an
+    mbarrier nothing completes; sets the timeout bit of err_word."""
+    import torch
+    _req(err_word, torch.int32, "err_word")
+    st = load().pkv_selftest_wait_timeout(int(limit_ns), _ptr(err_word), _stream(stream))
+    _check("pkv_selftest_wait_timeout", st)
 
 
 STATIC_SCRATCH_BYTES = 32 << 20  # PKV_ATTN_STATIC_SCRATCH_BYTES

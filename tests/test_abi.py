@@ -73,6 +73,9 @@ def test_host_validation_rejects_before_launch(lib):
     st = lib.pkv_paged_decode_attn(ctypes.byref(g3), P, 0, P, 4, 1.0, P, 100, P, P, 1, P, 0, None,
                                    None, 0, None, None)  # 4 splits, no workspace
     assert st == 4
+    assert lib.pkv_selftest_wait_timeout(0, P, None) == 1  # no limit
+    assert lib.pkv_selftest_wait_timeout(2 * 10**9, P, None) == 1  # over a second
+    assert lib.pkv_selftest_wait_timeout(1000, None, None) == 1  # no error word
     st = lib.pkv_seeded_sample(P, 16, 1, 16, P, P, 1, P, P, P, P, P, 0, 1, None, 0, 0, 0, P, P,
                                None, 0, None, None)  # no workspace
     assert st == 4
