@@ -51,7 +51,7 @@ constexpr int PF_M = 128;          // MMA rows of a tile
 constexpr int PF_N = 128;          // keys of a KV tile
 constexpr int PF_BLK = 16;         // tokens of one cache block (one TMA box)
 constexpr int PF_SM_WARPS = 8;     // two softmax warpgroups, one per q tile of the unit
-constexpr int PF_THREADS = 352;    // + K load warp, MMA warp, V load warp
+constexpr int PF_THREADS = 384;    // + K load warp, tile A's MMA warp, V load warp, tile B's MMA warp
 constexpr int PF_CHUNK = 16384;    // 128 rows x 128 bytes (64 bf16): one swizzle column
 constexpr int PF_TMEM_COLS = 512;  // S of both tiles (128 columns each), O of both (128 each)
 constexpr int PF_PLAN_THREADS = 1024;
@@ -272,7 +272,7 @@ struct PfShape {
   static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
   static constexpr int OFF_P = OFF_V + NV * TILE_BYTES;  // [2 tiles]
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int NBAR = 18;
+  static constexpr int NBAR = 19;
   // + alignment slack; at least 120 KB, so that one CTA (which holds all
   // 512 tensor-memory columns) is resident per SM
   static constexpr int RAW = OFF_BAR + NBAR * 8 + 16 + 1024;
@@ -312,7 +312,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   uint64_t *bar_o = bars + 11;      // [tile] P.V computed
   uint64_t *bar_kfree = bars + 13;  // [2] the S products of the K stage's tile have completed
   uint64_t *bar_vfree = bars + 15;  // [2] the P.V products of the V stage's tile have completed
-  uint64_t *bar_fin = bars + 17;
+  uint64_t *bar_fin = bars + 17;   // both MMA warps' products have completed
+  uint64_t *bar_vz = bars + 18;    // the stale V rows are zeroed (tile A's MMA warp)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::NBAR);
 
   const int tid = threadIdx.x;
@@ -391,7 +392,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
   if (tid == 0) {
     for (int i = 0; i < S::NBAR; ++i)
-      mbar_init(&bars[i], (i >= 7 && i <= 10) ? 128u : 1u);  // sfree, p: one arrival per row
+      // sfree, p: one arrival per row; K / V stage releases and the drain:
+      // one commit per MMA warp
+      mbar_init(&bars[i], (i >= 7 && i <= 10) ? 128u : ((i >= 13 && i <= 17) ? 2u : 1u));
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -483,23 +486,25 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       load_kv(kt, raw, kv, buf + st * S::TILE_BYTES, &full[st]);
       raw = raw_next;
     }
-  } else if (warp == PF_SM_WARPS + 1) {
-    // ------------------------------------------------------------ MMA warp
-    // per KV tile kt: S of both tiles for kt + 1 as soon as each softmax has
-    // read its S of kt (they run on the tensor cores during the softmax),
-    // then P.V of both tiles for kt
+  } else if (warp == PF_SM_WARPS + 1 || warp == PF_SM_WARPS + 3) {
+    // ------------------------------------------------------------ MMA warps
+    // one per tile (A: warp 9, B: warp 11), each issuing its own tile's
+    // products as their inputs come: S(kt + 1) as soon as the softmax has
+    // read S(kt), P.V(kt) once P(kt) is written.  The two tiles' accumulation
+    // chains are independent, so the tensor pipe overlaps them.  A K or V
+    // stage is free once both warps' products that read it have completed
+    // (one commit per warp, also for KV tiles a shorter tile B does not read)
+    const int x = warp == PF_SM_WARPS + 1 ? 0 : 1;
+    const int mine = tl[x].nkv;
     constexpr uint32_t IDESC_S = bf16_idesc(PF_M, PF_N, false);
     constexpr uint32_t IDESC_O = bf16_idesc(PF_M, D, true);
-    // descriptors of the operand bases, built once; a K step only moves the
-    // start address (bits 0-13, in 16-byte units; every address here is
-    // below 256 KB, so the sum never carries out of the field)
     const uint64_t dq = sw128_desc(smem_addr(qs), 16, 1024);
     const uint64_t dk = sw128_desc(smem_addr(ks), 16, 1024);
     const uint64_t dv = sw128_desc(smem_addr(vs), PF_CHUNK, 1024);
     const uint64_t dp = sw128_desc(smem_addr(ps), 16, 1024);
     constexpr uint32_t TILE16 = S::TILE_BYTES >> 4;
     constexpr uint32_t P16 = S::P_BYTES >> 4;
-    auto issue_s = [&](int x, int stage) {  // S_x = Q_x K^T
+    auto issue_s = [&](int stage) {  // S_x = Q_x K^T
       const uint64_t qb = dq + x * TILE16, kb = dk + stage * TILE16;
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
@@ -508,7 +513,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       }
       tc_commit(&bar_s[x]);
     };
-    auto issue_o = [&](int x, int stage, bool acc) {  // O_x += P_x V
+    auto issue_o = [&](int stage, bool acc) {  // O_x += P_x V
       const uint64_t pb = dp + x * P16, vb = dv + stage * TILE16;
 #pragma unroll
       for (int k = 0; k < PF_N / 16; ++k) {
@@ -522,52 +527,56 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     wait(&bar_k[0], 0);
     if (alive && lane == 0) {
       tc_fence_after();
-      issue_s(0, 0);
-      if (tl[1].nkv > 0) issue_s(1, 0);
+      if (mine > 0) issue_s(0);
       tc_commit(&bar_kfree[0]);
     }
     for (int kt = 0; kt < nkv && alive; ++kt) {
       const int nx = kt + 1;
-      const uint32_t par = (uint32_t)(kt & 1);
-      if (nx < nkv) wait(&bar_k[nx & 1], (uint32_t)((nx >> 1) & 1));
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (kt < tl[x].nkv) wait(&bar_sfree[x], par);
-        if (alive && nx < tl[x].nkv && lane == 0) {
+      if (nx < nkv) {
+        wait(&bar_k[nx & 1], (uint32_t)((nx >> 1) & 1));
+        if (nx < mine) wait(&bar_sfree[x], (uint32_t)(kt & 1));
+        if (!alive) break;
+        if (lane == 0) {
           tc_fence_after();
-          issue_s(x, nx & 1);
+          if (nx < mine) issue_s(nx & 1);
+          tc_commit(&bar_kfree[nx & 1]);
         }
       }
-      if (alive && nx < nkv && lane == 0) tc_commit(&bar_kfree[nx & 1]);
       const int vst = kt % NV;
       wait(&bar_v[vst], (uint32_t)((kt / NV) & 1));
       if (!alive) break;
       tc_fence_after();
-      if (kt == kt_stale) {
-        // slots past the request's last position: zero the V rows
-        const int r0 = n - kt * PF_N;
-        unsigned char *vt = vs + vst * S::TILE_BYTES;
-        for (int r = r0 + lane; r < PF_N; r += 32)
-          for (int c = 0; c < NCH; ++c) {
-            uint4 *row = reinterpret_cast<uint4 *>(vt + c * PF_CHUNK + r * 128);
+      if (kt == kt_stale && kt < mine) {
+        if (x == 0) {
+          // slots past the request's last position: zero the V rows, then
+          // let tile B's warp (if it reads this tile) go on
+          const int r0 = n - kt * PF_N;
+          unsigned char *vt = vs + vst * S::TILE_BYTES;
+          for (int r = r0 + lane; r < PF_N; r += 32)
+            for (int c = 0; c < NCH; ++c) {
+              uint4 *row = reinterpret_cast<uint4 *>(vt + c * PF_CHUNK + r * 128);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) row[j] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (kt >= tl[x].nkv) continue;
-        wait(&bar_p[x], par);  // P_x[kt] written, O_x rescaled
-        if (alive && lane == 0) {
-          tc_fence_after();
-          issue_o(x, vst, kt > 0);
+              for (int j = 0; j < 8; ++j) row[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_vz);
+        } else {
+          wait(bar_vz, 0u);
+          if (!alive) break;
         }
       }
-      if (alive && lane == 0) tc_commit(&bar_vfree[vst]);
+      if (kt < mine) {
+        wait(&bar_p[x], (uint32_t)(kt & 1));  // P_x[kt] written, O_x rescaled
+        if (!alive) break;
+        if (lane == 0) {
+          tc_fence_after();
+          issue_o(vst, kt > 0);
+        }
+      }
+      if (lane == 0) tc_commit(&bar_vfree[vst]);
     }
-    // drain: every MMA this thread issued has completed
+    // drain: every MMA of both warps has completed
     if (lane == 0) {
       tc_commit(bar_fin);
       if (!mbar_wait_spin(bar_fin, 0)) report(a.err, PKV_DEV_ERR_TIMEOUT);
