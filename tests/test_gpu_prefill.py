@@ -33,7 +33,7 @@ CASES = {
         name="p128_small", index=41, num_layers=1, num_qo_heads=32, num_kv_heads=8,
         head_dim=128, page_size=128, reqs=((0, 300), (129, 257), (1000, 1), (0, 1)),
         shuffle_pages=True),
-    # 33-64 requests: each lane looks at two schedule positions
+    # 33-64 requests: the unit lookup takes a second 32-position ballot
     "requests_45": W.PrefillConfig(
         name="req45", index=44, num_layers=1, num_qo_heads=16, num_kv_heads=4, head_dim=128,
         page_size=32, reqs=tuple(((11 * i) % 150, 1 + (17 * i) % 70) for i in range(45)),
