@@ -209,6 +209,47 @@ int pkv_paged_decode_attn_static(const pkv_cache_t *geom, const void *cache,
                                  void *stream);
 
 /* ------------------------------------------------------------------------
+ * pkv_decode_plan / pkv_paged_decode_attn_planned -- the same attention as
+ * pkv_paged_decode_attn, with its schedule made once for all of a step's
+ * layers.  "Supported Models" (sections "Nemotron VoiceChat (nemotron_duplex)
+ * notes" and "Chatterbox notes") declare an attention plan on the paged
+ * cache, shared by a step's layers and by the captured decode graph of a
+ * batch size; the reading taken is that the plan depends on the batch's
+ * rows and lengths only, so one plan serves every layer of the step.
+ *
+ * pkv_decode_plan writes into `workspace` the schedule of a batch: which
+ * 512-token splits of which rows form the attention units, longest first.
+ * It reads seq_lens and active (on the device, in stream order) and nothing
+ * else.  Arguments as for pkv_paged_decode_attn; the cache, q and output
+ * are not needed.
+ *
+ * pkv_paged_decode_attn_planned then runs one layer's attention on that
+ * schedule, without the planner: the same arguments as
+ * pkv_paged_decode_attn.  The workspace must hold a plan that
+ * pkv_decode_plan wrote, earlier in the same stream, with the same geom,
+ * num_qo_heads, max_pages, batch and the same contents of seq_lens and
+ * active (the caller's contract; the library cannot check it).  Any number
+ * of planned calls may follow one plan; each leaves the plan ready for the
+ * next.  Results are bit-identical to pkv_paged_decode_attn on the same
+ * inputs.  A row that pkv_decode_plan reported as malformed
+ * (PKV_DEV_ERR_SEQ_LEN) is reported by the plan only, once per step.
+ * Errors: as for pkv_paged_decode_attn.
+ * ---------------------------------------------------------------------- */
+int pkv_decode_plan(const pkv_cache_t *geom, int num_qo_heads, int max_pages,
+                    const int32_t *seq_lens, const int32_t *active, int batch,
+                    void *workspace, size_t workspace_bytes, int32_t *err_word,
+                    void *stream);
+
+int pkv_paged_decode_attn_planned(const pkv_cache_t *geom, const void *cache,
+                                  int layer, const void *q, int num_qo_heads,
+                                  float sm_scale, const int32_t *page_table,
+                                  int max_pages, const int32_t *seq_lens,
+                                  const int32_t *active, int batch, void *out,
+                                  int out_fp32, float *lse, void *workspace,
+                                  size_t workspace_bytes, int32_t *err_word,
+                                  void *stream);
+
+/* ------------------------------------------------------------------------
  * Prefill and mixed steps ("Adding a Model", "How a program runs": lm_prefill
  * runs prompt rows, one graph per row bucket; "Supported Models", Qwen3.5 /
  * Qwen3.8 notes: text prefill and mixed steps, replayed by total tokens).

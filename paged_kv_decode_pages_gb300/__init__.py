@@ -15,6 +15,7 @@ does, and raises if it is missing.
 _BINDING = (
     "load", "library_path", "version", "error_string", "PkvError",
     "kv_append", "paged_decode_attn", "decode_workspace_bytes", "paged_decode_attn_static",
+    "decode_plan", "paged_decode_attn_planned",
     "kv_append_tokens", "prefill_attn", "prefill_workspace_bytes",
     "seeded_sample", "sample_workspace_bytes", "seeded_sample_ext", "sample_ext_workspace_bytes",
     "codebook_frame_sample", "frame_workspace_bytes",

@@ -46,6 +46,9 @@ SIGNATURES = {
                                    _P, _I, _P, _I, _P, _P, _SZ, _P, _P]),
     "pkv_paged_decode_attn_static": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _I, _F, _P,
                                           _I, _P, _P, _I, _P, _I, _P, _P, _P]),
+    "pkv_decode_plan": (_I, [ctypes.POINTER(pkv_cache_t), _I, _I, _P, _P, _I, _P, _SZ, _P, _P]),
+    "pkv_paged_decode_attn_planned": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _I, _F, _P,
+                                           _I, _P, _P, _I, _P, _I, _P, _P, _SZ, _P, _P]),
     "pkv_kv_append_tokens": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _P, _I, _P, _P, _I,
                                   _P, _P, _I, _P, _P]),
     "pkv_prefill_workspace_bytes": (_SZ, [_I]),
@@ -165,7 +168,9 @@ def decode_workspace_bytes(batch, num_qo_heads, head_dim, max_pages, page_size=1
 
 
 def paged_decode_attn(cache, layer, q, page_table, seq_lens, active, out, workspace,
-                      lse=None, sm_scale=None, err_word=None, stream=None):
+                      lse=None, sm_scale=None, err_word=None, stream=None, planned=False):
+    """pkv_paged_decode_attn, or with planned=True pkv_paged_decode_attn_planned
+    (the workspace then holds a plan from decode_plan for this batch)."""
     import torch
     _req(cache, torch.bfloat16, "cache")
     _req(q, torch.bfloat16, "q")
@@ -179,12 +184,37 @@ def paged_decode_attn(cache, layer, q, page_table, seq_lens, active, out, worksp
     if sm_scale is None:
         sm_scale = 1.0 / (D ** 0.5)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = load().pkv_paged_decode_attn(
+    name = "pkv_paged_decode_attn_planned" if planned else "pkv_paged_decode_attn"
+    st = getattr(load(), name)(
         ctypes.byref(g), _ptr(cache), int(layer), _ptr(q), Hq, float(sm_scale), _ptr(page_table),
         page_table.shape[1], _ptr(seq_lens), _ptr(active), B, _ptr(out),
         int(out.dtype == torch.float32), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(err_word),
         _stream(stream))
-    _check("pkv_paged_decode_attn", st)
+    _check(name, st)
+
+
+def paged_decode_attn_planned(cache, layer, q, page_table, seq_lens, active, out, workspace,
+                              lse=None, sm_scale=None, err_word=None, stream=None):
+    """pkv_paged_decode_attn_planned: one layer's attention on the plan that
+    decode_plan wrote into the workspace."""
+    paged_decode_attn(cache, layer, q, page_table, seq_lens, active, out, workspace, lse=lse,
+                      sm_scale=sm_scale, err_word=err_word, stream=stream, planned=True)
+
+
+def decode_plan(cache, num_qo_heads, max_pages, seq_lens, active, workspace, err_word=None,
+                stream=None):
+    """pkv_decode_plan: the batch's attention schedule, once per step, for
+    paged_decode_attn(..., planned=True) calls of every layer."""
+    import torch
+    _req(cache, torch.bfloat16, "cache")
+    _req(seq_lens, torch.int32, "seq_lens")
+    _req(active, torch.int32, "active")
+    g = _geom(cache)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().pkv_decode_plan(ctypes.byref(g), int(num_qo_heads), int(max_pages),
+                                _ptr(seq_lens), _ptr(active), seq_lens.shape[0],
+                                _ptr(workspace), ws_bytes, _ptr(err_word), _stream(stream))
+    _check("pkv_decode_plan", st)
 
 
 def selftest_wait_timeout(limit_ns, err_word, stream=None):

@@ -43,6 +43,7 @@
 //    blocking atomics sit in the streaming loop: the next unit's id is
 //    fetched one unit ahead.
 #include <math.h>
+#include <string.h>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -705,6 +706,9 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_merge_kernel(const AttnArgs
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();  // the partials of the persistent kernel
   pdl_trigger();
+  // the persistent grid has completed: its unit counter starts again at zero
+  // for the next call that runs on the same plan
+  if (h == 0 && b == 0 && threadIdx.x == 0) a.plan->counter = 0;
   const int64_t bh = (int64_t)b * a.num_qo_heads + h;
   const int n = a.seq_lens[b];
   if (!a.active[b] || n < 1 || (int64_t)n > a.max_tokens) {
@@ -787,8 +791,12 @@ static int heads_per_cta(int D, int group) {
   return gp < cap ? gp : cap;
 }
 
+// what a call launches: the planner, the attention kernels, or both
+enum AttnMode { ATTN_PLAN_AND_RUN = 0, ATTN_PLAN_ONLY = 1, ATTN_RUN_ONLY = 2 };
+
 template <int D, int GP, int NS>
-static int launch_attn(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t st) {
+static int launch_attn(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t st,
+                       AttnMode mode) {
   using S = AttnShape<D, GP, NS>;
   auto kern = attn_persistent_kernel<D, GP, NS>;
   static int grid_for_device[64] = {0};  // persistent grid per device (0: not known yet)
@@ -808,8 +816,10 @@ static int launch_attn(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t 
     if (per_sm < 1) return PKV_ERR_UNSUPPORTED;
     grid = sms * per_sm;
   }
-  if (launch_pdl(attn_plan_kernel, dim3(1), dim3(PLAN_THREADS), 0, st, a) != cudaSuccess)
+  if (mode != ATTN_RUN_ONLY &&
+      launch_pdl(attn_plan_kernel, dim3(1), dim3(PLAN_THREADS), 0, st, a) != cudaSuccess)
     return PKV_ERR_CUDA;
+  if (mode == ATTN_PLAN_ONLY) return launch_status();
   if (launch_pdl(kern, dim3(grid), dim3(ATTN_THREADS), S::SMEM_BYTES, st, a, tmap) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (launch_pdl(attn_merge_kernel<D>, dim3((unsigned)a.num_qo_heads, (unsigned)a.batch),
@@ -819,13 +829,14 @@ static int launch_attn(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t 
 }
 
 template <int D>
-static int dispatch_gp(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t st) {
+static int dispatch_gp(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t st,
+                       AttnMode mode) {
   constexpr int NS = D == 128 ? 3 : 6;
   switch (a.gp) {
-    case 2: return launch_attn<D, 2, NS>(a, tmap, st);
-    case 4: return launch_attn<D, 4, NS>(a, tmap, st);
+    case 2: return launch_attn<D, 2, NS>(a, tmap, st, mode);
+    case 4: return launch_attn<D, 4, NS>(a, tmap, st, mode);
     default:
-      if constexpr (D == 64) return launch_attn<D, 8, NS>(a, tmap, st);
+      if constexpr (D == 64) return launch_attn<D, 8, NS>(a, tmap, st, mode);
       return PKV_ERR_UNSUPPORTED;
   }
 }
@@ -894,16 +905,19 @@ extern "C" size_t pkv_decode_workspace_bytes(int batch, int num_qo_heads, int he
   return ws_layout(batch, num_qo_heads, head_dim, (int64_t)max_pages * page_size).total;
 }
 
-extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache, int layer,
-                                     const void *q, int num_qo_heads, float sm_scale,
-                                     const int32_t *page_table, int max_pages,
-                                     const int32_t *seq_lens, const int32_t *active, int batch,
-                                     void *out, int out_fp32, float *lse, void *workspace,
-                                     size_t workspace_bytes, int32_t *err_word, void *stream) {
-  using namespace pkv;
+namespace pkv {
+
+// Checks a call's arguments and fills the kernels' arguments.  With
+// plan_only the call has no cache, q or output (the planner reads none).
+static int attn_setup(const pkv_cache_t *geom, const void *cache, int layer, const void *q,
+                      int num_qo_heads, float sm_scale, const int32_t *page_table, int max_pages,
+                      const int32_t *seq_lens, const int32_t *active, int batch, void *out,
+                      int out_fp32, float *lse, void *workspace, size_t workspace_bytes,
+                      int32_t *err_word, bool plan_only, AttnArgs *pa, CUtensorMap *tmap) {
   int st = check_geometry(geom);
   if (st != PKV_OK) return st;
-  if (!cache || !q || !page_table || !seq_lens || !active || !out) return PKV_ERR_INVALID_ARG;
+  if (!seq_lens || !active) return PKV_ERR_INVALID_ARG;
+  if (!plan_only && (!cache || !q || !page_table || !out)) return PKV_ERR_INVALID_ARG;
   if (batch <= 0 || max_pages <= 0 || layer < 0 || layer >= geom->num_layers ||
       num_qo_heads <= 0 || num_qo_heads % geom->num_kv_heads != 0)
     return PKV_ERR_INVALID_ARG;
@@ -918,12 +932,13 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
       (int64_t)batch * num_qo_heads * (int64_t)nsplit_for(max_tokens) > (1ll << 30) ||
       (int64_t)geom->num_pages * (geom->page_size / ATTN_PAGE) > INT32_MAX)
     return PKV_ERR_UNSUPPORTED;
-  if (!aligned16(cache) || !aligned16(q)) return PKV_ERR_INVALID_ARG;
+  if (!plan_only && (!aligned16(cache) || !aligned16(q))) return PKV_ERR_INVALID_ARG;
   const WsLayout wl = ws_layout(batch, num_qo_heads, D, max_tokens);
   if (workspace == nullptr || workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
+  if ((int64_t)geom->num_layers * geom->num_pages > INT32_MAX) return PKV_ERR_UNSUPPORTED;
 
-  AttnArgs a;
+  AttnArgs &a = *pa;
   const int64_t row_bytes = (int64_t)D * 2;
   a.cache = static_cast<const unsigned char *>(cache);
   a.tok_stride = row_bytes * geom->num_kv_heads;
@@ -958,12 +973,61 @@ extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
   a.plan = reinterpret_cast<PlanHeader *>(ws + wl.plan);
   a.err = err_word;
   a.layer = layer;
-  if ((int64_t)geom->num_layers * geom->num_pages > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (!plan_only) {
+    st = encode_cache_map(tmap, cache, geom);
+    if (st != PKV_OK) return st;
+  }
+  return PKV_OK;
+}
+
+static int attn_call(const pkv_cache_t *geom, const void *cache, int layer, const void *q,
+                     int num_qo_heads, float sm_scale, const int32_t *page_table, int max_pages,
+                     const int32_t *seq_lens, const int32_t *active, int batch, void *out,
+                     int out_fp32, float *lse, void *workspace, size_t workspace_bytes,
+                     int32_t *err_word, void *stream, AttnMode mode) {
+  AttnArgs a;
   alignas(64) CUtensorMap tmap;
-  st = encode_cache_map(&tmap, cache, geom);
+  memset(&tmap, 0, sizeof(tmap));
+  const int st = attn_setup(geom, cache, layer, q, num_qo_heads, sm_scale, page_table, max_pages,
+                            seq_lens, active, batch, out, out_fp32, lse, workspace,
+                            workspace_bytes, err_word, mode == ATTN_PLAN_ONLY, &a, &tmap);
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return D == 128 ? dispatch_gp<128>(a, tmap, s) : dispatch_gp<64>(a, tmap, s);
+  return a.head_dim == 128 ? dispatch_gp<128>(a, tmap, s, mode) : dispatch_gp<64>(a, tmap, s, mode);
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache, int layer,
+                                     const void *q, int num_qo_heads, float sm_scale,
+                                     const int32_t *page_table, int max_pages,
+                                     const int32_t *seq_lens, const int32_t *active, int batch,
+                                     void *out, int out_fp32, float *lse, void *workspace,
+                                     size_t workspace_bytes, int32_t *err_word, void *stream) {
+  return pkv::attn_call(geom, cache, layer, q, num_qo_heads, sm_scale, page_table, max_pages,
+                        seq_lens, active, batch, out, out_fp32, lse, workspace, workspace_bytes,
+                        err_word, stream, pkv::ATTN_PLAN_AND_RUN);
+}
+
+extern "C" int pkv_decode_plan(const pkv_cache_t *geom, int num_qo_heads, int max_pages,
+                               const int32_t *seq_lens, const int32_t *active, int batch,
+                               void *workspace, size_t workspace_bytes, int32_t *err_word,
+                               void *stream) {
+  return pkv::attn_call(geom, nullptr, 0, nullptr, num_qo_heads, 1.0f, nullptr, max_pages,
+                        seq_lens, active, batch, nullptr, 0, nullptr, workspace, workspace_bytes,
+                        err_word, stream, pkv::ATTN_PLAN_ONLY);
+}
+
+extern "C" int pkv_paged_decode_attn_planned(const pkv_cache_t *geom, const void *cache, int layer,
+                                             const void *q, int num_qo_heads, float sm_scale,
+                                             const int32_t *page_table, int max_pages,
+                                             const int32_t *seq_lens, const int32_t *active,
+                                             int batch, void *out, int out_fp32, float *lse,
+                                             void *workspace, size_t workspace_bytes,
+                                             int32_t *err_word, void *stream) {
+  return pkv::attn_call(geom, cache, layer, q, num_qo_heads, sm_scale, page_table, max_pages,
+                        seq_lens, active, batch, out, out_fp32, lse, workspace, workspace_bytes,
+                        err_word, stream, pkv::ATTN_RUN_ONLY);
 }
 
 // ---------------------------------------------------------------------------

@@ -2,7 +2,8 @@
 
 ``DecodeStep`` owns the device-side inputs and outputs of one batch (page
 tables, lengths, per-slot sampler state, attention outputs, workspaces) and
-runs the hot path: for every layer kv_append then paged_decode_attn, then
+runs the hot path: decode_plan once (the batch's attention schedule, shared
+by the layers), for every layer kv_append then paged_decode_attn_planned, then
 seeded_sample over the logits, then (frame workloads) one frame: a
 frame_sample (stop/continue on channel 0, then the codebooks) when the
 workload has control logits, else a codebook_frame_sample.  It only orders
@@ -22,7 +23,7 @@ from .workloads import Batch, Tensors
 class DecodeStep:
     def __init__(self, batch: Batch, tensors: Tensors, device="cuda", stop_tokens=None,
                  audio_lo: int = 0, audio_hi: int = 0, out_fp32: bool = False,
-                 with_lse: bool = True):
+                 with_lse: bool = True, plan_once: bool = True):
         import torch
         cfg = batch.cfg
         self.batch = batch
@@ -71,6 +72,9 @@ class DecodeStep:
             self.frame_ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
             self.frame_kind = torch.empty(Bn, dtype=i32, device=dev)
         self.err = torch.zeros(1, dtype=i32, device=dev)
+        # plan_once: one decode_plan per step, then the planned attention
+        # per layer; else every layer's call plans for itself
+        self.plan_once = bool(plan_once)
         self.graph = None
         self._warm = False
 
@@ -80,12 +84,18 @@ class DecodeStep:
         B.kv_append(t.cache, layer, t.k[layer], t.v[layer], self.page_table, self.seq_lens,
                     self.active, err_word=self.err, stream=stream)
 
+    def plan(self, stream=None):
+        """The batch's attention schedule into the attention workspace."""
+        B.decode_plan(self.t.cache, self.cfg.num_qo_heads, self.page_table.shape[1],
+                      self.seq_lens, self.active, self.attn_ws, err_word=self.err,
+                      stream=stream)
+
     def attend(self, layer: int, stream=None):
         t = self.t
         B.paged_decode_attn(t.cache, layer, t.q[layer], self.page_table, self.seq_lens,
                             self.active, self.out[layer], self.attn_ws,
                             lse=None if self.lse is None else self.lse[layer],
-                            err_word=self.err, stream=stream)
+                            err_word=self.err, stream=stream, planned=self.plan_once)
 
     def sample(self, advance=True, salt=0, stream=None):
         B.seeded_sample(self.t.logits, self.slots, self.active, self.seeds, self.steps,
@@ -147,6 +157,8 @@ class DecodeStep:
         L = self.t.layers
         st = stream if stream is not None else torch.cuda.current_stream()
         self._warm = True
+        if self.plan_once:
+            self.plan(stream=st)
         for l in (layers if layers is not None else range(L)):
             self.append(l, stream=st)
             if attn_events is not None:
@@ -189,8 +201,9 @@ class DecodeStep:
         self.graph.replay()
 
     def capture_attention(self):
-        """Capture the attention calls of every layer alone (planner,
-        persistent kernel and merge per layer, back to back) as a second
+        """Capture the attention calls of every layer alone (with plan_once
+        the step's plan, then the persistent kernel and merge per layer;
+        else planner, persistent kernel and merge per layer) as a second
         graph, to time the attention kernels without host launch gaps.
         Needs a run() (or capture()) first."""
         import torch
@@ -199,6 +212,8 @@ class DecodeStep:
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
+            if self.plan_once:
+                self.plan()
             for l in range(self.t.layers):
                 self.attend(l)
         self.attn_graph = g
@@ -208,10 +223,11 @@ class DecodeStep:
         self.attn_graph.replay()
 
     def launches_per_step(self) -> int:
-        """Kernel launches of one run(): per layer append 1 + attention 3
-        (planner, persistent kernel, split merge); sampler 2; frame 1."""
+        """Kernel launches of one run(): with plan_once one planner, then per
+        layer append 1 + attention 2 (persistent kernel, split merge); else
+        per layer append 1 + attention 3 (planner too); sampler 2; frame 1."""
         L = self.t.layers
-        n = L * 4
+        n = 1 + L * 3 if self.plan_once else L * 4
         if self.t.logits is not None:
             n += 2
         if self.t.base is not None:

@@ -73,6 +73,19 @@ def test_host_validation_rejects_before_launch(lib):
     st = lib.pkv_paged_decode_attn(ctypes.byref(g3), P, 0, P, 4, 1.0, P, 100, P, P, 1, P, 0, None,
                                    None, 0, None, None)  # 4 splits, no workspace
     assert st == 4
+    # the plan / planned pair: the same checks as the per-call entry point
+    st = lib.pkv_decode_plan(ctypes.byref(g3), 4, 100, P, P, 1, None, 0, None, None)
+    assert st == 4  # no workspace
+    st = lib.pkv_decode_plan(ctypes.byref(g3), 4, 100, None, P, 1, P, 1 << 20, None, None)
+    assert st == 1  # no seq_lens
+    st = lib.pkv_decode_plan(ctypes.byref(g3), 3, 100, P, P, 1, P, 1 << 20, None, None)
+    assert st == 1  # 3 q heads over 2 kv heads
+    st = lib.pkv_paged_decode_attn_planned(ctypes.byref(g2), P, 0, P, 4, 1.0, P, 1, P, P, 1, P,
+                                           0, None, None, 0, None, None)
+    assert st == 2  # head_dim 96
+    st = lib.pkv_paged_decode_attn_planned(ctypes.byref(g3), P, 0, P, 4, 1.0, P, 100, P, P, 1,
+                                           P, 0, None, None, 0, None, None)
+    assert st == 4  # no workspace
     assert lib.pkv_selftest_wait_timeout(0, P, None) == 1  # no limit
     assert lib.pkv_selftest_wait_timeout(2 * 10**9, P, None) == 1  # over a second
     assert lib.pkv_selftest_wait_timeout(1000, None, None) == 1  # no error word

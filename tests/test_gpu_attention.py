@@ -117,6 +117,33 @@ def test_append_and_attention_match_oracle(name, out_fp32):
         assert worst < 1e-4, worst
 
 
+@pytest.mark.parametrize("name", list(CASES))
+def test_planned_calls_equal_per_call_plans(name):
+    """One decode_plan for the step, then the planned attention of every
+    layer, gives the same bits as each layer's call planning for itself
+    (the planned calls after the first rely on the merge resetting the unit
+    counter); two more rounds on one new plan give them again."""
+    batch, host, cache_bits, step = _run(CASES[name], True)
+    assert step.plan_once
+    planned = step.out.clone()
+    planned_lse = step.lse.clone()
+    step.plan_once = False
+    for l in range(host.layers):
+        step.attend(l)
+    torch.cuda.synchronize()
+    assert torch.equal(step.out.view(torch.int32), planned.view(torch.int32)), name
+    assert torch.equal(step.lse.view(torch.int32), planned_lse.view(torch.int32)), name
+    step.plan_once = True
+    step.plan()
+    for _ in range(2):  # the second round follows planned calls only
+        step.out.zero_()
+        for l in range(host.layers):
+            step.attend(l)
+    torch.cuda.synchronize()
+    assert torch.equal(step.out.view(torch.int32), planned.view(torch.int32)), name
+    assert int(step.err.item()) == 0
+
+
 def test_single_token_and_identical_keys_closed_forms():
     """n = 1 gives v itself; identical keys give the mean of V."""
     from paged_kv_decode_pages_gb300.step import DecodeStep
