@@ -599,9 +599,9 @@ def main(argv=None):
     total_ms = max_over_ranks(e0.elapsed_time(e1))
     barrier()
 
-    # ---- the attention kernels alone: every layer's planner + persistent
-    # kernel + merge captured as one graph, events around K replays (the
-    # roofline of the attention kernel) ------------------------------------
+    # ---- the attention kernels alone: the step's plan, then every layer's
+    # persistent kernel + merge, captured as one graph, events around K
+    # replays (the roofline of the attention kernel) ----------------------
     step.capture_attention()
     for _ in range(3):
         step.replay_attention()
@@ -628,7 +628,7 @@ def main(argv=None):
                   "value": world * sizes["step"] / (eager_ms / 1e3) / 1e9, "unit": "GB/s",
                   "attn_us_per_call": float(np.mean(attn_ms)) * 1e3,
                   "note": "kernel-by-kernel launches with an event pair around each "
-                          "attention call (these events keep the planner from overlapping "
+                          "attention call (these events keep the attention from overlapping "
                           "the KV append; on small layers the host's launch time shows)"}
     barrier()
 
@@ -772,8 +772,9 @@ def main(argv=None):
                  "timing": "graph of every layer's attention calls, %d replays" % args.steps},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": attn_traffic(cfg.name),
-                     "kernel": "pkv_paged_decode_attn (planner, persistent split kernel, merge "
-                               "kernel), per layer",
+                     "kernel": "pkv_paged_decode_attn_planned (persistent split kernel, "
+                               "merge kernel) per layer, with the step's pkv_decode_plan "
+                               "amortised over the layers",
                      "peak_source": peak_src},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
