@@ -95,3 +95,40 @@ def test_attention_only_graph_equals_eager():
     assert torch.equal(step.out, want_out)
     assert torch.equal(step.lse, want_lse)
     assert int(step.err.item()) == 0
+
+
+def test_graph_replans_when_lengths_change():
+    """The captured step holds its attention plan: a replay after the
+    lengths change (every active row 517 tokens shorter, so rows cross a
+    512-token split boundary) plans again and equals the eager step on the
+    new lengths."""
+    cfg = W.small_variant(W.CONFIGS["qwen2_0p5b"], n_active=9, ctx_hi=1500, layers=2)
+    batch = W.make_batch(cfg)
+    dev = W.Tensors(batch, device="cuda")
+    step = DecodeStep(batch, dev)
+    cache0 = dev.cache.clone()
+    steps0 = step.steps.clone()
+    step.capture()
+    first = None
+    new_lens = torch.where(step.active.bool(), torch.clamp(step.seq_lens - 517, min=1),
+                           step.seq_lens)
+    assert not torch.equal(new_lens, step.seq_lens)
+    for mode in ("before", "eager", "graph"):
+        dev.cache.copy_(cache0)
+        step.steps.copy_(steps0)
+        step.out.zero_()
+        if mode != "before":
+            step.seq_lens.copy_(new_lens)
+        if mode == "graph":
+            step.replay()
+        else:
+            step.run()
+        torch.cuda.synchronize()
+        if mode == "before":
+            first = _outputs(step)
+        elif mode == "eager":
+            want = _outputs(step)
+        else:
+            _same(want, _outputs(step))
+    assert not torch.equal(want["out"], first["out"])
+    assert int(want["err"].item()) == 0
