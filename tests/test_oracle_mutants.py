@@ -72,6 +72,12 @@ MUTANTS = [
      "        const int64_t pos = (int64_t)pos0 + i + 1;"),
     ("prefill keys of another request", "      const int32_t pg = page_table[(int64_t)b * max_pages + j / page_size];\n      const int64_t off = cache_offset(num_pages, page_size, num_kv_heads, D, layer,\n                                       pg, 0, j % page_size, g);",
      "      const int32_t pg = page_table[(int64_t)(b > 0 ? b - 1 : b) * max_pages + j / page_size];\n      const int64_t off = cache_offset(num_pages, page_size, num_kv_heads, D, layer,\n                                       pg, 0, j % page_size, g);"),
+    ("gumbel noise indexed by the sorted rank",
+     "double sc = ord[r].x + pkvo_gumbel(seed, salt, id, step);",
+     "double sc = ord[r].x + pkvo_gumbel(seed, salt, r, step);"),
+    ("gumbel counter words swapped",
+     "double sc = ord[r].x + pkvo_gumbel(seed, salt, id, step);",
+     "double sc = ord[r].x + pkvo_gumbel(seed, salt, step, id);"),
     ("penalty window from the oldest token",
      "pen[n_pen++] = history[(int64_t)s * hist_cap + (len - 1 - i) % hist_cap];",
      "pen[n_pen++] = history[(int64_t)s * hist_cap + i % hist_cap];"),
@@ -84,6 +90,9 @@ def _pins():
         ("philox", lambda: [TS.test_philox_matches_numpy_raw_words(k, c) for k, c in [
             ((12345, 7), (41, 3, 0, 0)), ((2**64 - 1, 2**63 + 5), (2**64 - 1, 2**64 - 1, 9, 0))]]),
         ("uniform", TS.test_uniform_uses_word0_and_is_strictly_inside_unit_interval),
+        ("exact draw", lambda: [TS.test_sampled_token_is_the_gumbel_argmax_of_numpy_philox_noise(v)
+                                for v in (6, 16)]),
+        ("batched draw", TS.test_batched_and_frame_draws_use_the_slot_step_and_call_salt),
         ("append", TA.test_append_writes_exactly_the_slot_and_nothing_else),
         ("sdpa", lambda: [TA.test_attention_matches_torch_sdpa_fp64(*a)
                           for a in [(4, 64, True), (3, 128, True)]]),

@@ -502,3 +502,94 @@ def test_seeded_sample_ext_history_ring_and_window():
     assert tok2[1] == 9
     assert list(steps) == [0, 1, 1]
     assert np.all(lproc == 0.0)  # greedy
+
+
+# ---------------------------------------------------------------------------
+# The exact draw: which token id and step each kept token's noise comes from
+# ---------------------------------------------------------------------------
+def _numpy_gumbel(seed, salt, token, step):
+    """Gumbel noise of (seed, salt, token, step) from numpy's own Philox4x64-10
+    (key = (seed, salt), counter = (token, step, 0, 0)), word 0 mapped to
+    u = (2 * (w >> 12) + 1) * 2^-53, then -log(-log u)."""
+    key = np.array([seed, salt], np.uint64)
+    ctr = np.array([token, step, 0, 0], np.uint64)
+    w = int(np.random.Philox(counter=_dec(ctr), key=key).random_raw(4)[0])
+    u = (2 * (w >> 12) + 1) * 2.0 ** -53
+    return -math.log(-math.log(u))
+
+
+def _expected_draw(x32, seed, salt, step, temp, top_k, top_p):
+    """Gumbel-max over the brute-force kept set, the noise of each kept token
+    drawn for its own id at the request's step; ties to the lowest id.
+    Returns (token, gap between the two best scores)."""
+    kept, _ = _brute_kept(x32, temp, top_k, top_p)
+    T = float(np.float32(temp))
+    scores = sorted(((float(x32[i]) / T + _numpy_gumbel(seed, salt, i, step), i) for i in kept),
+                    key=lambda si: (-si[0], si[1]))
+    gap = scores[0][0] - scores[1][0] if len(scores) > 1 else math.inf
+    return scores[0][1], gap
+
+
+@pytest.mark.parametrize("V", [6, 16])
+def test_sampled_token_is_the_gumbel_argmax_of_numpy_philox_noise(V):
+    """"Adding a Model", "How a program runs" (draws from per-request seeds)
+    and "2. The program" (a salt per sampling call): the token equals the
+    argmax of x_i + g(seed, salt, i, step) over the kept set, with g built
+    here from numpy's Philox words, for top-k / top-p on and off.  Noise
+    indexed by the sorted rank, or with step and token swapped in the
+    counter, picks another token on many of these draws."""
+    rng = np.random.default_rng(100 + V)
+    settings = [(1.0, 0, 1.0), (0.7, 4, 1.0), (1.3, 0, 0.8), (0.9, 5, 0.85)]
+    checked = 0
+    for trial in range(160):
+        x = rng.normal(0, 1.0, V).astype(np.float32)
+        temp, k, p = settings[trial % len(settings)]
+        seed = int(rng.integers(0, 2**63)) * (1 + trial % 2)
+        salt = int(rng.integers(0, 13))
+        step = int(rng.integers(0, 5000))
+        want, gap = _expected_draw(x, seed, salt, step, temp, k, p)
+        if gap < 1e-9:
+            continue  # an exact or last-ulp tie between two scores decides nothing
+        tok, _ = oracle.sample_row(x, seed, step, salt, temp, k, p)
+        assert tok == want, (trial, seed, salt, step, temp, k, p)
+        tok_ext, _ = oracle.sample_row_ext(x, seed, step, salt, temp, k, p, min_p=0.0,
+                                           rep_penalty=1.0, pen_tokens=[])
+        assert tok_ext == want
+        checked += 1
+    assert checked >= 150
+
+
+def test_batched_and_frame_draws_use_the_slot_step_and_call_salt():
+    """The batched sampler draws row b at its slot's step (before the
+    advance) with the call's salt; a frame's codebook j draws with salt 1 + j
+    at the frame's step: both against numpy-Philox noise."""
+    rng = np.random.default_rng(7)
+    V = 12
+    x = rng.normal(0, 1.0, (3, V)).astype(np.float32)
+    slots = np.array([2, 1, 3], np.int32)
+    active = np.ones(3, np.int32)
+    seeds = np.array([0, 91, 92, 93], np.uint64)
+    steps = np.array([0, 40, 7, 1234], np.int64)
+    T = np.full(4, 0.8, np.float32)
+    K = np.zeros(4, np.int32)
+    P = np.ones(4, np.float32)
+    before = steps.copy()
+    tok, _, _, bad = oracle.seeded_sample(x, slots, active, seeds, steps, T, K, P, salt=5,
+                                          advance=True)
+    assert bad == 0
+    for b in range(3):
+        s = slots[b]
+        want, gap = _expected_draw(x[b], int(seeds[s]), 5, int(before[s]), 0.8, 0, 1.0)
+        assert gap > 1e-9 and tok[b] == want
+    base = rng.normal(0, 1.0, (12, 3, V)).astype(np.float32)
+    steps2 = before.copy()
+    codes, _, _, bad = oracle.codebook_frame_sample(base, None, slots, active, seeds, steps2,
+                                                    T, K, P)
+    assert bad == 0
+    for b in range(3):
+        s = slots[b]
+        for j in range(12):
+            want, gap = _expected_draw(base[j, b], int(seeds[s]), 1 + j, int(before[s]), 0.8, 0,
+                                       1.0)
+            if gap > 1e-9:
+                assert codes[b, j] == want, (b, j)
