@@ -18,6 +18,13 @@ production launch; bit-identical to launching the kernels one by one);
 second graph (CUDA events around its replays), and a third pass launches
 the step's kernels one by one (reported under ``eager``).
 
+After the headline workload (long_context by default) the other decode
+configurations are measured the same way, with fewer phases, under
+``configs``; for each, the oracle runs beside the GPU on the path the bench
+times (one more replay of the step graph): ``cpu_baseline`` is its
+throughput on a bounded sample and ``parity`` the element-wise comparison,
+with the count of sampler near-ties.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
 
@@ -102,39 +109,54 @@ def attn_traffic(workload, source="decode_attn.cu"):
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class Clocks:
+    """nvidia-smi samples of the GPU's clocks and throttle reasons, taken every
+    100 ms while started; start() / pause() bracket each timed phase, and
+    summary() covers every phase sampled so far."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index):
+    def __init__(self, device_index, start=True):
         self.proc = None
-        self.dev = device_index
+        self.lines = []
+        self.phases = 0
         try:
             import torch
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         except Exception:
-            sel = str(device_index)
+            self.sel = str(device_index)
+        if start:
+            self.start()
+
+    def start(self):
+        if self.proc is not None:
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-i", sel, "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
-                text=True)
+                 "-i", self.sel, "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.phases += 1
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def pause(self):
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        self.lines.extend(out.strip().splitlines())
+        self.proc = None
+
+    def summary(self):
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in self.lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -149,7 +171,11 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "phases": self.phases}
+
+    def stop(self):
+        self.pause()
+        return self.summary()
 
 
 # ---------------------------------------------------------------------------
@@ -196,48 +222,124 @@ class OracleRunner:
                 W.bf16_bits(self.t.v[l]))
 
     def run_layer(self, inputs):
+        """One layer's append + attention; returns (seconds, out, lse)."""
         cb, q, k, v = inputs
         b = self.batch
         t0 = time.perf_counter()
         self.oracle.kv_append(cb, 0, k, v, self.pt, b.seq_lens, b.active)
-        self.oracle.paged_decode_attn(cb, 0, q, self.pt, b.seq_lens, b.active)
-        return time.perf_counter() - t0
+        out, lse, _ = self.oracle.paged_decode_attn(cb, 0, q, self.pt, b.seq_lens, b.active)
+        return time.perf_counter() - t0, out, lse
 
-    def run_sampler(self):
+    def run_sampler(self, steps=None):
+        """The sampler, then the frame, from the per-slot ``steps`` (default:
+        the batch's); returns (seconds, results)."""
         b = self.batch
         t0 = time.perf_counter()
-        steps = b.steps.copy()
+        steps = (b.steps if steps is None else steps).copy()
+        res = {}
         if self.logits is not None:
-            self.oracle.seeded_sample(self.logits, b.slots, b.active, b.seeds, steps,
-                                      b.temperature, b.top_k, b.top_p)
+            res["sample"] = self.oracle.seeded_sample(self.logits, b.slots, b.active, b.seeds,
+                                                      steps, b.temperature, b.top_k, b.top_p)
         if self.base is not None and self.ctrl is not None:
-            self.oracle.frame_sample(self.ctrl, b.cfg.ctrl_stop, self.base, self.fb, b.slots,
-                                     b.active, b.seeds, steps, b.temperature, b.top_k, b.top_p)
+            res["frame"] = self.oracle.frame_sample(self.ctrl, b.cfg.ctrl_stop, self.base,
+                                                    self.fb, b.slots, b.active, b.seeds, steps,
+                                                    b.temperature, b.top_k, b.top_p)
         elif self.base is not None:
-            self.oracle.codebook_frame_sample(self.base, self.fb, b.slots, b.active, b.seeds,
-                                              steps, b.temperature, b.top_k, b.top_p)
-        return time.perf_counter() - t0
+            res["frame"] = self.oracle.codebook_frame_sample(self.base, self.fb, b.slots,
+                                                             b.active, b.seeds, steps,
+                                                             b.temperature, b.top_k, b.top_p)
+        res["steps"] = steps
+        return time.perf_counter() - t0, res
 
 
-def cpu_baseline(batch, tensors, sizes, budget_s=12.0):
-    """The oracle on a bounded sample of the workload: whole layers (every
-    row) until about budget_s seconds of oracle compute, plus the sampler."""
+NEAR_TIE = 1e-6  # relative: the top two perturbed scores, or a top-p / min_p cut
+
+
+def oracle_check(batch, tensors, sizes, step, budget_s=12.0):
+    """The oracle beside the GPU on the path the bench times.  One more replay
+    of the captured step graph, then the oracle on the same inputs: whole
+    layers (every row; as many as fit in about budget_s seconds), the
+    sampler over every row and the frame.  Returns (cpu_baseline, parity):
+    the oracle's throughput on that sample, and the element-wise comparison
+    (attention max-abs / mean-abs, tokens that differ outside and at
+    near-ties, with the count of near-ties)."""
+    import numpy as np
+    import torch
     import oracle
+    steps_before = step.steps.cpu().numpy().copy()
+    step.out.fill_(float("nan"))
+    step.out_tok.fill_(-1)
+    if tensors.base is not None:
+        step.out_codes.fill_(-9)
+    step.replay()
+    torch.cuda.synchronize()
+    dev_err = int(step.err.item())
     r = OracleRunner(batch, tensors)
+    act = batch.active.astype(bool)
     L = batch.cfg.num_layers
     t_total, nbytes, layers = 0.0, 0.0, 0
+    amax, asum, acount, lmax = 0.0, 0.0, 0, 0.0
     for l in range(L):
-        t_total += r.run_layer(r.layer_inputs(l))
+        t, want, want_lse = r.run_layer(r.layer_inputs(l))
+        t_total += t
         nbytes += sizes["attn_per_layer"] + sizes["append_per_layer"]
+        got = step.out[l].float().cpu().numpy().astype(np.float64)[act]
+        e = np.abs(got - want[act])
+        amax = max(amax, float(e.max()))
+        asum += float(e.sum())
+        acount += e.size
+        gl = step.lse[l].cpu().numpy().astype(np.float64)[act]
+        lmax = max(lmax, float(np.abs(gl - want_lse[act]).max()))
         layers += 1
         if t_total >= budget_s:
             break
-    t_total += r.run_sampler()
+    ts, res = r.run_sampler(steps_before)
+    t_total += ts
     nbytes += sizes["logits"] + sizes["frame"]
-    return {"value": nbytes / t_total / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+    parity = {"path": "one replay of the captured step graph (the timed path), the slots' "
+                      "step counters as that replay read them",
+              "device_error_word": dev_err,
+              "attn": {"layers": layers, "of_layers": L, "rows": int(act.sum()),
+                       "max_abs": amax, "mean_abs": asum / max(acount, 1), "lse_max_abs": lmax,
+                       "tolerance": "max-abs 1e-2, mean-abs 1e-3, lse 1e-3",
+                       "ok": amax <= 1e-2 and asum / max(acount, 1) <= 1e-3 and lmax <= 1e-3}}
+    if "sample" in res:
+        tok, _, info, _ = res["sample"]
+        got_tok = step.out_tok.cpu().numpy()
+        near = ((info["top2_gap_rel"] < NEAR_TIE) | (info["member_margin"] < NEAR_TIE)) & act
+        mism = (got_tok != tok) & act
+        parity["tokens"] = {"rows": int(act.sum()), "mismatched": int(mism.sum()),
+                            "mismatched_outside_near_ties": int((mism & ~near).sum()),
+                            "near_ties": int(near.sum()),
+                            "near_tie_rule": "top two perturbed scores within 1e-6 relative, "
+                                             "or a top-p cut within 1e-6 of p*Z"}
+    if "frame" in res:
+        codes, _, finfo, _ = res["frame"]
+        got = step.out_codes.cpu().numpy()
+        n_near = diverge = bad = 0
+        for b in np.nonzero(act)[0]:
+            for j in range(got.shape[1]):
+                nt = finfo[b, j]
+                # samplings that ran in both (a stopped row's pad codes have none)
+                if got[b, j] == codes[b, j] and codes[b, j] < 0:
+                    continue
+                tie = nt["top2_gap_rel"] < NEAR_TIE or nt["member_margin"] < NEAR_TIE
+                n_near += int(tie)
+                if got[b, j] != codes[b, j]:
+                    diverge += 1
+                    bad += int(not tie)
+                    break  # after a near-tie the fed-back codes may legitimately part
+        parity["frame"] = {"rows": int(act.sum()), "samplings_per_row": int(got.shape[1]),
+                           "rows_diverging": diverge, "diverging_outside_near_ties": bad,
+                           "near_ties": n_near}
+        parity["steps_match"] = bool(np.array_equal(step.steps.cpu().numpy(), res["steps"]))
+    elif "sample" in res:
+        parity["steps_match"] = bool(np.array_equal(step.steps.cpu().numpy(), res["steps"]))
+    base = {"value": nbytes / t_total / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": "%d of %d layers (append + attention, all %d rows) + sampler%s, %.1f s"
                       % (layers, L, batch.B, " + frame" if sizes["frame"] else "", t_total)}
+    return base, parity
 
 
 # ---------------------------------------------------------------------------
@@ -495,6 +597,12 @@ def workload_config(cfg, batch, l2_note):
             "top_p": cfg.top_p, "n_codebooks": cfg.n_codebooks, "l2": l2_note}
 
 
+def l2_note(cfg, sizes):
+    """How the timed inputs relate to L2 (the same string in both arms)."""
+    return ("inputs larger than L2: %.1f GB of KV per step"
+            % (sizes["kv_per_layer"] * cfg.num_layers / 1e9))
+
+
 def run_reference(args, rank, world):
     """The oracle, as it stands, on the host cores: each step is one whole
     layer of the workload (rotating) plus the sampler."""
@@ -509,7 +617,7 @@ def run_reference(args, rank, world):
     L = cfg.num_layers
     tot, nbytes = 0.0, 0.0
     for i in range(args.warmup + args.steps):
-        t = r.run_layer(r.layer_inputs(i % L)) + r.run_sampler()
+        t = r.run_layer(r.layer_inputs(i % L))[0] + r.run_sampler()[0]
         if i >= args.warmup:
             tot += t
             nbytes += (sizes["attn_per_layer"] + sizes["append_per_layer"] + sizes["logits"]
@@ -521,7 +629,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(cfg, batch, "host memory"),
+            "config": workload_config(cfg, batch, l2_note(cfg, sizes)),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -539,6 +647,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--configs", default="qwen2_0p5b,llama3_3b,qwen3_4b_frame,tiny",
+                    help="further decode workloads measured after the headline one")
+    ap.add_argument("--config-cpu-budget", type=float, default=3.0)
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
@@ -553,11 +664,9 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args, rank, world)
 
-    import numpy as np
     import torch
     import torch.distributed as dist
     import paged_kv_decode_pages_gb300 as pkv
-    from paged_kv_decode_pages_gb300.step import DecodeStep
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
@@ -565,8 +674,48 @@ def main(argv=None):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     pkv.load()
+    clocks = Clocks(local, start=False)
+    line, step, rest = measure_decode(args.workload, args, rank, world, local, clocks, full=True)
+    lead = rank == 0 and world == 1
+    if lead and not args.no_cpu_baseline:
+        line["cpu_baseline"], line["parity"] = oracle_check(*rest, step, args.cpu_budget)
+    del step, rest
+    torch.cuda.empty_cache()
+    # the other configurations: kernel figures, a bounded oracle sample and
+    # parity each (on rank 0 at N = 1 the oracle legs; every rank times)
+    others = [c for c in args.configs.split(",") if c and c != args.workload]
+    if others:
+        line["configs"] = {}
+    for name in others:
+        sub, sub_step, sub_rest = measure_decode(name, args, rank, world, local, clocks,
+                                                 full=False)
+        if lead and not args.no_cpu_baseline:
+            sub["cpu_baseline"], sub["parity"] = oracle_check(*sub_rest, sub_step,
+                                                              args.config_cpu_budget)
+        line["configs"][name] = sub
+        del sub_step, sub_rest
+        torch.cuda.empty_cache()
+    line["clocks"] = clocks.summary()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
 
-    cfg, batch, tensors = make_workload(args.workload, "cuda")
+
+def measure_decode(name, args, rank, world, local, clocks, full):
+    """Times one decode workload.  Every configuration: the step as one
+    captured CUDA graph (args.steps replays), the attention calls of every
+    layer as a second graph (the roofline), the sampler alone and the frame
+    alone.  With full (the headline workload) also the kernel-by-kernel
+    pass, the extended sampler and the end-to-end run from pinned host
+    memory.  Returns (line, step, (batch, tensors, sizes)); clocks samples
+    every timed phase."""
+    import numpy as np
+    import torch
+    from paged_kv_decode_pages_gb300.step import DecodeStep
+
+    cfg, batch, tensors = make_workload(name, "cuda")
     sizes = step_bytes(batch, cfg, cfg.vocab, cfg.frame_vocab)
     step = DecodeStep(batch, tensors)
     stream = torch.cuda.current_stream()
@@ -577,6 +726,23 @@ def main(argv=None):
     def max_over_ranks(x):
         return rank_max(x, world, "cuda")
 
+    def timed(fn, n):
+        """n calls of fn between CUDA events on the launch stream, with the
+        clocks sampled; returns the max over ranks of the elapsed ms."""
+        barrier()
+        clocks.start()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        clocks.pause()
+        ms = max_over_ranks(e0.elapsed_time(e1))
+        barrier()
+        return ms
+
     for _ in range(args.warmup):
         step.run(stream)
     barrier()
@@ -586,18 +752,7 @@ def main(argv=None):
     step.capture()
     for _ in range(3):
         step.replay()
-    barrier()
-    clocks = Clocks(local)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step.replay()
-    e1.record(stream)
-    e1.synchronize()
-    clk = clocks.stop()
-    total_ms = max_over_ranks(e0.elapsed_time(e1))
-    barrier()
+    total_ms = timed(step.replay, args.steps)
 
     # ---- the attention kernels alone: the step's plan, then every layer's
     # persistent kernel + merge, captured as one graph, events around K
@@ -605,81 +760,85 @@ def main(argv=None):
     step.capture_attention()
     for _ in range(3):
         step.replay_attention()
-    barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        step.replay_attention()
-    e1.record(stream)
-    e1.synchronize()
-    attn_avg_s = max_over_ranks(e0.elapsed_time(e1)) / 1e3 / (args.steps * cfg.num_layers)
-    barrier()
+    attn_avg_s = timed(step.replay_attention, args.steps) / 1e3 / (args.steps * cfg.num_layers)
 
-    # ---- the same step launched kernel by kernel, with CUDA events around
-    # every attention call -------------------------------------------------
-    attn_ev = []
-    e0.record(stream)
-    for _ in range(args.steps):
-        step.run(stream, attn_events=attn_ev)
-    e1.record(stream)
-    e1.synchronize()
-    eager_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
-    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
-    eager_line = {"ms_per_step": eager_ms,
-                  "value": world * sizes["step"] / (eager_ms / 1e3) / 1e9, "unit": "GB/s",
-                  "attn_us_per_call": float(np.mean(attn_ms)) * 1e3,
-                  "note": "kernel-by-kernel launches with an event pair around each "
-                          "attention call (these events keep the attention from overlapping "
-                          "the KV append; on small layers the host's launch time shows)"}
-    barrier()
-
-    # ---- sampler alone (rows/s), same stream, after the timed step loop
-    s0 = torch.cuda.Event(enable_timing=True)
-    s1 = torch.cuda.Event(enable_timing=True)
+    # ---- sampler alone (rows/s) and frame alone -------------------------
     n_samp = 50
-    s0.record(stream)
-    for _ in range(n_samp):
-        step.sample(stream=stream)
-    s1.record(stream)
-    s1.synchronize()
-    sampler_us = s0.elapsed_time(s1) / n_samp * 1e3
-    barrier()
-
-    # ---- the sampler with min_p, repetition penalty and log-probs ------
-    ext_line = None
+    sampler_us = None
     if tensors.logits is not None:
-        ext_set = dict(min_p=0.05, rep_penalty=1.2, rep_window=-1, hist_cap=256)
-        step.enable_ext(**ext_set)
         for _ in range(3):
-            step.sample_ext(stream=stream)
-        s0.record(stream)
-        for _ in range(n_samp):
-            step.sample_ext(stream=stream)
-        s1.record(stream)
-        s1.synchronize()
-        ext_us = s0.elapsed_time(s1) / n_samp * 1e3
-        ext_line = {"us_per_call": ext_us, "rows_per_s": sizes["n_active"] / (ext_us / 1e6),
-                    "settings": dict(ext_set, logprobs="raw and processed")}
-        barrier()
-
-    # ---- the frame alone (frame workloads), same stream ----------------
+            step.sample(stream=stream)
+        sampler_us = timed(lambda: step.sample(stream=stream), n_samp) / n_samp * 1e3
     frame_line = None
     if tensors.base is not None:
-        f0 = torch.cuda.Event(enable_timing=True)
-        f1 = torch.cuda.Event(enable_timing=True)
-        n_frames = 50
-        f0.record(stream)
-        for _ in range(n_frames):
+        for _ in range(3):
             step.frame(stream=stream)
-        f1.record(stream)
-        f1.synchronize()
-        frame_us = f0.elapsed_time(f1) / n_frames * 1e3
+        frame_us = timed(lambda: step.frame(stream=stream), n_samp) / n_samp * 1e3
         n_cb = tensors.base.shape[0]
         frame_line = {"us_per_frame": frame_us,
                       "frames_per_s": sizes["n_active"] / (frame_us / 1e6),
                       "samplings_per_frame": n_cb + (1 if tensors.ctrl is not None else 0),
                       "codes_per_s": sizes["n_active"] * n_cb / (frame_us / 1e6)}
-        barrier()
 
+    ms_per_step = total_ms / args.steps
+    achieved = sizes["attn_per_layer"] / attn_avg_s / 1e9
+    peak, peak_src = peaks()
+    line = {
+        "metric": METRIC,
+        "value": replicas_throughput(sizes["step"] * args.steps, world, total_ms) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "compute": "bf16 in, fp32 accumulate (attention); sampler decisions in fp64, "
+                   "chunk normalisers in double-float fp32 pairs",
+        "data": "synthetic",
+        "config": workload_config(cfg, batch, l2_note(cfg, sizes)),
+        "sampled_rows_per_s": world * sizes["n_active"] * args.steps / (total_ms / 1e3),
+        "launch": "one captured CUDA graph per step (%d kernels)" % step.launches_per_step(),
+        "attn": {"us_per_layer": attn_avg_s * 1e6, "gbs": achieved,
+                 "bytes_per_layer": sizes["attn_per_layer"],
+                 "timing": "graph of every layer's attention calls, %d replays" % args.steps},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": attn_traffic(cfg.name),
+                     "kernel": "pkv_paged_decode_attn_planned (persistent split kernel, "
+                               "merge kernel) per layer, with the step's pkv_decode_plan "
+                               "amortised over the layers",
+                     "peak_source": peak_src},
+        "gpu_launches": args.steps * step.launches_per_step(),
+    }
+    if sampler_us is not None:
+        line["sampler"] = {"us_per_call": sampler_us,
+                           "rows_per_s": sizes["n_active"] / (sampler_us / 1e6),
+                           "gbs": sizes["logits"] / (sampler_us / 1e6) / 1e9,
+                           "frac": sizes["logits"] / (sampler_us / 1e6) / 1e9 / peak}
+    if frame_line:
+        line["frame"] = frame_line
+    if not full:
+        return line, step, (batch, tensors, sizes)
+
+    # ---- the same step launched kernel by kernel, with CUDA events around
+    # every attention call -------------------------------------------------
+    attn_ev = []
+    eager_ms = timed(lambda: step.run(stream, attn_events=attn_ev), args.steps) / args.steps
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    line["eager"] = {"ms_per_step": eager_ms,
+                     "value": world * sizes["step"] / (eager_ms / 1e3) / 1e9, "unit": "GB/s",
+                     "attn_us_per_call": float(np.mean(attn_ms)) * 1e3,
+                     "note": "kernel-by-kernel launches with an event pair around each "
+                             "attention call (these events keep the attention from "
+                             "overlapping the KV append; on small layers the host's launch "
+                             "time shows)"}
+
+    # ---- the sampler with min_p, repetition penalty and log-probs ------
+    if tensors.logits is not None:
+        ext_set = dict(min_p=0.05, rep_penalty=1.2, rep_window=-1, hist_cap=256)
+        step.enable_ext(**ext_set)
+        for _ in range(3):
+            step.sample_ext(stream=stream)
+        ext_us = timed(lambda: step.sample_ext(stream=stream), n_samp) / n_samp * 1e3
+        line["sampler_ext"] = {"us_per_call": ext_us,
+                               "rows_per_s": sizes["n_active"] / (ext_us / 1e6),
+                               "settings": dict(ext_set, logprobs="raw and processed")}
 
     # ---- end to end: host (pinned) inputs in, tokens out, every step ----
     # Two copies of the step's input buffers (the KV cache is shared), each
@@ -690,9 +849,9 @@ def main(argv=None):
     from paged_kv_decode_pages_gb300 import workloads as W
     tensors2 = W.Tensors.__new__(W.Tensors)
     tensors2.layers, tensors2.cache = tensors.layers, tensors.cache
-    for name in ("q", "k", "v", "logits", "base", "fb", "ctrl"):
-        t = getattr(tensors, name, None)
-        setattr(tensors2, name, None if t is None else (t if name == "fb" else t.clone()))
+    for nm in ("q", "k", "v", "logits", "base", "fb", "ctrl"):
+        t = getattr(tensors, nm, None)
+        setattr(tensors2, nm, None if t is None else (t if nm == "fb" else t.clone()))
     step2 = DecodeStep(batch, tensors2)
     step2.run(stream)
     step2.capture()
@@ -703,9 +862,9 @@ def main(argv=None):
                (st_.page_table, step.page_table.cpu().pin_memory()),
                (st_.seq_lens, step.seq_lens.cpu().pin_memory()),
                (st_.active, step.active.cpu().pin_memory())]
-        for name in ("logits", "base", "ctrl"):
-            if getattr(tn, name, None) is not None:
-                ins.append((getattr(tn, name), getattr(tensors, name).cpu().pin_memory()))
+        for nm in ("logits", "base", "ctrl"):
+            if getattr(tn, nm, None) is not None:
+                ins.append((getattr(tn, nm), getattr(tensors, nm).cpu().pin_memory()))
         outs = [st_.out_tok, st_.out_kind] + ([st_.out_codes] if tn.base is not None else [])
         sets.append((st_, ins, outs))
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in sets[0][2]]
@@ -715,15 +874,9 @@ def main(argv=None):
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     done = [torch.cuda.Event(), torch.cuda.Event()]
     started = torch.cuda.Event()
-    barrier()
-    x0 = torch.cuda.Event(enable_timing=True)
-    x1 = torch.cuda.Event(enable_timing=True)
-    x0.record(stream)
-    started.record(stream)
-    copy_stream.wait_event(started)
 
     def copy_in(i):
-        st_, ins, _ = sets[i % 2]
+        _, ins, _ = sets[i % 2]
         with torch.cuda.stream(copy_stream):
             if i >= 2:
                 copy_stream.wait_event(done[i % 2])  # the set's previous step has finished
@@ -731,8 +884,14 @@ def main(argv=None):
                 d.copy_(h, non_blocking=True)
             copied[i % 2].record(copy_stream)
 
-    copy_in(0)
-    for i in range(args.steps):
+    state = {"i": 0}
+
+    def e2e_step():
+        i = state["i"]
+        if i == 0:
+            started.record(stream)
+            copy_stream.wait_event(started)
+            copy_in(0)
         if i + 1 < args.steps:
             copy_in(i + 1)
         st_, _, outs = sets[i % 2]
@@ -741,53 +900,14 @@ def main(argv=None):
         for d, h in zip(outs, host_out):
             h.copy_(d, non_blocking=True)
         done[i % 2].record(stream)
-    x1.record(stream)
-    x1.synchronize()
-    e2e_ms = max_over_ranks(x0.elapsed_time(x1))
-    barrier()
+        state["i"] = i + 1
 
-    ms_per_step = total_ms / args.steps
-    value = replicas_throughput(sizes["step"] * args.steps, world, total_ms) / 1e9
-    e2e_value = replicas_throughput(sizes["step"] * args.steps, world, e2e_ms) / 1e9
-    achieved = sizes["attn_per_layer"] / attn_avg_s / 1e9
-    peak, peak_src = peaks()
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "compute": "bf16 in, fp32 accumulate (attention); sampler decisions in fp64, "
-                   "chunk normalisers in double-float fp32 pairs",
-        "data": "synthetic",
-        "config": workload_config(cfg, batch, "inputs larger than L2: %.1f GB of KV per step"
-                                  % (sizes["kv_per_layer"] * cfg.num_layers / 1e9)),
-        "sampled_rows_per_s": world * sizes["n_active"] * args.steps / (total_ms / 1e3),
-        "sampler": {"us_per_call": sampler_us,
-                    "rows_per_s": sizes["n_active"] / (sampler_us / 1e6)},
-        "launch": "one captured CUDA graph per step (%d kernels)" % step.launches_per_step(),
-        "eager": eager_line,
-        **({"sampler_ext": ext_line} if ext_line else {}),
-        **({"frame": frame_line} if frame_line else {}),
-        "attn": {"us_per_layer": attn_avg_s * 1e6, "gbs": achieved,
-                 "bytes_per_layer": sizes["attn_per_layer"],
-                 "timing": "graph of every layer's attention calls, %d replays" % args.steps},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": attn_traffic(cfg.name),
-                     "kernel": "pkv_paged_decode_attn_planned (persistent split kernel, "
-                               "merge kernel) per layer, with the step's pkv_decode_plan "
-                               "amortised over the layers",
-                     "peak_source": peak_src},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": args.steps * step.launches_per_step(),
-        "clocks": clk,
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(batch, tensors, sizes, args.cpu_budget)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
-    return 0
+    e2e_ms = timed(e2e_step, args.steps)
+    line["e2e"] = {"value": replicas_throughput(sizes["step"] * args.steps, world, e2e_ms) / 1e9,
+                   "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "ms_per_step": e2e_ms / args.steps}
+    del step2, tensors2, sets
+    return line, step, (batch, tensors, sizes)
 
 
 if __name__ == "__main__":

@@ -187,16 +187,19 @@ int pkv_paged_decode_attn(const pkv_cache_t *geom, const void *cache,
  * library holds it until the process exits).  It allocates and frees
  * nothing.
  *
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress with that device current) and remembers it;
- *     make that first call before any stream capture begins.
- *   - Problems whose pkv_decode_workspace_bytes(...) exceeds
- *     PKV_ATTN_STATIC_SCRATCH_BYTES are rejected with PKV_ERR_WORKSPACE
+ *   - The first call in each CUDA context (normally once per device; again
+ *     after cudaDeviceReset makes a new one) looks up the array's device
+ *     address (cudaGetSymbolAddress with that device current) and remembers
+ *     it; host threads share that lookup safely.  Make the first call on a
+ *     device before any stream capture begins.
+ *   - Arguments are checked first, exactly as for pkv_paged_decode_attn;
+ *     then problems whose pkv_decode_workspace_bytes(...) exceeds
+ *     PKV_ATTN_STATIC_SCRATCH_BYTES are rejected with PKV_ERR_WORKSPACE,
  *     before anything is launched.
  *   - All calls share the one array, which keeps the last call's contents
  *     (nothing in it needs to start at zero): calls that can overlap on the
  *     GPU (other streams, other host threads) race on it; serialise them.
- * Results are those of pkv_paged_decode_attn on the same inputs.
+ * Results are bit-identical to pkv_paged_decode_attn on the same inputs.
  * ---------------------------------------------------------------------- */
 #define PKV_ATTN_STATIC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
 
@@ -232,7 +235,12 @@ int pkv_paged_decode_attn_static(const pkv_cache_t *geom, const void *cache,
  * of planned calls may follow one plan; each leaves the plan ready for the
  * next.  Results are bit-identical to pkv_paged_decode_attn on the same
  * inputs.  A row that pkv_decode_plan reported as malformed
- * (PKV_DEV_ERR_SEQ_LEN) is reported by the plan only, once per step.
+ * (PKV_DEV_ERR_SEQ_LEN) is reported by the plan only, once per step.  If a
+ * row's length changes after the plan so that a planned unit no longer lies
+ * inside it (or inside max_pages), the planned call reads nothing for that
+ * unit, writes no partial for it and reports PKV_DEV_ERR_SEQ_LEN; that row's
+ * output is then undefined, and nothing outside the call's buffers is read
+ * or written.
  * Errors: as for pkv_paged_decode_attn.
  * ---------------------------------------------------------------------- */
 int pkv_decode_plan(const pkv_cache_t *geom, int num_qo_heads, int max_pages,

@@ -45,6 +45,10 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+#include <mutex>
+#include <utility>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -222,6 +226,7 @@ struct Unit {
   int valid;
   int b, split, g, h0, nh;
   int n, p_begin, p_count;
+  int bad;  // the row's length disagrees with the plan: skipped, reported
 };
 
 constexpr int ATTN_SMEM_ROWS = 512;  // rows whose split table lives in shared memory
@@ -238,7 +243,7 @@ __device__ __forceinline__ Unit decode_unit(const AttnArgs &a, int u, int gp, in
   Unit U;
   const int HB = a.num_kv_heads * a.qblocks;
   U.valid = u < total_units;
-  U.b = U.split = U.g = U.h0 = U.nh = U.n = U.p_begin = U.p_count = 0;
+  U.b = U.split = U.g = U.h0 = U.nh = U.n = U.p_begin = U.p_count = U.bad = 0;
   if (!U.valid) return U;
   const int su = u / HB, hb = u % HB;
   if (su < full) {
@@ -263,10 +268,20 @@ __device__ __forceinline__ Unit decode_unit(const AttnArgs &a, int u, int gp, in
   U.h0 = U.g * a.group + qb * gp;
   U.nh = min(gp, a.group - qb * gp);
   U.n = seq[U.b];
-  const int npages = (U.n + ATTN_PAGE - 1) / ATTN_PAGE;
+  const bool n_ok = U.n >= 1 && (int64_t)U.n <= a.max_tokens;
+  const int npages = n_ok ? (U.n + ATTN_PAGE - 1) / ATTN_PAGE : 0;
   if (U.split < 0) U.split = npages / ATTN_PAGES_PER_SPLIT;
   U.p_begin = U.split * ATTN_PAGES_PER_SPLIT;
   U.p_count = min(npages - U.p_begin, ATTN_PAGES_PER_SPLIT);
+  U.bad = 0;
+  if (U.p_count <= 0 || U.split >= a.nsplit_max) {
+    // the row's length no longer matches the plan the unit came from (it
+    // changed after pkv_decode_plan): no blocks are read and no partial is
+    // written for it
+    U.bad = 1;
+    U.p_count = 0;
+    report(a.err, PKV_DEV_ERR_SEQ_LEN);
+  }
   return U;
 }
 
@@ -364,7 +379,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
     if (lane < cnt) {
       const int blk = U.p_begin + warp + lane * ATTN_WARPS;
       const int pg = a.bpp == 1 ? blk : blk / a.bpp;
-      pid = __ldg(a.page_table + (int64_t)U.b * a.max_pages + pg);
+      // the unit's blocks lie inside the row's page-table row (decode_unit
+      // checked the length); the clamp keeps the read there regardless
+      pid = __ldg(a.page_table + (int64_t)U.b * a.max_pages + min(pg, a.max_pages - 1));
       if (pid < 0 || pid >= a.num_pages) {
         report(a.err, PKV_DEV_ERR_PAGE);
         pid = 0;
@@ -645,7 +662,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
 
     // ---- merge the 4 warps into the split's partial (m, l, o) ----------
     const int64_t bh0 = (int64_t)cur.b * Hq + cur.h0;
-    for (int idx = tid; idx < cur.nh * D; idx += ATTN_THREADS) {
+    for (int idx = tid; idx < (cur.bad ? 0 : cur.nh * D); idx += ATTN_THREADS) {
       const int h = idx / D, d = idx % D;
       float M = ATTN_NEG;
 #pragma unroll
@@ -799,10 +816,12 @@ static int launch_attn(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t 
                        AttnMode mode) {
   using S = AttnShape<D, GP, NS>;
   auto kern = attn_persistent_kernel<D, GP, NS>;
-  static int grid_for_device[64] = {0};  // persistent grid per device (0: not known yet)
+  // persistent grid per device (0: not known yet); host threads may race to
+  // fill a slot, and all write the same value
+  static std::atomic<int> grid_for_device[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  int &grid = grid_for_device[dev & 63];
+  int grid = grid_for_device[dev & 63].load(std::memory_order_acquire);
   if (grid == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES) !=
         cudaSuccess)
@@ -815,6 +834,7 @@ static int launch_attn(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t 
       return PKV_ERR_CUDA;
     if (per_sm < 1) return PKV_ERR_UNSUPPORTED;
     grid = sms * per_sm;
+    grid_for_device[dev & 63].store(grid, std::memory_order_release);
   }
   if (mode != ATTN_RUN_ONLY &&
       launch_pdl(attn_plan_kernel, dim3(1), dim3(PLAN_THREADS), 0, st, a) != cudaSuccess)
@@ -844,15 +864,15 @@ static int dispatch_gp(const AttnArgs &a, const CUtensorMap &tmap, cudaStream_t 
 // The driver's tensor-map encoder, fetched once through the runtime (no
 // link-time dependency on libcuda).
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -907,14 +927,14 @@ extern "C" size_t pkv_decode_workspace_bytes(int batch, int num_qo_heads, int he
 
 namespace pkv {
 
-// Checks a call's arguments and fills the kernels' arguments.  With
-// plan_only the call has no cache, q or output (the planner reads none).
-static int attn_setup(const pkv_cache_t *geom, const void *cache, int layer, const void *q,
+// Checks a call's arguments other than the workspace; *ws_need gets the
+// workspace bytes the call needs.  With plan_only the call has no cache, q
+// or output (the planner reads none).
+static int attn_check(const pkv_cache_t *geom, const void *cache, int layer, const void *q,
                       int num_qo_heads, float sm_scale, const int32_t *page_table, int max_pages,
-                      const int32_t *seq_lens, const int32_t *active, int batch, void *out,
-                      int out_fp32, float *lse, void *workspace, size_t workspace_bytes,
-                      int32_t *err_word, bool plan_only, AttnArgs *pa, CUtensorMap *tmap) {
-  int st = check_geometry(geom);
+                      const int32_t *seq_lens, const int32_t *active, int batch, const void *out,
+                      bool plan_only, size_t *ws_need) {
+  const int st = check_geometry(geom);
   if (st != PKV_OK) return st;
   if (!seq_lens || !active) return PKV_ERR_INVALID_ARG;
   if (!plan_only && (!cache || !q || !page_table || !out)) return PKV_ERR_INVALID_ARG;
@@ -933,10 +953,27 @@ static int attn_setup(const pkv_cache_t *geom, const void *cache, int layer, con
       (int64_t)geom->num_pages * (geom->page_size / ATTN_PAGE) > INT32_MAX)
     return PKV_ERR_UNSUPPORTED;
   if (!plan_only && (!aligned16(cache) || !aligned16(q))) return PKV_ERR_INVALID_ARG;
-  const WsLayout wl = ws_layout(batch, num_qo_heads, D, max_tokens);
-  if (workspace == nullptr || workspace_bytes < wl.total) return PKV_ERR_WORKSPACE;
-  if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
   if ((int64_t)geom->num_layers * geom->num_pages > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  *ws_need = ws_layout(batch, num_qo_heads, D, max_tokens).total;
+  return PKV_OK;
+}
+
+// Checks a call's arguments and fills the kernels' arguments.
+static int attn_setup(const pkv_cache_t *geom, const void *cache, int layer, const void *q,
+                      int num_qo_heads, float sm_scale, const int32_t *page_table, int max_pages,
+                      const int32_t *seq_lens, const int32_t *active, int batch, void *out,
+                      int out_fp32, float *lse, void *workspace, size_t workspace_bytes,
+                      int32_t *err_word, bool plan_only, AttnArgs *pa, CUtensorMap *tmap) {
+  size_t need = 0;
+  int st = attn_check(geom, cache, layer, q, num_qo_heads, sm_scale, page_table, max_pages,
+                      seq_lens, active, batch, out, plan_only, &need);
+  if (st != PKV_OK) return st;
+  if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return PKV_ERR_INVALID_ARG;
+  const int D = geom->head_dim;
+  const int group = num_qo_heads / geom->num_kv_heads;
+  const int64_t max_tokens = (int64_t)max_pages * geom->page_size;
+  const WsLayout wl = ws_layout(batch, num_qo_heads, D, max_tokens);
 
   AttnArgs &a = *pa;
   const int64_t row_bytes = (int64_t)D * 2;
@@ -1042,22 +1079,66 @@ namespace pkv {
 // partial is written before it is read.
 static __device__ __align__(256) unsigned char g_attn_scratch[PKV_ATTN_STATIC_SCRATCH_BYTES];
 
-constexpr int MAX_DEVICES = 64;
-static void *g_scratch_addr[MAX_DEVICES];  // device address of g_attn_scratch, per device
+// Device address of the array in each CUDA context that has used it.  The
+// host-side name is only a stand-in for that address, and a context that is
+// destroyed and made again (cudaDeviceReset) loads the module anew, possibly
+// at another address: the cache is keyed by the driver's context id, which
+// is never reused within a process.  Host threads share it under a mutex.
+struct ScratchAddr {
+  unsigned long long ctx_id;
+  void *ptr;
+};
+constexpr int SCRATCH_CTX_SLOTS = 64;
+static std::mutex g_scratch_mu;
+static ScratchAddr g_scratch_addr[SCRATCH_CTX_SLOTS];
+static int g_scratch_used = 0;
 
-// Device address of the array on the current device, looked up once per
-// device (the host-side name is only a stand-in for it).
+static int current_context_id(unsigned long long *id) {
+  static const auto fns = []() {
+    std::pair<PFN_cuCtxGetCurrent_v4000, PFN_cuCtxGetId_v12000> f{nullptr, nullptr};
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.first = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.second = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    return f;
+  }();
+  if (fns.first == nullptr || fns.second == nullptr) return PKV_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (fns.first(&ctx) != CUDA_SUCCESS || ctx == nullptr) return PKV_ERR_CUDA;
+  return fns.second(ctx, id) == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Device address of the array in the current context (the current device's
+// context), looked up with cudaGetSymbolAddress the first time a context
+// uses it.
 static int static_scratch_address(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 0 || dev >= MAX_DEVICES) return PKV_ERR_UNSUPPORTED;
-  if (g_scratch_addr[dev] == nullptr) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || ptr == nullptr)
-      return PKV_ERR_CUDA;
-    g_scratch_addr[dev] = ptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  unsigned long long id = 0;
+  if (current_context_id(&id) == PKV_OK) {
+    for (int i = 0; i < g_scratch_used; ++i)
+      if (g_scratch_addr[i].ctx_id == id) {
+        *out = g_scratch_addr[i].ptr;
+        return PKV_OK;
+      }
   }
-  *out = g_scratch_addr[dev];
+  // first use in this context: the lookup also makes the runtime's context
+  // of the device current if no call has done so yet
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || ptr == nullptr)
+    return PKV_ERR_CUDA;
+  if (current_context_id(&id) != PKV_OK) return PKV_ERR_CUDA;
+  const int slot = g_scratch_used < SCRATCH_CTX_SLOTS ? g_scratch_used++
+                                                      : (int)(id % SCRATCH_CTX_SLOTS);
+  g_scratch_addr[slot] = ScratchAddr{id, ptr};
+  *out = ptr;
   return PKV_OK;
 }
 
@@ -1070,13 +1151,15 @@ extern "C" int pkv_paged_decode_attn_static(const pkv_cache_t *geom, const void 
                                             int batch, void *out, int out_fp32, float *lse,
                                             int32_t *err_word, void *stream) {
   using namespace pkv;
-  if (geom == nullptr) return PKV_ERR_INVALID_ARG;
-  const size_t need =
-      pkv_decode_workspace_bytes(batch, num_qo_heads, geom->head_dim, max_pages, geom->page_size);
-  if (need == 0) return PKV_ERR_INVALID_ARG;
+  // every argument check first, so that the status names what is wrong with
+  // the call whatever its size; then the size against the array
+  size_t need = 0;
+  int st = attn_check(geom, cache, layer, q, num_qo_heads, sm_scale, page_table, max_pages,
+                      seq_lens, active, batch, out, false, &need);
+  if (st != PKV_OK) return st;
   if (need > (size_t)PKV_ATTN_STATIC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;
   void *scratch = nullptr;
-  const int st = static_scratch_address(&scratch);
+  st = static_scratch_address(&scratch);
   if (st != PKV_OK) return st;
   return pkv_paged_decode_attn(geom, cache, layer, q, num_qo_heads, sm_scale, page_table,
                                max_pages, seq_lens, active, batch, out, out_fp32, lse, scratch,

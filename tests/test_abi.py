@@ -86,6 +86,21 @@ def test_host_validation_rejects_before_launch(lib):
     st = lib.pkv_paged_decode_attn_planned(ctypes.byref(g3), P, 0, P, 4, 1.0, P, 100, P, P, 1,
                                            P, 0, None, None, 0, None, None)
     assert st == 4  # no workspace
+    # the static-scratch form: argument errors are named whatever the size,
+    # and an oversized problem is refused before any CUDA call
+    big = 1 << 20  # max_pages: far more scratch than the library's array
+    st = lib.pkv_paged_decode_attn_static(ctypes.byref(g2), P, 0, P, 4, 1.0, P, big, P, P, 64, P,
+                                          0, None, None, None)
+    assert st == 2  # head_dim 96, not "workspace too small"
+    st = lib.pkv_paged_decode_attn_static(ctypes.byref(g3), P, 0, P, 3, 1.0, P, big, P, P, 64, P,
+                                          0, None, None, None)
+    assert st == 1  # 3 q heads over 2 kv heads
+    st = lib.pkv_paged_decode_attn_static(ctypes.byref(g3), P, 0, None, 4, 1.0, P, big, P, P, 64,
+                                          P, 0, None, None, None)
+    assert st == 1  # no q
+    st = lib.pkv_paged_decode_attn_static(ctypes.byref(g3), P, 0, P, 4, 1.0, P, big, P, P, 64, P,
+                                          0, None, None, None)
+    assert st == 4  # well-formed, larger than the array
     assert lib.pkv_selftest_wait_timeout(0, P, None) == 1  # no limit
     assert lib.pkv_selftest_wait_timeout(2 * 10**9, P, None) == 1  # over a second
     assert lib.pkv_selftest_wait_timeout(1000, None, None) == 1  # no error word

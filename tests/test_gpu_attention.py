@@ -206,3 +206,60 @@ def test_bad_inputs_set_error_bits_and_spare_other_rows():
     # the append wrote nothing for rows 1 (bad page) and 2 (bad length)
     got_cache = W.bf16_bits(step.t.cache)
     np.testing.assert_array_equal(got_cache[:, 1:], cache_bits[:, 1:])
+
+
+def test_planned_call_on_lengths_changed_after_the_plan_is_reported_and_stays_in_bounds():
+    """The planned attention trusts the caller to keep the lengths of the
+    plan.  When they change after pkv_decode_plan (row 0 past max_pages, row
+    1 exactly max_pages so that its planned last split lies past the end, row
+    2 shorter), the call reports PKV_DEV_ERR_SEQ_LEN, writes nothing outside
+    its workspace and outputs, and the next plan on correct lengths gives the
+    per-call result again."""
+    import paged_kv_decode_pages_gb300 as pkv
+    cfg = W.Config(name="replan", index=17, num_layers=1, num_qo_heads=8, num_kv_heads=2,
+                   head_dim=128, page_size=16, n_active=3, n_pad=1, ctx=(100, 700, 40))
+    batch = W.make_batch(cfg, max_pages=64)  # max_tokens 1024: two splits at most
+    host = W.Tensors(batch, device="cpu", with_logits=False, with_frame=False)
+    cache, q = host.cache.cuda(), host.q[0].cuda()
+    pt = torch.from_numpy(batch.page_table).cuda()
+    seq = torch.from_numpy(batch.seq_lens).cuda()
+    act = torch.from_numpy(batch.active).cuda()
+    B, Hq, D = batch.B, cfg.num_qo_heads, cfg.head_dim
+    need = pkv.decode_workspace_bytes(B, Hq, D, batch.max_pages)
+    guard = 4096
+    ws_full = torch.zeros(need + guard, dtype=torch.uint8, device="cuda")
+    ws = ws_full[:need]
+    ws_full[need:] = 0x5A
+    out = torch.zeros((B, Hq, D), dtype=torch.float32, device="cuda")
+    lse = torch.zeros((B, Hq), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache_before = cache.clone()
+
+    pkv.decode_plan(cache, Hq, batch.max_pages, seq, act, ws, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    seq_changed = seq.clone()
+    seq_changed[0] = batch.max_pages * 16 + 5
+    seq_changed[1] = batch.max_pages * 16
+    seq_changed[2] = 30
+    pkv.paged_decode_attn_planned(cache, 0, q, pt, seq_changed, act, out, ws, lse=lse,
+                                  err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 0x2  # PKV_DEV_ERR_SEQ_LEN
+    assert torch.all(ws_full[need:] == 0x5A)
+    assert torch.equal(cache, cache_before)
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))  # past max_pages
+    assert torch.all(out[3] == 0)  # the padding row
+
+    # a new plan on the original lengths: planned = per-call, bit for bit
+    err.zero_()
+    pkv.decode_plan(cache, Hq, batch.max_pages, seq, act, ws, err_word=err)
+    pkv.paged_decode_attn_planned(cache, 0, q, pt, seq, act, out, ws, lse=lse, err_word=err)
+    want = torch.empty_like(out)
+    want_lse = torch.empty_like(lse)
+    pkv.paged_decode_attn(cache, 0, q, pt, seq, act, want, ws, lse=want_lse, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out.view(torch.int32), want.view(torch.int32))
+    assert torch.equal(lse.view(torch.int32), want_lse.view(torch.int32))
+    assert torch.all(ws_full[need:] == 0x5A)

@@ -1,8 +1,11 @@
 """Full-size parity: each configuration's whole step (every layer's append and
-attention, the sampler, the frame loop) runs at its full size in the launch
-configuration bench.py times; the oracle then recomputes sampled outputs
-one by one (two rows at the first and last layer) from the inputs drawn
-before the step ran, plus every row of the sampler."""
+attention, the sampler, the frame loop) runs at its full size, launched
+call by call and as the one captured CUDA graph that bench.py replays (the
+step's single attention plan, then every layer); the oracle then recomputes
+sampled outputs one by one (two rows at the first and last layer) from the
+inputs drawn before the step ran, plus every row of the sampler and the
+frame.  The graph of the attention calls alone, which bench.py times for the
+roofline, is checked the same way."""
 import numpy as np
 import pytest
 import torch
@@ -29,36 +32,17 @@ def _snapshot(dev, batch, layer, b):
     return W.bf16_bits(compact), pt
 
 
-@pytest.mark.parametrize("name", ["qwen2_0p5b", "llama3_3b", "qwen3_4b_frame", "long_context",
-                                  "long_context_p128"])
-def test_full_size_step_sampled_rows(name):
-    cfg = W.CONFIGS[name]
-    batch = W.make_batch(cfg)
-    dev = W.Tensors(batch, device="cuda")
-    L = cfg.num_layers
-    rows = [0, cfg.n_active - 1]
-    layers = [0, L - 1]
-    snaps = {(l, b): _snapshot(dev, batch, l, b) for l in layers for b in rows}
-    logits = dev.logits.cpu().numpy()
-    base = None if dev.base is None else dev.base.cpu().numpy()
-    fb = None if dev.fb is None else dev.fb.cpu().numpy()
-    ctrl = None if dev.ctrl is None else dev.ctrl.cpu().numpy()
-    qkv = {(l, b): (W.bf16_bits(dev.q[l, b:b + 1]), W.bf16_bits(dev.k[l, b:b + 1]),
-                    W.bf16_bits(dev.v[l, b:b + 1])) for l in layers for b in rows}
-    steps0 = batch.steps.copy()
-
-    step = DecodeStep(batch, dev)
-    step.run()
-    torch.cuda.synchronize()
-    assert int(step.err.item()) == 0
-
+def _check_attention(name, cfg, batch, step, snaps, qkv):
+    """The sampled (layer, row) outputs of step.out / step.lse against the
+    oracle; returns the worst max-abs error."""
     worst = 0.0
     for (l, b), (cbits, pt) in snaps.items():
         q, k, v = qkv[(l, b)]
         sl = batch.seq_lens[b:b + 1]
         one = np.ones(1, np.int32)
-        assert oracle.kv_append(cbits, 0, k, v, pt, sl, one) == 0
-        want, want_lse, bad = oracle.paged_decode_attn(cbits, 0, q, pt, sl, one)
+        cb = cbits.copy()
+        assert oracle.kv_append(cb, 0, k, v, pt, sl, one) == 0
+        want, want_lse, bad = oracle.paged_decode_attn(cb, 0, q, pt, sl, one)
         assert bad == 0
         got = step.out[l, b].float().cpu().numpy().astype(np.float64)
         err = np.abs(got - want[0])
@@ -76,6 +60,57 @@ def test_full_size_step_sampled_rows(name):
     pad = batch.active == 0
     if pad.any():
         assert torch.all(step.out[:, torch.from_numpy(pad)] == 0)
+    return worst
+
+
+@pytest.mark.parametrize("mode", ["eager", "graph"])
+@pytest.mark.parametrize("name", ["qwen2_0p5b", "llama3_3b", "qwen3_4b_frame", "long_context",
+                                  "long_context_p128"])
+def test_full_size_step_sampled_rows(name, mode):
+    cfg = W.CONFIGS[name]
+    batch = W.make_batch(cfg)
+    dev = W.Tensors(batch, device="cuda")
+    L = cfg.num_layers
+    rows = [0, cfg.n_active - 1]
+    layers = [0, L - 1]
+    snaps = {(l, b): _snapshot(dev, batch, l, b) for l in layers for b in rows}
+    logits = dev.logits.cpu().numpy()
+    base = None if dev.base is None else dev.base.cpu().numpy()
+    fb = None if dev.fb is None else dev.fb.cpu().numpy()
+    ctrl = None if dev.ctrl is None else dev.ctrl.cpu().numpy()
+    qkv = {(l, b): (W.bf16_bits(dev.q[l, b:b + 1]), W.bf16_bits(dev.k[l, b:b + 1]),
+                    W.bf16_bits(dev.v[l, b:b + 1])) for l in layers for b in rows}
+
+    step = DecodeStep(batch, dev)
+    if mode == "eager":
+        steps0 = batch.steps.copy()
+        step.run()
+    else:
+        # as bench.py: capture the whole step (one plan, every layer, the
+        # sampler and the frame; a warm-up step runs first and advances the
+        # step counters), then replay it once into cleared outputs
+        step.capture()
+        torch.cuda.synchronize()
+        steps0 = step.steps.cpu().numpy().copy()
+        step.out.fill_(float("nan"))
+        step.lse.fill_(float("nan"))
+        step.out_tok.fill_(-1)
+        if base is not None:
+            step.out_codes.fill_(-9)
+        step.replay()
+    torch.cuda.synchronize()
+    assert int(step.err.item()) == 0
+
+    worst = _check_attention(name, cfg, batch, step, snaps, qkv)
+    if mode == "graph":
+        # the attention calls alone, as timed for the roofline
+        step.capture_attention()
+        step.out.fill_(float("nan"))
+        step.lse.fill_(float("nan"))
+        step.replay_attention()
+        torch.cuda.synchronize()
+        assert int(step.err.item()) == 0
+        worst = max(worst, _check_attention(name, cfg, batch, step, snaps, qkv))
 
     # sampler: every row
     s_steps = steps0.copy()
@@ -85,7 +120,7 @@ def test_full_size_step_sampled_rows(name):
     got_tok = step.out_tok.cpu().numpy()
     near = (info["top2_gap_rel"] < NEAR) | (info["member_margin"] < NEAR)
     assert not np.any((got_tok != tok) & ~near), np.nonzero(got_tok != tok)
-    print(name, "sampler near-ties:", int(near.sum()), "attn worst max-abs:", worst)
+    print(name, mode, "sampler near-ties:", int(near.sum()), "attn worst max-abs:", worst)
 
     if base is not None:
         f_steps = s_steps.copy()
