@@ -638,6 +638,37 @@ def run_reference(args, rank, world):
     return 0
 
 
+def profile_case(args):
+    """A small, self-contained run of one workload for profilers (ncu): the
+    full shapes of a configuration with ``--layers`` layers, ``--steps``
+    steps, nothing timed.  ``--part sampler`` (or ``frame``) runs only the
+    sampler (or the frame) of a decode workload, each step one call; a
+    prefill / mixed-step workload runs its append + tensor-core attention
+    per layer."""
+    import torch
+    import paged_kv_decode_pages_gb300 as pkv
+    from paged_kv_decode_pages_gb300 import workloads as W
+    from paged_kv_decode_pages_gb300.step import DecodeStep, PrefillStep
+    pkv.load()
+    if args.workload in W.PREFILL_CONFIGS:
+        cfg = W.PREFILL_CONFIGS[args.workload]
+        batch = W.make_prefill_batch(cfg)
+        step = PrefillStep(batch, W.PrefillTensors(batch, device="cuda", layers=args.layers))
+        run = step.run
+    else:
+        cfg = W.CONFIGS[args.workload]
+        batch = W.make_batch(cfg)
+        step = DecodeStep(batch, W.Tensors(batch, device="cuda", layers=args.layers))
+        run = {"all": step.run, "sampler": step.sample, "frame": step.frame}[args.part]
+    for _ in range(args.steps):
+        run()
+    torch.cuda.synchronize()
+    err = int(step.err.item())
+    print("profile case %s (%s): %d layers x %d steps, err=%d"
+          % (cfg.name, args.part, args.layers, args.steps, err))
+    return 1 if err else 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -650,7 +681,14 @@ def main(argv=None):
     ap.add_argument("--configs", default="qwen2_0p5b,llama3_3b,qwen3_4b_frame,tiny",
                     help="further decode workloads measured after the headline one")
     ap.add_argument("--config-cpu-budget", type=float, default=3.0)
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run a small untimed case for a profiler instead of the bench")
+    ap.add_argument("--layers", type=int, default=2, help="layers of the profile case")
+    ap.add_argument("--part", default="all", choices=["all", "sampler", "frame"],
+                    help="what the profile case runs of a decode workload")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        return profile_case(args)
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -762,18 +800,27 @@ def measure_decode(name, args, rank, world, local, clocks, full):
         step.replay_attention()
     attn_avg_s = timed(step.replay_attention, args.steps) / 1e3 / (args.steps * cfg.num_layers)
 
+    def per_call_us(fn, n=50, reps=4):
+        """fn's kernels captured n times over as one CUDA graph (as they run
+        inside the step's graph: no host launch gaps), the graph replayed
+        reps times between events; microseconds per call."""
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(n):
+                fn()
+        g.replay()
+        return timed(g.replay, reps) / (reps * n) * 1e3
+
     # ---- sampler alone (rows/s) and frame alone -------------------------
-    n_samp = 50
     sampler_us = None
     if tensors.logits is not None:
-        for _ in range(3):
-            step.sample(stream=stream)
-        sampler_us = timed(lambda: step.sample(stream=stream), n_samp) / n_samp * 1e3
+        sampler_us = per_call_us(lambda: step.sample())
     frame_line = None
     if tensors.base is not None:
-        for _ in range(3):
-            step.frame(stream=stream)
-        frame_us = timed(lambda: step.frame(stream=stream), n_samp) / n_samp * 1e3
+        frame_us = per_call_us(lambda: step.frame())
         n_cb = tensors.base.shape[0]
         frame_line = {"us_per_frame": frame_us,
                       "frames_per_s": sizes["n_active"] / (frame_us / 1e6),
@@ -807,7 +854,7 @@ def measure_decode(name, args, rank, world, local, clocks, full):
         "gpu_launches": args.steps * step.launches_per_step(),
     }
     if sampler_us is not None:
-        line["sampler"] = {"us_per_call": sampler_us,
+        line["sampler"] = {"us_per_call": sampler_us, "timing": "graph of 50 calls, 4 replays",
                            "rows_per_s": sizes["n_active"] / (sampler_us / 1e6),
                            "gbs": sizes["logits"] / (sampler_us / 1e6) / 1e9,
                            "frac": sizes["logits"] / (sampler_us / 1e6) / 1e9 / peak}
@@ -833,9 +880,7 @@ def measure_decode(name, args, rank, world, local, clocks, full):
     if tensors.logits is not None:
         ext_set = dict(min_p=0.05, rep_penalty=1.2, rep_window=-1, hist_cap=256)
         step.enable_ext(**ext_set)
-        for _ in range(3):
-            step.sample_ext(stream=stream)
-        ext_us = timed(lambda: step.sample_ext(stream=stream), n_samp) / n_samp * 1e3
+        ext_us = per_call_us(lambda: step.sample_ext())
         line["sampler_ext"] = {"us_per_call": ext_us,
                                "rows_per_s": sizes["n_active"] / (ext_us / 1e6),
                                "settings": dict(ext_set, logprobs="raw and processed")}

@@ -219,6 +219,13 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
   return u >> 16;
 }
 
+// log2 on the SFU (lg2.approx; for normal positive inputs).
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // 2^x on the SFU (ex2.approx, flush-to-zero).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -74,25 +74,23 @@ constexpr int NCAND = 512;              // most candidates kept per chunk
 constexpr int NC_MIN = 64;              // least candidates kept per chunk
 constexpr int MAX_CHUNKS = 64;          // vocab <= 64 * 8192
 constexpr int GEN_BLOCK = 1024;         // sorted block (finish and general path)
-constexpr int GUMBEL_PRE = 128;         // top-k up to this: noise computed beside the exponentials
 
 enum Mode : int { MODE_GREEDY = 0, MODE_TOPK_SMALL = 1, MODE_TOPP_FULL = 2, MODE_ALL = 3, MODE_GENERAL = 4 };
 
 struct ChunkRec {
   uint64_t top1;       // largest composite of the chunk (0: chunk empty)
-  double mx;           // x of top1
-  double z;            // sum over the chunk of exp(x - mx)        (MODE_TOPP_FULL)
+  uint64_t thr;        // the smallest of them when the chunk holds more tokens (else 0)
   double gscore;       // best x + g of the chunk                  (MODE_ALL)
   int32_t gid;         // its token
   int32_t ncand;       // candidates kept
-  uint64_t thr;        // the smallest of them when the chunk holds more tokens (else 0)
-  uint64_t cand[NCAND];
+  float zh, zl;        // sum over the chunk of 2^(t - t_top1), double-float  (need_z)
   float rmax;          // largest unprocessed logit of the chunk      (raw log-probs)
   float rzh, rzl;      // sum over the chunk of exp(logit - rmax)      (raw log-probs)
   uint32_t gkey;       // order key of gid                            (MODE_ALL)
+  uint64_t pad_;
+  uint64_t cand[NCAND];
 };
 static_assert(sizeof(ChunkRec) % 64 == 0, "ChunkRec");
-static_assert(((GUMBEL_PRE + 31) & ~31) + GUMBEL_PRE <= SB, "noise warps fit the CTA");
 
 struct RowParams {
   float temperature;
@@ -272,6 +270,39 @@ __device__ __forceinline__ double gumbel(const RowParams &P, int token) {
   return -log(-log(u));
 }
 
+constexpr float LN2F = 0.693147180559945309f;
+
+// The same noise in fp32, for screening only: within ~1e-5 absolute of the
+// fp64 value (see finish_row's margin).  E = -ln(u) is formed without
+// cancellation: for u < 1/2 from u itself (relative error 2^-24 in u), for
+// u >= 1/2 from v = 1 - u = (2^53 - 2j - 1) 2^-53, which is exact as an
+// integer, by the series v + v^2/2 + ... + v^8/8 when v < 1/8 (the rest is
+// below 1e-9 v) and by ln(1 - v) otherwise (then E > 0.13).
+__device__ __forceinline__ float gumbel32(const RowParams &P, int token) {
+  const uint64_t w = philox_word0(P.seed, P.salt, (uint64_t)(uint32_t)token, (uint64_t)P.step);
+  const uint64_t j = w >> 12;
+  float e;
+  if (j < (1ull << 51)) {
+    e = -lg2_approx(__ull2float_rn(2ull * j + 1ull) * 0x1p-53f) * LN2F;
+  } else {
+    const float v = __ull2float_rn((1ull << 53) - 2ull * j - 1ull) * 0x1p-53f;
+    if (v < 0.125f) {
+      float q = 1.0f / 8.0f;
+      q = fmaf(q, v, 1.0f / 7.0f);
+      q = fmaf(q, v, 1.0f / 6.0f);
+      q = fmaf(q, v, 1.0f / 5.0f);
+      q = fmaf(q, v, 1.0f / 4.0f);
+      q = fmaf(q, v, 1.0f / 3.0f);
+      q = fmaf(q, v, 1.0f / 2.0f);
+      q = fmaf(q, v, 1.0f);
+      e = q * v;
+    } else {
+      e = -lg2_approx(1.0f - v) * LN2F;
+    }
+  }
+  return -lg2_approx(e) * LN2F;
+}
+
 // ---------------------------------------------------------------------------
 // order keys
 // ---------------------------------------------------------------------------
@@ -346,7 +377,13 @@ struct SampSmem {
   uint32_t penbits[CHUNK / 32];  // penalised tokens of the chunk
   uint64_t sortbuf[GEN_BLOCK];
   double es[GEN_BLOCK];
-  double gs[GUMBEL_PRE];  // Gumbel noise of the first ranks (top-k of at most GUMBEL_PRE)
+  uint64_t gbuf[SB];             // block_top_n's gather buffer (finish)
+  float eh[NCAND], el[NCAND];    // 2^(t_r - t_0) of the sorted candidates, double-float
+  float g32[NCAND];              // their fp32 Gumbel noise
+  float s32[NCAND];              // their fp32 scores
+  float fh[MAX_CHUNKS], fl[MAX_CHUNKS];  // the chunks' rescaled normalisers
+  float wbs[SB / 32];            // per-warp best fp32 scores
+  float zh, zl;                  // a normaliser, double-float
 };
 
 // ---------------------------------------------------------------------------
@@ -501,16 +538,51 @@ __device__ void select_bin(SampSmem &sm, int shift) {
 // ---------------------------------------------------------------------------
 // chunk pass
 // ---------------------------------------------------------------------------
-// sum over the chunk of 2^(v * c2 - t_max), in double-float; all threads
-// get it
-__device__ __forceinline__ DF chunk_exp_sum(const uint32_t (&key)[EPT], int cnt,
-                                            const Exp2Ctx &ctx, SampSmem &sm) {
+// The per-logit loops below with a long body (the double-float exponential,
+// the fp64 Gumbel noise) are rolled loops over the chunk as it lies in global
+// memory (just loaded, so served from L1 / L2): unrolled over the thread's
+// 32 values they were tens of kilobytes of straight-line code, executed once
+// per CTA and stalled on instruction fetch.
+
+// Sum over the chunk's logits v (penalised where the chunk's bitmap in
+// sm.penbits says so, when pen_on) of 2^(v * c2 - t_max), in double-float;
+// all threads get it.  NaN and -inf logits add 0.
+__device__ __forceinline__ DF chunk_exp_sum(const float *row, int start, int cnt, const Exp2Ctx ctx,
+                                         bool pen_on, float pen, SampSmem &sm) {
   DF acc = {0.0f, 0.0f};
-#pragma unroll
-  for (int j = 0; j < EPT; ++j)
-    if ((int)threadIdx.x + j * SB < cnt)
-      df_accumulate(acc, df_exp2_rel(key_value(key[j]), ctx, sm.e2h, sm.e2l));
+#pragma unroll 2
+  for (int i = (int)threadIdx.x; i < cnt; i += SB) {
+    float v = row[start + i];
+    if (pen_on && ((sm.penbits[i >> 5] >> (i & 31)) & 1u)) v = penalise(v, pen);
+    if (v == 0.0f) v = 0.0f;  // -0 ranks as +0
+    df_accumulate(acc, df_exp2_rel(v, ctx, sm.e2h, sm.e2l));
+  }
   return block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
+}
+
+// Keep everything: the thread's best x + g (fp64, the definition) over the
+// chunk's tokens; *bid < 0 when the thread has none.
+__device__ __forceinline__ void chunk_gumbel_all(const float *row, int start, int cnt,
+                                              const RowParams P, SampSmem &sm, double *bs,
+                                              int *bid, uint32_t *bkey) {
+  *bs = 0.0;
+  *bid = -1;
+  *bkey = 0u;
+  const bool pen_on = P.n_pen > 0;
+#pragma unroll 1
+  for (int i = (int)threadIdx.x; i < cnt; i += SB) {
+    float v = row[start + i];
+    if (pen_on && ((sm.penbits[i >> 5] >> (i & 31)) & 1u)) v = penalise(v, P.pen);
+    bool bad = false;
+    const uint32_t key = order_key(v, bad);
+    const int tok = start + i;
+    const double s = (double)key_value(key) / (double)P.temperature + gumbel(P, tok);
+    if (better(s, tok, *bs, *bid)) {
+      *bs = s;
+      *bid = tok;
+      *bkey = key;
+    }
+  }
 }
 
 // The largest of a thread's N values get(j), as four independent partial
@@ -630,8 +702,9 @@ __device__ __forceinline__ void load_chunk(const float *row, int V, int c, float
 // raw: the thread's logits of chunk c (load_chunk).  pbits: the row's
 // penalty bitmap in global memory, written for this chunk when the row is
 // penalised (may be null otherwise)
-__device__ void chunk_pass(const float (&raw)[EPT], int V, int c, const RowParams &P,
-                           ChunkRec *rec, uint32_t *pbits, SampSmem &sm, int32_t *err) {
+__device__ void chunk_pass(const float (&raw)[EPT], const float *row, int V, int c,
+                           const RowParams &P, ChunkRec *rec, uint32_t *pbits, SampSmem &sm,
+                           int32_t *err) {
   const int tid = threadIdx.x;
   const int start = c * CHUNK;
   const int cnt = min(CHUNK, V - start);
@@ -651,7 +724,8 @@ __device__ void chunk_pass(const float (&raw)[EPT], int V, int c, const RowParam
     for (int j = 0; j < EPT; ++j)
       if (tid + j * SB < cnt) km = key[j] > km ? key[j] : km;
     const float rmax = key_value((uint32_t)block_max_u64(km, sm));
-    const DF z = chunk_exp_sum(key, cnt, exp2_ctx(LOG2E_H, LOG2E_L, rmax), sm);
+    const DF z = chunk_exp_sum(row, start, cnt, exp2_ctx(LOG2E_H, LOG2E_L, rmax), false, 1.0f,
+                               sm);
     if (tid == 0) {
       rec->rmax = rmax;
       rec->rzh = z.h;
@@ -699,22 +773,10 @@ __device__ void chunk_pass(const float (&raw)[EPT], int V, int c, const RowParam
   if (P.mode == MODE_GREEDY || P.mode == MODE_GENERAL) return;
 
   if (P.mode == MODE_ALL) {
-    double bs = 0.0;
-    int bid = -1;
-    uint32_t bkey = 0;
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int i = tid + j * SB;
-      if (i < cnt) {
-        const int tok = start + i;
-        const double s = (double)key_value(key[j]) / (double)P.temperature + gumbel(P, tok);
-        if (better(s, tok, bs, bid)) {
-          bs = s;
-          bid = tok;
-          bkey = key[j];
-        }
-      }
-    }
+    double bs;
+    int bid;
+    uint32_t bkey;
+    chunk_gumbel_all(row, start, cnt, P, sm, &bs, &bid, &bkey);
     double best;
     const int id = block_argmax(bs, bid, sm, &best);
     if (tid == 0) {
@@ -781,10 +843,10 @@ __device__ void chunk_pass(const float (&raw)[EPT], int V, int c, const RowParam
   if (P.need_z) {
     // sum over the chunk of exp(x - mx) = 2^(t - t_max), t = logit * log2(e) / T
     const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
-    const DF z = chunk_exp_sum(key, cnt, ctx, sm);
+    const DF z = chunk_exp_sum(row, start, cnt, ctx, P.n_pen > 0, P.pen, sm);
     if (tid == 0) {
-      rec->mx = comp_x(top1, P.temperature);
-      rec->z = (double)z.h + (double)z.l;
+      rec->zh = z.h;
+      rec->zl = z.l;
     }
   }
   __syncthreads();
@@ -975,40 +1037,215 @@ __device__ int general_sample(const RowView &rv, int V, const RowParams &P, uint
 }
 
 // ---------------------------------------------------------------------------
-// top-p scan (one warp): rank r is kept iff r == 0 or the sum of the kept
-// probabilities before it is below p * Z.  Scans es[0, n) of ranks r0 + i
-// with the running sum `carry` (prefix sums over 32 ranks at a time by
-// shuffles); returns true when the cut falls inside, with *kept = the
-// number kept from this block.
-// ---------------------------------------------------------------------------
-__device__ bool topp_scan_warp(const double *es, int n, int r0, double &carry, double pz,
-                               int *kept) {
-  const int lane = threadIdx.x & 31;
-  for (int base = 0; base < n; base += 32) {
-    const int r = base + lane;
-    double inc = r < n ? es[r] : 0.0;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const double o = __shfl_up_sync(FULL_MASK, inc, off);
-      if (lane >= off) inc += o;
-    }
-    double ex = __shfl_up_sync(FULL_MASK, inc, 1);
-    if (lane == 0) ex = 0.0;
-    const bool stop = r < n && r0 + r > 0 && !(carry + ex < pz);
-    const unsigned bm = __ballot_sync(FULL_MASK, stop);
-    if (bm) {
-      *kept = base + __ffs(bm) - 1;
-      return true;
-    }
-    carry += __shfl_sync(FULL_MASK, inc, 31);
-  }
-  *kept = n;
-  return false;
-}
-
-// ---------------------------------------------------------------------------
 // finish: one CTA per row
 // ---------------------------------------------------------------------------
+// Arithmetic of the decision.  The definition is stated in fp64 (x = logit
+// / T, e^(x - m), prefix sums against p * Z, x + Gumbel noise).  One fp64
+// warp instruction costs this GPU as much issue time as several dozen fp32
+// ones, and an fp64 logarithm thousands of cycles, so the finish works in
+// double-float arithmetic and takes fp64 only where a decision could
+// otherwise differ from the definition:
+//  * e^(x_r - m) = 2^(t_r - t_0) by df_exp2_rel (within 3e-9 of itself), the
+//    normaliser and the top-p prefix sums as double-float sums, so a cut can
+//    differ from the fp64 definition only where a prefix sum lies within
+//    ~1e-8 of p * Z, or e_r within ~1e-8 of min_p (near-ties);
+//  * Gumbel-max: every kept rank's score x + g is formed in fp32 (x by a
+//    correctly rounded division, g by gumbel32; within 2e-5 + 2.5e-7 |score|
+//    of the fp64 score).  When no other kept rank lies within
+//    1e-4 + 2e-6 |best| of the best fp32 score the fp32 winner is the fp64
+//    winner; otherwise the ranks within that margin are scored again in fp64
+//    exactly as the definition states, and the token is theirs.
+
+constexpr int UNION_PT = 8;               // union slots per thread in union_top_n
+constexpr int UNION_MAX = UNION_PT * SB;  // largest union taken by union_top_n
+
+// The n largest composites of the union of the chunks' candidates (chunk c
+// holds nc slots, zero past its ncand), in descending order, into
+// sm.sortbuf[0, n).  Needs nu = nch * nc <= UNION_MAX, n <= SB and n
+// nonzero slots; false (nothing written) when more than SB slots pass the
+// selection bound.
+__device__ bool union_top_n(const ChunkRec *recs, int nc, int nu, int n, SampSmem &sm) {
+  const uint64_t magic = ((1ull << 32) + (uint64_t)nc - 1ull) / (uint64_t)nc;  // i / nc, i < 2^16
+  auto get = [&](int k) -> uint64_t {
+    const int i = (int)threadIdx.x + k * SB;
+    if (i >= nu) return 0ull;
+    const int c = (int)(((uint64_t)i * magic) >> 32);
+    return recs[c].cand[i - c * nc];
+  };
+  uint64_t t1;
+  return block_top_n<UNION_PT>(get, n, sm.sortbuf, nullptr, sm.gbuf, sm, t1);
+}
+
+// The nv largest composites of the union in descending order into
+// sm.sortbuf[0, nv) (nv <= NCAND): a radix select of the nv-th, the gather,
+// a bitonic sort.
+__device__ void union_sorted_slow(const ChunkRec *recs, int nc, int nu, int nv, SampSmem &sm) {
+  const int tid = threadIdx.x;
+  auto cand_at = [&](int i) -> uint64_t { return recs[i / nc].cand[i % nc]; };
+  const uint64_t thr = select_rank_of(nu, cand_at, ~0ull, nv - 1, sm);
+  if (tid == 0) sm.cnt = 0;
+  __syncthreads();
+  for (int i = tid; i < nu; i += SB) {
+    const uint64_t cc = cand_at(i);
+    if (cc != 0ull && cc >= thr) {
+      const uint32_t pos = atomicAdd(&sm.cnt, 1u);
+      if (pos < (uint32_t)nv) sm.sortbuf[pos] = cc;
+    }
+  }
+  __syncthreads();
+  int n2 = 1;
+  while (n2 < nv) n2 <<= 1;
+  for (int i = nv + tid; i < n2; i += SB) sm.sortbuf[i] = 0ull;
+  __syncthreads();
+  block_sort_desc(sm.sortbuf, n2);
+}
+
+// The normaliser of the whole row relative to its maximum: the chunks'
+// partials z_c (relative to each chunk's maximum) times 2^(t_c - t_0),
+// added in chunk order.
+__device__ DF row_normaliser(const ChunkRec *recs, int nch, const Exp2Ctx &ctx, SampSmem &sm) {
+  const int tid = threadIdx.x;
+  __syncthreads();
+  if (tid < nch) {
+    DF f = {0.0f, 0.0f};
+    if (recs[tid].top1 != 0ull) {
+      const DF w = df_exp2_rel(key_value((uint32_t)(recs[tid].top1 >> 32)), ctx, sm.e2h, sm.e2l);
+      f = df_mul(DF{recs[tid].zh, recs[tid].zl}, w);
+    }
+    sm.fh[tid] = f.h;
+    sm.fl[tid] = f.l;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    DF z = {0.0f, 0.0f};
+    for (int c = 0; c < nch; ++c) z = df_add(z, DF{sm.fh[c], sm.fl[c]});
+    sm.zh = z.h;
+    sm.zl = z.l;
+  }
+  __syncthreads();
+  const DF z = {sm.zh, sm.zl};
+  __syncthreads();
+  return z;
+}
+
+// Warp 0: the first rank r >= max(lo, 1) in [lo, hi) with e_r < min_p, or -1.
+__device__ int minp_boundary_warp(const SampSmem &sm, int lo, int hi, float min_p) {
+  for (int base = max(lo, 1); base < hi; base += 32) {
+    const int r = base + (int)(threadIdx.x & 31);
+    bool below = false;
+    if (r < hi) below = sm.eh[r] < min_p || (sm.eh[r] == min_p && sm.el[r] < 0.0f);
+    const unsigned bm = __ballot_sync(FULL_MASK, below);
+    if (bm) return base + __ffs(bm) - 1;
+  }
+  return -1;
+}
+
+// Warp 0: top-p over ranks [0, n): rank r is kept iff r == 0 or the sum of
+// the e's before it is below pz (double-float prefix sums, 32 ranks at a
+// time by shuffles).  Returns the first rank not kept, or n.
+__device__ int topp_cut_warp(const SampSmem &sm, int n, DF pz) {
+  const int lane = threadIdx.x & 31;
+  DF carry = {0.0f, 0.0f};
+  for (int base = 0; base < n; base += 32) {
+    const int r = base + lane;
+    DF inc = r < n ? DF{sm.eh[r], sm.el[r]} : DF{0.0f, 0.0f};
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const DF o = df_shfl_up(inc, off);
+      if (lane >= off) inc = df_add(inc, o);
+    }
+    DF ex = df_shfl_up(inc, 1);
+    if (lane == 0) ex = DF{0.0f, 0.0f};
+    const DF before = df_add(carry, ex);
+    const bool stop = r < n && r > 0 && !df_lt(before, pz);
+    const unsigned bm = __ballot_sync(FULL_MASK, stop);
+    if (bm) return base + __ffs(bm) - 1;
+    carry = df_add(carry, df_shfl(inc, 31));
+  }
+  return n;
+}
+
+// Gumbel-max over the kept ranks [0, kept) of sm.sortbuf, whose fp32 noise
+// is in sm.g32: the fp32 screen, then fp64 scores for the contenders within
+// the margin (see the arithmetic note above).  Returns the composite of the
+// winner.
+__device__ uint64_t gumbel_argmax_sorted(const RowParams &P, int kept, SampSmem &sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (kept == 1) return sm.sortbuf[0];
+  float bs = -INFINITY;
+  uint64_t bc = 0ull;
+  for (int r = tid; r < kept; r += SB) {
+    const uint64_t cc = sm.sortbuf[r];
+    const float s = __fadd_rn(__fdiv_rn(key_value((uint32_t)(cc >> 32)), P.temperature), sm.g32[r]);
+    sm.s32[r] = s;
+    if (bc == 0ull || s > bs || (s == bs && comp_token(cc) < comp_token(bc))) {
+      bs = s;
+      bc = cc;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float os = __shfl_xor_sync(FULL_MASK, bs, off);
+    const uint64_t oc = __shfl_xor_sync(FULL_MASK, bc, off);
+    if (oc != 0ull && (bc == 0ull || os > bs || (os == bs && comp_token(oc) < comp_token(bc)))) {
+      bs = os;
+      bc = oc;
+    }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    sm.wbs[warp] = bs;
+    sm.red_u64[warp] = bc;
+  }
+  __syncthreads();
+  float best = -INFINITY;
+  uint64_t bestc = 0ull;
+  for (int w = 0; w < SB / 32; ++w) {
+    const uint64_t oc = sm.red_u64[w];
+    const float os = sm.wbs[w];
+    if (oc != 0ull && (bestc == 0ull || os > best || (os == best && comp_token(oc) < comp_token(bestc)))) {
+      best = os;
+      bestc = oc;
+    }
+  }
+  const float margin = 1e-4f + 2e-6f * fabsf(best);
+  const float floor_s = best - margin;
+  int close = 0;
+  for (int r = tid; r < kept; r += SB) close += sm.s32[r] >= floor_s ? 1 : 0;
+  close = __reduce_add_sync(FULL_MASK, close);
+  if (tid == 0) sm.cnt = 0;
+  __syncthreads();
+  if (lane == 0 && close) atomicAdd(&sm.cnt, (uint32_t)close);
+  __syncthreads();
+  const bool screened = isfinite(best) && sm.cnt == 1u;
+  __syncthreads();
+  if (screened) return bestc;
+  // fp64 scores of the contenders (every kept rank when the screen cannot
+  // decide at all)
+  const bool all = !isfinite(best);
+  double ds = 0.0;
+  int did = -1;
+  for (int r = tid; r < kept; r += SB) {
+    if (all || sm.s32[r] >= floor_s) {
+      const uint64_t cc = sm.sortbuf[r];
+      const int tok = comp_token(cc);
+      const double s = comp_x(cc, P.temperature) + gumbel(P, tok);
+      if (better(s, tok, ds, did)) {
+        ds = s;
+        did = tok;
+      }
+    }
+  }
+  const int id = block_argmax(ds, did, sm);
+  // its composite: the kept rank holding that token
+  for (int r = tid; r < kept; r += SB)
+    if (comp_token(sm.sortbuf[r]) == id) sm.red_u64[0] = sm.sortbuf[r];
+  __syncthreads();
+  const uint64_t c = sm.red_u64[0];
+  __syncthreads();
+  return c;
+}
+
 // With log-probs requested (and not greedy), leaves the kept mass relative
 // to the row maximum, that maximum's x and the sampled token's x in
 // sm.s_kept, sm.m_row and sm.xbest.
@@ -1034,16 +1271,11 @@ __device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
       }
     if (P.lp_proc) {
       // the kept mass is the whole row's: the chunks' normalisers
-      const double m = comp_x(top1, P.temperature);
-      __syncthreads();
-      if (tid < nch)
-        sm.red_d[tid] = recs[tid].top1 != 0ull ? recs[tid].z * exp(recs[tid].mx - m) : 0.0;
-      __syncthreads();
+      const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
+      const DF z = row_normaliser(recs, nch, ctx, sm);
       if (tid == 0) {
-        double z = 0.0;
-        for (int c = 0; c < nch; ++c) z += sm.red_d[c];
-        sm.s_kept = z;
-        sm.m_row = m;
+        sm.s_kept = (double)z.h + (double)z.l;
+        sm.m_row = comp_x(top1, P.temperature);
         sm.xbest = (double)key_value(bkey) / (double)P.temperature;
       }
       __syncthreads();
@@ -1052,195 +1284,141 @@ __device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
   }
   if (P.mode == MODE_GENERAL) return general_sample(rv, V, P, top1, -1.0, sm);
 
-  // the largest of the union of the chunks' candidates, sorted: the top-k,
-  // or (K == V with top-p or min_p) up to NCAND tokens
+  // candidate modes: the sorted prefix of the union of the chunks'
+  // candidates, extended only as far as the decision reads
   const int nc = P.nc;
   const int nu = nch * nc;
   const bool full = P.mode == MODE_TOPP_FULL;
-  auto cand_at = [&](int i) -> uint64_t { return recs[i / nc].cand[i % nc]; };
+  const bool topp = P.top_p < 1.0f;
+  const bool minp = P.min_p > 0.0f;
   if (tid == 0) sm.cnt = 0;
   __syncthreads();
   if (tid < nch) atomicAdd(&sm.cnt, (uint32_t)recs[tid].ncand);
   __syncthreads();
   const int nreal = (int)sm.cnt;
+  // ranks the decision may read: the top-k, or for top-p over the whole
+  // vocabulary up to NCAND candidates (past them: the general path)
   const int nv = min(full ? NCAND : P.K, nreal);
   __syncthreads();
-  int nsort;
-  bool sorted = false;
-  if (nu <= GEN_BLOCK && nv <= SB) {
-    // the nv largest of the union, in order (the decision reads no further)
-    auto get = [&](int k) -> uint64_t {
-      const int i = tid + k * SB;
-      return i < nu ? cand_at(i) : 0ull;
-    };
-    uint64_t t1;
-    sorted = block_top_n<GEN_BLOCK / SB>(get, nv, sm.sortbuf, nullptr,
-                                         reinterpret_cast<uint64_t *>(sm.es), sm, t1);
-  }
-  if (sorted) {
-    nsort = nv;
-  } else if (nu <= GEN_BLOCK) {
-    nsort = nu;
-    for (int i = tid; i < nu; i += SB) sm.sortbuf[i] = cand_at(i);
-  } else {
-    const uint64_t thr = select_rank_of(nu, cand_at, ~0ull, nv - 1, sm);
-    if (tid == 0) sm.cnt = 0;
-    __syncthreads();
-    for (int i = tid; i < nu; i += SB) {
-      const uint64_t cc = cand_at(i);
-      if (cc != 0ull && cc >= thr) {
-        const uint32_t pos = atomicAdd(&sm.cnt, 1u);
-        if (pos < (uint32_t)nv) sm.sortbuf[pos] = cc;
-      }
-    }
-    nsort = nv;
-  }
-  if (!sorted) {
-    int n2 = 1;
-    while (n2 < nsort) n2 <<= 1;
-    for (int i = nsort + tid; i < n2; i += SB) sm.sortbuf[i] = 0ull;
-    __syncthreads();
-    block_sort_desc(sm.sortbuf, n2);
-  }
-  const double m = comp_x(sm.sortbuf[0], P.temperature);
-  const bool topp = P.top_p < 1.0f;
-  const bool minp = P.min_p > 0.0f;
-  // Z: the normaliser the top-p cut is taken against.  Top-p over the whole
-  // vocabulary without min_p: the chunks' partial normalisers, rescaled to
-  // the row maximum in parallel and added in chunk order; otherwise the sum
-  // over the ranks that pass top-k and min_p, once those are known.
-  double Z = 0.0;
-  bool zready = false;
-  if (full && !minp) {
-    if (tid < nch) sm.red_d[tid] = recs[tid].top1 != 0ull ? recs[tid].z * exp(recs[tid].mx - m) : 0.0;
-    __syncthreads();
-    if (tid == 0) {
-      double z = 0.0;
-      for (int c = 0; c < nch; ++c) z += sm.red_d[c];
-      sm.zsum = z;
-    }
-    __syncthreads();
-    Z = sm.zsum;
-    zready = true;
-  }
-  // e^(x - m) of the sorted candidates, in blocks of 64, 128, ... only as far
-  // as the min_p boundary and the top-p scan reach (all of them for top-k)
-  double carry = 0.0;  // warp 0: the running sum before the scanned block
-  int lo = 0, hi = full ? min(64, nv) : nv;
-  int kp = minp ? -1 : nv;  // ranks [0, kp) pass min_p (-1: not found yet)
-  int scan_lo = 0;
-  if (tid == 0) sm.flag = 0;
-  // A top-k of at most GUMBEL_PRE: the Gumbel noise of every candidate is
-  // computed now, by the warps the first block of exponentials (ranks
-  // [0, nv), threads [0, nv)) leaves idle, instead of after the top-p cut;
-  // the values are the same, the fp64 work overlaps.
-  const bool pre_g = !full && nv <= GUMBEL_PRE;
-  if (pre_g) {
-    const int g0 = (nv + 31) & ~31;  // first thread of the noise warps
-    if (tid >= g0 && tid < g0 + nv) sm.gs[tid - g0] = gumbel(P, comp_token(sm.sortbuf[tid - g0]));
-  }
+  const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
+  // top-p over the whole vocabulary without min_p: Z is the whole row's
+  DF Z = {0.0f, 0.0f};
+  const bool z_row = full && !minp;
+  if (z_row) Z = row_normaliser(recs, nch, ctx, sm);
+
+  int M = full ? min(64, nv) : nv;
+  int have = 0;  // ranks whose e and noise are in shared memory
+  int kept = 0, kp = nv;
+  bool general = false;
   for (;;) {
-    for (int r = lo + tid; r < hi; r += SB) sm.es[r] = exp(comp_x(sm.sortbuf[r], P.temperature) - m);
+    // the sorted prefix [0, M)
+    const bool fast = nu <= UNION_MAX && M <= SB && union_top_n(recs, nc, nu, M, sm);
+    if (!fast) {
+      union_sorted_slow(recs, nc, nu, nv, sm);
+      M = nv;
+    }
+    // e_r = 2^(t_r - t_0) and the fp32 noise of the new ranks
+    for (int r = have + tid; r < M; r += SB) {
+      const uint64_t cc = sm.sortbuf[r];
+      const DF e = df_exp2_rel(key_value((uint32_t)(cc >> 32)), ctx, sm.e2h, sm.e2l);
+      sm.eh[r] = e.h;
+      sm.el[r] = e.l;
+      sm.g32[r] = gumbel32(P, comp_token(cc));
+    }
+    have = M;
     __syncthreads();
-    if (kp < 0) {
-      // the first rank >= 1 below min_p (relative to the maximum)
-      if (tid < 32) {
-        int found = -1;
-        for (int base = max(lo, 1); base < hi && found < 0; base += 32) {
-          const int r = base + tid;
-          const unsigned bm = __ballot_sync(FULL_MASK, r < hi && sm.es[r] < (double)P.min_p);
-          if (bm) found = base + __ffs(bm) - 1;
+    // decision over [0, M) by warp 0: 0 = decided, 1 = extend, 2 = general
+    if (tid < 32) {
+      int state = 0, k_p = M, k_t = M;
+      if (minp) {
+        const int b = minp_boundary_warp(sm, 0, M, P.min_p);
+        if (b >= 0) {
+          k_p = b;
+        } else if (M < nv) {
+          state = 1;
+        } else {
+          k_p = nv;
+          if (full && nv < V) state = 2;  // the boundary lies beyond the candidates
         }
-        if (tid == 0) sm.kp = found >= 0 ? found : (hi == nv ? nv : -1);
+      } else if (!full) {
+        k_p = nv;  // the top-k
       }
-      __syncthreads();
-      kp = sm.kp;
-      __syncthreads();
-      if (kp < 0) {
-        lo = hi;
-        hi = min(2 * hi + 64, nv);
-        continue;
+      if (state == 0 && topp) {
+        DF z = Z;
+        if (!z_row) {
+          // the normaliser over the ranks that pass top-k and min_p (one warp,
+          // a fixed order: lanes in rank order, then a xor tree)
+          DF part = {0.0f, 0.0f};
+          for (int r = tid; r < k_p; r += 32) part = df_add(part, DF{sm.eh[r], sm.el[r]});
+#pragma unroll
+          for (int off = 16; off; off >>= 1) part = df_add(part, df_shfl_xor(part, off));
+          z = part;
+        }
+        k_t = topp_cut_warp(sm, k_p, df_mul_f(z, P.top_p));
+        if (k_t == k_p && !minp && full) {
+          // no cut within the candidates read so far
+          if (M < nv) state = 1;
+          else if (nv < V) state = 2;
+        }
+        if (tid == 0) {
+          sm.zh = z.h;
+          sm.zl = z.l;
+        }
+      } else {
+        k_t = k_p;
       }
-      if (full && kp == nv && nv < V) {
-        // every candidate passes min_p: the boundary lies beyond them
-        if (tid == 0) sm.flag = 1;
-        __syncthreads();
-        break;
+      if (tid == 0) {
+        sm.flag = state;
+        sm.kp = k_p;
+        sm.kept = k_t;
       }
     }
-    if (!topp) {
-      if (tid == 0) sm.kept = kp;
-      __syncthreads();
+    __syncthreads();
+    const int state = sm.flag;
+    kp = sm.kp;
+    kept = sm.kept;
+    Z = DF{sm.zh, sm.zl};
+    __syncthreads();
+    if (state == 2) {
+      general = true;
       break;
     }
-    if (!zready) {
-      double part = 0.0;
-      for (int r = tid; r < kp; r += SB) part += sm.es[r];
-      Z = block_sum_d(part, sm);
-      zready = true;
-    }
-    const int end = min(hi, kp);
-    if (tid < 32) {
-      int k;
-      const bool cut =
-          topp_scan_warp(sm.es + scan_lo, end - scan_lo, scan_lo, carry, (double)P.top_p * Z, &k);
-      if (tid == 0) {
-        sm.done = (cut || end == kp) ? 1 : 0;
-        sm.kept = scan_lo + k;
-        // top-p over the whole vocabulary still open after the candidates
-        sm.flag = (!cut && end == kp && kp == nv && full && nv < V) ? 1 : 0;
-      }
-    }
-    __syncthreads();
-    const bool done = sm.done != 0;
-    __syncthreads();
-    if (done) break;
-    scan_lo = end;
-    lo = hi;
-    hi = min(2 * hi + 64, nv);
+    if (state == 0) break;
+    M = min(2 * M, nv);
   }
   // The extracted prefix is the exact global order over the prefix the
   // decision read (the kept set; the ranks through the min_p boundary; for
   // top-k the K survivors) unless a chunk that holds more tokens than it
-  // gave has its last candidate strictly inside that prefix.  The top-k
-  // also needs K candidates in the union.
-  if (!sm.flag) {
-    const int decided = !full ? nv : (minp ? min(kp + 1, nv) : sm.kept);
+  // gave has its bound strictly inside that prefix.  The top-k also needs K
+  // candidates in the union.
+  if (!general) {
+    const int decided = !full ? nv : (minp ? min(kp + 1, nv) : kept);
     const uint64_t last = sm.sortbuf[decided - 1];
     __syncthreads();
-    if (tid == 0 && !full && P.K > nreal) sm.flag = 1;
+    if (tid == 0) sm.flag = (!full && P.K > nreal) ? 1 : 0;
+    __syncthreads();
     if (tid < nch && recs[tid].thr > last) sm.flag = 1;
     __syncthreads();
+    general = sm.flag != 0;
+    __syncthreads();
   }
-  // (the chunks' normaliser is exact whatever the candidates; the top-k one
-  // is not when the union missed some of the top-k)
-  if (sm.flag) return general_sample(rv, V, P, top1, (full && !minp) ? Z : -1.0, sm);
-  const int kept = sm.kept;
-  double bs = 0.0, bx = 0.0;
-  int bid = -1;
-  for (int r = tid; r < kept; r += SB) {
-    const int tok = comp_token(sm.sortbuf[r]);
-    const double x = comp_x(sm.sortbuf[r], P.temperature);
-    const double s = x + (pre_g ? sm.gs[r] : gumbel(P, tok));
-    if (better(s, tok, bs, bid)) {
-      bs = s;
-      bid = tok;
-      bx = x;
-    }
+  if (general) {
+    const double zk = z_row ? (double)Z.h + (double)Z.l : -1.0;
+    return general_sample(rv, V, P, top1, zk, sm);
   }
-  const int id = block_argmax(bs, bid, sm);
+  const uint64_t win = gumbel_argmax_sorted(P, kept, sm);
   if (P.lp_proc) {
-    double part = 0.0;
-    for (int r = tid; r < kept; r += SB) part += sm.es[r];
-    const double sk = block_sum_d(part, sm);
-    if (bid == id) sm.xbest = bx;
+    DF part = {0.0f, 0.0f};
+    for (int r = tid; r < kept; r += SB) part = df_add(part, DF{sm.eh[r], sm.el[r]});
+    const DF sk = block_sum_df(part, sm);
     if (tid == 0) {
-      sm.s_kept = sk;
-      sm.m_row = m;
+      sm.s_kept = (double)sk.h + (double)sk.l;
+      sm.m_row = comp_x(sm.sortbuf[0], P.temperature);
+      sm.xbest = comp_x(win, P.temperature);
     }
     __syncthreads();
   }
-  return id;
+  return comp_token(win);
 }
 
 // ---------------------------------------------------------------------------
@@ -1362,6 +1540,9 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   __shared__ SampSmem sm;
   const int b = blockIdx.y;
   const int c = blockIdx.x;
+  // launched behind its predecessor on the stream (programmatic dependent
+  // launch): nothing is read before that grid has completed
+  pdl_wait();
   // the logits first (every row of the batch is readable), so that their
   // loads overlap the row's flags and settings
   float raw[EPT];
@@ -1371,7 +1552,11 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   if (slot < 0 || slot >= a.num_slots) return;
   load_exp2_table(sm);  // read after the first barrier of the chunk pass
   const RowParams P = sample_row_params(a, slot);
-  chunk_pass(raw, a.vocab, c, P, a.recs + (int64_t)b * a.nch + c, row_pbits(a, b), sm, a.err);
+  chunk_pass(raw, a.logits + (int64_t)b * a.row_stride, a.vocab, c, P,
+             a.recs + (int64_t)b * a.nch + c, row_pbits(a, b), sm, a.err);
+  // the finish kernel may be scheduled once every chunk CTA is here (late,
+  // so that its waiting CTAs do not take SM room from the chunk pass)
+  pdl_trigger();
 }
 
 __device__ __forceinline__ void sample_skip_row(const SampleArgs &a, int b) {
@@ -1385,6 +1570,7 @@ __global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
   __shared__ SampSmem sm;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
+  pdl_wait();  // the chunk records (and everything before them)
   if (!a.active[b]) {
     if (tid == 0) sample_skip_row(a, b);
     return;
@@ -1397,6 +1583,7 @@ __global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
     }
     return;
   }
+  load_exp2_table(sm);  // read after finish_row's first barrier
   const RowParams P = sample_row_params(a, slot);
   const float *row = a.logits + (int64_t)b * a.row_stride;
   const ChunkRec *recs = a.recs + (int64_t)b * a.nch;
@@ -1473,6 +1660,7 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
   const int tid = threadIdx.x;
   const int V = a.vocab;
   int32_t *out = a.out_codes + (int64_t)b * a.row_w;
+  pdl_wait();  // the predecessor's writes (the sampler's step counters)
   if (!a.active[b]) {
     for (int j = tid; j < a.row_w; j += SB) out[j] = 0;
     if (tid == 0) a.out_kind[b] = PKV_KIND_OTHER;
@@ -1498,7 +1686,7 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     for (int c = 0; c < a.ctrl_nch; ++c) {
       float raw[EPT];
       load_chunk(crow, a.ctrl_vocab, c, raw);
-      chunk_pass(raw, a.ctrl_vocab, c, P, recs + c, nullptr, sm, a.err);
+      chunk_pass(raw, crow, a.ctrl_vocab, c, P, recs + c, nullptr, sm, a.err);
       __syncthreads();
     }
     const int tok = finish_row(RowView{crow, nullptr, 1.0f}, a.ctrl_vocab, a.ctrl_nch, P, recs, sm);
@@ -1534,7 +1722,7 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     for (int c = 0; c < a.nch; ++c) {
       float raw[EPT];
       load_chunk(row, V, c, raw);
-      chunk_pass(raw, V, c, P, recs + c, nullptr, sm, a.err);
+      chunk_pass(raw, row, V, c, P, recs + c, nullptr, sm, a.err);
       __syncthreads();
     }
     const int tok = finish_row(RowView{row, nullptr, 1.0f}, V, a.nch, P, recs, sm);
@@ -1666,10 +1854,11 @@ static int launch_sample(const float *logits, int64_t row_stride, int batch, int
                                                  pkv_sample_workspace_bytes(batch, vocab))
                   : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  sample_chunk_kernel<<<dim3((unsigned)a.nch, (unsigned)batch), SB, 0, s>>>(a);
-  int rc = launch_status();
-  if (rc != PKV_OK) return rc;
-  sample_finish_kernel<<<(unsigned)batch, SB, 0, s>>>(a);
+  if (launch_pdl(sample_chunk_kernel, dim3((unsigned)a.nch, (unsigned)batch), dim3(SB), 0, s, a) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (launch_pdl(sample_finish_kernel, dim3((unsigned)batch), dim3(SB), 0, s, a) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return launch_status();
 }
 
@@ -1746,7 +1935,9 @@ static int launch_frame(const float *ctrl, int ctrl_vocab, int32_t stop_ctrl, co
   a.rows = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) +
                                      align_up((size_t)batch * rec_nch * sizeof(ChunkRec), 256));
   a.err = err_word;
-  frame_kernel<<<(unsigned)batch, SB, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (launch_pdl(frame_kernel, dim3((unsigned)batch), dim3(SB), 0,
+                 static_cast<cudaStream_t>(stream), a) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return launch_status();
 }
 

@@ -9,4 +9,9 @@ constexpr unsigned FULL_MASK = 0xffffffffu;
 inline void report(int32_t *err, int bits) {
   if (err != nullptr) atomicOr(err, (int32_t)bits);
 }
+// one grid at a time here: the programmatic-launch hooks have nothing to do
+inline void pdl_wait() {}
+inline void pdl_trigger() {}
+// the SFU's log2 (an approximation there; exact enough here)
+inline float lg2_approx(float x) { return std::log2(x); }
 }  // namespace pkv
