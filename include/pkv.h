@@ -87,6 +87,17 @@ const char *pkv_error_string(int status);
 /* Number of device-side error bits defined above (for binding checks). */
 int pkv_num_dev_error_bits(void);
 
+/* The CUDA runtime error code (a cudaError_t value) behind the calling
+ * thread's most recent PKV_ERR_CUDA, or the launch error still pending on
+ * this thread; 0 when there is none.  A fault in a kernel (an illegal or
+ * misaligned address, an illegal instruction) is sticky: every later call
+ * in the same CUDA context reports it too.  Host only, no device work. */
+int pkv_last_cuda_error(void);
+
+/* The CUDA runtime's name for an error code, e.g. "cudaErrorIllegalAddress"
+ * (a static string owned by the CUDA runtime). */
+const char *pkv_cuda_error_name(int code);
+
 /* pkv_selftest_wait_timeout -- a diagnostic, not part of the decode step.
  * Every wait of the library's kernels (an mbarrier that a bulk copy or
  * another warp completes) is bounded: when it runs out, the kernel sets

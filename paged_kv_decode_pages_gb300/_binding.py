@@ -38,6 +38,8 @@ SIGNATURES = {
     "pkv_version": (ctypes.c_char_p, []),
     "pkv_error_string": (ctypes.c_char_p, [_I]),
     "pkv_num_dev_error_bits": (_I, []),
+    "pkv_last_cuda_error": (_I, []),
+    "pkv_cuda_error_name": (ctypes.c_char_p, [_I]),
     "pkv_kv_append": (_I, [ctypes.POINTER(pkv_cache_t), _P, _I, _P, _P, _P, _I, _P, _P, _I, _P,
                            _P]),
     "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
@@ -76,7 +78,15 @@ _lib = None
 class PkvError(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
-        super().__init__("%s failed: %s (status %d)" % (fn, error_string(status), status))
+        msg = "%s failed: %s (status %d)" % (fn, error_string(status), status)
+        self.cuda_error = 0
+        if status == 3:  # PKV_ERR_CUDA: name the CUDA runtime's error
+            lib = load()
+            self.cuda_error = int(lib.pkv_last_cuda_error())
+            if self.cuda_error:
+                msg += ": %s (%d)" % (lib.pkv_cuda_error_name(self.cuda_error).decode(),
+                                      self.cuda_error)
+        super().__init__(msg)
 
 
 def library_path() -> str:

@@ -18,6 +18,21 @@ extern "C" const char *pkv_error_string(int status) {
 extern "C" int pkv_num_dev_error_bits(void) { return 7; }
 
 namespace pkv {
+static thread_local int g_last_cuda_error = 0;
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+}  // namespace pkv
+
+extern "C" int pkv_last_cuda_error(void) {
+  if (pkv::g_last_cuda_error != 0) return pkv::g_last_cuda_error;
+  // a launch that failed before its status was read leaves its error pending
+  return static_cast<int>(cudaPeekAtLastError());
+}
+
+extern "C" const char *pkv_cuda_error_name(int code) {
+  return cudaGetErrorName(static_cast<cudaError_t>(code));
+}
+
+namespace pkv {
 
 // one thread block waits, through the kernels' own bounded wait, on an
 // mbarrier that nothing arrives on

@@ -20,10 +20,16 @@ inline int check_geometry(const pkv_cache_t *g) {
   return PKV_OK;
 }
 
+// The CUDA runtime error behind this thread's latest PKV_ERR_CUDA from
+// launch_status() (pkv_last_cuda_error reads it).
+void record_cuda_error(cudaError_t e);
+
 // Status of the launches just made on this thread; does not synchronise.
 inline int launch_status() {
   cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  if (e == cudaSuccess) return PKV_OK;
+  record_cuda_error(e);
+  return PKV_ERR_CUDA;
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

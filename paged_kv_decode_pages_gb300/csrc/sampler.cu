@@ -9,25 +9,28 @@
 // <= 1e-5 is greedy; a top-k of 0 or >= vocab is no filter.  Randomness:
 // Gumbel-max with Philox4x64-10 (Salmon et al., SC 2011) keyed by
 // (seed, salt) at counter (token, step, 0, 0), so a row's sample depends on
-// its own logits and slot state only.  Every decision (order, top-p cut,
-// Gumbel argmax) is taken in fp64; the values compared are exact functions
-// of the fp32 logits except the top-p normaliser's chunk partials, which
-// are within 3e-9 of themselves (see the chunk pass).
+// its own logits and slot state only.  The order is exact (integer keys of
+// the fp32 logits); the top-p and min_p cuts are taken on double-float
+// sums whose terms are within 3e-9 of themselves, so they can differ from
+// the fp64 definition only at near-ties; the Gumbel argmax is screened in
+// fp32 and decided in fp64 among the ranks within the screen's error margin
+// (see "Arithmetic of the decision" below).
 //
 // Structure:
 //  * order key: the fp32 logit mapped to a uint32 that sorts like the float
 //    (-0 folded onto +0); composite = key << 32 | ~token, so a larger
 //    composite comes first in (value desc, id asc) order, and composites
 //    are unique.
-//  * chunk pass (one CTA per 8192-token chunk of a row; its logits are
-//    loaded before the row's settings): chunk maximum; the chunk's nc
-//    largest composites, nc = min(kcap, max(64, ceil(kcap / chunks))) with
-//    kcap = the top-k, or 512 for top-p over the whole vocabulary, and the
-//    smallest of them.  For nc <= 256 they come from a lower bound taken
-//    from the warps' sorted thread maxima and exact rank counting over the
-//    few composites above it (block_top_n), in descending order; otherwise,
-//    or when more than 256 composites pass the bound, from a radix select
-//    over 8-bit digits;
+//  * chunk pass (one CTA per 8192-token chunk of a row; the chunk is staged
+//    in shared memory with cp.async and turned into order keys in place):
+//    chunk maximum; the chunk's nc largest composites, nc = min(kcap,
+//    max(64, ceil(kcap / chunks))) with kcap = the top-k, or 512 for top-p
+//    over the whole vocabulary, and the smallest of them.  For nc <= 256
+//    they come from a lower bound taken from the warps' sorted thread
+//    maxima (select_bound), a gather of the keys at or above it and exact
+//    rank counting over those (rank_out), in descending order; otherwise,
+//    or when more than 1024 keys pass the bound, from a radix select over
+//    8-bit digits;
 //    for top-p over the whole vocabulary, the partial normaliser
 //    sum exp(x - x_chunkmax) = sum 2^(logit * log2(e) / T - t_chunkmax) in
 //    double-float arithmetic (fp32 pairs): Tang's table-driven exp2 (ACM
@@ -38,10 +41,11 @@
 //    per-logit transcendental of the path; for "keep everything", the
 //    chunk's Gumbel argmax.  The chunking depends on the vocabulary only.
 //  * finish (one CTA per row): the kcap largest of the chunks' candidates,
-//    in order (block_top_n over the union when kcap <= 256, else a radix
-//    select over the union and a bitonic sort); top-k / top-p with fp64 prefix
-//    sums in sorted order (a warp prefix scan, exponentials computed in
-//    blocks only as far as the scan reaches); the Gumbel argmax.  The
+//    in order (for a top-k up to 64 a selection bound from the lists' heads
+//    and rank counting, otherwise bitonic merges of the chunks' sorted
+//    lists, or a radix select and a sort when the union does not fit in
+//    shared memory); min_p, then top-p with double-float prefix sums in
+//    sorted order; the Gumbel argmax (arithmetic below).  The
 //    sorted candidates are the exact global order over the prefix the
 //    decision read unless a chunk holding more tokens than it gave has its
 //    smallest candidate strictly inside that prefix; such rows, and rows
@@ -61,6 +65,7 @@
 //  * the frame kernel runs the same chunk pass and finish for each of the
 //    codebooks in turn inside one CTA per row.
 #include <math.h>
+#include <stddef.h>
 
 #include "pkv_device.cuh"
 #include "pkv_host.h"
@@ -69,7 +74,6 @@ namespace pkv {
 
 constexpr int SB = 256;                 // threads per sampler CTA
 constexpr int CHUNK = 8192;             // tokens per chunk
-constexpr int EPT = CHUNK / SB;         // tokens per thread in a chunk pass
 constexpr int NCAND = 512;              // most candidates kept per chunk
 constexpr int NC_MIN = 64;              // least candidates kept per chunk
 constexpr int MAX_CHUNKS = 64;          // vocab <= 64 * 8192
@@ -87,7 +91,8 @@ struct ChunkRec {
   float rmax;          // largest unprocessed logit of the chunk      (raw log-probs)
   float rzh, rzl;      // sum over the chunk of exp(logit - rmax)      (raw log-probs)
   uint32_t gkey;       // order key of gid                            (MODE_ALL)
-  uint64_t pad_;
+  int32_t sorted;      // cand[0, ncand) is in descending order
+  int32_t pad_;
   uint64_t cand[NCAND];
 };
 static_assert(sizeof(ChunkRec) % 64 == 0, "ChunkRec");
@@ -242,13 +247,15 @@ __device__ __forceinline__ void df_accumulate(DF &acc, DF e) {
 // ---------------------------------------------------------------------------
 // Philox4x64-10 and Gumbel noise
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t philox_word0(uint64_t seed, uint32_t salt, uint64_t token,
-                                                 uint64_t step) {
+// (rolled, out of line: the sampler's kernels run most of their code once
+// per call, so code size rather than issue count sets their latency)
+__device__ __noinline__ uint64_t philox_word0(uint64_t seed, uint32_t salt, uint64_t token,
+                                              uint64_t step) {
   const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
   const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
   uint64_t c0 = token, c1 = step, c2 = 0, c3 = 0;
   uint64_t k0 = seed, k1 = salt;
-#pragma unroll
+#pragma unroll 1
   for (int r = 0; r < 10; ++r) {
     const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
     const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
@@ -264,7 +271,7 @@ __device__ __forceinline__ uint64_t philox_word0(uint64_t seed, uint32_t salt, u
   return c0;
 }
 
-__device__ __forceinline__ double gumbel(const RowParams &P, int token) {
+__device__ __noinline__ double gumbel(const RowParams &P, int token) {
   const uint64_t w = philox_word0(P.seed, P.salt, (uint64_t)(uint32_t)token, (uint64_t)P.step);
   const double u = (double)(2ull * (w >> 12) + 1ull) * 0x1p-53;
   return -log(-log(u));
@@ -318,6 +325,15 @@ __device__ __forceinline__ uint32_t order_key(float f, bool &bad) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// order_key without the checks: the fp32 bits mapped to a uint32 that
+// sorts like the float, -0 folded onto +0.  A NaN maps outside
+// [key(-inf), key(+inf)]; keys_fix_bad() repairs those.
+__device__ __forceinline__ uint32_t fast_key(uint32_t u) {
+  const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+  return k == 0x7fffffffu ? 0x80000000u : k;
+}
+constexpr uint32_t KEY_NEG_INF = 0x007fffffu, KEY_POS_INF = 0xff800000u;
+
 __device__ __forceinline__ float key_value(uint32_t key) {
   const uint32_t u = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
   return __uint_as_float(u);
@@ -327,7 +343,7 @@ __device__ __forceinline__ uint64_t composite(uint32_t key, int token) {
   return ((uint64_t)key << 32) | (uint32_t)(~(uint32_t)token);
 }
 __device__ __forceinline__ int comp_token(uint64_t c) { return (int)(~(uint32_t)c); }
-__device__ __forceinline__ double comp_x(uint64_t c, float temperature) {
+__device__ __noinline__ double comp_x(uint64_t c, float temperature) {
   return (double)key_value((uint32_t)(c >> 32)) / (double)temperature;
 }
 
@@ -353,15 +369,42 @@ struct RowView {
 // ---------------------------------------------------------------------------
 // shared scratch
 // ---------------------------------------------------------------------------
-struct SampSmem {
+constexpr int UNION_MAX = 2048;  // largest candidate union a finish stages in shared memory
+
+struct ChunkScratch {
+  uint32_t keys[CHUNK];          // the chunk: fp32 logits, then their order keys
+  uint32_t penbits[CHUNK / 32];  // penalised tokens of the chunk
+};
+struct DecideScratch {
+  float eh[NCAND], el[NCAND];    // 2^(t_r - t_0) of the sorted candidates, double-float
+  float g32[NCAND];              // their fp32 Gumbel noise
+  float s32[NCAND];              // their fp32 scores
+};
+struct FinishScratch {
+  uint64_t uni[UNION_MAX];       // the chunks' candidates, packed in chunk order
+  union {
+    uint64_t gather[GEN_BLOCK];  // candidates above a selection bound
+    DecideScratch d;             // (after the selection)
+    double es[GEN_BLOCK];        // general path
+  } a;
+};
+
+struct __align__(16) SampSmem {
   float e2h[32], e2l[32];  // the 2^(j/32) table
   float wh[SB / 32], wl[SB / 32];
   uint32_t hist[256];
   uint64_t red_u64[SB / 32];
   uint64_t red_u64b[SB / 32];
-  double red_d[SB];
-  int32_t red_i[SB];
+  uint32_t offer[SB / 32], wtop[SB / 32];
+  double wd[SB / 32];                        // per-warp fp64 partials
+  int32_t wi[SB / 32];                       // per-warp ids
+  int32_t cn[MAX_CHUNKS], coff[MAX_CHUNKS];  // candidates per chunk and their offsets
+  uint64_t htop[MAX_CHUNKS], hthr[MAX_CHUNKS];  // the chunks' largest composites and bounds
+  float fh[MAX_CHUNKS], fl[MAX_CHUNKS];      // the chunks' rescaled normalisers
+  float wbs[SB / 32];                        // per-warp best fp32 scores
   uint64_t sel_prefix;
+  uint64_t nth;      // rank_out: the composite of rank n - 1
+  uint64_t first;    // rank_out: the composite of rank 0
   uint32_t sel_want;
   uint32_t sel_done;
   uint32_t cnt;
@@ -370,21 +413,20 @@ struct SampSmem {
   int32_t kept;
   int32_t done;
   int32_t kp;
+  float zh, zl;      // a normaliser, double-float
   double zsum;
   double s_kept;     // mass (relative to the row maximum) of the kept tokens
   double m_row;      // x of the row maximum
   double xbest;      // x of the sampled token
-  uint32_t penbits[CHUNK / 32];  // penalised tokens of the chunk
-  uint64_t sortbuf[GEN_BLOCK];
-  double es[GEN_BLOCK];
-  uint64_t gbuf[SB];             // block_top_n's gather buffer (finish)
-  float eh[NCAND], el[NCAND];    // 2^(t_r - t_0) of the sorted candidates, double-float
-  float g32[NCAND];              // their fp32 Gumbel noise
-  float s32[NCAND];              // their fp32 scores
-  float fh[MAX_CHUNKS], fl[MAX_CHUNKS];  // the chunks' rescaled normalisers
-  float wbs[SB / 32];            // per-warp best fp32 scores
-  float zh, zl;                  // a normaliser, double-float
+  uint64_t sortbuf[GEN_BLOCK];  // sorted prefixes; the chunk pass's candidate buffer
+  union {
+    ChunkScratch ch;
+    FinishScratch fi;
+  } u;
 };
+static_assert(sizeof(SampSmem) <= 48 * 1024, "static shared memory of one sampler CTA");
+static_assert(offsetof(SampSmem, u) % 16 == 0 && offsetof(SampSmem, sortbuf) % 16 == 0,
+              "16-byte copies into the chunk buffer and the union");
 
 // ---------------------------------------------------------------------------
 // block primitives (all SB threads must call)
@@ -405,16 +447,15 @@ __device__ uint64_t block_max_u64(uint64_t v, SampSmem &sm) {
   return r;
 }
 
-// Sum in a fixed order: thread partials, then a fixed binary tree.
-__device__ double block_sum_d(double v, SampSmem &sm) {
+// Sum in a fixed order: a xor tree in each warp, then the warps in order.
+__device__ __noinline__ double block_sum_d(double v, SampSmem &sm) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(FULL_MASK, v, off);
   __syncthreads();
-  sm.red_d[threadIdx.x] = v;
+  if ((threadIdx.x & 31) == 0) sm.wd[threadIdx.x >> 5] = v;
   __syncthreads();
-  for (int s = SB / 2; s > 0; s >>= 1) {
-    if ((int)threadIdx.x < s) sm.red_d[threadIdx.x] += sm.red_d[threadIdx.x + s];
-    __syncthreads();
-  }
-  const double r = sm.red_d[0];
+  double r = sm.wd[0];
+  for (int w = 1; w < SB / 32; ++w) r += sm.wd[w];
   __syncthreads();
   return r;
 }
@@ -451,26 +492,33 @@ __device__ __forceinline__ bool better(double s, int id, double bs, int bid) {
   return s > bs || (s == bs && id < bid);
 }
 
-__device__ int block_argmax(double s, int id, SampSmem &sm, double *best_score = nullptr) {
-  __syncthreads();
-  sm.red_d[threadIdx.x] = s;
-  sm.red_i[threadIdx.x] = id;
-  __syncthreads();
-  for (int st = SB / 2; st > 0; st >>= 1) {
-    if ((int)threadIdx.x < st) {
-      const double s2 = sm.red_d[threadIdx.x + st];
-      const int i2 = sm.red_i[threadIdx.x + st];
-      if (better(s2, i2, sm.red_d[threadIdx.x], sm.red_i[threadIdx.x])) {
-        sm.red_d[threadIdx.x] = s2;
-        sm.red_i[threadIdx.x] = i2;
-      }
+__device__ __noinline__ int block_argmax(double s, int id, SampSmem &sm,
+                                         double *best_score = nullptr) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const double s2 = __shfl_xor_sync(FULL_MASK, s, off);
+    const int i2 = __shfl_xor_sync(FULL_MASK, id, off);
+    if (better(s2, i2, s, id)) {
+      s = s2;
+      id = i2;
     }
-    __syncthreads();
   }
-  const int r = sm.red_i[0];
-  if (best_score) *best_score = sm.red_d[0];
   __syncthreads();
-  return r;
+  if ((threadIdx.x & 31) == 0) {
+    sm.wd[threadIdx.x >> 5] = s;
+    sm.wi[threadIdx.x >> 5] = id;
+  }
+  __syncthreads();
+  double bs = sm.wd[0];
+  int bid = sm.wi[0];
+  for (int w = 1; w < SB / 32; ++w)
+    if (better(sm.wd[w], sm.wi[w], bs, bid)) {
+      bs = sm.wd[w];
+      bid = sm.wi[w];
+    }
+  if (best_score) *best_score = bs;
+  __syncthreads();
+  return bid;
 }
 
 // Bitonic sort of n (power of two) u64 values in shared memory, descending.
@@ -536,314 +584,498 @@ __device__ void select_bin(SampSmem &sm, int shift) {
 }
 
 // ---------------------------------------------------------------------------
-// chunk pass
+// candidate selection (chunk pass and finish)
 // ---------------------------------------------------------------------------
-// The per-logit loops below with a long body (the double-float exponential,
-// the fp64 Gumbel noise) are rolled loops over the chunk as it lies in global
-// memory (just loaded, so served from L1 / L2): unrolled over the thread's
-// 32 values they were tens of kilobytes of straight-line code, executed once
-// per CTA and stalled on instruction fetch.
+// The sampler kernels run each phase once per row or chunk, so the code they
+// execute is mostly fetched cold: every new line of instructions costs an L2
+// round trip.  The per-element phases are therefore short rolled loops over
+// data staged in shared memory (the chunk's keys, the candidate union), not
+// loops unrolled over register arrays, and the rarely taken paths are kept
+// out of the hot code.
 
-// Sum over the chunk's logits v (penalised where the chunk's bitmap in
-// sm.penbits says so, when pen_on) of 2^(v * c2 - t_max), in double-float;
-// all threads get it.  NaN and -inf logits add 0.
-__device__ __forceinline__ DF chunk_exp_sum(const float *row, int start, int cnt, const Exp2Ctx ctx,
-                                         bool pen_on, float pen, SampSmem &sm) {
-  DF acc = {0.0f, 0.0f};
-#pragma unroll 2
-  for (int i = (int)threadIdx.x; i < cnt; i += SB) {
-    float v = row[start + i];
-    if (pen_on && ((sm.penbits[i >> 5] >> (i & 31)) & 1u)) v = penalise(v, pen);
-    if (v == 0.0f) v = 0.0f;  // -0 ranks as +0
-    df_accumulate(acc, df_exp2_rel(v, ctx, sm.e2h, sm.e2l));
-  }
-  return block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
-}
-
-// Keep everything: the thread's best x + g (fp64, the definition) over the
-// chunk's tokens; *bid < 0 when the thread has none.
-__device__ __forceinline__ void chunk_gumbel_all(const float *row, int start, int cnt,
-                                              const RowParams P, SampSmem &sm, double *bs,
-                                              int *bid, uint32_t *bkey) {
-  *bs = 0.0;
-  *bid = -1;
-  *bkey = 0u;
-  const bool pen_on = P.n_pen > 0;
-#pragma unroll 1
-  for (int i = (int)threadIdx.x; i < cnt; i += SB) {
-    float v = row[start + i];
-    if (pen_on && ((sm.penbits[i >> 5] >> (i & 31)) & 1u)) v = penalise(v, P.pen);
-    bool bad = false;
-    const uint32_t key = order_key(v, bad);
-    const int tok = start + i;
-    const double s = (double)key_value(key) / (double)P.temperature + gumbel(P, tok);
-    if (better(s, tok, *bs, *bid)) {
-      *bs = s;
-      *bid = tok;
-      *bkey = key;
-    }
-  }
-}
-
-// The largest of a thread's N values get(j), as four independent partial
-// maxima (short dependency chains)
-template <int N, class Get>
-__device__ __forceinline__ uint64_t thread_max(Get get) {
-  uint64_t m[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    const uint64_t x = get(j);
-    m[j & 3] = x > m[j & 3] ? x : m[j & 3];
-  }
-  const uint64_t a = m[0] > m[1] ? m[0] : m[1], b = m[2] > m[3] ? m[2] : m[3];
-  return a > b ? a : b;
-}
-
-// The n largest of the block's values without a radix select or a full
-// sort.  Each thread holds N values, get(j) for j < N; 0 means "no value" and
-// the other values are distinct.  Needs n <= SB and at least n nonzero
-// values.  A lower bound L with at least n values >= L comes from the
-// threads' largest values: each warp sorts its 32 (a bitonic network over
-// the lanes) and offers its q-th largest, q = ceil(n / 8); L is the
-// smallest offer, so every warp holds q values >= L (or L is 0 and every
-// nonzero value passes).  The nonzero values >= L -- typically a few dozen
-// more than n -- are gathered into gbuf (SB entries, shared memory) and
-// each one's rank among them is counted: ranks 0 .. n-1 are the n largest,
-// written to out[rank] (descending order), and rank n-1 also to *thr when
-// thr is not null.  top1 receives the largest value in any case.  Returns
-// false, having written nothing to out, when more than SB values pass the
-// bound.
-template <int N, class Get>
-__device__ bool block_top_n(Get get, int n, uint64_t *out, uint64_t *thr, uint64_t *gbuf,
-                            SampSmem &sm, uint64_t &top1) {
-  constexpr int NW = SB / 32;
-  static_assert(N <= 32, "N");
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int q = (n + NW - 1) / NW;
-  uint64_t v = thread_max<N>(get);
+// From the threads' largest keys m: a bound L such that at least n of the
+// block's keys are >= L -- each warp sorts its 32 maxima (a bitonic network
+// over the lanes) and offers its q-th largest, q = ceil(n / 8), and L is the
+// smallest offer, so every warp holds q keys >= L -- and the block's
+// largest key in *top.  n <= SB.  All threads get both.
+__device__ uint32_t select_bound(uint32_t m, int n, SampSmem &sm, uint32_t *top) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int q = (n + (SB / 32) - 1) / (SB / 32);
+  uint32_t v = m;
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1)
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
-      const uint64_t o = __shfl_xor_sync(FULL_MASK, v, j);
+      const uint32_t o = __shfl_xor_sync(FULL_MASK, v, j);
       const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
       v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
     }
-  const uint64_t offer = __shfl_sync(FULL_MASK, v, q - 1);
-  __syncthreads();  // earlier readers of red_u64, red_u64b, cnt and gbuf are done
+  const uint32_t offer = __shfl_sync(FULL_MASK, v, q - 1);
+  __syncthreads();  // earlier readers of the per-warp slots are done
   if (lane == 0) {
-    sm.red_u64[warp] = offer;
-    sm.red_u64b[warp] = v;  // the warp's largest
+    sm.offer[warp] = offer;
+    sm.wtop[warp] = v;  // the warp's largest (lane 0 after the descending sort)
   }
-  if (tid == 0) sm.cnt = 0;
   __syncthreads();
-  uint64_t L = sm.red_u64[0], top = sm.red_u64b[0];
+  uint32_t L = sm.offer[0], t = sm.wtop[0];
 #pragma unroll
-  for (int w = 1; w < NW; ++w) {
-    L = sm.red_u64[w] < L ? sm.red_u64[w] : L;
-    top = sm.red_u64b[w] > top ? sm.red_u64b[w] : top;
+  for (int w = 1; w < SB / 32; ++w) {
+    L = sm.offer[w] < L ? sm.offer[w] : L;
+    t = sm.wtop[w] > t ? sm.wtop[w] : t;
   }
-  top1 = top;
-  // gather: a slot range per warp (one atomic), lanes in order inside it;
-  // bit j of pm marks the thread's value j (independent tests, no chain)
-  uint32_t pm = 0;
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    const uint64_t x = get(j);
-    if (x != 0ull && x >= L) pm |= 1u << j;
-  }
-  const int cnt = __popc(pm);
-  int incl = cnt;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int t = __shfl_up_sync(FULL_MASK, incl, off);
-    if (lane >= off) incl += t;
-  }
-  int base = 0;
-  if (lane == 31) base = (int)atomicAdd(&sm.cnt, (uint32_t)incl);
-  base = __shfl_sync(FULL_MASK, base, 31);
-  const int pos = base + incl - cnt;
-#pragma unroll
-  for (int j = 0; j < N; ++j)
-    if ((pm >> j) & 1u) {
-      const int at = pos + __popc(pm & ((1u << j) - 1u));
-      if (at < SB) gbuf[at] = get(j);
+  *top = t;
+  return L;
+}
+
+// Appends composite(k_i, id0 + i) of every i < n with key k_i = key(i) >= L
+// to gbuf (capacity cap; warp-aggregated appends) and returns how many
+// passed (which may exceed cap).
+template <class Key>
+__device__ int gather_above(int n, Key key, uint32_t L, int id0, uint64_t *gbuf, int cap,
+                            SampSmem &sm) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) sm.cnt = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += SB) {  // warp-uniform trip count
+    const int i = base + (int)threadIdx.x;
+    const uint32_t k = i < n ? key(i) : 0u;
+    const bool hit = i < n && k >= L;
+    const unsigned bm = __ballot_sync(FULL_MASK, hit);
+    if (bm) {
+      int pos = 0;
+      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
+      pos = __shfl_sync(FULL_MASK, pos, 0);
+      if (hit) {
+        const int at = pos + __popc(bm & ((1u << lane) - 1u));
+        if (at < cap) gbuf[at] = composite(k, id0 + i);
+      }
     }
+  }
   __syncthreads();
-  const int C = (int)sm.cnt;
-  if (C > SB) return false;  // the same answer in every thread
-  if (tid < C) {
-    const uint64_t me = gbuf[tid];
+  return (int)sm.cnt;
+}
+
+// The same for composites already formed (the candidate union): every
+// u[i] whose key is >= L.
+__device__ int gather_comp_above(const uint64_t *u, int n, uint32_t L, uint64_t *gbuf, int cap,
+                                 SampSmem &sm) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) sm.cnt = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += SB) {
+    const int i = base + (int)threadIdx.x;
+    const uint64_t c = i < n ? u[i] : 0ull;
+    const bool hit = c != 0ull && (uint32_t)(c >> 32) >= L;
+    const unsigned bm = __ballot_sync(FULL_MASK, hit);
+    if (bm) {
+      int pos = 0;
+      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
+      pos = __shfl_sync(FULL_MASK, pos, 0);
+      if (hit) {
+        const int at = pos + __popc(bm & ((1u << lane) - 1u));
+        if (at < cap) gbuf[at] = c;
+      }
+    }
+  }
+  __syncthreads();
+  return (int)sm.cnt;
+}
+
+// The n largest of the C distinct composites in gbuf, in descending order,
+// to out[0, min(n, C)): each one's rank is the number of larger ones.  Also
+// leaves the composite of rank 0 in sm.first and of rank n - 1 in sm.nth
+// (0 when C < n).
+__device__ void rank_out(const uint64_t *gbuf, int C, int n, uint64_t *out, SampSmem &sm) {
+  if (threadIdx.x == 0) sm.nth = 0ull;
+  __syncthreads();
+  for (int e = threadIdx.x; e < C; e += SB) {
+    const uint64_t me = gbuf[e];
     int r = 0;
+#pragma unroll 4
     for (int k = 0; k < C; ++k) r += gbuf[k] > me ? 1 : 0;
     if (r < n) out[r] = me;
-    if (r == n - 1 && thr != nullptr) *thr = me;
+    if (r == 0) sm.first = me;
+    if (r == n - 1) sm.nth = me;
   }
   __syncthreads();
-  return true;
 }
 
-// The thread's logits of chunk c (element tid + j * SB in raw[j]), every
-// load issued before any is used so that all of them are in flight at once.
-// The frame kernel writes the rows it samples: plain loads, no __ldg.
-__device__ __forceinline__ void load_chunk(const float *row, int V, int c, float (&raw)[EPT]) {
-  const int tid = threadIdx.x;
-  const int start = c * CHUNK;
-  const int cnt = min(CHUNK, V - start);
-  if (cnt == CHUNK) {
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) raw[j] = row[start + tid + j * SB];
+// ---------------------------------------------------------------------------
+// chunk pass
+// ---------------------------------------------------------------------------
+// The chunk [start, start + cnt) of `row` into buf as fp32 bits; every copy
+// is issued before any is waited for.
+__device__ __forceinline__ void stage_chunk(const float *row, int start, int cnt, uint32_t *buf) {
+  const float *src = row + start;
+  if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (cnt & 3) == 0) {
+    for (int i = 4 * (int)threadIdx.x; i < cnt; i += 4 * SB) cp_async16(buf + i, src + i);
   } else {
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) raw[j] = tid + j * SB < cnt ? row[start + tid + j * SB] : 0.0f;
+    for (int i = (int)threadIdx.x; i < cnt; i += SB) cp_async4(buf + i, src + i);
   }
+  cp_async_wait_all();
+  __syncthreads();
 }
 
-// raw: the thread's logits of chunk c (load_chunk).  pbits: the row's
-// penalty bitmap in global memory, written for this chunk when the row is
-// penalised (may be null otherwise)
-__device__ void chunk_pass(const float (&raw)[EPT], const float *row, int V, int c,
-                           const RowParams &P, ChunkRec *rec, uint32_t *pbits, SampSmem &sm,
-                           int32_t *err) {
-  const int tid = threadIdx.x;
-  const int start = c * CHUNK;
-  const int cnt = min(CHUNK, V - start);
-  uint32_t key[EPT];
+// Sum over the chunk of 2^(key_value(k) * c2 - t_max), in double-float; all
+// threads get it.  NaN and -inf logits add 0.
+__device__ DF chunk_exp_sum(const uint32_t *keys, int cnt, const Exp2Ctx ctx, SampSmem &sm) {
+  DF acc = {0.0f, 0.0f};
+#pragma unroll 2
+  for (int i = (int)threadIdx.x; i < cnt; i += SB)
+    df_accumulate(acc, df_exp2_rel(key_value(keys[i]), ctx, sm.e2h, sm.e2l));
+  return block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
+}
+
+// The keys of NaN logits (outside [key(-inf), key(+inf)]) set to key(-inf):
+// a NaN ranks like -inf; NaN and +inf are reported.  Returns the thread's
+// largest key after the repair.
+__device__ __noinline__ uint32_t keys_fix_bad(uint32_t *keys, int cnt, int32_t *err) {
+  uint32_t m = 0;
   bool bad = false;
-#pragma unroll
-  for (int j = 0; j < EPT; ++j) {
-    const int i = tid + j * SB;
-    key[j] = (i < cnt) ? order_key(raw[j], bad) : 0u;
+  for (int i = threadIdx.x; i < cnt; i += SB) {
+    uint32_t k = keys[i];
+    if (k > KEY_POS_INF || k < KEY_NEG_INF) {
+      k = KEY_NEG_INF;
+      keys[i] = k;
+      bad = true;
+    } else if (k == KEY_POS_INF) {
+      bad = true;
+    }
+    m = k > m ? k : m;
   }
   if (bad) report(err, PKV_DEV_ERR_LOGITS);
-  if (P.lp_raw) {
-    // raw log-softmax partials: chunk maximum of the unprocessed logits and
-    // sum exp(logit - max) = sum 2^((logit - max) log2(e))
-    uint32_t km = 0;
+  return m;
+}
+
+// Appends composite(k, id0 + i) of every key k = keys[i] >= L (i < n) to
+// gbuf (capacity cap; warp-aggregated) and returns how many passed (which
+// may exceed cap).  Four keys per thread at a time, then the tail.
+__device__ int gather_keys_above(const uint32_t *keys, int n, uint32_t L, int id0,
+                                 uint64_t *gbuf, int cap, SampSmem &sm) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) sm.cnt = 0;
+  __syncthreads();
+  const int nq = n >> 2;
+  const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
+  for (int base = 0; base < nq; base += SB) {  // warp-uniform trip count
+    const int q = base + (int)threadIdx.x;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (q < nq) u = k4[q];
+    const uint32_t h = (u.x >= L ? 1u : 0u) | (u.y >= L ? 2u : 0u) | (u.z >= L ? 4u : 0u) |
+                       (u.w >= L ? 8u : 0u);
+    const uint32_t hm = q < nq ? h : 0u;
+    if (__ballot_sync(FULL_MASK, hm != 0u)) {
+      const int mine = __popc(hm);
+      int incl = mine;
 #pragma unroll
-    for (int j = 0; j < EPT; ++j)
-      if (tid + j * SB < cnt) km = key[j] > km ? key[j] : km;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(FULL_MASK, incl, off);
+        if (lane >= off) incl += o;
+      }
+      int pos = 0;
+      if (lane == 31) pos = (int)atomicAdd(&sm.cnt, (uint32_t)incl);
+      pos = __shfl_sync(FULL_MASK, pos, 31) + incl - mine;
+      const uint32_t kk[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((hm >> e) & 1u) {
+          if (pos < cap) gbuf[pos] = composite(kk[e], id0 + 4 * q + e);
+          ++pos;
+        }
+    }
+  }
+  for (int base = 4 * nq; base < n; base += SB) {
+    const int i = base + (int)threadIdx.x;
+    const uint32_t k = i < n ? keys[i] : 0u;
+    const bool hit = i < n && k >= L;
+    const unsigned bm = __ballot_sync(FULL_MASK, hit);
+    if (bm) {
+      int pos = 0;
+      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
+      pos = __shfl_sync(FULL_MASK, pos, 0);
+      if (hit) {
+        const int at = pos + __popc(bm & ((1u << lane) - 1u));
+        if (at < cap) gbuf[at] = composite(k, id0 + i);
+      }
+    }
+  }
+  __syncthreads();
+  return (int)sm.cnt;
+}
+
+// chunk_exp_sum, split by size: a term below 2^-24 of the chunk's largest
+// (t - t_max < -24, t formed in fp32) is taken on the SFU in fp32 -- its
+// error, under 2^-24 * 3e-6 of the largest, is far below the double-float
+// sum's -- and only the larger ones (the chunk's top few percent) get the
+// double-float exponential, from a list of their positions.  The same sum
+// as chunk_exp_sum to ~1e-9 relative; all threads get it.
+__device__ DF chunk_exp_sum_split(const uint32_t *keys, int cnt, const Exp2Ctx ctx,
+                                  SampSmem &sm) {
+  const int lane = threadIdx.x & 31;
+  uint32_t *big = reinterpret_cast<uint32_t *>(sm.sortbuf);  // positions of the larger terms
+  constexpr int BIG_CAP = GEN_BLOCK * 2;
+  if (threadIdx.x == 0) sm.cnt = 0;
+  __syncthreads();
+  float small = 0.0f;
+  for (int base = 0; base < cnt; base += SB) {  // warp-uniform trip count
+    const int i = base + (int)threadIdx.x;
+    bool is_big = false;
+    if (i < cnt) {
+      const float t = fmaf(key_value(keys[i]), ctx.c2h, -ctx.th);
+      if (t < -24.0f)
+        small += fast_exp2(t);  // NaN and -inf logits give 0
+      else
+        is_big = true;
+    }
+    const unsigned bm = __ballot_sync(FULL_MASK, is_big);
+    if (bm) {
+      int pos = 0;
+      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
+      pos = __shfl_sync(FULL_MASK, pos, 0);
+      if (is_big) {
+        const int at = pos + __popc(bm & ((1u << lane) - 1u));
+        if (at < BIG_CAP) big[at] = (uint32_t)i;
+      }
+    }
+  }
+  __syncthreads();
+  const int nbig = (int)sm.cnt;
+  if (nbig > BIG_CAP) return chunk_exp_sum(keys, cnt, ctx, sm);  // every term in double-float
+  DF acc = {0.0f, 0.0f};
+  for (int j = threadIdx.x; j < nbig; j += SB)
+    df_accumulate(acc, df_exp2_rel(key_value(keys[big[j]]), ctx, sm.e2h, sm.e2l));
+  df_accumulate(acc, DF{small, 0.0f});
+  return block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
+}
+
+// Keep everything: the chunk's Gumbel argmax in fp64 (the definition);
+// block result in *bs, *bid, *bkey (tid 0).
+__device__ __noinline__ void chunk_gumbel_all(const uint32_t *keys, int start, int cnt,
+                                              const RowParams P, SampSmem &sm, double *bs,
+                                              int *bid, uint32_t *bkey) {
+  double s0 = 0.0;
+  int id0 = -1;
+  uint32_t k0 = 0u;
+  for (int i = (int)threadIdx.x; i < cnt; i += SB) {
+    const int tok = start + i;
+    const double s = (double)key_value(keys[i]) / (double)P.temperature + gumbel(P, tok);
+    if (better(s, tok, s0, id0)) {
+      s0 = s;
+      id0 = tok;
+      k0 = keys[i];
+    }
+  }
+  double best;
+  const int id = block_argmax(s0, id0, sm, &best);
+  if (id0 == id && id >= 0) sm.token = (int32_t)k0;
+  __syncthreads();
+  *bs = best;
+  *bid = id;
+  *bkey = (uint32_t)sm.token;
+}
+
+// The chunk's nc largest composites (unsorted) and their bound by an exact
+// radix select over 8-bit digits: for top-k above 256, or when the
+// selection bound lets more than GEN_BLOCK keys through (many ties).
+__device__ __noinline__ void chunk_radix_top(const uint32_t *keys, int start, int cnt, int nc,
+                                             ChunkRec *rec, SampSmem &sm) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    sm.sel_prefix = 0;
+    sm.sel_want = (uint32_t)nc;
+    sm.sel_done = 0;
+  }
+  __syncthreads();
+  uint64_t mask = 0;
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    for (int i = tid; i < 256; i += SB) sm.hist[i] = 0;
+    __syncthreads();
+    const uint64_t prefix = sm.sel_prefix;
+    for (int i = tid; i < cnt; i += SB) {
+      const uint64_t cc = composite(keys[i], start + i);
+      if ((cc & mask) == prefix) atomicAdd(&sm.hist[(cc >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    select_bin(sm, shift);
+    mask |= 255ull << shift;
+    if (sm.sel_done) break;
+  }
+  const uint64_t thr = sm.sel_prefix;
+  __syncthreads();
+  if (tid == 0) sm.cnt = 0;
+  __syncthreads();
+  for (int i = tid; i < cnt; i += SB) {
+    const uint64_t cc = composite(keys[i], start + i);
+    if (cc >= thr) {
+      const uint32_t pos = atomicAdd(&sm.cnt, 1u);
+      if (pos < (uint32_t)nc) rec->cand[pos] = cc;
+    }
+  }
+  __syncthreads();
+  const int got = min((int)sm.cnt, nc);
+  for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0ull;
+  if (tid == 0) {
+    rec->ncand = got;
+    rec->thr = thr;
+    rec->sorted = 0;
+  }
+}
+
+// One chunk of a row: stage it, form the order keys (penalty applied), then
+// per mode the chunk's largest composite, its nc largest composites with
+// their bound, the normaliser partial or the Gumbel winner, into *rec.
+// pbits: the row's penalty bitmap in global memory, written for this chunk
+// when the row is penalised (may be null otherwise).  prestaged: the
+// caller has already put the chunk's logits into sm.u.ch.keys.
+__device__ __noinline__ void chunk_pass(const float *row, int V, int c, const RowParams &P,
+                                        ChunkRec *rec,
+                           uint32_t *pbits, SampSmem &sm, int32_t *err, bool prestaged = false) {
+  const int tid = threadIdx.x;
+  const int start = c * CHUNK;
+  const int cnt = min(CHUNK, V - start);
+  uint32_t *keys = sm.u.ch.keys;
+  if (!prestaged) stage_chunk(row, start, cnt, keys);
+  if (P.lp_raw) {
+    // raw log-softmax partials: the chunk maximum of the unprocessed logits
+    // and sum exp(logit - max) = sum 2^((logit - max) log2(e))
+    uint32_t km = 0;
+    bool b2 = false;
+    for (int i = tid; i < cnt; i += SB) {
+      const uint32_t k = order_key(__uint_as_float(keys[i]), b2);
+      km = k > km ? k : km;
+    }
     const float rmax = key_value((uint32_t)block_max_u64(km, sm));
-    const DF z = chunk_exp_sum(row, start, cnt, exp2_ctx(LOG2E_H, LOG2E_L, rmax), false, 1.0f,
-                               sm);
+    const Exp2Ctx ctx = exp2_ctx(LOG2E_H, LOG2E_L, rmax);
+    DF acc = {0.0f, 0.0f};
+    for (int i = tid; i < cnt; i += SB)
+      df_accumulate(acc, df_exp2_rel(key_value(order_key(__uint_as_float(keys[i]), b2)), ctx,
+                                     sm.e2h, sm.e2l));
+    const DF z = block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
     if (tid == 0) {
       rec->rmax = rmax;
       rec->rzh = z.h;
       rec->rzl = z.l;
     }
   }
-  if (P.n_pen > 0) {
+  const bool pen_on = P.n_pen > 0;
+  uint32_t *penbits = sm.u.ch.penbits;
+  if (pen_on) {
     // the penalty window's tokens that fall in this chunk, as a bitmap
     // (a token repeated in the window is penalised once)
-    for (int w = tid; w < CHUNK / 32; w += SB) sm.penbits[w] = 0u;
+    for (int w = tid; w < CHUNK / 32; w += SB) penbits[w] = 0u;
     __syncthreads();
     for (int i = tid; i < P.n_pen; i += SB) {
       const int32_t t = pen_token(P, i);
       if (t >= start && t < start + cnt)
-        atomicOr(&sm.penbits[(t - start) >> 5], 1u << ((t - start) & 31));
+        atomicOr(&penbits[(t - start) >> 5], 1u << ((t - start) & 31));
     }
     __syncthreads();
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int i = tid + j * SB;
-      if (i < cnt && ((sm.penbits[i >> 5] >> (i & 31)) & 1u)) {
-        bool b2 = false;
-        key[j] = order_key(penalise(key_value(key[j]), P.pen), b2);
-      }
-    }
     if (pbits != nullptr)
-      for (int w = tid; w < (cnt + 31) / 32; w += SB) pbits[c * (CHUNK / 32) + w] = sm.penbits[w];
+      for (int w = tid; w < (cnt + 31) / 32; w += SB) pbits[c * (CHUNK / 32) + w] = penbits[w];
   }
-  auto comp_at = [&](int j) -> uint64_t {
-    const int i = tid + j * SB;
-    return i < cnt ? composite(key[j], start + i) : 0ull;
-  };
-  // the chunk's nc largest composites (candidate modes), and its largest
+  // the order keys, in place, and the thread's largest: four per thread at
+  // a time (16-byte shared-memory accesses), then the tail
+  uint32_t m = 0;
+  const int nq = cnt >> 2;
+  uint4 *k4 = reinterpret_cast<uint4 *>(keys);
+  if (!pen_on) {
+    uint32_t kmin = 0xffffffffu;
+#pragma unroll 2
+    for (int q = tid; q < nq; q += SB) {
+      uint4 u = k4[q];
+      u.x = fast_key(u.x);
+      u.y = fast_key(u.y);
+      u.z = fast_key(u.z);
+      u.w = fast_key(u.w);
+      k4[q] = u;
+      const uint32_t a = u.x > u.y ? u.x : u.y, b = u.z > u.w ? u.z : u.w;
+      const uint32_t c2 = u.x < u.y ? u.x : u.y, d2 = u.z < u.w ? u.z : u.w;
+      m = max(m, max(a, b));
+      kmin = min(kmin, min(c2, d2));
+    }
+    for (int i = 4 * nq + tid; i < cnt; i += SB) {
+      const uint32_t k = fast_key(keys[i]);
+      keys[i] = k;
+      m = max(m, k);
+      kmin = min(kmin, k);
+    }
+    // a NaN or +inf anywhere in the chunk: every thread repairs its part
+    // (in the one-per-thread layout, once all the keys are written)
+    if (__syncthreads_or(m >= KEY_POS_INF || kmin < KEY_NEG_INF)) m = keys_fix_bad(keys, cnt, err);
+  } else {
+    bool bad = false;
+    for (int i = tid; i < cnt; i += SB) {
+      float v = __uint_as_float(keys[i]);
+      if ((penbits[i >> 5] >> (i & 31)) & 1u) v = penalise(v, P.pen);
+      const uint32_t k = order_key(v, bad);
+      keys[i] = k;
+      m = k > m ? k : m;
+    }
+    if (bad) report(err, PKV_DEV_ERR_LOGITS);
+  }
+  __syncthreads();  // the keys, written four per thread, are read in other layouts below
   const int nc = P.nc;
   const bool sel = P.mode == MODE_TOPK_SMALL || P.mode == MODE_TOPP_FULL;
-  uint64_t top1 = 0;
-  bool fast = false;
-  if (sel && cnt > nc && nc <= SB) {
-    fast = block_top_n<EPT>(comp_at, nc, rec->cand, &rec->thr, sm.sortbuf, sm, top1);
-    if (fast && tid == 0) rec->ncand = nc;
-  } else {
-    top1 = block_max_u64(thread_max<EPT>(comp_at), sm);
+  uint64_t top1 = 0ull;
+  if (sel && nc <= SB) {
+    // the keys at or above a bound that lets at least nc through, then the
+    // nc largest of those in order
+    uint32_t topkey;
+    const uint32_t L = select_bound(m, nc, sm, &topkey);
+    const int C = gather_keys_above(keys, cnt, L, start, sm.sortbuf, GEN_BLOCK, sm);
+    if (C <= GEN_BLOCK) {
+      rank_out(sm.sortbuf, C, nc, rec->cand, sm);
+      const int got = min(C, nc);
+      for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0ull;
+      if (tid == 0) {
+        rec->ncand = got;
+        rec->sorted = 1;
+        // every token not given is below the bound: the nc-th candidate
+        // when more passed, else the bound's key
+        rec->thr = cnt > got ? (C > nc ? sm.nth : (uint64_t)L << 32) : 0ull;
+      }
+      top1 = sm.first;
+    } else {
+      chunk_radix_top(keys, start, cnt, nc, rec, sm);
+    }
+  } else if (sel) {
+    chunk_radix_top(keys, start, cnt, nc, rec, sm);
   }
-  if (tid == 0) rec->top1 = top1;
-  if (P.mode == MODE_GREEDY || P.mode == MODE_GENERAL) return;
+  if (top1 == 0ull) {
+    // the chunk's largest composite: its largest key at its lowest id
+    uint64_t best = 0ull;
+    for (int i = tid; i < cnt; i += SB) {
+      const uint64_t cc = composite(keys[i], start + i);
+      best = cc > best ? cc : best;
+    }
+    top1 = block_max_u64(best, sm);
+  }
+  if (tid == 0) {
+    rec->top1 = top1;
+    if (!sel) {  // no candidates in this mode: a defined, empty list
+      rec->ncand = 0;
+      rec->thr = 0ull;
+      rec->sorted = 1;
+    }
+    if (!P.need_z) rec->zh = rec->zl = 0.0f;
+  }
 
   if (P.mode == MODE_ALL) {
     double bs;
     int bid;
     uint32_t bkey;
-    chunk_gumbel_all(row, start, cnt, P, sm, &bs, &bid, &bkey);
-    double best;
-    const int id = block_argmax(bs, bid, sm, &best);
+    chunk_gumbel_all(keys, start, cnt, P, sm, &bs, &bid, &bkey);
     if (tid == 0) {
-      rec->gscore = best;
-      rec->gid = id;
-    }
-    if (bid == id && id >= 0) rec->gkey = bkey;
-  } else {
-    // the chunk's nc largest composites, unless the fast selection wrote them
-    uint64_t thr = 0;  // keep composites >= thr
-    if (!fast && cnt > nc) {
-      if (tid == 0) {
-        sm.sel_prefix = 0;
-        sm.sel_want = (uint32_t)nc;
-        sm.sel_done = 0;
-      }
-      __syncthreads();
-      uint64_t mask = 0;
-      for (int pass = 0; pass < 8; ++pass) {
-        const int shift = 56 - 8 * pass;
-        for (int i = tid; i < 256; i += SB) sm.hist[i] = 0;
-        __syncthreads();
-        const uint64_t prefix = sm.sel_prefix;
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) {
-          const int i = tid + j * SB;
-          if (i < cnt) {
-            const uint64_t cc = composite(key[j], start + i);
-            if ((cc & mask) == prefix) atomicAdd(&sm.hist[(cc >> shift) & 255u], 1u);
-          }
-        }
-        __syncthreads();
-        select_bin(sm, shift);
-        mask |= 255ull << shift;
-        if (sm.sel_done) break;
-      }
-      thr = sm.sel_prefix;
-      __syncthreads();
-    }
-    if (!fast) {
-      if (tid == 0) sm.cnt = 0;
-      __syncthreads();
-#pragma unroll
-      for (int j = 0; j < EPT; ++j) {
-        const int i = tid + j * SB;
-        if (i < cnt) {
-          const uint64_t cc = composite(key[j], start + i);
-          if (cc >= thr) {
-            const uint32_t pos = atomicAdd(&sm.cnt, 1u);
-            if (pos < (uint32_t)nc) rec->cand[pos] = cc;
-          }
-        }
-      }
-      __syncthreads();
-      const int got = min((int)sm.cnt, nc);
-      for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0;
-      if (tid == 0) {
-        rec->ncand = got;
-        rec->thr = cnt > nc ? thr : 0ull;
-      }
+      rec->gscore = bs;
+      rec->gid = bid;
+      rec->gkey = bkey;
     }
   }
-
   if (P.need_z) {
     // sum over the chunk of exp(x - mx) = 2^(t - t_max), t = logit * log2(e) / T
     const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
-    const DF z = chunk_exp_sum(row, start, cnt, ctx, P.n_pen > 0, P.pen, sm);
+    const DF z = chunk_exp_sum_split(keys, cnt, ctx, sm);
     if (tid == 0) {
       rec->zh = z.h;
       rec->zl = z.l;
@@ -922,7 +1154,7 @@ __device__ uint64_t select_rank(const RowView &rv, int V, uint64_t upper, int ra
 // relative to the row maximum (top-p over the whole vocabulary, min_p off).
 // With log-probs requested, leaves the kept mass, the row maximum's x and
 // the sampled token's x in sm.s_kept, sm.m_row and sm.xbest.
-__device__ int general_sample(const RowView &rv, int V, const RowParams &P, uint64_t top1,
+__device__ __noinline__ int general_sample(const RowView &rv, int V, const RowParams &P, uint64_t top1,
                               double z_known, SampSmem &sm) {
   const int tid = threadIdx.x;
   const int K = P.K;
@@ -973,13 +1205,13 @@ __device__ int general_sample(const RowView &rv, int V, const RowParams &P, uint
       for (int i = M + tid; i < n2; i += SB) sm.sortbuf[i] = 0;
       __syncthreads();
       block_sort_desc(sm.sortbuf, n2);
-      for (int r = tid; r < M; r += SB) sm.es[r] = exp(comp_x(sm.sortbuf[r], P.temperature) - m);
+      for (int r = tid; r < M; r += SB) sm.u.fi.a.es[r] = exp(comp_x(sm.sortbuf[r], P.temperature) - m);
       __syncthreads();
       if (tid == 0) {
         int r = 0;
         for (; r < M; ++r) {
-          if (taken + r == 0 || (S < pz && (!minp || sm.es[r] >= (double)P.min_p))) {
-            S += sm.es[r];
+          if (taken + r == 0 || (S < pz && (!minp || sm.u.fi.a.es[r] >= (double)P.min_p))) {
+            S += sm.u.fi.a.es[r];
             cutoff = sm.sortbuf[r];
           } else {
             break;
@@ -1056,30 +1288,137 @@ __device__ int general_sample(const RowView &rv, int V, const RowParams &P, uint
 //    winner; otherwise the ranks within that margin are scored again in fp64
 //    exactly as the definition states, and the token is theirs.
 
-constexpr int UNION_PT = 8;               // union slots per thread in union_top_n
-constexpr int UNION_MAX = UNION_PT * SB;  // largest union taken by union_top_n
+// The chunk records' headers into shared memory (one pass, every chunk at
+// once): candidates, largest composite, bound, normaliser partial; and the
+// candidates themselves into sm.u.fi.uni at stride R (a power of two >= nc;
+// zeros past each chunk's count) when nch * R <= UNION_MAX.  Returns the
+// total number of candidates; *all_sorted tells whether every chunk's list
+// is in descending order.
+__device__ int stage_records(const ChunkRec *recs, int nch, int nc, int R, SampSmem &sm,
+                             bool *all_sorted) {
+  const int tid = threadIdx.x;
+  if (tid < nch) {
+    const ChunkRec &rc = recs[tid];
+    sm.cn[tid] = rc.ncand;
+    sm.htop[tid] = rc.top1;
+    sm.hthr[tid] = rc.thr;
+    sm.fh[tid] = rc.zh;
+    sm.fl[tid] = rc.zl;
+    sm.coff[tid] = rc.sorted;
+  }
+  if (nch * R <= UNION_MAX) {
+    uint64_t *uni = sm.u.fi.uni;
+    for (int i = tid; i < nch * R; i += SB) {
+      const int c = i / R, k = i - c * R;  // R is a power of two
+      if (k < nc)
+        cp_async8(uni + i, recs[c].cand + k);
+      else
+        uni[i] = 0ull;
+    }
+    cp_async_wait_all();
+  }
+  __syncthreads();
+  int total = 0;
+  bool srt = true;
+  for (int c = 0; c < nch; ++c) {
+    total += sm.cn[c];
+    srt = srt && sm.coff[c] != 0;
+  }
+  *all_sorted = srt;
+  return total;
+}
 
-// The n largest composites of the union of the chunks' candidates (chunk c
-// holds nc slots, zero past its ncand), in descending order, into
-// sm.sortbuf[0, n).  Needs nu = nch * nc <= UNION_MAX, n <= SB and n
-// nonzero slots; false (nothing written) when more than SB slots pass the
-// selection bound.
-__device__ bool union_top_n(const ChunkRec *recs, int nc, int nu, int n, SampSmem &sm) {
-  const uint64_t magic = ((1ull << 32) + (uint64_t)nc - 1ull) / (uint64_t)nc;  // i / nc, i < 2^16
-  auto get = [&](int k) -> uint64_t {
-    const int i = (int)threadIdx.x + k * SB;
-    if (i >= nu) return 0ull;
-    const int c = (int)(((uint64_t)i * magic) >> 32);
-    return recs[c].cand[i - c * nc];
-  };
-  uint64_t t1;
-  return block_top_n<UNION_PT>(get, n, sm.sortbuf, nullptr, sm.gbuf, sm, t1);
+// The n largest composites of the staged union (nch lists at stride R,
+// each in descending order, zeros past its count), in descending order,
+// into sm.sortbuf[0, n).  The bound comes from the lists' heads: the n-th
+// largest of the first d = ceil(n / nch) + 4 entries of every list is at
+// most the union's n-th largest, so every composite of the union at or
+// above it (typically a few more than n) is gathered and ranked.  n <= SB;
+// false (nothing written) when more than SB heads or GEN_BLOCK composites
+// would take part.
+__device__ bool union_select(int nch, int R, int n, SampSmem &sm) {
+  const uint64_t *uni = sm.u.fi.uni;
+  uint64_t *g = sm.u.fi.a.gather;
+  const int d = min(R, (n + nch - 1) / nch + 4);
+  const int ns = nch * d;
+  if (ns > SB) return false;
+  // the heads, then the n-th largest of them
+  const int t = threadIdx.x;
+  if (t < ns) g[t] = uni[(t / d) * R + t % d];
+  if (t == 0) {
+    sm.nth = 0ull;
+    sm.cnt = 0;
+  }
+  __syncthreads();
+  if (t < ns && g[t] != 0ull) {
+    const uint64_t me = g[t];
+    int r = 0;
+    for (int k = 0; k < ns; ++k) r += g[k] > me ? 1 : 0;
+    if (r == n - 1) sm.nth = me;
+  }
+  __syncthreads();
+  const uint64_t bound = sm.nth;  // 0 when the heads hold fewer than n: take everything
+  __syncthreads();
+  // every composite of the union at or above the bound
+  const int lane = t & 31;
+  for (int base = 0; base < nch * R; base += SB) {
+    const int i = base + t;
+    const uint64_t c = i < nch * R ? uni[i] : 0ull;
+    const bool hit = c != 0ull && c >= bound;
+    const unsigned bm = __ballot_sync(FULL_MASK, hit);
+    if (bm) {
+      int pos = 0;
+      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
+      pos = __shfl_sync(FULL_MASK, pos, 0);
+      if (hit) {
+        const int at = pos + __popc(bm & ((1u << lane) - 1u));
+        if (at < GEN_BLOCK) g[at] = c;
+      }
+    }
+  }
+  __syncthreads();
+  const int C = (int)sm.cnt;
+  if (C > GEN_BLOCK) return false;
+  rank_out(g, C, n, sm.sortbuf, sm);
+  return true;
+}
+
+// Sorts v[0, n) descending, n a power of two, given runs of length R (a
+// power of two) that are each already descending: bitonic merges of pairs
+// of runs (the second run taken in reverse, then half-cleaners), run length
+// doubling up to n.  R = 1 sorts from scratch.
+__device__ void block_merge_runs_desc(uint64_t *v, int n, int R) {
+  for (int len = 2 * R; len <= n; len <<= 1) {
+    const int half = len >> 1;
+    for (int p = threadIdx.x; p < n / 2; p += SB) {
+      const int blk = p / half, i = p - blk * half;
+      const int a = blk * len + i, b = blk * len + len - 1 - i;
+      const uint64_t x = v[a], y = v[b];
+      if (x < y) {
+        v[a] = y;
+        v[b] = x;
+      }
+    }
+    __syncthreads();
+    for (int j = half >> 1; j > 0; j >>= 1) {
+      for (int p = threadIdx.x; p < n / 2; p += SB) {
+        const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
+        const uint64_t x = v[i], y = v[i + j];
+        if (x < y) {
+          v[i] = y;
+          v[i + j] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
 }
 
 // The nv largest composites of the union in descending order into
-// sm.sortbuf[0, nv) (nv <= NCAND): a radix select of the nv-th, the gather,
-// a bitonic sort.
-__device__ void union_sorted_slow(const ChunkRec *recs, int nc, int nu, int nv, SampSmem &sm) {
+// sm.sortbuf[0, nv) (nv <= NCAND), read from the records in global memory:
+// a radix select of the nv-th, the gather, a bitonic sort.
+__device__ __noinline__ void union_sorted_slow(const ChunkRec *recs, int nc, int nu, int nv,
+                                               SampSmem &sm) {
   const int tid = threadIdx.x;
   auto cand_at = [&](int i) -> uint64_t { return recs[i / nc].cand[i % nc]; };
   const uint64_t thr = select_rank_of(nu, cand_at, ~0ull, nv - 1, sm);
@@ -1101,17 +1440,17 @@ __device__ void union_sorted_slow(const ChunkRec *recs, int nc, int nu, int nv, 
 }
 
 // The normaliser of the whole row relative to its maximum: the chunks'
-// partials z_c (relative to each chunk's maximum) times 2^(t_c - t_0),
-// added in chunk order.
-__device__ DF row_normaliser(const ChunkRec *recs, int nch, const Exp2Ctx &ctx, SampSmem &sm) {
+// partials z_c (relative to each chunk's maximum; staged in sm.fh / sm.fl)
+// times 2^(t_c - t_0), added in chunk order.
+__device__ DF row_normaliser(int nch, const Exp2Ctx &ctx, SampSmem &sm) {
   const int tid = threadIdx.x;
+  DF f = {0.0f, 0.0f};
+  if (tid < nch && sm.htop[tid] != 0ull) {
+    const DF w = df_exp2_rel(key_value((uint32_t)(sm.htop[tid] >> 32)), ctx, sm.e2h, sm.e2l);
+    f = df_mul(DF{sm.fh[tid], sm.fl[tid]}, w);
+  }
   __syncthreads();
   if (tid < nch) {
-    DF f = {0.0f, 0.0f};
-    if (recs[tid].top1 != 0ull) {
-      const DF w = df_exp2_rel(key_value((uint32_t)(recs[tid].top1 >> 32)), ctx, sm.e2h, sm.e2l);
-      f = df_mul(DF{recs[tid].zh, recs[tid].zl}, w);
-    }
     sm.fh[tid] = f.h;
     sm.fl[tid] = f.l;
   }
@@ -1128,56 +1467,100 @@ __device__ DF row_normaliser(const ChunkRec *recs, int nch, const Exp2Ctx &ctx, 
   return z;
 }
 
-// Warp 0: the first rank r >= max(lo, 1) in [lo, hi) with e_r < min_p, or -1.
-__device__ int minp_boundary_warp(const SampSmem &sm, int lo, int hi, float min_p) {
-  for (int base = max(lo, 1); base < hi; base += 32) {
-    const int r = base + (int)(threadIdx.x & 31);
-    bool below = false;
-    if (r < hi) below = sm.eh[r] < min_p || (sm.eh[r] == min_p && sm.el[r] < 0.0f);
-    const unsigned bm = __ballot_sync(FULL_MASK, below);
-    if (bm) return base + __ffs(bm) - 1;
-  }
-  return -1;
+// The first rank r in [1, n) with e_r < min_p, or n (all threads).
+__device__ int minp_boundary(int n, float min_p, SampSmem &sm) {
+  const DecideScratch &d = sm.u.fi.a.d;
+  int first = n;
+  for (int r = 1 + (int)threadIdx.x; r < n; r += SB)
+    if ((d.eh[r] < min_p || (d.eh[r] == min_p && d.el[r] < 0.0f)) && r < first) first = r;
+  first = __reduce_min_sync(FULL_MASK, first);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.wi[threadIdx.x >> 5] = first;
+  __syncthreads();
+  int m = sm.wi[0];
+  for (int w = 1; w < SB / 32; ++w) m = sm.wi[w] < m ? sm.wi[w] : m;
+  __syncthreads();
+  return m;
 }
 
-// Warp 0: top-p over ranks [0, n): rank r is kept iff r == 0 or the sum of
-// the e's before it is below pz (double-float prefix sums, 32 ranks at a
-// time by shuffles).  Returns the first rank not kept, or n.
-__device__ int topp_cut_warp(const SampSmem &sm, int n, DF pz) {
-  const int lane = threadIdx.x & 31;
-  DF carry = {0.0f, 0.0f};
-  for (int base = 0; base < n; base += 32) {
-    const int r = base + lane;
-    DF inc = r < n ? DF{sm.eh[r], sm.el[r]} : DF{0.0f, 0.0f};
+// Sum of e_r over ranks [0, n) in a fixed order (each thread its ranks in
+// order, then a xor tree per warp, then the warps in order); all threads.
+__device__ DF mass_of_prefix(int n, SampSmem &sm) {
+  const DecideScratch &d = sm.u.fi.a.d;
+  DF part = {0.0f, 0.0f};
+  for (int r = threadIdx.x; r < n; r += SB) part = df_add(part, DF{d.eh[r], d.el[r]});
+  return block_sum_df(part, sm);
+}
+
+// Top-p over ranks [0, n), n <= SB * 2: rank r is kept iff r == 0 or the
+// sum of the e's before it is below pz.  Each warp scans its 64 ranks
+// (double-float prefix sums by shuffles), the warps' totals give each its
+// carry, and the first rank not kept is the smallest over the warps.
+// Returns it, or n (all threads).
+__device__ int topp_cut_block(int n, DF pz, SampSmem &sm) {
+  const DecideScratch &d = sm.u.fi.a.d;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r0 = warp * 64;
+  DF inc[2];
+  DF tot = {0.0f, 0.0f};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = r0 + 32 * h + lane;
+    DF v = r < n ? DF{d.eh[r], d.el[r]} : DF{0.0f, 0.0f};
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const DF o = df_shfl_up(inc, off);
-      if (lane >= off) inc = df_add(inc, o);
+      const DF o = df_shfl_up(v, off);
+      if (lane >= off) v = df_add(v, o);
     }
-    DF ex = df_shfl_up(inc, 1);
-    if (lane == 0) ex = DF{0.0f, 0.0f};
-    const DF before = df_add(carry, ex);
-    const bool stop = r < n && r > 0 && !df_lt(before, pz);
-    const unsigned bm = __ballot_sync(FULL_MASK, stop);
-    if (bm) return base + __ffs(bm) - 1;
-    carry = df_add(carry, df_shfl(inc, 31));
+    inc[h] = df_add(tot, v);  // inclusive prefix within the warp's 64 ranks
+    tot = df_add(tot, df_shfl(v, 31));
   }
-  return n;
+  __syncthreads();
+  if (lane == 0) {
+    sm.wh[warp] = tot.h;
+    sm.wl[warp] = tot.l;
+  }
+  __syncthreads();
+  DF carry = {0.0f, 0.0f};
+  for (int w = 0; w < warp; ++w) carry = df_add(carry, DF{sm.wh[w], sm.wl[w]});
+  int first = n;
+  const DF end0 = df_shfl(inc[0], 31);  // the prefix through the first 32 ranks
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = r0 + 32 * h + lane;
+    // the sum before rank r: the carry plus the inclusive prefix of rank r - 1
+    DF prev = df_shfl_up(inc[h], 1);
+    if (lane == 0) prev = h == 0 ? DF{0.0f, 0.0f} : end0;
+    const DF before = df_add(carry, prev);
+    if (r < n && r > 0 && !df_lt(before, pz) && r < first) first = r;
+  }
+  first = __reduce_min_sync(FULL_MASK, first);
+  __syncthreads();
+  if (lane == 0) sm.wi[warp] = first;
+  __syncthreads();
+  int m = sm.wi[0];
+  for (int w = 1; w < SB / 32; ++w) m = sm.wi[w] < m ? sm.wi[w] : m;
+  __syncthreads();
+  return m;
 }
 
-// Gumbel-max over the kept ranks [0, kept) of sm.sortbuf, whose fp32 noise
-// is in sm.g32: the fp32 screen, then fp64 scores for the contenders within
-// the margin (see the arithmetic note above).  Returns the composite of the
+// Gumbel-max over the kept ranks [0, kept) of the sorted candidates s,
+// whose fp32 noise is in sm's g32 for ranks below SB (computed here for the
+// others): the fp32 screen, then fp64 scores for the contenders within the
+// margin (see the arithmetic note above).  Returns the composite of the
 // winner.
-__device__ uint64_t gumbel_argmax_sorted(const RowParams &P, int kept, SampSmem &sm) {
+__device__ uint64_t gumbel_argmax_sorted(const uint64_t *srt, const RowParams &P, int kept,
+                                         SampSmem &sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (kept == 1) return sm.sortbuf[0];
+  DecideScratch &d = sm.u.fi.a.d;
+  if (kept == 1) return srt[0];
   float bs = -INFINITY;
   uint64_t bc = 0ull;
   for (int r = tid; r < kept; r += SB) {
-    const uint64_t cc = sm.sortbuf[r];
-    const float s = __fadd_rn(__fdiv_rn(key_value((uint32_t)(cc >> 32)), P.temperature), sm.g32[r]);
-    sm.s32[r] = s;
+    const uint64_t cc = srt[r];
+    const float g = r < SB ? d.g32[r] : gumbel32(P, comp_token(cc));
+    const float s = __fadd_rn(__fdiv_rn(key_value((uint32_t)(cc >> 32)), P.temperature), g);
+    d.s32[r] = s;
     if (bc == 0ull || s > bs || (s == bs && comp_token(cc) < comp_token(bc))) {
       bs = s;
       bc = cc;
@@ -1211,7 +1594,7 @@ __device__ uint64_t gumbel_argmax_sorted(const RowParams &P, int kept, SampSmem 
   const float margin = 1e-4f + 2e-6f * fabsf(best);
   const float floor_s = best - margin;
   int close = 0;
-  for (int r = tid; r < kept; r += SB) close += sm.s32[r] >= floor_s ? 1 : 0;
+  for (int r = tid; r < kept; r += SB) close += d.s32[r] >= floor_s ? 1 : 0;
   close = __reduce_add_sync(FULL_MASK, close);
   if (tid == 0) sm.cnt = 0;
   __syncthreads();
@@ -1226,8 +1609,8 @@ __device__ uint64_t gumbel_argmax_sorted(const RowParams &P, int kept, SampSmem 
   double ds = 0.0;
   int did = -1;
   for (int r = tid; r < kept; r += SB) {
-    if (all || sm.s32[r] >= floor_s) {
-      const uint64_t cc = sm.sortbuf[r];
+    if (all || d.s32[r] >= floor_s) {
+      const uint64_t cc = srt[r];
       const int tok = comp_token(cc);
       const double s = comp_x(cc, P.temperature) + gumbel(P, tok);
       if (better(s, tok, ds, did)) {
@@ -1239,7 +1622,7 @@ __device__ uint64_t gumbel_argmax_sorted(const RowParams &P, int kept, SampSmem 
   const int id = block_argmax(ds, did, sm);
   // its composite: the kept rank holding that token
   for (int r = tid; r < kept; r += SB)
-    if (comp_token(sm.sortbuf[r]) == id) sm.red_u64[0] = sm.sortbuf[r];
+    if (comp_token(srt[r]) == id) sm.red_u64[0] = srt[r];
   __syncthreads();
   const uint64_t c = sm.red_u64[0];
   __syncthreads();
@@ -1249,16 +1632,19 @@ __device__ uint64_t gumbel_argmax_sorted(const RowParams &P, int kept, SampSmem 
 // With log-probs requested (and not greedy), leaves the kept mass relative
 // to the row maximum, that maximum's x and the sampled token's x in
 // sm.s_kept, sm.m_row and sm.xbest.
-__device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
-                          const ChunkRec *recs, SampSmem &sm) {
+__device__ __noinline__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
+                                       const ChunkRec *recs, SampSmem &sm) {
   const int tid = threadIdx.x;
-  if (P.mode == MODE_GREEDY) {
-    uint64_t best = 0;
-    for (int c = 0; c < nch; ++c) best = recs[c].top1 > best ? recs[c].top1 : best;
-    return comp_token(best);
-  }
+  const int nc = P.nc;
+  int R = 1;
+  while (R < nc) R <<= 1;
+  bool all_sorted;
+  const bool cand_mode = P.mode == MODE_TOPK_SMALL || P.mode == MODE_TOPP_FULL;
+  const int nreal = stage_records(recs, nch, nc, cand_mode ? R : 0, sm, &all_sorted);
   uint64_t top1 = 0;
-  for (int c = 0; c < nch; ++c) top1 = recs[c].top1 > top1 ? recs[c].top1 : top1;
+  for (int c = 0; c < nch; ++c) top1 = sm.htop[c] > top1 ? sm.htop[c] : top1;
+  if (P.mode == MODE_GREEDY) return comp_token(top1);
+  const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
   if (P.mode == MODE_ALL) {
     double bs = 0.0;
     int bid = -1;
@@ -1271,8 +1657,7 @@ __device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
       }
     if (P.lp_proc) {
       // the kept mass is the whole row's: the chunks' normalisers
-      const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
-      const DF z = row_normaliser(recs, nch, ctx, sm);
+      const DF z = row_normaliser(nch, ctx, sm);
       if (tid == 0) {
         sm.s_kept = (double)z.h + (double)z.l;
         sm.m_row = comp_x(top1, P.temperature);
@@ -1285,135 +1670,77 @@ __device__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
   if (P.mode == MODE_GENERAL) return general_sample(rv, V, P, top1, -1.0, sm);
 
   // candidate modes: the sorted prefix of the union of the chunks'
-  // candidates, extended only as far as the decision reads
-  const int nc = P.nc;
-  const int nu = nch * nc;
+  // candidates that the decision reads
+  const int nu = nch * R;
   const bool full = P.mode == MODE_TOPP_FULL;
   const bool topp = P.top_p < 1.0f;
   const bool minp = P.min_p > 0.0f;
-  if (tid == 0) sm.cnt = 0;
-  __syncthreads();
-  if (tid < nch) atomicAdd(&sm.cnt, (uint32_t)recs[tid].ncand);
-  __syncthreads();
-  const int nreal = (int)sm.cnt;
+  DecideScratch &d = sm.u.fi.a.d;
   // ranks the decision may read: the top-k, or for top-p over the whole
   // vocabulary up to NCAND candidates (past them: the general path)
   const int nv = min(full ? NCAND : P.K, nreal);
-  __syncthreads();
-  const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
   // top-p over the whole vocabulary without min_p: Z is the whole row's
-  DF Z = {0.0f, 0.0f};
   const bool z_row = full && !minp;
-  if (z_row) Z = row_normaliser(recs, nch, ctx, sm);
-
-  int M = full ? min(64, nv) : nv;
-  int have = 0;  // ranks whose e and noise are in shared memory
-  int kept = 0, kp = nv;
-  bool general = false;
-  for (;;) {
-    // the sorted prefix [0, M)
-    const bool fast = nu <= UNION_MAX && M <= SB && union_top_n(recs, nc, nu, M, sm);
-    if (!fast) {
-      union_sorted_slow(recs, nc, nu, nv, sm);
-      M = nv;
+  DF Z = {0.0f, 0.0f};
+  if (z_row) Z = row_normaliser(nch, ctx, sm);
+  const uint64_t *srt = sm.sortbuf;
+  if (nu <= UNION_MAX) {
+    // a small top-k from a selection bound; otherwise the whole union sorted
+    // by merging the chunks' sorted lists
+    if (full || nv > 64 || !all_sorted || !union_select(nch, R, nv, sm)) {
+      int n2 = R;
+      while (n2 < nu) n2 <<= 1;
+      for (int i = nu + tid; i < n2; i += SB) sm.u.fi.uni[i] = 0ull;
+      __syncthreads();
+      block_merge_runs_desc(sm.u.fi.uni, n2, all_sorted ? R : 1);
+      srt = sm.u.fi.uni;
     }
-    // e_r = 2^(t_r - t_0) and the fp32 noise of the new ranks
-    for (int r = have + tid; r < M; r += SB) {
-      const uint64_t cc = sm.sortbuf[r];
-      const DF e = df_exp2_rel(key_value((uint32_t)(cc >> 32)), ctx, sm.e2h, sm.e2l);
-      sm.eh[r] = e.h;
-      sm.el[r] = e.l;
-      sm.g32[r] = gumbel32(P, comp_token(cc));
-    }
-    have = M;
-    __syncthreads();
-    // decision over [0, M) by warp 0: 0 = decided, 1 = extend, 2 = general
-    if (tid < 32) {
-      int state = 0, k_p = M, k_t = M;
-      if (minp) {
-        const int b = minp_boundary_warp(sm, 0, M, P.min_p);
-        if (b >= 0) {
-          k_p = b;
-        } else if (M < nv) {
-          state = 1;
-        } else {
-          k_p = nv;
-          if (full && nv < V) state = 2;  // the boundary lies beyond the candidates
-        }
-      } else if (!full) {
-        k_p = nv;  // the top-k
-      }
-      if (state == 0 && topp) {
-        DF z = Z;
-        if (!z_row) {
-          // the normaliser over the ranks that pass top-k and min_p (one warp,
-          // a fixed order: lanes in rank order, then a xor tree)
-          DF part = {0.0f, 0.0f};
-          for (int r = tid; r < k_p; r += 32) part = df_add(part, DF{sm.eh[r], sm.el[r]});
-#pragma unroll
-          for (int off = 16; off; off >>= 1) part = df_add(part, df_shfl_xor(part, off));
-          z = part;
-        }
-        k_t = topp_cut_warp(sm, k_p, df_mul_f(z, P.top_p));
-        if (k_t == k_p && !minp && full) {
-          // no cut within the candidates read so far
-          if (M < nv) state = 1;
-          else if (nv < V) state = 2;
-        }
-        if (tid == 0) {
-          sm.zh = z.h;
-          sm.zl = z.l;
-        }
-      } else {
-        k_t = k_p;
-      }
-      if (tid == 0) {
-        sm.flag = state;
-        sm.kp = k_p;
-        sm.kept = k_t;
-      }
-    }
-    __syncthreads();
-    const int state = sm.flag;
-    kp = sm.kp;
-    kept = sm.kept;
-    Z = DF{sm.zh, sm.zl};
-    __syncthreads();
-    if (state == 2) {
-      general = true;
-      break;
-    }
-    if (state == 0) break;
-    M = min(2 * M, nv);
+  } else {
+    union_sorted_slow(recs, nc, nch * nc, nv, sm);
   }
-  // The extracted prefix is the exact global order over the prefix the
+  // e_r = 2^(t_r - t_0) of the ranks the decision may read, and the fp32
+  // noise of the first SB of them
+  for (int r = tid; r < nv; r += SB) {
+    const uint64_t cc = srt[r];
+    const DF e = df_exp2_rel(key_value((uint32_t)(cc >> 32)), ctx, sm.e2h, sm.e2l);
+    d.eh[r] = e.h;
+    d.el[r] = e.l;
+    if (r < SB) d.g32[r] = gumbel32(P, comp_token(cc));
+  }
+  __syncthreads();
+  // min_p, then top-p over the ranks that pass top-k and min_p
+  const int kp = minp ? minp_boundary(nv, P.min_p, sm) : nv;
+  bool general = minp && full && kp == nv && nv < V;  // the boundary lies past the candidates
+  int kept = kp;
+  if (!general && topp) {
+    const DF z = z_row ? Z : mass_of_prefix(kp, sm);
+    if (!z_row) Z = z;
+    kept = topp_cut_block(kp, df_mul_f(z, P.top_p), sm);
+    // top-p over the whole vocabulary still open after the candidates
+    if (kept == kp && !minp && full && nv < V) general = true;
+  }
+  // The sorted prefix is the exact global order over the ranks the
   // decision read (the kept set; the ranks through the min_p boundary; for
   // top-k the K survivors) unless a chunk that holds more tokens than it
   // gave has its bound strictly inside that prefix.  The top-k also needs K
   // candidates in the union.
   if (!general) {
     const int decided = !full ? nv : (minp ? min(kp + 1, nv) : kept);
-    const uint64_t last = sm.sortbuf[decided - 1];
-    __syncthreads();
-    if (tid == 0) sm.flag = (!full && P.K > nreal) ? 1 : 0;
-    __syncthreads();
-    if (tid < nch && recs[tid].thr > last) sm.flag = 1;
-    __syncthreads();
-    general = sm.flag != 0;
-    __syncthreads();
+    const uint64_t last = srt[decided - 1];
+    if (!full && P.K > nreal) general = true;
+    for (int c = 0; c < nch; ++c)
+      if (sm.hthr[c] > last) general = true;
   }
   if (general) {
     const double zk = z_row ? (double)Z.h + (double)Z.l : -1.0;
     return general_sample(rv, V, P, top1, zk, sm);
   }
-  const uint64_t win = gumbel_argmax_sorted(P, kept, sm);
+  const uint64_t win = gumbel_argmax_sorted(srt, P, kept, sm);
   if (P.lp_proc) {
-    DF part = {0.0f, 0.0f};
-    for (int r = tid; r < kept; r += SB) part = df_add(part, DF{sm.eh[r], sm.el[r]});
-    const DF sk = block_sum_df(part, sm);
+    const DF sk = mass_of_prefix(kept, sm);
     if (tid == 0) {
       sm.s_kept = (double)sk.h + (double)sk.l;
-      sm.m_row = comp_x(sm.sortbuf[0], P.temperature);
+      sm.m_row = comp_x(srt[0], P.temperature);
       sm.xbest = comp_x(win, P.temperature);
     }
     __syncthreads();
@@ -1543,16 +1870,12 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   // launched behind its predecessor on the stream (programmatic dependent
   // launch): nothing is read before that grid has completed
   pdl_wait();
-  // the logits first (every row of the batch is readable), so that their
-  // loads overlap the row's flags and settings
-  float raw[EPT];
-  load_chunk(a.logits + (int64_t)b * a.row_stride, a.vocab, c, raw);
   if (!a.active[b]) return;
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) return;
   load_exp2_table(sm);  // read after the first barrier of the chunk pass
   const RowParams P = sample_row_params(a, slot);
-  chunk_pass(raw, a.logits + (int64_t)b * a.row_stride, a.vocab, c, P,
+  chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, c, P,
              a.recs + (int64_t)b * a.nch + c, row_pbits(a, b), sm, a.err);
   // the finish kernel may be scheduled once every chunk CTA is here (late,
   // so that its waiting CTAs do not take SM room from the chunk pass)
@@ -1570,21 +1893,24 @@ __global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
   __shared__ SampSmem sm;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
-  pdl_wait();  // the chunk records (and everything before them)
-  if (!a.active[b]) {
-    if (tid == 0) sample_skip_row(a, b);
-    return;
-  }
+  // This grid starts once every chunk CTA has passed its own wait for its
+  // predecessors, so everything but the chunk records (the flags, the slot
+  // settings and step counters, the history ring) is final already: read it
+  // before waiting for the chunk records.
+  const int active = a.active[b];
   const int slot = a.slots[b];
-  if (slot < 0 || slot >= a.num_slots) {
+  const bool ok = active && slot >= 0 && slot < a.num_slots;
+  RowParams P;
+  if (ok) P = sample_row_params(a, slot);
+  load_exp2_table(sm);  // read after finish_row's first barrier
+  pdl_wait();  // the chunk records
+  if (!ok) {
     if (tid == 0) {
       sample_skip_row(a, b);
-      report(a.err, PKV_DEV_ERR_SLOT);
+      if (active) report(a.err, PKV_DEV_ERR_SLOT);
     }
     return;
   }
-  load_exp2_table(sm);  // read after finish_row's first barrier
-  const RowParams P = sample_row_params(a, slot);
   const float *row = a.logits + (int64_t)b * a.row_stride;
   const ChunkRec *recs = a.recs + (int64_t)b * a.nch;
   const RowView rv = {row, P.n_pen > 0 ? row_pbits(a, b) : nullptr, P.pen};
@@ -1596,13 +1922,14 @@ __global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
     float rm = recs[0].rmax;
     for (int c = 1; c < a.nch; ++c) rm = fmaxf(rm, recs[c].rmax);
     __syncthreads();
+    double *part = sm.u.fi.a.es;  // free once the decision is taken
     if (tid < a.nch)
-      sm.red_d[tid] = ((double)recs[tid].rzh + (double)recs[tid].rzl) *
-                      exp((double)recs[tid].rmax - (double)rm);
+      part[tid] = ((double)recs[tid].rzh + (double)recs[tid].rzl) *
+                  exp((double)recs[tid].rmax - (double)rm);
     __syncthreads();
     if (tid == 0) {
       double z = 0.0;
-      for (int c = 0; c < a.nch; ++c) z += sm.red_d[c];
+      for (int c = 0; c < a.nch; ++c) z += part[c];
       lse_raw = (double)rm + log(z);
     }
   }
@@ -1684,9 +2011,7 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     const RowParams P = row_params(a.ctrl_vocab, a.seeds[slot], step, a.temperature[slot],
                                    a.top_k[slot], a.top_p[slot], 0u);
     for (int c = 0; c < a.ctrl_nch; ++c) {
-      float raw[EPT];
-      load_chunk(crow, a.ctrl_vocab, c, raw);
-      chunk_pass(raw, crow, a.ctrl_vocab, c, P, recs + c, nullptr, sm, a.err);
+      chunk_pass(crow, a.ctrl_vocab, c, P, recs + c, nullptr, sm, a.err);
       __syncthreads();
     }
     const int tok = finish_row(RowView{crow, nullptr, 1.0f}, a.ctrl_vocab, a.ctrl_nch, P, recs, sm);
@@ -1711,18 +2036,26 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
   int prev = 0;
   for (int j = 0; j < a.n_cb; ++j) {
     const float *row = a.base + ((int64_t)j * a.batch + b) * V;
+    bool prestaged = false;
     if (j > 0 && a.fb != nullptr) {
+      // base[j] + fb[j][code_{j-1}], rounded once to fp32: into the chunk
+      // buffer directly when the row is one chunk, and to the row buffer in
+      // global memory (which the general path and longer rows read)
       const float *f = a.fb + ((int64_t)j * V + prev) * V;
-      for (int i = tid; i < V; i += SB) rowbuf[i] = __fadd_rn(row[i], f[i]);
+      prestaged = V <= CHUNK;
+      for (int i = tid; i < V; i += SB) {
+        const float v = __fadd_rn(row[i], f[i]);
+        rowbuf[i] = v;
+        if (prestaged) sm.u.ch.keys[i] = __float_as_uint(v);
+      }
+      __threadfence_block();
       __syncthreads();
       row = rowbuf;
     }
     const RowParams P = row_params(V, a.seeds[slot], step, a.temperature[slot], a.top_k[slot],
                                    a.top_p[slot], (uint32_t)(1 + j));
     for (int c = 0; c < a.nch; ++c) {
-      float raw[EPT];
-      load_chunk(row, V, c, raw);
-      chunk_pass(raw, row, V, c, P, recs + c, nullptr, sm, a.err);
+      chunk_pass(row, V, c, P, recs + c, nullptr, sm, a.err, prestaged);
       __syncthreads();
     }
     const int tok = finish_row(RowView{row, nullptr, 1.0f}, V, a.nch, P, recs, sm);
@@ -1742,7 +2075,9 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
 
 static int chunks_for(int V) { return (V + CHUNK - 1) / CHUNK; }
 
+
 }  // namespace pkv
+
 
 extern "C" size_t pkv_sample_workspace_bytes(int batch, int vocab) {
   using namespace pkv;

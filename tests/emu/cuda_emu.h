@@ -22,6 +22,7 @@
 #define __global__
 #define __host__
 #define __forceinline__ inline
+#define __noinline__ __attribute__((noinline))
 #define __constant__
 #define __shared__ static
 #define __launch_bounds__(...)
@@ -45,6 +46,16 @@ struct EmuBlock {
 inline EmuBlock g_block;
 
 inline void __syncthreads() { g_block.bar->arrive_and_wait(); }
+inline std::atomic<int> g_sync_or{0};
+inline int __syncthreads_or(int pred) {
+  if (pred) g_sync_or.store(1);
+  g_block.bar->arrive_and_wait();
+  const int r = g_sync_or.load();
+  g_block.bar->arrive_and_wait();
+  if (threadIdx.x == 0) g_sync_or.store(0);
+  g_block.bar->arrive_and_wait();
+  return r;
+}
 inline EmuWarp &emu_warp() { return g_block.warps[threadIdx.x / 32]; }
 inline void __syncwarp(unsigned = 0xffffffffu) { emu_warp().bar.arrive_and_wait(); }
 
@@ -87,6 +98,16 @@ inline int __reduce_add_sync(unsigned, int v) {
   w.bar.arrive_and_wait();
   return s;
 }
+inline int __reduce_min_sync(unsigned, int v) {
+  EmuWarp &w = emu_warp();
+  const int lane = threadIdx.x & 31;
+  w.slot[lane] = (uint64_t)(uint32_t)v;
+  w.bar.arrive_and_wait();
+  int m = (int)(uint32_t)w.slot[0];
+  for (int i = 1; i < 32; ++i) m = (int)(uint32_t)w.slot[i] < m ? (int)(uint32_t)w.slot[i] : m;
+  w.bar.arrive_and_wait();
+  return m;
+}
 template <class T> inline T atomicAdd(T *p, T v) { return __atomic_fetch_add(p, v, __ATOMIC_SEQ_CST); }
 template <class T> inline T atomicOr(T *p, T v) { return __atomic_fetch_or(p, v, __ATOMIC_SEQ_CST); }
 
@@ -106,10 +127,26 @@ inline long long clock64() { return 0; }
 template <class T> inline T __ldg(const T *p) { return *p; }
 inline int min(int a, int b) { return a < b ? a : b; }
 inline int max(int a, int b) { return a > b ? a : b; }
+inline unsigned min(unsigned a, unsigned b) { return a < b ? a : b; }
+inline unsigned max(unsigned a, unsigned b) { return a > b ? a : b; }
+struct alignas(16) uint4 { unsigned x, y, z, w; };
+inline uint4 make_uint4(unsigned x, unsigned y, unsigned z, unsigned w) { return {x, y, z, w}; }
 
 
 
 
+
+// Shared memory starts undefined on the device: each block's static shared
+// object is overwritten with a byte pattern first (EMU_SMEM_FILL, default
+// 0xA5), so that a read of what the block did not write shows up.
+inline void emu_poison_shared(void *p, size_t n) {
+  if (threadIdx.x == 0) {
+    const char *e = std::getenv("EMU_SMEM_FILL");
+    const int v = e != nullptr ? (int)std::strtol(e, nullptr, 0) : 0xA5;
+    std::memset(p, v, n);
+  }
+  g_block.bar->arrive_and_wait();
+}
 
 // run kernel(args) over grid with SB threads per block, one block at a time
 template <class K, class A>

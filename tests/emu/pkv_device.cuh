@@ -12,6 +12,22 @@ inline void report(int32_t *err, int bits) {
 // one grid at a time here: the programmatic-launch hooks have nothing to do
 inline void pdl_wait() {}
 inline void pdl_trigger() {}
+// asynchronous copies: plain copies here, with the hardware's alignment rule
+// (both addresses aligned to the copy's size) checked
+inline void emu_cp_async(void *dst, const void *src, size_t n) {
+  if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) % n != 0) {
+    std::fprintf(stderr, "misaligned cp.async of %zu bytes: dst %p src %p\n", n, dst, src);
+    std::abort();
+  }
+  std::memcpy(dst, src, n);
+}
+inline void cp_async4(void *dst, const void *src) { emu_cp_async(dst, src, 4); }
+inline void cp_async8(void *dst, const void *src) { emu_cp_async(dst, src, 8); }
+inline void cp_async16(void *dst, const void *src) { emu_cp_async(dst, src, 16); }
+inline void cp_async_wait_all() {}
+inline void __threadfence_block() { std::atomic_thread_fence(std::memory_order_seq_cst); }
+// the SFU's exp2 (an approximation there; exact enough here)
+inline float fast_exp2(float x) { return std::exp2(x); }
 // the SFU's log2 (an approximation there; exact enough here)
 inline float lg2_approx(float x) { return std::log2(x); }
 }  // namespace pkv

@@ -44,6 +44,9 @@ def test_version_and_error_strings(lib):
     assert pkv.error_string(0) == "ok"
     assert "workspace" in pkv.error_string(4)
     assert lib.pkv_num_dev_error_bits() == 7
+    # a CUDA failure is named by the runtime's own error names (host only)
+    assert lib.pkv_cuda_error_name(700) == b"cudaErrorIllegalAddress"
+    assert lib.pkv_cuda_error_name(716) == b"cudaErrorMisalignedAddress"
 
 
 def test_workspace_sizes_are_host_only(lib):

@@ -31,7 +31,10 @@ def emu_binary(tmp_path_factory):
     d = tmp_path_factory.mktemp("sampler_emu")
     src = open(os.path.join(ROOT, "paged_kv_decode_pages_gb300", "csrc", "sampler.cu")).read()
     end = src.index("}  // namespace pkv") + len("}  // namespace pkv")
-    (d / "sampler_dev.inc").write_text(src[:end] + "\n")
+    # every block's shared scratch starts as garbage, as on the device
+    dev = src[:end].replace("__shared__ SampSmem sm;",
+                            "__shared__ SampSmem sm;\n  emu_poison_shared(&sm, sizeof(sm));")
+    (d / "sampler_dev.inc").write_text(dev + "\n")
     exe = d / "sampler_emu"
     cmd = [gxx, "-std=c++20", "-O1", "-g", "-fsanitize=address,undefined",
            "-fno-sanitize-recover=all", "-ffp-contract=off",
@@ -117,6 +120,11 @@ def test_emulated_sampler_matches_oracle(emu_binary, tmp_path, B, V, std, T, k, 
     elif dist == "thread":
         x[:, np.arange(V) % 256 == 5] += np.float32(6.0)
     x[0, 3 % V] = -np.inf  # a masked token
+    x_ref = x.copy()
+    if B > 1:
+        # a NaN logit: reported, and ranked like -inf (the oracle sees -inf)
+        x[1, (7 * V) // 11] = np.nan
+        x_ref[1, (7 * V) // 11] = -np.inf
     B1 = B + 1  # plus one padding row
     x = np.concatenate([x, np.zeros((1, V), np.float32)])
     slots = np.arange(1, B1 + 1, dtype=np.int32)
@@ -130,9 +138,12 @@ def test_emulated_sampler_matches_oracle(emu_binary, tmp_path, B, V, std, T, k, 
     top_k = np.full(S, k, np.int32)
     top_p = np.full(S, p, np.float32)
     got, kind, err = _run(emu_binary, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p)
-    want, wkind, info, _ = oracle.seeded_sample(x, slots, active, seeds, steps.copy(), temp,
+    x_ref = np.concatenate([x_ref, np.zeros((1, V), np.float32)])
+    want, wkind, info, _ = oracle.seeded_sample(x_ref, slots, active, seeds, steps.copy(), temp,
                                                    top_k, top_p, advance=False)
-    assert err & ~0x10 == 0  # only the logits bit (the -inf token) may be set
+    assert err & ~0x10 == 0  # only the logits bit may be set
+    if B > 1:
+        assert err & 0x10  # the NaN is reported
     near = (info["top2_gap_rel"] < NEAR) | (info["member_margin"] < NEAR)
     mism = got != want
     assert not np.any(mism & ~near), (np.nonzero(mism & ~near), got, want)
