@@ -387,6 +387,7 @@ struct FinishScratch {
     DecideScratch d;             // (after the selection)
     double es[GEN_BLOCK];        // general path
   } a;
+  uint64_t mrg[GEN_BLOCK];       // the other buffer of the pairwise merges
 };
 
 struct __align__(16) SampSmem {
@@ -399,6 +400,8 @@ struct __align__(16) SampSmem {
   double wd[SB / 32];                        // per-warp fp64 partials
   int32_t wi[SB / 32];                       // per-warp ids
   int32_t cn[MAX_CHUNKS], coff[MAX_CHUNKS];  // candidates per chunk and their offsets
+  int32_t csorted[MAX_CHUNKS];               // whether each chunk's list is in order
+  int32_t wcnt[SB / 32];                     // per-warp list lengths
   uint64_t htop[MAX_CHUNKS], hthr[MAX_CHUNKS];  // the chunks' largest composites and bounds
   float fh[MAX_CHUNKS], fl[MAX_CHUNKS];      // the chunks' rescaled normalisers
   float wbs[SB / 32];                        // per-warp best fp32 scores
@@ -425,6 +428,8 @@ struct __align__(16) SampSmem {
   } u;
 };
 static_assert(sizeof(SampSmem) <= 48 * 1024, "static shared memory of one sampler CTA");
+static_assert(sizeof(FinishScratch) <= sizeof(ChunkScratch), "the finish's scratch fits the chunk's");
+static_assert(CHUNK == 1 << 13, "a token's chunk is token >> 13");
 static_assert(offsetof(SampSmem, u) % 16 == 0 && offsetof(SampSmem, sortbuf) % 16 == 0,
               "16-byte copies into the chunk buffer and the union");
 
@@ -627,77 +632,101 @@ __device__ uint32_t select_bound(uint32_t m, int n, SampSmem &sm, uint32_t *top)
   return L;
 }
 
-// Appends composite(k_i, id0 + i) of every i < n with key k_i = key(i) >= L
-// to gbuf (capacity cap; warp-aggregated appends) and returns how many
-// passed (which may exceed cap).
-template <class Key>
-__device__ int gather_above(int n, Key key, uint32_t L, int id0, uint64_t *gbuf, int cap,
-                            SampSmem &sm) {
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) sm.cnt = 0;
-  __syncthreads();
-  for (int base = 0; base < n; base += SB) {  // warp-uniform trip count
-    const int i = base + (int)threadIdx.x;
-    const uint32_t k = i < n ? key(i) : 0u;
-    const bool hit = i < n && k >= L;
-    const unsigned bm = __ballot_sync(FULL_MASK, hit);
-    if (bm) {
-      int pos = 0;
-      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
-      pos = __shfl_sync(FULL_MASK, pos, 0);
-      if (hit) {
-        const int at = pos + __popc(bm & ((1u << lane) - 1u));
-        if (at < cap) gbuf[at] = composite(k, id0 + i);
+
+
+
+// ---------------------------------------------------------------------------
+// selection with independent work per thread
+// ---------------------------------------------------------------------------
+// One or a few sampler CTAs share an SM, so these loops are bound by the
+// latency of dependent instructions rather than by issue: every thread gets
+// several independent loads and sums per step (four keys per lane, eight
+// comparisons per counting step, several lists per binary-search step),
+// and hits are collected with warp ballots (no shared counters, no prefix
+// chains).
+constexpr int WCAP = GEN_BLOCK / (SB / 32);  // 128: longest per-warp list
+
+// Appends, for the calling warp, composite(k, id0 + i) of every key
+// k = keys[i] >= L among the warp's share of keys[0, cnt) (uint4 q = base +
+// lane, base = warp * 32 + m * SB; the tail cnt % 4 goes to warp 0) to lst
+// (positions from four ballots per step); returns the warp's count
+// (warp-uniform; entries past WCAP are dropped, the count is not).
+__device__ __forceinline__ int warp_collect_above(const uint32_t *keys, int cnt, int id0,
+                                                  uint32_t L, uint64_t *lst) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int nq = cnt >> 2;
+  const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
+  int nw = 0;
+#pragma unroll 1
+  for (int base = warp * 32; base < nq; base += SB) {  // the same trip count in every lane
+    const int q = base + lane;
+    const bool v = q < nq;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (v) u = k4[q];
+    const unsigned b0 = __ballot_sync(FULL_MASK, v && u.x >= L);
+    const unsigned b1 = __ballot_sync(FULL_MASK, v && u.y >= L);
+    const unsigned b2 = __ballot_sync(FULL_MASK, v && u.z >= L);
+    const unsigned b3 = __ballot_sync(FULL_MASK, v && u.w >= L);
+    if ((b0 | b1 | b2 | b3) != 0u) {
+      const int n1 = nw + __popc(b0), n2 = n1 + __popc(b1), n3 = n2 + __popc(b2);
+      const int id = id0 + 4 * q;
+      int pos;
+      if ((b0 >> lane) & 1u) {
+        pos = nw + __popc(b0 & lt);
+        if (pos < WCAP) lst[pos] = composite(u.x, id);
       }
+      if ((b1 >> lane) & 1u) {
+        pos = n1 + __popc(b1 & lt);
+        if (pos < WCAP) lst[pos] = composite(u.y, id + 1);
+      }
+      if ((b2 >> lane) & 1u) {
+        pos = n2 + __popc(b2 & lt);
+        if (pos < WCAP) lst[pos] = composite(u.z, id + 2);
+      }
+      if ((b3 >> lane) & 1u) {
+        pos = n3 + __popc(b3 & lt);
+        if (pos < WCAP) lst[pos] = composite(u.w, id + 3);
+      }
+      nw = n3 + __popc(b3);
     }
   }
-  __syncthreads();
-  return (int)sm.cnt;
-}
-
-// The same for composites already formed (the candidate union): every
-// u[i] whose key is >= L.
-__device__ int gather_comp_above(const uint64_t *u, int n, uint32_t L, uint64_t *gbuf, int cap,
-                                 SampSmem &sm) {
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) sm.cnt = 0;
-  __syncthreads();
-  for (int base = 0; base < n; base += SB) {
-    const int i = base + (int)threadIdx.x;
-    const uint64_t c = i < n ? u[i] : 0ull;
-    const bool hit = c != 0ull && (uint32_t)(c >> 32) >= L;
+  if (warp == 0) {
+    const int i = 4 * nq + lane;
+    const bool hit = i < cnt && keys[i] >= L;
     const unsigned bm = __ballot_sync(FULL_MASK, hit);
-    if (bm) {
-      int pos = 0;
-      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
-      pos = __shfl_sync(FULL_MASK, pos, 0);
-      if (hit) {
-        const int at = pos + __popc(bm & ((1u << lane) - 1u));
-        if (at < cap) gbuf[at] = c;
-      }
+    if (hit) {
+      const int pos = nw + __popc(bm & lt);
+      if (pos < WCAP) lst[pos] = composite(keys[i], id0 + i);
     }
+    nw += __popc(bm);
   }
-  __syncthreads();
-  return (int)sm.cnt;
+  return nw;
 }
 
-// The n largest of the C distinct composites in gbuf, in descending order,
-// to out[0, min(n, C)): each one's rank is the number of larger ones.  Also
-// leaves the composite of rank 0 in sm.first and of rank n - 1 in sm.nth
-// (0 when C < n).
-__device__ void rank_out(const uint64_t *gbuf, int C, int n, uint64_t *out, SampSmem &sm) {
-  if (threadIdx.x == 0) sm.nth = 0ull;
-  __syncthreads();
+// The nc largest of the C distinct composites g[0, C) (16-byte aligned), in
+// descending order, to out[0, min(nc, C)): each one's rank is the number of
+// larger ones, counted eight at a time with two running counts.  Leaves
+// rank 0 in sm.first and rank nc - 1 in sm.nth (which the caller clears).
+__device__ __noinline__ void rank_count_out(const uint64_t *g, int C, int nc, uint64_t *out,
+                                            SampSmem &sm) {
+  const ulonglong2 *g2 = reinterpret_cast<const ulonglong2 *>(g);
   for (int e = threadIdx.x; e < C; e += SB) {
-    const uint64_t me = gbuf[e];
-    int r = 0;
-#pragma unroll 4
-    for (int k = 0; k < C; ++k) r += gbuf[k] > me ? 1 : 0;
-    if (r < n) out[r] = me;
-    if (r == 0) sm.first = me;
-    if (r == n - 1) sm.nth = me;
+    const uint64_t x = g[e];
+    int r0 = 0, r1 = 0, k = 0;
+#pragma unroll 1
+    for (; k + 8 <= C; k += 8) {
+      const ulonglong2 a = g2[k >> 1], b = g2[(k >> 1) + 1], c = g2[(k >> 1) + 2],
+                       d = g2[(k >> 1) + 3];
+      r0 += (a.x > x) + (a.y > x) + (b.x > x) + (b.y > x);
+      r1 += (c.x > x) + (c.y > x) + (d.x > x) + (d.y > x);
+    }
+    for (; k < C; ++k) r0 += g[k] > x ? 1 : 0;
+    const int r = r0 + r1;
+    if (r < nc) out[r] = x;
+    if (r == 0) sm.first = x;
+    if (r == nc - 1) sm.nth = x;
   }
-  __syncthreads();
 }
 
 // ---------------------------------------------------------------------------
@@ -716,15 +745,6 @@ __device__ __forceinline__ void stage_chunk(const float *row, int start, int cnt
   __syncthreads();
 }
 
-// Sum over the chunk of 2^(key_value(k) * c2 - t_max), in double-float; all
-// threads get it.  NaN and -inf logits add 0.
-__device__ DF chunk_exp_sum(const uint32_t *keys, int cnt, const Exp2Ctx ctx, SampSmem &sm) {
-  DF acc = {0.0f, 0.0f};
-#pragma unroll 2
-  for (int i = (int)threadIdx.x; i < cnt; i += SB)
-    df_accumulate(acc, df_exp2_rel(key_value(keys[i]), ctx, sm.e2h, sm.e2l));
-  return block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
-}
 
 // The keys of NaN logits (outside [key(-inf), key(+inf)]) set to key(-inf):
 // a NaN ranks like -inf; NaN and +inf are reported.  Returns the thread's
@@ -747,105 +767,120 @@ __device__ __noinline__ uint32_t keys_fix_bad(uint32_t *keys, int cnt, int32_t *
   return m;
 }
 
-// Appends composite(k, id0 + i) of every key k = keys[i] >= L (i < n) to
-// gbuf (capacity cap; warp-aggregated) and returns how many passed (which
-// may exceed cap).  Four keys per thread at a time, then the tail.
-__device__ int gather_keys_above(const uint32_t *keys, int n, uint32_t L, int id0,
-                                 uint64_t *gbuf, int cap, SampSmem &sm) {
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) sm.cnt = 0;
-  __syncthreads();
-  const int nq = n >> 2;
-  const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
-  for (int base = 0; base < nq; base += SB) {  // warp-uniform trip count
-    const int q = base + (int)threadIdx.x;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (q < nq) u = k4[q];
-    const uint32_t h = (u.x >= L ? 1u : 0u) | (u.y >= L ? 2u : 0u) | (u.z >= L ? 4u : 0u) |
-                       (u.w >= L ? 8u : 0u);
-    const uint32_t hm = q < nq ? h : 0u;
-    if (__ballot_sync(FULL_MASK, hm != 0u)) {
-      const int mine = __popc(hm);
-      int incl = mine;
+
+// The chunk's nc largest composites at or above the bound L, in descending
+// order, to out[0, min(nc, C)) with C the number of keys >= L: each warp
+// collects its own keys' hits into its own list in sortbuf, the lists are
+// closed up into one, and every entry is placed by counting the larger
+// ones.  Leaves rank 0 in sm.first and rank nc - 1 in sm.nth.  Returns C,
+// or -1 (nothing written) when a warp holds more than WCAP hits.
+__device__ __noinline__ int chunk_select_sorted(const uint32_t *keys, int cnt, int id0, uint32_t L,
+                                                int nc, uint64_t *out, SampSmem &sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t *lst = sm.sortbuf + warp * WCAP;
+  const int nw = warp_collect_above(keys, cnt, id0, L, lst);
+  if (lane == 0) sm.wcnt[warp] = nw;
+  if (threadIdx.x == 0) sm.nth = 0ull;
+  if (__syncthreads_or(nw > WCAP)) return -1;
+  int off = 0, C = 0;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(FULL_MASK, incl, off);
-        if (lane >= off) incl += o;
-      }
-      int pos = 0;
-      if (lane == 31) pos = (int)atomicAdd(&sm.cnt, (uint32_t)incl);
-      pos = __shfl_sync(FULL_MASK, pos, 31) + incl - mine;
-      const uint32_t kk[4] = {u.x, u.y, u.z, u.w};
+  for (int w = 0; w < SB / 32; ++w) {
+    const int c = sm.wcnt[w];
+    off += w < warp ? c : 0;
+    C += c;
+  }
+  uint64_t v[WCAP / 32];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if ((hm >> e) & 1u) {
-          if (pos < cap) gbuf[pos] = composite(kk[e], id0 + 4 * q + e);
-          ++pos;
-        }
-    }
-  }
-  for (int base = 4 * nq; base < n; base += SB) {
-    const int i = base + (int)threadIdx.x;
-    const uint32_t k = i < n ? keys[i] : 0u;
-    const bool hit = i < n && k >= L;
-    const unsigned bm = __ballot_sync(FULL_MASK, hit);
-    if (bm) {
-      int pos = 0;
-      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
-      pos = __shfl_sync(FULL_MASK, pos, 0);
-      if (hit) {
-        const int at = pos + __popc(bm & ((1u << lane) - 1u));
-        if (at < cap) gbuf[at] = composite(k, id0 + i);
-      }
-    }
-  }
+  for (int e = 0; e < WCAP / 32; ++e) v[e] = e * 32 + lane < nw ? lst[e * 32 + lane] : 0ull;
   __syncthreads();
-  return (int)sm.cnt;
+#pragma unroll
+  for (int e = 0; e < WCAP / 32; ++e)
+    if (e * 32 + lane < nw) sm.sortbuf[off + e * 32 + lane] = v[e];
+  __syncthreads();
+  rank_count_out(sm.sortbuf, C, nc, out, sm);
+  __syncthreads();
+  return C;
 }
 
-// chunk_exp_sum, split by size: a term below 2^-24 of the chunk's largest
-// (t - t_max < -24, t formed in fp32) is taken on the SFU in fp32 -- its
-// error, under 2^-24 * 3e-6 of the largest, is far below the double-float
-// sum's -- and only the larger ones (the chunk's top few percent) get the
-// double-float exponential, from a list of their positions.  The same sum
-// as chunk_exp_sum to ~1e-9 relative; all threads get it.
-__device__ DF chunk_exp_sum_split(const uint32_t *keys, int cnt, const Exp2Ctx ctx,
-                                  SampSmem &sm) {
-  const int lane = threadIdx.x & 31;
-  uint32_t *big = reinterpret_cast<uint32_t *>(sm.sortbuf);  // positions of the larger terms
-  constexpr int BIG_CAP = GEN_BLOCK * 2;
-  if (threadIdx.x == 0) sm.cnt = 0;
-  __syncthreads();
-  float small = 0.0f;
-  for (int base = 0; base < cnt; base += SB) {  // warp-uniform trip count
-    const int i = base + (int)threadIdx.x;
-    bool is_big = false;
-    if (i < cnt) {
-      const float t = fmaf(key_value(keys[i]), ctx.c2h, -ctx.th);
-      if (t < -24.0f)
-        small += fast_exp2(t);  // NaN and -inf logits give 0
-      else
-        is_big = true;
+// Sum over the chunk of 2^(key_value(k) * c2 - t_max), in double-float; all
+// threads get it.  A term below 2^-24 of the chunk's largest (t - t_max <
+// -24, t formed in fp32) is taken on the SFU in fp32 -- its error, under
+// 2^-24 * 3e-6 of the largest, is far below the double-float sum's.  The
+// larger terms' keys are gathered, per warp, over the keys the warp has
+// already read (word j % 128 of its (j / 128)-th block of 32 uint4), and
+// then taken in double-float two at a time.  This destroys the keys.  The
+// same sum as with every term in double-float to ~1e-9 relative.
+__device__ __noinline__ DF chunk_exp_sum_split(uint32_t *keys, int cnt, const Exp2Ctx ctx,
+                                               SampSmem &sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int nq = cnt >> 2;
+  const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
+  uint32_t *own = keys + 4 * warp * 32;  // the warp's first block; block m is at own + 4 * m * SB
+  float s0 = 0.0f, s1 = 0.0f;
+  int nb = 0;  // warp-uniform
+#pragma unroll 1
+  for (int base = warp * 32; base < nq; base += SB) {  // the same trip count in every lane
+    const int q = base + lane;
+    const bool v = q < nq;
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+    if (v) u = k4[q];
+    const float t0 = fmaf(key_value(u.x), ctx.c2h, -ctx.th);
+    const float t1 = fmaf(key_value(u.y), ctx.c2h, -ctx.th);
+    const float t2 = fmaf(key_value(u.z), ctx.c2h, -ctx.th);
+    const float t3 = fmaf(key_value(u.w), ctx.c2h, -ctx.th);
+    // NaN and -inf logits give t = -inf: a zero small term
+    if (v) {
+      s0 += (t0 < -24.0f ? fast_exp2(t0) : 0.0f) + (t1 < -24.0f ? fast_exp2(t1) : 0.0f);
+      s1 += (t2 < -24.0f ? fast_exp2(t2) : 0.0f) + (t3 < -24.0f ? fast_exp2(t3) : 0.0f);
     }
-    const unsigned bm = __ballot_sync(FULL_MASK, is_big);
-    if (bm) {
-      int pos = 0;
-      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
-      pos = __shfl_sync(FULL_MASK, pos, 0);
-      if (is_big) {
-        const int at = pos + __popc(bm & ((1u << lane) - 1u));
-        if (at < BIG_CAP) big[at] = (uint32_t)i;
+    const unsigned b0 = __ballot_sync(FULL_MASK, v && !(t0 < -24.0f));
+    const unsigned b1 = __ballot_sync(FULL_MASK, v && !(t1 < -24.0f));
+    const unsigned b2 = __ballot_sync(FULL_MASK, v && !(t2 < -24.0f));
+    const unsigned b3 = __ballot_sync(FULL_MASK, v && !(t3 < -24.0f));
+    if ((b0 | b1 | b2 | b3) != 0u) {
+      // every lane has read this block (the ballots wait for it), and at
+      // most 128 (k + 1) terms were found in the first k + 1 blocks
+      const int n1 = nb + __popc(b0), n2 = n1 + __popc(b1), n3 = n2 + __popc(b2);
+      int j;
+      if ((b0 >> lane) & 1u) {
+        j = nb + __popc(b0 & lt);
+        own[4 * (j >> 7) * SB + (j & 127)] = u.x;
       }
+      if ((b1 >> lane) & 1u) {
+        j = n1 + __popc(b1 & lt);
+        own[4 * (j >> 7) * SB + (j & 127)] = u.y;
+      }
+      if ((b2 >> lane) & 1u) {
+        j = n2 + __popc(b2 & lt);
+        own[4 * (j >> 7) * SB + (j & 127)] = u.z;
+      }
+      if ((b3 >> lane) & 1u) {
+        j = n3 + __popc(b3 & lt);
+        own[4 * (j >> 7) * SB + (j & 127)] = u.w;
+      }
+      nb = n3 + __popc(b3);
     }
   }
-  __syncthreads();
-  const int nbig = (int)sm.cnt;
-  if (nbig > BIG_CAP) return chunk_exp_sum(keys, cnt, ctx, sm);  // every term in double-float
-  DF acc = {0.0f, 0.0f};
-  for (int j = threadIdx.x; j < nbig; j += SB)
-    df_accumulate(acc, df_exp2_rel(key_value(keys[big[j]]), ctx, sm.e2h, sm.e2l));
-  df_accumulate(acc, DF{small, 0.0f});
-  return block_sum_df(df_fast_two_sum(acc.h, acc.l), sm);
+  DF a0 = {0.0f, 0.0f}, a1 = {0.0f, 0.0f};
+  if (warp == 0) {  // the last cnt % 4 keys, straight in double-float
+    const int i = 4 * nq + lane;
+    if (i < cnt) df_accumulate(a0, df_exp2_rel(key_value(keys[i]), ctx, sm.e2h, sm.e2l));
+  }
+  __syncwarp();
+  int j = lane;
+#pragma unroll 1
+  for (; j + 32 < nb; j += 64) {
+    const uint32_t ka = own[4 * (j >> 7) * SB + (j & 127)];
+    const uint32_t kb = own[4 * ((j + 32) >> 7) * SB + ((j + 32) & 127)];
+    df_accumulate(a0, df_exp2_rel(key_value(ka), ctx, sm.e2h, sm.e2l));
+    df_accumulate(a1, df_exp2_rel(key_value(kb), ctx, sm.e2h, sm.e2l));
+  }
+  if (j < nb) df_accumulate(a0, df_exp2_rel(key_value(own[4 * (j >> 7) * SB + (j & 127)]), ctx,
+                                            sm.e2h, sm.e2l));
+  df_accumulate(a1, DF{s0, 0.0f});
+  df_accumulate(a1, DF{s1, 0.0f});
+  return block_sum_df(df_add(df_fast_two_sum(a0.h, a0.l), df_fast_two_sum(a1.h, a1.l)), sm);
 }
 
 // Keep everything: the chunk's Gumbel argmax in fp64 (the definition);
@@ -1023,9 +1058,8 @@ __device__ __noinline__ void chunk_pass(const float *row, int V, int c, const Ro
     // nc largest of those in order
     uint32_t topkey;
     const uint32_t L = select_bound(m, nc, sm, &topkey);
-    const int C = gather_keys_above(keys, cnt, L, start, sm.sortbuf, GEN_BLOCK, sm);
-    if (C <= GEN_BLOCK) {
-      rank_out(sm.sortbuf, C, nc, rec->cand, sm);
+    const int C = chunk_select_sorted(keys, cnt, start, L, nc, rec->cand, sm);
+    if (C >= 0) {
       const int got = min(C, nc);
       for (int i = got + tid; i < nc; i += SB) rec->cand[i] = 0ull;
       if (tid == 0) {
@@ -1304,7 +1338,7 @@ __device__ int stage_records(const ChunkRec *recs, int nch, int nc, int R, SampS
     sm.hthr[tid] = rc.thr;
     sm.fh[tid] = rc.zh;
     sm.fl[tid] = rc.zl;
-    sm.coff[tid] = rc.sorted;
+    sm.csorted[tid] = rc.sorted;
   }
   if (nch * R <= UNION_MAX) {
     uint64_t *uni = sm.u.fi.uni;
@@ -1322,96 +1356,97 @@ __device__ int stage_records(const ChunkRec *recs, int nch, int nc, int R, SampS
   bool srt = true;
   for (int c = 0; c < nch; ++c) {
     total += sm.cn[c];
-    srt = srt && sm.coff[c] != 0;
+    srt = srt && sm.csorted[c] != 0;
   }
   *all_sorted = srt;
   return total;
 }
 
-// The n largest composites of the staged union (nch lists at stride R,
-// each in descending order, zeros past its count), in descending order,
-// into sm.sortbuf[0, n).  The bound comes from the lists' heads: the n-th
-// largest of the first d = ceil(n / nch) + 4 entries of every list is at
-// most the union's n-th largest, so every composite of the union at or
-// above it (typically a few more than n) is gathered and ranked.  n <= SB;
-// false (nothing written) when more than SB heads or GEN_BLOCK composites
-// would take part.
-__device__ bool union_select(int nch, int R, int n, SampSmem &sm) {
-  const uint64_t *uni = sm.u.fi.uni;
-  uint64_t *g = sm.u.fi.a.gather;
-  const int d = min(R, (n + nch - 1) / nch + 4);
-  const int ns = nch * d;
-  if (ns > SB) return false;
-  // the heads, then the n-th largest of them
-  const int t = threadIdx.x;
-  if (t < ns) g[t] = uni[(t / d) * R + t % d];
-  if (t == 0) {
-    sm.nth = 0ull;
-    sm.cnt = 0;
-  }
-  __syncthreads();
-  if (t < ns && g[t] != 0ull) {
-    const uint64_t me = g[t];
-    int r = 0;
-    for (int k = 0; k < ns; ++k) r += g[k] > me ? 1 : 0;
-    if (r == n - 1) sm.nth = me;
-  }
-  __syncthreads();
-  const uint64_t bound = sm.nth;  // 0 when the heads hold fewer than n: take everything
-  __syncthreads();
-  // every composite of the union at or above the bound
-  const int lane = t & 31;
-  for (int base = 0; base < nch * R; base += SB) {
-    const int i = base + t;
-    const uint64_t c = i < nch * R ? uni[i] : 0ull;
-    const bool hit = c != 0ull && c >= bound;
-    const unsigned bm = __ballot_sync(FULL_MASK, hit);
-    if (bm) {
-      int pos = 0;
-      if (lane == 0) pos = (int)atomicAdd(&sm.cnt, (uint32_t)__popc(bm));
-      pos = __shfl_sync(FULL_MASK, pos, 0);
-      if (hit) {
-        const int at = pos + __popc(bm & ((1u << lane) - 1u));
-        if (at < GEN_BLOCK) g[at] = c;
-      }
-    }
-  }
-  __syncthreads();
-  const int C = (int)sm.cnt;
-  if (C > GEN_BLOCK) return false;
-  rank_out(g, C, n, sm.sortbuf, sm);
-  return true;
+
+
+// Number of entries of the descending list l[0, len) greater than x
+// (binary lifting over any length).
+__device__ __forceinline__ int count_greater_n(const uint64_t *l, int len, uint64_t x) {
+  int c = 0;
+#pragma unroll 1
+  for (int st = len > 0 ? 1 << (31 - __clz(len)) : 0; st > 0; st >>= 1)
+    if (c + st <= len && l[c + st - 1] > x) c += st;
+  return c;
 }
 
-// Sorts v[0, n) descending, n a power of two, given runs of length R (a
-// power of two) that are each already descending: bitonic merges of pairs
-// of runs (the second run taken in reverse, then half-cleaners), run length
-// doubling up to n.  R = 1 sorts from scratch.
-__device__ void block_merge_runs_desc(uint64_t *v, int n, int R) {
-  for (int len = 2 * R; len <= n; len <<= 1) {
-    const int half = len >> 1;
-    for (int p = threadIdx.x; p < n / 2; p += SB) {
-      const int blk = p / half, i = p - blk * half;
-      const int a = blk * len + i, b = blk * len + len - 1 - i;
-      const uint64_t x = v[a], y = v[b];
-      if (x < y) {
-        v[a] = y;
-        v[b] = x;
+// The exact order of the staged union's largest entries into sm.sortbuf.
+// The union: nch descending lists at stride R in sm.u.fi.uni, sm.cn[c]
+// long, list c holding tokens of chunk c.  The first min(cn[c], H + 1)
+// entries of every list are merged pairwise, level after level (at level
+// v the lists are the runs of 2^v chunks), each entry moving to its index
+// in its own run plus its rank in the partner run (a binary search); the
+// two buffers are sortbuf and sm.u.fi.mrg.  The (H + 1)-th entry of a
+// longer list is a sentinel: below the smallest final position m* of a
+// sentinel the merged order is the union's: sortbuf[0, min(m*, entries
+// merged)) is exact, and that count is returned.  nch * (H + 1) <=
+// GEN_BLOCK.
+__device__ __noinline__ int merge_heads(int nch, int R, int H, SampSmem &sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint64_t *uni = sm.u.fi.uni;
+  // the heads' lengths and offsets in list order (warp 0: lists lane and lane + 32)
+  if (tid < 32) {
+    int h0 = lane < nch ? min(sm.cn[lane], H + 1) : 0;
+    int h1 = lane + 32 < nch ? min(sm.cn[lane + 32], H + 1) : 0;
+    int i0 = h0, i1 = h1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o0 = __shfl_up_sync(FULL_MASK, i0, off), o1 = __shfl_up_sync(FULL_MASK, i1, off);
+      if (lane >= off) {
+        i0 += o0;
+        i1 += o1;
       }
+    }
+    const int t0 = __shfl_sync(FULL_MASK, i0, 31);
+    if (lane < nch) sm.coff[lane] = i0 - h0;
+    if (lane + 32 < nch) sm.coff[lane + 32] = t0 + i1 - h1;
+    if (lane == 31) sm.cnt = (uint32_t)(t0 + i1);
+    if (lane == 0) sm.done = 0x7fffffff;
+  }
+  __syncthreads();
+  const int total = (int)sm.cnt;
+  // offset of list c's heads (the total past the last list)
+  auto offat = [&](int c) -> int { return c < nch ? sm.coff[c] : total; };
+  int levels = 0;
+  while ((1 << levels) < nch) ++levels;
+  // start in the buffer that makes the last level write sortbuf
+  uint64_t *X = (levels & 1) ? sm.u.fi.mrg : sm.sortbuf;
+  uint64_t *Y = (levels & 1) ? sm.sortbuf : sm.u.fi.mrg;
+  const int per = H + 1;
+#pragma unroll 1
+  for (int i = tid; i < nch * per; i += SB) {
+    const int c = i / per, k = i - c * per;
+    if (k < min(sm.cn[c], per)) X[sm.coff[c] + k] = uni[c * R + k];
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int v = 0; v < levels; ++v) {
+#pragma unroll 1
+    for (int g = tid; g < total; g += SB) {
+      const uint64_t x = X[g];
+      const int L = (comp_token(x) >> 13) >> v, P = L ^ 1;
+      const int sL = offat(L << v), sP = offat(min(P << v, nch));
+      const int eP = offat(min((P + 1) << v, nch));
+      Y[min(sL, sP) + (g - sL) + count_greater_n(X + sP, eP - sP, x)] = x;
     }
     __syncthreads();
-    for (int j = half >> 1; j > 0; j >>= 1) {
-      for (int p = threadIdx.x; p < n / 2; p += SB) {
-        const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
-        const uint64_t x = v[i], y = v[i + j];
-        if (x < y) {
-          v[i] = y;
-          v[i + j] = x;
-        }
-      }
-      __syncthreads();
-    }
+    uint64_t *t = X;
+    X = Y;
+    Y = t;
   }
+  // the sentinels' final positions
+  if (tid < nch && sm.cn[tid] > per - 1) {
+    const int pos = count_greater_n(sm.sortbuf, total, uni[tid * R + H]);
+    atomicMin(&sm.done, pos);
+  }
+  __syncthreads();
+  const int exact = min(total, (int)sm.done);
+  __syncthreads();
+  return exact;
 }
 
 // The nv largest composites of the union in descending order into
@@ -1683,53 +1718,78 @@ __device__ __noinline__ int finish_row(const RowView &rv, int V, int nch, const 
   const bool z_row = full && !minp;
   DF Z = {0.0f, 0.0f};
   if (z_row) Z = row_normaliser(nch, ctx, sm);
+  // The sorted prefix the decision reads: a top-k's survivors; for top-p
+  // over the whole vocabulary the first 256 ranks, then, if the decision is
+  // still open there, all NCAND.  A single chunk's list is in order already.
+  const bool staged = nu <= UNION_MAX && all_sorted;
+  uint64_t bound = 0ull;  // the chunks hold no token outside the union above it
+  for (int c = 0; c < nch; ++c) bound = sm.hthr[c] > bound ? sm.hthr[c] : bound;
   const uint64_t *srt = sm.sortbuf;
-  if (nu <= UNION_MAX) {
-    // a small top-k from a selection bound; otherwise the whole union sorted
-    // by merging the chunks' sorted lists
-    if (full || nv > 64 || !all_sorted || !union_select(nch, R, nv, sm)) {
-      int n2 = R;
-      while (n2 < nu) n2 <<= 1;
-      for (int i = nu + tid; i < n2; i += SB) sm.u.fi.uni[i] = 0ull;
-      __syncthreads();
-      block_merge_runs_desc(sm.u.fi.uni, n2, all_sorted ? R : 1);
+  int kept = 0, kp = nv;
+  bool general = true;
+  const int hmax = GEN_BLOCK / nch - 1;  // longest heads that fit the merge buffers
+  for (int attempt = 0; attempt < 3; ++attempt) {
+    int avail = nv;
+    if (nch == 1 && staged) {
       srt = sm.u.fi.uni;
+      attempt = 2;  // nothing more to read later
+    } else if (staged && attempt < 2) {
+      // the heads of the lists first, about twice each list's share of the
+      // ranks wanted (for top-p over the whole vocabulary 256 at first),
+      // then as much of them as the merge buffers hold
+      int H = hmax;
+      if (attempt == 0) {
+        const int want = full ? min(256, nv) : nv;
+        H = 8;
+        while (H < hmax && H * nch < 2 * want) H <<= 1;
+        H = min(H, hmax);
+      }
+      avail = min(nv, merge_heads(nch, R, H, sm));
+      srt = sm.sortbuf;
+      if (H >= nc) attempt = 2;  // the whole lists were read
+    } else {
+      union_sorted_slow(recs, nc, nch * nc, nv, sm);
+      srt = sm.sortbuf;
+      attempt = 2;
     }
-  } else {
-    union_sorted_slow(recs, nc, nch * nc, nv, sm);
-  }
-  // e_r = 2^(t_r - t_0) of the ranks the decision may read, and the fp32
-  // noise of the first SB of them
-  for (int r = tid; r < nv; r += SB) {
-    const uint64_t cc = srt[r];
-    const DF e = df_exp2_rel(key_value((uint32_t)(cc >> 32)), ctx, sm.e2h, sm.e2l);
-    d.eh[r] = e.h;
-    d.el[r] = e.l;
-    if (r < SB) d.g32[r] = gumbel32(P, comp_token(cc));
-  }
-  __syncthreads();
-  // min_p, then top-p over the ranks that pass top-k and min_p
-  const int kp = minp ? minp_boundary(nv, P.min_p, sm) : nv;
-  bool general = minp && full && kp == nv && nv < V;  // the boundary lies past the candidates
-  int kept = kp;
-  if (!general && topp) {
-    const DF z = z_row ? Z : mass_of_prefix(kp, sm);
-    if (!z_row) Z = z;
-    kept = topp_cut_block(kp, df_mul_f(z, P.top_p), sm);
-    // top-p over the whole vocabulary still open after the candidates
-    if (kept == kp && !minp && full && nv < V) general = true;
-  }
-  // The sorted prefix is the exact global order over the ranks the
-  // decision read (the kept set; the ranks through the min_p boundary; for
-  // top-k the K survivors) unless a chunk that holds more tokens than it
-  // gave has its bound strictly inside that prefix.  The top-k also needs K
-  // candidates in the union.
-  if (!general) {
-    const int decided = !full ? nv : (minp ? min(kp + 1, nv) : kept);
-    const uint64_t last = srt[decided - 1];
-    if (!full && P.K > nreal) general = true;
-    for (int c = 0; c < nch; ++c)
-      if (sm.hthr[c] > last) general = true;
+    if (!full && avail < nv) continue;  // the top-k survivors are not all in order yet
+    // e_r = 2^(t_r - t_0) of the ranks the decision may read, and the fp32
+    // noise of the first SB of them
+    for (int r = tid; r < avail; r += SB) {
+      const uint64_t cc = srt[r];
+      const DF e = df_exp2_rel(key_value((uint32_t)(cc >> 32)), ctx, sm.e2h, sm.e2l);
+      d.eh[r] = e.h;
+      d.el[r] = e.l;
+      if (r < SB) d.g32[r] = gumbel32(P, comp_token(cc));
+    }
+    __syncthreads();
+    // ranks of the row past the ones read here
+    const bool beyond = full && avail < V;
+    // min_p, then top-p over the ranks that pass top-k and min_p
+    kp = minp ? minp_boundary(avail, P.min_p, sm) : avail;
+    bool open = minp && kp == avail && beyond;  // min_p boundary not reached
+    kept = kp;
+    if (!open && topp) {
+      const DF z = z_row ? Z : mass_of_prefix(kp, sm);
+      if (!z_row) Z = z;
+      kept = topp_cut_block(kp, df_mul_f(z, P.top_p), sm);
+      if (kept == kp && !minp && beyond) open = true;  // top-p not reached
+    }
+    // The sorted prefix is the exact global order over the ranks the
+    // decision read (the kept set; the ranks through the min_p boundary;
+    // for top-k the K survivors) when its last one is at or above the
+    // bound under which the chunks hold tokens not in the union.  The top-k
+    // also needs K candidates in the union.
+    bool exact = !open;
+    if (exact) {
+      const int decided = !full ? nv : (minp ? min(kp + 1, avail) : kept);
+      exact = srt[decided - 1] >= bound && !(!full && P.K > nreal);
+    }
+    if (exact) {
+      general = false;
+      break;
+    }
+    if (avail == nv) break;  // every candidate was read
   }
   if (general) {
     const double zk = z_row ? (double)Z.h + (double)Z.l : -1.0;

@@ -106,6 +106,13 @@ CASES = [
     # ... a short last chunk (808 tokens) and a chunk with idle warps
     (3, 9000, 1.0, 1.0, 100, 1.0, "normal"),
     (3, 200, 1.0, 1.0, 20, 0.9, "normal"),
+    # longer per-warp candidate lists (sorted 64 and 128 to a warp), and a
+    # finish that deals 64 union entries to each warp
+    (3, 6561, 1.0, 1.0, 128, 0.95, "normal"),
+    (3, 6561, 1.0, 1.0, 200, 0.9, "normal"),
+    (3, 20000, 1.0, 1.0, 400, 0.97, "normal"),
+    (3, 8192, 1.0, 1.0, 230, 0.95, "normal"),   # 90-106 to a warp
+    (3, 8192, 1.0, 1.0, 256, 0.95, "normal"),   # over 128 to a warp: radix select
 ]
 
 
