@@ -390,6 +390,13 @@ struct FinishScratch {
   uint64_t mrg[GEN_BLOCK];       // the other buffer of the pairwise merges
 };
 
+// A chunk of at most SREC_MAX_V keys leaves the merge buffer of the shared
+// union free, room for one chunk record.
+constexpr int SREC_MAX_V = (int)(sizeof(FinishScratch) - GEN_BLOCK * sizeof(uint64_t)) / 4;
+static_assert(sizeof(ChunkRec) <= GEN_BLOCK * sizeof(uint64_t), "a chunk record fits the merge buffer");
+static_assert(offsetof(FinishScratch, mrg) == sizeof(FinishScratch) - GEN_BLOCK * sizeof(uint64_t),
+              "the merge buffer ends the finish scratch");
+
 struct __align__(16) SampSmem {
   float e2h[32], e2l[32];  // the 2^(j/32) table
   float wh[SB / 32], wl[SB / 32];
@@ -1329,7 +1336,7 @@ __device__ __noinline__ int general_sample(const RowView &rv, int V, const RowPa
 // total number of candidates; *all_sorted tells whether every chunk's list
 // is in descending order.
 __device__ int stage_records(const ChunkRec *recs, int nch, int nc, int R, SampSmem &sm,
-                             bool *all_sorted) {
+                             bool *all_sorted, bool rec_smem = false) {
   const int tid = threadIdx.x;
   if (tid < nch) {
     const ChunkRec &rc = recs[tid];
@@ -1340,7 +1347,7 @@ __device__ int stage_records(const ChunkRec *recs, int nch, int nc, int R, SampS
     sm.fl[tid] = rc.zl;
     sm.csorted[tid] = rc.sorted;
   }
-  if (nch * R <= UNION_MAX) {
+  if (nch * R <= UNION_MAX && !rec_smem) {
     uint64_t *uni = sm.u.fi.uni;
     for (int i = tid; i < nch * R; i += SB) {
       const int c = i / R, k = i - c * R;  // R is a power of two
@@ -1664,18 +1671,186 @@ __device__ uint64_t gumbel_argmax_sorted(const uint64_t *srt, const RowParams &P
   return c;
 }
 
+// The decision over a top-k of at most 64 sorted ranks srt[0, n), taken
+// by warp 0 alone (ranks lane and lane + 32; shuffles and ballots, no block
+// barrier but the last): the same arithmetic in the same order as the
+// block-wide steps (minp_boundary, mass_of_prefix, topp_cut_block,
+// gumbel_argmax_sorted) take for n <= 64, so the same token.  With
+// log-probs requested, also leaves sm.s_kept, sm.m_row and sm.xbest.
+// Returns the winner's composite (all threads).
+__device__ __noinline__ uint64_t decide_small(const uint64_t *srt, int n, const RowParams &P,
+                                              const Exp2Ctx &ctx, SampSmem &sm) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const DF zero = {0.0f, 0.0f};
+    uint64_t c[2];
+    DF e[2];
+    float g[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = lane + 32 * h;
+      c[h] = r < n ? srt[r] : 0ull;
+      e[h] = zero;
+      g[h] = 0.0f;
+      if (r < n) {
+        e[h] = df_exp2_rel(key_value((uint32_t)(c[h] >> 32)), ctx, sm.e2h, sm.e2l);
+        g[h] = gumbel32(P, comp_token(c[h]));
+      }
+    }
+    // min_p: the first rank >= 1 with e_r < min_p
+    int kp = n;
+    if (P.min_p > 0.0f) {
+      unsigned m[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        const bool cut = r >= 1 && r < n &&
+                         (e[h].h < P.min_p || (e[h].h == P.min_p && e[h].l < 0.0f));
+        m[h] = __ballot_sync(FULL_MASK, cut);
+      }
+      kp = m[0] ? __ffs(m[0]) - 1 : (m[1] ? 32 + __ffs(m[1]) - 1 : n);
+    }
+    // top-p over ranks [0, kp): Z as one xor tree per 32 ranks, then the
+    // two added; the prefix sums as one scan per 32 ranks with the carry
+    int kept = kp;
+    if (P.top_p < 1.0f) {
+      DF t[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        DF v = lane + 32 * h < kp ? df_add(zero, e[h]) : zero;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) v = df_add(v, df_shfl_xor(v, off));
+        t[h] = v;
+      }
+      const DF pz = df_mul_f(df_add(t[0], t[1]), P.top_p);
+      DF inc[2];
+      DF tot = zero;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        DF v = lane + 32 * h < kp ? e[h] : zero;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const DF o = df_shfl_up(v, off);
+          if (lane >= off) v = df_add(v, o);
+        }
+        inc[h] = df_add(tot, v);
+        tot = df_add(tot, df_shfl(v, 31));
+      }
+      const DF end0 = df_shfl(inc[0], 31);
+      int first = kp;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        DF prev = df_shfl_up(inc[h], 1);
+        if (lane == 0) prev = h == 0 ? zero : end0;
+        const DF before = df_add(zero, prev);
+        if (r < kp && r > 0 && !df_lt(before, pz) && r < first) first = r;
+      }
+      kept = __reduce_min_sync(FULL_MASK, first);
+    }
+    // Gumbel-max over ranks [0, kept): the fp32 screen, fp64 for contenders
+    uint64_t win = __shfl_sync(FULL_MASK, c[0], 0);
+    if (kept > 1) {
+      float sc[2];
+      float bs = -INFINITY;
+      uint64_t bc = 0ull;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        sc[h] = -INFINITY;
+        if (r < kept) {
+          sc[h] = __fadd_rn(__fdiv_rn(key_value((uint32_t)(c[h] >> 32)), P.temperature), g[h]);
+          if (bc == 0ull || sc[h] > bs || (sc[h] == bs && comp_token(c[h]) < comp_token(bc))) {
+            bs = sc[h];
+            bc = c[h];
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float os = __shfl_xor_sync(FULL_MASK, bs, off);
+        const uint64_t oc = __shfl_xor_sync(FULL_MASK, bc, off);
+        if (oc != 0ull && (bc == 0ull || os > bs || (os == bs && comp_token(oc) < comp_token(bc)))) {
+          bs = os;
+          bc = oc;
+        }
+      }
+      const float floor_s = bs - (1e-4f + 2e-6f * fabsf(bs));
+      const int close = __popc(__ballot_sync(FULL_MASK, lane < kept && sc[0] >= floor_s)) +
+                        __popc(__ballot_sync(FULL_MASK, lane + 32 < kept && sc[1] >= floor_s));
+      if (isfinite(bs) && close == 1) {
+        win = bc;
+      } else {
+        const bool all = !isfinite(bs);
+        double ds = 0.0;
+        int did = -1;
+        uint64_t dc = 0ull;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = lane + 32 * h;
+          if (r < kept && (all || sc[h] >= floor_s)) {
+            const int tok = comp_token(c[h]);
+            const double v = comp_x(c[h], P.temperature) + gumbel(P, tok);
+            if (better(v, tok, ds, did)) {
+              ds = v;
+              did = tok;
+              dc = c[h];
+            }
+          }
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+          const double os = __shfl_xor_sync(FULL_MASK, ds, off);
+          const int oi = __shfl_xor_sync(FULL_MASK, did, off);
+          const uint64_t oc = __shfl_xor_sync(FULL_MASK, dc, off);
+          if (better(os, oi, ds, did)) {
+            ds = os;
+            did = oi;
+            dc = oc;
+          }
+        }
+        win = dc;
+      }
+    }
+    if (P.lp_proc) {
+      // the kept ranks' mass, summed as mass_of_prefix sums it
+      DF t[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        DF v = lane + 32 * h < kept ? df_add(zero, e[h]) : zero;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) v = df_add(v, df_shfl_xor(v, off));
+        t[h] = v;
+      }
+      const DF sk = df_add(t[0], t[1]);
+      if (lane == 0) {
+        sm.s_kept = (double)sk.h + (double)sk.l;
+        sm.m_row = comp_x(c[0], P.temperature);
+        sm.xbest = comp_x(win, P.temperature);
+      }
+    }
+    if (lane == 0) sm.first = win;
+  }
+  __syncthreads();
+  const uint64_t w = sm.first;
+  __syncthreads();
+  return w;
+}
+
 // With log-probs requested (and not greedy), leaves the kept mass relative
 // to the row maximum, that maximum's x and the sampled token's x in
 // sm.s_kept, sm.m_row and sm.xbest.
+// rec_smem: the single chunk's record is in shared memory (its candidate
+// list is read in place).
 __device__ __noinline__ int finish_row(const RowView &rv, int V, int nch, const RowParams &P,
-                                       const ChunkRec *recs, SampSmem &sm) {
+                                       const ChunkRec *recs, SampSmem &sm, bool rec_smem = false) {
   const int tid = threadIdx.x;
   const int nc = P.nc;
   int R = 1;
   while (R < nc) R <<= 1;
   bool all_sorted;
   const bool cand_mode = P.mode == MODE_TOPK_SMALL || P.mode == MODE_TOPP_FULL;
-  const int nreal = stage_records(recs, nch, nc, cand_mode ? R : 0, sm, &all_sorted);
+  const int nreal = stage_records(recs, nch, nc, cand_mode ? R : 0, sm, &all_sorted, rec_smem);
   uint64_t top1 = 0;
   for (int c = 0; c < nch; ++c) top1 = sm.htop[c] > top1 ? sm.htop[c] : top1;
   if (P.mode == MODE_GREEDY) return comp_token(top1);
@@ -1731,7 +1906,7 @@ __device__ __noinline__ int finish_row(const RowView &rv, int V, int nch, const 
   for (int attempt = 0; attempt < 3; ++attempt) {
     int avail = nv;
     if (nch == 1 && staged) {
-      srt = sm.u.fi.uni;
+      srt = rec_smem ? recs[0].cand : sm.u.fi.uni;
       attempt = 2;  // nothing more to read later
     } else if (staged && attempt < 2) {
       // the heads of the lists first, about twice each list's share of the
@@ -1753,6 +1928,12 @@ __device__ __noinline__ int finish_row(const RowView &rv, int V, int nch, const 
       attempt = 2;
     }
     if (!full && avail < nv) continue;  // the top-k survivors are not all in order yet
+    if (!full && nv <= 64) {
+      // a top-k of at most 64: decided by one warp when the order is exact
+      if (srt[nv - 1] >= bound && !(P.K > nreal))
+        return comp_token(decide_small(srt, nv, P, ctx, sm));
+      break;  // every candidate was read: the general path
+    }
     // e_r = 2^(t_r - t_0) of the ranks the decision may read, and the fp32
     // noise of the first SB of them
     for (int r = tid; r < avail; r += SB) {
@@ -2065,16 +2246,24 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
   load_exp2_table(sm);  // read after the first barrier of the chunk pass
   const int64_t step = a.steps[slot];
   ChunkRec *recs = a.recs + (int64_t)b * (a.nch > a.ctrl_nch ? a.nch : a.ctrl_nch);
+  // A single-chunk row of up to SREC_MAX_V tokens keeps its record in the
+  // part of the shared union that its keys leave free (the merge buffer,
+  // which a single chunk's finish does not use): no round trip through
+  // global memory between the chunk pass and the finish.
+  ChunkRec *srec = reinterpret_cast<ChunkRec *>(sm.u.fi.mrg);
   if (a.ctrl != nullptr) {
     // channel 0: the stop/continue sample (salt 0); a stop ends the frame
     const float *crow = a.ctrl + (int64_t)b * a.ctrl_vocab;
     const RowParams P = row_params(a.ctrl_vocab, a.seeds[slot], step, a.temperature[slot],
                                    a.top_k[slot], a.top_p[slot], 0u);
+    const bool cs = a.ctrl_nch == 1 && a.ctrl_vocab <= SREC_MAX_V;
+    ChunkRec *cr = cs ? srec : recs;
     for (int c = 0; c < a.ctrl_nch; ++c) {
-      chunk_pass(crow, a.ctrl_vocab, c, P, recs + c, nullptr, sm, a.err);
+      chunk_pass(crow, a.ctrl_vocab, c, P, cr + c, nullptr, sm, a.err);
       __syncthreads();
     }
-    const int tok = finish_row(RowView{crow, nullptr, 1.0f}, a.ctrl_vocab, a.ctrl_nch, P, recs, sm);
+    const int tok =
+        finish_row(RowView{crow, nullptr, 1.0f}, a.ctrl_vocab, a.ctrl_nch, P, cr, sm, cs);
     if (tid == 0) {
       out[0] = tok;
       sm.token = tok;
@@ -2114,11 +2303,13 @@ __global__ void __launch_bounds__(SB) frame_kernel(const FrameArgs a) {
     }
     const RowParams P = row_params(V, a.seeds[slot], step, a.temperature[slot], a.top_k[slot],
                                    a.top_p[slot], (uint32_t)(1 + j));
+    const bool rs = a.nch == 1 && V <= SREC_MAX_V;
+    ChunkRec *rr = rs ? srec : recs;
     for (int c = 0; c < a.nch; ++c) {
-      chunk_pass(row, V, c, P, recs + c, nullptr, sm, a.err, prestaged);
+      chunk_pass(row, V, c, P, rr + c, nullptr, sm, a.err, prestaged);
       __syncthreads();
     }
-    const int tok = finish_row(RowView{row, nullptr, 1.0f}, V, a.nch, P, recs, sm);
+    const int tok = finish_row(RowView{row, nullptr, 1.0f}, V, a.nch, P, rr, sm, rs);
     if (tid == 0) {
       codes[j] = tok;
       sm.token = tok;

@@ -132,6 +132,8 @@ inline int __popc(unsigned x) { return __builtin_popcount(x); }
 inline int __clz(int x) { return x == 0 ? 32 : __builtin_clz((unsigned)x); }
 inline long long clock64() { return 0; }
 template <class T> inline T __ldg(const T *p) { return *p; }
+template <class T> inline T __ldcg(const T *p) { return __atomic_load_n(p, __ATOMIC_SEQ_CST); }
+inline void __threadfence() { std::atomic_thread_fence(std::memory_order_seq_cst); }
 inline int min(int a, int b) { return a < b ? a : b; }
 inline int max(int a, int b) { return a > b ? a : b; }
 inline unsigned min(unsigned a, unsigned b) { return a < b ? a : b; }
