@@ -138,9 +138,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) attn_plan_kernel(const AttnArgs 
   __shared__ int32_t scan[PLAN_THREADS];
   __shared__ int32_t carry;
   __shared__ int32_t bin[SPL];  // short last splits per size, then the next slot of each size
-  // the persistent kernel may launch and set up now; it waits for this grid
-  // to complete before it reads the table
-  pdl_trigger();
+  // No early launch of dependents: a kernel after this one starts only once
+  // the plan is complete, so it may read the plan before its own wait.
   const int tid = threadIdx.x;
   const int HB = a.num_kv_heads * a.qblocks;
   if (tid == 0) carry = 0;
@@ -340,16 +339,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
     }
     fence_barrier_init();
   }
-  pdl_wait();     // the planner's table and counter
-  pdl_trigger();  // the merge kernel may queue behind this grid now
-  // every CTA starts on unit blockIdx.x; later units come from the counter
-  // (offset by the grid), so a batch with fewer units than CTAs gives each
-  // CTA at most one instead of two to the first half of the grid
-  if (tid == 0) {
-    s_unit[0] = (int)blockIdx.x;
-    s_unit[1] = (int)gridDim.x + atomicAdd(&a.plan->counter, 1);
-  }
-  // the split table of the batch, in shared memory when it fits
+  // The plan, the lengths and flags and the page table were final before
+  // this grid's predecessor started: the planner lets no kernel start before
+  // it completes, and the library's other kernels wait for their own
+  // predecessor before they let a dependent start.  So the split table is
+  // read, the first unit (unit blockIdx.x) decoded and its page ids loaded
+  // while the predecessor (the KV append) may still run; q, the cache and
+  // the unit counter are read only after the wait.
   const bool small_batch = a.batch <= ATTN_SMEM_ROWS;
   __shared__ int32_t s_full;  // full splits (read once per unit, not held in registers)
   const int total_units = a.plan->total_units;
@@ -364,13 +360,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
   const int32_t *seq = small_batch ? s_seq : a.seq_lens;
   const uint64_t policy = l2_evict_first_policy();
   const int layer_page0 = a.layer * a.num_pages;
-
-  int ordinal = 0;
-  Unit cur = decode_unit(a, s_unit[0], GP, total_units, s_full, rs, seq);
-  Unit nxt = decode_unit(a, s_unit[1], GP, total_units, s_full, rs, seq);
-  int cur_cnt = warp_pages(cur, warp);
-  int nxt_cnt = warp_pages(nxt, warp);
-  int next_id = 0;  // id of the unit after next, fetched a unit ahead (thread 0)
 
   // the warp's blocks of a unit: lane i holds the i-th as page * bpp + the
   // block's index inside its page
@@ -390,7 +379,24 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2)
     }
     return pid;
   };
+  int ordinal = 0;
+  // every CTA starts on unit blockIdx.x; later units come from the counter
+  // (offset by the grid), so a batch with fewer units than CTAs gives each
+  // CTA at most one instead of two to the first half of the grid
+  Unit cur = decode_unit(a, (int)blockIdx.x, GP, total_units, s_full, rs, seq);
+  int cur_cnt = warp_pages(cur, warp);
   int pid_cur = load_pids(cur, cur_cnt);
+
+  pdl_wait();     // the predecessor: the cache (the append), q, the unit counter
+  pdl_trigger();  // the merge kernel may queue behind this grid now
+  if (tid == 0) {
+    s_unit[0] = (int)blockIdx.x;
+    s_unit[1] = (int)gridDim.x + atomicAdd(&a.plan->counter, 1);
+  }
+  __syncthreads();
+  Unit nxt = decode_unit(a, s_unit[1], GP, total_units, s_full, rs, seq);
+  int nxt_cnt = warp_pages(nxt, warp);
+  int next_id = 0;  // id of the unit after next, fetched a unit ahead (thread 0)
   int pid_nxt = load_pids(nxt, nxt_cnt);
 
   // q rows of a unit's heads (contiguous in HBM) into q buffer `buf`
