@@ -75,7 +75,7 @@ namespace pkv {
 constexpr int SB = 256;                 // threads per sampler CTA
 constexpr int CHUNK = 8192;             // tokens per chunk
 constexpr int NCAND = 512;              // most candidates kept per chunk
-constexpr int NC_MIN = 64;              // least candidates kept per chunk
+constexpr int NC_MIN = 16;              // least candidates kept per chunk
 constexpr int MAX_CHUNKS = 64;          // vocab <= 64 * 8192
 constexpr int GEN_BLOCK = 1024;         // sorted block (finish and general path)
 
