@@ -1671,100 +1671,82 @@ __device__ uint64_t gumbel_argmax_sorted(const uint64_t *srt, const RowParams &P
   return c;
 }
 
-// The decision over a top-k of at most 64 sorted ranks srt[0, n), taken
-// by warp 0 alone (ranks lane and lane + 32; shuffles and ballots, no block
-// barrier but the last): the same arithmetic in the same order as the
-// block-wide steps (minp_boundary, mass_of_prefix, topp_cut_block,
-// gumbel_argmax_sorted) take for n <= 64, so the same token.  With
-// log-probs requested, also leaves sm.s_kept, sm.m_row and sm.xbest.
+// The decision over a top-k of at most 64 sorted ranks srt[0, n): every
+// thread of the block takes one rank's exponential e_r and fp32 noise first
+// (into DecideScratch), then warp 0 alone decides with shuffles and ballots
+// (no further block barrier but the last), lane l holding ranks 2l and
+// 2l + 1: min_p (the first rank >= 1 with e_r < min_p), top-p (one
+// double-float scan over the lanes' pair sums; Z is its total), the Gumbel
+// argmax (the fp32 screen, fp64 for the contenders within its margin).
+// A row takes this path or the block-wide one by its own settings alone.
+// With log-probs requested, also leaves sm.s_kept, sm.m_row and sm.xbest.
 // Returns the winner's composite (all threads).
 __device__ __noinline__ uint64_t decide_small(const uint64_t *srt, int n, const RowParams &P,
                                               const Exp2Ctx &ctx, SampSmem &sm) {
+  DecideScratch &d = sm.u.fi.a.d;
+  for (int r = threadIdx.x; r < n; r += SB) {
+    const uint64_t cc = srt[r];
+    const DF e = df_exp2_rel(key_value((uint32_t)(cc >> 32)), ctx, sm.e2h, sm.e2l);
+    d.eh[r] = e.h;
+    d.el[r] = e.l;
+    d.g32[r] = gumbel32(P, comp_token(cc));
+  }
+  __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const DF zero = {0.0f, 0.0f};
-    uint64_t c[2];
-    DF e[2];
-    float g[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = lane + 32 * h;
-      c[h] = r < n ? srt[r] : 0ull;
-      e[h] = zero;
-      g[h] = 0.0f;
-      if (r < n) {
-        e[h] = df_exp2_rel(key_value((uint32_t)(c[h] >> 32)), ctx, sm.e2h, sm.e2l);
-        g[h] = gumbel32(P, comp_token(c[h]));
-      }
-    }
+    const int r0 = 2 * lane, r1 = 2 * lane + 1;
+    const bool v0 = r0 < n, v1 = r1 < n;
+    const uint64_t c0 = v0 ? srt[r0] : 0ull, c1 = v1 ? srt[r1] : 0ull;
+    const DF e0 = v0 ? DF{d.eh[r0], d.el[r0]} : zero;
+    const DF e1 = v1 ? DF{d.eh[r1], d.el[r1]} : zero;
     // min_p: the first rank >= 1 with e_r < min_p
     int kp = n;
     if (P.min_p > 0.0f) {
-      unsigned m[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = lane + 32 * h;
-        const bool cut = r >= 1 && r < n &&
-                         (e[h].h < P.min_p || (e[h].h == P.min_p && e[h].l < 0.0f));
-        m[h] = __ballot_sync(FULL_MASK, cut);
-      }
-      kp = m[0] ? __ffs(m[0]) - 1 : (m[1] ? 32 + __ffs(m[1]) - 1 : n);
+      const bool cut0 = r0 >= 1 && v0 && (e0.h < P.min_p || (e0.h == P.min_p && e0.l < 0.0f));
+      const bool cut1 = v1 && (e1.h < P.min_p || (e1.h == P.min_p && e1.l < 0.0f));
+      kp = __reduce_min_sync(FULL_MASK, cut0 ? r0 : (cut1 ? r1 : n));
     }
-    // top-p over ranks [0, kp): Z as one xor tree per 32 ranks, then the
-    // two added; the prefix sums as one scan per 32 ranks with the carry
+    // top-p over ranks [0, kp): rank r is kept iff r == 0 or the sum of the
+    // e's before it is below p * Z
     int kept = kp;
     if (P.top_p < 1.0f) {
-      DF t[2];
+      const DF a0 = r0 < kp ? e0 : zero, a1 = r1 < kp ? e1 : zero;
+      const DF pair = df_add(a0, a1);
+      DF incl = pair;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        DF v = lane + 32 * h < kp ? df_add(zero, e[h]) : zero;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) v = df_add(v, df_shfl_xor(v, off));
-        t[h] = v;
+      for (int off = 1; off < 32; off <<= 1) {
+        const DF o = df_shfl_up(incl, off);
+        if (lane >= off) incl = df_add(o, incl);
       }
-      const DF pz = df_mul_f(df_add(t[0], t[1]), P.top_p);
-      DF inc[2];
-      DF tot = zero;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        DF v = lane + 32 * h < kp ? e[h] : zero;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const DF o = df_shfl_up(v, off);
-          if (lane >= off) v = df_add(v, o);
-        }
-        inc[h] = df_add(tot, v);
-        tot = df_add(tot, df_shfl(v, 31));
-      }
-      const DF end0 = df_shfl(inc[0], 31);
+      const DF pz = df_mul_f(df_shfl(incl, 31), P.top_p);
+      DF before0 = df_shfl_up(incl, 1);  // the sum over ranks < r0
+      if (lane == 0) before0 = zero;
+      const DF before1 = df_add(before0, a0);
       int first = kp;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = lane + 32 * h;
-        DF prev = df_shfl_up(inc[h], 1);
-        if (lane == 0) prev = h == 0 ? zero : end0;
-        const DF before = df_add(zero, prev);
-        if (r < kp && r > 0 && !df_lt(before, pz) && r < first) first = r;
-      }
+      if (r1 < kp && !df_lt(before1, pz)) first = r1;
+      if (r0 >= 1 && r0 < kp && !df_lt(before0, pz)) first = r0;
       kept = __reduce_min_sync(FULL_MASK, first);
     }
     // Gumbel-max over ranks [0, kept): the fp32 screen, fp64 for contenders
-    uint64_t win = __shfl_sync(FULL_MASK, c[0], 0);
+    uint64_t win = __shfl_sync(FULL_MASK, c0, 0);
     if (kept > 1) {
-      float sc[2];
+      const float s0 = r0 < kept
+                           ? __fadd_rn(__fdiv_rn(key_value((uint32_t)(c0 >> 32)), P.temperature), d.g32[r0])
+                           : -INFINITY;
+      const float s1 = r1 < kept
+                           ? __fadd_rn(__fdiv_rn(key_value((uint32_t)(c1 >> 32)), P.temperature), d.g32[r1])
+                           : -INFINITY;
+      // the lane's better of its two ranks (score descending, token ascending)
       float bs = -INFINITY;
       uint64_t bc = 0ull;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = lane + 32 * h;
-        sc[h] = -INFINITY;
-        if (r < kept) {
-          sc[h] = __fadd_rn(__fdiv_rn(key_value((uint32_t)(c[h] >> 32)), P.temperature), g[h]);
-          if (bc == 0ull || sc[h] > bs || (sc[h] == bs && comp_token(c[h]) < comp_token(bc))) {
-            bs = sc[h];
-            bc = c[h];
-          }
-        }
+      if (r0 < kept) {
+        bs = s0;
+        bc = c0;
+      }
+      if (r1 < kept && (bc == 0ull || s1 > bs || (s1 == bs && comp_token(c1) < comp_token(bc)))) {
+        bs = s1;
+        bc = c1;
       }
 #pragma unroll
       for (int off = 16; off; off >>= 1) {
@@ -1776,8 +1758,8 @@ __device__ __noinline__ uint64_t decide_small(const uint64_t *srt, int n, const 
         }
       }
       const float floor_s = bs - (1e-4f + 2e-6f * fabsf(bs));
-      const int close = __popc(__ballot_sync(FULL_MASK, lane < kept && sc[0] >= floor_s)) +
-                        __popc(__ballot_sync(FULL_MASK, lane + 32 < kept && sc[1] >= floor_s));
+      const int close = __popc(__ballot_sync(FULL_MASK, r0 < kept && s0 >= floor_s)) +
+                        __popc(__ballot_sync(FULL_MASK, r1 < kept && s1 >= floor_s));
       if (isfinite(bs) && close == 1) {
         win = bc;
       } else {
@@ -1785,17 +1767,17 @@ __device__ __noinline__ uint64_t decide_small(const uint64_t *srt, int n, const 
         double ds = 0.0;
         int did = -1;
         uint64_t dc = 0ull;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = lane + 32 * h;
-          if (r < kept && (all || sc[h] >= floor_s)) {
-            const int tok = comp_token(c[h]);
-            const double v = comp_x(c[h], P.temperature) + gumbel(P, tok);
-            if (better(v, tok, ds, did)) {
-              ds = v;
-              did = tok;
-              dc = c[h];
-            }
+        if (r0 < kept && (all || s0 >= floor_s)) {
+          ds = comp_x(c0, P.temperature) + gumbel(P, comp_token(c0));
+          did = comp_token(c0);
+          dc = c0;
+        }
+        if (r1 < kept && (all || s1 >= floor_s)) {
+          const double v = comp_x(c1, P.temperature) + gumbel(P, comp_token(c1));
+          if (better(v, comp_token(c1), ds, did)) {
+            ds = v;
+            did = comp_token(c1);
+            dc = c1;
           }
         }
 #pragma unroll
@@ -1813,19 +1795,13 @@ __device__ __noinline__ uint64_t decide_small(const uint64_t *srt, int n, const 
       }
     }
     if (P.lp_proc) {
-      // the kept ranks' mass, summed as mass_of_prefix sums it
-      DF t[2];
+      // the kept ranks' mass
+      DF v = df_add(r0 < kept ? e0 : zero, r1 < kept ? e1 : zero);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        DF v = lane + 32 * h < kept ? df_add(zero, e[h]) : zero;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) v = df_add(v, df_shfl_xor(v, off));
-        t[h] = v;
-      }
-      const DF sk = df_add(t[0], t[1]);
+      for (int off = 16; off; off >>= 1) v = df_add(v, df_shfl_xor(v, off));
       if (lane == 0) {
-        sm.s_kept = (double)sk.h + (double)sk.l;
-        sm.m_row = comp_x(c[0], P.temperature);
+        sm.s_kept = (double)v.h + (double)v.l;
+        sm.m_row = comp_x(c0, P.temperature);
         sm.xbest = comp_x(win, P.temperature);
       }
     }
