@@ -671,11 +671,12 @@ __device__ __forceinline__ int warp_collect_above(const uint32_t *keys, int cnt,
     const bool v = q < nq;
     uint4 u = make_uint4(0u, 0u, 0u, 0u);
     if (v) u = k4[q];
-    const unsigned b0 = __ballot_sync(FULL_MASK, v && u.x >= L);
-    const unsigned b1 = __ballot_sync(FULL_MASK, v && u.y >= L);
-    const unsigned b2 = __ballot_sync(FULL_MASK, v && u.z >= L);
-    const unsigned b3 = __ballot_sync(FULL_MASK, v && u.w >= L);
-    if ((b0 | b1 | b2 | b3) != 0u) {
+    const uint32_t um = max(max(u.x, u.y), max(u.z, u.w));
+    if (__ballot_sync(FULL_MASK, v && um >= L) != 0u) {  // most steps have no hit at all
+      const unsigned b0 = __ballot_sync(FULL_MASK, v && u.x >= L);
+      const unsigned b1 = __ballot_sync(FULL_MASK, v && u.y >= L);
+      const unsigned b2 = __ballot_sync(FULL_MASK, v && u.z >= L);
+      const unsigned b3 = __ballot_sync(FULL_MASK, v && u.w >= L);
       const int n1 = nw + __popc(b0), n2 = n1 + __popc(b1), n3 = n2 + __popc(b2);
       const int id = id0 + 4 * q;
       int pos;
@@ -875,19 +876,25 @@ __device__ __noinline__ DF chunk_exp_sum_split(uint32_t *keys, int cnt, const Ex
     if (i < cnt) df_accumulate(a0, df_exp2_rel(key_value(keys[i]), ctx, sm.e2h, sm.e2l));
   }
   __syncwarp();
+  // four independent terms a step, each into its own sum
+  DF a2 = {0.0f, 0.0f}, a3 = {0.0f, 0.0f};
+  auto big_at = [&](int k) { return key_value(own[4 * (k >> 7) * SB + (k & 127)]); };
   int j = lane;
 #pragma unroll 1
-  for (; j + 32 < nb; j += 64) {
-    const uint32_t ka = own[4 * (j >> 7) * SB + (j & 127)];
-    const uint32_t kb = own[4 * ((j + 32) >> 7) * SB + ((j + 32) & 127)];
-    df_accumulate(a0, df_exp2_rel(key_value(ka), ctx, sm.e2h, sm.e2l));
-    df_accumulate(a1, df_exp2_rel(key_value(kb), ctx, sm.e2h, sm.e2l));
+  for (; j + 96 < nb; j += 128) {
+    const float xa = big_at(j), xb = big_at(j + 32), xc = big_at(j + 64), xd = big_at(j + 96);
+    df_accumulate(a0, df_exp2_rel(xa, ctx, sm.e2h, sm.e2l));
+    df_accumulate(a1, df_exp2_rel(xb, ctx, sm.e2h, sm.e2l));
+    df_accumulate(a2, df_exp2_rel(xc, ctx, sm.e2h, sm.e2l));
+    df_accumulate(a3, df_exp2_rel(xd, ctx, sm.e2h, sm.e2l));
   }
-  if (j < nb) df_accumulate(a0, df_exp2_rel(key_value(own[4 * (j >> 7) * SB + (j & 127)]), ctx,
-                                            sm.e2h, sm.e2l));
+#pragma unroll 1
+  for (; j < nb; j += 32) df_accumulate(a0, df_exp2_rel(big_at(j), ctx, sm.e2h, sm.e2l));
   df_accumulate(a1, DF{s0, 0.0f});
   df_accumulate(a1, DF{s1, 0.0f});
-  return block_sum_df(df_add(df_fast_two_sum(a0.h, a0.l), df_fast_two_sum(a1.h, a1.l)), sm);
+  const DF lo = df_add(df_fast_two_sum(a0.h, a0.l), df_fast_two_sum(a1.h, a1.l));
+  const DF hi = df_add(df_fast_two_sum(a2.h, a2.l), df_fast_two_sum(a3.h, a3.l));
+  return block_sum_df(df_add(lo, hi), sm);
 }
 
 // Keep everything: the chunk's Gumbel argmax in fp64 (the definition);
@@ -1483,7 +1490,8 @@ __device__ __noinline__ void union_sorted_slow(const ChunkRec *recs, int nc, int
 
 // The normaliser of the whole row relative to its maximum: the chunks'
 // partials z_c (relative to each chunk's maximum; staged in sm.fh / sm.fl)
-// times 2^(t_c - t_0), added in chunk order.
+// times 2^(t_c - t_0), added by warp 0 in a fixed order (chunks c and
+// c + 32 per lane, then a xor tree).
 __device__ DF row_normaliser(int nch, const Exp2Ctx &ctx, SampSmem &sm) {
   const int tid = threadIdx.x;
   DF f = {0.0f, 0.0f};
@@ -1491,17 +1499,23 @@ __device__ DF row_normaliser(int nch, const Exp2Ctx &ctx, SampSmem &sm) {
     const DF w = df_exp2_rel(key_value((uint32_t)(sm.htop[tid] >> 32)), ctx, sm.e2h, sm.e2l);
     f = df_mul(DF{sm.fh[tid], sm.fl[tid]}, w);
   }
+  // warp 0 adds the (at most 64) rescaled partials: lanes c and c + 32,
+  // then a xor tree
   __syncthreads();
-  if (tid < nch) {
+  if (tid >= 32 && tid < nch) {
     sm.fh[tid] = f.h;
     sm.fl[tid] = f.l;
   }
   __syncthreads();
-  if (tid == 0) {
-    DF z = {0.0f, 0.0f};
-    for (int c = 0; c < nch; ++c) z = df_add(z, DF{sm.fh[c], sm.fl[c]});
-    sm.zh = z.h;
-    sm.zl = z.l;
+  if (tid < 32) {
+    DF z = f;
+    if (tid + 32 < nch) z = df_add(z, DF{sm.fh[tid + 32], sm.fl[tid + 32]});
+#pragma unroll
+    for (int off = 16; off; off >>= 1) z = df_add(z, df_shfl_xor(z, off));
+    if (tid == 0) {
+      sm.zh = z.h;
+      sm.zl = z.l;
+    }
   }
   __syncthreads();
   const DF z = {sm.zh, sm.zl};
