@@ -810,88 +810,27 @@ __device__ __noinline__ int chunk_select_sorted(const uint32_t *keys, int cnt, i
   return C;
 }
 
-// Sum over the chunk of 2^(key_value(k) * c2 - t_max), in double-float; all
-// threads get it.  A term below 2^-24 of the chunk's largest (t - t_max <
-// -24, t formed in fp32) is taken on the SFU in fp32 -- its error, under
-// 2^-24 * 3e-6 of the largest, is far below the double-float sum's.  The
-// larger terms' keys are gathered, per warp, over the keys the warp has
-// already read (word j % 128 of its (j / 128)-th block of 32 uint4), and
-// then taken in double-float two at a time.  This destroys the keys.  The
-// same sum as with every term in double-float to ~1e-9 relative.
-__device__ __noinline__ DF chunk_exp_sum_split(uint32_t *keys, int cnt, const Exp2Ctx ctx,
-                                               SampSmem &sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned lt = (1u << lane) - 1u;
+// Sum over the chunk of 2^(key_value(k) * c2 - t_max), every term in
+// double-float (Tang's table-driven exp2, exact two-sum accumulation); all
+// threads get it.  Each thread takes four keys at a time (a uint4) into four
+// independent sums.  (Taking the terms below 2^-24 of the largest on the
+// SFU in fp32 and listing only the larger ones for double-float was slower
+// on every logit spread measured: the listing costs more than it saves.)
+__device__ __noinline__ DF chunk_exp_sum_all(const uint32_t *keys, int cnt, const Exp2Ctx ctx,
+                                             SampSmem &sm) {
   const int nq = cnt >> 2;
   const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
-  uint32_t *own = keys + 4 * warp * 32;  // the warp's first block; block m is at own + 4 * m * SB
-  float s0 = 0.0f, s1 = 0.0f;
-  int nb = 0;  // warp-uniform
+  DF a0 = {0.0f, 0.0f}, a1 = {0.0f, 0.0f}, a2 = {0.0f, 0.0f}, a3 = {0.0f, 0.0f};
 #pragma unroll 1
-  for (int base = warp * 32; base < nq; base += SB) {  // the same trip count in every lane
-    const int q = base + lane;
-    const bool v = q < nq;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (v) u = k4[q];
-    const float t0 = fmaf(key_value(u.x), ctx.c2h, -ctx.th);
-    const float t1 = fmaf(key_value(u.y), ctx.c2h, -ctx.th);
-    const float t2 = fmaf(key_value(u.z), ctx.c2h, -ctx.th);
-    const float t3 = fmaf(key_value(u.w), ctx.c2h, -ctx.th);
-    // NaN and -inf logits give t = -inf: a zero small term
-    if (v) {
-      s0 += (t0 < -24.0f ? fast_exp2(t0) : 0.0f) + (t1 < -24.0f ? fast_exp2(t1) : 0.0f);
-      s1 += (t2 < -24.0f ? fast_exp2(t2) : 0.0f) + (t3 < -24.0f ? fast_exp2(t3) : 0.0f);
-    }
-    const unsigned b0 = __ballot_sync(FULL_MASK, v && !(t0 < -24.0f));
-    const unsigned b1 = __ballot_sync(FULL_MASK, v && !(t1 < -24.0f));
-    const unsigned b2 = __ballot_sync(FULL_MASK, v && !(t2 < -24.0f));
-    const unsigned b3 = __ballot_sync(FULL_MASK, v && !(t3 < -24.0f));
-    if ((b0 | b1 | b2 | b3) != 0u) {
-      // every lane has read this block (the ballots wait for it), and at
-      // most 128 (k + 1) terms were found in the first k + 1 blocks
-      const int n1 = nb + __popc(b0), n2 = n1 + __popc(b1), n3 = n2 + __popc(b2);
-      int j;
-      if ((b0 >> lane) & 1u) {
-        j = nb + __popc(b0 & lt);
-        own[4 * (j >> 7) * SB + (j & 127)] = u.x;
-      }
-      if ((b1 >> lane) & 1u) {
-        j = n1 + __popc(b1 & lt);
-        own[4 * (j >> 7) * SB + (j & 127)] = u.y;
-      }
-      if ((b2 >> lane) & 1u) {
-        j = n2 + __popc(b2 & lt);
-        own[4 * (j >> 7) * SB + (j & 127)] = u.z;
-      }
-      if ((b3 >> lane) & 1u) {
-        j = n3 + __popc(b3 & lt);
-        own[4 * (j >> 7) * SB + (j & 127)] = u.w;
-      }
-      nb = n3 + __popc(b3);
-    }
+  for (int q = threadIdx.x; q < nq; q += SB) {
+    const uint4 u = k4[q];
+    df_accumulate(a0, df_exp2_rel(key_value(u.x), ctx, sm.e2h, sm.e2l));
+    df_accumulate(a1, df_exp2_rel(key_value(u.y), ctx, sm.e2h, sm.e2l));
+    df_accumulate(a2, df_exp2_rel(key_value(u.z), ctx, sm.e2h, sm.e2l));
+    df_accumulate(a3, df_exp2_rel(key_value(u.w), ctx, sm.e2h, sm.e2l));
   }
-  DF a0 = {0.0f, 0.0f}, a1 = {0.0f, 0.0f};
-  if (warp == 0) {  // the last cnt % 4 keys, straight in double-float
-    const int i = 4 * nq + lane;
-    if (i < cnt) df_accumulate(a0, df_exp2_rel(key_value(keys[i]), ctx, sm.e2h, sm.e2l));
-  }
-  __syncwarp();
-  // four independent terms a step, each into its own sum
-  DF a2 = {0.0f, 0.0f}, a3 = {0.0f, 0.0f};
-  auto big_at = [&](int k) { return key_value(own[4 * (k >> 7) * SB + (k & 127)]); };
-  int j = lane;
-#pragma unroll 1
-  for (; j + 96 < nb; j += 128) {
-    const float xa = big_at(j), xb = big_at(j + 32), xc = big_at(j + 64), xd = big_at(j + 96);
-    df_accumulate(a0, df_exp2_rel(xa, ctx, sm.e2h, sm.e2l));
-    df_accumulate(a1, df_exp2_rel(xb, ctx, sm.e2h, sm.e2l));
-    df_accumulate(a2, df_exp2_rel(xc, ctx, sm.e2h, sm.e2l));
-    df_accumulate(a3, df_exp2_rel(xd, ctx, sm.e2h, sm.e2l));
-  }
-#pragma unroll 1
-  for (; j < nb; j += 32) df_accumulate(a0, df_exp2_rel(big_at(j), ctx, sm.e2h, sm.e2l));
-  df_accumulate(a1, DF{s0, 0.0f});
-  df_accumulate(a1, DF{s1, 0.0f});
+  for (int i = 4 * nq + (int)threadIdx.x; i < cnt; i += SB)
+    df_accumulate(a0, df_exp2_rel(key_value(keys[i]), ctx, sm.e2h, sm.e2l));
   const DF lo = df_add(df_fast_two_sum(a0.h, a0.l), df_fast_two_sum(a1.h, a1.l));
   const DF hi = df_add(df_fast_two_sum(a2.h, a2.l), df_fast_two_sum(a3.h, a3.l));
   return block_sum_df(df_add(lo, hi), sm);
@@ -1123,7 +1062,7 @@ __device__ __noinline__ void chunk_pass(const float *row, int V, int c, const Ro
   if (P.need_z) {
     // sum over the chunk of exp(x - mx) = 2^(t - t_max), t = logit * log2(e) / T
     const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
-    const DF z = chunk_exp_sum_split(keys, cnt, ctx, sm);
+    const DF z = chunk_exp_sum_all(keys, cnt, ctx, sm);
     if (tid == 0) {
       rec->zh = z.h;
       rec->zl = z.l;
