@@ -836,8 +836,8 @@ def measure_decode(name, args, rank, world, local, clocks, full):
         "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
-        "compute": "bf16 in, fp32 accumulate (attention); sampler decisions in fp64, "
-                   "chunk normalisers in double-float fp32 pairs",
+        "compute": "bf16 in, fp32 accumulate (attention); sampler: the fp64 decisions via "
+                   "double-float (fp32 pair) sums and an fp32 Gumbel screen, fp64 for contenders",
         "data": "synthetic",
         "config": workload_config(cfg, batch, l2_note(cfg, sizes)),
         "sampled_rows_per_s": world * sizes["n_active"] * args.steps / (total_ms / 1e3),
