@@ -67,6 +67,8 @@
 #include <math.h>
 #include <stddef.h>
 
+#include <atomic>
+
 #include "pkv_device.cuh"
 #include "pkv_host.h"
 
@@ -916,15 +918,21 @@ __device__ __noinline__ void chunk_radix_top(const uint32_t *keys, int start, in
 // pbits: the row's penalty bitmap in global memory, written for this chunk
 // when the row is penalised (may be null otherwise).  prestaged: the
 // caller has already put the chunk's logits into sm.u.ch.keys.
+// What a chunk CTA computes: everything, or (a row whose chunks each get
+// two CTAs) the candidates and the rest, or the two normaliser partials
+// (the raw log-softmax one and the processed one, each when asked for).
+enum ChunkPart : int { PART_ALL = 0, PART_SELECT = 1, PART_NORM = 2 };
+
 __device__ __noinline__ void chunk_pass(const float *row, int V, int c, const RowParams &P,
-                                        ChunkRec *rec,
-                           uint32_t *pbits, SampSmem &sm, int32_t *err, bool prestaged = false) {
+                                        ChunkRec *rec, uint32_t *pbits, SampSmem &sm,
+                                        int32_t *err, bool prestaged = false,
+                                        int part = PART_ALL) {
   const int tid = threadIdx.x;
   const int start = c * CHUNK;
   const int cnt = min(CHUNK, V - start);
   uint32_t *keys = sm.u.ch.keys;
   if (!prestaged) stage_chunk(row, start, cnt, keys);
-  if (P.lp_raw) {
+  if (P.lp_raw && part != PART_SELECT) {
     // raw log-softmax partials: the chunk maximum of the unprocessed logits
     // and sum exp(logit - max) = sum 2^((logit - max) log2(e))
     uint32_t km = 0;
@@ -946,6 +954,7 @@ __device__ __noinline__ void chunk_pass(const float *row, int V, int c, const Ro
       rec->rzl = z.l;
     }
   }
+  if (part == PART_NORM && !P.need_z) return;
   const bool pen_on = P.n_pen > 0;
   uint32_t *penbits = sm.u.ch.penbits;
   if (pen_on) {
@@ -1003,6 +1012,18 @@ __device__ __noinline__ void chunk_pass(const float *row, int V, int c, const Ro
     if (bad) report(err, PKV_DEV_ERR_LOGITS);
   }
   __syncthreads();  // the keys, written four per thread, are read in other layouts below
+  if (part == PART_NORM) {
+    // the normaliser partial alone, relative to the chunk's largest key
+    const uint32_t kmax = (uint32_t)block_max_u64(m, sm);
+    const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value(kmax));
+    const DF z = chunk_exp_sum_all(keys, cnt, ctx, sm);
+    if (tid == 0) {
+      rec->zh = z.h;
+      rec->zl = z.l;
+    }
+    __syncthreads();
+    return;
+  }
   const int nc = P.nc;
   const bool sel = P.mode == MODE_TOPK_SMALL || P.mode == MODE_TOPP_FULL;
   uint64_t top1 = 0ull;
@@ -1059,7 +1080,7 @@ __device__ __noinline__ void chunk_pass(const float *row, int V, int c, const Ro
       rec->gkey = bkey;
     }
   }
-  if (P.need_z) {
+  if (P.need_z && part == PART_ALL) {
     // sum over the chunk of exp(x - mx) = 2^(t - t_max), t = logit * log2(e) / T
     const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
     const DF z = chunk_exp_sum_all(keys, cnt, ctx, sm);
@@ -1993,6 +2014,7 @@ struct SampleArgs {
   int32_t *out_tok;
   int32_t *out_kind;
   ChunkRec *recs;  // [B][nch]
+  int zsplit;      // a second CTA per chunk (grid rows B..2B-1) takes the normaliser
   int32_t *err;
   // further controls (null: off)
   const float *min_p;          // [num_slots]
@@ -2033,9 +2055,13 @@ __device__ __forceinline__ uint32_t *row_pbits(const SampleArgs &a, int b) {
   return a.pbits != nullptr ? a.pbits + (int64_t)b * a.nch * (CHUNK / 32) : nullptr;
 }
 
+// One CTA per (chunk, row); with zsplit, grid rows B..2B-1 are a second CTA
+// per chunk that computes the chunk's normaliser partial while the first
+// selects the candidates (rows that need no normaliser leave it at once).
 __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   __shared__ SampSmem sm;
-  const int b = blockIdx.y;
+  const bool zcta = (int)blockIdx.y >= a.batch;
+  const int b = zcta ? (int)blockIdx.y - a.batch : (int)blockIdx.y;
   const int c = blockIdx.x;
   // launched behind its predecessor on the stream (programmatic dependent
   // launch): nothing is read before that grid has completed
@@ -2043,10 +2069,16 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   if (!a.active[b]) return;
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) return;
-  load_exp2_table(sm);  // read after the first barrier of the chunk pass
   const RowParams P = sample_row_params(a, slot);
+  int part = PART_ALL;
+  if (a.zsplit && (P.need_z || P.lp_raw))
+    part = zcta ? PART_NORM : PART_SELECT;
+  else if (zcta)
+    return;
+  load_exp2_table(sm);  // read after the first barrier of the chunk pass
   chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, c, P,
-             a.recs + (int64_t)b * a.nch + c, row_pbits(a, b), sm, a.err);
+             a.recs + (int64_t)b * a.nch + c, part == PART_NORM ? nullptr : row_pbits(a, b), sm,
+             a.err, false, part);
   // the finish kernel may be scheduled once every chunk CTA is here (late,
   // so that its waiting CTAs do not take SM room from the chunk pass)
   pdl_trigger();
@@ -2305,6 +2337,19 @@ static int check_sampler_common(int batch, int vocab, const int32_t *slots, cons
 
 static bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
 
+// SMs of the current device (0 when it cannot be read); cached per device
+static int sm_count() {
+  static std::atomic<int> count[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int n = count[dev & 63].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    count[dev & 63].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 static int launch_sample(const float *logits, int64_t row_stride, int batch, int vocab,
                          const int32_t *slots, const int32_t *active, int num_slots,
                          const uint64_t *seeds, int64_t *steps, const float *temperature,
@@ -2369,8 +2414,13 @@ static int launch_sample(const float *logits, int64_t row_stride, int batch, int
                                                  pkv_sample_workspace_bytes(batch, vocab))
                   : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_pdl(sample_chunk_kernel, dim3((unsigned)a.nch, (unsigned)batch), dim3(SB), 0, s, a) !=
-      cudaSuccess)
+  // a second CTA per chunk for the normaliser when the chunk grid leaves
+  // room on the SMs (two CTAs per SM at most)
+  const int sms = sm_count();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  a.zsplit = (int64_t)a.nch * batch <= 2 * (int64_t)sms ? 1 : 0;
+  if (launch_pdl(sample_chunk_kernel, dim3((unsigned)a.nch, (unsigned)(batch * (1 + a.zsplit))),
+                 dim3(SB), 0, s, a) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (launch_pdl(sample_finish_kernel, dim3((unsigned)batch), dim3(SB), 0, s, a) != cudaSuccess)
     return PKV_ERR_CUDA;

@@ -100,7 +100,10 @@ int main(int argc, char **argv) {
     a.pbits = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(ws) + rec_bytes);
   }
   a.err = &err;
-  emu_launch(sample_chunk_kernel, dim3(a.nch, B), SB, a);
+  // the second CTA per chunk for the normaliser: on unless EMU_ZSPLIT=0
+  const char *zs = std::getenv("EMU_ZSPLIT");
+  a.zsplit = (zs != nullptr && zs[0] == '0') ? 0 : 1;
+  emu_launch(sample_chunk_kernel, dim3(a.nch, B * (1 + a.zsplit)), SB, a);
   emu_launch(sample_finish_kernel, dim3(B), SB, a);
   free(ws);
 

@@ -45,9 +45,11 @@ def emu_binary(tmp_path_factory):
     return exe
 
 
-def _run(exe, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p, ext=None):
+def _run(exe, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p, ext=None, zsplit=1):
     """ext: dict of min_p, rep_penalty, rep_window, history [S, cap],
-    hist_len, advance (the pkv_seeded_sample_ext settings).  Returns
+    hist_len, advance (the pkv_seeded_sample_ext settings).  zsplit: launch
+    the second CTA per chunk that computes the normaliser (the host does so
+    whenever the chunk grid is at most two CTAs per SM).  Returns
     (out_tok, out_kind, err) and, with ext, also (logprob_raw, logprob_proc,
     hist_len, history, steps) after the call."""
     B, V = x.shape
@@ -65,7 +67,7 @@ def _run(exe, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p, ext=
                      (np.array([int(ext["advance"])]), np.int32)]
         for arr, dt in arrs:
             np.ascontiguousarray(arr, dtype=dt).tofile(f)
-    env = dict(os.environ, ASAN_OPTIONS="detect_leaks=0")
+    env = dict(os.environ, ASAN_OPTIONS="detect_leaks=0", EMU_ZSPLIT=str(int(zsplit)))
     r = subprocess.run([str(exe), str(inp), str(out)], capture_output=True, text=True, env=env,
                        timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
@@ -116,8 +118,22 @@ CASES = [
 ]
 
 
+# cases that need the row normaliser, run again with one CTA per chunk (the
+# launch for grids larger than two CTAs per SM)
+ONE_CTA_CASES = [CASES[3], CASES[7], CASES[8], CASES[12]]
+
+
 @pytest.mark.parametrize("B,V,std,T,k,p,dist", CASES)
 def test_emulated_sampler_matches_oracle(emu_binary, tmp_path, B, V, std, T, k, p, dist):
+    _check_case(emu_binary, tmp_path, B, V, std, T, k, p, dist, zsplit=1)
+
+
+@pytest.mark.parametrize("B,V,std,T,k,p,dist", ONE_CTA_CASES)
+def test_emulated_sampler_one_cta_per_chunk(emu_binary, tmp_path, B, V, std, T, k, p, dist):
+    _check_case(emu_binary, tmp_path, B, V, std, T, k, p, dist, zsplit=0)
+
+
+def _check_case(emu_binary, tmp_path, B, V, std, T, k, p, dist, zsplit):
     rng = np.random.default_rng(V + k)
     x = rng.normal(0, std, (B, V)).astype(np.float32)
     if dist == "conc":
@@ -144,7 +160,8 @@ def test_emulated_sampler_matches_oracle(emu_binary, tmp_path, B, V, std, T, k, 
     temp = np.full(S, T, np.float32)
     top_k = np.full(S, k, np.int32)
     top_p = np.full(S, p, np.float32)
-    got, kind, err = _run(emu_binary, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p)
+    got, kind, err = _run(emu_binary, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p,
+                          zsplit=zsplit)
     x_ref = np.concatenate([x_ref, np.zeros((1, V), np.float32)])
     want, wkind, info, _ = oracle.seeded_sample(x_ref, slots, active, seeds, steps.copy(), temp,
                                                    top_k, top_p, advance=False)
