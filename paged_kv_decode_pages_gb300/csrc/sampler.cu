@@ -413,6 +413,9 @@ struct __align__(16) SampSmem {
   int32_t wcnt[SB / 32];                     // per-warp list lengths
   uint64_t htop[MAX_CHUNKS], hthr[MAX_CHUNKS];  // the chunks' largest composites and bounds
   float fh[MAX_CHUNKS], fl[MAX_CHUNKS];      // the chunks' rescaled normalisers
+  uint64_t s_top1, s_bound;                  // over the chunks: largest composite, largest bound
+  int32_t s_total, s_sorted;                 // over the chunks: candidates, all lists in order
+  int32_t s_pad[2];                          // keeps the buffers below 16-byte aligned
   float wbs[SB / 32];                        // per-warp best fp32 scores
   uint64_t sel_prefix;
   uint64_t nth;      // rank_out: the composite of rank n - 1
@@ -1305,14 +1308,45 @@ __device__ __noinline__ int general_sample(const RowView &rv, int V, const RowPa
 __device__ int stage_records(const ChunkRec *recs, int nch, int nc, int R, SampSmem &sm,
                              bool *all_sorted, bool rec_smem = false) {
   const int tid = threadIdx.x;
-  if (tid < nch) {
-    const ChunkRec &rc = recs[tid];
-    sm.cn[tid] = rc.ncand;
-    sm.htop[tid] = rc.top1;
-    sm.hthr[tid] = rc.thr;
-    sm.fh[tid] = rc.zh;
-    sm.fl[tid] = rc.zl;
-    sm.csorted[tid] = rc.sorted;
+  if (tid < 32) {
+    // warp 0: the headers of chunks lane and lane + 32, and over all chunks
+    // the largest composite, the largest bound, the candidate count and
+    // whether every list is in order
+    uint64_t t1 = 0ull, bd = 0ull;
+    int tot = 0, uns = 0;
+#pragma unroll
+    for (int h = 0; h < MAX_CHUNKS / 32; ++h) {
+      const int c = tid + 32 * h;
+      if (c < nch) {
+        const ChunkRec &rc = recs[c];
+        const int cn = rc.ncand, so = rc.sorted;
+        const uint64_t top = rc.top1, thr = rc.thr;
+        sm.cn[c] = cn;
+        sm.htop[c] = top;
+        sm.hthr[c] = thr;
+        sm.fh[c] = rc.zh;
+        sm.fl[c] = rc.zl;
+        sm.csorted[c] = so;
+        t1 = top > t1 ? top : t1;
+        bd = thr > bd ? thr : bd;
+        tot += cn;
+        uns |= so == 0;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      const uint64_t a = __shfl_xor_sync(FULL_MASK, t1, off), b = __shfl_xor_sync(FULL_MASK, bd, off);
+      t1 = a > t1 ? a : t1;
+      bd = b > bd ? b : bd;
+    }
+    tot = __reduce_add_sync(FULL_MASK, tot);
+    uns = __ballot_sync(FULL_MASK, uns) != 0u;
+    if (tid == 0) {
+      sm.s_top1 = t1;
+      sm.s_bound = bd;
+      sm.s_total = tot;
+      sm.s_sorted = !uns;
+    }
   }
   if (nch * R <= UNION_MAX && !rec_smem) {
     uint64_t *uni = sm.u.fi.uni;
@@ -1326,14 +1360,8 @@ __device__ int stage_records(const ChunkRec *recs, int nch, int nc, int R, SampS
     cp_async_wait_all();
   }
   __syncthreads();
-  int total = 0;
-  bool srt = true;
-  for (int c = 0; c < nch; ++c) {
-    total += sm.cn[c];
-    srt = srt && sm.csorted[c] != 0;
-  }
-  *all_sorted = srt;
-  return total;
+  *all_sorted = sm.s_sorted != 0;
+  return sm.s_total;
 }
 
 
@@ -1421,6 +1449,108 @@ __device__ __noinline__ int merge_heads(int nch, int R, int H, SampSmem &sm) {
   const int exact = min(total, (int)sm.done);
   __syncthreads();
   return exact;
+}
+
+// The whole union in descending order into sm.u.fi.uni[0, P), P = E * SB:
+// the nch lists there at stride R (a power of two, R >= E), each in
+// descending order and sm.cn[c] long, padded with zeros (which order last)
+// past each list and past the last list, then runs of R, 2R, ... merged
+// pairwise by bitonic merging: a stage that compares entry j of a run with
+// entry 2n - 1 - j of the pair (n the run length; the partner of entry i
+// is i ^ (2n - 1)), then stages at distances d = n/2, ..., 1 within each
+// half (partner i ^ d).  Thread t holds entries tE .. tE + E - 1 in
+// registers: distances below E are compare-exchanges in the thread, those
+// within the warp's 32E entries shuffles, longer ones go through shared
+// memory (the two halves of sm.u.fi.uni in turn, so that one barrier per
+// stage suffices).  nch * R <= P.
+template <int E>
+__device__ __noinline__ void bitonic_union(int nch, int R, SampSmem &sm) {
+  static_assert(E == 2 || E == 4, "two or four entries a thread");
+  constexpr int P = E * SB, WSPAN = 32 * E;
+  static_assert(2 * P <= UNION_MAX, "two stage buffers fit the union buffer");
+  uint64_t *buf = sm.u.fi.uni;
+  const int tid = threadIdx.x;
+  const int lr = 31 - __clz(R);
+  const int b0 = tid * E;
+  uint64_t v[E];
+  auto load_e = [&](const uint64_t *src, uint64_t (&w)[E]) {
+#pragma unroll
+    for (int h = 0; h < E / 2; ++h) {
+      const ulonglong2 q = reinterpret_cast<const ulonglong2 *>(src)[h];
+      w[2 * h] = q.x;
+      w[2 * h + 1] = q.y;
+    }
+  };
+  auto store_e = [&](uint64_t *dst) {
+#pragma unroll
+    for (int h = 0; h < E / 2; ++h) {
+      ulonglong2 q;
+      q.x = v[2 * h];
+      q.y = v[2 * h + 1];
+      reinterpret_cast<ulonglong2 *>(dst)[h] = q;
+    }
+  };
+  // the larger of the pair to the lower index
+  auto keep = [](uint64_t a, uint64_t b, bool lower) -> uint64_t {
+    return (lower == (b > a)) ? b : a;
+  };
+  load_e(buf + b0, v);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = b0 + e, c = i >> lr;
+    if (c >= nch || (i & (R - 1)) >= sm.cn[c]) v[e] = 0ull;
+  }
+  int half = 1;  // the stage buffer the next stage through shared memory uses
+#pragma unroll 1
+  for (int n = R; n < P; n <<= 1) {
+    const bool lo = (b0 & n) == 0;  // this thread's entries are in the first run of the pair
+    uint64_t y[E];
+    if (2 * n <= WSPAN) {
+      const int m = (2 * n - 1) / E;  // the partner thread: lane ^ m, entry E - 1 - e
+#pragma unroll
+      for (int e = 0; e < E; ++e) y[e] = __shfl_xor_sync(FULL_MASK, v[E - 1 - e], m);
+    } else {
+      uint64_t *st = buf + half * P;
+      store_e(st + b0);
+      __syncthreads();
+      uint64_t w[E];
+      load_e(st + (b0 ^ (2 * n - E)), w);  // the partner's entries, in reverse
+#pragma unroll
+      for (int e = 0; e < E; ++e) y[e] = w[E - 1 - e];
+      half ^= 1;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = keep(v[e], y[e], lo);
+#pragma unroll 1
+    for (int d = n >> 1; d >= E; d >>= 1) {
+      const bool dl = (b0 & d) == 0;
+      if (d < WSPAN) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) y[e] = __shfl_xor_sync(FULL_MASK, v[e], d / E);
+      } else {
+        uint64_t *st = buf + half * P;
+        store_e(st + b0);
+        __syncthreads();
+        load_e(st + (b0 ^ d), y);
+        half ^= 1;
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = keep(v[e], y[e], dl);
+    }
+    // distances below E, in the thread
+#pragma unroll
+    for (int dd = E / 2; dd >= 1; dd >>= 1)
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if ((e & dd) == 0) {
+          const uint64_t a = v[e], b = v[e + dd];
+          v[e] = a > b ? a : b;
+          v[e + dd] = a > b ? b : a;
+        }
+  }
+  __syncthreads();  // the last stage through shared memory may have read buf[0, P)
+  store_e(buf + b0);
+  __syncthreads();
 }
 
 // The nv largest composites of the union in descending order into
@@ -1801,8 +1931,9 @@ __device__ __noinline__ int finish_row(const RowView &rv, int V, int nch, const 
   bool all_sorted;
   const bool cand_mode = P.mode == MODE_TOPK_SMALL || P.mode == MODE_TOPP_FULL;
   const int nreal = stage_records(recs, nch, nc, cand_mode ? R : 0, sm, &all_sorted, rec_smem);
-  uint64_t top1 = 0;
-  for (int c = 0; c < nch; ++c) top1 = sm.htop[c] > top1 ? sm.htop[c] : top1;
+  const uint64_t top1 = sm.s_top1;
+  // the chunks hold no token outside the union above this bound
+  const uint64_t bound = sm.s_bound;
   if (P.mode == MODE_GREEDY) return comp_token(top1);
   const Exp2Ctx ctx = exp2_ctx(P.c2h, P.c2l, key_value((uint32_t)(top1 >> 32)));
   if (P.mode == MODE_ALL) {
@@ -1847,8 +1978,6 @@ __device__ __noinline__ int finish_row(const RowView &rv, int V, int nch, const 
   // over the whole vocabulary the first 256 ranks, then, if the decision is
   // still open there, all NCAND.  A single chunk's list is in order already.
   const bool staged = nu <= UNION_MAX && all_sorted;
-  uint64_t bound = 0ull;  // the chunks hold no token outside the union above it
-  for (int c = 0; c < nch; ++c) bound = sm.hthr[c] > bound ? sm.hthr[c] : bound;
   const uint64_t *srt = sm.sortbuf;
   int kept = 0, kp = nv;
   bool general = true;
@@ -1858,6 +1987,14 @@ __device__ __noinline__ int finish_row(const RowView &rv, int V, int nch, const 
     if (nch == 1 && staged) {
       srt = rec_smem ? recs[0].cand : sm.u.fi.uni;
       attempt = 2;  // nothing more to read later
+    } else if (staged && !rec_smem && R >= 4 && nch * R <= 4 * SB) {
+      // the whole union in order, in place
+      if (nch * R <= 2 * SB)
+        bitonic_union<2>(nch, R, sm);
+      else
+        bitonic_union<4>(nch, R, sm);
+      srt = sm.u.fi.uni;
+      attempt = 2;
     } else if (staged && attempt < 2) {
       // the heads of the lists first, about twice each list's share of the
       // ranks wanted (for top-p over the whole vocabulary 256 at first),
