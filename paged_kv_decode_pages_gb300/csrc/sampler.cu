@@ -2152,6 +2152,7 @@ struct SampleArgs {
   int32_t *out_kind;
   ChunkRec *recs;  // [B][nch]
   int zsplit;      // a second CTA per chunk (grid rows B..2B-1) takes the normaliser
+  int one_wave;    // every chunk CTA is resident at once
   int32_t *err;
   // further controls (null: off)
   const float *min_p;          // [num_slots]
@@ -2203,6 +2204,13 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   // launched behind its predecessor on the stream (programmatic dependent
   // launch): nothing is read before that grid has completed
   pdl_wait();
+  // The finish kernel may be scheduled once every chunk CTA has passed its
+  // wait (or exited).  When the chunk grid runs in one wave that is at
+  // once: the finish CTAs take only the room that chunk CTAs leave, and
+  // have their prologue done when the last chunk CTA ends.  Otherwise at
+  // the end, so that waiting finish CTAs do not hold room the later chunk
+  // CTAs need.
+  if (a.one_wave) pdl_trigger();
   if (!a.active[b]) return;
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) return;
@@ -2216,9 +2224,7 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, c, P,
              a.recs + (int64_t)b * a.nch + c, part == PART_NORM ? nullptr : row_pbits(a, b), sm,
              a.err, false, part);
-  // the finish kernel may be scheduled once every chunk CTA is here (late,
-  // so that its waiting CTAs do not take SM room from the chunk pass)
-  pdl_trigger();
+  if (!a.one_wave) pdl_trigger();
 }
 
 __device__ __forceinline__ void sample_skip_row(const SampleArgs &a, int b) {
@@ -2474,14 +2480,20 @@ static int check_sampler_common(int batch, int vocab, const int32_t *slots, cons
 
 static bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
 
-// SMs of the current device (0 when it cannot be read); cached per device
-static int sm_count() {
+// Chunk CTAs resident at once on the current device (SMs x CTAs per SM; 0
+// when it cannot be read); cached per device
+static int chunk_ctas_resident() {
   static std::atomic<int> count[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   int n = count[dev & 63].load(std::memory_order_relaxed);
   if (n == 0) {
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    int sms = 0, per = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, pkv::sample_chunk_kernel, pkv::SB, 0) !=
+            cudaSuccess)
+      return 0;
+    n = sms * per;
     count[dev & 63].store(n, std::memory_order_relaxed);
   }
   return n;
@@ -2551,11 +2563,13 @@ static int launch_sample(const float *logits, int64_t row_stride, int batch, int
                                                  pkv_sample_workspace_bytes(batch, vocab))
                   : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // a second CTA per chunk for the normaliser when the chunk grid leaves
-  // room on the SMs (two CTAs per SM at most)
-  const int sms = sm_count();
-  if (sms <= 0) return PKV_ERR_CUDA;
-  a.zsplit = (int64_t)a.nch * batch <= 2 * (int64_t)sms ? 1 : 0;
+  // a second CTA per chunk for the normaliser when the two fit on the SMs
+  // at once
+  const int64_t resident = chunk_ctas_resident();
+  if (resident <= 0) return PKV_ERR_CUDA;
+  const int64_t ctas = (int64_t)a.nch * batch;
+  a.zsplit = 2 * ctas <= resident ? 1 : 0;
+  a.one_wave = ctas * (1 + a.zsplit) <= resident ? 1 : 0;
   if (launch_pdl(sample_chunk_kernel, dim3((unsigned)a.nch, (unsigned)(batch * (1 + a.zsplit))),
                  dim3(SB), 0, s, a) != cudaSuccess)
     return PKV_ERR_CUDA;
