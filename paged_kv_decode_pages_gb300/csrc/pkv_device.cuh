@@ -204,6 +204,11 @@ __device__ __forceinline__ f32x2 fmul2(f32x2 a, f32x2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ f32x2 fsub2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 // two bf16 (one 32-bit word, low half first) -> an fp32 pair, exactly
 __device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) {
   f32x2 r;

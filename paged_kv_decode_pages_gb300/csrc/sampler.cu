@@ -245,6 +245,59 @@ __device__ __forceinline__ void df_accumulate(DF &acc, DF e) {
   acc.l = __fadd_rn(acc.l, __fadd_rn(s.l, e.l));
 }
 
+// The same two computations on packed fp32 pairs, each half exactly the
+// scalar function's operations (so each half's result is the scalar one):
+// df_exp2_rel of two values, df_accumulate of two accumulators.
+struct DF2 {
+  f32x2 h, l;
+};
+__device__ __forceinline__ DF2 df2_exp2_rel(f32x2 v, const Exp2Ctx &c, const float *tab_h,
+                                            const float *tab_l) {
+  constexpr f32x2 SIGN = 0x8000000080000000ull;
+  const f32x2 ph = fmul2(v, pack2(c.c2h, c.c2h));
+  const f32x2 pl = ffma2(v, pack2(c.c2l, c.c2l), ffma2(v, pack2(c.c2h, c.c2h), ph ^ SIGN));
+  // s = ph + (-th), exactly, as df_two_sum
+  const f32x2 nth = pack2(-c.th, -c.th);
+  const f32x2 sh = fadd2(ph, nth);
+  const f32x2 bb = fsub2(sh, ph);
+  const f32x2 sl = fadd2(fsub2(ph, fsub2(sh, bb)), fsub2(nth, bb));
+  const f32x2 tlow = fsub2(fadd2(sl, pl), pack2(c.tl, c.tl));
+  const f32x2 magic = pack2(12582912.0f, 12582912.0f);
+  const f32x2 y = ffma2(sh, pack2(32.0f, 32.0f), magic);
+  const f32x2 g = ffma2(fsub2(y, magic), pack2(-0.03125f, -0.03125f), sh);
+  const f32x2 r = fadd2(g, tlow);
+  const f32x2 u = ffma2(r, pack2(LN2_H, LN2_H), fmul2(r, pack2(LN2_L, LN2_L)));
+  f32x2 q = ffma2(u, pack2(1.0f / 24.0f, 1.0f / 24.0f), pack2(1.0f / 6.0f, 1.0f / 6.0f));
+  q = ffma2(q, u, pack2(0.5f, 0.5f));
+  q = ffma2(q, u, pack2(1.0f, 1.0f));
+  q = fmul2(q, u);
+  // n = rint(32 s.h) = 32 k + j per half (unsigned: a half out of range
+  // gives garbage here, which is masked off below)
+  const float2 yy = unpack2(y);
+  const uint32_t n0 = (uint32_t)__float_as_int(yy.x) - 0x4B400000u;
+  const uint32_t n1 = (uint32_t)__float_as_int(yy.y) - 0x4B400000u;
+  const int j0 = (int)(n0 & 31u), j1 = (int)(n1 & 31u);
+  const int k0 = (int)n0 >> 5, k1 = (int)n1 >> 5;
+  const f32x2 t0 = pack2(tab_h[j0], tab_h[j1]);
+  const f32x2 b = ffma2(t0, q, pack2(tab_l[j0], tab_l[j1]));
+  const f32x2 eh = fadd2(t0, b);
+  const f32x2 el = fsub2(b, fsub2(eh, t0));
+  const f32x2 sc = pack2(__int_as_float((int)(((uint32_t)(k0 + 127)) << 23)),
+                         __int_as_float((int)(((uint32_t)(k1 + 127)) << 23)));
+  // 0 for a half below 2^-125 or with a -inf value
+  const float2 s2 = unpack2(sh);
+  const f32x2 keep = (s2.x > -125.0f ? 0x00000000ffffffffull : 0ull) |
+                     (s2.y > -125.0f ? 0xffffffff00000000ull : 0ull);
+  return DF2{fmul2(eh, sc) & keep, fmul2(el, sc) & keep};
+}
+__device__ __forceinline__ void df2_accumulate(DF2 &acc, DF2 e) {
+  const f32x2 sh = fadd2(acc.h, e.h);
+  const f32x2 bb = fsub2(sh, acc.h);
+  const f32x2 sl = fadd2(fsub2(acc.h, fsub2(sh, bb)), fsub2(e.h, bb));
+  acc.h = sh;
+  acc.l = fadd2(acc.l, fadd2(sl, e.l));
+}
+
 
 // ---------------------------------------------------------------------------
 // Philox4x64-10 and Gumbel noise
@@ -825,15 +878,19 @@ __device__ __noinline__ DF chunk_exp_sum_all(const uint32_t *keys, int cnt, cons
                                              SampSmem &sm) {
   const int nq = cnt >> 2;
   const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
-  DF a0 = {0.0f, 0.0f}, a1 = {0.0f, 0.0f}, a2 = {0.0f, 0.0f}, a3 = {0.0f, 0.0f};
+  // four accumulators a0..a3 (components x, y, z, w of each 16-byte load),
+  // as the packed pairs (a0, a1) and (a2, a3)
+  DF2 a01 = {0ull, 0ull}, a23 = {0ull, 0ull};
 #pragma unroll 1
   for (int q = threadIdx.x; q < nq; q += SB) {
     const uint4 u = k4[q];
-    df_accumulate(a0, df_exp2_rel(key_value(u.x), ctx, sm.e2h, sm.e2l));
-    df_accumulate(a1, df_exp2_rel(key_value(u.y), ctx, sm.e2h, sm.e2l));
-    df_accumulate(a2, df_exp2_rel(key_value(u.z), ctx, sm.e2h, sm.e2l));
-    df_accumulate(a3, df_exp2_rel(key_value(u.w), ctx, sm.e2h, sm.e2l));
+    df2_accumulate(a01, df2_exp2_rel(pack2(key_value(u.x), key_value(u.y)), ctx, sm.e2h, sm.e2l));
+    df2_accumulate(a23, df2_exp2_rel(pack2(key_value(u.z), key_value(u.w)), ctx, sm.e2h, sm.e2l));
   }
+  const float2 h01 = unpack2(a01.h), l01 = unpack2(a01.l), h23 = unpack2(a23.h),
+               l23 = unpack2(a23.l);
+  DF a0 = {h01.x, l01.x};
+  const DF a1 = {h01.y, l01.y}, a2 = {h23.x, l23.x}, a3 = {h23.y, l23.y};
   for (int i = 4 * nq + (int)threadIdx.x; i < cnt; i += SB)
     df_accumulate(a0, df_exp2_rel(key_value(keys[i]), ctx, sm.e2h, sm.e2l));
   const DF lo = df_add(df_fast_two_sum(a0.h, a0.l), df_fast_two_sum(a1.h, a1.l));

@@ -26,6 +26,39 @@ inline void cp_async8(void *dst, const void *src) { emu_cp_async(dst, src, 8); }
 inline void cp_async16(void *dst, const void *src) { emu_cp_async(dst, src, 16); }
 inline void cp_async_wait_all() {}
 inline void __threadfence_block() { std::atomic_thread_fence(std::memory_order_seq_cst); }
+// packed fp32 pairs: .x in the low half of a 64-bit word; every operation
+// is the scalar IEEE one on each half
+typedef unsigned long long f32x2;
+inline f32x2 pack2(float a, float b) {
+  uint32_t x, y;
+  std::memcpy(&x, &a, 4);
+  std::memcpy(&y, &b, 4);
+  return (f32x2)x | ((f32x2)y << 32);
+}
+struct float2 { float x, y; };
+inline float2 unpack2(f32x2 v) {
+  const uint32_t x = (uint32_t)v, y = (uint32_t)(v >> 32);
+  float2 r;
+  std::memcpy(&r.x, &x, 4);
+  std::memcpy(&r.y, &y, 4);
+  return r;
+}
+inline f32x2 ffma2(f32x2 a, f32x2 b, f32x2 c) {
+  const float2 A = unpack2(a), B = unpack2(b), C = unpack2(c);
+  return pack2(std::fmaf(A.x, B.x, C.x), std::fmaf(A.y, B.y, C.y));
+}
+inline f32x2 fadd2(f32x2 a, f32x2 b) {
+  const float2 A = unpack2(a), B = unpack2(b);
+  return pack2(__fadd_rn(A.x, B.x), __fadd_rn(A.y, B.y));
+}
+inline f32x2 fsub2(f32x2 a, f32x2 b) {
+  const float2 A = unpack2(a), B = unpack2(b);
+  return pack2(__fsub_rn(A.x, B.x), __fsub_rn(A.y, B.y));
+}
+inline f32x2 fmul2(f32x2 a, f32x2 b) {
+  const float2 A = unpack2(a), B = unpack2(b);
+  return pack2(__fmul_rn(A.x, B.x), __fmul_rn(A.y, B.y));
+}
 // the SFU's exp2 (an approximation there; exact enough here)
 inline float fast_exp2(float x) { return std::exp2(x); }
 // the SFU's log2 (an approximation there; exact enough here)
