@@ -727,14 +727,18 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_merge_kernel(const AttnArgs
   const int h = blockIdx.x;
   const int b = blockIdx.y;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The lengths and flags were final before the persistent grid started
+  // (its CTAs let this grid start only after their own wait), so they are
+  // read before this grid's wait; the partials only after it.
+  const int64_t bh = (int64_t)b * a.num_qo_heads + h;
+  const int n = a.seq_lens[b];
+  const int act = a.active[b];
   pdl_wait();  // the partials of the persistent kernel
   pdl_trigger();
   // the persistent grid has completed: its unit counter starts again at zero
   // for the next call that runs on the same plan
   if (h == 0 && b == 0 && threadIdx.x == 0) a.plan->counter = 0;
-  const int64_t bh = (int64_t)b * a.num_qo_heads + h;
-  const int n = a.seq_lens[b];
-  if (!a.active[b] || n < 1 || (int64_t)n > a.max_tokens) {
+  if (!act || n < 1 || (int64_t)n > a.max_tokens) {
     for (int d = threadIdx.x; d < D; d += ATTN_THREADS) store_out(a, bh * D + d, 0.0f);
     if (threadIdx.x == 0 && a.lse != nullptr) a.lse[bh] = -INFINITY;
     return;

@@ -2209,7 +2209,6 @@ struct SampleArgs {
   int32_t *out_kind;
   ChunkRec *recs;  // [B][nch]
   int zsplit;      // a second CTA per chunk (grid rows B..2B-1) takes the normaliser
-  int one_wave;    // every chunk CTA is resident at once
   int32_t *err;
   // further controls (null: off)
   const float *min_p;          // [num_slots]
@@ -2261,13 +2260,11 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   // launched behind its predecessor on the stream (programmatic dependent
   // launch): nothing is read before that grid has completed
   pdl_wait();
-  // The finish kernel may be scheduled once every chunk CTA has passed its
-  // wait (or exited).  When the chunk grid runs in one wave that is at
-  // once: the finish CTAs take only the room that chunk CTAs leave, and
-  // have their prologue done when the last chunk CTA ends.  Otherwise at
-  // the end, so that waiting finish CTAs do not hold room the later chunk
-  // CTAs need.
-  if (a.one_wave) pdl_trigger();
+  // The finish kernel may be scheduled once every chunk CTA has passed this
+  // point (or exited), so once the last chunk CTA has started: its CTAs
+  // then take only the room that chunk CTAs leave, and have their prologue
+  // done when the last chunk CTA ends.
+  pdl_trigger();
   if (!a.active[b]) return;
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) return;
@@ -2281,7 +2278,6 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, c, P,
              a.recs + (int64_t)b * a.nch + c, part == PART_NORM ? nullptr : row_pbits(a, b), sm,
              a.err, false, part);
-  if (!a.one_wave) pdl_trigger();
 }
 
 __device__ __forceinline__ void sample_skip_row(const SampleArgs &a, int b) {
@@ -2626,7 +2622,6 @@ static int launch_sample(const float *logits, int64_t row_stride, int batch, int
   if (resident <= 0) return PKV_ERR_CUDA;
   const int64_t ctas = (int64_t)a.nch * batch;
   a.zsplit = 2 * ctas <= resident ? 1 : 0;
-  a.one_wave = ctas * (1 + a.zsplit) <= resident ? 1 : 0;
   if (launch_pdl(sample_chunk_kernel, dim3((unsigned)a.nch, (unsigned)(batch * (1 + a.zsplit))),
                  dim3(SB), 0, s, a) != cudaSuccess)
     return PKV_ERR_CUDA;
