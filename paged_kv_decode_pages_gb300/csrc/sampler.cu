@@ -663,24 +663,66 @@ __device__ void select_bin(SampSmem &sm, int shift) {
 // loops unrolled over register arrays, and the rarely taken paths are kept
 // out of the hot code.
 
+// The Q largest of the warp's 32 values v (Q = 2 or 4), in descending order
+// in every lane: five xor-shuffle rounds, each merging the lane's Q largest
+// with its partner's (the k-th largest of two descending lists a, b is the
+// largest of min(a[i], b[k - i]) over i, with a[0] = b[0] = +inf).  0 is
+// below every key.
+template <int Q>
+__device__ __forceinline__ void warp_top(uint32_t v, uint32_t (&t)[Q]) {
+  t[0] = v;
+#pragma unroll
+  for (int i = 1; i < Q; ++i) t[i] = 0u;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    uint32_t o[Q], r[Q];
+#pragma unroll
+    for (int i = 0; i < Q; ++i) o[i] = __shfl_xor_sync(FULL_MASK, t[i], off);
+#pragma unroll
+    for (int k = 1; k <= Q; ++k) {
+      uint32_t best = max(t[k - 1], o[k - 1]);  // the terms with i = k and i = 0
+#pragma unroll
+      for (int i = 1; i < k; ++i) best = max(best, min(t[i - 1], o[k - i - 1]));
+      r[k - 1] = best;
+    }
+#pragma unroll
+    for (int i = 0; i < Q; ++i) t[i] = r[i];
+  }
+}
+
 // From the threads' largest keys m: a bound L such that at least n of the
-// block's keys are >= L -- each warp sorts its 32 maxima (a bitonic network
-// over the lanes) and offers its q-th largest, q = ceil(n / 8), and L is the
-// smallest offer, so every warp holds q keys >= L -- and the block's
-// largest key in *top.  n <= SB.  All threads get both.
+// block's keys are >= L -- each warp offers the q-th largest of its 32
+// maxima, q = ceil(n / 8) (for q <= 4 a top-q reduction over the lanes,
+// else a bitonic sort over the lanes), and L is the smallest offer, so
+// every warp holds q keys >= L -- and the block's largest key in *top.
+// n <= SB.  All threads get both.
 __device__ uint32_t select_bound(uint32_t m, int n, SampSmem &sm, uint32_t *top) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int q = (n + (SB / 32) - 1) / (SB / 32);
-  uint32_t v = m;
+  uint32_t v, offer;
+  if (q <= 2) {
+    uint32_t t[2];
+    warp_top<2>(m, t);
+    v = t[0];
+    offer = t[q - 1];
+  } else if (q <= 4) {
+    uint32_t t[4];
+    warp_top<4>(m, t);
+    v = t[0];
+    offer = q == 3 ? t[2] : t[3];
+  } else {
+    v = m;
 #pragma unroll
-  for (int k = 2; k <= 32; k <<= 1)
+    for (int k = 2; k <= 32; k <<= 1)
 #pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const uint32_t o = __shfl_xor_sync(FULL_MASK, v, j);
-      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
-      v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
-    }
-  const uint32_t offer = __shfl_sync(FULL_MASK, v, q - 1);
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const uint32_t o = __shfl_xor_sync(FULL_MASK, v, j);
+        const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+        v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+      }
+    offer = __shfl_sync(FULL_MASK, v, q - 1);
+    v = __shfl_sync(FULL_MASK, v, 0);
+  }
   __syncthreads();  // earlier readers of the per-warp slots are done
   if (lane == 0) {
     sm.offer[warp] = offer;

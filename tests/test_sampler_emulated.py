@@ -115,6 +115,10 @@ CASES = [
     (3, 20000, 1.0, 1.0, 400, 0.97, "normal"),
     (3, 8192, 1.0, 1.0, 230, 0.95, "normal"),   # 90-106 to a warp
     (3, 8192, 1.0, 1.0, 256, 0.95, "normal"),   # over 128 to a warp: radix select
+    # lists of one or two slots: the heads' pairwise merge (not the bitonic
+    # union), its runs following a token's chunk
+    (3, 33000, 1.0, 1.0, 2, 1.0, "normal"),
+    (3, 33000, 1.0, 1.0, 1, 1.0, "normal"),
     # the finish's bitonic merge of the union with lists of 8 and 4 slots
     (3, 40000, 1.0, 1.0, 5, 0.9, "normal"),
     (3, 30000, 2.0, 1.0, 3, 1.0, "normal"),
