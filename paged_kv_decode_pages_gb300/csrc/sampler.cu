@@ -2329,32 +2329,15 @@ __device__ __forceinline__ void sample_skip_row(const SampleArgs &a, int b) {
   if (a.lp_proc != nullptr) a.lp_proc[b] = 0.0f;
 }
 
-__global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
-  __shared__ SampSmem sm;
-  const int b = blockIdx.x;
+// The finish of row b from its chunk records (in global memory, or for a
+// single-chunk row in shared memory): the decision, the log-probs, the
+// outputs and the slot's step counter and ring.
+__device__ __forceinline__ void finish_write(const SampleArgs &a, int b, int slot, const RowParams &P,
+                                          const ChunkRec *recs, SampSmem &sm, bool rec_smem) {
   const int tid = threadIdx.x;
-  // This grid starts once every chunk CTA has passed its own wait for its
-  // predecessors, so everything but the chunk records (the flags, the slot
-  // settings and step counters, the history ring) is final already: read it
-  // before waiting for the chunk records.
-  const int active = a.active[b];
-  const int slot = a.slots[b];
-  const bool ok = active && slot >= 0 && slot < a.num_slots;
-  RowParams P;
-  if (ok) P = sample_row_params(a, slot);
-  load_exp2_table(sm);  // read after finish_row's first barrier
-  pdl_wait();  // the chunk records
-  if (!ok) {
-    if (tid == 0) {
-      sample_skip_row(a, b);
-      if (active) report(a.err, PKV_DEV_ERR_SLOT);
-    }
-    return;
-  }
   const float *row = a.logits + (int64_t)b * a.row_stride;
-  const ChunkRec *recs = a.recs + (int64_t)b * a.nch;
   const RowView rv = {row, P.n_pen > 0 ? row_pbits(a, b) : nullptr, P.pen};
-  const int tok = finish_row(rv, a.vocab, a.nch, P, recs, sm);
+  const int tok = finish_row(rv, a.vocab, a.nch, P, recs, sm, rec_smem);
   double lse_raw = 0.0;
   if (P.lp_raw) {
     // log-sum-exp of the unprocessed row: the chunks' partials rescaled to
@@ -2392,6 +2375,61 @@ __global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(SB) sample_finish_kernel(const SampleArgs a) {
+  __shared__ SampSmem sm;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  // This grid starts once every chunk CTA has passed its own wait for its
+  // predecessors, so everything but the chunk records (the flags, the slot
+  // settings and step counters, the history ring) is final already: read it
+  // before waiting for the chunk records.
+  const int active = a.active[b];
+  const int slot = a.slots[b];
+  const bool ok = active && slot >= 0 && slot < a.num_slots;
+  RowParams P;
+  if (ok) P = sample_row_params(a, slot);
+  load_exp2_table(sm);  // read after finish_row's first barrier
+  pdl_wait();  // the chunk records
+  if (!ok) {
+    if (tid == 0) {
+      sample_skip_row(a, b);
+      if (active) report(a.err, PKV_DEV_ERR_SLOT);
+    }
+    return;
+  }
+  finish_write(a, b, slot, P, a.recs + (int64_t)b * a.nch, sm, false);
+}
+
+// A vocabulary of one chunk: one CTA per row runs the chunk pass and the
+// finish, with the chunk record in the part of the shared union the keys
+// leave free when the row has at most SREC_MAX_V tokens (else in the
+// workspace): the same arithmetic as the two kernels, without the second
+// launch and the records' round trip.
+__global__ void __launch_bounds__(SB) sample_single_kernel(const SampleArgs a) {
+  __shared__ SampSmem sm;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const int active = a.active[b];
+  const int slot = a.slots[b];
+  if (!active || slot < 0 || slot >= a.num_slots) {
+    if (tid == 0) {
+      sample_skip_row(a, b);
+      if (active) report(a.err, PKV_DEV_ERR_SLOT);
+    }
+    return;
+  }
+  const RowParams P = sample_row_params(a, slot);
+  load_exp2_table(sm);  // read after the first barrier of the chunk pass
+  const bool rs = a.vocab <= SREC_MAX_V;
+  ChunkRec *rec = rs ? reinterpret_cast<ChunkRec *>(sm.u.fi.mrg) : a.recs + (int64_t)b * a.nch;
+  chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, 0, P, rec, row_pbits(a, b), sm,
+             a.err);
+  __syncthreads();
+  finish_write(a, b, slot, P, rec, sm, rs);
 }
 
 struct FrameArgs {
@@ -2664,6 +2702,12 @@ static int launch_sample(const float *logits, int64_t row_stride, int batch, int
   if (resident <= 0) return PKV_ERR_CUDA;
   const int64_t ctas = (int64_t)a.nch * batch;
   a.zsplit = 2 * ctas <= resident ? 1 : 0;
+  if (a.nch == 1) {
+    // one chunk a row: chunk pass and finish in one CTA
+    if (launch_pdl(sample_single_kernel, dim3((unsigned)batch), dim3(SB), 0, s, a) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    return launch_status();
+  }
   if (launch_pdl(sample_chunk_kernel, dim3((unsigned)a.nch, (unsigned)(batch * (1 + a.zsplit))),
                  dim3(SB), 0, s, a) != cudaSuccess)
     return PKV_ERR_CUDA;

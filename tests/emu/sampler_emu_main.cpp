@@ -103,8 +103,13 @@ int main(int argc, char **argv) {
   // the second CTA per chunk for the normaliser: on unless EMU_ZSPLIT=0
   const char *zs = std::getenv("EMU_ZSPLIT");
   a.zsplit = (zs != nullptr && zs[0] == '0') ? 0 : 1;
-  emu_launch(sample_chunk_kernel, dim3(a.nch, B * (1 + a.zsplit)), SB, a);
-  emu_launch(sample_finish_kernel, dim3(B), SB, a);
+  if (a.nch == 1) {
+    // one chunk a row: the host launches the single-CTA kernel
+    emu_launch(sample_single_kernel, dim3(B), SB, a);
+  } else {
+    emu_launch(sample_chunk_kernel, dim3(a.nch, B * (1 + a.zsplit)), SB, a);
+    emu_launch(sample_finish_kernel, dim3(B), SB, a);
+  }
   free(ws);
 
   FILE *o = fopen(argv[2], "wb");
