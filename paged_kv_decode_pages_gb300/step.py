@@ -225,11 +225,13 @@ class DecodeStep:
     def launches_per_step(self) -> int:
         """Kernel launches of one run(): with plan_once one planner, then per
         layer append 1 + attention 2 (persistent kernel, split merge); else
-        per layer append 1 + attention 3 (planner too); sampler 2; frame 1."""
+        per layer append 1 + attention 3 (planner too); sampler 2 (chunk
+        pass, finish), or 1 for a vocabulary of one 8192-token chunk;
+        frame 1."""
         L = self.t.layers
         n = 1 + L * 3 if self.plan_once else L * 4
         if self.t.logits is not None:
-            n += 2
+            n += 1 if self.t.logits.shape[-1] <= 8192 else 2
         if self.t.base is not None:
             n += 1
         return n
