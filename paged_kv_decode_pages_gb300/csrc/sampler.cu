@@ -486,6 +486,8 @@ struct __align__(16) SampSmem {
   double s_kept;     // mass (relative to the row maximum) of the kept tokens
   double m_row;      // x of the row maximum
   double xbest;      // x of the sampled token
+  uint64_t stage_bar;  // completion of the chunk's bulk copies
+  uint64_t stage_pad;  // keeps the buffers below 16-byte aligned
   uint64_t sortbuf[GEN_BLOCK];  // sorted prefixes; the chunk pass's candidate buffer
   union {
     ChunkScratch ch;
@@ -842,17 +844,59 @@ __device__ __noinline__ void rank_count_out(const uint64_t *g, int C, int nc, ui
 // ---------------------------------------------------------------------------
 // The chunk [start, start + cnt) of `row` into buf as fp32 bits; every copy
 // is issued before any is waited for.
-__device__ __forceinline__ void stage_chunk(const float *row, int start, int cnt, uint32_t *buf) {
+__device__ __forceinline__ void stage_chunk_issue(const float *row, int start, int cnt,
+                                                  uint32_t *buf) {
   const float *src = row + start;
   if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (cnt & 3) == 0) {
     for (int i = 4 * (int)threadIdx.x; i < cnt; i += 4 * SB) cp_async16(buf + i, src + i);
   } else {
     for (int i = (int)threadIdx.x; i < cnt; i += SB) cp_async4(buf + i, src + i);
   }
+}
+__device__ __forceinline__ void stage_chunk(const float *row, int start, int cnt, uint32_t *buf) {
+  stage_chunk_issue(row, start, cnt, buf);
   cp_async_wait_all();
   __syncthreads();
 }
 
+
+// The chunk [start, start + cnt) of `row` into the chunk buffer in two
+// halves, so that other work can run while the copies are in flight.
+// stage_chunk_begin issues them: bulk copies from thread 0 (8 KB each, on
+// one mbarrier) when the chunk starts on a 16-byte boundary and is a
+// multiple of 16 bytes long, else cp.async from every thread; it returns
+// which.  stage_chunk_end waits for them (a block barrier included): false
+// when bulk copies did not land in time -- reported, and waited for once
+// more so that none is still writing when the CTA leaves.
+__device__ __forceinline__ bool stage_chunk_begin(const float *row, int start, int cnt,
+                                                  SampSmem &sm) {
+  const bool bulk = (reinterpret_cast<uintptr_t>(row + start) & 15u) == 0 && (cnt & 3) == 0;
+  if (bulk) {
+    if (threadIdx.x == 0) {
+      mbar_init(&sm.stage_bar, 1);
+      fence_barrier_init();
+      const uint32_t bytes = 4u * (uint32_t)cnt;
+      mbar_arrive_expect_tx(&sm.stage_bar, bytes);
+      const unsigned char *src = reinterpret_cast<const unsigned char *>(row + start);
+      unsigned char *dst = reinterpret_cast<unsigned char *>(sm.u.ch.keys);
+      for (uint32_t off = 0; off < bytes; off += 8192u)
+        bulk_copy_g2s(dst + off, src + off, min(8192u, bytes - off), &sm.stage_bar);
+    }
+  } else {
+    stage_chunk_issue(row, start, cnt, sm.u.ch.keys);
+  }
+  return bulk;
+}
+__device__ __forceinline__ bool stage_chunk_end(bool bulk, SampSmem &sm, int32_t *err) {
+  if (!bulk) cp_async_wait_all();
+  __syncthreads();
+  if (bulk && !__syncthreads_and(mbar_wait(&sm.stage_bar, 0))) {
+    if (threadIdx.x == 0) report(err, PKV_DEV_ERR_TIMEOUT);
+    (void)mbar_wait(&sm.stage_bar, 0);
+    return false;
+  }
+  return true;
+}
 
 // The keys of NaN logits (outside [key(-inf), key(+inf)]) set to key(-inf):
 // a NaN ranks like -inf; NaN and +inf are reported.  Returns the thread's
@@ -2310,16 +2354,34 @@ __global__ void __launch_bounds__(SB) sample_chunk_kernel(const SampleArgs a) {
   if (!a.active[b]) return;
   const int slot = a.slots[b];
   if (slot < 0 || slot >= a.num_slots) return;
-  const RowParams P = sample_row_params(a, slot);
-  int part = PART_ALL;
-  if (a.zsplit && (P.need_z || P.lp_raw))
-    part = zcta ? PART_NORM : PART_SELECT;
-  else if (zcta)
+  RowParams P;
+  if (zcta) {
+    // a second CTA: only when the row asks for a normaliser
+    P = sample_row_params(a, slot);
+    if (!(P.need_z || P.lp_raw)) return;
+  }
+  // the chunk's copies go out first; the row's parameters are formed while
+  // they are in flight
+  const float *row = a.logits + (int64_t)b * a.row_stride;
+  const bool bulk = stage_chunk_begin(row, c * CHUNK, min(CHUNK, a.vocab - c * CHUNK), sm);
+  if (!zcta) P = sample_row_params(a, slot);
+  load_exp2_table(sm);
+  if (!stage_chunk_end(bulk, sm, a.err)) {
+    // reported; the record says "no candidates" so that the finish reads a
+    // well-formed one
+    ChunkRec *rec = a.recs + (int64_t)b * a.nch + c;
+    if (!zcta && threadIdx.x == 0) {
+      rec->ncand = 0;
+      rec->sorted = 1;
+      rec->top1 = 0ull;
+      rec->thr = 0ull;
+    }
     return;
-  load_exp2_table(sm);  // read after the first barrier of the chunk pass
-  chunk_pass(a.logits + (int64_t)b * a.row_stride, a.vocab, c, P,
-             a.recs + (int64_t)b * a.nch + c, part == PART_NORM ? nullptr : row_pbits(a, b), sm,
-             a.err, false, part);
+  }
+  int part = PART_ALL;
+  if (a.zsplit && (P.need_z || P.lp_raw)) part = zcta ? PART_NORM : PART_SELECT;
+  chunk_pass(row, a.vocab, c, P, a.recs + (int64_t)b * a.nch + c,
+             part == PART_NORM ? nullptr : row_pbits(a, b), sm, a.err, true, part);
 }
 
 __device__ __forceinline__ void sample_skip_row(const SampleArgs &a, int b) {

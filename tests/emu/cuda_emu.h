@@ -56,6 +56,16 @@ inline int __syncthreads_or(int pred) {
   g_block.bar->arrive_and_wait();
   return r;
 }
+inline std::atomic<int> g_sync_and_miss{0};
+inline int __syncthreads_and(int pred) {
+  if (!pred) g_sync_and_miss.store(1);
+  g_block.bar->arrive_and_wait();
+  const int r = g_sync_and_miss.load() == 0;
+  g_block.bar->arrive_and_wait();
+  if (threadIdx.x == 0) g_sync_and_miss.store(0);
+  g_block.bar->arrive_and_wait();
+  return r;
+}
 inline EmuWarp &emu_warp() { return g_block.warps[threadIdx.x / 32]; }
 inline void __syncwarp(unsigned = 0xffffffffu) { emu_warp().bar.arrive_and_wait(); }
 

@@ -25,6 +25,19 @@ inline void cp_async4(void *dst, const void *src) { emu_cp_async(dst, src, 4); }
 inline void cp_async8(void *dst, const void *src) { emu_cp_async(dst, src, 8); }
 inline void cp_async16(void *dst, const void *src) { emu_cp_async(dst, src, 16); }
 inline void cp_async_wait_all() {}
+// mbarriers and bulk copies: the copy is done when issued, so a barrier's
+// phase is complete by the time anyone waits on it
+inline void mbar_init(uint64_t *, uint32_t) {}
+inline void fence_barrier_init() {}
+inline void mbar_arrive_expect_tx(uint64_t *, uint32_t) {}
+inline void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *) {
+  if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | bytes) % 16 != 0) {
+    std::fprintf(stderr, "misaligned bulk copy of %u bytes: dst %p src %p\n", bytes, dst, src);
+    std::abort();
+  }
+  std::memcpy(dst, src, bytes);
+}
+inline bool mbar_wait(uint64_t *, uint32_t, uint64_t = 0) { return true; }
 inline void __threadfence_block() { std::atomic_thread_fence(std::memory_order_seq_cst); }
 // packed fp32 pairs: .x in the low half of a 64-bit word; every operation
 // is the scalar IEEE one on each half

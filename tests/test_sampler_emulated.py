@@ -119,6 +119,9 @@ CASES = [
     # union), its runs following a token's chunk
     (3, 33000, 1.0, 1.0, 2, 1.0, "normal"),
     (3, 33000, 1.0, 1.0, 1, 1.0, "normal"),
+    # rows and last chunks off the 16-byte grid: the chunk copied by
+    # cp.async from every thread instead of bulk copies from one
+    (3, 20001, 1.0, 1.0, 0, 0.95, "normal"),
     # the finish's bitonic merge of the union with lists of 8 and 4 slots
     (3, 40000, 1.0, 1.0, 5, 0.9, "normal"),
     (3, 30000, 2.0, 1.0, 3, 1.0, "normal"),
