@@ -1882,15 +1882,12 @@ __device__ uint64_t gumbel_argmax_sorted(const uint64_t *srt, const RowParams &P
   }
   const float margin = 1e-4f + 2e-6f * fabsf(best);
   const float floor_s = best - margin;
-  int close = 0;
-  for (int r = tid; r < kept; r += SB) close += d.s32[r] >= floor_s ? 1 : 0;
-  close = __reduce_add_sync(FULL_MASK, close);
-  if (tid == 0) sm.cnt = 0;
-  __syncthreads();
-  if (lane == 0 && close) atomicAdd(&sm.cnt, (uint32_t)close);
-  __syncthreads();
-  const bool screened = isfinite(best) && sm.cnt == 1u;
-  __syncthreads();
+  // the screen decides unless a kept rank other than the best lies within
+  // the margin (the best itself always does)
+  bool other = false;
+  for (int r = tid; r < kept; r += SB)
+    other = other || (d.s32[r] >= floor_s && srt[r] != bestc);
+  const bool screened = isfinite(best) && !__syncthreads_or(other);
   if (screened) return bestc;
   // fp64 scores of the contenders (every kept rank when the screen cannot
   // decide at all)
