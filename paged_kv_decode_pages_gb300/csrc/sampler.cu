@@ -861,7 +861,7 @@ __device__ __forceinline__ void stage_chunk(const float *row, int start, int cnt
 
 
 // The chunk [start, start + cnt) of `row` into the chunk buffer in two
-// halves, so that other work can run while the copies are in flight.
+// steps, so that other work can run while the copies are in flight.
 // stage_chunk_begin issues them: bulk copies from thread 0 (8 KB each, on
 // one mbarrier) when the chunk starts on a 16-byte boundary and is a
 // multiple of 16 bytes long, else cp.async from every thread; it returns
