@@ -103,8 +103,10 @@ int main(int argc, char **argv) {
   // the second CTA per chunk for the normaliser: on unless EMU_ZSPLIT=0
   const char *zs = std::getenv("EMU_ZSPLIT");
   a.zsplit = (zs != nullptr && zs[0] == '0') ? 0 : 1;
-  if (a.nch == 1) {
-    // one chunk a row: the host launches the single-CTA kernel
+  const char *sg = std::getenv("EMU_SINGLE");
+  if (a.nch == 1 && !(sg != nullptr && sg[0] == '0')) {
+    // one chunk a row: the host launches the single-CTA kernel (EMU_SINGLE=0:
+    // the two kernels instead, to compare the two)
     emu_launch(sample_single_kernel, dim3(B), SB, a);
   } else {
     emu_launch(sample_chunk_kernel, dim3(a.nch, B * (1 + a.zsplit)), SB, a);

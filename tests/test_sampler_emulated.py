@@ -45,11 +45,14 @@ def emu_binary(tmp_path_factory):
     return exe
 
 
-def _run(exe, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p, ext=None, zsplit=1):
+def _run(exe, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p, ext=None, zsplit=1,
+         single=1):
     """ext: dict of min_p, rep_penalty, rep_window, history [S, cap],
     hist_len, advance (the pkv_seeded_sample_ext settings).  zsplit: launch
     the second CTA per chunk that computes the normaliser (the host does so
-    whenever the chunk grid is at most two CTAs per SM).  Returns
+    whenever the chunk grid is at most two CTAs per SM).  single: a
+    vocabulary of one chunk runs as one kernel (0: as the chunk and finish
+    kernels).  Returns
     (out_tok, out_kind, err) and, with ext, also (logprob_raw, logprob_proc,
     hist_len, history, steps) after the call."""
     B, V = x.shape
@@ -67,7 +70,8 @@ def _run(exe, tmp_path, x, slots, active, seeds, steps, temp, top_k, top_p, ext=
                      (np.array([int(ext["advance"])]), np.int32)]
         for arr, dt in arrs:
             np.ascontiguousarray(arr, dtype=dt).tofile(f)
-    env = dict(os.environ, ASAN_OPTIONS="detect_leaks=0", EMU_ZSPLIT=str(int(zsplit)))
+    env = dict(os.environ, ASAN_OPTIONS="detect_leaks=0", EMU_ZSPLIT=str(int(zsplit)),
+               EMU_SINGLE=str(int(single)))
     r = subprocess.run([str(exe), str(inp), str(out)], capture_output=True, text=True, env=env,
                        timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
@@ -206,9 +210,7 @@ EXT_CASES = [
 ]
 
 
-@pytest.mark.parametrize("B,V,std,T,k,p,mp,pen,win,dist", EXT_CASES)
-def test_emulated_sampler_ext_matches_oracle(emu_binary, tmp_path, B, V, std, T, k, p, mp, pen,
-                                             win, dist):
+def _ext_inputs(B, V, std, T, k, p, mp, pen, win, dist):
     rng = np.random.default_rng(V + k + 7)
     x = rng.normal(0, std, (B, V)).astype(np.float32)
     if dist == "conc":
@@ -239,6 +241,14 @@ def test_emulated_sampler_ext_matches_oracle(emu_binary, tmp_path, B, V, std, T,
     ext = dict(min_p=np.full(S, mp, np.float32), rep_penalty=np.full(S, pen, np.float32),
                rep_window=np.full(S, win, np.int32), history=history.copy(),
                hist_len=hist_len.copy(), advance=True)
+    return x, slots, active, seeds, steps, temp, top_k, top_p, history, hist_len, ext
+
+
+@pytest.mark.parametrize("B,V,std,T,k,p,mp,pen,win,dist", EXT_CASES)
+def test_emulated_sampler_ext_matches_oracle(emu_binary, tmp_path, B, V, std, T, k, p, mp, pen,
+                                             win, dist):
+    (x, slots, active, seeds, steps, temp, top_k, top_p, history, hist_len,
+     ext) = _ext_inputs(B, V, std, T, k, p, mp, pen, win, dist)
     got, kind, err, lraw, lproc, hl, hist, st = _run(emu_binary, tmp_path, x, slots, active, seeds,
                                                      steps, temp, top_k, top_p, ext)
     w_steps = steps.copy()
@@ -260,3 +270,35 @@ def test_emulated_sampler_ext_matches_oracle(emu_binary, tmp_path, B, V, std, T,
     np.testing.assert_array_equal(hl, w_len)
     if not np.any(mism):
         np.testing.assert_array_equal(hist, w_hist)
+
+
+# The launch shapes the host picks by the grid's size -- a second CTA per
+# chunk for the normalisers, one kernel for a vocabulary of one chunk --
+# must not change a bit of any output: every output of the default launch
+# against the same call launched the other way (tokens, kinds, both
+# log-probs' bits, rings, lengths, step counters, the error word).
+SHAPE_CASES = [
+    (EXT_CASES[2], "single"),   # 6 561 tokens, penalty, log-probs
+    (EXT_CASES[5], "single"),   # greedy with penalty
+    (EXT_CASES[4], "zsplit"),   # 20 000 tokens: raw log-prob in the second CTA
+    (EXT_CASES[3], "zsplit"),
+    ((2, 151936, 3.0, 0.7, 0, 0.95, 0.0, 1.0, -1, "normal"), "zsplit"),  # top-p normaliser
+]
+
+
+@pytest.mark.parametrize("case,shape", SHAPE_CASES)
+def test_emulated_launch_shapes_give_the_same_bits(emu_binary, tmp_path, case, shape):
+    outs = []
+    for alt in (False, True):
+        (x, slots, active, seeds, steps, temp, top_k, top_p, history, hist_len,
+         ext) = _ext_inputs(*case)
+        kw = {"zsplit": 0} if (alt and shape == "zsplit") else {}
+        if alt and shape == "single":
+            kw = {"single": 0}
+        outs.append(_run(emu_binary, tmp_path, x, slots, active, seeds, steps, temp, top_k,
+                         top_p, ext, **kw))
+    a, b = outs
+    for u, v in zip(a, b):
+        u, v = np.asarray(u), np.asarray(v)
+        assert u.dtype == v.dtype and u.shape == v.shape
+        assert u.tobytes() == v.tobytes(), (shape, u, v)
