@@ -22,30 +22,35 @@
 //    composite comes first in (value desc, id asc) order, and composites
 //    are unique.
 //  * chunk pass (one CTA per 8192-token chunk of a row; the chunk is staged
-//    in shared memory with cp.async and turned into order keys in place):
-//    chunk maximum; the chunk's nc largest composites, nc = min(kcap,
-//    max(64, ceil(kcap / chunks))) with kcap = the top-k, or 512 for top-p
-//    over the whole vocabulary, and the smallest of them.  For nc <= 256
-//    they come from a lower bound taken from the warps' sorted thread
-//    maxima (select_bound), a gather of the keys at or above it and exact
-//    rank counting over those (rank_out), in descending order; otherwise,
-//    or when more than 1024 keys pass the bound, from a radix select over
-//    8-bit digits;
-//    for top-p over the whole vocabulary, the partial normaliser
+//    in shared memory -- bulk copies from one thread on an mbarrier when it
+//    is 16-byte aligned, else cp.async from every thread -- and turned into
+//    order keys in place): the chunk's nc largest composites, nc =
+//    min(kcap, max(16, ceil(kcap / chunks))) with kcap = the top-k, or 512
+//    for top-p over the whole vocabulary, and the smallest of them.  For
+//    nc <= 256 they come from a lower bound taken from the warps' largest
+//    thread maxima (select_bound: a top-2 / top-4 reduction over the lanes,
+//    or a sort over the lanes), a per-warp gather of the keys at or above
+//    it and exact rank counting over those, in descending order; otherwise,
+//    or when a warp gathers more than 128, from a radix select over 8-bit
+//    digits.  For top-p over the whole vocabulary, the partial normaliser
 //    sum exp(x - x_chunkmax) = sum 2^(logit * log2(e) / T - t_chunkmax) in
-//    double-float arithmetic (fp32 pairs): Tang's table-driven exp2 (ACM
-//    TOMS 15(2), 1989) with a double-float table of 2^(j/32) and a degree-4
-//    polynomial, each term within 3e-9 of itself, summed with exact
-//    two-sum corrections -- on this GPU one fp64 warp instruction costs as
-//    much issue time as several dozen fp32 ones, and this is the only
-//    per-logit transcendental of the path; for "keep everything", the
-//    chunk's Gumbel argmax.  The chunking depends on the vocabulary only.
-//  * finish (one CTA per row): the kcap largest of the chunks' candidates,
-//    in order (for a top-k up to 64 a selection bound from the lists' heads
-//    and rank counting, otherwise bitonic merges of the chunks' sorted
-//    lists, or a radix select and a sort when the union does not fit in
-//    shared memory); min_p, then top-p with double-float prefix sums in
-//    sorted order; the Gumbel argmax (arithmetic below).  The
+//    double-float arithmetic (fp32 pairs, two terms at a time on packed
+//    f32x2 operations): Tang's table-driven exp2 (ACM TOMS 15(2), 1989)
+//    with a double-float table of 2^(j/32) and a degree-4 polynomial, each
+//    term within 3e-9 of itself, summed with exact two-sum corrections --
+//    on this GPU one fp64 warp instruction costs as much issue time as
+//    several dozen fp32 ones, and this is the only per-logit transcendental
+//    of the path; for "keep everything", the chunk's Gumbel argmax.  When
+//    two CTAs per chunk fit on the SMs at once, a second CTA per chunk
+//    computes the normaliser partials (the same arithmetic) while the first
+//    selects.  The chunking depends on the vocabulary only.
+//  * finish (one CTA per row, released as soon as the last chunk CTA has
+//    started): the chunks' candidates in order -- the whole union sorted by
+//    a register / shuffle bitonic merge of the sorted lists when it fits
+//    1024 entries, else a pairwise merge of the lists' heads, or a radix
+//    select and a sort from the records; min_p, then top-p with
+//    double-float prefix sums in sorted order (a top-k of at most 64 decided
+//    by one warp); the Gumbel argmax (arithmetic below).  The
 //    sorted candidates are the exact global order over the prefix the
 //    decision read unless a chunk holding more tokens than it gave has its
 //    smallest candidate strictly inside that prefix; such rows, and rows
@@ -53,6 +58,8 @@
 //    needing more than 512 tokens), take an exact general path that streams
 //    the row: radix select of the top-k threshold and progressive sorted
 //    extraction until the top-p crossing.
+//  * a vocabulary of one chunk runs the chunk pass and the finish in one
+//    CTA per row (sample_single_kernel), with the same arithmetic.
 //  * further settings (pkv_seeded_sample_ext; "Adding a Model", "2. The
 //    program", in the order of the Chatterbox notes of "Supported Models"
 //    with top-k before min_p): the repetition penalty is applied to the
