@@ -126,6 +126,11 @@ CASES = [
     # rows and last chunks off the 16-byte grid: the chunk copied by
     # cp.async from every thread instead of bulk copies from one
     (3, 20001, 1.0, 1.0, 0, 0.95, "normal"),
+    # the finish's bitonic union at its boundaries: 16 lists of 32 slots
+    # fill 512 entries exactly (two a thread), 17 lists need 1 024 (four a
+    # thread, fifteen lists of padding)
+    (2, 131072, 2.0, 0.8, 0, 0.9, "normal"),
+    (2, 139264, 2.0, 0.8, 0, 0.9, "normal"),
     # the finish's bitonic merge of the union with lists of 8 and 4 slots
     (3, 40000, 1.0, 1.0, 5, 0.9, "normal"),
     (3, 30000, 2.0, 1.0, 3, 1.0, "normal"),
