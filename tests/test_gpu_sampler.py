@@ -135,6 +135,10 @@ def test_config_samplers_match_oracle(name, B):
     dict(V=40000, T=1.0, k=200, p=0.99, std=1.0),      # top-k above the per-chunk candidates
     dict(V=40000, T=1.0, k=300, p=0.99, std=1.0, dist="conc"),  # one chunk holds the top-k
     dict(V=151936, T=0.5, k=0, p=0.95, std=1.0, dist="conc"),   # one chunk holds the top-p set
+    # the finish's bitonic union at its boundaries: 16 lists of 32 slots
+    # fill 512 entries (two a thread), 17 lists take 1 024 (four a thread)
+    dict(V=131072, T=0.8, k=0, p=0.9, std=2.0),
+    dict(V=139264, T=0.8, k=0, p=0.9, std=2.0),
 ])
 def test_sampler_modes_and_edges(case):
     B = 7
